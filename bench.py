@@ -1,0 +1,361 @@
+#!/usr/bin/env python
+"""Benchmark of the routed MoE decode layer served from the GPU expert-slot cache.
+
+Workload (default): the V4-Flash-shaped decode layer -- H=4096, I=2048, E=256
+routed MXFP4 experts (13,369,344 B each), top_k=8, one FP8 shared expert, a
+64-slot cache backed by a pinned host bank of all 256 experts, bf16 N(0,1)
+activations, fp32 N(0,1) router logits plus a log-Zipf(1.1) popularity bias,
+run over a seeded routing trace.  One step = one layer call on one trace step:
+router, ensure_experts, the one host sync, the misses copied from the pinned
+bank, the grouped expert MLP with the shared expert and combine.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s + HBM GB/s (decode); FP4 TFLOPS vs peak (prefill)"
+UNIT = "tokens/s"
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--T", type=int, default=64, help="decode batch of the headline line")
+    p.add_argument("--sweep", default="1,4,16,64", help="decode batches also measured (comma list, '' for none)")
+    p.add_argument("--cpu-sample-tokens", type=int, default=4)
+    return p.parse_args()
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.flush()
+        rows = []
+        with open(self.f.name) as fh:
+            for ln in fh:
+                parts = [x.strip() for x in ln.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.f.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------
+# CPU baseline: the oracle, as it stands, on a bounded sample of the workload
+# ----------------------------------------------------------------------------
+
+_CPU_SNIPPET = r"""
+import json, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+from oracle import formats as F
+from oracle.mlp import moe_layer
+from oracle.router import router_topk
+from oracle.slot_cache import FETCH, SlotCacheLRU
+from synth import configs, gen
+wl = configs.scaled(configs.DECODE, T={T})
+shared_bytes = gen.shared_expert(wl, 0)
+t0 = time.perf_counter()
+cache = SlotCacheLRU(wl.S, 1, wl.E)
+shw = F.decode_fp8_expert(shared_bytes, wl.H, wl.I)
+tokens = 0
+for step in range({steps}):
+    lg = gen.router_logits(wl, 0, step, wl.T)
+    x = gen.activations(wl, 0, step, wl.T)
+    ids, w = router_topk(lg, wl.k)
+    tb = 0
+    while tb < wl.T:
+        _, _, _, tb = cache.ensure(0, ids, 0, wl.k, FETCH, tb)
+    y = moe_layer(x, ids, w, lambda e, tag: F.decode_fp4_expert(gen.fp4_expert(wl, 0, e), wl.H, wl.I),
+                  shared=shw)
+    tokens += wl.T
+dt = time.perf_counter() - t0
+print(json.dumps({{"tokens": tokens, "seconds": dt}}))
+"""
+
+
+def cpu_baseline(T: int, steps: int = 1):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = _CPU_SNIPPET.format(root=ROOT, T=T, steps=steps)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": "failed: " + r.stderr.strip().splitlines()[-1][:200] if r.stderr else "failed"}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": d["tokens"] / d["seconds"], "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{steps} trace step(s) x {T} tokens of the decode workload (fp64 NumPy, "
+                      f"weights regenerated and decoded per expert), {d['seconds']:.1f} s single-threaded"}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from moe_expert_offload_router_gb300 import build as B
+    B.build()
+    import moe_expert_offload_router_gb300 as M
+    from synth import configs, gen
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    base = configs.DECODE
+    Ts = sorted({args.T} | {int(t) for t in args.sweep.split(",") if t.strip()})
+    Tmax = max(Ts)
+    H, I, E, k, S = base.H, base.I, base.E, base.k, base.S
+    Bx = M.moe_fp4_expert_bytes(H, I)
+    # pinned bank of all 256 experts, generated on the device by the seeded counter generator
+    bank = torch.empty(E * Bx, dtype=torch.uint8, pin_memory=True)
+    for e in range(E):
+        bank[e * Bx:(e + 1) * Bx].copy_(gen.fp4_expert(base, 0, e, device=dev))
+    slots = torch.empty(S * Bx, dtype=torch.uint8, device=dev)
+    shared = torch.from_numpy(gen.shared_expert(base, 0)).to(dev)
+    cache = M.moe_cache(S, 1, E, Bx, slots, bank)
+    views = M.make_views(H, I, slots, S, None, 0, shared)
+    runner = M.DecodeLayerRunner(cache, views, E, k, Tmax, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)     # > 129 MB L2
+    hbm_peak, peak_kind = _peaks()
+    stream = torch.cuda.current_stream(dev)
+    n_steps = args.warmup + args.steps
+
+    def inputs(T):
+        wl = configs.scaled(base, T=T)
+        lg = [torch.from_numpy(gen.router_logits(wl, 0, s % base.steps, T)).to(dev) for s in range(n_steps)]
+        xs = [torch.from_numpy(gen.activations(wl, 0, s % base.steps, T).view(np.int16)).to(dev)
+              for s in range(n_steps)]
+        return lg, xs
+
+    gu_expert = 2 * (I * H // 2 + I * H // 32)             # w1 + w3 bytes of one FP4 expert
+    gu_shared = 2 * (I * H + I * 4)                          # w1 + w3 of the FP8 shared expert
+    layer_shared = M.moe_fp8_expert_bytes(H, I)
+
+    def measure(T):
+        cache.reset()
+        torch.cuda.synchronize()
+        lg, xs = inputs(T)
+        y = torch.empty((T, H), dtype=torch.int16, device=dev)
+        for s in range(args.warmup):
+            runner.run(0, lg[s], xs[s], y)
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        acct_gu_bytes, acct_layer_bytes = 0, 0
+        misses0, bytes0 = runner.stats["misses"], runner.stats["bytes_copied"]
+        pairs_hit = 0
+        M.moe_profile_enable(True)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            s = args.warmup + i
+            flush.zero_()
+            ev[i][0].record(stream)
+            runner.run(0, lg[s], xs[s], y)
+            ev[i][1].record(stream)
+            # accounting (outside the events): distinct experts per forward chunk
+            ids = runner.ids[:T]
+            d = int(torch.unique(ids).numel())
+            acct_gu_bytes += d * gu_expert + gu_shared + T * H * 2 + (T * k + T) * I * 4
+            acct_layer_bytes += d * Bx + layer_shared + 2 * T * H * 2
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        wall = time.perf_counter() - t0
+        step_ms = [a.elapsed_time(b) for a, b in ev]
+        kt = {M.KERNEL_NAMES[kid]: M.moe_profile_query(kid) for kid in range(M.MOE_K_COUNT)}
+        M.moe_profile_enable(False)
+        ms = sum(step_ms) / len(step_ms)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t)
+        gu_ms, gu_n = kt["gateup"]
+        compute_ms = sum(v[0] for v in kt.values()) / args.steps
+        return {
+            "T": T, "ms_per_step": ms, "tokens_per_s": world * T / (ms / 1e3),
+            "compute_only_tokens_per_s": T / (compute_ms / 1e3),
+            "layer_gbs": acct_layer_bytes / args.steps / (ms / 1e3) / 1e9,
+            "gateup_ms": gu_ms / max(gu_n, 1), "gateup_launches": gu_n,
+            "gateup_gbs": (acct_gu_bytes / max(gu_n, 1)) / (gu_ms / max(gu_n, 1) / 1e3) / 1e9,
+            "gateup_bytes_per_launch": acct_gu_bytes / max(gu_n, 1),
+            "misses_per_step": (runner.stats["misses"] - misses0) / args.steps,
+            "h2d_gb_per_step": (runner.stats["bytes_copied"] - bytes0) / args.steps / 1e9,
+            "kernel_ms": {n: round(v[0] / args.steps, 4) for n, v in kt.items() if v[1]},
+            "launches": sum(v[1] for v in kt.values()),
+            "wall_s": wall,
+        }
+
+    def measure_e2e(T):
+        """Same steps through the public API with host buffers: inputs copied in
+        from pinned memory and the output read back, every step."""
+        lg, xs = inputs(T)
+        h_lg = [t.cpu().pin_memory() for t in lg]
+        h_x = [t.cpu().pin_memory() for t in xs]
+        d_lg = torch.empty_like(lg[0])
+        d_x = torch.empty_like(xs[0])
+        y = torch.empty((T, H), dtype=torch.int16, device=dev)
+        h_y = torch.empty((T, H), dtype=torch.int16, pin_memory=True)
+        cache.reset()
+        for s in range(args.warmup):
+            d_lg.copy_(h_lg[s], non_blocking=True)
+            d_x.copy_(h_x[s], non_blocking=True)
+            runner.run(0, d_lg, d_x, y)
+            h_y.copy_(y, non_blocking=True)
+        torch.cuda.synchronize()
+        tot = 0.0
+        for i in range(args.steps):
+            s = args.warmup + i
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            d_lg.copy_(h_lg[s], non_blocking=True)
+            d_x.copy_(h_x[s], non_blocking=True)
+            runner.run(0, d_lg, d_x, y)
+            h_y.copy_(y, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            tot += a.elapsed_time(b)
+        ms = tot / args.steps
+        return {"value": world * T / (ms / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": T * E * 4 + T * H * 2, "d2h_bytes_per_step": T * H * 2}
+
+    clocks = Clocks(local)
+    results = {}
+    clocks.start()
+    for T in Ts:
+        results[T] = measure(T)
+    ck = clocks.stop()
+    head = results[args.T]
+    e2e = measure_e2e(args.T)
+    cpu = cpu_baseline(args.cpu_sample_tokens) if (rank == 0 and world == 1) else None
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": head["tokens_per_s"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e2m1/e8m0 weights, f16 dot, f32 accumulate",
+            "data": "synthetic (seeded generator; no checkpoint weights)",
+            "config": {"workload": f"decode layer H=4096 I=2048 E=256 top_k=8 + FP8 shared, 64-slot cache over a pinned "
+                                   f"256-expert bank, Zipf(1.1) routing trace, T={args.T}",
+                       "T": args.T, "parallelism": "replicas" if world > 1 else "single GPU",
+                       "l2": "flushed (256 MB write) before every timed step"},
+            "roofline": {"bound": "hbm", "achieved": head["gateup_gbs"], "peak": hbm_peak, "unit": "GB/s",
+                         "frac": head["gateup_gbs"] / hbm_peak, "traffic": None,
+                         "kernel": "gateup_kernel", "peak_kind": peak_kind + " (copy bandwidth)",
+                         "bytes_per_launch": head["gateup_bytes_per_launch"], "ms_per_launch": head["gateup_ms"]},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": head["launches"],
+            "clocks": ck,
+            "compute_only_tokens_per_s": head["compute_only_tokens_per_s"],
+            "layer_gbs": head["layer_gbs"],
+            "misses_per_step": head["misses_per_step"],
+            "h2d_gb_per_step": head["h2d_gb_per_step"],
+            "kernel_ms_per_step": head["kernel_ms"],
+            "sweep": {str(T): {kk: (round(v, 4) if isinstance(v, float) else v) for kk, v in r.items()
+                               if kk not in ("kernel_ms",)} for T, r in results.items()},
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    T = args.cpu_sample_tokens
+    per = []
+    for _ in range(max(1, min(args.steps, 3))):
+        d = cpu_baseline(T, 1)
+        if d["value"] is None:
+            print(json.dumps({"impl": "reference", "unavailable": d["sample"]}))
+            return
+        per.append(T / d["value"])
+    ms = 1e3 * sum(per) / len(per)
+    value = T / (ms / 1e3)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": len(per), "warmup": 0, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generator)",
+        "config": {"workload": f"decode layer H=4096 I=2048 E=256 top_k=8 + FP8 shared, 64-slot cache, "
+                               f"Zipf(1.1) routing trace, bounded sample of T={T} tokens per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{len(per)} step(s) x {T} tokens, single-threaded fp64 NumPy"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+if __name__ == "__main__":
+    a = _args()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)

@@ -1,0 +1,274 @@
+/*
+ * moe_gb300.h -- C ABI of the routed mixture-of-experts layer served from a
+ * GPU expert-slot cache (single GB300 GPU, sm_103a).
+ *
+ * The calls follow the problem statement in "Running DeepSeek-V4-Flash across
+ * four free GPUs", section "What the expert cache actually does": the router
+ * picks top_k experts per token, ensure_experts remaps the expert ids in place
+ * onto cache slots, copy_missing moves only the misses from pinned host RAM,
+ * and a grouped expert GEMM runs over the slot views.  The per-layer single
+ * host synchronisation to read the router's picks is from "An elephant
+ * through a straw", section "43 graphs, 43 syncs"; the (a,b) precision ladder
+ * from its section "Not all six experts matter equally".
+ *
+ * Conventions for every call:
+ *  - The caller owns every buffer it passes (device tensors, the pinned host
+ *    bank, host miss lists).  The library owns only the opaque cache handle
+ *    and the cache's device LRU arrays.
+ *  - Pointers marked "device" must be device (or managed) memory; "host"
+ *    pointers must be host memory.  Sizes are element counts unless stated.
+ *  - Every call returns a moe_status.  Calls taking a cudaStream_t are
+ *    asynchronous on that stream unless stated otherwise.  No call aborts,
+ *    prints or synchronises the device implicitly.  moe_last_error() gives a
+ *    message for the calling thread's last failure.
+ *  - Errors that can only be seen on the device (an expert id >= E inside
+ *    ids, a capacity overflow found while scanning) are reported through the
+ *    device output words documented per call, never by a fault.
+ *  - Matrices are row-major.  An MXFP4 expert is stored in the canonical
+ *    layout: for gate w1 [I,H], up w3 [I,H], down w2 [H,I] in that order,
+ *    codes [N][K/2] (two E2M1 codes per byte, element 2j in the low nibble)
+ *    then E8M0 scales [N][K/32].  The 2-bit copy: codes [N][K/4] (element 4j+q
+ *    at bits 2q..2q+1, value (q - 1.5) * scale) then E4M3 scales [N][K/32].
+ *    The shared expert: E4M3 codes [N][K] then fp32 row scales [N].
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID = 1,   /* bad argument (null pointer, size, range, alignment) */
+  MOE_ERR_CAPACITY = 2,  /* a single token needs more experts than the pool has slots */
+  MOE_ERR_CUDA = 3,      /* a CUDA runtime call failed (message has the CUDA error) */
+  MOE_ERR_TIMEOUT = 4,   /* reserved: no call in this library waits on the device */
+  MOE_ERR_NOMEM = 5      /* library-owned allocation failed */
+} moe_status;
+
+enum { MOE_FETCH = 0, MOE_LOOKUP = 1 };
+enum { MOE_TAG_FP4 = 0, MOE_TAG_INT2 = 1, MOE_TAG_DROP = 2 };
+enum { MOE_POOL_FP4 = 0, MOE_POOL_INT2 = 1, MOE_POOL_SHARED = 2 };
+enum { MOE_W1 = 0, MOE_W3 = 1, MOE_W2 = 2 };
+
+/* Message of the calling thread's last failed call ("" if none).  The pointer
+ * stays valid until the thread's next library call. */
+const char* moe_last_error(void);
+int moe_version(void);
+
+/* Byte size of one expert in each format (0 if H or I is not a multiple of 32). */
+size_t moe_fp4_expert_bytes(int H, int I);
+size_t moe_int2_expert_bytes(int H, int I);
+size_t moe_fp8_expert_bytes(int H, int I);
+
+/* ---------------------------------------------------------------------------
+ * Router: softmax over E logits, keep the top k, renormalise.
+ * ("Running DeepSeek-V4-Flash across four free GPUs", section "What the expert
+ * cache actually does"; "An elephant through a straw", section "Not all six
+ * experts matter equally".)
+ *   logits   device fp32 [T, E], finite (non-finite logits give unspecified ids)
+ *   topk_ids device int32 [T, k] out: the k largest logits of each row, in
+ *            descending order, ties to the lower expert id
+ *   topk_w   device fp32 [T, k] out: renorm != 0 -> exp(l_j - max) / sum over
+ *            the kept of exp(l_i - max) (sums to 1); renorm == 0 -> the full
+ *            softmax probability of each kept expert
+ *   1 <= k <= min(E, 32), 1 <= E <= 2048, T >= 0 (T == 0 launches nothing).
+ * ------------------------------------------------------------------------- */
+moe_status moe_router_topk(const float* logits, int T, int E, int k, int renorm,
+                           int32_t* topk_ids, float* topk_w, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Expert-slot cache ("What the expert cache actually does": a fixed number of
+ * VRAM slots shared by all layers, LRU eviction, only misses copied from a
+ * pinned host bank).  Key of an expert = layer * num_experts + expert.
+ *   num_slots      S >= 1 slots of expert_bytes each at d_slots (device,
+ *                  caller-owned, S * expert_bytes bytes, 16-byte aligned)
+ *   h_bank         host memory holding num_layers * num_experts experts back to
+ *                  back (key * expert_bytes); must be page-locked (registered
+ *                  or cudaHostAlloc'ed); may be NULL for a cache that is only
+ *                  ever filled by the caller (then moe_copy_missing fails)
+ *   out            receives the handle; the cache starts empty.
+ * Allocates the device LRU state (slot_key int32 [S], slot_stamp uint64 [S],
+ * key_to_slot int32 [L*E], clock uint64) on the current device, synchronously.
+ * ------------------------------------------------------------------------- */
+typedef struct moe_cache moe_cache;
+
+moe_status moe_cache_create(int num_slots, int num_layers, int num_experts,
+                            size_t expert_bytes, void* d_slots, const void* h_bank,
+                            moe_cache** out);
+moe_status moe_cache_destroy(moe_cache* cache);
+/* Empty every slot and reset the clock (asynchronous on stream). */
+moe_status moe_cache_reset(moe_cache* cache, cudaStream_t stream);
+/* Device pointers of the LRU state, for inspection (not to be freed). */
+moe_status moe_cache_state(moe_cache* cache, int32_t** slot_key, uint64_t** slot_stamp,
+                           int32_t** key_to_slot, uint64_t** clock);
+/* Copy the LRU state to host arrays (slot_key [S], slot_stamp [S], clock [1]);
+ * synchronous.  moe_cache_import restores it (key_to_slot is rebuilt) and
+ * rejects states with out-of-range or duplicate keys. */
+moe_status moe_cache_export(moe_cache* cache, int32_t* h_slot_key, uint64_t* h_slot_stamp,
+                            uint64_t* h_clock);
+moe_status moe_cache_import(moe_cache* cache, const int32_t* h_slot_key,
+                            const uint64_t* h_slot_stamp, uint64_t clock);
+
+/* ---------------------------------------------------------------------------
+ * ensure_experts: remap expert ids of tokens [token_begin, T) and ranks
+ * [rank_lo, rank_hi) onto slots, in first-appearance order (token-major,
+ * then rank).  Entries holding a negative id are skipped.
+ *   ids        device int32 [T, k] expert ids (< num_experts)
+ *   slots_out  device int32 [T, k]; may alias ids (in-place remap, as the
+ *              pages' ensure_experts).  Only the processed entries are written.
+ *   mode MOE_FETCH:  the longest token prefix from token_begin whose distinct
+ *              experts fit the S slots is processed.  Hits keep their slot;
+ *              misses take empty slots (ascending index) then the least
+ *              recently used slots not needed by this call.  Every distinct
+ *              key's recency stamp becomes clock + its first-appearance index.
+ *              The misses are listed as (key, slot) pairs in first-appearance
+ *              order; the bytes must then be copied (moe_copy_missing) before
+ *              the slots are read.
+ *   mode MOE_LOOKUP: every token from token_begin is processed; hits get their
+ *              slot and a fresh stamp, misses get -1; nothing is evicted or listed.
+ *   d_miss_key, d_miss_slot  device int32 [>= min(S, num_experts)] out
+ *   d_miss_count   device int32 [1] out: number of misses; on a device-detected
+ *              error it is negative: -MOE_ERR_CAPACITY (a single token needs
+ *              more than S slots) or -MOE_ERR_INVALID (an id >= num_experts);
+ *              the cache state is then unchanged.
+ *   d_tokens_done  device int32 [1] out: one past the last processed token;
+ *              a value < T asks the caller to copy, compute and call again
+ *              with token_begin = tokens_done.
+ * Limits: k <= 64; (T - token_begin) * (rank_hi - rank_lo) <= 65536;
+ * num_experts <= 4096.  One thread block; stream-ordered with other calls on
+ * the same cache (calls on one cache must not overlap on the GPU).
+ * ------------------------------------------------------------------------- */
+moe_status moe_slot_ensure(moe_cache* cache, int layer_id, const int32_t* ids, int32_t* slots_out,
+                           int T, int k, int rank_lo, int rank_hi, int mode, int token_begin,
+                           int32_t* d_miss_key, int32_t* d_miss_slot, int32_t* d_miss_count,
+                           int32_t* d_tokens_done, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * copy_missing: for each listed miss, copy expert_bytes from
+ * h_bank + key * expert_bytes to d_slots + slot * expert_bytes with one
+ * cudaMemcpyAsync on copy_stream, in list order.  ready (may be NULL) is
+ * waited on by copy_stream first; done (may be NULL) is recorded on
+ * copy_stream after the last copy, for the compute stream to wait on.
+ *   h_miss_key, h_miss_slot  host int32 [n_miss] (the lists read back after
+ *                            the per-layer synchronisation)
+ * On a failed copy, the slots of that miss and of every later one are marked
+ * empty on the device (the earlier copies stand), and MOE_ERR_CUDA is returned.
+ * ------------------------------------------------------------------------- */
+moe_status moe_copy_missing(moe_cache* cache, const int32_t* h_miss_key,
+                            const int32_t* h_miss_slot, int n_miss, cudaStream_t copy_stream,
+                            cudaEvent_t ready, cudaEvent_t done);
+/* Test hook: make the copy with list index `index` of later moe_copy_missing
+ * calls fail on the host, as if cudaMemcpyAsync had returned an error
+ * (index < 0 disarms).  Nothing is issued to the device for a failed copy. */
+moe_status moe_debug_fail_copy(moe_cache* cache, int index);
+
+/* ---------------------------------------------------------------------------
+ * Precision ladder (a, b) over an FP4 cache and a 2-bit-copy cache
+ * ("An elephant through a straw", section "Not all six experts matter
+ * equally").  Ranks are 1-based on the page; here ranks [0, a) always use
+ * FP4 (fetched if missing); ranks [a, b) use FP4 if resident, else the 2-bit
+ * copy (fetched if missing); ranks [b, k) use FP4 if resident, else the 2-bit
+ * copy if resident, else are dropped.  Passes run over the whole chunk in
+ * that order; the chunk is the longest token prefix from token_begin whose
+ * distinct rank-[0,a) experts fit the FP4 cache and whose distinct
+ * rank-[a,b) experts fit the 2-bit cache.  Survivor weights are renormalised.
+ *   ids, w      device int32 / fp32 [T, k] (router output)
+ *   slots_out   device int32 [T, k]: slot in the tagged pool, -1 if dropped
+ *   tags_out    device int8  [T, k]: MOE_TAG_FP4 / MOE_TAG_INT2 / MOE_TAG_DROP
+ *   w_out       device fp32  [T, k]: renormalised weights, 0 if dropped
+ *   miss lists and counts per pool as for moe_slot_ensure (counts negative on
+ *   a device-detected error); d_tokens_done as for moe_slot_ensure.
+ * Limits as moe_slot_ensure; 1 <= a <= b <= k.
+ * ------------------------------------------------------------------------- */
+moe_status moe_ladder_classify(moe_cache* fp4_cache, moe_cache* int2_cache, int layer_id,
+                               const int32_t* ids, const float* w, int T, int k, int a, int b,
+                               int token_begin, int32_t* slots_out, int8_t* tags_out,
+                               float* w_out, int32_t* d_miss4_key, int32_t* d_miss4_slot,
+                               int32_t* d_miss4_count, int32_t* d_miss2_key,
+                               int32_t* d_miss2_slot, int32_t* d_miss2_count,
+                               int32_t* d_tokens_done, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Grouping of (token, rank) pairs by expert (the permutation in front of a
+ * grouped GEMM; "Running DeepSeek-V4-Flash across four free GPUs", section
+ * "All four workers die, but only on prompts over 32 tokens").
+ *   ids      device int32 [T, k]; negative ids are left out
+ *   offsets  device int32 [E + 1] out: first position of each expert in perm
+ *   perm     device int32 [T * k] out: flat pair indices t*k + j stably sorted
+ *            by id (positions >= offsets[E] are left unwritten)
+ *   d_error  device int32 [1] out: 0, or MOE_ERR_INVALID if an id >= E
+ * ------------------------------------------------------------------------- */
+moe_status moe_group_pairs(const int32_t* ids, int T, int k, int E, int32_t* offsets,
+                           int32_t* perm, int32_t* d_error, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Grouped expert MLP + combine.  For every kept pair (t, j):
+ * h = SiLU(W1 x_t) * (W3 x_t), o = W2 h, and
+ * y_t = sum_j w[t,j] * o[t,j] + shared(x_t), rounded to bf16.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  int H, I;                    /* hidden and intermediate sizes, multiples of 32 */
+  const uint8_t* fp4_slots;    /* device: FP4 slot s at fp4_slots + s * moe_fp4_expert_bytes */
+  int fp4_num_slots;
+  const uint8_t* int2_slots;   /* device or NULL: 2-bit-copy slot s at int2_slots + s * bytes */
+  int int2_num_slots;
+  const uint8_t* shared;       /* device or NULL: the FP8 shared expert */
+} moe_expert_views;
+
+/* Workspace bytes moe_expert_forward needs for T tokens of k pairs each. */
+size_t moe_expert_forward_workspace(const moe_expert_views* v, int T, int k);
+
+/*   x        device bf16 [T, H] (uint16 bit patterns)
+ *   slots    device int32 [T, k]: slot of each pair in the pool given by tags
+ *   tags     device int8 [T, k] or NULL (all MOE_TAG_FP4); MOE_TAG_DROP pairs
+ *            and pairs with a negative slot are skipped
+ *   w        device fp32 [T, k] router weights
+ *   y        device bf16 [T, H] out
+ *   workspace device, >= moe_expert_forward_workspace bytes, 256-byte aligned
+ *   d_error  device int32 [1] out: 0, or MOE_ERR_INVALID if a slot >= the
+ *            pool's slot count (the pair is then skipped)
+ * Numerics: weights are decoded exactly; activations are held in fp16 with a
+ * per-token power-of-two scale; 32-weight partial sums accumulate in fp16 and
+ * are scaled and summed in fp32; the combine runs in fp32 in rank order. */
+moe_status moe_expert_forward(const moe_expert_views* v, const uint16_t* x, int T, int k,
+                              const int32_t* slots, const int8_t* tags, const float* w,
+                              uint16_t* y, void* workspace, size_t workspace_bytes,
+                              int32_t* d_error, cudaStream_t stream);
+
+/* Decode one matrix of one slot to fp32 [N, K] (test hook; values are exact). */
+moe_status moe_dequant_debug(const moe_expert_views* v, int pool, int slot, int matrix,
+                             float* out, cudaStream_t stream);
+
+/* Next layer's input for a stack of layers: x_next = bf16(y / sqrt(mean(y^2) + eps))
+ * per token, computed in fp32 (a weightless RMSNorm).  y and x_next device bf16 [T, H]. */
+moe_status moe_rms_carry(const uint16_t* y, int T, int H, float eps, uint16_t* x_next,
+                         cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Per-kernel timing: when enabled, every kernel the library launches is
+ * bracketed by two CUDA events recorded on its launching stream.
+ * moe_profile_enable(1) clears the record and starts collecting; (0) stops.
+ * moe_profile_query synchronises on the recorded events and returns, for one
+ * kernel id, the summed elapsed milliseconds and the number of launches.
+ * ------------------------------------------------------------------------- */
+enum {
+  MOE_K_ROUTER = 0, MOE_K_ENSURE, MOE_K_LADDER, MOE_K_GROUP, MOE_K_PLAN, MOE_K_GATEUP,
+  MOE_K_DOWN, MOE_K_COMBINE, MOE_K_CARRY, MOE_K_COUNT
+};
+moe_status moe_profile_enable(int enable);
+moe_status moe_profile_query(int kernel, double* total_ms, int* launches);
+
+/* Runs a tiny router + cache + copy round trip on the current device and
+ * checks it (synchronous).  MOE_OK means the library executes here. */
+moe_status moe_selftest(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

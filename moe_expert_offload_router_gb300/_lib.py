@@ -1,0 +1,275 @@
+"""ctypes binding of libmoe_gb300.so: one Python function per C entry point,
+same names, argument marshalling only (torch tensors -> raw pointers, torch
+streams/events -> handles).  Every computation runs in the library's kernels;
+if the library is not built this module raises on import."""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
+
+MOE_OK, MOE_ERR_INVALID, MOE_ERR_CAPACITY, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_NOMEM = range(6)
+MOE_FETCH, MOE_LOOKUP = 0, 1
+MOE_TAG_FP4, MOE_TAG_INT2, MOE_TAG_DROP = 0, 1, 2
+MOE_POOL_FP4, MOE_POOL_INT2, MOE_POOL_SHARED = 0, 1, 2
+MOE_W1, MOE_W3, MOE_W2 = 0, 1, 2
+(MOE_K_ROUTER, MOE_K_ENSURE, MOE_K_LADDER, MOE_K_GROUP, MOE_K_PLAN, MOE_K_GATEUP, MOE_K_DOWN,
+ MOE_K_COMBINE, MOE_K_CARRY, MOE_K_COUNT) = range(10)
+KERNEL_NAMES = ["router", "ensure", "ladder", "group_pairs", "plan", "gateup", "down", "combine",
+                "rms_carry"]
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_CAPACITY", 3: "MOE_ERR_CUDA",
+                4: "MOE_ERR_TIMEOUT", 5: "MOE_ERR_NOMEM"}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is not built; run moe_expert_offload_router_gb300.build.build()")
+_lib = C.CDLL(LIB_PATH)
+
+vp, i32, sz, f32, u64 = C.c_void_p, C.c_int, C.c_size_t, C.c_float, C.c_uint64
+P_i32, P_u64 = C.POINTER(C.c_int32), C.POINTER(C.c_uint64)
+
+
+class moe_expert_views(C.Structure):
+    _fields_ = [("H", i32), ("I", i32), ("fp4_slots", vp), ("fp4_num_slots", i32),
+                ("int2_slots", vp), ("int2_num_slots", i32), ("shared", vp)]
+
+
+_SIGS = {
+    "moe_last_error": (C.c_char_p, []),
+    "moe_version": (i32, []),
+    "moe_fp4_expert_bytes": (sz, [i32, i32]),
+    "moe_int2_expert_bytes": (sz, [i32, i32]),
+    "moe_fp8_expert_bytes": (sz, [i32, i32]),
+    "moe_router_topk": (i32, [vp, i32, i32, i32, i32, vp, vp, vp]),
+    "moe_cache_create": (i32, [i32, i32, i32, sz, vp, vp, C.POINTER(vp)]),
+    "moe_cache_destroy": (i32, [vp]),
+    "moe_cache_reset": (i32, [vp, vp]),
+    "moe_cache_state": (i32, [vp, C.POINTER(vp), C.POINTER(vp), C.POINTER(vp), C.POINTER(vp)]),
+    "moe_cache_export": (i32, [vp, vp, vp, vp]),
+    "moe_cache_import": (i32, [vp, vp, vp, u64]),
+    "moe_slot_ensure": (i32, [vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp]),
+    "moe_copy_missing": (i32, [vp, vp, vp, i32, vp, vp, vp]),
+    "moe_debug_fail_copy": (i32, [vp, i32]),
+    "moe_ladder_classify": (i32, [vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp,
+                                  vp, vp, vp, vp, vp, vp, vp, vp]),
+    "moe_group_pairs": (i32, [vp, i32, i32, i32, vp, vp, vp, vp]),
+    "moe_expert_forward_workspace": (sz, [C.POINTER(moe_expert_views), i32, i32]),
+    "moe_expert_forward": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, vp,
+                                 sz, vp, vp]),
+    "moe_dequant_debug": (i32, [C.POINTER(moe_expert_views), i32, i32, i32, vp, vp]),
+    "moe_rms_carry": (i32, [vp, i32, i32, f32, vp, vp]),
+    "moe_selftest": (i32, []),
+    "moe_profile_enable": (i32, [i32]),
+    "moe_profile_query": (i32, [i32, C.POINTER(C.c_double), C.POINTER(C.c_int)]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+
+def raw():
+    """The ctypes library handle."""
+    return _lib
+
+
+def _check(status: int):
+    if status != MOE_OK:
+        raise MoeError(status, _lib.moe_last_error().decode(errors="replace"))
+
+
+def _p(t):
+    """Raw data pointer of a tensor (or None)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _s(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _e(event):
+    if event is None:
+        return None
+    return event.cuda_event
+
+
+def moe_version() -> int:
+    return _lib.moe_version()
+
+
+def moe_fp4_expert_bytes(H: int, I: int) -> int:
+    return _lib.moe_fp4_expert_bytes(H, I)
+
+
+def moe_int2_expert_bytes(H: int, I: int) -> int:
+    return _lib.moe_int2_expert_bytes(H, I)
+
+
+def moe_fp8_expert_bytes(H: int, I: int) -> int:
+    return _lib.moe_fp8_expert_bytes(H, I)
+
+
+def moe_router_topk(logits, k: int, renorm: bool = True, topk_ids=None, topk_w=None, stream=None):
+    T, E = logits.shape
+    dev = logits.device
+    if topk_ids is None:
+        topk_ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    _check(_lib.moe_router_topk(_p(logits), T, E, k, int(bool(renorm)), _p(topk_ids), _p(topk_w),
+                                _s(stream)))
+    return topk_ids, topk_w
+
+
+class moe_cache:
+    """Owner of one library slot cache (moe_cache_create / moe_cache_destroy)."""
+
+    def __init__(self, num_slots: int, num_layers: int, num_experts: int, expert_bytes: int,
+                 d_slots, h_bank=None):
+        h = vp()
+        _check(_lib.moe_cache_create(num_slots, num_layers, num_experts, expert_bytes, _p(d_slots),
+                                     _p(h_bank), C.byref(h)))
+        self.handle = h
+        self.S, self.L, self.E, self.B = num_slots, num_layers, num_experts, expert_bytes
+        self._keep = (d_slots, h_bank)
+
+    def close(self):
+        if self.handle:
+            _check(_lib.moe_cache_destroy(self.handle))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def reset(self, stream=None):
+        _check(_lib.moe_cache_reset(self.handle, _s(stream)))
+
+    def export(self):
+        import numpy as np
+        key = np.empty(self.S, dtype=np.int32)
+        stamp = np.empty(self.S, dtype=np.uint64)
+        clock = np.empty(1, dtype=np.uint64)
+        _check(_lib.moe_cache_export(self.handle, key.ctypes.data, stamp.ctypes.data, clock.ctypes.data))
+        return key, stamp, int(clock[0])
+
+    def import_(self, key, stamp, clock: int):
+        import numpy as np
+        key = np.ascontiguousarray(key, dtype=np.int32)
+        stamp = np.ascontiguousarray(stamp, dtype=np.uint64)
+        _check(_lib.moe_cache_import(self.handle, key.ctypes.data, stamp.ctypes.data, clock))
+
+    def state_pointers(self):
+        a, b, c, d = vp(), vp(), vp(), vp()
+        _check(_lib.moe_cache_state(self.handle, C.byref(a), C.byref(b), C.byref(c), C.byref(d)))
+        return a.value, b.value, c.value, d.value
+
+
+def moe_slot_ensure(cache: moe_cache, layer_id: int, ids, slots_out, rank_lo: int, rank_hi: int,
+                    mode: int, token_begin: int, d_miss_key, d_miss_slot, d_miss_count,
+                    d_tokens_done, stream=None):
+    T, k = ids.shape
+    _check(_lib.moe_slot_ensure(cache.handle, layer_id, _p(ids), _p(slots_out), T, k, rank_lo, rank_hi,
+                                mode, token_begin, _p(d_miss_key), _p(d_miss_slot), _p(d_miss_count),
+                                _p(d_tokens_done), _s(stream)))
+
+
+def moe_copy_missing(cache: moe_cache, h_miss_key, h_miss_slot, n_miss: int, copy_stream=None,
+                     ready=None, done=None):
+    """h_miss_key / h_miss_slot: host int32 arrays (numpy or CPU tensors)."""
+    def hp(a):
+        if a is None:
+            return None
+        return a.data_ptr() if hasattr(a, "data_ptr") else a.ctypes.data
+    _check(_lib.moe_copy_missing(cache.handle, hp(h_miss_key), hp(h_miss_slot), n_miss,
+                                 _s(copy_stream), _e(ready), _e(done)))
+
+
+def moe_debug_fail_copy(cache: moe_cache, index: int):
+    _check(_lib.moe_debug_fail_copy(cache.handle, index))
+
+
+def moe_ladder_classify(c4: moe_cache, c2: moe_cache, layer_id: int, ids, w, a: int, b: int,
+                        token_begin: int, slots_out, tags_out, w_out, miss4_key, miss4_slot,
+                        miss4_count, miss2_key, miss2_slot, miss2_count, tokens_done, stream=None):
+    T, k = ids.shape
+    _check(_lib.moe_ladder_classify(c4.handle, c2.handle, layer_id, _p(ids), _p(w), T, k, a, b,
+                                    token_begin, _p(slots_out), _p(tags_out), _p(w_out),
+                                    _p(miss4_key), _p(miss4_slot), _p(miss4_count), _p(miss2_key),
+                                    _p(miss2_slot), _p(miss2_count), _p(tokens_done), _s(stream)))
+
+
+def moe_group_pairs(ids, E: int, offsets=None, perm=None, d_error=None, stream=None):
+    T, k = ids.shape
+    dev = ids.device
+    if offsets is None:
+        offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    if perm is None:
+        perm = torch.empty(T * k, dtype=torch.int32, device=dev)
+    if d_error is None:
+        d_error = torch.empty(1, dtype=torch.int32, device=dev)
+    _check(_lib.moe_group_pairs(_p(ids), T, k, E, _p(offsets), _p(perm), _p(d_error), _s(stream)))
+    return offsets, perm, d_error
+
+
+def make_views(H: int, I: int, fp4_slots=None, fp4_num_slots: int = 0, int2_slots=None,
+               int2_num_slots: int = 0, shared=None) -> moe_expert_views:
+    v = moe_expert_views(H, I, _p(fp4_slots), fp4_num_slots, _p(int2_slots), int2_num_slots, _p(shared))
+    v._keep = (fp4_slots, int2_slots, shared)
+    return v
+
+
+def moe_expert_forward_workspace(views: moe_expert_views, T: int, k: int) -> int:
+    return _lib.moe_expert_forward_workspace(C.byref(views), T, k)
+
+
+def moe_expert_forward(views: moe_expert_views, x, slots, tags, w, y, workspace, d_error=None,
+                       stream=None):
+    T, k = slots.shape
+    _check(_lib.moe_expert_forward(C.byref(views), _p(x), T, k, _p(slots), _p(tags), _p(w), _p(y),
+                                   _p(workspace), workspace.numel() * workspace.element_size(),
+                                   _p(d_error), _s(stream)))
+
+
+def moe_dequant_debug(views: moe_expert_views, pool: int, slot: int, matrix: int, out, stream=None):
+    _check(_lib.moe_dequant_debug(C.byref(views), pool, slot, matrix, _p(out), _s(stream)))
+
+
+def moe_rms_carry(y, eps: float, x_next, stream=None):
+    T, H = y.shape
+    _check(_lib.moe_rms_carry(_p(y), T, H, eps, _p(x_next), _s(stream)))
+
+
+def moe_selftest():
+    _check(_lib.moe_selftest())
+
+
+def moe_profile_enable(enable: bool = True):
+    _check(_lib.moe_profile_enable(int(bool(enable))))
+
+
+def moe_profile_query(kernel: int):
+    """(total milliseconds, launches) recorded for one kernel id since profiling was enabled."""
+    ms, n = C.c_double(), C.c_int()
+    _check(_lib.moe_profile_query(kernel, C.byref(ms), C.byref(n)))
+    return ms.value, n.value

@@ -1,0 +1,387 @@
+// Host side of the C ABI: error reporting, the slot-cache handle, the miss
+// copies from the pinned host bank, and the load-time self test.
+//
+// The cache mirrors "Running DeepSeek-V4-Flash across four free GPUs",
+// section "What the expert cache actually does": expert banks in pinned host
+// RAM, a fixed number of VRAM slots, only the misses cross to the GPU.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+
+namespace moe {
+
+static thread_local std::string g_err;
+
+moe_status fail(moe_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+moe_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MOE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+void clear_error() { g_err.clear(); }
+
+// ------------------------------------------------------------- profiling --
+struct ProfRec {
+  int kernel;
+  cudaEvent_t start, stop;
+};
+static std::mutex g_prof_mu;
+static bool g_prof_on = false;
+static std::vector<ProfRec> g_prof;
+static std::vector<cudaEvent_t> g_prof_pool;
+
+static cudaEvent_t prof_event() {
+  if (!g_prof_pool.empty()) {
+    cudaEvent_t e = g_prof_pool.back();
+    g_prof_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+ProfScope::ProfScope(int kernel, cudaStream_t s) : k_(kernel), s_(s), stop_(nullptr) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof_on) return;
+  cudaEvent_t a = prof_event(), b = prof_event();
+  if (!a || !b) return;
+  cudaEventRecord(a, s);
+  g_prof.push_back({kernel, a, b});
+  stop_ = b;
+}
+
+ProfScope::~ProfScope() {
+  if (stop_) cudaEventRecord((cudaEvent_t)stop_, s_);
+}
+
+size_t fp4_bytes(int H, int I) {
+  if (H <= 0 || I <= 0 || H % 32 || I % 32) return 0;
+  size_t h = (size_t)H, i = (size_t)I;
+  return 3 * (h * i / 2 + h * i / 32);
+}
+size_t int2_bytes(int H, int I) {
+  if (H <= 0 || I <= 0 || H % 32 || I % 32) return 0;
+  size_t h = (size_t)H, i = (size_t)I;
+  return 3 * (h * i / 4 + h * i / 32);
+}
+size_t fp8_bytes(int H, int I) {
+  if (H <= 0 || I <= 0 || H % 32 || I % 32) return 0;
+  size_t h = (size_t)H, i = (size_t)I;
+  return 3 * h * i + (2 * i + h) * 4;
+}
+
+__global__ void cache_reset_kernel(CacheDev c) {
+  const int n = c.L * c.E;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    c.key_to_slot[i] = -1;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < c.S; i += gridDim.x * blockDim.x) {
+    c.slot_key[i] = -1;
+    c.slot_stamp[i] = 0;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *c.clock = 0;
+}
+
+__global__ void cache_mark_empty_kernel(CacheDev c, int slot) {
+  int key = c.slot_key[slot];
+  if (key >= 0) c.key_to_slot[key] = -1;
+  c.slot_key[slot] = -1;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_last_error(void) { return g_err.c_str(); }
+int moe_version(void) { return 1; }
+
+size_t moe_fp4_expert_bytes(int H, int I) { return fp4_bytes(H, I); }
+size_t moe_int2_expert_bytes(int H, int I) { return int2_bytes(H, I); }
+size_t moe_fp8_expert_bytes(int H, int I) { return fp8_bytes(H, I); }
+
+moe_status moe_cache_create(int num_slots, int num_layers, int num_experts, size_t expert_bytes,
+                            void* d_slots, const void* h_bank, moe_cache** out) {
+  clear_error();
+  MOE_ARG(out != nullptr, "out is null");
+  *out = nullptr;
+  MOE_ARG(num_slots >= 1, "num_slots must be >= 1 (got %d)", num_slots);
+  MOE_ARG(num_layers >= 1 && num_experts >= 1, "num_layers and num_experts must be >= 1");
+  MOE_ARG(num_experts <= 4096, "num_experts must be <= 4096");
+  MOE_ARG((long long)num_layers * num_experts < (1LL << 30), "too many keys");
+  MOE_ARG(expert_bytes > 0 && expert_bytes % 16 == 0, "expert_bytes must be a positive multiple of 16");
+  MOE_ARG(d_slots != nullptr, "d_slots is null");
+  MOE_ARG(((uintptr_t)d_slots & 15) == 0, "d_slots must be 16-byte aligned");
+  cudaPointerAttributes pa;
+  MOE_CUDA(cudaPointerGetAttributes(&pa, d_slots));
+  MOE_ARG(pa.type == cudaMemoryTypeDevice || pa.type == cudaMemoryTypeManaged,
+          "d_slots is not device memory");
+  if (h_bank != nullptr) {
+    cudaPointerAttributes hb;
+    MOE_CUDA(cudaPointerGetAttributes(&hb, h_bank));
+    MOE_ARG(hb.type == cudaMemoryTypeHost,
+            "h_bank is not page-locked host memory (allocate it pinned or register it)");
+  }
+  int dev = 0;
+  MOE_CUDA(cudaGetDevice(&dev));
+  const size_t S = (size_t)num_slots, K = (size_t)num_layers * num_experts;
+  const size_t bytes = S * 8 + S * 4 + K * 4 + 8 + 64;
+  void* state = nullptr;
+  cudaError_t e = cudaMalloc(&state, bytes);
+  if (e != cudaSuccess) return fail(MOE_ERR_NOMEM, "cudaMalloc of %zu bytes of cache state: %s", bytes,
+                                    cudaGetErrorString(e));
+  moe_cache* c = new moe_cache();
+  c->S = num_slots;
+  c->L = num_layers;
+  c->E = num_experts;
+  c->B = expert_bytes;
+  c->d_slots = (uint8_t*)d_slots;
+  c->h_bank = (const uint8_t*)h_bank;
+  c->d_state = state;
+  c->device = dev;
+  c->fail_copy_index = -1;
+  uint8_t* p = (uint8_t*)state;
+  c->dev.slot_stamp = (uint64_t*)p;
+  p += S * 8;
+  c->dev.clock = (uint64_t*)p;
+  p += 8;
+  c->dev.slot_key = (int32_t*)p;
+  p += S * 4;
+  c->dev.key_to_slot = (int32_t*)p;
+  c->dev.S = num_slots;
+  c->dev.L = num_layers;
+  c->dev.E = num_experts;
+  cache_reset_kernel<<<64, 256>>>(c->dev);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(state);
+    delete c;
+    return cuda_fail(e, "cache reset");
+  }
+  *out = c;
+  return MOE_OK;
+}
+
+moe_status moe_cache_destroy(moe_cache* c) {
+  clear_error();
+  if (c == nullptr) return MOE_OK;
+  cudaError_t e = cudaFree(c->d_state);
+  delete c;
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFree(cache state)");
+  return MOE_OK;
+}
+
+moe_status moe_cache_reset(moe_cache* c, cudaStream_t s) {
+  clear_error();
+  MOE_ARG(c != nullptr, "cache is null");
+  cache_reset_kernel<<<64, 256, 0, s>>>(c->dev);
+  return check_launch("cache_reset_kernel");
+}
+
+moe_status moe_cache_state(moe_cache* c, int32_t** slot_key, uint64_t** slot_stamp,
+                           int32_t** key_to_slot, uint64_t** clock) {
+  clear_error();
+  MOE_ARG(c != nullptr, "cache is null");
+  if (slot_key) *slot_key = c->dev.slot_key;
+  if (slot_stamp) *slot_stamp = c->dev.slot_stamp;
+  if (key_to_slot) *key_to_slot = c->dev.key_to_slot;
+  if (clock) *clock = c->dev.clock;
+  return MOE_OK;
+}
+
+moe_status moe_cache_export(moe_cache* c, int32_t* h_slot_key, uint64_t* h_slot_stamp,
+                            uint64_t* h_clock) {
+  clear_error();
+  MOE_ARG(c != nullptr && h_slot_key && h_slot_stamp && h_clock, "null argument");
+  MOE_CUDA(cudaDeviceSynchronize());
+  MOE_CUDA(cudaMemcpy(h_slot_key, c->dev.slot_key, (size_t)c->S * 4, cudaMemcpyDeviceToHost));
+  MOE_CUDA(cudaMemcpy(h_slot_stamp, c->dev.slot_stamp, (size_t)c->S * 8, cudaMemcpyDeviceToHost));
+  MOE_CUDA(cudaMemcpy(h_clock, c->dev.clock, 8, cudaMemcpyDeviceToHost));
+  return MOE_OK;
+}
+
+moe_status moe_cache_import(moe_cache* c, const int32_t* h_slot_key, const uint64_t* h_slot_stamp,
+                            uint64_t clock) {
+  clear_error();
+  MOE_ARG(c != nullptr && h_slot_key && h_slot_stamp, "null argument");
+  const int K = c->L * c->E;
+  std::vector<int32_t> k2s((size_t)K, -1);
+  std::vector<uint64_t> seen;
+  for (int s = 0; s < c->S; ++s) {
+    int key = h_slot_key[s];
+    if (key < 0) continue;
+    MOE_ARG(key < K, "slot %d holds key %d >= L*E", s, key);
+    MOE_ARG(k2s[key] < 0, "key %d held by two slots", key);
+    MOE_ARG(h_slot_stamp[s] < clock, "slot %d has a stamp not below the clock", s);
+    k2s[key] = s;
+    seen.push_back(h_slot_stamp[s]);
+  }
+  std::sort(seen.begin(), seen.end());
+  for (size_t i = 1; i < seen.size(); ++i) MOE_ARG(seen[i] != seen[i - 1], "duplicate stamps");
+  MOE_CUDA(cudaDeviceSynchronize());
+  MOE_CUDA(cudaMemcpy(c->dev.slot_key, h_slot_key, (size_t)c->S * 4, cudaMemcpyHostToDevice));
+  MOE_CUDA(cudaMemcpy(c->dev.slot_stamp, h_slot_stamp, (size_t)c->S * 8, cudaMemcpyHostToDevice));
+  MOE_CUDA(cudaMemcpy(c->dev.key_to_slot, k2s.data(), (size_t)K * 4, cudaMemcpyHostToDevice));
+  MOE_CUDA(cudaMemcpy(c->dev.clock, &clock, 8, cudaMemcpyHostToDevice));
+  return MOE_OK;
+}
+
+moe_status moe_debug_fail_copy(moe_cache* c, int index) {
+  clear_error();
+  MOE_ARG(c != nullptr, "cache is null");
+  c->fail_copy_index = index;
+  return MOE_OK;
+}
+
+moe_status moe_copy_missing(moe_cache* c, const int32_t* h_miss_key, const int32_t* h_miss_slot,
+                            int n_miss, cudaStream_t copy_stream, cudaEvent_t ready,
+                            cudaEvent_t done) {
+  clear_error();
+  MOE_ARG(c != nullptr, "cache is null");
+  MOE_ARG(n_miss >= 0 && n_miss <= c->S, "n_miss %d out of [0, S]", n_miss);
+  MOE_ARG(n_miss == 0 || (h_miss_key && h_miss_slot), "null miss list");
+  MOE_ARG(n_miss == 0 || c->h_bank != nullptr, "cache has no host bank");
+  const int K = c->L * c->E;
+  for (int i = 0; i < n_miss; ++i) {
+    MOE_ARG(h_miss_key[i] >= 0 && h_miss_key[i] < K, "miss %d: key %d out of range", i, h_miss_key[i]);
+    MOE_ARG(h_miss_slot[i] >= 0 && h_miss_slot[i] < c->S, "miss %d: slot %d out of range", i,
+            h_miss_slot[i]);
+  }
+  if (ready) MOE_CUDA(cudaStreamWaitEvent(copy_stream, ready, 0));
+  int failed_at = -1;
+  cudaError_t err = cudaSuccess;
+  for (int i = 0; i < n_miss; ++i) {
+    if (i == c->fail_copy_index) {
+      failed_at = i;
+      err = cudaErrorUnknown;
+      break;
+    }
+    err = cudaMemcpyAsync(c->d_slots + (size_t)h_miss_slot[i] * c->B,
+                          c->h_bank + (size_t)h_miss_key[i] * c->B, c->B, cudaMemcpyHostToDevice,
+                          copy_stream);
+    if (err != cudaSuccess) {
+      failed_at = i;
+      break;
+    }
+  }
+  if (failed_at >= 0) {
+    // roll back: the failed miss and every later one hold nothing
+    for (int i = failed_at; i < n_miss; ++i)
+      cache_mark_empty_kernel<<<1, 1, 0, copy_stream>>>(c->dev, h_miss_slot[i]);
+    if (done) cudaEventRecord(done, copy_stream);
+    return fail(MOE_ERR_CUDA, "copy of miss %d (key %d -> slot %d) failed: %s; %d slot(s) marked empty",
+                failed_at, h_miss_key[failed_at], h_miss_slot[failed_at],
+                c->fail_copy_index == failed_at ? "injected failure" : cudaGetErrorString(err),
+                n_miss - failed_at);
+  }
+  if (done) MOE_CUDA(cudaEventRecord(done, copy_stream));
+  return MOE_OK;
+}
+
+moe_status moe_profile_enable(int enable) {
+  clear_error();
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (auto& r : g_prof) {
+    g_prof_pool.push_back(r.start);
+    g_prof_pool.push_back(r.stop);
+  }
+  g_prof.clear();
+  g_prof_on = enable != 0;
+  return MOE_OK;
+}
+
+moe_status moe_profile_query(int kernel, double* total_ms, int* launches) {
+  clear_error();
+  MOE_ARG(kernel >= 0 && kernel < MOE_K_COUNT && total_ms && launches, "bad arguments");
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  double t = 0.0;
+  int n = 0;
+  for (auto& r : g_prof) {
+    if (r.kernel != kernel) continue;
+    MOE_CUDA(cudaEventSynchronize(r.stop));
+    float ms = 0.f;
+    MOE_CUDA(cudaEventElapsedTime(&ms, r.start, r.stop));
+    t += ms;
+    ++n;
+  }
+  *total_ms = t;
+  *launches = n;
+  return MOE_OK;
+}
+
+moe_status moe_selftest(void) {
+  clear_error();
+  // Router on one known row, then a two-slot cache round trip with copies.
+  const int E = 4, k = 2, S = 2, B = 64;
+  float h_logits[E] = {0.5f, -1.0f, 2.0f, 0.5f};
+  float* d_logits = nullptr;
+  int32_t* d_i = nullptr;  // ids[2], slots[2], miss_key[2], miss_slot[2], count, done
+  float* d_w = nullptr;
+  uint8_t* d_slots = nullptr;
+  uint8_t* h_bank = nullptr;
+  moe_cache* c = nullptr;
+  moe_status st = MOE_OK;
+  int32_t h_i[10];
+  float h_w[2];
+  uint8_t h_slot_bytes[S * B];
+#define ST_CUDA(x)                                    \
+  do {                                                \
+    cudaError_t _e = (x);                             \
+    if (_e != cudaSuccess) {                          \
+      st = cuda_fail(_e, #x);                         \
+      goto out;                                       \
+    }                                                 \
+  } while (0)
+  ST_CUDA(cudaMalloc(&d_logits, sizeof h_logits));
+  ST_CUDA(cudaMalloc(&d_i, sizeof h_i));
+  ST_CUDA(cudaMalloc(&d_w, sizeof h_w));
+  ST_CUDA(cudaMalloc(&d_slots, S * B));
+  ST_CUDA(cudaHostAlloc(&h_bank, E * B, cudaHostAllocDefault));
+  for (int i = 0; i < E * B; ++i) h_bank[i] = (uint8_t)(i * 7 + 1);
+  ST_CUDA(cudaMemcpy(d_logits, h_logits, sizeof h_logits, cudaMemcpyHostToDevice));
+  if ((st = moe_router_topk(d_logits, 1, E, k, 1, d_i, d_w, 0)) != MOE_OK) goto out;
+  if ((st = moe_cache_create(S, 1, E, B, d_slots, h_bank, &c)) != MOE_OK) goto out;
+  if ((st = moe_slot_ensure(c, 0, d_i, d_i + 2, 1, k, 0, k, MOE_FETCH, 0, d_i + 4, d_i + 6, d_i + 8,
+                            d_i + 9, 0)) != MOE_OK)
+    goto out;
+  ST_CUDA(cudaMemcpy(h_i, d_i, sizeof h_i, cudaMemcpyDeviceToHost));
+  ST_CUDA(cudaMemcpy(h_w, d_w, sizeof h_w, cudaMemcpyDeviceToHost));
+  if (h_i[0] != 2 || h_i[1] != 0 || h_i[2] != 0 || h_i[3] != 1 || h_i[8] != 2 || h_i[9] != 1 ||
+      h_i[4] != 2 || h_i[5] != 0 || h_i[6] != 0 || h_i[7] != 1 || !(h_w[0] > h_w[1]) ||
+      h_w[0] + h_w[1] < 0.999f || h_w[0] + h_w[1] > 1.001f) {
+    st = fail(MOE_ERR_CUDA, "selftest: router/ensure produced wrong results");
+    goto out;
+  }
+  if ((st = moe_copy_missing(c, h_i + 4, h_i + 6, h_i[8], 0, nullptr, nullptr)) != MOE_OK) goto out;
+  ST_CUDA(cudaMemcpy(h_slot_bytes, d_slots, S * B, cudaMemcpyDeviceToHost));
+  if (memcmp(h_slot_bytes, h_bank + 2 * B, B) != 0 || memcmp(h_slot_bytes + B, h_bank, B) != 0)
+    st = fail(MOE_ERR_CUDA, "selftest: copied slot bytes differ from the bank");
+out:
+#undef ST_CUDA
+  if (c) moe_cache_destroy(c);
+  cudaFree(d_logits);
+  cudaFree(d_i);
+  cudaFree(d_w);
+  cudaFree(d_slots);
+  if (h_bank) cudaFreeHost(h_bank);
+  return st;
+}
+
+}  // extern "C"

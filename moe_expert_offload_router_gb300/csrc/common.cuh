@@ -1,0 +1,127 @@
+// Shared helpers of the library's translation units (host error handling,
+// the cache handle, small device utilities).  Device-side code here performs
+// no MoE arithmetic of its own.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "moe_gb300.h"
+
+namespace moe {
+
+moe_status fail(moe_status s, const char* fmt, ...);
+moe_status cuda_fail(cudaError_t e, const char* what);
+void clear_error();
+
+// Kernel launch check: a launch error is returned, not printed.
+inline moe_status check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return MOE_OK;
+}
+
+// Records a start event now and a stop event when the scope ends, on the
+// launching stream, if profiling is enabled (moe_profile_enable).
+class ProfScope {
+ public:
+  ProfScope(int kernel, cudaStream_t s);
+  ~ProfScope();
+
+ private:
+  int k_;
+  cudaStream_t s_;
+  void* stop_;
+};
+
+size_t fp4_bytes(int H, int I);
+size_t int2_bytes(int H, int I);
+size_t fp8_bytes(int H, int I);
+
+// Device LRU state of one slot cache, as passed to kernels.
+struct CacheDev {
+  int32_t* slot_key;     // [S] key held by the slot, -1 = empty
+  uint64_t* slot_stamp;  // [S] recency stamp (unique among occupied slots)
+  int32_t* key_to_slot;  // [L*E] slot of a key, -1 = not resident
+  uint64_t* clock;       // [1]
+  int S, L, E;
+};
+
+}  // namespace moe
+
+struct moe_cache {
+  int S, L, E;
+  size_t B;               // bytes per expert
+  uint8_t* d_slots;       // caller-owned slot pool
+  const uint8_t* h_bank;  // caller-owned pinned bank (may be null)
+  void* d_state;          // library-owned block holding the LRU arrays
+  moe::CacheDev dev;
+  int device;
+  int fail_copy_index;    // host-side fault injection for moe_copy_missing (-1 = off)
+};
+
+#define MOE_ARG(cond, ...)                                   \
+  do {                                                       \
+    if (!(cond)) return moe::fail(MOE_ERR_INVALID, __VA_ARGS__); \
+  } while (0)
+
+#define MOE_CUDA(call)                                       \
+  do {                                                       \
+    cudaError_t _e = (call);                                 \
+    if (_e != cudaSuccess) return moe::cuda_fail(_e, #call); \
+  } while (0)
+
+// ---------------------------------------------------------------------------
+// device utilities
+// ---------------------------------------------------------------------------
+namespace moe {
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  // Streamed weight bytes: read once per launch, keep them out of L1.
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim.x a multiple of 32,
+// at most 1024).  `ws` needs 33 ints of shared memory.  Returns the exclusive
+// prefix; *total receives the sum.  Contains __syncthreads.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* ws, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) ws[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int t = lane < nw ? ws[lane] : 0;
+    int ti = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(0xffffffffu, ti, o);
+      if (lane >= o) ti += n;
+    }
+    ws[lane] = ti - t;  // exclusive warp offsets
+    if (lane == 31) ws[32] = ti;
+  }
+  __syncthreads();
+  int r = ws[wid] + incl - v;
+  *total = ws[32];
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ int block_sum(int v, int* ws) {
+  int tot;
+  block_exclusive_scan(v, ws, &tot);
+  return tot;
+}
+
+}  // namespace moe

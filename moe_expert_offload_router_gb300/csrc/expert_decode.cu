@@ -1,0 +1,1024 @@
+// Grouped expert MLP for decode-sized batches: gate/up GEMV + SwiGLU, down
+// GEMV, and the router-weighted combine with the shared expert.
+//
+// "Running DeepSeek-V4-Flash across four free GPUs", section "What the expert
+// cache actually does" (the grouped expert GEMM over the slot views);
+// "An elephant through a straw", sections "43 graphs, 43 syncs" (grouped-GEMV
+// expert kernels fired per layer) and "Rig, model & methodology" (MXFP4
+// experts, a 2.25-bit copy with fp8 group scales, one shared expert).
+//
+// Structure (all launches on the caller's stream):
+//   plan kernel   block 0 sorts the kept (pool, slot, pair) keys in shared
+//                 memory (bitonic) and cuts each slot's run into groups of up
+//                 to G tokens; blocks 1..T scale each token's activations by
+//                 a power of two so the largest is in [1, 2) and store fp16.
+//   gate/up       persistent; a work item is (group, 32-row tile).  The
+//                 group's activations are staged in shared memory in the
+//                 weight format's pairing; each warp streams gate row n and
+//                 up row n with 128-bit loads (lane l takes 16-byte chunks
+//                 l, l+32, ...), decodes two codes per instruction into
+//                 fp16x2, accumulates each 32-weight block in fp16x2, scales
+//                 the block sum in fp32, reduces across lanes with shuffles
+//                 and writes h = SiLU(g) * u in fp32.
+//   down          same over W2 with h staged the same way (per-pair scale).
+//   combine       y_t = sum_j w_tj o_tj (rank order) + shared, fp32 -> bf16.
+// fp16 block sums cannot overflow: |code| <= 6 (E2M1), 1.5 (2-bit), 448
+// (E4M3) times |activation| < 2 times 32 (16 for E4M3) terms stays below 2^15.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kG = 8;             // tokens per group
+constexpr int kFwdThreads = 256;  // 8 warps
+constexpr int kRowsGateUp = 32;   // rows of w1/w3 per gate/up work item
+constexpr int kRowsDown = 64;     // rows of w2 per down work item
+constexpr int kMaxPlanPairs = 4096;
+
+struct Group {
+  int pool, slot, begin, count;
+};
+
+struct FwdLayout {
+  size_t hdr, perm, groups, xsig, xs, h, o, total;
+};
+
+static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+static FwdLayout fwd_layout(int H, int I, int T, int k) {
+  const size_t P = (size_t)T * k;
+  const size_t ng = P + (T + kG - 1) / kG + 1;
+  FwdLayout L;
+  size_t off = 0;
+  L.hdr = off;
+  off = align256(off + 256);
+  L.perm = off;
+  off = align256(off + P * 4);
+  L.groups = off;
+  off = align256(off + ng * sizeof(Group));
+  L.xsig = off;
+  off = align256(off + (size_t)T * 4);
+  L.xs = off;
+  off = align256(off + (size_t)T * H * 2);
+  L.h = off;
+  off = align256(off + (P + T) * (size_t)I * 4);
+  L.o = off;
+  off = align256(off + (P + T) * (size_t)H * 4);
+  L.total = off;
+  return L;
+}
+
+struct FwdArgs {
+  int H, I, T, k, P;
+  const uint8_t* fp4;
+  int n4;
+  const uint8_t* int2;
+  int n2;
+  const uint8_t* shared;
+  size_t b4, b2;  // bytes per expert
+  const uint16_t* x;
+  const int32_t* slots;
+  const int8_t* tags;
+  const float* w;
+  uint16_t* y;
+  int32_t* err;
+  // workspace
+  int* hdr;
+  int* perm;
+  Group* groups;
+  int* xsig;
+  __half* xs;
+  float* h;
+  float* o;
+};
+
+// ------------------------------------------------------------------ decode --
+
+__device__ __forceinline__ float e8m0_f32(uint32_t e) {
+  // 2^(e-127): exponent field e for e >= 1; e = 0 is the subnormal 2^-127.
+  return e ? __uint_as_float(e << 23) : __uint_as_float(0x00400000u);
+}
+
+__device__ __forceinline__ void fp4_word_to_h2(uint32_t w, __half2* out) {
+  uint32_t r0, r1, r2, r3;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+      : "r"(w));
+  out[0] = *reinterpret_cast<__half2*>(&r0);
+  out[1] = *reinterpret_cast<__half2*>(&r1);
+  out[2] = *reinterpret_cast<__half2*>(&r2);
+  out[3] = *reinterpret_cast<__half2*>(&r3);
+}
+
+__device__ __forceinline__ __half2 e4m3x2_to_h2(uint32_t two_bytes) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo;\n\tcvt.u16.u32 lo, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+      : "=r"(r)
+      : "r"(two_bytes));
+  return *reinterpret_cast<__half2*>(&r);
+}
+
+__device__ __forceinline__ void fp8_word_to_h2(uint32_t w, __half2* out) {
+  out[0] = e4m3x2_to_h2(w & 0xffffu);
+  out[1] = e4m3x2_to_h2(w >> 16);
+}
+
+// 16 two-bit codes (element i at bits 2i) -> 8 fp16x2 holding the levels
+// (q - 1.5) of elements (i, i + 8): the code is placed in the mantissa of
+// 512 (ulp 0.5, so 512 + q exactly), then 513.5 is subtracted.
+__device__ __forceinline__ void int2_word_to_h2(uint32_t w, __half2* out) {
+  const __half2 bias = __halves2half2(__ushort_as_half((unsigned short)0x6003),
+                                      __ushort_as_half((unsigned short)0x6003));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t sh = i == 0 ? (w << 1) : (w >> (2 * i - 1));
+    const uint32_t v = (sh & 0x00060006u) | 0x60006000u;
+    out[i] = __hsub2(*reinterpret_cast<const __half2*>(&v), bias);
+  }
+}
+
+__device__ __forceinline__ float h2sum(__half2 a) {
+  const float2 f = __half22float2(a);
+  return f.x + f.y;
+}
+
+__device__ __forceinline__ void lds4(const uint4* p, __half2* x) {
+  const uint4 v = *p;
+  x[0] = *reinterpret_cast<const __half2*>(&v.x);
+  x[1] = *reinterpret_cast<const __half2*>(&v.y);
+  x[2] = *reinterpret_cast<const __half2*>(&v.z);
+  x[3] = *reinterpret_cast<const __half2*>(&v.w);
+}
+
+// Physical 16-byte unit within a chunk for each format's activation layout
+// (rotations that keep a quarter-warp's 128-bit shared loads conflict-free).
+__device__ __forceinline__ int unit_fp4(int c, int s) { return c * 4 + ((s + (c >> 1)) & 3); }
+__device__ __forceinline__ int unit_int2(int c, int s) { return c * 8 + ((s + c) & 7); }
+__device__ __forceinline__ int unit_fp8(int c, int s) { return c * 2 + ((s + (c >> 2)) & 1); }
+
+// --------------------------------------------------------- chunk processors --
+// Each adds, for two rows (r0, r1) and every staged token, one 16-byte code
+// chunk's contribution to the lane's fp32 accumulators.
+
+__device__ __forceinline__ void chunk_fp4(uint4 q0, uint32_t e0, uint4 q1, uint32_t e1, int c,
+                                          const uint4* xs, int xstride, int ntok, float* a0,
+                                          float* a1) {
+  __half2 w0[16], w1[16];
+  fp4_word_to_h2(q0.x, w0);
+  fp4_word_to_h2(q0.y, w0 + 4);
+  fp4_word_to_h2(q0.z, w0 + 8);
+  fp4_word_to_h2(q0.w, w0 + 12);
+  fp4_word_to_h2(q1.x, w1);
+  fp4_word_to_h2(q1.y, w1 + 4);
+  fp4_word_to_h2(q1.z, w1 + 8);
+  fp4_word_to_h2(q1.w, w1 + 12);
+  const float s0 = e8m0_f32(e0), s1 = e8m0_f32(e1);
+#pragma unroll
+  for (int t = 0; t < kG; ++t) {
+    if (t < ntok) {
+      const uint4* xp = xs + (size_t)t * xstride;
+      __half2 x[16];
+#pragma unroll
+      for (int s = 0; s < 4; ++s) lds4(xp + unit_fp4(c, s), x + 4 * s);
+      __half2 p0 = __hmul2(w0[0], x[0]), q0a = __hmul2(w0[8], x[8]);
+      __half2 p1 = __hmul2(w1[0], x[0]), q1a = __hmul2(w1[8], x[8]);
+#pragma unroll
+      for (int i = 1; i < 8; ++i) {
+        p0 = __hfma2(w0[i], x[i], p0);
+        q0a = __hfma2(w0[8 + i], x[8 + i], q0a);
+        p1 = __hfma2(w1[i], x[i], p1);
+        q1a = __hfma2(w1[8 + i], x[8 + i], q1a);
+      }
+      a0[t] = fmaf(h2sum(p0) + h2sum(q0a), s0, a0[t]);
+      a1[t] = fmaf(h2sum(p1) + h2sum(q1a), s1, a1[t]);
+    }
+  }
+}
+
+__device__ __forceinline__ void chunk_int2(uint4 q0, uint32_t e0, uint4 q1, uint32_t e1, int c,
+                                           const uint4* xs, int xstride, int ntok, float* a0,
+                                           float* a1) {
+  // 64 weights: words 0-1 form scale block 0, words 2-3 block 1
+  __half2 w0[32], w1[32];
+  int2_word_to_h2(q0.x, w0);
+  int2_word_to_h2(q0.y, w0 + 8);
+  int2_word_to_h2(q0.z, w0 + 16);
+  int2_word_to_h2(q0.w, w0 + 24);
+  int2_word_to_h2(q1.x, w1);
+  int2_word_to_h2(q1.y, w1 + 8);
+  int2_word_to_h2(q1.z, w1 + 16);
+  int2_word_to_h2(q1.w, w1 + 24);
+  const float2 s0 = __half22float2(e4m3x2_to_h2(e0));
+  const float2 s1 = __half22float2(e4m3x2_to_h2(e1));
+#pragma unroll
+  for (int t = 0; t < kG; ++t) {
+    if (t < ntok) {
+      const uint4* xp = xs + (size_t)t * xstride;
+      __half2 x[32];
+#pragma unroll
+      for (int s = 0; s < 8; ++s) lds4(xp + unit_int2(c, s), x + 4 * s);
+      __half2 pa = __hmul2(w0[0], x[0]), pb = __hmul2(w0[16], x[16]);
+      __half2 ra = __hmul2(w1[0], x[0]), rb = __hmul2(w1[16], x[16]);
+#pragma unroll
+      for (int i = 1; i < 16; ++i) {
+        pa = __hfma2(w0[i], x[i], pa);
+        pb = __hfma2(w0[16 + i], x[16 + i], pb);
+        ra = __hfma2(w1[i], x[i], ra);
+        rb = __hfma2(w1[16 + i], x[16 + i], rb);
+      }
+      a0[t] += h2sum(pa) * s0.x + h2sum(pb) * s0.y;
+      a1[t] += h2sum(ra) * s1.x + h2sum(rb) * s1.y;
+    }
+  }
+}
+
+__device__ __forceinline__ void chunk_fp8(uint4 q0, uint4 q1, int c, const uint4* xs, int xstride,
+                                          int ntok, float* a0, float* a1) {
+  __half2 w0[8], w1[8];
+  fp8_word_to_h2(q0.x, w0);
+  fp8_word_to_h2(q0.y, w0 + 2);
+  fp8_word_to_h2(q0.z, w0 + 4);
+  fp8_word_to_h2(q0.w, w0 + 6);
+  fp8_word_to_h2(q1.x, w1);
+  fp8_word_to_h2(q1.y, w1 + 2);
+  fp8_word_to_h2(q1.z, w1 + 4);
+  fp8_word_to_h2(q1.w, w1 + 6);
+#pragma unroll
+  for (int t = 0; t < kG; ++t) {
+    if (t < ntok) {
+      const uint4* xp = xs + (size_t)t * xstride;
+      __half2 x[8];
+      lds4(xp + unit_fp8(c, 0), x);
+      lds4(xp + unit_fp8(c, 1), x + 4);
+      __half2 p0 = __hmul2(w0[0], x[0]), p1 = __hmul2(w1[0], x[0]);
+#pragma unroll
+      for (int i = 1; i < 8; ++i) {
+        p0 = __hfma2(w0[i], x[i], p0);
+        p1 = __hfma2(w1[i], x[i], p1);
+      }
+      a0[t] += h2sum(p0);
+      a1[t] += h2sum(p1);
+    }
+  }
+}
+
+// ------------------------------------------------------------- row dot pairs --
+// Lane-partial dot products of two rows against the staged tokens.  K is the
+// row length; KC > 0 is K known at compile time (loads of all the lane's
+// chunks are issued before any is consumed).
+
+template <int KC>
+__device__ __forceinline__ void rows_fp4(const uint8_t* c0, const uint8_t* s0, const uint8_t* c1,
+                                         const uint8_t* s1, int K, const uint4* xs, int ntok,
+                                         float* a0, float* a1) {
+  const int lane = threadIdx.x & 31;
+  const int xstride = K / 8;
+  if constexpr (KC > 0 && KC % 1024 == 0) {
+    constexpr int CPL = KC / 1024;
+    uint4 q0[CPL], q1[CPL];
+    uint32_t e0[CPL], e1[CPL];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int c = lane + 32 * i;
+      q0[i] = ld_stream_v4(c0 + (size_t)c * 16);
+      q1[i] = ld_stream_v4(c1 + (size_t)c * 16);
+      e0[i] = __ldg(s0 + c);
+      e1[i] = __ldg(s1 + c);
+    }
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) chunk_fp4(q0[i], e0[i], q1[i], e1[i], lane + 32 * i, xs, xstride, ntok, a0, a1);
+  } else {
+    const int nch = K / 32;
+    for (int c = lane; c < nch; c += 32)
+      chunk_fp4(ld_stream_v4(c0 + (size_t)c * 16), __ldg(s0 + c), ld_stream_v4(c1 + (size_t)c * 16),
+                __ldg(s1 + c), c, xs, xstride, ntok, a0, a1);
+  }
+}
+
+template <int KC>
+__device__ __forceinline__ void rows_int2(const uint8_t* c0, const uint8_t* s0, const uint8_t* c1,
+                                          const uint8_t* s1, int K, const uint4* xs, int ntok,
+                                          float* a0, float* a1) {
+  const int lane = threadIdx.x & 31;
+  const int xstride = K / 8;
+  const int nch = K / 64;
+  auto sc = [](const uint8_t* p, int c) -> uint32_t {
+    return (uint32_t)__ldg(p + 2 * c) | ((uint32_t)__ldg(p + 2 * c + 1) << 8);
+  };
+  if constexpr (KC > 0 && KC % 2048 == 0) {
+    constexpr int CPL = KC / 2048;
+    uint4 q0[CPL], q1[CPL];
+    uint32_t e0[CPL], e1[CPL];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int c = lane + 32 * i;
+      q0[i] = ld_stream_v4(c0 + (size_t)c * 16);
+      q1[i] = ld_stream_v4(c1 + (size_t)c * 16);
+      e0[i] = sc(s0, c);
+      e1[i] = sc(s1, c);
+    }
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) chunk_int2(q0[i], e0[i], q1[i], e1[i], lane + 32 * i, xs, xstride, ntok, a0, a1);
+  } else {
+    for (int c = lane; c < nch; c += 32)
+      chunk_int2(ld_stream_v4(c0 + (size_t)c * 16), sc(s0, c), ld_stream_v4(c1 + (size_t)c * 16),
+                 sc(s1, c), c, xs, xstride, ntok, a0, a1);
+  }
+}
+
+template <int KC>
+__device__ __forceinline__ void rows_fp8(const uint8_t* c0, const uint8_t* c1, int K, const uint4* xs,
+                                         int ntok, float* a0, float* a1) {
+  const int lane = threadIdx.x & 31;
+  const int xstride = K / 8;
+  const int nch = K / 16;
+  if constexpr (KC > 0 && KC % 512 == 0) {
+    constexpr int CPL = KC / 512;
+    uint4 q0[CPL], q1[CPL];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int c = lane + 32 * i;
+      q0[i] = ld_stream_v4(c0 + (size_t)c * 16);
+      q1[i] = ld_stream_v4(c1 + (size_t)c * 16);
+    }
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) chunk_fp8(q0[i], q1[i], lane + 32 * i, xs, xstride, ntok, a0, a1);
+  } else {
+    for (int c = lane; c < nch; c += 32)
+      chunk_fp8(ld_stream_v4(c0 + (size_t)c * 16), ld_stream_v4(c1 + (size_t)c * 16), c, xs, xstride,
+                ntok, a0, a1);
+  }
+}
+
+__device__ __forceinline__ void warp_allreduce(float* a, int ntok) {
+#pragma unroll
+  for (int t = 0; t < kG; ++t) {
+    if (t < ntok) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) a[t] += __shfl_xor_sync(0xffffffffu, a[t], o);
+    }
+  }
+}
+
+// ------------------------------------------------------------ matrix views --
+// Canonical byte offsets of matrix m (0 = w1 [I,H], 1 = w3 [I,H], 2 = w2 [H,I])
+// inside one expert of each format.
+struct MatView {
+  const uint8_t* codes;
+  const uint8_t* scales;  // FP4: E8M0 [N][K/32]; INT2: E4M3 [N][K/32]; FP8: fp32 [N]
+  int N, K;
+};
+
+__device__ __forceinline__ MatView mat_view(int pool, const uint8_t* expert, int H, int I, int m) {
+  const size_t hi = (size_t)H * I;
+  MatView v;
+  v.N = (m == 2) ? H : I;
+  v.K = (m == 2) ? I : H;
+  size_t per, cb;
+  if (pool == MOE_POOL_FP4) {
+    cb = hi / 2;
+    per = cb + hi / 32;
+  } else if (pool == MOE_POOL_INT2) {
+    cb = hi / 4;
+    per = cb + hi / 32;
+  } else {
+    cb = hi;
+    per = 0;  // FP8 matrices differ in row-scale size; computed below
+  }
+  if (pool != MOE_POOL_SHARED) {
+    v.codes = expert + per * m;
+    v.scales = v.codes + cb;
+  } else {
+    const size_t w1 = hi + (size_t)I * 4;  // w1 and w3: codes [I,H] + scales [I]
+    v.codes = expert + w1 * m;
+    v.scales = v.codes + hi;
+  }
+  return v;
+}
+
+// ----------------------------------------------------------------- staging --
+// Copy ntok activation rows (fp16, already scaled) into the format's layout.
+// src_row(i) gives the fp16 row of staged token i.
+template <typename SrcFn>
+__device__ void stage_rows(int pool, int K, int ntok, SrcFn src_row, uint4* xs) {
+  const int units = K / 8;  // 16-byte units per row
+  for (int u = threadIdx.x; u < ntok * units; u += blockDim.x) {
+    const int i = u / units, uu = u % units;
+    const __half* src = src_row(i);
+    uint4 v;
+    if (pool == MOE_POOL_FP4) {
+      const int c = uu >> 2, sl = ((uu & 3) - (c >> 1)) & 3;
+      v = *reinterpret_cast<const uint4*>(src + c * 32 + sl * 8);
+    } else if (pool == MOE_POOL_SHARED) {
+      const int c = uu >> 1, sl = ((uu & 1) - (c >> 2)) & 1;
+      v = *reinterpret_cast<const uint4*>(src + c * 16 + sl * 8);
+    } else {
+      const int c = uu >> 3, sl = ((uu & 7) - c) & 7;
+      const int base = c * 64 + (sl >> 1) * 16 + (sl & 1) * 4;
+      __half2 hh[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) hh[m] = __halves2half2(src[base + m], src[base + m + 8]);
+      v = *reinterpret_cast<uint4*>(hh);
+    }
+    xs[(size_t)i * units + uu] = v;
+  }
+}
+
+// --------------------------------------------------------------- plan kernel --
+
+__device__ __forceinline__ float block_max(float v, float* red) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    float t = lane < nw ? red[lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
+    if (lane == 0) red[32] = t;
+  }
+  __syncthreads();
+  const float r = red[32];
+  __syncthreads();
+  return r;
+}
+
+// Power-of-two exponent s with amax * 2^-s in [1, 2) (0 when amax is 0).
+__device__ __forceinline__ int pow2_exponent(float amax) {
+  if (!(amax > 0.f)) return 0;
+  int e;
+  frexpf(amax, &e);
+  return e - 1;
+}
+
+__global__ void __launch_bounds__(1024) plan_kernel(FwdArgs a) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  if (blockIdx.x > 0) {
+    // activation prep for token t
+    float* red = reinterpret_cast<float*>(smem_raw);
+    const int t = blockIdx.x - 1;
+    const uint16_t* xr = a.x + (size_t)t * a.H;
+    float amax = 0.f;
+    for (int n = threadIdx.x; n < a.H; n += blockDim.x)
+      amax = fmaxf(amax, fabsf(__uint_as_float((uint32_t)xr[n] << 16)));
+    amax = block_max(amax, red);
+    const int sg = pow2_exponent(amax);
+    for (int n = threadIdx.x; n < a.H; n += blockDim.x)
+      a.xs[(size_t)t * a.H + n] = __float2half_rn(ldexpf(__uint_as_float((uint32_t)xr[n] << 16), -sg));
+    if (threadIdx.x == 0) a.xsig[t] = sg;
+    return;
+  }
+  // block 0: group kept pairs by (pool, slot)
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem_raw);
+  int* ws = reinterpret_cast<int*>(keys + kMaxPlanPairs);
+  int* scal = ws + 34;
+  const int P = a.P;
+  int NP = 1;
+  while (NP < P) NP <<= 1;
+  const int tid = threadIdx.x, NT = blockDim.x;
+  if (tid == 0) scal[0] = 0;
+  __syncthreads();
+  for (int p = tid; p < NP; p += NT) {
+    unsigned long long key = ~0ull;
+    if (p < P) {
+      const int sl = a.slots[p];
+      const int tag = a.tags ? (int)a.tags[p] : MOE_TAG_FP4;
+      if (sl >= 0 && tag != MOE_TAG_DROP) {
+        const int pool = tag == MOE_TAG_INT2 ? MOE_POOL_INT2 : MOE_POOL_FP4;
+        const int npool = pool == MOE_POOL_FP4 ? a.n4 : a.n2;
+        if ((tag == MOE_TAG_FP4 || tag == MOE_TAG_INT2) && sl < npool)
+          key = ((unsigned long long)((unsigned)pool << 30 | (unsigned)sl) << 32) | (unsigned)p;
+        else
+          scal[0] = 1;
+      }
+    }
+    keys[p] = key;
+  }
+  __syncthreads();
+  for (int size = 2; size <= NP; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < NP / 2; i += NT) {
+        const int pos = 2 * i - (i & (stride - 1));
+        const int par = pos + stride;
+        const bool up = (pos & size) == 0;
+        const unsigned long long x = keys[pos], y = keys[par];
+        if ((x > y) == up) {
+          keys[pos] = y;
+          keys[par] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // groups: runs of equal (pool, slot), cut every kG pairs.  Run starts are
+  // compacted in order; each pair finds its run by binary search.
+  int* starts = scal + 4;  // [NP]
+  const int per = (NP + NT - 1) / NT;
+  const int i0 = min(NP, tid * per), i1 = min(NP, i0 + per);
+  int ns = 0, nv = 0;
+  for (int i = i0; i < i1; ++i) {
+    const unsigned long long key = keys[i];
+    if (key == ~0ull) break;
+    ++nv;
+    ns += (i == 0 || (keys[i - 1] >> 32) != (key >> 32));
+  }
+  int NS, V;
+  int sb = block_exclusive_scan(ns, ws, &NS);
+  block_exclusive_scan(nv, ws, &V);
+  for (int i = i0; i < i1; ++i) {
+    const unsigned long long key = keys[i];
+    if (key == ~0ull) break;
+    if (i == 0 || (keys[i - 1] >> 32) != (key >> 32)) starts[sb++] = i;
+  }
+  __syncthreads();
+  auto run_of = [&](int i) {
+    int lo = 0, hi = NS;  // last start <= i
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (starts[mid] <= i) lo = mid; else hi = mid;
+    }
+    return lo;
+  };
+  int ng = 0;
+  for (int i = i0; i < min(i1, V); ++i) ng += ((i - starts[run_of(i)]) % kG) == 0;
+  int ngroups;
+  int gi = block_exclusive_scan(ng, ws, &ngroups);
+  for (int i = i0; i < min(i1, V); ++i) {
+    const unsigned long long key = keys[i];
+    a.perm[i] = (int)(key & 0xffffffffu);
+    const int r = run_of(i);
+    if ((i - starts[r]) % kG) continue;
+    const int run_end = r + 1 < NS ? starts[r + 1] : V;
+    Group g;
+    g.pool = (int)(key >> 62);
+    g.slot = (int)((key >> 32) & 0x3fffffffu);
+    g.begin = i;
+    g.count = min(kG, run_end - i);
+    a.groups[gi++] = g;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int n = ngroups;
+    if (a.shared) {
+      for (int t0 = 0; t0 < a.T; t0 += kG) {
+        Group g;
+        g.pool = MOE_POOL_SHARED;
+        g.slot = 0;
+        g.begin = t0;
+        g.count = min(kG, a.T - t0);
+        a.groups[n++] = g;
+      }
+    }
+    a.hdr[0] = n;
+    a.hdr[1] = ngroups;
+    if (a.err) *a.err = scal[0] ? MOE_ERR_INVALID : 0;
+  }
+}
+
+// ---------------------------------------------------------- gate/up kernel --
+
+// A work item's group is checked against the buffers it indexes before any
+// access; a bad group (which the plan never produces) is skipped and flagged.
+__device__ __forceinline__ bool group_ok(const FwdArgs& a, const Group& g) {
+  if (g.count < 1 || g.count > kG) return false;
+  if (g.pool == MOE_POOL_SHARED) return a.shared != nullptr && g.begin >= 0 && g.begin + g.count <= a.T;
+  const int npool = g.pool == MOE_POOL_FP4 ? a.n4 : (g.pool == MOE_POOL_INT2 ? a.n2 : 0);
+  return g.slot >= 0 && g.slot < npool && g.begin >= 0 && g.begin + g.count <= a.P;
+}
+
+__device__ __forceinline__ int n_groups_checked(const FwdArgs& a) {
+  const int n = a.hdr[0];
+  const int cap = a.P + (a.T + kG - 1) / kG + 1;
+  return (n < 0 || n > cap) ? 0 : n;
+}
+
+__device__ __forceinline__ const uint8_t* expert_base(const FwdArgs& a, int pool, int slot) {
+  if (pool == MOE_POOL_FP4) return a.fp4 + (size_t)slot * a.b4;
+  if (pool == MOE_POOL_INT2) return a.int2 + (size_t)slot * a.b2;
+  return a.shared;
+}
+
+template <int KH>
+__global__ void __launch_bounds__(kFwdThreads, 2) gateup_kernel(FwdArgs a) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint4* xs = reinterpret_cast<uint4*>(smem_raw);
+  int* tok = reinterpret_cast<int*>(smem_raw + (size_t)kG * a.H * 2);
+  int* hrow = tok + kG;
+  const int H = KH > 0 ? KH : a.H;
+  const int I = a.I;
+  const int tiles = (I + kRowsGateUp - 1) / kRowsGateUp;
+  const int n_items = n_groups_checked(a) * tiles;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const Group g = a.groups[item / tiles];
+    const int tile = item % tiles;
+    if (!group_ok(a, g)) {
+      if (threadIdx.x == 0 && a.err) *a.err = MOE_ERR_INVALID;
+      continue;
+    }
+    if (threadIdx.x < g.count) {
+      const int i = threadIdx.x;
+      if (g.pool == MOE_POOL_SHARED) {
+        tok[i] = g.begin + i;
+        hrow[i] = a.P + g.begin + i;
+      } else {
+        const int p = min(max(a.perm[g.begin + i], 0), a.P - 1);
+        tok[i] = p / a.k;
+        hrow[i] = p;
+      }
+    }
+    __syncthreads();
+    stage_rows(g.pool, H, g.count, [&](int i) { return a.xs + (size_t)tok[i] * H; }, xs);
+    __syncthreads();
+    const uint8_t* ex = expert_base(a, g.pool, g.slot);
+    const MatView w1 = mat_view(g.pool, ex, H, I, 0);
+    const MatView w3 = mat_view(g.pool, ex, H, I, 1);
+    for (int r = warp; r < kRowsGateUp; r += kFwdThreads / 32) {
+      const int n = tile * kRowsGateUp + r;
+      if (n >= I) break;
+      float ag[kG], au[kG];
+#pragma unroll
+      for (int t = 0; t < kG; ++t) ag[t] = au[t] = 0.f;
+      float rg = 1.f, ru = 1.f;
+      if (g.pool == MOE_POOL_FP4) {
+        rows_fp4<KH>(w1.codes + (size_t)n * (H / 2), w1.scales + (size_t)n * (H / 32),
+                     w3.codes + (size_t)n * (H / 2), w3.scales + (size_t)n * (H / 32), H, xs, g.count, ag, au);
+      } else if (g.pool == MOE_POOL_INT2) {
+        rows_int2<KH>(w1.codes + (size_t)n * (H / 4), w1.scales + (size_t)n * (H / 32),
+                      w3.codes + (size_t)n * (H / 4), w3.scales + (size_t)n * (H / 32), H, xs, g.count, ag, au);
+      } else {
+        rows_fp8<KH>(w1.codes + (size_t)n * H, w3.codes + (size_t)n * H, H, xs, g.count, ag, au);
+        rg = __ldg(reinterpret_cast<const float*>(w1.scales) + n);
+        ru = __ldg(reinterpret_cast<const float*>(w3.scales) + n);
+      }
+      warp_allreduce(ag, g.count);
+      warp_allreduce(au, g.count);
+#pragma unroll
+      for (int t = 0; t < kG; ++t) {
+        if (t == lane && t < g.count) {
+          const int sg = a.xsig[tok[t]];
+          const float gv = ldexpf(ag[t] * rg, sg);
+          const float uv = ldexpf(au[t] * ru, sg);
+          a.h[(size_t)hrow[t] * I + n] = gv / (1.f + expf(-gv)) * uv;
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// -------------------------------------------------------------- down kernel --
+
+template <int KI>
+__global__ void __launch_bounds__(kFwdThreads, 2) down_kernel(FwdArgs a) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  const int H = a.H;
+  const int I = KI > 0 ? KI : a.I;
+  uint4* xs = reinterpret_cast<uint4*>(smem_raw);
+  __half* hh = reinterpret_cast<__half*>(smem_raw + (size_t)kG * I * 2);  // [kG][I] natural order
+  int* hrow = reinterpret_cast<int*>(smem_raw + (size_t)kG * I * 4);
+  int* sig = hrow + kG;
+  const int tiles = (H + kRowsDown - 1) / kRowsDown;
+  const int n_items = n_groups_checked(a) * tiles;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const Group g = a.groups[item / tiles];
+    const int tile = item % tiles;
+    if (!group_ok(a, g)) {
+      if (threadIdx.x == 0 && a.err) *a.err = MOE_ERR_INVALID;
+      continue;
+    }
+    if (threadIdx.x < g.count) {
+      const int i = threadIdx.x;
+      const int p = g.pool == MOE_POOL_SHARED ? 0 : a.perm[g.begin + i];
+      hrow[i] = g.pool == MOE_POOL_SHARED ? a.P + g.begin + i : min(max(p, 0), a.P - 1);
+    }
+    __syncthreads();
+    // per-row power-of-two scale of h, then fp16 rows in natural order
+    for (int i = warp; i < g.count; i += kFwdThreads / 32) {
+      const float* src = a.h + (size_t)hrow[i] * I;
+      float m = 0.f;
+      for (int n = lane; n < I; n += 32) m = fmaxf(m, fabsf(src[n]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      const int sg = pow2_exponent(m);
+      if (lane == 0) sig[i] = sg;
+      for (int n = lane; n < I; n += 32) hh[(size_t)i * I + n] = __float2half_rn(ldexpf(src[n], -sg));
+    }
+    __syncthreads();
+    stage_rows(g.pool, I, g.count, [&](int i) { return (const __half*)(hh + (size_t)i * I); }, xs);
+    __syncthreads();
+    const uint8_t* ex = expert_base(a, g.pool, g.slot);
+    const MatView w2 = mat_view(g.pool, ex, H, I, 2);
+    for (int r = 2 * warp; r < kRowsDown; r += 2 * (kFwdThreads / 32)) {
+      const int n = tile * kRowsDown + r;
+      if (n >= H) break;
+      const int n1 = min(n + 1, H - 1);
+      float a0[kG], a1[kG];
+#pragma unroll
+      for (int t = 0; t < kG; ++t) a0[t] = a1[t] = 0.f;
+      float r0 = 1.f, r1 = 1.f;
+      if (g.pool == MOE_POOL_FP4) {
+        rows_fp4<KI>(w2.codes + (size_t)n * (I / 2), w2.scales + (size_t)n * (I / 32),
+                     w2.codes + (size_t)n1 * (I / 2), w2.scales + (size_t)n1 * (I / 32), I, xs, g.count, a0, a1);
+      } else if (g.pool == MOE_POOL_INT2) {
+        rows_int2<KI>(w2.codes + (size_t)n * (I / 4), w2.scales + (size_t)n * (I / 32),
+                      w2.codes + (size_t)n1 * (I / 4), w2.scales + (size_t)n1 * (I / 32), I, xs, g.count, a0, a1);
+      } else {
+        rows_fp8<KI>(w2.codes + (size_t)n * I, w2.codes + (size_t)n1 * I, I, xs, g.count, a0, a1);
+        r0 = __ldg(reinterpret_cast<const float*>(w2.scales) + n);
+        r1 = __ldg(reinterpret_cast<const float*>(w2.scales) + n1);
+      }
+      warp_allreduce(a0, g.count);
+      warp_allreduce(a1, g.count);
+#pragma unroll
+      for (int t = 0; t < kG; ++t) {
+        if (t < g.count) {
+          if (lane == t) a.o[(size_t)hrow[t] * H + n] = ldexpf(a0[t] * r0, sig[t]);
+          if (lane == 16 + t && n + 1 < H) a.o[(size_t)hrow[t] * H + n + 1] = ldexpf(a1[t] * r1, sig[t]);
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------ combine kernel --
+
+__global__ void __launch_bounds__(256) combine_kernel(FwdArgs a) {
+  const int t = blockIdx.y;
+  __shared__ float wk[64];
+  __shared__ int pk[64];
+  if (threadIdx.x < a.k) {
+    const int p = t * a.k + threadIdx.x;
+    const int sl = a.slots[p];
+    const int tag = a.tags ? (int)a.tags[p] : MOE_TAG_FP4;
+    const int npool = tag == MOE_TAG_INT2 ? a.n2 : a.n4;
+    const bool keep = sl >= 0 && (tag == MOE_TAG_FP4 || tag == MOE_TAG_INT2) && sl < npool;
+    wk[threadIdx.x] = keep ? a.w[p] : 0.f;
+    pk[threadIdx.x] = keep ? p : -1;
+  }
+  __syncthreads();
+  for (int n = blockIdx.x * blockDim.x + threadIdx.x; n < a.H; n += gridDim.x * blockDim.x) {
+    float acc = 0.f;
+    for (int j = 0; j < a.k; ++j)
+      if (pk[j] >= 0) acc = fmaf(wk[j], a.o[(size_t)pk[j] * a.H + n], acc);
+    if (a.shared) acc += a.o[(size_t)(a.P + t) * a.H + n];
+    a.y[(size_t)t * a.H + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+  }
+}
+
+// --------------------------------------------------------- dequant debug --
+
+__global__ void dequant_kernel(const uint8_t* expert, int pool, int H, int I, int m, float* out) {
+  const MatView v = mat_view(pool, expert, H, I, m);
+  const size_t total = (size_t)v.N * v.K;
+  for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx * 16 < total;
+       idx += (size_t)gridDim.x * blockDim.x) {
+    // 16 consecutive weights of one row
+    const size_t e0 = idx * 16;
+    const int n = (int)(e0 / v.K), kk = (int)(e0 % v.K);
+    float* o = out + e0;
+    if (pool == MOE_POOL_FP4) {
+      const uint8_t* c = v.codes + (size_t)n * (v.K / 2) + kk / 2;
+      const float s = e8m0_f32(v.scales[(size_t)n * (v.K / 32) + kk / 32]);
+      __half2 w[8];
+      fp4_word_to_h2(*reinterpret_cast<const uint32_t*>(c), w);
+      fp4_word_to_h2(*reinterpret_cast<const uint32_t*>(c + 4), w + 4);
+      for (int i = 0; i < 8; ++i) {
+        const float2 f = __half22float2(w[i]);
+        o[2 * i] = f.x * s;
+        o[2 * i + 1] = f.y * s;
+      }
+    } else if (pool == MOE_POOL_INT2) {
+      const uint8_t* c = v.codes + (size_t)n * (v.K / 4) + kk / 4;
+      const uint8_t sb = v.scales[(size_t)n * (v.K / 32) + kk / 32];
+      const float s = __half22float2(e4m3x2_to_h2(sb)).x;
+      __half2 w[8];
+      int2_word_to_h2(*reinterpret_cast<const uint32_t*>(c), w);
+      for (int i = 0; i < 8; ++i) {
+        const float2 f = __half22float2(w[i]);
+        o[i] = f.x * s;
+        o[i + 8] = f.y * s;
+      }
+    } else {
+      const uint8_t* c = v.codes + (size_t)n * v.K + kk;
+      const float s = reinterpret_cast<const float*>(v.scales)[n];
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t two = (uint32_t)c[2 * i] | ((uint32_t)c[2 * i + 1] << 8);
+        const float2 f = __half22float2(e4m3x2_to_h2(two));
+        o[2 * i] = f.x * s;
+        o[2 * i + 1] = f.y * s;
+      }
+    }
+  }
+}
+
+// -------------------------------------------------------------- rms carry --
+
+__global__ void __launch_bounds__(256) rms_carry_kernel(const uint16_t* y, int H, float eps, uint16_t* xn) {
+  __shared__ float red[33];
+  const int t = blockIdx.x;
+  const uint16_t* yr = y + (size_t)t * H;
+  float ss = 0.f;
+  for (int n = threadIdx.x; n < H; n += blockDim.x) {
+    const float v = __uint_as_float((uint32_t)yr[n] << 16);
+    ss = fmaf(v, v, ss);
+  }
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (lane == 0) red[wid] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += red[i];
+    red[32] = 1.f / sqrtf(s / (float)H + eps);
+  }
+  __syncthreads();
+  const float r = red[32];
+  for (int n = threadIdx.x; n < H; n += blockDim.x)
+    xn[(size_t)t * H + n] =
+        __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float((uint32_t)yr[n] << 16) * r));
+}
+
+// ------------------------------------------------------------------- host --
+
+static int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+template <typename K>
+static moe_status set_smem(K kernel, size_t bytes) {
+  if (bytes > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute((const void*)kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  }
+  return MOE_OK;
+}
+
+template <typename K>
+static int persistent_grid(K kernel, size_t smem, long long max_items) {
+  int per_sm = 1;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kFwdThreads, smem);
+  if (per_sm < 1) per_sm = 1;
+  long long g = (long long)sm_count() * per_sm;
+  if (max_items < g) g = max_items;
+  return (int)(g < 1 ? 1 : g);
+}
+
+static moe_status validate_views(const moe_expert_views* v) {
+  MOE_ARG(v != nullptr, "views is null");
+  MOE_ARG(v->H > 0 && v->I > 0 && v->H % 32 == 0 && v->I % 32 == 0, "H and I must be positive multiples of 32");
+  MOE_ARG(v->H % 64 == 0 && v->I % 64 == 0 || v->int2_slots == nullptr,
+          "the 2-bit pool needs H and I multiples of 64");
+  MOE_ARG(v->fp4_slots == nullptr || ((uintptr_t)v->fp4_slots & 15) == 0, "fp4_slots must be 16-byte aligned");
+  MOE_ARG(v->int2_slots == nullptr || ((uintptr_t)v->int2_slots & 15) == 0, "int2_slots must be 16-byte aligned");
+  MOE_ARG(v->shared == nullptr || ((uintptr_t)v->shared & 15) == 0, "shared must be 16-byte aligned");
+  return MOE_OK;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_expert_forward_workspace(const moe_expert_views* v, int T, int k) {
+  if (!v || T < 0 || k < 1) return 0;
+  return fwd_layout(v->H, v->I, T, k).total;
+}
+
+extern "C" moe_status moe_expert_forward(const moe_expert_views* v, const uint16_t* x, int T, int k,
+                                         const int32_t* slots, const int8_t* tags, const float* w,
+                                         uint16_t* y, void* workspace, size_t workspace_bytes,
+                                         int32_t* d_error, cudaStream_t stream) {
+  clear_error();
+  moe_status st = validate_views(v);
+  if (st != MOE_OK) return st;
+  MOE_ARG(T >= 0 && k >= 1 && k <= 64, "need T >= 0 and 1 <= k <= 64");
+  if (T == 0) return MOE_OK;
+  MOE_ARG((long long)T * k <= kMaxPlanPairs, "T * k = %lld exceeds %d pairs per call", (long long)T * k,
+          kMaxPlanPairs);
+  MOE_ARG(x && slots && w && y && workspace, "null pointer");
+  MOE_ARG(((uintptr_t)workspace & 255) == 0, "workspace must be 256-byte aligned");
+  const FwdLayout L = fwd_layout(v->H, v->I, T, k);
+  MOE_ARG(workspace_bytes >= L.total, "workspace too small: %zu < %zu", workspace_bytes, L.total);
+  MOE_ARG(v->fp4_slots || v->int2_slots, "no expert pool");
+  FwdArgs a;
+  a.H = v->H;
+  a.I = v->I;
+  a.T = T;
+  a.k = k;
+  a.P = T * k;
+  a.fp4 = v->fp4_slots;
+  a.n4 = v->fp4_slots ? v->fp4_num_slots : 0;
+  a.int2 = v->int2_slots;
+  a.n2 = v->int2_slots ? v->int2_num_slots : 0;
+  a.shared = v->shared;
+  a.b4 = fp4_bytes(v->H, v->I);
+  a.b2 = int2_bytes(v->H, v->I);
+  a.x = x;
+  a.slots = slots;
+  a.tags = tags;
+  a.w = w;
+  a.y = y;
+  a.err = d_error;
+  uint8_t* base = (uint8_t*)workspace;
+  a.hdr = (int*)(base + L.hdr);
+  a.perm = (int*)(base + L.perm);
+  a.groups = (Group*)(base + L.groups);
+  a.xsig = (int*)(base + L.xsig);
+  a.xs = (__half*)(base + L.xs);
+  a.h = (float*)(base + L.h);
+  a.o = (float*)(base + L.o);
+
+  const size_t plan_smem = (size_t)kMaxPlanPairs * 12 + 64 * 4;
+  if ((st = set_smem(plan_kernel, plan_smem)) != MOE_OK) return st;
+  {
+    ProfScope ps(MOE_K_PLAN, stream);
+    plan_kernel<<<1 + T, 1024, plan_smem, stream>>>(a);
+  }
+  if ((st = check_launch("plan_kernel")) != MOE_OK) return st;
+
+  const long long max_groups = (long long)T * k + (T + kG - 1) / kG + 1;
+  const size_t gu_smem = (size_t)kG * v->H * 2 + 2 * kG * 4;
+  const long long gu_items = max_groups * ((v->I + kRowsGateUp - 1) / kRowsGateUp);
+  if (v->H == 4096) {
+    if ((st = set_smem(gateup_kernel<4096>, gu_smem)) != MOE_OK) return st;
+    ProfScope ps(MOE_K_GATEUP, stream);
+    gateup_kernel<4096><<<persistent_grid(gateup_kernel<4096>, gu_smem, gu_items), kFwdThreads, gu_smem, stream>>>(a);
+  } else {
+    if ((st = set_smem(gateup_kernel<0>, gu_smem)) != MOE_OK) return st;
+    ProfScope ps(MOE_K_GATEUP, stream);
+    gateup_kernel<0><<<persistent_grid(gateup_kernel<0>, gu_smem, gu_items), kFwdThreads, gu_smem, stream>>>(a);
+  }
+  if ((st = check_launch("gateup_kernel")) != MOE_OK) return st;
+
+  const size_t dn_smem = (size_t)kG * v->I * 4 + 2 * kG * 4;
+  const long long dn_items = max_groups * ((v->H + kRowsDown - 1) / kRowsDown);
+  if (v->I == 2048) {
+    if ((st = set_smem(down_kernel<2048>, dn_smem)) != MOE_OK) return st;
+    ProfScope ps(MOE_K_DOWN, stream);
+    down_kernel<2048><<<persistent_grid(down_kernel<2048>, dn_smem, dn_items), kFwdThreads, dn_smem, stream>>>(a);
+  } else {
+    if ((st = set_smem(down_kernel<0>, dn_smem)) != MOE_OK) return st;
+    ProfScope ps(MOE_K_DOWN, stream);
+    down_kernel<0><<<persistent_grid(down_kernel<0>, dn_smem, dn_items), kFwdThreads, dn_smem, stream>>>(a);
+  }
+  if ((st = check_launch("down_kernel")) != MOE_OK) return st;
+
+  dim3 cg((v->H + 1023) / 1024, T);
+  ProfScope ps(MOE_K_COMBINE, stream);
+  combine_kernel<<<cg, 256, 0, stream>>>(a);
+  return check_launch("combine_kernel");
+}
+
+extern "C" moe_status moe_dequant_debug(const moe_expert_views* v, int pool, int slot, int matrix,
+                                        float* out, cudaStream_t stream) {
+  clear_error();
+  moe_status st = validate_views(v);
+  if (st != MOE_OK) return st;
+  MOE_ARG(out != nullptr, "out is null");
+  MOE_ARG(matrix >= 0 && matrix <= 2, "matrix must be MOE_W1, MOE_W3 or MOE_W2");
+  const uint8_t* ex = nullptr;
+  if (pool == MOE_POOL_FP4) {
+    MOE_ARG(v->fp4_slots && slot >= 0 && slot < v->fp4_num_slots, "bad FP4 slot");
+    ex = v->fp4_slots + (size_t)slot * fp4_bytes(v->H, v->I);
+  } else if (pool == MOE_POOL_INT2) {
+    MOE_ARG(v->int2_slots && slot >= 0 && slot < v->int2_num_slots, "bad 2-bit slot");
+    ex = v->int2_slots + (size_t)slot * int2_bytes(v->H, v->I);
+  } else {
+    MOE_ARG(pool == MOE_POOL_SHARED && v->shared, "bad pool");
+    ex = v->shared;
+  }
+  const size_t n16 = (size_t)v->H * v->I / 16;
+  const int blocks = (int)((n16 + 255) / 256 < 4096 ? (n16 + 255) / 256 : 4096);
+  dequant_kernel<<<blocks, 256, 0, stream>>>(ex, pool, v->H, v->I, matrix, out);
+  return check_launch("dequant_kernel");
+}
+
+extern "C" moe_status moe_rms_carry(const uint16_t* y, int T, int H, float eps, uint16_t* x_next,
+                                    cudaStream_t stream) {
+  clear_error();
+  MOE_ARG(T >= 0 && H > 0, "bad sizes");
+  if (T == 0) return MOE_OK;
+  MOE_ARG(y && x_next, "null pointer");
+  MOE_ARG(eps >= 0.f, "eps must be >= 0");
+  ProfScope ps(MOE_K_CARRY, stream);
+  rms_carry_kernel<<<T, 256, 0, stream>>>(y, H, eps, x_next);
+  return check_launch("rms_carry_kernel");
+}

@@ -1,0 +1,64 @@
+"""The C-ABI library builds, loads and exports every symbol its header declares (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.helpers import ROOT
+
+HEADER = os.path.join(ROOT, "include", "moe_gb300.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from moe_expert_offload_router_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_hot_path_calls():
+    names = _declared()
+    for n in ("moe_router_topk", "moe_slot_ensure", "moe_copy_missing", "moe_expert_forward",
+              "moe_ladder_classify", "moe_group_pairs", "moe_cache_create"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_host_only_calls(lib):
+    lib.moe_fp4_expert_bytes.restype = ctypes.c_size_t
+    lib.moe_int2_expert_bytes.restype = ctypes.c_size_t
+    lib.moe_fp8_expert_bytes.restype = ctypes.c_size_t
+    assert lib.moe_fp4_expert_bytes(4096, 2048) == 13369344
+    assert lib.moe_int2_expert_bytes(4096, 2048) == 7077888
+    assert lib.moe_fp8_expert_bytes(4096, 2048) == 25198592
+    assert lib.moe_fp4_expert_bytes(4096, 2047) == 0
+    assert lib.moe_version() >= 1
+
+
+def test_binding_names_match_header():
+    from moe_expert_offload_router_gb300 import _lib as L
+    for n in _declared():
+        if n in ("moe_cache_create", "moe_cache_destroy", "moe_cache_reset", "moe_cache_state",
+                 "moe_cache_export", "moe_cache_import", "moe_last_error"):
+            continue   # wrapped by the moe_cache class / error path
+        assert hasattr(L, n), n
+
+
+def test_oracle_not_imported_by_product_code():
+    pkg = os.path.join(ROOT, "moe_expert_offload_router_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                txt = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in txt and "from oracle" not in txt, f
