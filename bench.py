@@ -38,6 +38,7 @@ def _args():
     p.add_argument("--T", type=int, default=64, help="decode batch of the headline line")
     p.add_argument("--sweep", default="1,4,16,64", help="decode batches also measured (comma list, '' for none)")
     p.add_argument("--cpu-sample-tokens", type=int, default=4)
+    p.add_argument("--workload", default="decode", choices=["decode", "prefill", "ladder", "stack"])
     return p.parse_args()
 
 
@@ -326,6 +327,162 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def _tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured (cuBLAS bf16 burst)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def run_other(args):
+    """Prefill grouped GEMM, precision-ladder decode, or the 43-layer stack."""
+    import numpy as np
+    import torch
+
+    from moe_expert_offload_router_gb300 import build as B
+    B.build()
+    import moe_expert_offload_router_gb300 as M
+    from synth import configs, gen
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    hbm_peak, hbm_kind = _peaks()
+    out = {"metric": METRIC, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "data": "synthetic (seeded generator; no checkpoint weights)"}
+    clocks = Clocks(0)
+
+    def timed(step_fn, n):
+        ev = []
+        for i in range(n):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step_fn(i)
+            b.record(stream)
+            ev.append((a, b))
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / n
+
+    wl = {"prefill": configs.PREFILL, "ladder": configs.LADDER, "stack": configs.STACK}[args.workload]
+    H, I, E, k, T = wl.H, wl.I, wl.E, wl.k, wl.T
+    Bx = M.moe_fp4_expert_bytes(H, I)
+    if args.workload in ("prefill", "ladder"):
+        bank = torch.empty(E * Bx, dtype=torch.uint8, pin_memory=True)
+        for e in range(E):
+            bank[e * Bx:(e + 1) * Bx].copy_(gen.fp4_expert(wl, 0, e, device=dev))
+        slots = torch.empty(wl.S * Bx, dtype=torch.uint8, device=dev)
+        cache = M.moe_cache(wl.S, 1, E, Bx, slots, bank)
+        c2, s2 = None, None
+        if args.workload == "ladder":
+            B2 = M.moe_int2_expert_bytes(H, I)
+            bank2 = torch.empty(E * B2, dtype=torch.uint8, pin_memory=True)
+            for e in range(E):
+                bank2[e * B2:(e + 1) * B2] = torch.from_numpy(gen.int2_expert(wl, 0, e))
+            s2 = torch.empty(wl.S2 * B2, dtype=torch.uint8, device=dev)
+            c2 = M.moe_cache(wl.S2, 1, E, B2, s2, bank2)
+        views = M.make_views(H, I, slots, wl.S, s2, wl.S2 if s2 is not None else 0, None)
+        runner = M.DecodeLayerRunner(cache, views, E, k, T, dev, int2_cache=c2, ladder=wl.ladder)
+        n = args.warmup + args.steps
+        nsteps = max(wl.steps, 1)
+        lg = [torch.from_numpy(gen.router_logits(wl, 0, s % nsteps, T)).to(dev) for s in range(n)]
+        xs = [torch.from_numpy(gen.activations(wl, 0, s % nsteps, T).view(np.int16)).to(dev) for s in range(n)]
+        y = torch.empty((T, H), dtype=torch.int16, device=dev)
+        for s in range(args.warmup):
+            runner.run(0, lg[s], xs[s], y)
+        torch.cuda.synchronize()
+        m0 = runner.stats["misses"]
+        M.moe_profile_enable(True)
+        clocks.start()
+        ms = timed(lambda i: runner.run(0, lg[args.warmup + i], xs[args.warmup + i], y), args.steps)
+        ck = clocks.stop()
+        kt = {M.KERNEL_NAMES[kid]: M.moe_profile_query(kid) for kid in range(M.MOE_K_COUNT)}
+        M.moe_profile_enable(False)
+        out.update({"value": T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "clocks": ck,
+                    "gpu_launches": sum(v[1] for v in kt.values()),
+                    "kernel_ms_per_step": {nm: round(v[0] / args.steps, 4) for nm, v in kt.items() if v[1]},
+                    "misses_per_step": (runner.stats["misses"] - m0) / args.steps})
+        if args.workload == "prefill":
+            P = T * k
+            flops = 6.0 * P * H * I
+            gu_ms = kt["gateup"][0] / max(kt["gateup"][1], 1)
+            dn_ms = kt["down"][0] / max(kt["down"][1], 1)
+            gu_tf = 4.0 * P * H * I / (gu_ms / 1e3) / 1e12
+            peak, kind = _tensor_peak()
+            out["dtype"] = "bf16 MMA (fp32 accumulate) on exactly decoded MXFP4 weights"
+            out["config"] = {"workload": "prefill grouped GEMM H=4096 I=2048 E=256 top_k=6 T=8192, all 256 "
+                                         "experts resident", "T": T}
+            out["grouped_gemm_tflops"] = flops / ((gu_ms + dn_ms) / 1e3) / 1e12
+            out["roofline"] = {"bound": "tensor", "achieved": gu_tf, "peak": peak, "unit": "TFLOP/s",
+                               "frac": gu_tf / peak, "traffic": None, "kernel": "prefill_gemm_kernel (gate/up)",
+                               "peak_kind": kind, "ms_per_launch": gu_ms,
+                               "hbm_floor_ms_weights": 3 * E * (H * I // 2 + H * I // 32) / (hbm_peak * 1e6)}
+        else:
+            out["dtype"] = "e2m1/e8m0 + 2-bit/e4m3 weights, f16 dot, f32 accumulate"
+            out["config"] = {"workload": "ladder (2,4) decode H=4096 I=2048 E=256 top_k=6 T=32, 96 FP4 + "
+                                         "192 2-bit slots, Zipf(1.1) trace", "T": T}
+    else:
+        # 43-layer stack, every expert resident, no host sync per layer
+        L = wl.layers
+        S = L * E
+        pool = torch.empty(S * Bx, dtype=torch.uint8, device=dev)
+        for layer in range(L):
+            for e in range(E):
+                key = layer * E + e
+                pool[key * Bx:(key + 1) * Bx] = gen.fp4_expert(wl, layer, e, device=dev)
+        cache = M.moe_cache(S, L, E, Bx, pool, None)
+        cache.import_(np.arange(S, dtype=np.int32), np.arange(S, dtype=np.uint64), S)
+        shared = [torch.from_numpy(gen.shared_expert(wl, layer)).to(dev) for layer in range(L)]
+        views = [M.make_views(H, I, pool, S, None, 0, shared[layer]) for layer in range(L)]
+        runners = [M.DecodeLayerRunner(cache, views[layer], E, k, T, dev, assume_resident=True)
+                   for layer in range(L)]
+        for r in runners[1:]:
+            r.ws = runners[0].ws
+        n = args.warmup + args.steps
+        lg = [[torch.from_numpy(gen.router_logits(wl, layer, s % wl.steps, T)).to(dev) for layer in range(L)]
+              for s in range(n)]
+        x0 = torch.from_numpy(gen.activations(wl, 0, 0, T).view(np.int16)).to(dev)
+        ya = torch.empty((T, H), dtype=torch.int16, device=dev)
+        xb = torch.empty((T, H), dtype=torch.int16, device=dev)
+
+        def step(s):
+            x = x0
+            for layer in range(L):
+                runners[layer].run(layer, lg[s][layer], x, ya)
+                M.moe_rms_carry(ya, 1e-6, xb)
+                x = xb
+
+        for s in range(args.warmup):
+            step(s)
+        torch.cuda.synchronize()
+        M.moe_profile_enable(True)
+        clocks.start()
+        ms = timed(lambda i: step(args.warmup + i), args.steps)
+        ck = clocks.stop()
+        kt = {M.KERNEL_NAMES[kid]: M.moe_profile_query(kid) for kid in range(M.MOE_K_COUNT)}
+        M.moe_profile_enable(False)
+        # touched bytes per step: distinct experts per layer
+        tb = 0
+        for s in range(args.warmup, n):
+            for layer in range(L):
+                ids, _ = M.moe_router_topk(lg[s][layer], k)
+                tb += int(torch.unique(ids).numel()) * Bx + M.moe_fp8_expert_bytes(H, I)
+        gbs = tb / args.steps / (ms / 1e3) / 1e9
+        gu_ms, gu_n = kt["gateup"]
+        out.update({"value": T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "clocks": ck,
+                    "dtype": "e2m1/e8m0 weights, f16 dot, f32 accumulate",
+                    "config": {"workload": "43-layer stack decode, 256 FP4 experts + FP8 shared per layer, all "
+                                           "resident (148 GB), T=16, 70% step-to-step reuse", "T": T, "layers": L},
+                    "stack_hbm_gbs": gbs, "hbm_frac_of_step": gbs / hbm_peak,
+                    "gpu_launches": sum(v[1] for v in kt.values()),
+                    "kernel_ms_per_step": {nm: round(v[0] / args.steps, 4) for nm, v in kt.items() if v[1]}})
+    print(json.dumps(out))
+
+
 def run_reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -357,5 +514,7 @@ if __name__ == "__main__":
     a = _args()
     if a.impl == "reference":
         run_reference(a)
-    else:
+    elif a.workload == "decode":
         run_ours(a)
+    else:
+        run_other(a)

@@ -235,11 +235,31 @@ size_t moe_expert_forward_workspace(const moe_expert_views* v, int T, int k);
  *            pool's slot count (the pair is then skipped)
  * Numerics: weights are decoded exactly; activations are held in fp16 with a
  * per-token power-of-two scale; 32-weight partial sums accumulate in fp16 and
- * are scaled and summed in fp32; the combine runs in fp32 in rank order. */
+ * are scaled and summed in fp32; the combine runs in fp32 in rank order.
+ * Above 4096 pairs per call the grouped-GEMM path of moe_expert_prefill is
+ * taken (FP4 pool only, tags must be NULL). */
 moe_status moe_expert_forward(const moe_expert_views* v, const uint16_t* x, int T, int k,
                               const int32_t* slots, const int8_t* tags, const float* w,
                               uint16_t* y, void* workspace, size_t workspace_bytes,
                               int32_t* d_error, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Grouped-GEMM expert MLP for prefill-sized batches ("Running DeepSeek-V4-
+ * Flash across four free GPUs", section "All four workers die, but only on
+ * prompts over 32 tokens": past T * top_k >= num_experts the experts run as
+ * one grouped GEMM over all tokens routed to each).  Same inputs and result
+ * as moe_expert_forward for an FP4 pool without tags or shared expert; the
+ * pairs are grouped by slot (moe_group_pairs), each group's activations are
+ * gathered, and gate/up (with SwiGLU) and down run as tcgen05 bf16 MMAs with
+ * fp32 accumulators in tensor memory; weights are decoded to bf16 exactly,
+ * h is rounded to bf16.  Requires H and I multiples of 512, the FP4 pool
+ * only, d_error non-null.  d_error receives MOE_ERR_TIMEOUT if a pipeline
+ * wait on the device gave up (the output is then unspecified).
+ * ------------------------------------------------------------------------- */
+size_t moe_expert_prefill_workspace(const moe_expert_views* v, int T, int k);
+moe_status moe_expert_prefill(const moe_expert_views* v, const uint16_t* x, int T, int k,
+                              const int32_t* slots, const float* w, uint16_t* y, void* workspace,
+                              size_t workspace_bytes, int32_t* d_error, cudaStream_t stream);
 
 /* Decode one matrix of one slot to fp32 [N, K] (test hook; values are exact). */
 moe_status moe_dequant_debug(const moe_expert_views* v, int pool, int slot, int matrix,

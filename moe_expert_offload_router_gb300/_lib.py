@@ -67,6 +67,8 @@ _SIGS = {
     "moe_expert_forward": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, vp,
                                  sz, vp, vp]),
     "moe_dequant_debug": (i32, [C.POINTER(moe_expert_views), i32, i32, i32, vp, vp]),
+    "moe_expert_prefill_workspace": (sz, [C.POINTER(moe_expert_views), i32, i32]),
+    "moe_expert_prefill": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, sz, vp, vp]),
     "moe_rms_carry": (i32, [vp, i32, i32, f32, vp, vp]),
     "moe_selftest": (i32, []),
     "moe_profile_enable": (i32, [i32]),
@@ -249,6 +251,16 @@ def moe_expert_forward(views: moe_expert_views, x, slots, tags, w, y, workspace,
     _check(_lib.moe_expert_forward(C.byref(views), _p(x), T, k, _p(slots), _p(tags), _p(w), _p(y),
                                    _p(workspace), workspace.numel() * workspace.element_size(),
                                    _p(d_error), _s(stream)))
+
+
+def moe_expert_prefill_workspace(views: moe_expert_views, T: int, k: int) -> int:
+    return _lib.moe_expert_prefill_workspace(C.byref(views), T, k)
+
+
+def moe_expert_prefill(views: moe_expert_views, x, slots, w, y, workspace, d_error, stream=None):
+    T, k = slots.shape
+    _check(_lib.moe_expert_prefill(C.byref(views), _p(x), T, k, _p(slots), _p(w), _p(y), _p(workspace),
+                                   workspace.numel() * workspace.element_size(), _p(d_error), _s(stream)))
 
 
 def moe_dequant_debug(views: moe_expert_views, pool: int, slot: int, matrix: int, out, stream=None):

@@ -895,10 +895,18 @@ static moe_status validate_views(const moe_expert_views* v) {
 
 }  // namespace moe
 
+namespace moe {
+size_t prefill_workspace(int H, int I, int T, int k, int S);
+moe_status prefill_forward(const moe_expert_views* v, const uint16_t* x, int T, int k, const int32_t* slots,
+                           const float* w, uint16_t* y, void* workspace, size_t ws_bytes, int32_t* d_error,
+                           cudaStream_t stream);
+}  // namespace moe
+
 using namespace moe;
 
 extern "C" size_t moe_expert_forward_workspace(const moe_expert_views* v, int T, int k) {
   if (!v || T < 0 || k < 1) return 0;
+  if ((long long)T * k > kMaxPlanPairs) return prefill_workspace(v->H, v->I, T, k, v->fp4_num_slots);
   return fwd_layout(v->H, v->I, T, k).total;
 }
 
@@ -911,9 +919,14 @@ extern "C" moe_status moe_expert_forward(const moe_expert_views* v, const uint16
   if (st != MOE_OK) return st;
   MOE_ARG(T >= 0 && k >= 1 && k <= 64, "need T >= 0 and 1 <= k <= 64");
   if (T == 0) return MOE_OK;
-  MOE_ARG((long long)T * k <= kMaxPlanPairs, "T * k = %lld exceeds %d pairs per call", (long long)T * k,
-          kMaxPlanPairs);
   MOE_ARG(x && slots && w && y && workspace, "null pointer");
+  if ((long long)T * k > kMaxPlanPairs) {
+    // prefill-sized batch: grouped GEMM on the tensor cores (FP4 pool only)
+    MOE_ARG(tags == nullptr, "tags are not supported above %d pairs per call", kMaxPlanPairs);
+    MOE_ARG(((uintptr_t)workspace & 255) == 0, "workspace must be 256-byte aligned");
+    MOE_ARG(((uintptr_t)x & 15) == 0, "x must be 16-byte aligned");
+    return prefill_forward(v, x, T, k, slots, w, y, workspace, workspace_bytes, d_error, stream);
+  }
   MOE_ARG(((uintptr_t)workspace & 255) == 0, "workspace must be 256-byte aligned");
   const FwdLayout L = fwd_layout(v->H, v->I, T, k);
   MOE_ARG(workspace_bytes >= L.total, "workspace too small: %zu < %zu", workspace_bytes, L.total);

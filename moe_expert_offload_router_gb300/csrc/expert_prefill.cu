@@ -1,0 +1,631 @@
+// Grouped expert MLP for prefill-sized batches on the tcgen05 tensor cores.
+//
+// "Running DeepSeek-V4-Flash across four free GPUs", section "All four workers
+// die, but only on prompts over 32 tokens": past T * top_k >= num_experts a
+// prefill chunk touches most experts, and the expert work is one grouped GEMM
+// over all tokens routed to each expert.  Weights are the MXFP4 experts of
+// the slot pool (section "The model"); activations stay bf16 (W4A16, as every
+// page runs its experts).
+//
+// Pipeline of one call:
+//   group     pairs sorted by slot (stable counting sort, moe_group_pairs)
+//   items     per slot, tiles of <= 256 rows of its pairs
+//   gather    Xg[i] = x[token of the i-th sorted pair] (bf16 rows, 16-byte copies)
+//   GEMM1     per (item, 64-feature tile): D[128, n] = [W1;W3 interleaved] . Xg^T
+//             over K = H; epilogue h = SiLU(gate) * up -> bf16 rows of Hs
+//   GEMM2     per (item, 128-feature tile): D[128, n] = W2 . Hs^T over K = I;
+//             epilogue o[pair][feature] in fp32
+//   combine   y_t = sum_j w_tj o_tj in rank order -> bf16
+//
+// GEMM CTA (384 threads): warp 8 lane 0 issues TMA loads (raw FP4 codes of the
+// A tile into an 8-deep staging ring; the B tile straight into its 128-byte
+// swizzled K-major layout); warps 0-7 decode the raw codes to bf16 with the
+// E8M0 scale folded in (exact: E2M1 x 2^(e-127) fits bf16 for all scales) and
+// store them in the same swizzled layout; warp 9 lane 0 issues
+// tcgen05.mma.kind::f16 (M = 128, N = rows of the item rounded to 16, K = 16
+// per instruction) into a TMEM accumulator and commits each stage back to the
+// producers; warps 8-11 read TMEM with tcgen05.ld for the epilogue.  Every
+// mbarrier wait gives up after one second and records MOE_ERR_TIMEOUT.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kPfThreads = 384;
+constexpr int kPfStages = 3;      // A/B operand stages
+constexpr int kPfRaw = 8;         // raw FP4 code stages
+constexpr int kPfNMax = 256;      // rows per item (MMA N)
+constexpr int kPfKStep = 64;      // K elements per stage (128 bytes of bf16: one swizzle row)
+constexpr int kPfBox = 64;        // rows per TMA box of the B operand
+
+struct PfItem {
+  int slot, row0, count, pad;
+};
+
+// shared memory layout (offsets from a 1024-aligned base)
+constexpr int kATile = 128 * 128;                 // 16 KB
+constexpr int kBTile = kPfNMax * 128;             // 32 KB
+constexpr int kRawTile = 128 * 32;                // 4 KB
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kPfStages * kATile;
+constexpr int kOffRaw = kOffB + kPfStages * kBTile;
+constexpr int kOffScale = kOffRaw + kPfRaw * kRawTile;   // 128 rows x up to 128 scale bytes
+constexpr int kOffBar = kOffScale + 128 * 128;
+constexpr int kPfSmem = kOffBar + 256 + 1024;     // + alignment slack
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, int count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(su32(b)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase of parity `parity` to complete; gives up after 1 s (or
+// when another thread of the grid gave up) and returns false.
+__device__ __noinline__ bool mbar_wait(uint64_t* b, uint32_t parity, int* err) {
+  if (mbar_test(b, parity)) return true;
+  const uint64_t t0 = gtimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test(b, parity)) return true;
+    if ((it & 255) == 0) {
+      if (gtimer() - t0 > 1000000000ull) {
+        atomicExch(err, MOE_ERR_TIMEOUT);
+        return false;
+      }
+      if (*(volatile int*)err == MOE_ERR_TIMEOUT) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(su32(dst)),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(su32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          su32(dst)),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(su32(bar))
+      : "memory");
+}
+
+// UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row atoms 1024 B apart.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)1 << 16;                  // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;        // stride byte offset
+  d |= (uint64_t)1 << 46;                  // descriptor version
+  d |= (uint64_t)2 << 61;                  // 128-byte swizzle
+  return d;
+}
+
+// kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major, M = 128.
+__device__ __forceinline__ uint32_t idesc_bf16(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Two E2M1 codes -> bf16x2 (element 2j low) times the block scale, exact.
+__device__ __forceinline__ uint32_t fp4x2_to_bf16x2(uint32_t byte, uint32_t scale2) {
+  uint32_t h, r;
+  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(h) : "r"(byte));
+  asm("{\n\t.reg .b16 l, u, bl, bu;\n\tmov.b32 {l, u}, %1;\n\tcvt.rn.bf16.f16 bl, l;\n\tcvt.rn.bf16.f16 bu, u;\n\t"
+      "mov.b32 %0, {bl, bu};\n\t}"
+      : "=r"(r)
+      : "r"(h));
+  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&r);
+  const __nv_bfloat162 s = *reinterpret_cast<const __nv_bfloat162*>(&scale2);
+  v = __hmul2(v, s);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t e8m0_bf16x2(uint32_t e) {
+  const uint32_t b = e ? (e << 7) : 0x0040u;  // 2^(e-127) in bf16 (e = 0 is the subnormal 2^-127)
+  return b | (b << 16);
+}
+
+struct PfArgs {
+  int H, I, k, S;
+  int mode;           // 0: gate/up + SwiGLU, 1: down
+  int K;              // reduction length (H or I)
+  int tiles;          // feature tiles per item
+  const PfItem* items;
+  const int* n_items;
+  const int* perm;    // sorted position -> pair index (mode 1 epilogue)
+  __nv_bfloat16* hs;  // mode 0 output [P, I]
+  float* o;           // mode 1 output [P, H] by pair
+  int* err;
+};
+
+__global__ void __launch_bounds__(kPfThreads, 1)
+    prefill_gemm_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
+                        const __grid_constant__ CUtensorMap mS0, const __grid_constant__ CUtensorMap mS1,
+                        const __grid_constant__ CUtensorMap mB, PfArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bar = (uint64_t*)(sm + kOffBar);
+  uint64_t* full = bar;                  // [kPfStages]
+  uint64_t* empty = bar + kPfStages;     // [kPfStages]
+  uint64_t* rawf = bar + 2 * kPfStages;  // [kPfRaw]
+  uint64_t* rawe = rawf + kPfRaw;        // [kPfRaw]
+  uint64_t* sbar = rawe + kPfRaw;
+  uint64_t* done = sbar + 1;
+  uint32_t* tmem_slot = (uint32_t*)(done + 1);
+
+  const int item_idx = blockIdx.x / a.tiles;
+  const int tile = blockIdx.x % a.tiles;
+  if (item_idx >= *a.n_items) return;
+  const PfItem it = a.items[item_idx];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nk = a.K / kPfKStep;
+  const int sbytes = a.K / 32;                   // scale bytes per weight row
+  const int n_mma = (it.count + 15) & ~15;       // MMA N
+  const int n_box = (it.count + kPfBox - 1) / kPfBox;
+  const uint32_t b_bytes = (uint32_t)n_box * kPfBox * 128;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPfStages; ++s) {
+      mbar_init(&full[s], 256 + 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < kPfRaw; ++s) {
+      mbar_init(&rawf[s], 1);
+      mbar_init(&rawe[s], 256);
+    }
+    mbar_init(sbar, 1);
+    mbar_init(done, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 9) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                 "r"(256));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // feature rows of this tile in the weight matrices
+  const int f0 = a.mode == 0 ? tile * 64 : tile * 128;
+
+  if (warp == 8) {
+    if (lane == 0) {
+      // scales of the whole tile, once
+      if (a.mode == 0) {
+        mbar_expect_tx(sbar, 2 * 64 * sbytes);
+        tma_3d(sm + kOffScale, &mS0, 0, f0, it.slot, sbar);
+        tma_3d(sm + kOffScale + 64 * sbytes, &mS1, 0, f0, it.slot, sbar);
+      } else {
+        mbar_expect_tx(sbar, 128 * sbytes);
+        tma_3d(sm + kOffScale, &mS0, 0, f0, it.slot, sbar);
+      }
+      int raw_issued = 0;
+      bool ok = true;
+      for (int ks = 0; ks < nk && ok; ++ks) {
+        const int ahead = min(nk, ks + kPfRaw);
+        for (; raw_issued < ahead && ok; ++raw_issued) {
+          const int rs = raw_issued % kPfRaw, rr = raw_issued / kPfRaw;
+          if (rr > 0) ok = mbar_wait(&rawe[rs], (rr - 1) & 1, a.err);
+          if (!ok) break;
+          uint8_t* dst = sm + kOffRaw + rs * kRawTile;
+          mbar_expect_tx(&rawf[rs], kRawTile);
+          if (a.mode == 0) {
+            tma_3d(dst, &mA0, raw_issued * 32, f0, it.slot, &rawf[rs]);
+            tma_3d(dst + 64 * 32, &mA1, raw_issued * 32, f0, it.slot, &rawf[rs]);
+          } else {
+            tma_3d(dst, &mA0, raw_issued * 32, f0, it.slot, &rawf[rs]);
+          }
+        }
+        if (!ok) break;
+        const int s = ks % kPfStages, r = ks / kPfStages;
+        if (r > 0) ok = mbar_wait(&empty[s], (r - 1) & 1, a.err);
+        if (!ok) break;
+        uint8_t* bdst = sm + kOffB + s * kBTile;
+        mbar_expect_tx(&full[s], b_bytes);
+        for (int bx = 0; bx < n_box; ++bx)
+          tma_2d(bdst + bx * kPfBox * 128, &mB, ks * kPfKStep, it.row0 + bx * kPfBox, &full[s]);
+      }
+    }
+  } else if (warp == 9) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(n_mma);
+      bool ok = true;
+      for (int ks = 0; ks < nk && ok; ++ks) {
+        const int s = ks % kPfStages, r = ks / kPfStages;
+        ok = mbar_wait(&full[s], r & 1, a.err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t ad = umma_desc_sw128(su32(sm + kOffA + s * kATile));
+        const uint64_t bd = umma_desc_sw128(su32(sm + kOffB + s * kBTile));
+#pragma unroll
+        for (int kk = 0; kk < kPfKStep / 16; ++kk)
+          mma_bf16(tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (ks | kk) != 0);
+        mma_commit(&empty[s]);
+      }
+      mma_commit(done);  // fires when every issued MMA has completed
+    }
+  } else if (warp < 8) {
+    // converters: thread -> (row r, 32-weight half c) of the 128 x 64 A tile
+    const int t = threadIdx.x;
+    const int r = t >> 1, c = t & 1;
+    const int g = r & 1, i = r >> 1;  // mode 0: gate/up interleaved rows
+    const int raw_off = a.mode == 0 ? (g * 64 + i) * 32 + c * 16 : r * 32 + c * 16;
+    const uint8_t* srow = sm + kOffScale + (a.mode == 0 ? (g * 64 + i) : r) * sbytes;
+    bool ok = mbar_wait(sbar, 0, a.err);
+    for (int ks = 0; ks < nk && ok; ++ks) {
+      const int rs = ks % kPfRaw, rr = ks / kPfRaw;
+      const int s = ks % kPfStages, rnd = ks / kPfStages;
+      if (!(ok = mbar_wait(&rawf[rs], rr & 1, a.err))) break;
+      const uint4 q = *reinterpret_cast<const uint4*>(sm + kOffRaw + rs * kRawTile + raw_off);
+      const uint32_t sc2 = e8m0_bf16x2(srow[ks * 2 + c]);
+      mbar_arrive(&rawe[rs]);
+      if (rnd > 0 && !(ok = mbar_wait(&empty[s], (rnd - 1) & 1, a.err))) break;
+      uint8_t* arow = sm + kOffA + s * kATile + r * 128;
+      const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t wv = w4[u];
+        uint4 o;
+        o.x = fp4x2_to_bf16x2(wv & 0xff, sc2);
+        o.y = fp4x2_to_bf16x2((wv >> 8) & 0xff, sc2);
+        o.z = fp4x2_to_bf16x2((wv >> 16) & 0xff, sc2);
+        o.w = fp4x2_to_bf16x2(wv >> 24, sc2);
+        const int unit = c * 4 + u;
+        *reinterpret_cast<uint4*>(arow + ((unit ^ (r & 7)) << 4)) = o;
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(&full[s]);
+    }
+  }
+
+  // epilogue: warps 8-11 (TMEM lane quadrants 0-3)
+  if (warp >= 8) {
+    __syncwarp();
+    bool ok = mbar_wait(done, 0, a.err);
+    ok = __all_sync(0xffffffffu, ok);
+    __syncwarp();
+    tc_fence_after();
+    const int q = warp - 8;
+    const int row = q * 32 + lane;  // D row = A tile row
+    if (ok) {
+      for (int c0 = 0; c0 < n_mma; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
+        if (a.mode == 0) {
+          const int feat = f0 + (row >> 1);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float mine = __uint_as_float(v[j]);
+            const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+            const int col = c0 + j;
+            if ((row & 1) == 0 && col < it.count) {
+              const float hv = mine / (1.f + expf(-mine)) * other;
+              a.hs[(size_t)(it.row0 + col) * a.I + feat] = __float2bfloat16_rn(hv);
+            }
+          }
+        } else {
+          const int feat = f0 + row;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int col = c0 + j;
+            if (col < it.count) {
+              const int p = a.perm[it.row0 + col];
+              a.o[(size_t)p * a.H + feat] = __uint_as_float(v[j]);
+            }
+          }
+        }
+      }
+    }
+  }
+  // on a timeout, give copies still in flight time to land before the CTA exits
+  if (threadIdx.x == 8 * 32 && *(volatile int*)a.err == MOE_ERR_TIMEOUT) {
+    const uint64_t t0 = gtimer();
+    while (gtimer() - t0 < 2000000ull) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256));
+  }
+}
+
+// items: per slot, tiles of <= kPfNMax sorted rows
+__global__ void prefill_items_kernel(const int* offsets, int S, PfItem* items, int* n_items) {
+  __shared__ int ws[34];
+  const int tid = threadIdx.x, NT = blockDim.x;
+  const int per = (S + NT - 1) / NT;
+  const int s0 = min(S, tid * per), s1 = min(S, s0 + per);
+  int local = 0;
+  for (int s = s0; s < s1; ++s) local += (offsets[s + 1] - offsets[s] + kPfNMax - 1) / kPfNMax;
+  int total;
+  int pos = block_exclusive_scan(local, ws, &total);
+  for (int s = s0; s < s1; ++s) {
+    const int b = offsets[s], cnt = offsets[s + 1] - b;
+    for (int t = 0; t * kPfNMax < cnt; ++t) {
+      PfItem itm;
+      itm.slot = s;
+      itm.row0 = b + t * kPfNMax;
+      itm.count = min(kPfNMax, cnt - t * kPfNMax);
+      itm.pad = 0;
+      items[pos++] = itm;
+    }
+  }
+  if (tid == 0) *n_items = total;
+}
+
+__global__ void gather_rows_kernel(const uint16_t* x, int H, int k, const int* perm, const int* offsets, int S,
+                                   uint16_t* xg) {
+  const int n = offsets[S];
+  const int units = H / 8;
+  for (size_t u = (size_t)blockIdx.x * blockDim.x + threadIdx.x; u < (size_t)n * units;
+       u += (size_t)gridDim.x * blockDim.x) {
+    const int i = (int)(u / units), c = (int)(u % units);
+    const int tok = perm[i] / k;
+    reinterpret_cast<uint4*>(xg + (size_t)i * H)[c] = reinterpret_cast<const uint4*>(x + (size_t)tok * H)[c];
+  }
+}
+
+__global__ void prefill_combine_kernel(const float* o, const int32_t* slots, const float* w, int T, int k, int H,
+                                       int S, uint16_t* y) {
+  const int t = blockIdx.y;
+  for (int n = blockIdx.x * blockDim.x + threadIdx.x; n < H; n += gridDim.x * blockDim.x) {
+    float acc = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int p = t * k + j;
+      const int sl = slots[p];
+      if (sl >= 0 && sl < S) acc = fmaf(w[p], o[(size_t)p * H + n], acc);
+    }
+    y[(size_t)t * H + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+  }
+}
+
+// ------------------------------------------------------------------- host --
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  });
+  return fn;
+}
+
+// rank-3 byte map: (x: row bytes, y: rows, z: slots)
+static moe_status map_bytes3(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint64_t slots,
+                             uint64_t slot_stride, uint32_t box_x, uint32_t box_y) {
+  auto fn = encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[3] = {row_bytes, rows, slots};
+  cuuint64_t strides[2] = {row_bytes, slot_stride};
+  cuuint32_t box[3] = {box_x, box_y, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (weights) failed: %d", (int)r);
+  return MOE_OK;
+}
+
+// rank-2 bf16 map with 128-byte swizzle, box 64 x kPfBox
+static moe_status map_bf16_rows(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kPfBox};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (activations) failed: %d", (int)r);
+  return MOE_OK;
+}
+
+static size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct PfLayout {
+  size_t offsets, perm, items, nitems, err2, xg, hs, o, total;
+};
+
+static PfLayout pf_layout(int H, int I, int T, int k, int S) {
+  const size_t P = (size_t)T * k;
+  const size_t max_items = (size_t)S + P / kPfNMax + 1;
+  PfLayout L;
+  size_t off = 0;
+  L.offsets = off;
+  off = a256(off + (S + 1) * 4);
+  L.perm = off;
+  off = a256(off + P * 4);
+  L.items = off;
+  off = a256(off + max_items * sizeof(PfItem));
+  L.nitems = off;
+  off = a256(off + 16);
+  L.err2 = off;
+  off = a256(off + 16);
+  L.xg = off;
+  off = a256(off + P * H * 2);
+  L.hs = off;
+  off = a256(off + P * I * 2);
+  L.o = off;
+  off = a256(off + P * H * 4);
+  L.total = off;
+  return L;
+}
+
+size_t prefill_workspace(int H, int I, int T, int k, int S) { return pf_layout(H, I, T, k, S).total; }
+
+moe_status prefill_forward(const moe_expert_views* v, const uint16_t* x, int T, int k, const int32_t* slots,
+                           const float* w, uint16_t* y, void* workspace, size_t ws_bytes, int32_t* d_error,
+                           cudaStream_t stream) {
+  const int H = v->H, I = v->I, S = v->fp4_num_slots;
+  MOE_ARG(v->fp4_slots && S >= 1, "the grouped GEMM path needs the FP4 pool");
+  MOE_ARG(v->int2_slots == nullptr && v->shared == nullptr,
+          "the grouped GEMM path takes the FP4 pool only (no 2-bit pool, no shared expert)");
+  MOE_ARG(H % 512 == 0 && I % 512 == 0,
+          "the grouped GEMM path needs H and I multiples of 512 (16-byte rows of E8M0 scales)");
+  MOE_ARG(S <= 16384, "too many slots");
+  MOE_ARG(d_error != nullptr, "the grouped GEMM path needs d_error");
+  const PfLayout L = pf_layout(H, I, T, k, S);
+  MOE_ARG(ws_bytes >= L.total, "workspace too small: %zu < %zu", ws_bytes, L.total);
+  uint8_t* base = (uint8_t*)workspace;
+  int* offsets = (int*)(base + L.offsets);
+  int* perm = (int*)(base + L.perm);
+  PfItem* items = (PfItem*)(base + L.items);
+  int* nitems = (int*)(base + L.nitems);
+  uint16_t* xg = (uint16_t*)(base + L.xg);
+  __nv_bfloat16* hs = (__nv_bfloat16*)(base + L.hs);
+  float* o = (float*)(base + L.o);
+  const size_t P = (size_t)T * k;
+
+  moe_status st = moe_group_pairs(slots, T, k, S, offsets, perm, d_error, stream);
+  if (st != MOE_OK) return st;
+  prefill_items_kernel<<<1, 1024, 0, stream>>>(offsets, S, items, nitems);
+  if ((st = check_launch("prefill_items_kernel")) != MOE_OK) return st;
+  {
+    const int blocks = (int)std::min<size_t>((P * (H / 8) + 255) / 256, 152 * 16);
+    gather_rows_kernel<<<blocks, 256, 0, stream>>>(x, H, k, perm, offsets, S, xg);
+    if ((st = check_launch("gather_rows_kernel")) != MOE_OK) return st;
+  }
+  // weight maps over the whole pool: dims (row bytes, rows, slots)
+  const size_t B = fp4_bytes(H, I);
+  const uint8_t* pool = v->fp4_slots;
+  const size_t hi = (size_t)H * I;
+  const uint8_t* w1c = pool;
+  const uint8_t* w1s = pool + hi / 2;
+  const uint8_t* w3c = pool + (hi / 2 + hi / 32);
+  const uint8_t* w3s = w3c + hi / 2;
+  const uint8_t* w2c = pool + 2 * (hi / 2 + hi / 32);
+  const uint8_t* w2s = w2c + hi / 2;
+  CUtensorMap m1c, m3c, m1s, m3s, m2c, m2s, mx, mh;
+  if ((st = map_bytes3(&m1c, w1c, H / 2, I, S, B, 32, 64)) != MOE_OK) return st;
+  if ((st = map_bytes3(&m3c, w3c, H / 2, I, S, B, 32, 64)) != MOE_OK) return st;
+  if ((st = map_bytes3(&m1s, w1s, H / 32, I, S, B, H / 32, 64)) != MOE_OK) return st;
+  if ((st = map_bytes3(&m3s, w3s, H / 32, I, S, B, H / 32, 64)) != MOE_OK) return st;
+  if ((st = map_bytes3(&m2c, w2c, I / 2, H, S, B, 32, 128)) != MOE_OK) return st;
+  if ((st = map_bytes3(&m2s, w2s, I / 32, H, S, B, I / 32, 128)) != MOE_OK) return st;
+  if ((st = map_bf16_rows(&mx, xg, H, P)) != MOE_OK) return st;
+  if ((st = map_bf16_rows(&mh, hs, I, P)) != MOE_OK) return st;
+
+  static bool smem_set = false;
+  if (!smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_gemm_kernel)");
+    smem_set = true;
+  }
+  const int max_items = S + (int)(P / kPfNMax) + 1;
+  PfArgs pa;
+  pa.H = H;
+  pa.I = I;
+  pa.k = k;
+  pa.S = S;
+  pa.items = items;
+  pa.n_items = nitems;
+  pa.perm = perm;
+  pa.hs = hs;
+  pa.o = o;
+  pa.err = d_error;
+  // GEMM1: gate/up, 64 features per tile
+  pa.mode = 0;
+  pa.K = H;
+  pa.tiles = I / 64;
+  {
+    ProfScope ps(MOE_K_GATEUP, stream);
+    prefill_gemm_kernel<<<max_items * pa.tiles, kPfThreads, kPfSmem, stream>>>(m1c, m3c, m1s, m3s, mx, pa);
+  }
+  if ((st = check_launch("prefill_gemm_kernel (gate/up)")) != MOE_OK) return st;
+  // GEMM2: down, 128 features per tile
+  pa.mode = 1;
+  pa.K = I;
+  pa.tiles = H / 128;
+  {
+    ProfScope ps(MOE_K_DOWN, stream);
+    prefill_gemm_kernel<<<max_items * pa.tiles, kPfThreads, kPfSmem, stream>>>(m2c, m2c, m2s, m2s, mh, pa);
+  }
+  if ((st = check_launch("prefill_gemm_kernel (down)")) != MOE_OK) return st;
+  {
+    ProfScope ps(MOE_K_COMBINE, stream);
+    dim3 cg((H + 1023) / 1024, T);
+    prefill_combine_kernel<<<cg, 256, 0, stream>>>(o, slots, w, T, k, H, S, y);
+  }
+  return check_launch("prefill_combine_kernel");
+}
+
+}  // namespace moe
+
+extern "C" size_t moe_expert_prefill_workspace(const moe_expert_views* v, int T, int k) {
+  if (!v || T < 0 || k < 1) return 0;
+  return moe::prefill_workspace(v->H, v->I, T, k, v->fp4_num_slots);
+}
+
+extern "C" moe_status moe_expert_prefill(const moe_expert_views* v, const uint16_t* x, int T, int k,
+                                         const int32_t* slots, const float* w, uint16_t* y, void* workspace,
+                                         size_t workspace_bytes, int32_t* d_error, cudaStream_t stream) {
+  moe::clear_error();
+  MOE_ARG(v != nullptr, "views is null");
+  MOE_ARG(T >= 0 && k >= 1 && k <= 64, "need T >= 0 and 1 <= k <= 64");
+  if (T == 0) return MOE_OK;
+  MOE_ARG(x && slots && w && y && workspace, "null pointer");
+  MOE_ARG(((uintptr_t)workspace & 255) == 0, "workspace must be 256-byte aligned");
+  MOE_ARG(((uintptr_t)x & 15) == 0, "x must be 16-byte aligned");
+  return moe::prefill_forward(v, x, T, k, slots, w, y, workspace, workspace_bytes, d_error, stream);
+}
