@@ -131,6 +131,19 @@ print(json.dumps({{"tokens": tokens, "seconds": dt}}))
 """
 
 
+def aggregate(ms_local: float, tokens_local: int, world: int, device=None):
+    """Whole-job numbers for N independent replicas: the step time is the max
+    over ranks, the throughput counts every rank's tokens."""
+    ms = ms_local
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * tokens_local / (ms / 1e3)
+
+
 def cpu_baseline(T: int, steps: int = 1):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     code = _CPU_SNIPPET.format(root=ROOT, T=T, steps=steps)
@@ -232,15 +245,11 @@ def run_ours(args):
         step_ms = [a.elapsed_time(b) for a, b in ev]
         kt = {M.KERNEL_NAMES[kid]: M.moe_profile_query(kid) for kid in range(M.MOE_K_COUNT)}
         M.moe_profile_enable(False)
-        ms = sum(step_ms) / len(step_ms)
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t)
+        ms, tps = aggregate(sum(step_ms) / len(step_ms), T, world, dev)
         gu_ms, gu_n = kt["gateup"]
         compute_ms = sum(v[0] for v in kt.values()) / args.steps
         return {
-            "T": T, "ms_per_step": ms, "tokens_per_s": world * T / (ms / 1e3),
+            "T": T, "ms_per_step": ms, "tokens_per_s": tps,
             "compute_only_tokens_per_s": T / (compute_ms / 1e3),
             "layer_gbs": acct_layer_bytes / args.steps / (ms / 1e3) / 1e9,
             "gateup_ms": gu_ms / max(gu_n, 1), "gateup_launches": gu_n,

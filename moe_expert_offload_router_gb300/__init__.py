@@ -2,9 +2,22 @@
 
 The compute path is the C-ABI library ``libmoe_gb300.so`` (see
 ``include/moe_gb300.h``); this package is its ctypes binding plus a host-side
-layer runner.  Importing it fails if the library has not been built: there is
-no fallback path.
+layer runner.  The binding loads on first use of any of its names and raises
+if the library has not been built (``moe_expert_offload_router_gb300.build``):
+there is no fallback path.
 """
-from ._lib import *  # noqa: F401,F403
-from ._lib import MoeError, moe_cache, make_views, raw  # noqa: F401
-from .layer import DecodeLayerRunner  # noqa: F401
+import importlib
+
+_SUBMODULES = ("build", "layer", "_lib")
+
+
+def __getattr__(name):
+    if name in _SUBMODULES or name.startswith("__"):
+        raise AttributeError(name)   # the import system then loads the submodule
+    if name == "DecodeLayerRunner":
+        return importlib.import_module(__name__ + ".layer").DecodeLayerRunner
+    lib = importlib.import_module(__name__ + "._lib")
+    try:
+        return getattr(lib, name)
+    except AttributeError:
+        raise AttributeError(f"module {__name__!r} has no attribute {name!r}") from None

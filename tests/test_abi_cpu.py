@@ -46,7 +46,7 @@ def test_host_only_calls(lib):
     assert lib.moe_version() >= 1
 
 
-def test_binding_names_match_header():
+def test_binding_names_match_header(lib):
     from moe_expert_offload_router_gb300 import _lib as L
     for n in _declared():
         if n in ("moe_cache_create", "moe_cache_destroy", "moe_cache_reset", "moe_cache_state",
