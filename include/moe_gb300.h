@@ -261,6 +261,27 @@ moe_status moe_expert_prefill(const moe_expert_views* v, const uint16_t* x, int 
                               const int32_t* slots, const float* w, uint16_t* y, void* workspace,
                               size_t workspace_bytes, int32_t* d_error, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * moe_expert_forward without a caller-provided workspace.  The pages have no
+ * counterpart; this serves callers that cannot allocate device memory: hosts
+ * that hand a module a stream but own the device-memory budget, and serving
+ * loops that forbid cudaMalloc after start-up (it can synchronise the device
+ * and fail once memory is committed).  The scratch is a fixed 16 MiB array in
+ * the library's device memory (held by every GPU that loads the library until
+ * the process exits), enough for T = 64 tokens of top-8 at H = 4096,
+ * I = 2048; larger calls return MOE_ERR_INVALID.  The caller still passes the
+ * inputs and outputs; arguments as moe_expert_forward (decode path only:
+ * T * k <= 4096).  The first call on a device looks up the scratch's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  The call allocates nothing.  All calls
+ * share the one scratch, which keeps the last call's contents (nothing in it
+ * needs to start at zero): calls that overlap on the GPU race, so issue them
+ * on one stream or order them.
+ * ------------------------------------------------------------------------- */
+moe_status moe_expert_forward_noalloc(const moe_expert_views* v, const uint16_t* x, int T, int k,
+                                      const int32_t* slots, const int8_t* tags, const float* w,
+                                      uint16_t* y, int32_t* d_error, cudaStream_t stream);
+
 /* Decode one matrix of one slot to fp32 [N, K] (test hook; values are exact). */
 moe_status moe_dequant_debug(const moe_expert_views* v, int pool, int slot, int matrix,
                              float* out, cudaStream_t stream);

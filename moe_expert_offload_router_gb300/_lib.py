@@ -67,6 +67,7 @@ _SIGS = {
     "moe_expert_forward": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, vp,
                                  sz, vp, vp]),
     "moe_dequant_debug": (i32, [C.POINTER(moe_expert_views), i32, i32, i32, vp, vp]),
+    "moe_expert_forward_noalloc": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, vp, vp]),
     "moe_expert_prefill_workspace": (sz, [C.POINTER(moe_expert_views), i32, i32]),
     "moe_expert_prefill": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, sz, vp, vp]),
     "moe_rms_carry": (i32, [vp, i32, i32, f32, vp, vp]),
@@ -251,6 +252,13 @@ def moe_expert_forward(views: moe_expert_views, x, slots, tags, w, y, workspace,
     _check(_lib.moe_expert_forward(C.byref(views), _p(x), T, k, _p(slots), _p(tags), _p(w), _p(y),
                                    _p(workspace), workspace.numel() * workspace.element_size(),
                                    _p(d_error), _s(stream)))
+
+
+def moe_expert_forward_noalloc(views: moe_expert_views, x, slots, tags, w, y, d_error=None, stream=None):
+    """moe_expert_forward with the library's fixed device scratch instead of a workspace."""
+    T, k = slots.shape
+    _check(_lib.moe_expert_forward_noalloc(C.byref(views), _p(x), T, k, _p(slots), _p(tags), _p(w), _p(y),
+                                           _p(d_error), _s(stream)))
 
 
 def moe_expert_prefill_workspace(views: moe_expert_views, T: int, k: int) -> int:

@@ -27,6 +27,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -998,6 +1000,53 @@ extern "C" moe_status moe_expert_forward(const moe_expert_views* v, const uint16
   ProfScope ps(MOE_K_COMBINE, stream);
   combine_kernel<<<cg, 256, 0, stream>>>(a);
   return check_launch("combine_kernel");
+}
+
+// ------------------------------------------------------ allocation-free entry --
+// Scratch for moe_expert_forward_noalloc: a fixed array in device memory that
+// every GPU loading this library holds until the process exits.  Host code
+// cannot pass the array's name to a kernel (on the host it names a stand-in,
+// not device memory), so its device address is looked up once per device.
+constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_addr[128] = {};
+
+static moe_status noalloc_scratch(void** out) {
+  int dev = 0;
+  MOE_CUDA(cudaGetDevice(&dev));
+  MOE_ARG(dev >= 0 && dev < 128, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(fixed scratch)");
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_expert_forward_noalloc(const moe_expert_views* v, const uint16_t* x, int T, int k,
+                                                 const int32_t* slots, const int8_t* tags, const float* w,
+                                                 uint16_t* y, int32_t* d_error, cudaStream_t stream) {
+  clear_error();
+  moe_status st = validate_views(v);
+  if (st != MOE_OK) return st;
+  MOE_ARG(T >= 0 && k >= 1 && k <= 64, "need T >= 0 and 1 <= k <= 64");
+  if (T == 0) return MOE_OK;
+  MOE_ARG((long long)T * k <= kMaxPlanPairs, "T * k = %lld: the allocation-free call takes at most %d pairs",
+          (long long)T * k, kMaxPlanPairs);
+  const size_t need = fwd_layout(v->H, v->I, T, k).total;
+  MOE_ARG(need <= kNoAllocScratchBytes,
+          "this call needs %zu bytes of scratch but the fixed scratch holds %zu; pass fewer tokens per call", need,
+          kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != MOE_OK) return st;
+  // nothing in the scratch has to start at zero: every region is written
+  // by an earlier kernel of the same call before it is read
+  return moe_expert_forward(v, x, T, k, slots, tags, w, y, scratch, kNoAllocScratchBytes, d_error, stream);
 }
 
 extern "C" moe_status moe_dequant_debug(const moe_expert_views* v, int pool, int slot, int matrix,
