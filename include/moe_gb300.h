@@ -300,7 +300,7 @@ moe_status moe_rms_carry(const uint16_t* y, int T, int H, float eps, uint16_t* x
  * ------------------------------------------------------------------------- */
 enum {
   MOE_K_ROUTER = 0, MOE_K_ENSURE, MOE_K_LADDER, MOE_K_GROUP, MOE_K_PLAN, MOE_K_GATEUP,
-  MOE_K_DOWN, MOE_K_COMBINE, MOE_K_CARRY, MOE_K_COUNT
+  MOE_K_DOWN, MOE_K_COMBINE, MOE_K_CARRY, MOE_K_GEMM_GATEUP, MOE_K_GEMM_DOWN, MOE_K_COUNT
 };
 moe_status moe_profile_enable(int enable);
 moe_status moe_profile_query(int kernel, double* total_ms, int* launches);

@@ -18,9 +18,9 @@ MOE_TAG_FP4, MOE_TAG_INT2, MOE_TAG_DROP = 0, 1, 2
 MOE_POOL_FP4, MOE_POOL_INT2, MOE_POOL_SHARED = 0, 1, 2
 MOE_W1, MOE_W3, MOE_W2 = 0, 1, 2
 (MOE_K_ROUTER, MOE_K_ENSURE, MOE_K_LADDER, MOE_K_GROUP, MOE_K_PLAN, MOE_K_GATEUP, MOE_K_DOWN,
- MOE_K_COMBINE, MOE_K_CARRY, MOE_K_COUNT) = range(10)
+ MOE_K_COMBINE, MOE_K_CARRY, MOE_K_GEMM_GATEUP, MOE_K_GEMM_DOWN, MOE_K_COUNT) = range(12)
 KERNEL_NAMES = ["router", "ensure", "ladder", "group_pairs", "plan", "gateup", "down", "combine",
-                "rms_carry"]
+                "rms_carry", "gemm_gateup", "gemm_down"]
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_CAPACITY", 3: "MOE_ERR_CUDA",
                 4: "MOE_ERR_TIMEOUT", 5: "MOE_ERR_NOMEM"}
 

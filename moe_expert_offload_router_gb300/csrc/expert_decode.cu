@@ -30,6 +30,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "grouped_gemm.cuh"
 
 namespace moe {
 
@@ -38,18 +39,21 @@ constexpr int kFwdThreads = 256;  // 8 warps
 constexpr int kRowsGateUp = 32;   // rows of w1/w3 per gate/up work item
 constexpr int kRowsDown = 64;     // rows of w2 per down work item
 constexpr int kMaxPlanPairs = 4096;
+constexpr int kGemmMinPairs = 256;  // from here on the FP4 routed pairs take the tcgen05 grouped GEMM
 
 struct Group {
   int pool, slot, begin, count;
 };
 
 struct FwdLayout {
-  size_t hdr, perm, groups, xsig, xs, h, o, total;
+  size_t hdr, perm, groups, xsig, xs, h, o, gg, total;
+  bool gemm;  // the FP4 routed pairs may take the grouped GEMM
 };
 
 static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-static FwdLayout fwd_layout(int H, int I, int T, int k) {
+static FwdLayout fwd_layout(const moe_expert_views* v, int T, int k) {
+  const int H = v->H, I = v->I;
   const size_t P = (size_t)T * k;
   const size_t ng = P + (T + kG - 1) / kG + 1;
   FwdLayout L;
@@ -68,6 +72,9 @@ static FwdLayout fwd_layout(int H, int I, int T, int k) {
   off = align256(off + (P + T) * (size_t)I * 4);
   L.o = off;
   off = align256(off + (P + T) * (size_t)H * 4);
+  L.gemm = (long long)P >= kGemmMinPairs && grouped_gemm_supported(v);
+  L.gg = off;
+  if (L.gemm) off = align256(off + gg_index_bytes(T, k, v->fp4_num_slots));
   L.total = off;
   return L;
 }
@@ -86,6 +93,7 @@ struct FwdArgs {
   const float* w;
   uint16_t* y;
   int32_t* err;
+  int routed_gemm;  // routed pairs are computed by the grouped GEMM, not by these kernels
   // workspace
   int* hdr;
   int* perm;
@@ -169,6 +177,7 @@ __device__ __forceinline__ int unit_fp8(int c, int s) { return c * 2 + ((s + (c 
 // Each adds, for two rows (r0, r1) and every staged token, one 16-byte code
 // chunk's contribution to the lane's fp32 accumulators.
 
+template <int NT>
 __device__ __forceinline__ void chunk_fp4(uint4 q0, uint32_t e0, uint4 q1, uint32_t e1, int c,
                                           const uint4* xs, int xstride, int ntok, float* a0,
                                           float* a1) {
@@ -183,8 +192,8 @@ __device__ __forceinline__ void chunk_fp4(uint4 q0, uint32_t e0, uint4 q1, uint3
   fp4_word_to_h2(q1.w, w1 + 12);
   const float s0 = e8m0_f32(e0), s1 = e8m0_f32(e1);
 #pragma unroll
-  for (int t = 0; t < kG; ++t) {
-    if (t < ntok) {
+  for (int t = 0; t < NT; ++t) {
+    {
       const uint4* xp = xs + (size_t)t * xstride;
       __half2 x[16];
 #pragma unroll
@@ -204,43 +213,40 @@ __device__ __forceinline__ void chunk_fp4(uint4 q0, uint32_t e0, uint4 q1, uint3
   }
 }
 
+template <int NT>
 __device__ __forceinline__ void chunk_int2(uint4 q0, uint32_t e0, uint4 q1, uint32_t e1, int c,
                                            const uint4* xs, int xstride, int ntok, float* a0,
                                            float* a1) {
-  // 64 weights: words 0-1 form scale block 0, words 2-3 block 1
-  __half2 w0[32], w1[32];
-  int2_word_to_h2(q0.x, w0);
-  int2_word_to_h2(q0.y, w0 + 8);
-  int2_word_to_h2(q0.z, w0 + 16);
-  int2_word_to_h2(q0.w, w0 + 24);
-  int2_word_to_h2(q1.x, w1);
-  int2_word_to_h2(q1.y, w1 + 8);
-  int2_word_to_h2(q1.z, w1 + 16);
-  int2_word_to_h2(q1.w, w1 + 24);
+  // 64 weights: words 0-1 form scale block 0, words 2-3 block 1; one block at a time
   const float2 s0 = __half22float2(e4m3x2_to_h2(e0));
   const float2 s1 = __half22float2(e4m3x2_to_h2(e1));
 #pragma unroll
-  for (int t = 0; t < kG; ++t) {
-    if (t < ntok) {
-      const uint4* xp = xs + (size_t)t * xstride;
-      __half2 x[32];
+  for (int blk = 0; blk < 2; ++blk) {
+    __half2 w0[16], w1[16];
+    int2_word_to_h2(blk ? q0.z : q0.x, w0);
+    int2_word_to_h2(blk ? q0.w : q0.y, w0 + 8);
+    int2_word_to_h2(blk ? q1.z : q1.x, w1);
+    int2_word_to_h2(blk ? q1.w : q1.y, w1 + 8);
+    const float sa = blk ? s0.y : s0.x, sb = blk ? s1.y : s1.x;
 #pragma unroll
-      for (int s = 0; s < 8; ++s) lds4(xp + unit_int2(c, s), x + 4 * s);
-      __half2 pa = __hmul2(w0[0], x[0]), pb = __hmul2(w0[16], x[16]);
-      __half2 ra = __hmul2(w1[0], x[0]), rb = __hmul2(w1[16], x[16]);
+    for (int t = 0; t < NT; ++t) {
+      const uint4* xp = xs + (size_t)t * xstride;
+      __half2 x[16];
+#pragma unroll
+      for (int s = 0; s < 4; ++s) lds4(xp + unit_int2(c, 4 * blk + s), x + 4 * s);
+      __half2 pa = __hmul2(w0[0], x[0]), ra = __hmul2(w1[0], x[0]);
 #pragma unroll
       for (int i = 1; i < 16; ++i) {
         pa = __hfma2(w0[i], x[i], pa);
-        pb = __hfma2(w0[16 + i], x[16 + i], pb);
         ra = __hfma2(w1[i], x[i], ra);
-        rb = __hfma2(w1[16 + i], x[16 + i], rb);
       }
-      a0[t] += h2sum(pa) * s0.x + h2sum(pb) * s0.y;
-      a1[t] += h2sum(ra) * s1.x + h2sum(rb) * s1.y;
+      a0[t] = fmaf(h2sum(pa), sa, a0[t]);
+      a1[t] = fmaf(h2sum(ra), sb, a1[t]);
     }
   }
 }
 
+template <int NT>
 __device__ __forceinline__ void chunk_fp8(uint4 q0, uint4 q1, int c, const uint4* xs, int xstride,
                                           int ntok, float* a0, float* a1) {
   __half2 w0[8], w1[8];
@@ -253,8 +259,8 @@ __device__ __forceinline__ void chunk_fp8(uint4 q0, uint4 q1, int c, const uint4
   fp8_word_to_h2(q1.z, w1 + 4);
   fp8_word_to_h2(q1.w, w1 + 6);
 #pragma unroll
-  for (int t = 0; t < kG; ++t) {
-    if (t < ntok) {
+  for (int t = 0; t < NT; ++t) {
+    {
       const uint4* xp = xs + (size_t)t * xstride;
       __half2 x[8];
       lds4(xp + unit_fp8(c, 0), x);
@@ -276,7 +282,7 @@ __device__ __forceinline__ void chunk_fp8(uint4 q0, uint4 q1, int c, const uint4
 // row length; KC > 0 is K known at compile time (loads of all the lane's
 // chunks are issued before any is consumed).
 
-template <int KC>
+template <int KC, int NT>
 __device__ __forceinline__ void rows_fp4(const uint8_t* c0, const uint8_t* s0, const uint8_t* c1,
                                          const uint8_t* s1, int K, const uint4* xs, int ntok,
                                          float* a0, float* a1) {
@@ -295,16 +301,16 @@ __device__ __forceinline__ void rows_fp4(const uint8_t* c0, const uint8_t* s0, c
       e1[i] = __ldg(s1 + c);
     }
 #pragma unroll
-    for (int i = 0; i < CPL; ++i) chunk_fp4(q0[i], e0[i], q1[i], e1[i], lane + 32 * i, xs, xstride, ntok, a0, a1);
+    for (int i = 0; i < CPL; ++i) chunk_fp4<NT>(q0[i], e0[i], q1[i], e1[i], lane + 32 * i, xs, xstride, ntok, a0, a1);
   } else {
     const int nch = K / 32;
     for (int c = lane; c < nch; c += 32)
-      chunk_fp4(ld_stream_v4(c0 + (size_t)c * 16), __ldg(s0 + c), ld_stream_v4(c1 + (size_t)c * 16),
+      chunk_fp4<NT>(ld_stream_v4(c0 + (size_t)c * 16), __ldg(s0 + c), ld_stream_v4(c1 + (size_t)c * 16),
                 __ldg(s1 + c), c, xs, xstride, ntok, a0, a1);
   }
 }
 
-template <int KC>
+template <int KC, int NT>
 __device__ __forceinline__ void rows_int2(const uint8_t* c0, const uint8_t* s0, const uint8_t* c1,
                                           const uint8_t* s1, int K, const uint4* xs, int ntok,
                                           float* a0, float* a1) {
@@ -327,15 +333,15 @@ __device__ __forceinline__ void rows_int2(const uint8_t* c0, const uint8_t* s0, 
       e1[i] = sc(s1, c);
     }
 #pragma unroll
-    for (int i = 0; i < CPL; ++i) chunk_int2(q0[i], e0[i], q1[i], e1[i], lane + 32 * i, xs, xstride, ntok, a0, a1);
+    for (int i = 0; i < CPL; ++i) chunk_int2<NT>(q0[i], e0[i], q1[i], e1[i], lane + 32 * i, xs, xstride, ntok, a0, a1);
   } else {
     for (int c = lane; c < nch; c += 32)
-      chunk_int2(ld_stream_v4(c0 + (size_t)c * 16), sc(s0, c), ld_stream_v4(c1 + (size_t)c * 16),
+      chunk_int2<NT>(ld_stream_v4(c0 + (size_t)c * 16), sc(s0, c), ld_stream_v4(c1 + (size_t)c * 16),
                  sc(s1, c), c, xs, xstride, ntok, a0, a1);
   }
 }
 
-template <int KC>
+template <int KC, int NT>
 __device__ __forceinline__ void rows_fp8(const uint8_t* c0, const uint8_t* c1, int K, const uint4* xs,
                                          int ntok, float* a0, float* a1) {
   const int lane = threadIdx.x & 31;
@@ -351,21 +357,20 @@ __device__ __forceinline__ void rows_fp8(const uint8_t* c0, const uint8_t* c1, i
       q1[i] = ld_stream_v4(c1 + (size_t)c * 16);
     }
 #pragma unroll
-    for (int i = 0; i < CPL; ++i) chunk_fp8(q0[i], q1[i], lane + 32 * i, xs, xstride, ntok, a0, a1);
+    for (int i = 0; i < CPL; ++i) chunk_fp8<NT>(q0[i], q1[i], lane + 32 * i, xs, xstride, ntok, a0, a1);
   } else {
     for (int c = lane; c < nch; c += 32)
-      chunk_fp8(ld_stream_v4(c0 + (size_t)c * 16), ld_stream_v4(c1 + (size_t)c * 16), c, xs, xstride,
+      chunk_fp8<NT>(ld_stream_v4(c0 + (size_t)c * 16), ld_stream_v4(c1 + (size_t)c * 16), c, xs, xstride,
                 ntok, a0, a1);
   }
 }
 
-__device__ __forceinline__ void warp_allreduce(float* a, int ntok) {
+template <int NT>
+__device__ __forceinline__ void warp_allreduce(float* a) {
 #pragma unroll
-  for (int t = 0; t < kG; ++t) {
-    if (t < ntok) {
+  for (int t = 0; t < NT; ++t) {
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) a[t] += __shfl_xor_sync(0xffffffffu, a[t], o);
-    }
+    for (int o = 16; o > 0; o >>= 1) a[t] += __shfl_xor_sync(0xffffffffu, a[t], o);
   }
 }
 
@@ -496,10 +501,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(FwdArgs a) {
       if (sl >= 0 && tag != MOE_TAG_DROP) {
         const int pool = tag == MOE_TAG_INT2 ? MOE_POOL_INT2 : MOE_POOL_FP4;
         const int npool = pool == MOE_POOL_FP4 ? a.n4 : a.n2;
-        if ((tag == MOE_TAG_FP4 || tag == MOE_TAG_INT2) && sl < npool)
-          key = ((unsigned long long)((unsigned)pool << 30 | (unsigned)sl) << 32) | (unsigned)p;
-        else
+        if ((tag == MOE_TAG_FP4 || tag == MOE_TAG_INT2) && sl < npool) {
+          if (!a.routed_gemm)
+            key = ((unsigned long long)((unsigned)pool << 30 | (unsigned)sl) << 32) | (unsigned)p;
+        } else {
           scal[0] = 1;
+        }
       }
     }
     keys[p] = key;
@@ -608,6 +615,48 @@ __device__ __forceinline__ const uint8_t* expert_base(const FwdArgs& a, int pool
   return a.shared;
 }
 
+// Rows of one gate/up work item for a group of exactly NT tokens.
+template <int KH, int NT>
+__device__ __forceinline__ void gateup_rows(const FwdArgs& a, const Group& g, int tile, const uint4* xs,
+                                            const int* tok, const int* hrow, int H, int I) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint8_t* ex = expert_base(a, g.pool, g.slot);
+  const MatView w1 = mat_view(g.pool, ex, H, I, 0);
+  const MatView w3 = mat_view(g.pool, ex, H, I, 1);
+  for (int r = warp; r < kRowsGateUp; r += kFwdThreads / 32) {
+    const int n = tile * kRowsGateUp + r;
+    if (n >= I) break;
+    float ag[NT], au[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) ag[t] = au[t] = 0.f;
+    float rg = 1.f, ru = 1.f;
+    if (g.pool == MOE_POOL_FP4) {
+      rows_fp4<KH, NT>(w1.codes + (size_t)n * (H / 2), w1.scales + (size_t)n * (H / 32),
+                       w3.codes + (size_t)n * (H / 2), w3.scales + (size_t)n * (H / 32), H, xs, NT, ag, au);
+    } else if (g.pool == MOE_POOL_INT2) {
+      rows_int2<KH, NT>(w1.codes + (size_t)n * (H / 4), w1.scales + (size_t)n * (H / 32),
+                        w3.codes + (size_t)n * (H / 4), w3.scales + (size_t)n * (H / 32), H, xs, NT, ag, au);
+    } else {
+      rows_fp8<KH, NT>(w1.codes + (size_t)n * H, w3.codes + (size_t)n * H, H, xs, NT, ag, au);
+      rg = __ldg(reinterpret_cast<const float*>(w1.scales) + n);
+      ru = __ldg(reinterpret_cast<const float*>(w3.scales) + n);
+    }
+    warp_allreduce<NT>(ag);
+    warp_allreduce<NT>(au);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      if (t == lane) {
+        const int sg = a.xsig[tok[t]];
+        const float gv = ldexpf(ag[t] * rg, sg);
+        const float uv = ldexpf(au[t] * ru, sg);
+        a.h[(size_t)hrow[t] * I + n] = gv / (1.f + expf(-gv)) * uv;
+      }
+    }
+  }
+}
+
+// Each CTA takes a contiguous range of the (group, tile) items, so the group's
+// activations are staged once for all of the CTA's tiles of that group.
 template <int KH>
 __global__ void __launch_bounds__(kFwdThreads, 2) gateup_kernel(FwdArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -617,67 +666,84 @@ __global__ void __launch_bounds__(kFwdThreads, 2) gateup_kernel(FwdArgs a) {
   const int H = KH > 0 ? KH : a.H;
   const int I = a.I;
   const int tiles = (I + kRowsGateUp - 1) / kRowsGateUp;
-  const int n_items = n_groups_checked(a) * tiles;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const Group g = a.groups[item / tiles];
-    const int tile = item % tiles;
+  const long long n_items = (long long)n_groups_checked(a) * tiles;
+  const long long i0 = n_items * blockIdx.x / gridDim.x, i1 = n_items * (blockIdx.x + 1) / gridDim.x;
+  int staged = -1;
+  for (long long item = i0; item < i1; ++item) {
+    const int gi = (int)(item / tiles);
+    const int tile = (int)(item % tiles);
+    const Group g = a.groups[gi];
     if (!group_ok(a, g)) {
       if (threadIdx.x == 0 && a.err) *a.err = MOE_ERR_INVALID;
       continue;
     }
-    if (threadIdx.x < g.count) {
-      const int i = threadIdx.x;
-      if (g.pool == MOE_POOL_SHARED) {
-        tok[i] = g.begin + i;
-        hrow[i] = a.P + g.begin + i;
-      } else {
-        const int p = min(max(a.perm[g.begin + i], 0), a.P - 1);
-        tok[i] = p / a.k;
-        hrow[i] = p;
-      }
-    }
-    __syncthreads();
-    stage_rows(g.pool, H, g.count, [&](int i) { return a.xs + (size_t)tok[i] * H; }, xs);
-    __syncthreads();
-    const uint8_t* ex = expert_base(a, g.pool, g.slot);
-    const MatView w1 = mat_view(g.pool, ex, H, I, 0);
-    const MatView w3 = mat_view(g.pool, ex, H, I, 1);
-    for (int r = warp; r < kRowsGateUp; r += kFwdThreads / 32) {
-      const int n = tile * kRowsGateUp + r;
-      if (n >= I) break;
-      float ag[kG], au[kG];
-#pragma unroll
-      for (int t = 0; t < kG; ++t) ag[t] = au[t] = 0.f;
-      float rg = 1.f, ru = 1.f;
-      if (g.pool == MOE_POOL_FP4) {
-        rows_fp4<KH>(w1.codes + (size_t)n * (H / 2), w1.scales + (size_t)n * (H / 32),
-                     w3.codes + (size_t)n * (H / 2), w3.scales + (size_t)n * (H / 32), H, xs, g.count, ag, au);
-      } else if (g.pool == MOE_POOL_INT2) {
-        rows_int2<KH>(w1.codes + (size_t)n * (H / 4), w1.scales + (size_t)n * (H / 32),
-                      w3.codes + (size_t)n * (H / 4), w3.scales + (size_t)n * (H / 32), H, xs, g.count, ag, au);
-      } else {
-        rows_fp8<KH>(w1.codes + (size_t)n * H, w3.codes + (size_t)n * H, H, xs, g.count, ag, au);
-        rg = __ldg(reinterpret_cast<const float*>(w1.scales) + n);
-        ru = __ldg(reinterpret_cast<const float*>(w3.scales) + n);
-      }
-      warp_allreduce(ag, g.count);
-      warp_allreduce(au, g.count);
-#pragma unroll
-      for (int t = 0; t < kG; ++t) {
-        if (t == lane && t < g.count) {
-          const int sg = a.xsig[tok[t]];
-          const float gv = ldexpf(ag[t] * rg, sg);
-          const float uv = ldexpf(au[t] * ru, sg);
-          a.h[(size_t)hrow[t] * I + n] = gv / (1.f + expf(-gv)) * uv;
+    if (gi != staged) {
+      __syncthreads();  // the previous group's rows are done with xs
+      if (threadIdx.x < g.count) {
+        const int i = threadIdx.x;
+        if (g.pool == MOE_POOL_SHARED) {
+          tok[i] = g.begin + i;
+          hrow[i] = a.P + g.begin + i;
+        } else {
+          const int p = min(max(a.perm[g.begin + i], 0), a.P - 1);
+          tok[i] = p / a.k;
+          hrow[i] = p;
         }
       }
+      __syncthreads();
+      stage_rows(g.pool, H, g.count, [&](int i) { return a.xs + (size_t)tok[i] * H; }, xs);
+      __syncthreads();
+      staged = gi;
     }
-    __syncthreads();
+    switch (g.count) {
+      case 1: gateup_rows<KH, 1>(a, g, tile, xs, tok, hrow, H, I); break;
+      case 2: gateup_rows<KH, 2>(a, g, tile, xs, tok, hrow, H, I); break;
+      case 3: gateup_rows<KH, 3>(a, g, tile, xs, tok, hrow, H, I); break;
+      case 4: gateup_rows<KH, 4>(a, g, tile, xs, tok, hrow, H, I); break;
+      case 5: gateup_rows<KH, 5>(a, g, tile, xs, tok, hrow, H, I); break;
+      case 6: gateup_rows<KH, 6>(a, g, tile, xs, tok, hrow, H, I); break;
+      case 7: gateup_rows<KH, 7>(a, g, tile, xs, tok, hrow, H, I); break;
+      default: gateup_rows<KH, 8>(a, g, tile, xs, tok, hrow, H, I); break;
+    }
   }
 }
 
 // -------------------------------------------------------------- down kernel --
+
+template <int KI, int NT>
+__device__ __forceinline__ void down_rows(const FwdArgs& a, const Group& g, int tile, const uint4* xs,
+                                          const int* hrow, const int* sig, int H, int I) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint8_t* ex = expert_base(a, g.pool, g.slot);
+  const MatView w2 = mat_view(g.pool, ex, H, I, 2);
+  for (int r = 2 * warp; r < kRowsDown; r += 2 * (kFwdThreads / 32)) {
+    const int n = tile * kRowsDown + r;
+    if (n >= H) break;
+    const int n1 = min(n + 1, H - 1);
+    float a0[NT], a1[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) a0[t] = a1[t] = 0.f;
+    float r0 = 1.f, r1 = 1.f;
+    if (g.pool == MOE_POOL_FP4) {
+      rows_fp4<KI, NT>(w2.codes + (size_t)n * (I / 2), w2.scales + (size_t)n * (I / 32),
+                       w2.codes + (size_t)n1 * (I / 2), w2.scales + (size_t)n1 * (I / 32), I, xs, NT, a0, a1);
+    } else if (g.pool == MOE_POOL_INT2) {
+      rows_int2<KI, NT>(w2.codes + (size_t)n * (I / 4), w2.scales + (size_t)n * (I / 32),
+                        w2.codes + (size_t)n1 * (I / 4), w2.scales + (size_t)n1 * (I / 32), I, xs, NT, a0, a1);
+    } else {
+      rows_fp8<KI, NT>(w2.codes + (size_t)n * I, w2.codes + (size_t)n1 * I, I, xs, NT, a0, a1);
+      r0 = __ldg(reinterpret_cast<const float*>(w2.scales) + n);
+      r1 = __ldg(reinterpret_cast<const float*>(w2.scales) + n1);
+    }
+    warp_allreduce<NT>(a0);
+    warp_allreduce<NT>(a1);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      if (lane == t) a.o[(size_t)hrow[t] * H + n] = ldexpf(a0[t] * r0, sig[t]);
+      if (lane == 16 + t && n + 1 < H) a.o[(size_t)hrow[t] * H + n + 1] = ldexpf(a1[t] * r1, sig[t]);
+    }
+  }
+}
 
 template <int KI>
 __global__ void __launch_bounds__(kFwdThreads, 2) down_kernel(FwdArgs a) {
@@ -689,67 +755,52 @@ __global__ void __launch_bounds__(kFwdThreads, 2) down_kernel(FwdArgs a) {
   int* hrow = reinterpret_cast<int*>(smem_raw + (size_t)kG * I * 4);
   int* sig = hrow + kG;
   const int tiles = (H + kRowsDown - 1) / kRowsDown;
-  const int n_items = n_groups_checked(a) * tiles;
+  const long long n_items = (long long)n_groups_checked(a) * tiles;
+  const long long i0 = n_items * blockIdx.x / gridDim.x, i1 = n_items * (blockIdx.x + 1) / gridDim.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const Group g = a.groups[item / tiles];
-    const int tile = item % tiles;
+  int staged = -1;
+  for (long long item = i0; item < i1; ++item) {
+    const int gi = (int)(item / tiles);
+    const int tile = (int)(item % tiles);
+    const Group g = a.groups[gi];
     if (!group_ok(a, g)) {
       if (threadIdx.x == 0 && a.err) *a.err = MOE_ERR_INVALID;
       continue;
     }
-    if (threadIdx.x < g.count) {
-      const int i = threadIdx.x;
-      const int p = g.pool == MOE_POOL_SHARED ? 0 : a.perm[g.begin + i];
-      hrow[i] = g.pool == MOE_POOL_SHARED ? a.P + g.begin + i : min(max(p, 0), a.P - 1);
-    }
-    __syncthreads();
-    // per-row power-of-two scale of h, then fp16 rows in natural order
-    for (int i = warp; i < g.count; i += kFwdThreads / 32) {
-      const float* src = a.h + (size_t)hrow[i] * I;
-      float m = 0.f;
-      for (int n = lane; n < I; n += 32) m = fmaxf(m, fabsf(src[n]));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      const int sg = pow2_exponent(m);
-      if (lane == 0) sig[i] = sg;
-      for (int n = lane; n < I; n += 32) hh[(size_t)i * I + n] = __float2half_rn(ldexpf(src[n], -sg));
-    }
-    __syncthreads();
-    stage_rows(g.pool, I, g.count, [&](int i) { return (const __half*)(hh + (size_t)i * I); }, xs);
-    __syncthreads();
-    const uint8_t* ex = expert_base(a, g.pool, g.slot);
-    const MatView w2 = mat_view(g.pool, ex, H, I, 2);
-    for (int r = 2 * warp; r < kRowsDown; r += 2 * (kFwdThreads / 32)) {
-      const int n = tile * kRowsDown + r;
-      if (n >= H) break;
-      const int n1 = min(n + 1, H - 1);
-      float a0[kG], a1[kG];
-#pragma unroll
-      for (int t = 0; t < kG; ++t) a0[t] = a1[t] = 0.f;
-      float r0 = 1.f, r1 = 1.f;
-      if (g.pool == MOE_POOL_FP4) {
-        rows_fp4<KI>(w2.codes + (size_t)n * (I / 2), w2.scales + (size_t)n * (I / 32),
-                     w2.codes + (size_t)n1 * (I / 2), w2.scales + (size_t)n1 * (I / 32), I, xs, g.count, a0, a1);
-      } else if (g.pool == MOE_POOL_INT2) {
-        rows_int2<KI>(w2.codes + (size_t)n * (I / 4), w2.scales + (size_t)n * (I / 32),
-                      w2.codes + (size_t)n1 * (I / 4), w2.scales + (size_t)n1 * (I / 32), I, xs, g.count, a0, a1);
-      } else {
-        rows_fp8<KI>(w2.codes + (size_t)n * I, w2.codes + (size_t)n1 * I, I, xs, g.count, a0, a1);
-        r0 = __ldg(reinterpret_cast<const float*>(w2.scales) + n);
-        r1 = __ldg(reinterpret_cast<const float*>(w2.scales) + n1);
+    if (gi != staged) {
+      __syncthreads();
+      if (threadIdx.x < g.count) {
+        const int i = threadIdx.x;
+        const int p = g.pool == MOE_POOL_SHARED ? 0 : a.perm[g.begin + i];
+        hrow[i] = g.pool == MOE_POOL_SHARED ? a.P + g.begin + i : min(max(p, 0), a.P - 1);
       }
-      warp_allreduce(a0, g.count);
-      warp_allreduce(a1, g.count);
+      __syncthreads();
+      // per-row power-of-two scale of h, then fp16 rows in natural order
+      for (int i = warp; i < g.count; i += kFwdThreads / 32) {
+        const float* src = a.h + (size_t)hrow[i] * I;
+        float m = 0.f;
+        for (int n = lane; n < I; n += 32) m = fmaxf(m, fabsf(src[n]));
 #pragma unroll
-      for (int t = 0; t < kG; ++t) {
-        if (t < g.count) {
-          if (lane == t) a.o[(size_t)hrow[t] * H + n] = ldexpf(a0[t] * r0, sig[t]);
-          if (lane == 16 + t && n + 1 < H) a.o[(size_t)hrow[t] * H + n + 1] = ldexpf(a1[t] * r1, sig[t]);
-        }
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const int sg = pow2_exponent(m);
+        if (lane == 0) sig[i] = sg;
+        for (int n = lane; n < I; n += 32) hh[(size_t)i * I + n] = __float2half_rn(ldexpf(src[n], -sg));
       }
+      __syncthreads();
+      stage_rows(g.pool, I, g.count, [&](int i) { return (const __half*)(hh + (size_t)i * I); }, xs);
+      __syncthreads();
+      staged = gi;
     }
-    __syncthreads();
+    switch (g.count) {
+      case 1: down_rows<KI, 1>(a, g, tile, xs, hrow, sig, H, I); break;
+      case 2: down_rows<KI, 2>(a, g, tile, xs, hrow, sig, H, I); break;
+      case 3: down_rows<KI, 3>(a, g, tile, xs, hrow, sig, H, I); break;
+      case 4: down_rows<KI, 4>(a, g, tile, xs, hrow, sig, H, I); break;
+      case 5: down_rows<KI, 5>(a, g, tile, xs, hrow, sig, H, I); break;
+      case 6: down_rows<KI, 6>(a, g, tile, xs, hrow, sig, H, I); break;
+      case 7: down_rows<KI, 7>(a, g, tile, xs, hrow, sig, H, I); break;
+      default: down_rows<KI, 8>(a, g, tile, xs, hrow, sig, H, I); break;
+    }
   }
 }
 
@@ -909,7 +960,7 @@ using namespace moe;
 extern "C" size_t moe_expert_forward_workspace(const moe_expert_views* v, int T, int k) {
   if (!v || T < 0 || k < 1) return 0;
   if ((long long)T * k > kMaxPlanPairs) return prefill_workspace(v->H, v->I, T, k, v->fp4_num_slots);
-  return fwd_layout(v->H, v->I, T, k).total;
+  return fwd_layout(v, T, k).total;
 }
 
 extern "C" moe_status moe_expert_forward(const moe_expert_views* v, const uint16_t* x, int T, int k,
@@ -930,7 +981,7 @@ extern "C" moe_status moe_expert_forward(const moe_expert_views* v, const uint16
     return prefill_forward(v, x, T, k, slots, w, y, workspace, workspace_bytes, d_error, stream);
   }
   MOE_ARG(((uintptr_t)workspace & 255) == 0, "workspace must be 256-byte aligned");
-  const FwdLayout L = fwd_layout(v->H, v->I, T, k);
+  const FwdLayout L = fwd_layout(v, T, k);
   MOE_ARG(workspace_bytes >= L.total, "workspace too small: %zu < %zu", workspace_bytes, L.total);
   MOE_ARG(v->fp4_slots || v->int2_slots, "no expert pool");
   FwdArgs a;
@@ -952,6 +1003,7 @@ extern "C" moe_status moe_expert_forward(const moe_expert_views* v, const uint16
   a.w = w;
   a.y = y;
   a.err = d_error;
+  a.routed_gemm = L.gemm && tags == nullptr && d_error != nullptr;
   uint8_t* base = (uint8_t*)workspace;
   a.hdr = (int*)(base + L.hdr);
   a.perm = (int*)(base + L.perm);
@@ -961,6 +1013,16 @@ extern "C" moe_status moe_expert_forward(const moe_expert_views* v, const uint16
   a.h = (float*)(base + L.h);
   a.o = (float*)(base + L.o);
 
+  if (a.routed_gemm) {
+    // FP4 routed pairs on the tensor cores; its bf16 buffers reuse the routed
+    // rows of h and o, which the CUDA-core kernels do not touch in this mode
+    GgBufs gb;
+    gg_carve_index(base + L.gg, T, k, v->fp4_num_slots, &gb);
+    gb.xg = (uint16_t*)a.o;
+    gb.hs = (__nv_bfloat16*)a.h;
+    gb.o = a.o;
+    if ((st = grouped_gemm_fp4(v, x, T, k, slots, gb, d_error, stream)) != MOE_OK) return st;
+  }
   const size_t plan_smem = (size_t)kMaxPlanPairs * 12 + 64 * 4;
   if ((st = set_smem(plan_kernel, plan_smem)) != MOE_OK) return st;
   {
@@ -969,10 +1031,12 @@ extern "C" moe_status moe_expert_forward(const moe_expert_views* v, const uint16
   }
   if ((st = check_launch("plan_kernel")) != MOE_OK) return st;
 
+  const bool gemv = !a.routed_gemm || v->shared != nullptr;
   const long long max_groups = (long long)T * k + (T + kG - 1) / kG + 1;
   const size_t gu_smem = (size_t)kG * v->H * 2 + 2 * kG * 4;
   const long long gu_items = max_groups * ((v->I + kRowsGateUp - 1) / kRowsGateUp);
-  if (v->H == 4096) {
+  if (!gemv) {
+  } else if (v->H == 4096) {
     if ((st = set_smem(gateup_kernel<4096>, gu_smem)) != MOE_OK) return st;
     ProfScope ps(MOE_K_GATEUP, stream);
     gateup_kernel<4096><<<persistent_grid(gateup_kernel<4096>, gu_smem, gu_items), kFwdThreads, gu_smem, stream>>>(a);
@@ -985,7 +1049,8 @@ extern "C" moe_status moe_expert_forward(const moe_expert_views* v, const uint16
 
   const size_t dn_smem = (size_t)kG * v->I * 4 + 2 * kG * 4;
   const long long dn_items = max_groups * ((v->H + kRowsDown - 1) / kRowsDown);
-  if (v->I == 2048) {
+  if (!gemv) {
+  } else if (v->I == 2048) {
     if ((st = set_smem(down_kernel<2048>, dn_smem)) != MOE_OK) return st;
     ProfScope ps(MOE_K_DOWN, stream);
     down_kernel<2048><<<persistent_grid(down_kernel<2048>, dn_smem, dn_items), kFwdThreads, dn_smem, stream>>>(a);
@@ -1038,7 +1103,7 @@ extern "C" moe_status moe_expert_forward_noalloc(const moe_expert_views* v, cons
   if (T == 0) return MOE_OK;
   MOE_ARG((long long)T * k <= kMaxPlanPairs, "T * k = %lld: the allocation-free call takes at most %d pairs",
           (long long)T * k, kMaxPlanPairs);
-  const size_t need = fwd_layout(v->H, v->I, T, k).total;
+  const size_t need = fwd_layout(v, T, k).total;
   MOE_ARG(need <= kNoAllocScratchBytes,
           "this call needs %zu bytes of scratch but the fixed scratch holds %zu; pass fewer tokens per call", need,
           kNoAllocScratchBytes);

@@ -34,75 +34,28 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "grouped_gemm.cuh"
 
 namespace moe {
 
 constexpr int kPfThreads = 384;
 constexpr int kPfStages = 3;      // A/B operand stages
-constexpr int kPfRaw = 8;         // raw FP4 code stages
+constexpr int kPfRaw = 4;         // raw FP4 code stages
+constexpr int kPfMT = 2;          // 128-row weight tiles per CTA (two TMEM accumulators)
 constexpr int kPfNMax = 256;      // rows per item (MMA N)
 constexpr int kPfKStep = 64;      // K elements per stage (128 bytes of bf16: one swizzle row)
 constexpr int kPfBox = 64;        // rows per TMA box of the B operand
 
-struct PfItem {
-  int slot, row0, count, pad;
-};
-
 // shared memory layout (offsets from a 1024-aligned base)
-constexpr int kATile = 128 * 128;                 // 16 KB
+constexpr int kATile = 128 * 128;                 // 16 KB per 128-row tile
+constexpr int kAStage = kPfMT * kATile;           // 32 KB
 constexpr int kBTile = kPfNMax * 128;             // 32 KB
-constexpr int kRawTile = 128 * 32;                // 4 KB
+constexpr int kRawTile = kPfMT * 128 * 32;        // 8 KB of packed codes per stage
 constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kPfStages * kATile;
+constexpr int kOffB = kOffA + kPfStages * kAStage;
 constexpr int kOffRaw = kOffB + kPfStages * kBTile;
-constexpr int kOffScale = kOffRaw + kPfRaw * kRawTile;   // 128 rows x up to 128 scale bytes
-constexpr int kOffBar = kOffScale + 128 * 128;
+constexpr int kOffBar = kOffRaw + kPfRaw * kRawTile;
 constexpr int kPfSmem = kOffBar + 256 + 1024;     // + alignment slack
-
-__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ uint64_t gtimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* b, int count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count));
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
-  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(su32(b)) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
-  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(su32(b)),
-               "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(su32(b)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Waits for the phase of parity `parity` to complete; gives up after 1 s (or
-// when another thread of the grid gave up) and returns false.
-__device__ __noinline__ bool mbar_wait(uint64_t* b, uint32_t parity, int* err) {
-  if (mbar_test(b, parity)) return true;
-  const uint64_t t0 = gtimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_test(b, parity)) return true;
-    if ((it & 255) == 0) {
-      if (gtimer() - t0 > 1000000000ull) {
-        atomicExch(err, MOE_ERR_TIMEOUT);
-        return false;
-      }
-      if (*(volatile int*)err == MOE_ERR_TIMEOUT) return false;
-    }
-  }
-}
 
 __device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
   asm volatile(
@@ -181,6 +134,9 @@ struct PfArgs {
   int mode;           // 0: gate/up + SwiGLU, 1: down
   int K;              // reduction length (H or I)
   int tiles;          // feature tiles per item
+  const uint8_t* sc0; // E8M0 scales of the first matrix (w1 or w2) of slot 0; slot s at + s * B
+  const uint8_t* sc1; // E8M0 scales of w3 (mode 0)
+  size_t B;           // bytes per expert
   const PfItem* items;
   const int* n_items;
   const int* perm;    // sorted position -> pair index (mode 1 epilogue)
@@ -191,7 +147,6 @@ struct PfArgs {
 
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
-                        const __grid_constant__ CUtensorMap mS0, const __grid_constant__ CUtensorMap mS1,
                         const __grid_constant__ CUtensorMap mB, PfArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -200,8 +155,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint64_t* empty = bar + kPfStages;     // [kPfStages]
   uint64_t* rawf = bar + 2 * kPfStages;  // [kPfRaw]
   uint64_t* rawe = rawf + kPfRaw;        // [kPfRaw]
-  uint64_t* sbar = rawe + kPfRaw;
-  uint64_t* done = sbar + 1;
+  uint64_t* done = rawe + kPfRaw;
   uint32_t* tmem_slot = (uint32_t*)(done + 1);
 
   const int item_idx = blockIdx.x / a.tiles;
@@ -224,13 +178,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_init(&rawf[s], 1);
       mbar_init(&rawe[s], 256);
     }
-    mbar_init(sbar, 1);
     mbar_init(done, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 9) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
-                 "r"(256));
+                 "r"(512));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
@@ -238,20 +191,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // feature rows of this tile in the weight matrices
-  const int f0 = a.mode == 0 ? tile * 64 : tile * 128;
+  // first weight row of this CTA: mode 0 -> feature f0 of w1 and of w3 (128
+  // features = 2 tiles of 64 gate/up pairs); mode 1 -> row f0 of w2 (256 rows)
+  const int f0 = a.mode == 0 ? tile * 128 : tile * 256;
 
   if (warp == 8) {
     if (lane == 0) {
-      // scales of the whole tile, once
-      if (a.mode == 0) {
-        mbar_expect_tx(sbar, 2 * 64 * sbytes);
-        tma_3d(sm + kOffScale, &mS0, 0, f0, it.slot, sbar);
-        tma_3d(sm + kOffScale + 64 * sbytes, &mS1, 0, f0, it.slot, sbar);
-      } else {
-        mbar_expect_tx(sbar, 128 * sbytes);
-        tma_3d(sm + kOffScale, &mS0, 0, f0, it.slot, sbar);
-      }
       int raw_issued = 0;
       bool ok = true;
       for (int ks = 0; ks < nk && ok; ++ks) {
@@ -264,7 +209,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           mbar_expect_tx(&rawf[rs], kRawTile);
           if (a.mode == 0) {
             tma_3d(dst, &mA0, raw_issued * 32, f0, it.slot, &rawf[rs]);
-            tma_3d(dst + 64 * 32, &mA1, raw_issued * 32, f0, it.slot, &rawf[rs]);
+            tma_3d(dst + 128 * 32, &mA1, raw_issued * 32, f0, it.slot, &rawf[rs]);
           } else {
             tma_3d(dst, &mA0, raw_issued * 32, f0, it.slot, &rawf[rs]);
           }
@@ -288,43 +233,80 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         ok = mbar_wait(&full[s], r & 1, a.err);
         if (!ok) break;
         tc_fence_after();
-        const uint64_t ad = umma_desc_sw128(su32(sm + kOffA + s * kATile));
         const uint64_t bd = umma_desc_sw128(su32(sm + kOffB + s * kBTile));
 #pragma unroll
-        for (int kk = 0; kk < kPfKStep / 16; ++kk)
-          mma_bf16(tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (ks | kk) != 0);
+        for (int mt = 0; mt < kPfMT; ++mt) {
+          const uint64_t ad = umma_desc_sw128(su32(sm + kOffA + s * kAStage + mt * kATile));
+#pragma unroll
+          for (int kk = 0; kk < kPfKStep / 16; ++kk)
+            mma_bf16(tmem + (uint32_t)(mt * 256), ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
+                     (ks | kk) != 0);
+        }
         mma_commit(&empty[s]);
       }
       mma_commit(done);  // fires when every issued MMA has completed
     }
   } else if (warp < 8) {
-    // converters: thread -> (row r, 32-weight half c) of the 128 x 64 A tile
+    // converters: thread -> (row r, 32-weight half c) of each 128 x 64 A tile
     const int t = threadIdx.x;
     const int r = t >> 1, c = t & 1;
     const int g = r & 1, i = r >> 1;  // mode 0: gate/up interleaved rows
-    const int raw_off = a.mode == 0 ? (g * 64 + i) * 32 + c * 16 : r * 32 + c * 16;
-    const uint8_t* srow = sm + kOffScale + (a.mode == 0 ? (g * 64 + i) : r) * sbytes;
-    bool ok = mbar_wait(sbar, 0, a.err);
+    int raw_off[kPfMT];
+    const uint8_t* srow[kPfMT];
+#pragma unroll
+    for (int mt = 0; mt < kPfMT; ++mt) {
+      if (a.mode == 0) {
+        raw_off[mt] = g * (128 * 32) + (64 * mt + i) * 32 + c * 16;
+        srow[mt] = (g ? a.sc1 : a.sc0) + (size_t)it.slot * a.B + (size_t)(f0 + 64 * mt + i) * sbytes;
+      } else {
+        raw_off[mt] = (128 * mt + r) * 32 + c * 16;
+        srow[mt] = a.sc0 + (size_t)it.slot * a.B + (size_t)(f0 + 128 * mt + r) * sbytes;
+      }
+    }
+    // scale bytes: 16 at a time (8 k-steps), loaded one group ahead
+    uint4 scur[kPfMT], snext[kPfMT];
+#pragma unroll
+    for (int mt = 0; mt < kPfMT; ++mt) {
+      scur[mt] = __ldg(reinterpret_cast<const uint4*>(srow[mt]));
+      snext[mt] = sbytes > 16 ? __ldg(reinterpret_cast<const uint4*>(srow[mt] + 16)) : scur[mt];
+    }
+    bool ok = true;
     for (int ks = 0; ks < nk && ok; ++ks) {
       const int rs = ks % kPfRaw, rr = ks / kPfRaw;
       const int s = ks % kPfStages, rnd = ks / kPfStages;
+      if ((ks & 7) == 0 && ks > 0) {
+#pragma unroll
+        for (int mt = 0; mt < kPfMT; ++mt) {
+          scur[mt] = snext[mt];
+          const int nxt = (ks / 8 + 1) * 16;
+          if (nxt < sbytes) snext[mt] = __ldg(reinterpret_cast<const uint4*>(srow[mt] + nxt));
+        }
+      }
       if (!(ok = mbar_wait(&rawf[rs], rr & 1, a.err))) break;
-      const uint4 q = *reinterpret_cast<const uint4*>(sm + kOffRaw + rs * kRawTile + raw_off);
-      const uint32_t sc2 = e8m0_bf16x2(srow[ks * 2 + c]);
+      uint4 q[kPfMT];
+#pragma unroll
+      for (int mt = 0; mt < kPfMT; ++mt)
+        q[mt] = *reinterpret_cast<const uint4*>(sm + kOffRaw + rs * kRawTile + raw_off[mt]);
       mbar_arrive(&rawe[rs]);
       if (rnd > 0 && !(ok = mbar_wait(&empty[s], (rnd - 1) & 1, a.err))) break;
-      uint8_t* arow = sm + kOffA + s * kATile + r * 128;
-      const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+      const int sb = (ks & 7) * 2 + c;  // scale byte within the 16 loaded
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint32_t wv = w4[u];
-        uint4 o;
-        o.x = fp4x2_to_bf16x2(wv & 0xff, sc2);
-        o.y = fp4x2_to_bf16x2((wv >> 8) & 0xff, sc2);
-        o.z = fp4x2_to_bf16x2((wv >> 16) & 0xff, sc2);
-        o.w = fp4x2_to_bf16x2(wv >> 24, sc2);
-        const int unit = c * 4 + u;
-        *reinterpret_cast<uint4*>(arow + ((unit ^ (r & 7)) << 4)) = o;
+      for (int mt = 0; mt < kPfMT; ++mt) {
+        const uint32_t sw = sb < 4 ? scur[mt].x : sb < 8 ? scur[mt].y : sb < 12 ? scur[mt].z : scur[mt].w;
+        const uint32_t sc2 = e8m0_bf16x2((sw >> (8 * (sb & 3))) & 0xff);
+        uint8_t* arow = sm + kOffA + s * kAStage + mt * kATile + r * 128;
+        const uint32_t w4[4] = {q[mt].x, q[mt].y, q[mt].z, q[mt].w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t wv = w4[u];
+          uint4 o;
+          o.x = fp4x2_to_bf16x2(wv & 0xff, sc2);
+          o.y = fp4x2_to_bf16x2((wv >> 8) & 0xff, sc2);
+          o.z = fp4x2_to_bf16x2((wv >> 16) & 0xff, sc2);
+          o.w = fp4x2_to_bf16x2(wv >> 24, sc2);
+          const int unit = c * 4 + u;
+          *reinterpret_cast<uint4*>(arow + ((unit ^ (r & 7)) << 4)) = o;
+        }
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(&full[s]);
@@ -341,29 +323,31 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int q = warp - 8;
     const int row = q * 32 + lane;  // D row = A tile row
     if (ok) {
-      for (int c0 = 0; c0 < n_mma; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
-        if (a.mode == 0) {
-          const int feat = f0 + (row >> 1);
+      for (int mt = 0; mt < kPfMT; ++mt) {
+        for (int c0 = 0; c0 < n_mma; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(mt * 256 + c0), v);
+          if (a.mode == 0) {
+            const int feat = f0 + 64 * mt + (row >> 1);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float mine = __uint_as_float(v[j]);
-            const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-            const int col = c0 + j;
-            if ((row & 1) == 0 && col < it.count) {
-              const float hv = mine / (1.f + expf(-mine)) * other;
-              a.hs[(size_t)(it.row0 + col) * a.I + feat] = __float2bfloat16_rn(hv);
+            for (int j = 0; j < 16; ++j) {
+              const float mine = __uint_as_float(v[j]);
+              const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+              const int col = c0 + j;
+              if ((row & 1) == 0 && col < it.count) {
+                const float hv = mine / (1.f + expf(-mine)) * other;
+                a.hs[(size_t)(it.row0 + col) * a.I + feat] = __float2bfloat16_rn(hv);
+              }
             }
-          }
-        } else {
-          const int feat = f0 + row;
+          } else {
+            const int feat = f0 + 128 * mt + row;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = c0 + j;
-            if (col < it.count) {
-              const int p = a.perm[it.row0 + col];
-              a.o[(size_t)p * a.H + feat] = __uint_as_float(v[j]);
+            for (int j = 0; j < 16; ++j) {
+              const int col = c0 + j;
+              if (col < it.count) {
+                const int p = a.perm[it.row0 + col];
+                a.o[(size_t)p * a.H + feat] = __uint_as_float(v[j]);
+              }
             }
           }
         }
@@ -380,7 +364,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   __syncthreads();
   if (warp == 9) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
   }
 }
 
@@ -481,27 +465,123 @@ static moe_status map_bf16_rows(CUtensorMap* m, const void* base, uint64_t cols,
   return MOE_OK;
 }
 
+moe_status group_pairs_multi(const int32_t* ids, int P, int E, int32_t* offsets, int32_t* perm, int32_t* d_error,
+                             int* cnt_ws, cudaStream_t stream);
+size_t group_pairs_multi_ws(int P, int E);
+
 static size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+bool grouped_gemm_supported(const moe_expert_views* v) {
+  return v && v->fp4_slots && v->fp4_num_slots >= 1 && v->fp4_num_slots <= 16384 && v->H % 512 == 0 &&
+         v->I % 512 == 0;
+}
+
+size_t gg_index_bytes(int T, int k, int S) {
+  const size_t P = (size_t)T * k;
+  const size_t max_items = (size_t)S + P / kPfNMax + 1;
+  return a256((S + 1) * 4) + a256(P * 4) + a256(max_items * sizeof(PfItem)) + a256(16) +
+         a256(group_pairs_multi_ws((int)P, S));
+}
+
+void gg_carve_index(uint8_t* base, int T, int k, int S, GgBufs* b) {
+  const size_t P = (size_t)T * k;
+  const size_t max_items = (size_t)S + P / kPfNMax + 1;
+  size_t off = 0;
+  b->offsets = (int*)(base + off);
+  off += a256((S + 1) * 4);
+  b->perm = (int*)(base + off);
+  off += a256(P * 4);
+  b->items = (PfItem*)(base + off);
+  off += a256(max_items * sizeof(PfItem));
+  b->nitems = (int*)(base + off);
+  off += a256(16);
+  b->cnt = (int*)(base + off);
+}
+
+moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T, int k, const int32_t* slots,
+                            const GgBufs& b, int32_t* d_error, cudaStream_t stream) {
+  const int H = v->H, I = v->I, S = v->fp4_num_slots;
+  const size_t P = (size_t)T * k;
+  moe_status st = group_pairs_multi(slots, (int)P, S, b.offsets, b.perm, d_error, b.cnt, stream);
+  if (st != MOE_OK) return st;
+  prefill_items_kernel<<<1, 1024, 0, stream>>>(b.offsets, S, b.items, b.nitems);
+  if ((st = check_launch("prefill_items_kernel")) != MOE_OK) return st;
+  {
+    const int blocks = (int)std::min<size_t>((P * (H / 8) + 255) / 256, 152 * 16);
+    gather_rows_kernel<<<blocks, 256, 0, stream>>>(x, H, k, b.perm, b.offsets, S, b.xg);
+    if ((st = check_launch("gather_rows_kernel")) != MOE_OK) return st;
+  }
+  // weight maps over the whole pool: dims (row bytes, rows, slots)
+  const size_t B = fp4_bytes(H, I);
+  const uint8_t* pool = v->fp4_slots;
+  const size_t hi = (size_t)H * I;
+  const uint8_t* w1c = pool;
+  const uint8_t* w1s = pool + hi / 2;
+  const uint8_t* w3c = pool + (hi / 2 + hi / 32);
+  const uint8_t* w3s = w3c + hi / 2;
+  const uint8_t* w2c = pool + 2 * (hi / 2 + hi / 32);
+  const uint8_t* w2s = w2c + hi / 2;
+  CUtensorMap m1c, m3c, m2c, mx, mh;
+  if ((st = map_bytes3(&m1c, w1c, H / 2, I, S, B, 32, 128)) != MOE_OK) return st;
+  if ((st = map_bytes3(&m3c, w3c, H / 2, I, S, B, 32, 128)) != MOE_OK) return st;
+  if ((st = map_bytes3(&m2c, w2c, I / 2, H, S, B, 32, 256)) != MOE_OK) return st;
+  if ((st = map_bf16_rows(&mx, b.xg, H, P)) != MOE_OK) return st;
+  if ((st = map_bf16_rows(&mh, b.hs, I, P)) != MOE_OK) return st;
+
+  static bool smem_set = false;
+  if (!smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_gemm_kernel)");
+    smem_set = true;
+  }
+  // items: at most one per used slot plus one per 256 further rows
+  const int max_items = (int)std::min<size_t>((size_t)S, P) + (int)(P / kPfNMax) + 1;
+  PfArgs pa;
+  pa.H = H;
+  pa.I = I;
+  pa.k = k;
+  pa.S = S;
+  pa.items = b.items;
+  pa.n_items = b.nitems;
+  pa.perm = b.perm;
+  pa.hs = b.hs;
+  pa.o = b.o;
+  pa.err = d_error;
+  pa.B = B;
+  // GEMM1: gate/up, 128 features (two tiles of 64 gate/up pairs) per CTA
+  pa.mode = 0;
+  pa.K = H;
+  pa.tiles = I / 128;
+  pa.sc0 = w1s;
+  pa.sc1 = w3s;
+  {
+    ProfScope ps(MOE_K_GEMM_GATEUP, stream);
+    prefill_gemm_kernel<<<max_items * pa.tiles, kPfThreads, kPfSmem, stream>>>(m1c, m3c, mx, pa);
+  }
+  if ((st = check_launch("prefill_gemm_kernel (gate/up)")) != MOE_OK) return st;
+  // GEMM2: down, 256 output features (two tiles of 128) per CTA
+  pa.mode = 1;
+  pa.K = I;
+  pa.tiles = H / 256;
+  pa.sc0 = w2s;
+  pa.sc1 = w2s;
+  {
+    ProfScope ps(MOE_K_GEMM_DOWN, stream);
+    prefill_gemm_kernel<<<max_items * pa.tiles, kPfThreads, kPfSmem, stream>>>(m2c, m2c, mh, pa);
+  }
+  return check_launch("prefill_gemm_kernel (down)");
+}
+
 struct PfLayout {
-  size_t offsets, perm, items, nitems, err2, xg, hs, o, total;
+  size_t index, xg, hs, o, total;
 };
 
 static PfLayout pf_layout(int H, int I, int T, int k, int S) {
   const size_t P = (size_t)T * k;
-  const size_t max_items = (size_t)S + P / kPfNMax + 1;
   PfLayout L;
   size_t off = 0;
-  L.offsets = off;
-  off = a256(off + (S + 1) * 4);
-  L.perm = off;
-  off = a256(off + P * 4);
-  L.items = off;
-  off = a256(off + max_items * sizeof(PfItem));
-  L.nitems = off;
-  off = a256(off + 16);
-  L.err2 = off;
-  off = a256(off + 16);
+  L.index = off;
+  off = a256(off + gg_index_bytes(T, k, S));
   L.xg = off;
   off = a256(off + P * H * 2);
   L.hs = off;
@@ -528,84 +608,17 @@ moe_status prefill_forward(const moe_expert_views* v, const uint16_t* x, int T, 
   const PfLayout L = pf_layout(H, I, T, k, S);
   MOE_ARG(ws_bytes >= L.total, "workspace too small: %zu < %zu", ws_bytes, L.total);
   uint8_t* base = (uint8_t*)workspace;
-  int* offsets = (int*)(base + L.offsets);
-  int* perm = (int*)(base + L.perm);
-  PfItem* items = (PfItem*)(base + L.items);
-  int* nitems = (int*)(base + L.nitems);
-  uint16_t* xg = (uint16_t*)(base + L.xg);
-  __nv_bfloat16* hs = (__nv_bfloat16*)(base + L.hs);
-  float* o = (float*)(base + L.o);
-  const size_t P = (size_t)T * k;
-
-  moe_status st = moe_group_pairs(slots, T, k, S, offsets, perm, d_error, stream);
+  GgBufs b;
+  gg_carve_index(base + L.index, T, k, S, &b);
+  b.xg = (uint16_t*)(base + L.xg);
+  b.hs = (__nv_bfloat16*)(base + L.hs);
+  b.o = (float*)(base + L.o);
+  moe_status st = grouped_gemm_fp4(v, x, T, k, slots, b, d_error, stream);
   if (st != MOE_OK) return st;
-  prefill_items_kernel<<<1, 1024, 0, stream>>>(offsets, S, items, nitems);
-  if ((st = check_launch("prefill_items_kernel")) != MOE_OK) return st;
-  {
-    const int blocks = (int)std::min<size_t>((P * (H / 8) + 255) / 256, 152 * 16);
-    gather_rows_kernel<<<blocks, 256, 0, stream>>>(x, H, k, perm, offsets, S, xg);
-    if ((st = check_launch("gather_rows_kernel")) != MOE_OK) return st;
-  }
-  // weight maps over the whole pool: dims (row bytes, rows, slots)
-  const size_t B = fp4_bytes(H, I);
-  const uint8_t* pool = v->fp4_slots;
-  const size_t hi = (size_t)H * I;
-  const uint8_t* w1c = pool;
-  const uint8_t* w1s = pool + hi / 2;
-  const uint8_t* w3c = pool + (hi / 2 + hi / 32);
-  const uint8_t* w3s = w3c + hi / 2;
-  const uint8_t* w2c = pool + 2 * (hi / 2 + hi / 32);
-  const uint8_t* w2s = w2c + hi / 2;
-  CUtensorMap m1c, m3c, m1s, m3s, m2c, m2s, mx, mh;
-  if ((st = map_bytes3(&m1c, w1c, H / 2, I, S, B, 32, 64)) != MOE_OK) return st;
-  if ((st = map_bytes3(&m3c, w3c, H / 2, I, S, B, 32, 64)) != MOE_OK) return st;
-  if ((st = map_bytes3(&m1s, w1s, H / 32, I, S, B, H / 32, 64)) != MOE_OK) return st;
-  if ((st = map_bytes3(&m3s, w3s, H / 32, I, S, B, H / 32, 64)) != MOE_OK) return st;
-  if ((st = map_bytes3(&m2c, w2c, I / 2, H, S, B, 32, 128)) != MOE_OK) return st;
-  if ((st = map_bytes3(&m2s, w2s, I / 32, H, S, B, I / 32, 128)) != MOE_OK) return st;
-  if ((st = map_bf16_rows(&mx, xg, H, P)) != MOE_OK) return st;
-  if ((st = map_bf16_rows(&mh, hs, I, P)) != MOE_OK) return st;
-
-  static bool smem_set = false;
-  if (!smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_gemm_kernel)");
-    smem_set = true;
-  }
-  const int max_items = S + (int)(P / kPfNMax) + 1;
-  PfArgs pa;
-  pa.H = H;
-  pa.I = I;
-  pa.k = k;
-  pa.S = S;
-  pa.items = items;
-  pa.n_items = nitems;
-  pa.perm = perm;
-  pa.hs = hs;
-  pa.o = o;
-  pa.err = d_error;
-  // GEMM1: gate/up, 64 features per tile
-  pa.mode = 0;
-  pa.K = H;
-  pa.tiles = I / 64;
-  {
-    ProfScope ps(MOE_K_GATEUP, stream);
-    prefill_gemm_kernel<<<max_items * pa.tiles, kPfThreads, kPfSmem, stream>>>(m1c, m3c, m1s, m3s, mx, pa);
-  }
-  if ((st = check_launch("prefill_gemm_kernel (gate/up)")) != MOE_OK) return st;
-  // GEMM2: down, 128 features per tile
-  pa.mode = 1;
-  pa.K = I;
-  pa.tiles = H / 128;
-  {
-    ProfScope ps(MOE_K_DOWN, stream);
-    prefill_gemm_kernel<<<max_items * pa.tiles, kPfThreads, kPfSmem, stream>>>(m2c, m2c, m2s, m2s, mh, pa);
-  }
-  if ((st = check_launch("prefill_gemm_kernel (down)")) != MOE_OK) return st;
   {
     ProfScope ps(MOE_K_COMBINE, stream);
     dim3 cg((H + 1023) / 1024, T);
-    prefill_combine_kernel<<<cg, 256, 0, stream>>>(o, slots, w, T, k, H, S, y);
+    prefill_combine_kernel<<<cg, 256, 0, stream>>>(b.o, slots, w, T, k, H, S, y);
   }
   return check_launch("prefill_combine_kernel");
 }

@@ -1,0 +1,34 @@
+// The FP4 grouped GEMM (gate/up with SwiGLU, then down) shared by the prefill
+// entry point and the decode forward.  Implemented in expert_prefill.cu.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+struct PfItem {
+  int slot, row0, count, pad;
+};
+
+// Buffers of one grouped-GEMM call (all device memory, caller-carved).
+struct GgBufs {
+  int* offsets;        // [S + 1]
+  int* perm;           // [P] sorted position -> pair index
+  PfItem* items;       // [S + P / 256 + 1]
+  int* nitems;         // [1]
+  int* cnt;            // grouping scratch
+  uint16_t* xg;        // [P, H] bf16 gathered activations
+  __nv_bfloat16* hs;   // [P, I] bf16 SwiGLU outputs
+  float* o;            // [P, H] fp32 per-pair outputs (row = pair index t*k + j)
+};
+
+bool grouped_gemm_supported(const moe_expert_views* v);
+size_t gg_index_bytes(int T, int k, int S);                   // offsets .. cnt, 256-aligned pieces
+void gg_carve_index(uint8_t* base, int T, int k, int S, GgBufs* b);
+// Writes o rows of every pair with 0 <= slot < S; other rows are untouched.
+moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T, int k, const int32_t* slots,
+                            const GgBufs& b, int32_t* d_error, cudaStream_t stream);
+
+}  // namespace moe

@@ -500,6 +500,95 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
+// Multi-block form of the same stable grouping for large pair counts: each
+// block owns a contiguous segment of kSeg pairs.  (1) per-segment histograms;
+// (2) one block turns them into per-(segment, expert) start positions, ordered
+// expert-major then segment; (3) each segment places its pairs in order, the
+// warps of a tile taking turns, so the order within an expert is pair order.
+constexpr int kSeg = 1024;
+
+__global__ void __launch_bounds__(1024) group_hist_kernel(const int32_t* ids, int P, int E, int* cnt, int32_t* err) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  int* h = (int*)smem_raw;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
+  __syncthreads();
+  const int p0 = blockIdx.x * kSeg, p1 = min(P, p0 + kSeg);
+  for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
+    const int e = ids[p];
+    if (e >= E) atomicExch(err, MOE_ERR_INVALID);
+    else if (e >= 0) atomicAdd(&h[e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[(size_t)blockIdx.x * E + e] = h[e];
+}
+
+__global__ void __launch_bounds__(1024) group_scan_kernel(int nb, int E, int* cnt, int32_t* offsets) {
+  __shared__ int ws[34];
+  const int tid = threadIdx.x, NT = blockDim.x;
+  const int ept = (E + NT - 1) / NT;
+  const int e0 = min(E, tid * ept), e1 = min(E, e0 + ept);
+  int local = 0;
+  for (int e = e0; e < e1; ++e)
+    for (int b = 0; b < nb; ++b) local += cnt[(size_t)b * E + e];
+  int total;
+  int run = block_exclusive_scan(local, ws, &total);
+  for (int e = e0; e < e1; ++e) {
+    offsets[e] = run;
+    for (int b = 0; b < nb; ++b) {
+      const int c = cnt[(size_t)b * E + e];
+      cnt[(size_t)b * E + e] = run;
+      run += c;
+    }
+  }
+  if (tid == 0) offsets[E] = total;
+}
+
+__global__ void __launch_bounds__(1024) group_place_kernel(const int32_t* ids, int P, int E, const int* cnt,
+                                                           int32_t* perm) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  int* off = (int*)smem_raw;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nwarps = blockDim.x >> 5;
+  for (int e = tid; e < E; e += blockDim.x) off[e] = cnt[(size_t)blockIdx.x * E + e];
+  __syncthreads();
+  const int p0 = blockIdx.x * kSeg, p1 = min(P, p0 + kSeg);
+  for (int base = p0; base < p1; base += blockDim.x) {
+    const int p = base + tid;
+    const int e = (p < p1) ? ids[p] : -1;
+    const bool valid = e >= 0 && e < E;
+    const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    for (int w = 0; w < nwarps; ++w) {
+      if (wid == w && valid) {
+        perm[off[e] + rank] = p;
+        __syncwarp(peers);
+        if (rank == 0) off[e] += __popc(peers);
+      }
+      __syncthreads();
+    }
+  }
+}
+
+moe_status group_pairs_multi(const int32_t* ids, int P, int E, int32_t* offsets, int32_t* perm, int32_t* d_error,
+                             int* cnt_ws, cudaStream_t stream) {
+  const int nb = (P + kSeg - 1) / kSeg;
+  const size_t smem = (size_t)E * 4;
+  if (smem > 48 * 1024) {
+    cudaError_t e1 = cudaFuncSetAttribute(group_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e2 = cudaFuncSetAttribute(group_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e1 != cudaSuccess) return cuda_fail(e1, "cudaFuncSetAttribute(group_hist_kernel)");
+    if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFuncSetAttribute(group_place_kernel)");
+  }
+  ProfScope ps(MOE_K_GROUP, stream);
+  cudaError_t e = cudaMemsetAsync(d_error, 0, sizeof(int32_t), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(d_error)");
+  if (nb > 0) group_hist_kernel<<<nb, 1024, smem, stream>>>(ids, P, E, cnt_ws, d_error);
+  group_scan_kernel<<<1, 1024, 0, stream>>>(nb, E, cnt_ws, offsets);
+  if (nb > 0) group_place_kernel<<<nb, 1024, smem, stream>>>(ids, P, E, cnt_ws, perm);
+  return check_launch("group_pairs_multi");
+}
+
+size_t group_pairs_multi_ws(int P, int E) { return (size_t)((P + kSeg - 1) / kSeg) * E * 4; }
+
 static moe_status prepare_smem(const void* kernel, size_t bytes) {
   static_assert(sizeof(int) == 4, "int");
   if (bytes > 48 * 1024) {
