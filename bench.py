@@ -237,7 +237,8 @@ def run_ours(args):
             ids = runner.ids[:T]
             d = int(torch.unique(ids).numel())
             acct_gemm_bytes += d * gu_expert + T * H * 2 + T * k * I * 2
-            acct_gu_bytes += gu_shared + T * H * 2 + T * I * 4 + (0 if T * k >= 64 else
+            # the routed pairs take the grouped GEMM from 256 pairs per call on
+            acct_gu_bytes += gu_shared + T * H * 2 + T * I * 4 + (0 if T * k >= 256 else
                                                                    d * gu_expert + T * k * I * 4)
             acct_layer_bytes += d * Bx + layer_shared + 2 * T * H * 2
         torch.cuda.synchronize()

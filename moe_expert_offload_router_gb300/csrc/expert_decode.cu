@@ -655,8 +655,9 @@ __device__ __forceinline__ void gateup_rows(const FwdArgs& a, const Group& g, in
   }
 }
 
-// Each CTA takes a contiguous range of the (group, tile) items, so the group's
-// activations are staged once for all of the CTA's tiles of that group.
+// Items (group, tile) are taken with a grid stride, so the token groups of one
+// popular expert run at about the same time and its re-read rows hit L2; a
+// group's activations are restaged only when the group changes.
 template <int KH>
 __global__ void __launch_bounds__(kFwdThreads, 2) gateup_kernel(FwdArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -667,9 +668,8 @@ __global__ void __launch_bounds__(kFwdThreads, 2) gateup_kernel(FwdArgs a) {
   const int I = a.I;
   const int tiles = (I + kRowsGateUp - 1) / kRowsGateUp;
   const long long n_items = (long long)n_groups_checked(a) * tiles;
-  const long long i0 = n_items * blockIdx.x / gridDim.x, i1 = n_items * (blockIdx.x + 1) / gridDim.x;
   int staged = -1;
-  for (long long item = i0; item < i1; ++item) {
+  for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int gi = (int)(item / tiles);
     const int tile = (int)(item % tiles);
     const Group g = a.groups[gi];
@@ -756,10 +756,9 @@ __global__ void __launch_bounds__(kFwdThreads, 2) down_kernel(FwdArgs a) {
   int* sig = hrow + kG;
   const int tiles = (H + kRowsDown - 1) / kRowsDown;
   const long long n_items = (long long)n_groups_checked(a) * tiles;
-  const long long i0 = n_items * blockIdx.x / gridDim.x, i1 = n_items * (blockIdx.x + 1) / gridDim.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int staged = -1;
-  for (long long item = i0; item < i1; ++item) {
+  for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int gi = (int)(item / tiles);
     const int tile = (int)(item % tiles);
     const Group g = a.groups[gi];
@@ -1014,11 +1013,13 @@ extern "C" moe_status moe_expert_forward(const moe_expert_views* v, const uint16
   a.o = (float*)(base + L.o);
 
   if (a.routed_gemm) {
-    // FP4 routed pairs on the tensor cores; its bf16 buffers reuse the routed
-    // rows of h and o, which the CUDA-core kernels do not touch in this mode
+    // FP4 routed pairs on the tensor cores; its 16-bit buffers (two activation
+    // copies of P x H each, h of P x I) reuse the routed rows of the fp32 o and
+    // h buffers, which the CUDA-core kernels do not touch in this mode
     GgBufs gb;
     gg_carve_index(base + L.gg, T, k, v->fp4_num_slots, &gb);
     gb.xg = (uint16_t*)a.o;
+    gb.xg16 = (__half*)((uint8_t*)a.o + (size_t)T * k * v->H * 2);
     gb.hs = (__nv_bfloat16*)a.h;
     gb.o = a.o;
     if ((st = grouped_gemm_fp4(v, x, T, k, slots, gb, d_error, stream)) != MOE_OK) return st;

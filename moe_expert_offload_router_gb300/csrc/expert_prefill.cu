@@ -17,9 +17,10 @@
 //             epilogue o[pair][feature] in fp32
 //   combine   y_t = sum_j w_tj o_tj in rank order -> bf16
 //
-// GEMM CTA (384 threads): warp 8 lane 0 issues TMA loads (raw FP4 codes of the
-// A tile into an 8-deep staging ring; the B tile straight into its 128-byte
-// swizzled K-major layout); warps 0-7 decode the raw codes to bf16 with the
+// GEMM CTA (384 threads): warp 8 lane 0 streams the raw FP4 codes of the A
+// tiles by TMA into a staging ring, as far ahead as the ring allows; warp 10
+// lane 0 loads the B tile by TMA straight into its 128-byte swizzled K-major
+// layout, one stage per free operand slot; warps 0-7 decode the raw codes to bf16 with the
 // E8M0 scale folded in (exact: E2M1 x 2^(e-127) fits bf16 for all scales) and
 // store them in the same swizzled layout; warp 9 lane 0 issues
 // tcgen05.mma.kind::f16 (M = 128, N = rows of the item rounded to 16, K = 16
@@ -83,9 +84,11 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
   return d;
 }
 
-// kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major, M = 128.
-__device__ __forceinline__ uint32_t idesc_bf16(int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+// kind::f16 instruction descriptor: D fp32, A and B both bf16 (or both fp16),
+// both K-major, M = 128.
+__device__ __forceinline__ uint32_t idesc_16bit(int n, bool bf16) {
+  const uint32_t t = bf16 ? 1u : 0u;
+  return (1u << 4) | (t << 7) | (t << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -124,6 +127,24 @@ __device__ __forceinline__ uint32_t fp4x2_to_bf16x2(uint32_t byte, uint32_t scal
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Two E2M1 codes -> fp16x2 times the block scale 2^(e-127) given as fp16x2;
+// exact when e is within [kF16ScaleLo, kF16ScaleHi].
+__device__ __forceinline__ uint32_t fp4x2_to_f16x2(uint32_t byte, uint32_t scale2) {
+  uint32_t h;
+  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(h) : "r"(byte));
+  __half2 v = __hmul2(*reinterpret_cast<__half2*>(&h), *reinterpret_cast<const __half2*>(&scale2));
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// E8M0 range for which E2M1 x 2^(e-127) is a normal fp16 (or zero) with an
+// fp16-normal scale: 2^-12 <= 0.5 * 2^(e-127) and 6 * 2^(e-127) <= 49152.
+constexpr uint32_t kF16ScaleLo = 115, kF16ScaleHi = 140;
+
+__device__ __forceinline__ uint32_t e8m0_f16x2(uint32_t e) {
+  const uint32_t h = (e - 127 + 15) << 10;  // 2^(e-127) as fp16 (normal within the range above)
+  return h | (h << 16);
+}
+
 __device__ __forceinline__ uint32_t e8m0_bf16x2(uint32_t e) {
   const uint32_t b = e ? (e << 7) : 0x0040u;  // 2^(e-127) in bf16 (e = 0 is the subnormal 2^-127)
   return b | (b << 16);
@@ -134,6 +155,8 @@ struct PfArgs {
   int mode;           // 0: gate/up + SwiGLU, 1: down
   int K;              // reduction length (H or I)
   int tiles;          // feature tiles per item
+  const int* xsig;    // mode 0: power-of-two exponent of each sorted row of the fp16 activation copy
+  int allow_f16;      // mode 0: tiles whose scales all lie in the fp16 range run as fp16 MMAs
   const uint8_t* sc0; // E8M0 scales of the first matrix (w1 or w2) of slot 0; slot s at + s * B
   const uint8_t* sc1; // E8M0 scales of w3 (mode 0)
   size_t B;           // bytes per expert
@@ -147,7 +170,8 @@ struct PfArgs {
 
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
-                        const __grid_constant__ CUtensorMap mB, PfArgs a) {
+                        const __grid_constant__ CUtensorMap mB, const __grid_constant__ CUtensorMap mB16,
+                        PfArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bar = (uint64_t*)(sm + kOffBar);
@@ -157,6 +181,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint64_t* rawe = rawf + kPfRaw;        // [kPfRaw]
   uint64_t* done = rawe + kPfRaw;
   uint32_t* tmem_slot = (uint32_t*)(done + 1);
+  int* f16_flag = (int*)(tmem_slot + 1);
 
   const int item_idx = blockIdx.x / a.tiles;
   const int tile = blockIdx.x % a.tiles;
@@ -195,38 +220,78 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   // features = 2 tiles of 64 gate/up pairs); mode 1 -> row f0 of w2 (256 rows)
   const int f0 = a.mode == 0 ? tile * 128 : tile * 256;
 
+  // fp16 or bf16 operands for this tile: fp16 when every block scale of the
+  // tile keeps the scaled E2M1 values exact in fp16 (gate/up only)
+  if (threadIdx.x == 0) *f16_flag = (a.mode == 0 && a.allow_f16) ? 1 : 0;
+  __syncthreads();
+  if (a.mode == 0 && a.allow_f16 && warp < 8) {
+    const int r = threadIdx.x >> 1, c = threadIdx.x & 1;
+    const int g = r & 1, i = r >> 1;
+    bool in_range = true;
+    for (int mt = 0; mt < kPfMT; ++mt) {
+      const uint8_t* row = (g ? a.sc1 : a.sc0) + (size_t)it.slot * a.B + (size_t)(f0 + 64 * mt + i) * sbytes;
+      for (int off = c * 16; off < sbytes; off += 32) {
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(row + off));
+        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const uint32_t e = (w4[u] >> (8 * b)) & 0xff;
+            in_range = in_range && e >= kF16ScaleLo && e <= kF16ScaleHi;
+          }
+      }
+    }
+    if (!in_range) atomicAnd(f16_flag, 0);
+  }
+  __syncthreads();
+  const bool f16 = *f16_flag != 0;
+
   if (warp == 8) {
+    // weight codes: as far ahead as the raw ring allows, independent of MMA progress
     if (lane == 0) {
-      int raw_issued = 0;
+      bool ok = true;
+      for (int rk = 0; rk < nk && ok; ++rk) {
+        const int rs = rk % kPfRaw, rr = rk / kPfRaw;
+        if (rr > 0) ok = mbar_wait(&rawe[rs], (rr - 1) & 1, a.err);
+        if (!ok) break;
+        uint8_t* dst = sm + kOffRaw + rs * kRawTile;
+        mbar_expect_tx(&rawf[rs], kRawTile);
+        if (a.mode == 0) {
+          tma_3d(dst, &mA0, rk * 32, f0, it.slot, &rawf[rs]);
+          tma_3d(dst + 128 * 32, &mA1, rk * 32, f0, it.slot, &rawf[rs]);
+        } else {
+          tma_3d(dst, &mA0, rk * 32, f0, it.slot, &rawf[rs]);
+        }
+      }
+      if (!ok) {  // let copies already issued land before the CTA can exit
+        const uint64_t t0 = gtimer();
+        while (gtimer() - t0 < 2000000ull) {
+        }
+      }
+    }
+  } else if (warp == 10) {
+    // activation tiles: one stage per free operand slot
+    if (lane == 0) {
       bool ok = true;
       for (int ks = 0; ks < nk && ok; ++ks) {
-        const int ahead = min(nk, ks + kPfRaw);
-        for (; raw_issued < ahead && ok; ++raw_issued) {
-          const int rs = raw_issued % kPfRaw, rr = raw_issued / kPfRaw;
-          if (rr > 0) ok = mbar_wait(&rawe[rs], (rr - 1) & 1, a.err);
-          if (!ok) break;
-          uint8_t* dst = sm + kOffRaw + rs * kRawTile;
-          mbar_expect_tx(&rawf[rs], kRawTile);
-          if (a.mode == 0) {
-            tma_3d(dst, &mA0, raw_issued * 32, f0, it.slot, &rawf[rs]);
-            tma_3d(dst + 128 * 32, &mA1, raw_issued * 32, f0, it.slot, &rawf[rs]);
-          } else {
-            tma_3d(dst, &mA0, raw_issued * 32, f0, it.slot, &rawf[rs]);
-          }
-        }
-        if (!ok) break;
         const int s = ks % kPfStages, r = ks / kPfStages;
         if (r > 0) ok = mbar_wait(&empty[s], (r - 1) & 1, a.err);
         if (!ok) break;
         uint8_t* bdst = sm + kOffB + s * kBTile;
         mbar_expect_tx(&full[s], b_bytes);
         for (int bx = 0; bx < n_box; ++bx)
-          tma_2d(bdst + bx * kPfBox * 128, &mB, ks * kPfKStep, it.row0 + bx * kPfBox, &full[s]);
+          tma_2d(bdst + bx * kPfBox * 128, f16 ? &mB16 : &mB, ks * kPfKStep, it.row0 + bx * kPfBox, &full[s]);
+      }
+      if (!ok) {
+        const uint64_t t0 = gtimer();
+        while (gtimer() - t0 < 2000000ull) {
+        }
       }
     }
   } else if (warp == 9) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(n_mma);
+      const uint32_t idesc = idesc_16bit(n_mma, !f16);
       bool ok = true;
       for (int ks = 0; ks < nk && ok; ++ks) {
         const int s = ks % kPfStages, r = ks / kPfStages;
@@ -293,17 +358,25 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
       for (int mt = 0; mt < kPfMT; ++mt) {
         const uint32_t sw = sb < 4 ? scur[mt].x : sb < 8 ? scur[mt].y : sb < 12 ? scur[mt].z : scur[mt].w;
-        const uint32_t sc2 = e8m0_bf16x2((sw >> (8 * (sb & 3))) & 0xff);
+        const uint32_t e8 = (sw >> (8 * (sb & 3))) & 0xff;
+        const uint32_t sc2 = f16 ? e8m0_f16x2(e8) : e8m0_bf16x2(e8);
         uint8_t* arow = sm + kOffA + s * kAStage + mt * kATile + r * 128;
         const uint32_t w4[4] = {q[mt].x, q[mt].y, q[mt].z, q[mt].w};
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const uint32_t wv = w4[u];
           uint4 o;
-          o.x = fp4x2_to_bf16x2(wv & 0xff, sc2);
-          o.y = fp4x2_to_bf16x2((wv >> 8) & 0xff, sc2);
-          o.z = fp4x2_to_bf16x2((wv >> 16) & 0xff, sc2);
-          o.w = fp4x2_to_bf16x2(wv >> 24, sc2);
+          if (f16) {
+            o.x = fp4x2_to_f16x2(wv & 0xff, sc2);
+            o.y = fp4x2_to_f16x2((wv >> 8) & 0xff, sc2);
+            o.z = fp4x2_to_f16x2((wv >> 16) & 0xff, sc2);
+            o.w = fp4x2_to_f16x2(wv >> 24, sc2);
+          } else {
+            o.x = fp4x2_to_bf16x2(wv & 0xff, sc2);
+            o.y = fp4x2_to_bf16x2((wv >> 8) & 0xff, sc2);
+            o.z = fp4x2_to_bf16x2((wv >> 16) & 0xff, sc2);
+            o.w = fp4x2_to_bf16x2(wv >> 24, sc2);
+          }
           const int unit = c * 4 + u;
           *reinterpret_cast<uint4*>(arow + ((unit ^ (r & 7)) << 4)) = o;
         }
@@ -331,9 +404,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const int feat = f0 + 64 * mt + (row >> 1);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const float mine = __uint_as_float(v[j]);
-              const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
               const int col = c0 + j;
+              const int sg = (f16 && col < it.count) ? a.xsig[it.row0 + col] : 0;
+              const float mine = ldexpf(__uint_as_float(v[j]), sg);
+              const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
               if ((row & 1) == 0 && col < it.count) {
                 const float hv = mine / (1.f + expf(-mine)) * other;
                 a.hs[(size_t)(it.row0 + col) * a.I + feat] = __float2bfloat16_rn(hv);
@@ -352,12 +426,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
         }
       }
-    }
-  }
-  // on a timeout, give copies still in flight time to land before the CTA exits
-  if (threadIdx.x == 8 * 32 && *(volatile int*)a.err == MOE_ERR_TIMEOUT) {
-    const uint64_t t0 = gtimer();
-    while (gtimer() - t0 < 2000000ull) {
     }
   }
   tc_fence_before();
@@ -392,15 +460,47 @@ __global__ void prefill_items_kernel(const int* offsets, int S, PfItem* items, i
   if (tid == 0) *n_items = total;
 }
 
+// One warp per sorted row: copy the token's bf16 row, and an fp16 copy scaled
+// by the power of two that brings its largest magnitude into [1, 2).
 __global__ void gather_rows_kernel(const uint16_t* x, int H, int k, const int* perm, const int* offsets, int S,
-                                   uint16_t* xg) {
+                                   uint16_t* xg, __half* xg16, int* xsig) {
   const int n = offsets[S];
+  const int lane = threadIdx.x & 31;
   const int units = H / 8;
-  for (size_t u = (size_t)blockIdx.x * blockDim.x + threadIdx.x; u < (size_t)n * units;
-       u += (size_t)gridDim.x * blockDim.x) {
-    const int i = (int)(u / units), c = (int)(u % units);
+  for (int i = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5); i < n;
+       i += (int)((gridDim.x * (size_t)blockDim.x) >> 5)) {
     const int tok = perm[i] / k;
-    reinterpret_cast<uint4*>(xg + (size_t)i * H)[c] = reinterpret_cast<const uint4*>(x + (size_t)tok * H)[c];
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)tok * H);
+    uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)i * H);
+    float m = 0.f;
+    for (int c = lane; c < units; c += 32) {
+      const uint4 v = src[c];
+      dst[c] = v;
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[q] << 16)), fabsf(__uint_as_float(w4[q] & 0xffff0000u))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    int sg = 0;
+    if (m > 0.f) {
+      int e;
+      frexpf(m, &e);
+      sg = e - 1;
+    }
+    if (lane == 0) xsig[i] = sg;
+    __half* d16 = xg16 + (size_t)i * H;
+    for (int c = lane; c < units; c += 32) {
+      const uint4 v = src[c];
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+      __half2 hv[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        hv[q] = __floats2half2_rn(ldexpf(__uint_as_float(w4[q] << 16), -sg),
+                                  ldexpf(__uint_as_float(w4[q] & 0xffff0000u), -sg));
+      reinterpret_cast<uint4*>(d16)[c] = *reinterpret_cast<uint4*>(hv);
+    }
   }
 }
 
@@ -450,15 +550,16 @@ static moe_status map_bytes3(CUtensorMap* m, const void* base, uint64_t row_byte
   return MOE_OK;
 }
 
-// rank-2 bf16 map with 128-byte swizzle, box 64 x kPfBox
-static moe_status map_bf16_rows(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+// rank-2 16-bit map (bf16 or fp16) with 128-byte swizzle, box 64 x kPfBox
+static moe_status map_bf16_rows(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                                CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encode_fn();
   if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
   cuuint32_t box[2] = {64, (cuuint32_t)kPfBox};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (activations) failed: %d", (int)r);
@@ -480,7 +581,7 @@ size_t gg_index_bytes(int T, int k, int S) {
   const size_t P = (size_t)T * k;
   const size_t max_items = (size_t)S + P / kPfNMax + 1;
   return a256((S + 1) * 4) + a256(P * 4) + a256(max_items * sizeof(PfItem)) + a256(16) +
-         a256(group_pairs_multi_ws((int)P, S));
+         a256(group_pairs_multi_ws((int)P, S)) + a256(P * 4);
 }
 
 void gg_carve_index(uint8_t* base, int T, int k, int S, GgBufs* b) {
@@ -496,6 +597,8 @@ void gg_carve_index(uint8_t* base, int T, int k, int S, GgBufs* b) {
   b->nitems = (int*)(base + off);
   off += a256(16);
   b->cnt = (int*)(base + off);
+  off += a256(group_pairs_multi_ws((int)P, S));
+  b->xsig = (int*)(base + off);
 }
 
 moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T, int k, const int32_t* slots,
@@ -507,8 +610,8 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
   prefill_items_kernel<<<1, 1024, 0, stream>>>(b.offsets, S, b.items, b.nitems);
   if ((st = check_launch("prefill_items_kernel")) != MOE_OK) return st;
   {
-    const int blocks = (int)std::min<size_t>((P * (H / 8) + 255) / 256, 152 * 16);
-    gather_rows_kernel<<<blocks, 256, 0, stream>>>(x, H, k, b.perm, b.offsets, S, b.xg);
+    const int blocks = (int)std::min<size_t>((P + 7) / 8, 152 * 16);
+    gather_rows_kernel<<<blocks, 256, 0, stream>>>(x, H, k, b.perm, b.offsets, S, b.xg, b.xg16, b.xsig);
     if ((st = check_launch("gather_rows_kernel")) != MOE_OK) return st;
   }
   // weight maps over the whole pool: dims (row bytes, rows, slots)
@@ -521,11 +624,12 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
   const uint8_t* w3s = w3c + hi / 2;
   const uint8_t* w2c = pool + 2 * (hi / 2 + hi / 32);
   const uint8_t* w2s = w2c + hi / 2;
-  CUtensorMap m1c, m3c, m2c, mx, mh;
+  CUtensorMap m1c, m3c, m2c, mx, mx16, mh;
   if ((st = map_bytes3(&m1c, w1c, H / 2, I, S, B, 32, 128)) != MOE_OK) return st;
   if ((st = map_bytes3(&m3c, w3c, H / 2, I, S, B, 32, 128)) != MOE_OK) return st;
   if ((st = map_bytes3(&m2c, w2c, I / 2, H, S, B, 32, 256)) != MOE_OK) return st;
   if ((st = map_bf16_rows(&mx, b.xg, H, P)) != MOE_OK) return st;
+  if ((st = map_bf16_rows(&mx16, b.xg16, H, P, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != MOE_OK) return st;
   if ((st = map_bf16_rows(&mh, b.hs, I, P)) != MOE_OK) return st;
 
   static bool smem_set = false;
@@ -548,15 +652,17 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
   pa.o = b.o;
   pa.err = d_error;
   pa.B = B;
+  pa.xsig = b.xsig;
   // GEMM1: gate/up, 128 features (two tiles of 64 gate/up pairs) per CTA
   pa.mode = 0;
   pa.K = H;
   pa.tiles = I / 128;
   pa.sc0 = w1s;
   pa.sc1 = w3s;
+  pa.allow_f16 = 1;
   {
     ProfScope ps(MOE_K_GEMM_GATEUP, stream);
-    prefill_gemm_kernel<<<max_items * pa.tiles, kPfThreads, kPfSmem, stream>>>(m1c, m3c, mx, pa);
+    prefill_gemm_kernel<<<max_items * pa.tiles, kPfThreads, kPfSmem, stream>>>(m1c, m3c, mx, mx16, pa);
   }
   if ((st = check_launch("prefill_gemm_kernel (gate/up)")) != MOE_OK) return st;
   // GEMM2: down, 256 output features (two tiles of 128) per CTA
@@ -565,15 +671,16 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
   pa.tiles = H / 256;
   pa.sc0 = w2s;
   pa.sc1 = w2s;
+  pa.allow_f16 = 0;
   {
     ProfScope ps(MOE_K_GEMM_DOWN, stream);
-    prefill_gemm_kernel<<<max_items * pa.tiles, kPfThreads, kPfSmem, stream>>>(m2c, m2c, mh, pa);
+    prefill_gemm_kernel<<<max_items * pa.tiles, kPfThreads, kPfSmem, stream>>>(m2c, m2c, mh, mh, pa);
   }
   return check_launch("prefill_gemm_kernel (down)");
 }
 
 struct PfLayout {
-  size_t index, xg, hs, o, total;
+  size_t index, xg, xg16, hs, o, total;
 };
 
 static PfLayout pf_layout(int H, int I, int T, int k, int S) {
@@ -583,6 +690,8 @@ static PfLayout pf_layout(int H, int I, int T, int k, int S) {
   L.index = off;
   off = a256(off + gg_index_bytes(T, k, S));
   L.xg = off;
+  off = a256(off + P * H * 2);
+  L.xg16 = off;
   off = a256(off + P * H * 2);
   L.hs = off;
   off = a256(off + P * I * 2);
@@ -611,6 +720,7 @@ moe_status prefill_forward(const moe_expert_views* v, const uint16_t* x, int T, 
   GgBufs b;
   gg_carve_index(base + L.index, T, k, S, &b);
   b.xg = (uint16_t*)(base + L.xg);
+  b.xg16 = (__half*)(base + L.xg16);
   b.hs = (__nv_bfloat16*)(base + L.hs);
   b.o = (float*)(base + L.o);
   moe_status st = grouped_gemm_fp4(v, x, T, k, slots, b, d_error, stream);

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 
@@ -20,6 +21,8 @@ struct GgBufs {
   int* nitems;         // [1]
   int* cnt;            // grouping scratch
   uint16_t* xg;        // [P, H] bf16 gathered activations
+  __half* xg16;        // [P, H] fp16 copy, each row scaled by 2^-xsig[row]
+  int* xsig;           // [P]
   __nv_bfloat16* hs;   // [P, I] bf16 SwiGLU outputs
   float* o;            // [P, H] fp32 per-pair outputs (row = pair index t*k + j)
 };
