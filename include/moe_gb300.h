@@ -305,6 +305,12 @@ enum {
 moe_status moe_profile_enable(int enable);
 moe_status moe_profile_query(int kernel, double* total_ms, int* launches);
 
+/* Test hook for failure detection without a fault: launches one thread that
+ * waits on an mbarrier nothing arrives on, with the library's bounded wait and
+ * a limit of limit_ns (at most 2 s); *d_status (device int32) becomes
+ * MOE_ERR_TIMEOUT when the wait gives up.  The context stays usable. */
+moe_status moe_debug_timeout_probe(int64_t limit_ns, int32_t* d_status, cudaStream_t stream);
+
 /* Runs a tiny router + cache + copy round trip on the current device and
  * checks it (synchronous).  MOE_OK means the library executes here. */
 moe_status moe_selftest(void);

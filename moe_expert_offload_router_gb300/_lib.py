@@ -72,6 +72,7 @@ _SIGS = {
     "moe_expert_prefill": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, sz, vp, vp]),
     "moe_rms_carry": (i32, [vp, i32, i32, f32, vp, vp]),
     "moe_selftest": (i32, []),
+    "moe_debug_timeout_probe": (i32, [C.c_int64, vp, vp]),
     "moe_profile_enable": (i32, [i32]),
     "moe_profile_query": (i32, [i32, C.POINTER(C.c_double), C.POINTER(C.c_int)]),
 }
@@ -278,6 +279,10 @@ def moe_dequant_debug(views: moe_expert_views, pool: int, slot: int, matrix: int
 def moe_rms_carry(y, eps: float, x_next, stream=None):
     T, H = y.shape
     _check(_lib.moe_rms_carry(_p(y), T, H, eps, _p(x_next), _s(stream)))
+
+
+def moe_debug_timeout_probe(limit_ns: int, d_status, stream=None):
+    _check(_lib.moe_debug_timeout_probe(limit_ns, _p(d_status), _s(stream)))
 
 
 def moe_selftest():

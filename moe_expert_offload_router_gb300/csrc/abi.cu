@@ -103,6 +103,20 @@ __global__ void cache_mark_empty_kernel(CacheDev c, int slot) {
   c.slot_key[slot] = -1;
 }
 
+// One thread waits on an mbarrier that nothing arrives on; the bounded wait
+// gives up after limit_ns and reports MOE_ERR_TIMEOUT (the same wait every
+// pipelined kernel of this library uses).
+__global__ void timeout_probe_kernel(uint64_t limit_ns, int32_t* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    *status = 0;
+    const bool ok = mbar_wait(&bar, 0, status, limit_ns);
+    if (ok) *status = -1;  // cannot happen: nothing arrives
+  }
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -324,6 +338,14 @@ moe_status moe_profile_query(int kernel, double* total_ms, int* launches) {
   *total_ms = t;
   *launches = n;
   return MOE_OK;
+}
+
+moe_status moe_debug_timeout_probe(int64_t limit_ns, int32_t* d_status, cudaStream_t stream) {
+  clear_error();
+  MOE_ARG(d_status != nullptr, "d_status is null");
+  MOE_ARG(limit_ns > 0 && limit_ns <= 2000000000LL, "limit_ns must be in (0, 2e9]");
+  timeout_probe_kernel<<<1, 32, 0, stream>>>((uint64_t)limit_ns, d_status);
+  return check_launch("timeout_probe_kernel");
 }
 
 moe_status moe_selftest(void) {

@@ -153,15 +153,17 @@ __device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Waits for the phase of parity `parity` to complete; gives up after 1 s (or
-// when another thread of the grid gave up) and returns false.
-static __device__ __noinline__ bool mbar_wait(uint64_t* b, uint32_t parity, int* err) {
+// Waits for the phase of parity `parity` to complete; gives up after
+// limit_ns (1 s by default) or when another thread of the grid gave up, and
+// then records MOE_ERR_TIMEOUT in *err and returns false.
+static __device__ __noinline__ bool mbar_wait(uint64_t* b, uint32_t parity, int* err,
+                                              uint64_t limit_ns = 1000000000ull) {
   if (mbar_test(b, parity)) return true;
   const uint64_t t0 = gtimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_test(b, parity)) return true;
     if ((it & 255) == 0) {
-      if (gtimer() - t0 > 1000000000ull) {
+      if (gtimer() - t0 > limit_ns) {
         atomicExch(err, MOE_ERR_TIMEOUT);
         return false;
       }

@@ -615,6 +615,41 @@ __device__ __forceinline__ const uint8_t* expert_base(const FwdArgs& a, int pool
   return a.shared;
 }
 
+
+// ------------------------------------------------- two-deep row pipelining --
+// For FP4 groups of one or two tokens the per-row compute is short, so a warp
+// loads the codes of its next row pair before it computes the current one:
+// twice the bytes in flight per warp.
+template <int CPL>
+struct Fp4Rows {
+  uint4 q0[CPL], q1[CPL];
+  uint32_t e0[CPL], e1[CPL];
+};
+
+template <int CPL>
+__device__ __forceinline__ void fp4_load(Fp4Rows<CPL>& b, const uint8_t* c0, const uint8_t* s0, const uint8_t* c1,
+                                         const uint8_t* s1) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const int c = lane + 32 * i;
+    b.q0[i] = ld_stream_v4(c0 + (size_t)c * 16);
+    b.q1[i] = ld_stream_v4(c1 + (size_t)c * 16);
+    b.e0[i] = __ldg(s0 + c);
+    b.e1[i] = __ldg(s1 + c);
+  }
+}
+
+template <int CPL, int NT>
+__device__ __forceinline__ void fp4_compute(const Fp4Rows<CPL>& b, const uint4* xs, int xstride, float* a0,
+                                            float* a1) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int t = 0; t < NT; ++t) a0[t] = a1[t] = 0.f;
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) chunk_fp4<NT>(b.q0[i], b.e0[i], b.q1[i], b.e1[i], lane + 32 * i, xs, xstride, NT, a0, a1);
+}
+
 // Rows of one gate/up work item for a group of exactly NT tokens.
 template <int KH, int NT>
 __device__ __forceinline__ void gateup_rows(const FwdArgs& a, const Group& g, int tile, const uint4* xs,
@@ -623,6 +658,38 @@ __device__ __forceinline__ void gateup_rows(const FwdArgs& a, const Group& g, in
   const uint8_t* ex = expert_base(a, g.pool, g.slot);
   const MatView w1 = mat_view(g.pool, ex, H, I, 0);
   const MatView w3 = mat_view(g.pool, ex, H, I, 1);
+  if constexpr (KH > 0 && KH <= 2048 && KH % 1024 == 0 && NT <= 2) {
+    if (g.pool == MOE_POOL_FP4 && I % kRowsGateUp == 0) {
+      constexpr int CPL = KH / 1024;
+      constexpr int NR = kRowsGateUp / (kFwdThreads / 32);  // row pairs per warp
+      Fp4Rows<CPL> buf[2];
+      auto load = [&](int j, Fp4Rows<CPL>& b) {
+        const int n = tile * kRowsGateUp + warp + j * (kFwdThreads / 32);
+        fp4_load<CPL>(b, w1.codes + (size_t)n * (H / 2), w1.scales + (size_t)n * (H / 32),
+                      w3.codes + (size_t)n * (H / 2), w3.scales + (size_t)n * (H / 32));
+      };
+      load(0, buf[0]);
+#pragma unroll
+      for (int j = 0; j < NR; ++j) {
+        if (j + 1 < NR) load(j + 1, buf[(j + 1) & 1]);
+        float ag[NT], au[NT];
+        fp4_compute<CPL, NT>(buf[j & 1], xs, H / 8, ag, au);
+        warp_allreduce<NT>(ag);
+        warp_allreduce<NT>(au);
+        const int n = tile * kRowsGateUp + warp + j * (kFwdThreads / 32);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          if (t == lane) {
+            const int sg = a.xsig[tok[t]];
+            const float gv = ldexpf(ag[t], sg);
+            const float uv = ldexpf(au[t], sg);
+            a.h[(size_t)hrow[t] * I + n] = gv / (1.f + expf(-gv)) * uv;
+          }
+        }
+      }
+      return;
+    }
+  }
   for (int r = warp; r < kRowsGateUp; r += kFwdThreads / 32) {
     const int n = tile * kRowsGateUp + r;
     if (n >= I) break;
@@ -716,6 +783,34 @@ __device__ __forceinline__ void down_rows(const FwdArgs& a, const Group& g, int 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint8_t* ex = expert_base(a, g.pool, g.slot);
   const MatView w2 = mat_view(g.pool, ex, H, I, 2);
+  if constexpr (KI > 0 && KI % 1024 == 0 && NT <= 2) {
+    if (g.pool == MOE_POOL_FP4 && H % kRowsDown == 0) {
+      constexpr int CPL = KI / 1024;
+      constexpr int NR = kRowsDown / (2 * (kFwdThreads / 32));  // row pairs per warp
+      Fp4Rows<CPL> buf[2];
+      auto load = [&](int j, Fp4Rows<CPL>& b) {
+        const int n = tile * kRowsDown + 2 * warp + j * 2 * (kFwdThreads / 32);
+        fp4_load<CPL>(b, w2.codes + (size_t)n * (I / 2), w2.scales + (size_t)n * (I / 32),
+                      w2.codes + (size_t)(n + 1) * (I / 2), w2.scales + (size_t)(n + 1) * (I / 32));
+      };
+      load(0, buf[0]);
+#pragma unroll
+      for (int j = 0; j < NR; ++j) {
+        if (j + 1 < NR) load(j + 1, buf[(j + 1) & 1]);
+        float a0[NT], a1[NT];
+        fp4_compute<CPL, NT>(buf[j & 1], xs, I / 8, a0, a1);
+        warp_allreduce<NT>(a0);
+        warp_allreduce<NT>(a1);
+        const int n = tile * kRowsDown + 2 * warp + j * 2 * (kFwdThreads / 32);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          if (lane == t) a.o[(size_t)hrow[t] * H + n] = ldexpf(a0[t], sig[t]);
+          if (lane == 16 + t) a.o[(size_t)hrow[t] * H + n + 1] = ldexpf(a1[t], sig[t]);
+        }
+      }
+      return;
+    }
+  }
   for (int r = 2 * warp; r < kRowsDown; r += 2 * (kFwdThreads / 32)) {
     const int n = tile * kRowsDown + r;
     if (n >= H) break;

@@ -386,42 +386,44 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
   }
 
-  // epilogue: warps 8-11 (TMEM lane quadrants 0-3)
-  if (warp >= 8) {
+  // epilogue: all 12 warps.  Warp w reads TMEM lane quadrant w % 4 and takes
+  // every third 16-column chunk (w / 4 picks which), over both accumulators.
+  {
     __syncwarp();
     bool ok = mbar_wait(done, 0, a.err);
     ok = __all_sync(0xffffffffu, ok);
     __syncwarp();
     tc_fence_after();
-    const int q = warp - 8;
+    const int q = warp & 3, part = warp >> 2;
     const int row = q * 32 + lane;  // D row = A tile row
+    const int nchunks = n_mma / 16;
     if (ok) {
-      for (int mt = 0; mt < kPfMT; ++mt) {
-        for (int c0 = 0; c0 < n_mma; c0 += 16) {
-          uint32_t v[16];
-          tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(mt * 256 + c0), v);
-          if (a.mode == 0) {
-            const int feat = f0 + 64 * mt + (row >> 1);
+      for (int cc = part; cc < kPfMT * nchunks; cc += 3) {
+        const int mt = cc / nchunks, c0 = (cc % nchunks) * 16;
+        uint32_t v[16];
+        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(mt * 256 + c0), v);
+        if (a.mode == 0) {
+          const int feat = f0 + 64 * mt + (row >> 1);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int col = c0 + j;
-              const int sg = (f16 && col < it.count) ? a.xsig[it.row0 + col] : 0;
-              const float mine = ldexpf(__uint_as_float(v[j]), sg);
-              const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-              if ((row & 1) == 0 && col < it.count) {
-                const float hv = mine / (1.f + expf(-mine)) * other;
-                a.hs[(size_t)(it.row0 + col) * a.I + feat] = __float2bfloat16_rn(hv);
-              }
+          for (int j = 0; j < 16; ++j) {
+            const int col = c0 + j;
+            // exact power-of-two rescale of the fp16 activation copy
+            const int sg = (f16 && col < it.count) ? a.xsig[it.row0 + col] : 0;
+            const float mine = __uint_as_float(v[j]) * __uint_as_float((uint32_t)(127 + sg) << 23);
+            const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+            if ((row & 1) == 0 && col < it.count) {
+              const float hv = __fdividef(mine, 1.f + __expf(-mine)) * other;
+              a.hs[(size_t)(it.row0 + col) * a.I + feat] = __float2bfloat16_rn(hv);
             }
-          } else {
-            const int feat = f0 + 128 * mt + row;
+          }
+        } else {
+          const int feat = f0 + 128 * mt + row;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int col = c0 + j;
-              if (col < it.count) {
-                const int p = a.perm[it.row0 + col];
-                a.o[(size_t)p * a.H + feat] = __uint_as_float(v[j]);
-              }
+          for (int j = 0; j < 16; ++j) {
+            const int col = c0 + j;
+            if (col < it.count) {
+              const int p = a.perm[it.row0 + col];
+              a.o[(size_t)p * a.H + feat] = __uint_as_float(v[j]);
             }
           }
         }
@@ -487,7 +489,7 @@ __global__ void gather_rows_kernel(const uint16_t* x, int H, int k, const int* p
     if (m > 0.f) {
       int e;
       frexpf(m, &e);
-      sg = e - 1;
+      sg = min(100, max(-100, e - 1));  // keeps 2^sg a normal float for the epilogue
     }
     if (lane == 0) xsig[i] = sg;
     __half* d16 = xg16 + (size_t)i * H;
