@@ -51,7 +51,7 @@ typedef enum {
   MOE_ERR_NOMEM = 5      /* library-owned allocation failed */
 } moe_status;
 
-enum { MOE_FETCH = 0, MOE_LOOKUP = 1 };
+enum { MOE_FETCH = 0, MOE_LOOKUP = 1, MOE_FETCH_MARK_REST = 2 };
 enum { MOE_TAG_FP4 = 0, MOE_TAG_INT2 = 1, MOE_TAG_DROP = 2 };
 enum { MOE_POOL_FP4 = 0, MOE_POOL_INT2 = 1, MOE_POOL_SHARED = 2 };
 enum { MOE_W1 = 0, MOE_W3 = 1, MOE_W2 = 2 };
@@ -132,6 +132,10 @@ moe_status moe_cache_import(moe_cache* cache, const int32_t* h_slot_key,
  *              the slots are read.
  *   mode MOE_LOOKUP: every token from token_begin is processed; hits get their
  *              slot and a fresh stamp, misses get -1; nothing is evicted or listed.
+ *   mode MOE_FETCH_MARK_REST: as MOE_FETCH, and the entries of tokens from
+ *              tokens_done on (within the rank range, non-negative ids) are set
+ *              to -1 in slots_out, so a forward enqueued for all T tokens skips
+ *              them; slots_out must not alias ids in this mode.
  *   d_miss_key, d_miss_slot  device int32 [>= min(S, num_experts)] out
  *   d_miss_count   device int32 [1] out: number of misses; on a device-detected
  *              error it is negative: -MOE_ERR_CAPACITY (a single token needs
@@ -163,6 +167,19 @@ moe_status moe_slot_ensure(moe_cache* cache, int layer_id, const int32_t* ids, i
 moe_status moe_copy_missing(moe_cache* cache, const int32_t* h_miss_key,
                             const int32_t* h_miss_slot, int n_miss, cudaStream_t copy_stream,
                             cudaEvent_t ready, cudaEvent_t done);
+/* ---------------------------------------------------------------------------
+ * copy_missing driven from the device: reads the miss list and count written
+ * by moe_slot_ensure (device int32 arrays) and copies every miss with GPU
+ * loads of the pinned bank over the host-device link, stream-ordered on
+ * `stream` -- no host synchronisation between ensure and the forward.  The
+ * bank must be mapped into the device address space (true for pinned memory
+ * on systems with unified addressing); otherwise MOE_ERR_INVALID.  Entries
+ * with an out-of-range key or slot are skipped.
+ * ------------------------------------------------------------------------- */
+moe_status moe_copy_missing_device(moe_cache* cache, const int32_t* d_miss_key,
+                                   const int32_t* d_miss_slot, const int32_t* d_miss_count,
+                                   cudaStream_t stream);
+
 /* Test hook: make the copy with list index `index` of later moe_copy_missing
  * calls fail on the host, as if cudaMemcpyAsync had returned an error
  * (index < 0 disarms).  Nothing is issued to the device for a failed copy. */
@@ -300,7 +317,7 @@ moe_status moe_rms_carry(const uint16_t* y, int T, int H, float eps, uint16_t* x
  * ------------------------------------------------------------------------- */
 enum {
   MOE_K_ROUTER = 0, MOE_K_ENSURE, MOE_K_LADDER, MOE_K_GROUP, MOE_K_PLAN, MOE_K_GATEUP,
-  MOE_K_DOWN, MOE_K_COMBINE, MOE_K_CARRY, MOE_K_GEMM_GATEUP, MOE_K_GEMM_DOWN, MOE_K_COUNT
+  MOE_K_DOWN, MOE_K_COMBINE, MOE_K_CARRY, MOE_K_GEMM_GATEUP, MOE_K_GEMM_DOWN, MOE_K_COPY, MOE_K_COUNT
 };
 moe_status moe_profile_enable(int enable);
 moe_status moe_profile_query(int kernel, double* total_ms, int* launches);

@@ -13,14 +13,14 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
 
 MOE_OK, MOE_ERR_INVALID, MOE_ERR_CAPACITY, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_NOMEM = range(6)
-MOE_FETCH, MOE_LOOKUP = 0, 1
+MOE_FETCH, MOE_LOOKUP, MOE_FETCH_MARK_REST = 0, 1, 2
 MOE_TAG_FP4, MOE_TAG_INT2, MOE_TAG_DROP = 0, 1, 2
 MOE_POOL_FP4, MOE_POOL_INT2, MOE_POOL_SHARED = 0, 1, 2
 MOE_W1, MOE_W3, MOE_W2 = 0, 1, 2
 (MOE_K_ROUTER, MOE_K_ENSURE, MOE_K_LADDER, MOE_K_GROUP, MOE_K_PLAN, MOE_K_GATEUP, MOE_K_DOWN,
- MOE_K_COMBINE, MOE_K_CARRY, MOE_K_GEMM_GATEUP, MOE_K_GEMM_DOWN, MOE_K_COUNT) = range(12)
+ MOE_K_COMBINE, MOE_K_CARRY, MOE_K_GEMM_GATEUP, MOE_K_GEMM_DOWN, MOE_K_COPY, MOE_K_COUNT) = range(13)
 KERNEL_NAMES = ["router", "ensure", "ladder", "group_pairs", "plan", "gateup", "down", "combine",
-                "rms_carry", "gemm_gateup", "gemm_down"]
+                "rms_carry", "gemm_gateup", "gemm_down", "copy_device"]
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_CAPACITY", 3: "MOE_ERR_CUDA",
                 4: "MOE_ERR_TIMEOUT", 5: "MOE_ERR_NOMEM"}
 
@@ -60,6 +60,7 @@ _SIGS = {
     "moe_slot_ensure": (i32, [vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp]),
     "moe_copy_missing": (i32, [vp, vp, vp, i32, vp, vp, vp]),
     "moe_debug_fail_copy": (i32, [vp, i32]),
+    "moe_copy_missing_device": (i32, [vp, vp, vp, vp, vp]),
     "moe_ladder_classify": (i32, [vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp,
                                   vp, vp, vp, vp, vp, vp, vp, vp]),
     "moe_group_pairs": (i32, [vp, i32, i32, i32, vp, vp, vp, vp]),
@@ -207,6 +208,11 @@ def moe_copy_missing(cache: moe_cache, h_miss_key, h_miss_slot, n_miss: int, cop
         return a.data_ptr() if hasattr(a, "data_ptr") else a.ctypes.data
     _check(_lib.moe_copy_missing(cache.handle, hp(h_miss_key), hp(h_miss_slot), n_miss,
                                  _s(copy_stream), _e(ready), _e(done)))
+
+
+def moe_copy_missing_device(cache: moe_cache, d_miss_key, d_miss_slot, d_miss_count, stream=None):
+    _check(_lib.moe_copy_missing_device(cache.handle, _p(d_miss_key), _p(d_miss_slot), _p(d_miss_count),
+                                        _s(stream)))
 
 
 def moe_debug_fail_copy(cache: moe_cache, index: int):

@@ -103,6 +103,55 @@ __global__ void cache_mark_empty_kernel(CacheDev c, int slot) {
   c.slot_key[slot] = -1;
 }
 
+// Copies the listed misses with GPU loads of the pinned bank (over the
+// host-device link) and stores into the slots; reads the miss list and count
+// on the device, so it needs no host round trip.  16-byte units, four loads in
+// flight per thread before their stores.
+template <typename Idx>
+__device__ __forceinline__ void copy_units(const CacheDev& c, const uint8_t* bank, uint8_t* slots, size_t B,
+                                           const int32_t* miss_key, const int32_t* miss_slot, Idx total) {
+  const Idx per = (Idx)(B / 16);
+  const Idx stride = (Idx)gridDim.x * blockDim.x;
+  const int K = c.L * c.E;
+  for (Idx u0 = (Idx)blockIdx.x * blockDim.x + threadIdx.x; u0 < total; u0 += 4 * stride) {
+    uint4 v[4];
+    size_t dst[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const Idx u = u0 + (Idx)j * stride;
+      dst[j] = (size_t)-1;
+      if (u < total) {
+        const int m = (int)(u / per);
+        const size_t off = (size_t)(u - (Idx)m * per) * 16;
+        const int key = miss_key[m], sl = miss_slot[m];
+        if (key >= 0 && key < K && sl >= 0 && sl < c.S) {
+          v[j] = __ldcs(reinterpret_cast<const uint4*>(bank + (size_t)key * B + off));
+          dst[j] = (size_t)sl * B + off;
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (dst[j] != (size_t)-1) *reinterpret_cast<uint4*>(slots + dst[j]) = v[j];
+  }
+}
+
+// Copies the listed misses with GPU loads of the pinned bank (over the
+// host-device link) and stores into the slots; reads the miss list and count
+// on the device, so it needs no host round trip.  16-byte units, four loads in
+// flight per thread before their stores.
+__global__ void __launch_bounds__(256) copy_missing_kernel(CacheDev c, const uint8_t* bank, uint8_t* slots,
+                                                           size_t B, const int32_t* miss_key,
+                                                           const int32_t* miss_slot, const int32_t* miss_count) {
+  const int n = *miss_count;
+  if (n <= 0) return;
+  const size_t total = (size_t)n * (B / 16);
+  if (total < 0xFFFFFFFFull)
+    copy_units<uint32_t>(c, bank, slots, B, miss_key, miss_slot, (uint32_t)total);
+  else
+    copy_units<size_t>(c, bank, slots, B, miss_key, miss_slot, total);
+}
+
 // One thread waits on an mbarrier that nothing arrives on; the bounded wait
 // gives up after limit_ns and reports MOE_ERR_TIMEOUT (the same wait every
 // pipelined kernel of this library uses).
@@ -170,6 +219,14 @@ moe_status moe_cache_create(int num_slots, int num_layers, int num_experts, size
   c->d_state = state;
   c->device = dev;
   c->fail_copy_index = -1;
+  c->bank_dev = nullptr;
+  if (h_bank != nullptr) {
+    void* dp = nullptr;
+    if (cudaHostGetDevicePointer(&dp, const_cast<void*>(h_bank), 0) == cudaSuccess)
+      c->bank_dev = (const uint8_t*)dp;
+    else
+      cudaGetLastError();  // not mapped: moe_copy_missing_device is unavailable for this cache
+  }
   uint8_t* p = (uint8_t*)state;
   c->dev.slot_stamp = (uint64_t*)p;
   p += S * 8;
@@ -255,6 +312,22 @@ moe_status moe_cache_import(moe_cache* c, const int32_t* h_slot_key, const uint6
   MOE_CUDA(cudaMemcpy(c->dev.key_to_slot, k2s.data(), (size_t)K * 4, cudaMemcpyHostToDevice));
   MOE_CUDA(cudaMemcpy(c->dev.clock, &clock, 8, cudaMemcpyHostToDevice));
   return MOE_OK;
+}
+
+moe_status moe_copy_missing_device(moe_cache* c, const int32_t* d_miss_key, const int32_t* d_miss_slot,
+                                   const int32_t* d_miss_count, cudaStream_t stream) {
+  clear_error();
+  MOE_ARG(c != nullptr, "cache is null");
+  MOE_ARG(d_miss_key && d_miss_slot && d_miss_count, "null miss list");
+  MOE_ARG(c->bank_dev != nullptr, "the host bank is not mapped into the device address space");
+  MOE_ARG(c->B % 16 == 0, "expert bytes %zu not a multiple of 16", c->B);
+  int dev = 0, sms = 1;
+  MOE_CUDA(cudaGetDevice(&dev));
+  MOE_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  ProfScope ps(MOE_K_COPY, stream);
+  copy_missing_kernel<<<sms * 4, 256, 0, stream>>>(c->dev, c->bank_dev, c->d_slots, c->B, d_miss_key, d_miss_slot,
+                                                  d_miss_count);
+  return check_launch("copy_missing_kernel");
 }
 
 moe_status moe_debug_fail_copy(moe_cache* c, int index) {

@@ -60,6 +60,7 @@ struct moe_cache {
   moe::CacheDev dev;
   int device;
   int fail_copy_index;    // host-side fault injection for moe_copy_missing (-1 = off)
+  const uint8_t* bank_dev;  // device-side address of h_bank (null if not mapped)
 };
 
 #define MOE_ARG(cond, ...)                                   \

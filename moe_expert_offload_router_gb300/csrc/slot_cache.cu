@@ -324,8 +324,18 @@ __global__ void __launch_bounds__(kEnsureThreads)
   extern __shared__ __align__(16) uint8_t smem_raw[];
   PassSmem s = carve(smem_raw, c.E, W, CMAX);
   Entries en{ids, nullptr, k, lo, hi, tb, max(T, tb)};
+  const bool mark_rest = mode == MOE_FETCH_MARK_REST;
+  if (mark_rest) mode = MOE_FETCH;
+  // MOE_FETCH_MARK_REST: entries of tokens [from, T) get slot -1.
+  auto mark_from = [&](int from) {
+    if (!mark_rest) return;
+    Entries rest{ids, nullptr, k, lo, hi, from, en.tend};
+    for (int f = threadIdx.x; f < rest.count(); f += blockDim.x)
+      if (rest.expert(f) >= 0) slots_out[rest.index(f)] = -1;
+  };
   const int dtotal = analyze(s, en);
   if (dtotal < 0) {
+    mark_from(tb);
     if (threadIdx.x == 0) {
       *miss_count = -MOE_ERR_INVALID;
       *tokens_done = tb;
@@ -336,6 +346,7 @@ __global__ void __launch_bounds__(kEnsureThreads)
   if (mode == MOE_FETCH) {
     n_rel = chunk_tokens(s, en, dtotal, c.S, &D);
     if (n_rel == 0 && en.tend > en.tb) {
+      mark_from(tb);
       if (threadIdx.x == 0) {
         *miss_count = -MOE_ERR_CAPACITY;
         *tokens_done = tb;
@@ -344,6 +355,7 @@ __global__ void __launch_bounds__(kEnsureThreads)
     }
   }
   const int M = resolve(s, c, layer, D, mode, miss_key, miss_slot);
+  mark_from(tb + n_rel);
   en.tend = en.tb + n_rel;
   write_slots(s, en, slots_out, nullptr, 0);
   if (threadIdx.x == 0) {
@@ -612,7 +624,9 @@ extern "C" moe_status moe_slot_ensure(moe_cache* cache, int layer_id, const int3
   MOE_ARG(layer_id >= 0 && layer_id < cache->L, "layer_id %d out of [0, %d)", layer_id, cache->L);
   MOE_ARG(T >= 0 && k >= 1 && k <= 64, "need T >= 0 and 1 <= k <= 64");
   MOE_ARG(0 <= rank_lo && rank_lo <= rank_hi && rank_hi <= k, "bad rank range [%d, %d)", rank_lo, rank_hi);
-  MOE_ARG(mode == MOE_FETCH || mode == MOE_LOOKUP, "mode must be MOE_FETCH or MOE_LOOKUP");
+  MOE_ARG(mode == MOE_FETCH || mode == MOE_LOOKUP || mode == MOE_FETCH_MARK_REST, "bad mode");
+  MOE_ARG(mode != MOE_FETCH_MARK_REST || (const void*)ids != (const void*)slots_out,
+          "MOE_FETCH_MARK_REST needs slots_out separate from ids");
   MOE_ARG(token_begin >= 0, "token_begin < 0");
   MOE_ARG(ids && slots_out && d_miss_count && d_tokens_done, "null pointer");
   MOE_ARG(mode == MOE_LOOKUP || (d_miss_key && d_miss_slot), "FETCH needs miss lists");

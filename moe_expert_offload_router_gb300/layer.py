@@ -9,6 +9,17 @@ the grouped expert MLP.  When a token chunk needs more distinct experts than
 there are slots, ensure reports how far it got and the sequence repeats for
 the rest.  All arithmetic runs in the library's kernels; this file only
 sequences calls and owns buffers.
+
+With ``copy="device"`` the misses are instead copied by a kernel that reads
+the miss list on the device (``moe_copy_missing_device``), so router, ensure,
+copy and forward are enqueued back to back.  Ensure runs in the mode that
+marks tokens past its chunk as skipped, the forward is enqueued for every
+remaining token, and the host reads ``tokens_done`` afterwards, while the GPU
+works; a second chunk (if any) then recomputes the rows it owns.  When the
+batch cannot need more distinct experts than there are slots
+(``min(E, T*k) <= S``) there is a single chunk by construction and the host
+does not wait at all: the status of each layer is checked on the next call
+(or by :meth:`check`).
 """
 from __future__ import annotations
 
@@ -24,7 +35,7 @@ class DecodeLayerRunner:
 
     def __init__(self, cache: L.moe_cache, views: L.moe_expert_views, E: int, k: int,
                  T_max: int, device=None, int2_cache: Optional[L.moe_cache] = None,
-                 ladder=None, assume_resident: bool = False):
+                 ladder=None, assume_resident: bool = False, copy: str = "engine"):
         self.cache, self.views, self.E, self.k, self.T_max = cache, views, E, k, T_max
         self.dev = torch.device(device or "cuda")
         self.c2, self.ladder = int2_cache, ladder
@@ -48,6 +59,14 @@ class DecodeLayerRunner:
         self.copy_stream = torch.cuda.Stream(device=dev)
         self.ready = torch.cuda.Event()
         self.done = torch.cuda.Event()
+        if copy not in ("engine", "device"):
+            raise ValueError("copy must be 'engine' or 'device'")
+        if copy == "device" and ladder is not None:
+            raise ValueError("copy='device' serves the FP4-only path")
+        self.copy = copy
+        self.status_h = torch.zeros(4, dtype=torch.int32, pin_memory=True)
+        self.status_ev = torch.cuda.Event()
+        self.pending = None   # (layer_id, T) whose status is still to be read
         self.assume_resident = assume_resident
         if assume_resident and cache.S < cache.L * cache.E:
             raise ValueError("assume_resident needs a cache with a slot for every key")
@@ -60,14 +79,60 @@ class DecodeLayerRunner:
                     slots4=i[4 + m4:4 + 2 * m4], keys2=i[4 + 2 * m4:4 + 2 * m4 + m2],
                     slots2=i[4 + 2 * m4 + m2:4 + 2 * m4 + 2 * m2])
 
+    def check(self):
+        """Reads the status of the last device-mode layer whose check was deferred."""
+        if self.pending is None:
+            return
+        layer_id, T = self.pending
+        self.pending = None
+        self.status_ev.synchronize()
+        n4, done = int(self.status_h[0]), int(self.status_h[1])
+        if n4 < 0:
+            raise L.MoeError(-n4, f"slot ensure failed on the device (layer {layer_id})")
+        self.stats["misses"] += n4
+        self.stats["bytes_copied"] += n4 * self.cache.B
+        if done != T:
+            raise L.MoeError(L.MOE_ERR_CAPACITY, f"layer {layer_id}: single chunk expected, got {done}/{T}")
+
+    def _run_device(self, layer_id, T, ids, w, slots, x, y, stream):
+        v = self._views(T)
+        k = self.k
+        single = min(self.E, T * k) <= self.cache.S
+        tb = 0
+        while tb < T:
+            L.moe_slot_ensure(self.cache, layer_id, ids, slots, 0, k, L.MOE_FETCH_MARK_REST, tb,
+                              v["keys4"], v["slots4"], v["count4"], v["done"], stream)
+            with torch.cuda.stream(stream):
+                self.status_h.copy_(self.info[0:4], non_blocking=True)
+            self.status_ev.record(stream)
+            L.moe_copy_missing_device(self.cache, v["keys4"], v["slots4"], v["count4"], stream)
+            self.stats["chunks"] += 1
+            L.moe_expert_forward(self.views, x[tb:T], slots[tb:T], None, w[tb:T], y[tb:T], self.ws,
+                                 self.err, stream)
+            if single:
+                self.pending = (layer_id, T)
+                return y
+            self.status_ev.synchronize()
+            n4, done = int(self.status_h[0]), int(self.status_h[1])
+            if n4 < 0:
+                raise L.MoeError(-n4, f"slot ensure failed on the device (token_begin={tb})")
+            self.stats["misses"] += n4
+            self.stats["bytes_copied"] += n4 * self.cache.B
+            tb = done
+        return y
+
     def run(self, layer_id: int, logits, x, y, stream=None):
         """y[T, H] (bf16 bits) = the MoE layer applied to x[T, H] with router logits [T, E]."""
         T = logits.shape[0]
         assert T <= self.T_max
         stream = stream or torch.cuda.current_stream(self.dev)
         k = self.k
+        self.check()
         ids, w, slots = self.ids[:T], self.w[:T], self.slots[:T]
         L.moe_router_topk(logits, k, True, ids, w, stream)
+        if self.copy == "device" and not self.assume_resident:
+            self.stats["calls"] += 1
+            return self._run_device(layer_id, T, ids, w, slots, x, y, stream)
         v = self._views(T)
         tb = 0
         self.stats["calls"] += 1
