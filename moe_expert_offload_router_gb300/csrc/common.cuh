@@ -154,25 +154,43 @@ __device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// One poll that may suspend the thread in hardware until the phase completes
+// or about hint_ns pass: a waiting warp then takes no issue slots from the
+// warps that share its scheduler.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
 // Waits for the phase of parity `parity` to complete; gives up after
 // limit_ns (1 s by default) or when another thread of the grid gave up, and
-// then records MOE_ERR_TIMEOUT in *err and returns false.
+// then records MOE_ERR_TIMEOUT in *err and returns false.  Each poll suspends
+// for at most a quarter of the limit (and 1 ms), so the limit holds to within
+// that.
 static __device__ __noinline__ bool mbar_wait(uint64_t* b, uint32_t parity, int* err,
                                               uint64_t limit_ns = 1000000000ull) {
   if (mbar_test(b, parity)) return true;
   const uint64_t t0 = gtimer();
+  const uint32_t hint = (uint32_t)(limit_ns / 4 < 1000000ull ? limit_ns / 4 : 1000000ull);
   for (uint32_t it = 1;; ++it) {
-    if (mbar_test(b, parity)) return true;
-    if ((it & 255) == 0) {
-      if (gtimer() - t0 > limit_ns) {
-        atomicExch(err, MOE_ERR_TIMEOUT);
-        return false;
-      }
-      if (*(volatile int*)err == MOE_ERR_TIMEOUT) return false;
+    if (mbar_try_wait(b, parity, hint)) return true;
+    if (gtimer() - t0 > limit_ns) {
+      atomicExch(err, MOE_ERR_TIMEOUT);
+      return false;
     }
+    if ((it & 15) == 0 && *(volatile int*)err == MOE_ERR_TIMEOUT) return false;
   }
 }
 
+
+// mbar_wait with the ready case inline (no call when the phase is complete).
+__device__ __forceinline__ bool mbar_wait_fast(uint64_t* b, uint32_t parity, int* err) {
+  return mbar_test(b, parity) || mbar_wait(b, parity, err);
+}
 
 // One-dimensional bulk copy global -> shared (16-byte aligned, size a multiple
 // of 16), completing as transaction bytes on an mbarrier.

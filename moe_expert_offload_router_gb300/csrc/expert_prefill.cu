@@ -20,13 +20,13 @@
 // GEMM CTA (384 threads): warp 8 lane 0 streams the raw FP4 codes of the A
 // tiles by TMA into a staging ring, as far ahead as the ring allows; warp 10
 // lane 0 loads the B tile by TMA straight into its 128-byte swizzled K-major
-// layout, one stage per free operand slot; warps 0-7 decode the raw codes to bf16 with the
-// E8M0 scale folded in (exact: E2M1 x 2^(e-127) fits bf16 for all scales) and
-// store them in the same swizzled layout; warp 9 lane 0 issues
-// tcgen05.mma.kind::f16 (M = 128, N = rows of the item rounded to 16, K = 16
-// per instruction) into a TMEM accumulator and commits each stage back to the
-// producers; warps 8-11 read TMEM with tcgen05.ld for the epilogue.  Every
-// mbarrier wait gives up after one second and records MOE_ERR_TIMEOUT.
+// layout, one stage per free operand slot; warps 0-7 decode the raw codes to
+// 16-bit with the E8M0 scale folded in (exact) and store them in the same
+// swizzled layout; warp 9 lane 0 issues tcgen05.mma.kind::f16 (M = 128,
+// N = rows of the item rounded to 16, K = 16 per instruction) into two TMEM
+// accumulators and commits each stage back to the producers; all 12 warps
+// read TMEM with tcgen05.ld for the epilogue.  Every mbarrier wait gives up
+// after one second and records MOE_ERR_TIMEOUT.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -41,22 +41,40 @@ namespace moe {
 
 constexpr int kPfThreads = 384;
 constexpr int kPfStages = 3;      // A/B operand stages
-constexpr int kPfRaw = 4;         // raw FP4 code stages
 constexpr int kPfMT = 2;          // 128-row weight tiles per CTA (two TMEM accumulators)
-constexpr int kPfNMax = 256;      // rows per item (MMA N)
+constexpr int kPfNMax = 256;      // rows per item (MMA N) of the item list
 constexpr int kPfKStep = 64;      // K elements per stage (128 bytes of bf16: one swizzle row)
 constexpr int kPfBox = 64;        // rows per TMA box of the B operand
+// Converter warps 0-7 form two groups of 128 threads; group g converts the
+// K steps ks with ks % 2 == g, one A row per thread.  Each group then has two
+// steps' time per wait round, which halves the wait overhead per step.
+constexpr int kPfConvGroups = 2;
+constexpr int kPfConvThreads = 128;
 
 // shared memory layout (offsets from a 1024-aligned base)
 constexpr int kATile = 128 * 128;                 // 16 KB per 128-row tile
 constexpr int kAStage = kPfMT * kATile;           // 32 KB
-constexpr int kBTile = kPfNMax * 128;             // 32 KB
 constexpr int kRawTile = kPfMT * 128 * 32;        // 8 KB of packed codes per stage
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kPfStages * kAStage;
-constexpr int kOffRaw = kOffB + kPfStages * kBTile;
-constexpr int kOffBar = kOffRaw + kPfRaw * kRawTile;
-constexpr int kPfSmem = kOffBar + 256 + 1024;     // + alignment slack
+
+// Two shapes of the GEMM CTA: items of up to 256 rows with a 4-deep raw-code
+// ring (prefill: tensor-bound), or items of up to 64 rows, whose smaller B
+// stages leave room for a 12-deep ring (decode batches: the weight stream is
+// the bound, and one CTA per SM needs ~100 KB in flight to cover HBM latency).
+template <int NMAX, int RAW>
+struct PfCfg {
+  static constexpr int kNMax = NMAX;
+  static constexpr int kRaw = RAW;
+  static constexpr int kBTile = NMAX * 128;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kPfStages * kAStage;
+  static constexpr int kOffRaw = kOffB + kPfStages * kBTile;
+  static constexpr int kOffBar = kOffRaw + RAW * kRawTile;
+  static constexpr int kSmem = kOffBar + 512 + 1024;  // barriers + alignment slack
+  static_assert((2 * kPfStages + 2 * RAW + 1) * 8 + 8 <= 512, "barrier area");
+  static_assert(kSmem <= 232448, "shared memory per CTA");
+};
+using PfBig = PfCfg<256, 4>;
+using PfSmall = PfCfg<64, 12>;
 
 __device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
   asm volatile(
@@ -168,18 +186,19 @@ struct PfArgs {
   int* err;
 };
 
+template <class C>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
                         const __grid_constant__ CUtensorMap mB, const __grid_constant__ CUtensorMap mB16,
                         PfArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t* bar = (uint64_t*)(sm + kOffBar);
+  uint64_t* bar = (uint64_t*)(sm + C::kOffBar);
   uint64_t* full = bar;                  // [kPfStages]
   uint64_t* empty = bar + kPfStages;     // [kPfStages]
-  uint64_t* rawf = bar + 2 * kPfStages;  // [kPfRaw]
-  uint64_t* rawe = rawf + kPfRaw;        // [kPfRaw]
-  uint64_t* done = rawe + kPfRaw;
+  uint64_t* rawf = bar + 2 * kPfStages;  // [C::kRaw]
+  uint64_t* rawe = rawf + C::kRaw;       // [C::kRaw]
+  uint64_t* done = rawe + C::kRaw;
   uint32_t* tmem_slot = (uint32_t*)(done + 1);
   int* f16_flag = (int*)(tmem_slot + 1);
 
@@ -187,6 +206,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const int tile = blockIdx.x % a.tiles;
   if (item_idx >= *a.n_items) return;
   const PfItem it = a.items[item_idx];
+  if (it.count > C::kNMax || it.count < 1) {  // the host picks the shape from T; never expected
+    if (threadIdx.x == 0) atomicCAS(a.err, 0, MOE_ERR_INVALID);
+    return;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = a.K / kPfKStep;
   const int sbytes = a.K / 32;                   // scale bytes per weight row
@@ -196,14 +219,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPfStages; ++s) {
-      mbar_init(&full[s], 256 + 1);
+      mbar_init(&full[s], kPfConvThreads + 1);
       mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < kPfRaw; ++s) {
+    for (int s = 0; s < C::kRaw; ++s) {
       mbar_init(&rawf[s], 1);
-      mbar_init(&rawe[s], 256);
+      mbar_init(&rawe[s], kPfConvThreads);
     }
     mbar_init(done, 1);
+    *f16_flag = (a.mode == 0 && a.allow_f16) ? 1 : 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 9) {
@@ -221,41 +245,53 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const int f0 = a.mode == 0 ? tile * 128 : tile * 256;
 
   // fp16 or bf16 operands for this tile: fp16 when every block scale of the
-  // tile keeps the scaled E2M1 values exact in fp16 (gate/up only)
-  if (threadIdx.x == 0) *f16_flag = (a.mode == 0 && a.allow_f16) ? 1 : 0;
-  __syncthreads();
-  if (a.mode == 0 && a.allow_f16 && warp < 8) {
-    const int r = threadIdx.x >> 1, c = threadIdx.x & 1;
-    const int g = r & 1, i = r >> 1;
-    bool in_range = true;
-    for (int mt = 0; mt < kPfMT; ++mt) {
-      const uint8_t* row = (g ? a.sc1 : a.sc0) + (size_t)it.slot * a.B + (size_t)(f0 + 64 * mt + i) * sbytes;
-      for (int off = c * 16; off < sbytes; off += 32) {
-        const uint4 q = __ldg(reinterpret_cast<const uint4*>(row + off));
-        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+  // tile keeps the scaled E2M1 values exact in fp16 (gate/up only).  The vote
+  // runs in every warp but the raw-code producer, which starts streaming at once.
+  bool f16 = false;
+  if (warp != 8) {
+    if (a.mode == 0 && a.allow_f16 && warp < 8) {
+      const int r = threadIdx.x >> 1, c = threadIdx.x & 1;
+      const int g = r & 1, i = r >> 1;
+      uint4 q[kPfMT][4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+      for (int mt = 0; mt < kPfMT; ++mt) {
+        const uint8_t* row = (g ? a.sc1 : a.sc0) + (size_t)it.slot * a.B + (size_t)(f0 + 64 * mt + i) * sbytes;
 #pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            const uint32_t e = (w4[u] >> (8 * b)) & 0xff;
-            in_range = in_range && e >= kF16ScaleLo && e <= kF16ScaleHi;
-          }
+        for (int j = 0; j < 4; ++j) {
+          const int off = c * 16 + j * 32;
+          q[mt][j] = off < sbytes ? __ldg(reinterpret_cast<const uint4*>(row + off))
+                                  : make_uint4(0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
+        }
       }
+      bool in_range = true;
+#pragma unroll
+      for (int mt = 0; mt < kPfMT; ++mt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t w4[4] = {q[mt][j].x, q[mt][j].y, q[mt][j].z, q[mt][j].w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              const uint32_t e = (w4[u] >> (8 * b)) & 0xff;
+              in_range = in_range && e >= kF16ScaleLo && e <= kF16ScaleHi;
+            }
+        }
+      if (!in_range) atomicAnd(f16_flag, 0);
     }
-    if (!in_range) atomicAnd(f16_flag, 0);
+    asm volatile("bar.sync 1, %0;" ::"n"(kPfThreads - 32) : "memory");
+    f16 = *(volatile int*)f16_flag != 0;
   }
-  __syncthreads();
-  const bool f16 = *f16_flag != 0;
 
   if (warp == 8) {
     // weight codes: as far ahead as the raw ring allows, independent of MMA progress
     if (lane == 0) {
       bool ok = true;
       for (int rk = 0; rk < nk && ok; ++rk) {
-        const int rs = rk % kPfRaw, rr = rk / kPfRaw;
-        if (rr > 0) ok = mbar_wait(&rawe[rs], (rr - 1) & 1, a.err);
+        const int rs = rk % C::kRaw, rr = rk / C::kRaw;
+        if (rr > 0) ok = mbar_wait_fast(&rawe[rs], (rr - 1) & 1, a.err);
         if (!ok) break;
-        uint8_t* dst = sm + kOffRaw + rs * kRawTile;
+        uint8_t* dst = sm + C::kOffRaw + rs * kRawTile;
         mbar_expect_tx(&rawf[rs], kRawTile);
         if (a.mode == 0) {
           tma_3d(dst, &mA0, rk * 32, f0, it.slot, &rawf[rs]);
@@ -276,9 +312,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       bool ok = true;
       for (int ks = 0; ks < nk && ok; ++ks) {
         const int s = ks % kPfStages, r = ks / kPfStages;
-        if (r > 0) ok = mbar_wait(&empty[s], (r - 1) & 1, a.err);
+        if (r > 0) ok = mbar_wait_fast(&empty[s], (r - 1) & 1, a.err);
         if (!ok) break;
-        uint8_t* bdst = sm + kOffB + s * kBTile;
+        uint8_t* bdst = sm + C::kOffB + s * C::kBTile;
         mbar_expect_tx(&full[s], b_bytes);
         for (int bx = 0; bx < n_box; ++bx)
           tma_2d(bdst + bx * kPfBox * 128, f16 ? &mB16 : &mB, ks * kPfKStep, it.row0 + bx * kPfBox, &full[s]);
@@ -295,13 +331,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       bool ok = true;
       for (int ks = 0; ks < nk && ok; ++ks) {
         const int s = ks % kPfStages, r = ks / kPfStages;
-        ok = mbar_wait(&full[s], r & 1, a.err);
+        ok = mbar_wait_fast(&full[s], r & 1, a.err);
         if (!ok) break;
         tc_fence_after();
-        const uint64_t bd = umma_desc_sw128(su32(sm + kOffB + s * kBTile));
+        const uint64_t bd = umma_desc_sw128(su32(sm + C::kOffB + s * C::kBTile));
 #pragma unroll
         for (int mt = 0; mt < kPfMT; ++mt) {
-          const uint64_t ad = umma_desc_sw128(su32(sm + kOffA + s * kAStage + mt * kATile));
+          const uint64_t ad = umma_desc_sw128(su32(sm + C::kOffA + s * kAStage + mt * kATile));
 #pragma unroll
           for (int kk = 0; kk < kPfKStep / 16; ++kk)
             mma_bf16(tmem + (uint32_t)(mt * 256), ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
@@ -312,23 +348,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mma_commit(done);  // fires when every issued MMA has completed
     }
   } else if (warp < 8) {
-    // converters: thread -> (row r, 32-weight half c) of each 128 x 64 A tile
-    const int t = threadIdx.x;
-    const int r = t >> 1, c = t & 1;
+    // converters: group cg takes the K steps of its parity; thread -> row r
+    // of both 128 x 64 A tiles (two 32-weight halves each)
+    const int cg = warp >> 2;
+    const int r = threadIdx.x & (kPfConvThreads - 1);
     const int g = r & 1, i = r >> 1;  // mode 0: gate/up interleaved rows
     int raw_off[kPfMT];
     const uint8_t* srow[kPfMT];
 #pragma unroll
     for (int mt = 0; mt < kPfMT; ++mt) {
       if (a.mode == 0) {
-        raw_off[mt] = g * (128 * 32) + (64 * mt + i) * 32 + c * 16;
+        raw_off[mt] = g * (128 * 32) + (64 * mt + i) * 32;
         srow[mt] = (g ? a.sc1 : a.sc0) + (size_t)it.slot * a.B + (size_t)(f0 + 64 * mt + i) * sbytes;
       } else {
-        raw_off[mt] = (128 * mt + r) * 32 + c * 16;
+        raw_off[mt] = (128 * mt + r) * 32;
         srow[mt] = a.sc0 + (size_t)it.slot * a.B + (size_t)(f0 + 128 * mt + r) * sbytes;
       }
     }
-    // scale bytes: 16 at a time (8 k-steps), loaded one group ahead
+    // scale bytes: 16 at a time (8 K steps), loaded one group ahead
     uint4 scur[kPfMT], snext[kPfMT];
 #pragma unroll
     for (int mt = 0; mt < kPfMT; ++mt) {
@@ -336,10 +373,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       snext[mt] = sbytes > 16 ? __ldg(reinterpret_cast<const uint4*>(srow[mt] + 16)) : scur[mt];
     }
     bool ok = true;
-    for (int ks = 0; ks < nk && ok; ++ks) {
-      const int rs = ks % kPfRaw, rr = ks / kPfRaw;
+    for (int ks = cg; ks < nk && ok; ks += kPfConvGroups) {
+      const int rs = ks % C::kRaw, rr = ks / C::kRaw;
       const int s = ks % kPfStages, rnd = ks / kPfStages;
-      if ((ks & 7) == 0 && ks > 0) {
+      if ((ks & 7) == cg && ks >= 8) {
 #pragma unroll
         for (int mt = 0; mt < kPfMT; ++mt) {
           scur[mt] = snext[mt];
@@ -347,38 +384,44 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           if (nxt < sbytes) snext[mt] = __ldg(reinterpret_cast<const uint4*>(srow[mt] + nxt));
         }
       }
-      if (!(ok = mbar_wait(&rawf[rs], rr & 1, a.err))) break;
-      uint4 q[kPfMT];
-#pragma unroll
-      for (int mt = 0; mt < kPfMT; ++mt)
-        q[mt] = *reinterpret_cast<const uint4*>(sm + kOffRaw + rs * kRawTile + raw_off[mt]);
-      mbar_arrive(&rawe[rs]);
-      if (rnd > 0 && !(ok = mbar_wait(&empty[s], (rnd - 1) & 1, a.err))) break;
-      const int sb = (ks & 7) * 2 + c;  // scale byte within the 16 loaded
+      if (!(ok = mbar_wait_fast(&rawf[rs], rr & 1, a.err))) break;
+      uint4 q[kPfMT][2];
 #pragma unroll
       for (int mt = 0; mt < kPfMT; ++mt) {
-        const uint32_t sw = sb < 4 ? scur[mt].x : sb < 8 ? scur[mt].y : sb < 12 ? scur[mt].z : scur[mt].w;
-        const uint32_t e8 = (sw >> (8 * (sb & 3))) & 0xff;
-        const uint32_t sc2 = f16 ? e8m0_f16x2(e8) : e8m0_bf16x2(e8);
-        uint8_t* arow = sm + kOffA + s * kAStage + mt * kATile + r * 128;
-        const uint32_t w4[4] = {q[mt].x, q[mt].y, q[mt].z, q[mt].w};
+        const uint8_t* src = sm + C::kOffRaw + rs * kRawTile + raw_off[mt];
+        q[mt][0] = *reinterpret_cast<const uint4*>(src);
+        q[mt][1] = *reinterpret_cast<const uint4*>(src + 16);
+      }
+      mbar_arrive(&rawe[rs]);
+      if (rnd > 0 && !(ok = mbar_wait_fast(&empty[s], (rnd - 1) & 1, a.err))) break;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t wv = w4[u];
-          uint4 o;
-          if (f16) {
-            o.x = fp4x2_to_f16x2(wv & 0xff, sc2);
-            o.y = fp4x2_to_f16x2((wv >> 8) & 0xff, sc2);
-            o.z = fp4x2_to_f16x2((wv >> 16) & 0xff, sc2);
-            o.w = fp4x2_to_f16x2(wv >> 24, sc2);
-          } else {
-            o.x = fp4x2_to_bf16x2(wv & 0xff, sc2);
-            o.y = fp4x2_to_bf16x2((wv >> 8) & 0xff, sc2);
-            o.z = fp4x2_to_bf16x2((wv >> 16) & 0xff, sc2);
-            o.w = fp4x2_to_bf16x2(wv >> 24, sc2);
+      for (int mt = 0; mt < kPfMT; ++mt) {
+        uint8_t* arow = sm + C::kOffA + s * kAStage + mt * kATile + r * 128;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int sb = (ks & 7) * 2 + c;  // scale byte within the 16 loaded
+          const uint32_t sw = sb < 4 ? scur[mt].x : sb < 8 ? scur[mt].y : sb < 12 ? scur[mt].z : scur[mt].w;
+          const uint32_t e8 = (sw >> (8 * (sb & 3))) & 0xff;
+          const uint32_t sc2 = f16 ? e8m0_f16x2(e8) : e8m0_bf16x2(e8);
+          const uint32_t w4[4] = {q[mt][c].x, q[mt][c].y, q[mt][c].z, q[mt][c].w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t wv = w4[u];
+            uint4 o;
+            if (f16) {
+              o.x = fp4x2_to_f16x2(wv & 0xff, sc2);
+              o.y = fp4x2_to_f16x2((wv >> 8) & 0xff, sc2);
+              o.z = fp4x2_to_f16x2((wv >> 16) & 0xff, sc2);
+              o.w = fp4x2_to_f16x2(wv >> 24, sc2);
+            } else {
+              o.x = fp4x2_to_bf16x2(wv & 0xff, sc2);
+              o.y = fp4x2_to_bf16x2((wv >> 8) & 0xff, sc2);
+              o.z = fp4x2_to_bf16x2((wv >> 16) & 0xff, sc2);
+              o.w = fp4x2_to_bf16x2(wv >> 24, sc2);
+            }
+            const int unit = c * 4 + u;
+            *reinterpret_cast<uint4*>(arow + ((unit ^ (r & 7)) << 4)) = o;
           }
-          const int unit = c * 4 + u;
-          *reinterpret_cast<uint4*>(arow + ((unit ^ (r & 7)) << 4)) = o;
         }
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -394,6 +437,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     ok = __all_sync(0xffffffffu, ok);
     __syncwarp();
     tc_fence_after();
+    if (warp == 8) f16 = *(volatile int*)f16_flag != 0;  // final: every converter has passed the vote
     const int q = warp & 3, part = warp >> 2;
     const int row = q * 32 + lane;  // D row = A tile row
     const int nchunks = n_mma / 16;
@@ -634,14 +678,20 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
   if ((st = map_bf16_rows(&mx16, b.xg16, H, P, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != MOE_OK) return st;
   if ((st = map_bf16_rows(&mh, b.hs, I, P)) != MOE_OK) return st;
 
-  static bool smem_set = false;
-  if (!smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+  // items hold at most T rows (each token routes to a slot once): up to 64
+  // tokens take the deep-ring shape
+  const bool small = T <= PfSmall::kNMax;
+  static bool smem_set[2] = {false, false};
+  if (!smem_set[small]) {
+    cudaError_t e = small ? cudaFuncSetAttribute(prefill_gemm_kernel<PfSmall>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, PfSmall::kSmem)
+                          : cudaFuncSetAttribute(prefill_gemm_kernel<PfBig>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, PfBig::kSmem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_gemm_kernel)");
-    smem_set = true;
+    smem_set[small] = true;
   }
-  // items: at most one per used slot plus one per 256 further rows
-  const int max_items = (int)std::min<size_t>((size_t)S, P) + (int)(P / kPfNMax) + 1;
+  // items: at most one per used slot, plus one per 256 further rows (wide shape)
+  const int max_items = (int)std::min<size_t>((size_t)S, P) + (small ? 0 : (int)(P / kPfNMax) + 1);
   PfArgs pa;
   pa.H = H;
   pa.I = I;
@@ -655,6 +705,12 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
   pa.err = d_error;
   pa.B = B;
   pa.xsig = b.xsig;
+  auto launch = [&](const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& bm, const CUtensorMap& bm16) {
+    if (small)
+      prefill_gemm_kernel<PfSmall><<<max_items * pa.tiles, kPfThreads, PfSmall::kSmem, stream>>>(a0, a1, bm, bm16, pa);
+    else
+      prefill_gemm_kernel<PfBig><<<max_items * pa.tiles, kPfThreads, PfBig::kSmem, stream>>>(a0, a1, bm, bm16, pa);
+  };
   // GEMM1: gate/up, 128 features (two tiles of 64 gate/up pairs) per CTA
   pa.mode = 0;
   pa.K = H;
@@ -664,7 +720,7 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
   pa.allow_f16 = 1;
   {
     ProfScope ps(MOE_K_GEMM_GATEUP, stream);
-    prefill_gemm_kernel<<<max_items * pa.tiles, kPfThreads, kPfSmem, stream>>>(m1c, m3c, mx, mx16, pa);
+    launch(m1c, m3c, mx, mx16);
   }
   if ((st = check_launch("prefill_gemm_kernel (gate/up)")) != MOE_OK) return st;
   // GEMM2: down, 256 output features (two tiles of 128) per CTA
@@ -676,7 +732,7 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
   pa.allow_f16 = 0;
   {
     ProfScope ps(MOE_K_GEMM_DOWN, stream);
-    prefill_gemm_kernel<<<max_items * pa.tiles, kPfThreads, kPfSmem, stream>>>(m2c, m2c, mh, mh, pa);
+    launch(m2c, m2c, mh, mh);
   }
   return check_launch("prefill_gemm_kernel (down)");
 }

@@ -91,14 +91,16 @@ def test_prefill_full_size_via_forward_dispatch_sampled():
     assert bf16_rel_err(y[sample], ref) <= TOL
 
 
-def test_prefill_matches_decode_path():
-    # the two expert paths agree on the same call (both within the oracle tolerance)
+@pytest.mark.parametrize("T", [64, 100])
+def test_prefill_matches_decode_path(T):
+    # the two expert paths agree on the same call (both within the oracle
+    # tolerance); T = 64 takes the deep-ring GEMM shape, T = 100 the wide one
     M = load_lib()
     wl = configs.scaled(configs.PREFILL, H=512, I=1024, E=16)
     S = 8
     pool, views, weights = _pool(M, wl, S)
     rng = np.random.default_rng(5)
-    T, k = 64, 4
+    k = 4
     slots = np.stack([rng.choice(S, size=k, replace=False) for _ in range(T)])
     w = rng.random((T, k)).astype(np.float32)
     x = gen.activations(wl, 0, 1, T)
@@ -107,6 +109,28 @@ def test_prefill_matches_decode_path():
     assert e1 == 0 and e2 == 0
     ref = moe_layer(x, slots, w.astype(np.float64), weights)
     assert bf16_rel_err(y1, ref) <= TOL and bf16_rel_err(y2, ref) <= TOL
+
+
+def test_grouped_gemm_item_sizes_at_the_shape_limit():
+    # decode-sized call through the grouped GEMM: one slot routed from all 64
+    # tokens (an item of exactly 64 rows), one from at least 33, the rest ragged
+    M = load_lib()
+    wl = configs.scaled(configs.PREFILL, H=1024, I=512, E=16)
+    S = 10
+    pool, views, weights = _pool(M, wl, S)
+    rng = np.random.default_rng(9)
+    T, k = 64, 6
+    slots = np.zeros((T, k), dtype=np.int64)
+    for t in range(T):
+        rest = [s for s in range(S) if s != 3 and (t >= 33 or s != 5)]
+        picks = list(rng.choice(rest, size=k - (1 if t >= 33 else 2), replace=False))
+        slots[t] = [3] + ([] if t >= 33 else [5]) + picks
+    w = rng.random((T, k)).astype(np.float32)
+    x = gen.activations(wl, 0, 2, T)
+    y, err = _run(M, views, x, slots, w, "forward")
+    assert err == 0
+    ref = moe_layer(x, slots, w.astype(np.float64), weights)
+    assert bf16_rel_err(y, ref) <= TOL
 
 
 def test_prefill_rejects_unsupported():
