@@ -39,7 +39,7 @@ def _args():
     p.add_argument("--sweep", default="1,4,16,64", help="decode batches also measured (comma list, '' for none)")
     p.add_argument("--cpu-sample-tokens", type=int, default=4)
     p.add_argument("--workload", default="decode", choices=["decode", "prefill", "ladder", "stack"])
-    p.add_argument("--copy", default="engine", choices=["engine", "device"],
+    p.add_argument("--copy", default="device", choices=["engine", "device"],
                    help="miss copies: copy engine after one host sync, or a kernel reading the miss list")
     return p.parse_args()
 
