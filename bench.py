@@ -41,6 +41,8 @@ def _args():
     p.add_argument("--workload", default="decode", choices=["decode", "prefill", "ladder", "stack"])
     p.add_argument("--copy", default="device", choices=["engine", "device"],
                    help="miss copies: copy engine after one host sync, or a kernel reading the miss list")
+    p.add_argument("--no-overlap", action="store_true",
+                   help="device copy: run the forward after the copies instead of beside them")
     return p.parse_args()
 
 
@@ -194,7 +196,8 @@ def run_ours(args):
     shared = torch.from_numpy(gen.shared_expert(base, 0)).to(dev)
     cache = M.moe_cache(S, 1, E, Bx, slots, bank)
     views = M.make_views(H, I, slots, S, None, 0, shared)
-    runner = M.DecodeLayerRunner(cache, views, E, k, Tmax, dev, copy=args.copy)
+    overlap = "auto" if args.copy == "device" and not args.no_overlap else False
+    runner = M.DecodeLayerRunner(cache, views, E, k, Tmax, dev, copy=args.copy, overlap=overlap)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)     # > 129 MB L2
     hbm_peak, peak_kind = _peaks()
     stream = torch.cuda.current_stream(dev)
@@ -327,7 +330,7 @@ def run_ours(args):
             "data": "synthetic (seeded generator; no checkpoint weights)",
             "config": {"workload": f"decode layer H=4096 I=2048 E=256 top_k=8 + FP8 shared, 64-slot cache over a pinned "
                                    f"256-expert bank, Zipf(1.1) routing trace, T={args.T}",
-                       "T": args.T, "copy": args.copy,
+                       "T": args.T, "copy": args.copy, "overlap": overlap,
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "l2": "flushed (256 MB write) before every timed step"},
             "roofline": {"bound": "hbm", "achieved": head["gateup_gbs"], "peak": hbm_peak, "unit": "GB/s",

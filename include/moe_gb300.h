@@ -174,11 +174,13 @@ moe_status moe_copy_missing(moe_cache* cache, const int32_t* h_miss_key,
  * `stream` -- no host synchronisation between ensure and the forward.  The
  * bank must be mapped into the device address space (true for pinned memory
  * on systems with unified addressing); otherwise MOE_ERR_INVALID.  Entries
- * with an out-of-range key or slot are skipped.
+ * with an out-of-range key or slot are skipped.  max_ctas bounds the grid
+ * (0: four CTAs of 256 threads per SM); a small grid leaves the SMs to
+ * kernels that run concurrently, such as moe_expert_forward_overlap.
  * ------------------------------------------------------------------------- */
 moe_status moe_copy_missing_device(moe_cache* cache, const int32_t* d_miss_key,
                                    const int32_t* d_miss_slot, const int32_t* d_miss_count,
-                                   cudaStream_t stream);
+                                   int max_ctas, cudaStream_t stream);
 
 /* Test hook: make the copy with list index `index` of later moe_copy_missing
  * calls fail on the host, as if cudaMemcpyAsync had returned an error
@@ -259,6 +261,33 @@ moe_status moe_expert_forward(const moe_expert_views* v, const uint16_t* x, int 
                               const int32_t* slots, const int8_t* tags, const float* w,
                               uint16_t* y, void* workspace, size_t workspace_bytes,
                               int32_t* d_error, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_expert_forward for a chunk whose missed experts are still being copied
+ * in.  On the pages the copies of a layer's misses take most of its time
+ * ("An elephant through a straw", section "43 graphs, 43 syncs"; "Running
+ * DeepSeek-V4-Flash across four free GPUs", section "What the expert cache
+ * actually does"); here the pairs routed to resident experts, and the shared
+ * expert, are computed while the copies run, and only the pairs whose slot is
+ * on the miss list wait for them.
+ *   slots, w, x, y  as moe_expert_forward (FP4 pool, no tags)
+ *   d_miss_slot     device int32: the chunk's miss list slots (as written by
+ *                   moe_slot_ensure); d_miss_count device int32 [1]: its length
+ *                   (negative counts as 0; at most max_miss entries are read)
+ *   copies_done     event recorded after this chunk's copies (on any stream),
+ *                   or NULL when they are already complete
+ *   workspace       device, >= moe_expert_forward_overlap_workspace bytes,
+ *                   256-byte aligned
+ *   d_error         as moe_expert_forward (cleared by the call)
+ * The result equals moe_expert_forward's for the same slots (one combine over
+ * all pairs in rank order).  Limits: T * k <= 4096, FP4 pool, no tags.
+ * ------------------------------------------------------------------------- */
+size_t moe_expert_forward_overlap_workspace(const moe_expert_views* v, int T, int k);
+moe_status moe_expert_forward_overlap(const moe_expert_views* v, const uint16_t* x, int T, int k,
+                                      const int32_t* slots, const float* w, const int32_t* d_miss_slot,
+                                      const int32_t* d_miss_count, int max_miss, cudaEvent_t copies_done,
+                                      uint16_t* y, void* workspace, size_t workspace_bytes,
+                                      int32_t* d_error, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Grouped-GEMM expert MLP for prefill-sized batches ("Running DeepSeek-V4-

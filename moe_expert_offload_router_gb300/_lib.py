@@ -60,7 +60,7 @@ _SIGS = {
     "moe_slot_ensure": (i32, [vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp]),
     "moe_copy_missing": (i32, [vp, vp, vp, i32, vp, vp, vp]),
     "moe_debug_fail_copy": (i32, [vp, i32]),
-    "moe_copy_missing_device": (i32, [vp, vp, vp, vp, vp]),
+    "moe_copy_missing_device": (i32, [vp, vp, vp, vp, i32, vp]),
     "moe_ladder_classify": (i32, [vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp,
                                   vp, vp, vp, vp, vp, vp, vp, vp]),
     "moe_group_pairs": (i32, [vp, i32, i32, i32, vp, vp, vp, vp]),
@@ -68,6 +68,9 @@ _SIGS = {
     "moe_expert_forward": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, vp,
                                  sz, vp, vp]),
     "moe_dequant_debug": (i32, [C.POINTER(moe_expert_views), i32, i32, i32, vp, vp]),
+    "moe_expert_forward_overlap_workspace": (sz, [C.POINTER(moe_expert_views), i32, i32]),
+    "moe_expert_forward_overlap": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, i32, vp,
+                                         vp, vp, sz, vp, vp]),
     "moe_expert_forward_noalloc": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, vp, vp]),
     "moe_expert_prefill_workspace": (sz, [C.POINTER(moe_expert_views), i32, i32]),
     "moe_expert_prefill": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, sz, vp, vp]),
@@ -210,9 +213,10 @@ def moe_copy_missing(cache: moe_cache, h_miss_key, h_miss_slot, n_miss: int, cop
                                  _s(copy_stream), _e(ready), _e(done)))
 
 
-def moe_copy_missing_device(cache: moe_cache, d_miss_key, d_miss_slot, d_miss_count, stream=None):
+def moe_copy_missing_device(cache: moe_cache, d_miss_key, d_miss_slot, d_miss_count, stream=None,
+                            max_ctas: int = 0):
     _check(_lib.moe_copy_missing_device(cache.handle, _p(d_miss_key), _p(d_miss_slot), _p(d_miss_count),
-                                        _s(stream)))
+                                        max_ctas, _s(stream)))
 
 
 def moe_debug_fail_copy(cache: moe_cache, index: int):
@@ -259,6 +263,19 @@ def moe_expert_forward(views: moe_expert_views, x, slots, tags, w, y, workspace,
     _check(_lib.moe_expert_forward(C.byref(views), _p(x), T, k, _p(slots), _p(tags), _p(w), _p(y),
                                    _p(workspace), workspace.numel() * workspace.element_size(),
                                    _p(d_error), _s(stream)))
+
+
+def moe_expert_forward_overlap_workspace(views: moe_expert_views, T: int, k: int) -> int:
+    return _lib.moe_expert_forward_overlap_workspace(C.byref(views), T, k)
+
+
+def moe_expert_forward_overlap(views: moe_expert_views, x, slots, w, d_miss_slot, d_miss_count, max_miss: int,
+                               copies_done, y, workspace, d_error=None, stream=None):
+    T, k = slots.shape
+    _check(_lib.moe_expert_forward_overlap(C.byref(views), _p(x), T, k, _p(slots), _p(w), _p(d_miss_slot),
+                                           _p(d_miss_count), max_miss, _e(copies_done), _p(y), _p(workspace),
+                                           workspace.numel() * workspace.element_size(), _p(d_error),
+                                           _s(stream)))
 
 
 def moe_expert_forward_noalloc(views: moe_expert_views, x, slots, tags, w, y, d_error=None, stream=None):

@@ -315,7 +315,7 @@ moe_status moe_cache_import(moe_cache* c, const int32_t* h_slot_key, const uint6
 }
 
 moe_status moe_copy_missing_device(moe_cache* c, const int32_t* d_miss_key, const int32_t* d_miss_slot,
-                                   const int32_t* d_miss_count, cudaStream_t stream) {
+                                   const int32_t* d_miss_count, int max_ctas, cudaStream_t stream) {
   clear_error();
   MOE_ARG(c != nullptr, "cache is null");
   MOE_ARG(d_miss_key && d_miss_slot && d_miss_count, "null miss list");
@@ -325,7 +325,9 @@ moe_status moe_copy_missing_device(moe_cache* c, const int32_t* d_miss_key, cons
   MOE_CUDA(cudaGetDevice(&dev));
   MOE_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   ProfScope ps(MOE_K_COPY, stream);
-  copy_missing_kernel<<<sms * 4, 256, 0, stream>>>(c->dev, c->bank_dev, c->d_slots, c->B, d_miss_key, d_miss_slot,
+  MOE_ARG(max_ctas >= 0, "max_ctas < 0");
+  const int grid = max_ctas > 0 && max_ctas < sms * 4 ? max_ctas : sms * 4;
+  copy_missing_kernel<<<grid, 256, 0, stream>>>(c->dev, c->bank_dev, c->d_slots, c->B, d_miss_key, d_miss_slot,
                                                   d_miss_count);
   return check_launch("copy_missing_kernel");
 }

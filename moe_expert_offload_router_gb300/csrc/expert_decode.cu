@@ -588,7 +588,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(FwdArgs a) {
     }
     a.hdr[0] = n;
     a.hdr[1] = ngroups;
-    if (a.err) *a.err = scal[0] ? MOE_ERR_INVALID : 0;
+    if (a.err && scal[0]) atomicCAS(a.err, 0, MOE_ERR_INVALID);  // the caller's call cleared it
   }
 }
 
@@ -1057,27 +1057,19 @@ extern "C" size_t moe_expert_forward_workspace(const moe_expert_views* v, int T,
   return fwd_layout(v, T, k).total;
 }
 
-extern "C" moe_status moe_expert_forward(const moe_expert_views* v, const uint16_t* x, int T, int k,
-                                         const int32_t* slots, const int8_t* tags, const float* w,
-                                         uint16_t* y, void* workspace, size_t workspace_bytes,
-                                         int32_t* d_error, cudaStream_t stream) {
-  clear_error();
-  moe_status st = validate_views(v);
-  if (st != MOE_OK) return st;
-  MOE_ARG(T >= 0 && k >= 1 && k <= 64, "need T >= 0 and 1 <= k <= 64");
-  if (T == 0) return MOE_OK;
-  MOE_ARG(x && slots && w && y && workspace, "null pointer");
-  if ((long long)T * k > kMaxPlanPairs) {
-    // prefill-sized batch: grouped GEMM on the tensor cores (FP4 pool only)
-    MOE_ARG(tags == nullptr, "tags are not supported above %d pairs per call", kMaxPlanPairs);
-    MOE_ARG(((uintptr_t)workspace & 255) == 0, "workspace must be 256-byte aligned");
-    MOE_ARG(((uintptr_t)x & 15) == 0, "x must be 16-byte aligned");
-    return prefill_forward(v, x, T, k, slots, w, y, workspace, workspace_bytes, d_error, stream);
-  }
-  MOE_ARG(((uintptr_t)workspace & 255) == 0, "workspace must be 256-byte aligned");
-  const FwdLayout L = fwd_layout(v, T, k);
-  MOE_ARG(workspace_bytes >= L.total, "workspace too small: %zu < %zu", workspace_bytes, L.total);
-  MOE_ARG(v->fp4_slots || v->int2_slots, "no expert pool");
+namespace moe {
+
+// Options of one pass of the decode forward over a subset of the pairs.
+struct FwdPass {
+  bool shared = true;            // include the shared expert
+  bool combine = true;           // finish with the router-weighted combine into y
+  uint8_t* gemm_bufs = nullptr;  // grouped GEMM activation / h copies (else aliased into o / h)
+};
+
+static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int T, int k, const int32_t* slots,
+                               const int8_t* tags, const float* w, uint16_t* y, uint8_t* base, const FwdLayout& L,
+                               int32_t* d_error, cudaStream_t stream, const FwdPass& pass) {
+  moe_status st;
   FwdArgs a;
   a.H = v->H;
   a.I = v->I;
@@ -1088,7 +1080,7 @@ extern "C" moe_status moe_expert_forward(const moe_expert_views* v, const uint16
   a.n4 = v->fp4_slots ? v->fp4_num_slots : 0;
   a.int2 = v->int2_slots;
   a.n2 = v->int2_slots ? v->int2_num_slots : 0;
-  a.shared = v->shared;
+  a.shared = pass.shared ? v->shared : nullptr;
   a.b4 = fp4_bytes(v->H, v->I);
   a.b2 = int2_bytes(v->H, v->I);
   a.x = x;
@@ -1098,7 +1090,6 @@ extern "C" moe_status moe_expert_forward(const moe_expert_views* v, const uint16
   a.y = y;
   a.err = d_error;
   a.routed_gemm = L.gemm && tags == nullptr && d_error != nullptr;
-  uint8_t* base = (uint8_t*)workspace;
   a.hdr = (int*)(base + L.hdr);
   a.perm = (int*)(base + L.perm);
   a.groups = (Group*)(base + L.groups);
@@ -1110,12 +1101,21 @@ extern "C" moe_status moe_expert_forward(const moe_expert_views* v, const uint16
   if (a.routed_gemm) {
     // FP4 routed pairs on the tensor cores; its 16-bit buffers (two activation
     // copies of P x H each, h of P x I) reuse the routed rows of the fp32 o and
-    // h buffers, which the CUDA-core kernels do not touch in this mode
+    // h buffers, which the CUDA-core kernels do not touch in this mode, unless
+    // the pass brings its own (a second pass must not overwrite the first
+    // pass's outputs in o)
     GgBufs gb;
     gg_carve_index(base + L.gg, T, k, v->fp4_num_slots, &gb);
-    gb.xg = (uint16_t*)a.o;
-    gb.xg16 = (__half*)((uint8_t*)a.o + (size_t)T * k * v->H * 2);
-    gb.hs = (__nv_bfloat16*)a.h;
+    const size_t P = (size_t)T * k;
+    if (pass.gemm_bufs) {
+      gb.xg = (uint16_t*)pass.gemm_bufs;
+      gb.xg16 = (__half*)(pass.gemm_bufs + P * v->H * 2);
+      gb.hs = (__nv_bfloat16*)(pass.gemm_bufs + P * v->H * 4);
+    } else {
+      gb.xg = (uint16_t*)a.o;
+      gb.xg16 = (__half*)((uint8_t*)a.o + P * v->H * 2);
+      gb.hs = (__nv_bfloat16*)a.h;
+    }
     gb.o = a.o;
     if ((st = grouped_gemm_fp4(v, x, T, k, slots, gb, d_error, stream)) != MOE_OK) return st;
   }
@@ -1127,7 +1127,7 @@ extern "C" moe_status moe_expert_forward(const moe_expert_views* v, const uint16
   }
   if ((st = check_launch("plan_kernel")) != MOE_OK) return st;
 
-  const bool gemv = !a.routed_gemm || v->shared != nullptr;
+  const bool gemv = !a.routed_gemm || a.shared != nullptr;
   const long long max_groups = (long long)T * k + (T + kG - 1) / kG + 1;
   const size_t gu_smem = (size_t)kG * v->H * 2 + 2 * kG * 4;
   const long long gu_items = max_groups * ((v->I + kRowsGateUp - 1) / kRowsGateUp);
@@ -1156,7 +1156,136 @@ extern "C" moe_status moe_expert_forward(const moe_expert_views* v, const uint16
     down_kernel<0><<<persistent_grid(down_kernel<0>, dn_smem, dn_items), kFwdThreads, dn_smem, stream>>>(a);
   }
   if ((st = check_launch("down_kernel")) != MOE_OK) return st;
+  if (!pass.combine) return MOE_OK;
 
+  dim3 cg((v->H + 1023) / 1024, T);
+  ProfScope ps(MOE_K_COMBINE, stream);
+  combine_kernel<<<cg, 256, 0, stream>>>(a);
+  return check_launch("combine_kernel");
+}
+
+// Splits the pairs of a chunk by whether their slot is on the miss list:
+// hit[p] keeps the slot of pairs whose expert was resident, miss[p] the slot
+// of pairs whose expert is being copied in (every other entry -1).
+__global__ void __launch_bounds__(1024) split_miss_kernel(const int32_t* slots, int P, const int32_t* miss_slot,
+                                                          const int32_t* miss_count, int max_miss, int S,
+                                                          int32_t* hit, int32_t* miss) {
+  extern __shared__ uint32_t bits[];
+  const int nw = (S + 31) >> 5;
+  for (int i = threadIdx.x; i < nw; i += blockDim.x) bits[i] = 0;
+  __syncthreads();
+  const int n = min(max(*miss_count, 0), max_miss);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int sl = miss_slot[i];
+    if (sl >= 0 && sl < S) atomicOr(&bits[sl >> 5], 1u << (sl & 31));
+  }
+  __syncthreads();
+  for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < P; p += gridDim.x * blockDim.x) {
+    const int sl = slots[p];
+    const bool m = sl >= 0 && sl < S && ((bits[sl >> 5] >> (sl & 31)) & 1u);
+    hit[p] = m ? -1 : sl;
+    miss[p] = m ? sl : -1;
+  }
+}
+
+static size_t overlap_extra(const moe_expert_views* v, int T, int k, const FwdLayout& L) {
+  const size_t P = (size_t)T * k;
+  size_t b = 2 * align256(P * 4);
+  if (L.gemm) b += align256(P * v->H * 4 + P * v->I * 2);
+  return b;
+}
+
+}  // namespace moe
+
+extern "C" moe_status moe_expert_forward(const moe_expert_views* v, const uint16_t* x, int T, int k,
+                                         const int32_t* slots, const int8_t* tags, const float* w,
+                                         uint16_t* y, void* workspace, size_t workspace_bytes,
+                                         int32_t* d_error, cudaStream_t stream) {
+  clear_error();
+  moe_status st = validate_views(v);
+  if (st != MOE_OK) return st;
+  MOE_ARG(T >= 0 && k >= 1 && k <= 64, "need T >= 0 and 1 <= k <= 64");
+  if (T == 0) return MOE_OK;
+  MOE_ARG(x && slots && w && y && workspace, "null pointer");
+  if ((long long)T * k > kMaxPlanPairs) {
+    // prefill-sized batch: grouped GEMM on the tensor cores (FP4 pool only)
+    MOE_ARG(tags == nullptr, "tags are not supported above %d pairs per call", kMaxPlanPairs);
+    MOE_ARG(((uintptr_t)workspace & 255) == 0, "workspace must be 256-byte aligned");
+    MOE_ARG(((uintptr_t)x & 15) == 0, "x must be 16-byte aligned");
+    return prefill_forward(v, x, T, k, slots, w, y, workspace, workspace_bytes, d_error, stream);
+  }
+  MOE_ARG(((uintptr_t)workspace & 255) == 0, "workspace must be 256-byte aligned");
+  const FwdLayout L = fwd_layout(v, T, k);
+  MOE_ARG(workspace_bytes >= L.total, "workspace too small: %zu < %zu", workspace_bytes, L.total);
+  MOE_ARG(v->fp4_slots || v->int2_slots, "no expert pool");
+  if (d_error) MOE_CUDA(cudaMemsetAsync(d_error, 0, sizeof(int32_t), stream));
+  return forward_pass(v, x, T, k, slots, tags, w, y, (uint8_t*)workspace, L, d_error, stream, FwdPass());
+}
+
+extern "C" size_t moe_expert_forward_overlap_workspace(const moe_expert_views* v, int T, int k) {
+  if (!v || T < 0 || k < 1 || (long long)T * k > kMaxPlanPairs) return 0;
+  const FwdLayout L = fwd_layout(v, T, k);
+  return L.total + overlap_extra(v, T, k, L);
+}
+
+extern "C" moe_status moe_expert_forward_overlap(const moe_expert_views* v, const uint16_t* x, int T, int k,
+                                                 const int32_t* slots, const float* w, const int32_t* d_miss_slot,
+                                                 const int32_t* d_miss_count, int max_miss,
+                                                 cudaEvent_t copies_done, uint16_t* y, void* workspace,
+                                                 size_t workspace_bytes, int32_t* d_error, cudaStream_t stream) {
+  clear_error();
+  moe_status st = validate_views(v);
+  if (st != MOE_OK) return st;
+  MOE_ARG(T >= 0 && k >= 1 && k <= 64, "need T >= 0 and 1 <= k <= 64");
+  if (T == 0) return MOE_OK;
+  MOE_ARG((long long)T * k <= kMaxPlanPairs, "T * k = %lld above the %d pairs of one overlapped call",
+          (long long)T * k, kMaxPlanPairs);
+  MOE_ARG(x && slots && w && y && workspace && d_miss_slot && d_miss_count, "null pointer");
+  MOE_ARG(v->fp4_slots != nullptr, "no FP4 pool");
+  MOE_ARG(max_miss >= 0, "max_miss < 0");
+  MOE_ARG(((uintptr_t)workspace & 255) == 0, "workspace must be 256-byte aligned");
+  const FwdLayout L = fwd_layout(v, T, k);
+  const size_t need = L.total + overlap_extra(v, T, k, L);
+  MOE_ARG(workspace_bytes >= need, "workspace too small: %zu < %zu", workspace_bytes, need);
+  uint8_t* base = (uint8_t*)workspace;
+  const size_t P = (size_t)T * k;
+  int32_t* hit = (int32_t*)(base + L.total);
+  int32_t* miss = (int32_t*)(base + L.total + align256(P * 4));
+  uint8_t* gemm_bufs = L.gemm ? base + L.total + 2 * align256(P * 4) : nullptr;
+  if (d_error) MOE_CUDA(cudaMemsetAsync(d_error, 0, sizeof(int32_t), stream));
+  const int S = v->fp4_num_slots;
+  const size_t bits = (size_t)((S + 31) / 32) * 4;
+  if ((st = set_smem(split_miss_kernel, bits)) != MOE_OK) return st;
+  split_miss_kernel<<<(int)((P + 1023) / 1024), 1024, bits, stream>>>(slots, (int)P, d_miss_slot, d_miss_count,
+                                                                      max_miss, S, hit, miss);
+  if ((st = check_launch("split_miss_kernel")) != MOE_OK) return st;
+  // pass 1: pairs whose experts were resident, and the shared expert, while
+  // the misses are still being copied
+  FwdPass p1;
+  p1.combine = false;
+  if ((st = forward_pass(v, x, T, k, hit, nullptr, w, y, base, L, d_error, stream, p1)) != MOE_OK) return st;
+  if (copies_done) MOE_CUDA(cudaStreamWaitEvent(stream, copies_done, 0));
+  // pass 2: the pairs whose experts have just been copied in
+  FwdPass p2;
+  p2.shared = false;
+  p2.combine = false;
+  p2.gemm_bufs = gemm_bufs;
+  if ((st = forward_pass(v, x, T, k, miss, nullptr, w, y, base, L, d_error, stream, p2)) != MOE_OK) return st;
+  // one combine over every pair of the chunk
+  FwdArgs a{};
+  a.H = v->H;
+  a.I = v->I;
+  a.T = T;
+  a.k = k;
+  a.P = (int)P;
+  a.n4 = v->fp4_num_slots;
+  a.n2 = 0;
+  a.shared = v->shared;
+  a.slots = slots;
+  a.tags = nullptr;
+  a.w = w;
+  a.y = y;
+  a.o = (float*)(base + L.o);
   dim3 cg((v->H + 1023) / 1024, T);
   ProfScope ps(MOE_K_COMBINE, stream);
   combine_kernel<<<cg, 256, 0, stream>>>(a);

@@ -781,6 +781,7 @@ moe_status prefill_forward(const moe_expert_views* v, const uint16_t* x, int T, 
   b.xg16 = (__half*)(base + L.xg16);
   b.hs = (__nv_bfloat16*)(base + L.hs);
   b.o = (float*)(base + L.o);
+  MOE_CUDA(cudaMemsetAsync(d_error, 0, sizeof(int32_t), stream));
   moe_status st = grouped_gemm_fp4(v, x, T, k, slots, b, d_error, stream);
   if (st != MOE_OK) return st;
   {

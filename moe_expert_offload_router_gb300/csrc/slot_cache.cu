@@ -591,8 +591,7 @@ moe_status group_pairs_multi(const int32_t* ids, int P, int E, int32_t* offsets,
     if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFuncSetAttribute(group_place_kernel)");
   }
   ProfScope ps(MOE_K_GROUP, stream);
-  cudaError_t e = cudaMemsetAsync(d_error, 0, sizeof(int32_t), stream);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(d_error)");
+  // d_error is cleared by the calling entry point, once per call
   if (nb > 0) group_hist_kernel<<<nb, 1024, smem, stream>>>(ids, P, E, cnt_ws, d_error);
   group_scan_kernel<<<1, 1024, 0, stream>>>(nb, E, cnt_ws, offsets);
   if (nb > 0) group_place_kernel<<<nb, 1024, smem, stream>>>(ids, P, E, cnt_ws, perm);

@@ -20,6 +20,11 @@ batch cannot need more distinct experts than there are slots
 (``min(E, T*k) <= S``) there is a single chunk by construction and the host
 does not wait at all: the status of each layer is checked on the next call
 (or by :meth:`check`).
+
+With ``overlap=True`` (device copy only) the copy kernel runs on a side stream
+with a small grid while ``moe_expert_forward_overlap`` computes the pairs of
+resident experts and the shared expert; only the pairs of missed experts wait
+for the copies.  ``overlap="auto"`` does so from 256 pairs per call.
 """
 from __future__ import annotations
 
@@ -33,9 +38,14 @@ from . import _lib as L
 class DecodeLayerRunner:
     """Buffers and streams for running layers of one model shape on one cache."""
 
+    # overlap="auto" overlaps copies and compute from this many pairs per call:
+    # below it the second forward pass costs more than the short copies hide
+    OVERLAP_MIN_PAIRS = 256
+
     def __init__(self, cache: L.moe_cache, views: L.moe_expert_views, E: int, k: int,
                  T_max: int, device=None, int2_cache: Optional[L.moe_cache] = None,
-                 ladder=None, assume_resident: bool = False, copy: str = "engine"):
+                 ladder=None, assume_resident: bool = False, copy: str = "engine",
+                 overlap=False, copy_ctas: int = 64):
         self.cache, self.views, self.E, self.k, self.T_max = cache, views, E, k, T_max
         self.dev = torch.device(device or "cuda")
         self.c2, self.ladder = int2_cache, ladder
@@ -64,6 +74,13 @@ class DecodeLayerRunner:
         if copy == "device" and ladder is not None:
             raise ValueError("copy='device' serves the FP4-only path")
         self.copy = copy
+        if overlap not in (False, True, "auto"):
+            raise ValueError("overlap must be False, True or 'auto'")
+        if overlap and copy != "device":
+            raise ValueError("overlap needs copy='device'")
+        self.overlap, self.copy_ctas = overlap, copy_ctas
+        self.ws_ov = (torch.empty(L.moe_expert_forward_overlap_workspace(views, T_max, k), dtype=torch.uint8,
+                                  device=dev) if overlap else None)
         self.status_h = torch.zeros(4, dtype=torch.int32, pin_memory=True)
         self.status_ev = torch.cuda.Event()
         self.pending = None   # (layer_id, T) whose status is still to be read
@@ -105,10 +122,21 @@ class DecodeLayerRunner:
             with torch.cuda.stream(stream):
                 self.status_h.copy_(self.info[0:4], non_blocking=True)
             self.status_ev.record(stream)
-            L.moe_copy_missing_device(self.cache, v["keys4"], v["slots4"], v["count4"], stream)
             self.stats["chunks"] += 1
-            L.moe_expert_forward(self.views, x[tb:T], slots[tb:T], None, w[tb:T], y[tb:T], self.ws,
-                                 self.err, stream)
+            if self.overlap is True or (self.overlap == "auto" and T * k >= self.OVERLAP_MIN_PAIRS):
+                # copies on the side stream; resident experts' pairs compute meanwhile
+                self.ready.record(stream)
+                self.copy_stream.wait_event(self.ready)
+                L.moe_copy_missing_device(self.cache, v["keys4"], v["slots4"], v["count4"], self.copy_stream,
+                                          self.copy_ctas)
+                self.done.record(self.copy_stream)
+                L.moe_expert_forward_overlap(self.views, x[tb:T], slots[tb:T], w[tb:T], v["slots4"],
+                                             v["count4"], self.m4, self.done, y[tb:T], self.ws_ov, self.err,
+                                             stream)
+            else:
+                L.moe_copy_missing_device(self.cache, v["keys4"], v["slots4"], v["count4"], stream)
+                L.moe_expert_forward(self.views, x[tb:T], slots[tb:T], None, w[tb:T], y[tb:T], self.ws,
+                                     self.err, stream)
             if single:
                 self.pending = (layer_id, T)
                 return y
