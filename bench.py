@@ -41,6 +41,9 @@ def _args():
     p.add_argument("--workload", default="decode", choices=["decode", "prefill", "ladder", "stack"])
     p.add_argument("--copy", default="device", choices=["engine", "device"],
                    help="miss copies: copy engine after one host sync, or a kernel reading the miss list")
+    p.add_argument("--prefill-experts", type=int, default=0,
+                   help="prefill workload with this many experts (all resident), for profiling a smaller case")
+    p.add_argument("--prefill-tokens", type=int, default=0, help="prefill workload with this many tokens")
     p.add_argument("--no-overlap", action="store_true",
                    help="device copy: run the forward after the copies instead of beside them")
     return p.parse_args()
@@ -396,6 +399,9 @@ def run_other(args):
         return sum(a.elapsed_time(b) for a, b in ev) / n
 
     wl = {"prefill": configs.PREFILL, "ladder": configs.LADDER, "stack": configs.STACK}[args.workload]
+    if args.workload == "prefill" and (args.prefill_experts or args.prefill_tokens):
+        e = args.prefill_experts or wl.E
+        wl = configs.scaled(wl, E=e, S=e, T=args.prefill_tokens or wl.T)
     H, I, E, k, T = wl.H, wl.I, wl.E, wl.k, wl.T
     Bx = M.moe_fp4_expert_bytes(H, I)
     if args.workload in ("prefill", "ladder"):
@@ -441,7 +447,7 @@ def run_other(args):
             gu_tf = 4.0 * P * H * I / (gu_ms / 1e3) / 1e12
             peak, kind = _tensor_peak()
             out["dtype"] = "bf16 MMA (fp32 accumulate) on exactly decoded MXFP4 weights"
-            out["config"] = {"workload": "prefill grouped GEMM H=4096 I=2048 E=256 top_k=6 T=8192, all 256 "
+            out["config"] = {"workload": f"prefill grouped GEMM H=4096 I=2048 E={E} top_k=6 T={T}, all {E} "
                                          "experts resident", "T": T}
             out["grouped_gemm_tflops"] = flops / ((gu_ms + dn_ms) / 1e3) / 1e12
             out["roofline"] = {"bound": "tensor", "achieved": gu_tf, "peak": peak, "unit": "TFLOP/s",
