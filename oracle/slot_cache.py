@@ -107,7 +107,7 @@ class SlotCacheLRU:
             pinned = {self.key_to_slot[key] for key in chunk if self.key_to_slot[key] >= 0}
             misses = [key for key in chunk if self.key_to_slot[key] < 0]
             empties = [s for s in range(self.S) if self.slot_key[s] < 0]
-            untouched = sorted((self.slot_stamp[s], s) for s in range(self.S)
+            untouched = sorted((self._evict_order(s), s) for s in range(self.S)
                                if self.slot_key[s] >= 0 and s not in pinned)
             victims = empties[:len(misses)]
             victims += [s for _, s in untouched[:len(misses) - len(victims)]]
@@ -125,6 +125,7 @@ class SlotCacheLRU:
             if s >= 0:
                 self.slot_stamp[s] = self.clock + q
         self.clock += D
+        self._after_call(chunk)
 
         for t in range(token_begin, end):
             for j in range(rank_lo, rank_hi):
@@ -134,6 +135,14 @@ class SlotCacheLRU:
                 out[t, j] = self.key_to_slot[base + e]
         return out, miss_keys, miss_slots, end
 
+    # -- eviction policy hooks ---------------------------------------------------
+    def _evict_order(self, s):
+        """Sort key of an occupied, unneeded slot among eviction candidates."""
+        return self.slot_stamp[s]
+
+    def _after_call(self, chunk):
+        pass
+
     def mark_empty(self, slots):
         """Roll back: the given slots hold nothing (their copy did not land)."""
         for s in slots:
@@ -141,3 +150,63 @@ class SlotCacheLRU:
             if key >= 0:
                 self.key_to_slot[key] = -1
             self.slot_key[s] = -1
+
+
+class SlotCacheLFU(SlotCacheLRU):
+    """The same slot cache with LFU eviction and frequency decay.
+
+    "An elephant through a straw", section "Rig, model & methodology": the
+    best configuration evicts by LFU with frequency decay, seeded from a
+    routing trace.  The pages give no more; the readings here are:
+
+    * every key (layer * E + expert) has an integer count; each ensure call
+      adds 1 to the count of every distinct key it handles (hits and misses,
+      FETCH and LOOKUP), capped at CAP;
+    * decay halves every count once per decay_calls ensure calls: the epoch of
+      a call is calls // decay_calls (calls counts the ensure calls that
+      returned), and a count last written in epoch e0 is worth
+      count >> min(31, epoch - e0) in epoch `epoch`;
+    * misses take empty slots by ascending index, then the untouched slots
+      with the lowest worth, ties by the older stamp (stamps are unique), so
+      with equal counts the order is exactly LRU's;
+    * seed(counts) sets every key's count (capped) in the current epoch.
+    """
+
+    CAP = (1 << 20) - 1
+
+    def __init__(self, num_slots: int, num_layers: int, num_experts: int, decay_calls: int):
+        super().__init__(num_slots, num_layers, num_experts)
+        if decay_calls < 1:
+            raise ValueError("decay_calls must be >= 1")
+        self.decay_calls = decay_calls
+        self.count = [0] * (num_layers * num_experts)
+        self.count_epoch = [0] * (num_layers * num_experts)
+        self.calls = 0
+
+    def epoch(self):
+        return self.calls // self.decay_calls
+
+    def worth(self, key):
+        return self.count[key] >> min(31, self.epoch() - self.count_epoch[key])
+
+    def seed(self, counts):
+        counts = np.asarray(counts)
+        if counts.shape != (self.L * self.E,) or np.any(counts < 0):
+            raise ValueError("counts must be L*E non-negative integers")
+        e = self.epoch()
+        for key, c in enumerate(counts):
+            self.count[key] = min(int(c), self.CAP)
+            self.count_epoch[key] = e
+
+    def frequency_state(self):
+        return (np.array(self.count, dtype=np.int64), np.array(self.count_epoch, dtype=np.int64), self.calls)
+
+    def _evict_order(self, s):
+        return (self.worth(self.slot_key[s]), self.slot_stamp[s])
+
+    def _after_call(self, chunk):
+        e = self.epoch()
+        for key in chunk:
+            self.count[key] = min(self.worth(key) + 1, self.CAP)
+            self.count_epoch[key] = e
+        self.calls += 1
