@@ -44,6 +44,9 @@ def _args():
     p.add_argument("--prefill-experts", type=int, default=0,
                    help="prefill workload with this many experts (all resident), for profiling a smaller case")
     p.add_argument("--prefill-tokens", type=int, default=0, help="prefill workload with this many tokens")
+    p.add_argument("--evict", default="lru", choices=["lru", "lfu"],
+                   help="decode: slot eviction policy (lfu: counts seeded from a disjoint stretch of the trace)")
+    p.add_argument("--lfu-decay", type=int, default=64, help="decode, lfu: ensure calls per count halving")
     p.add_argument("--no-overlap", action="store_true",
                    help="device copy: run the forward after the copies instead of beside them")
     return p.parse_args()
@@ -199,6 +202,16 @@ def run_ours(args):
     shared = torch.from_numpy(gen.shared_expert(base, 0)).to(dev)
     cache = M.moe_cache(S, 1, E, Bx, slots, bank)
     views = M.make_views(H, I, slots, S, None, 0, shared)
+    if args.evict == "lfu":
+        # seed: how often each expert was routed over 64 steps of the trace that the timed steps do not replay
+        seed = np.zeros(E, dtype=np.int64)
+        for st in range(1000, 1064):
+            ids_s = np.argsort(-gen.router_logits(configs.scaled(base, T=Tmax), 0, st, Tmax), axis=1, kind="stable")
+            np.add.at(seed, np.unique(ids_s[:, :k]), 1)
+        M.moe_cache_set_policy(cache, M.MOE_EVICT_LFU, args.lfu_decay)
+        lfu_seed = seed
+    else:
+        lfu_seed = None
     overlap = "auto" if args.copy == "device" and not args.no_overlap else False
     runner = M.DecodeLayerRunner(cache, views, E, k, Tmax, dev, copy=args.copy, overlap=overlap)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)     # > 129 MB L2
@@ -220,6 +233,8 @@ def run_ours(args):
     def measure(T):
         cache.reset()
         torch.cuda.synchronize()
+        if lfu_seed is not None:
+            M.moe_cache_seed_frequency(cache, lfu_seed)
         lg, xs = inputs(T)
         y = torch.empty((T, H), dtype=torch.int16, device=dev)
         for s in range(args.warmup):
@@ -293,6 +308,9 @@ def run_ours(args):
         y = torch.empty((T, H), dtype=torch.int16, device=dev)
         h_y = torch.empty((T, H), dtype=torch.int16, pin_memory=True)
         cache.reset()
+        if lfu_seed is not None:
+            torch.cuda.synchronize()
+            M.moe_cache_seed_frequency(cache, lfu_seed)
         for s in range(args.warmup):
             d_lg.copy_(h_lg[s], non_blocking=True)
             d_x.copy_(h_x[s], non_blocking=True)
@@ -334,6 +352,8 @@ def run_ours(args):
             "config": {"workload": f"decode layer H=4096 I=2048 E=256 top_k=8 + FP8 shared, 64-slot cache over a pinned "
                                    f"256-expert bank, Zipf(1.1) routing trace, T={args.T}",
                        "T": args.T, "copy": args.copy, "overlap": overlap,
+                       "evict": args.evict if args.evict == "lru" else f"lfu (decay every {args.lfu_decay} calls, "
+                                                                        "seeded from 64 other trace steps)",
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "l2": "flushed (256 MB write) before every timed step"},
             "roofline": {"bound": "hbm", "achieved": head["gateup_gbs"], "peak": hbm_peak, "unit": "GB/s",

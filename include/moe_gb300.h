@@ -168,6 +168,35 @@ moe_status moe_copy_missing(moe_cache* cache, const int32_t* h_miss_key,
                             const int32_t* h_miss_slot, int n_miss, cudaStream_t copy_stream,
                             cudaEvent_t ready, cudaEvent_t done);
 /* ---------------------------------------------------------------------------
+ * Eviction policy.  "An elephant through a straw", section "Rig, model &
+ * methodology": the best configuration evicts by LFU with frequency decay,
+ * seeded from a routing trace.  MOE_EVICT_LRU (the default) is the policy of
+ * "Running DeepSeek-V4-Flash across four free GPUs", section "What the expert
+ * cache actually does".  Under MOE_EVICT_LFU every key has an integer count:
+ * each moe_slot_ensure call adds 1 to the count of every distinct key it
+ * handles (FETCH and LOOKUP, hits and misses), capped at 2^20 - 1; the epoch
+ * of a call is (ensure calls returned so far) / decay_calls, and a count last
+ * written in epoch e0 is worth count >> min(31, epoch - e0); misses take empty
+ * slots by ascending index, then the untouched slots of lowest worth, ties by
+ * the older stamp.  moe_ladder_classify needs LRU caches (MOE_ERR_INVALID).
+ * ------------------------------------------------------------------------- */
+enum { MOE_EVICT_LRU = 0, MOE_EVICT_LFU = 1 };
+
+/* Sets the policy for calls enqueued from now on; decay_calls >= 1 (LFU). */
+moe_status moe_cache_set_policy(moe_cache* cache, int policy, int decay_calls);
+
+/* Seeds the LFU counts from a routing trace: h_counts host uint32 [L*E]
+ * (key = layer * E + expert), capped at 2^20 - 1, written in the current
+ * epoch.  Synchronous (waits for the device). */
+moe_status moe_cache_seed_frequency(moe_cache* cache, const uint32_t* h_counts);
+
+/* Copies the LFU state to the host: counts [L*E], their epochs [L*E] and the
+ * number of ensure calls counted so far.  Synchronous.  moe_cache_reset
+ * clears all three. */
+moe_status moe_cache_export_frequency(moe_cache* cache, uint32_t* h_counts, uint32_t* h_epochs,
+                                      uint64_t* h_calls);
+
+/* ---------------------------------------------------------------------------
  * copy_missing driven from the device: reads the miss list and count written
  * by moe_slot_ensure (device int32 arrays) and copies every miss with GPU
  * loads of the pinned bank over the host-device link, stream-ordered on

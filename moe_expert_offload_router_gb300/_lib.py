@@ -14,6 +14,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
 
 MOE_OK, MOE_ERR_INVALID, MOE_ERR_CAPACITY, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_NOMEM = range(6)
 MOE_FETCH, MOE_LOOKUP, MOE_FETCH_MARK_REST = 0, 1, 2
+MOE_EVICT_LRU, MOE_EVICT_LFU = 0, 1
 MOE_TAG_FP4, MOE_TAG_INT2, MOE_TAG_DROP = 0, 1, 2
 MOE_POOL_FP4, MOE_POOL_INT2, MOE_POOL_SHARED = 0, 1, 2
 MOE_W1, MOE_W3, MOE_W2 = 0, 1, 2
@@ -61,6 +62,9 @@ _SIGS = {
     "moe_copy_missing": (i32, [vp, vp, vp, i32, vp, vp, vp]),
     "moe_debug_fail_copy": (i32, [vp, i32]),
     "moe_copy_missing_device": (i32, [vp, vp, vp, vp, i32, vp]),
+    "moe_cache_set_policy": (i32, [vp, i32, i32]),
+    "moe_cache_seed_frequency": (i32, [vp, vp]),
+    "moe_cache_export_frequency": (i32, [vp, vp, vp, vp]),
     "moe_ladder_classify": (i32, [vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp,
                                   vp, vp, vp, vp, vp, vp, vp, vp]),
     "moe_group_pairs": (i32, [vp, i32, i32, i32, vp, vp, vp, vp]),
@@ -191,6 +195,30 @@ class moe_cache:
         a, b, c, d = vp(), vp(), vp(), vp()
         _check(_lib.moe_cache_state(self.handle, C.byref(a), C.byref(b), C.byref(c), C.byref(d)))
         return a.value, b.value, c.value, d.value
+
+
+def moe_cache_set_policy(cache: moe_cache, policy: int, decay_calls: int = 1):
+    _check(_lib.moe_cache_set_policy(cache.handle, policy, decay_calls))
+
+
+def moe_cache_seed_frequency(cache: moe_cache, counts):
+    """counts: host array of L*E non-negative integers (key = layer * E + expert)."""
+    import numpy as np
+    c = np.ascontiguousarray(np.minimum(np.asarray(counts, dtype=np.int64), 2 ** 32 - 1), dtype=np.uint32)
+    if c.shape != (cache.L * cache.E,):
+        raise ValueError("counts must have L*E entries")
+    _check(_lib.moe_cache_seed_frequency(cache.handle, c.ctypes.data))
+
+
+def moe_cache_export_frequency(cache: moe_cache):
+    """(counts [L*E] uint32, epochs [L*E] uint32, calls) of the LFU state."""
+    import numpy as np
+    n = cache.L * cache.E
+    cnt = np.empty(n, dtype=np.uint32)
+    ep = np.empty(n, dtype=np.uint32)
+    calls = np.empty(1, dtype=np.uint64)
+    _check(_lib.moe_cache_export_frequency(cache.handle, cnt.ctypes.data, ep.ctypes.data, calls.ctypes.data))
+    return cnt, ep, int(calls[0])
 
 
 def moe_slot_ensure(cache: moe_cache, layer_id: int, ids, slots_out, rank_lo: int, rank_hi: int,

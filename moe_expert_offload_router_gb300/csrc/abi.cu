@@ -94,7 +94,14 @@ __global__ void cache_reset_kernel(CacheDev c) {
     c.slot_key[i] = -1;
     c.slot_stamp[i] = 0;
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) *c.clock = 0;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    c.freq[i] = 0;
+    c.freq_epoch[i] = 0;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *c.clock = 0;
+    *c.calls = 0;
+  }
 }
 
 __global__ void cache_mark_empty_kernel(CacheDev c, int slot) {
@@ -204,7 +211,7 @@ moe_status moe_cache_create(int num_slots, int num_layers, int num_experts, size
   int dev = 0;
   MOE_CUDA(cudaGetDevice(&dev));
   const size_t S = (size_t)num_slots, K = (size_t)num_layers * num_experts;
-  const size_t bytes = S * 8 + S * 4 + K * 4 + 8 + 64;
+  const size_t bytes = S * 8 + 8 + 8 + S * 4 + K * 4 + K * 8 + 64;
   void* state = nullptr;
   cudaError_t e = cudaMalloc(&state, bytes);
   if (e != cudaSuccess) return fail(MOE_ERR_NOMEM, "cudaMalloc of %zu bytes of cache state: %s", bytes,
@@ -235,6 +242,14 @@ moe_status moe_cache_create(int num_slots, int num_layers, int num_experts, size
   c->dev.slot_key = (int32_t*)p;
   p += S * 4;
   c->dev.key_to_slot = (int32_t*)p;
+  p += K * 4;
+  c->dev.freq = (uint32_t*)p;
+  p += K * 4;
+  c->dev.freq_epoch = (uint32_t*)p;
+  p += K * 4;
+  c->dev.calls = (uint64_t*)(((uintptr_t)p + 7) & ~(uintptr_t)7);
+  c->dev.policy = MOE_EVICT_LRU;
+  c->dev.decay_calls = 1;
   c->dev.S = num_slots;
   c->dev.L = num_layers;
   c->dev.E = num_experts;
@@ -311,6 +326,42 @@ moe_status moe_cache_import(moe_cache* c, const int32_t* h_slot_key, const uint6
   MOE_CUDA(cudaMemcpy(c->dev.slot_stamp, h_slot_stamp, (size_t)c->S * 8, cudaMemcpyHostToDevice));
   MOE_CUDA(cudaMemcpy(c->dev.key_to_slot, k2s.data(), (size_t)K * 4, cudaMemcpyHostToDevice));
   MOE_CUDA(cudaMemcpy(c->dev.clock, &clock, 8, cudaMemcpyHostToDevice));
+  return MOE_OK;
+}
+
+moe_status moe_cache_set_policy(moe_cache* c, int policy, int decay_calls) {
+  clear_error();
+  MOE_ARG(c != nullptr, "cache is null");
+  MOE_ARG(policy == MOE_EVICT_LRU || policy == MOE_EVICT_LFU, "policy must be MOE_EVICT_LRU or MOE_EVICT_LFU");
+  MOE_ARG(decay_calls >= 1, "decay_calls must be >= 1");
+  c->dev.policy = policy;
+  c->dev.decay_calls = decay_calls;
+  return MOE_OK;
+}
+
+moe_status moe_cache_seed_frequency(moe_cache* c, const uint32_t* h_counts) {
+  clear_error();
+  MOE_ARG(c != nullptr && h_counts != nullptr, "null argument");
+  const size_t K = (size_t)c->L * c->E;
+  MOE_CUDA(cudaDeviceSynchronize());
+  uint64_t calls = 0;
+  MOE_CUDA(cudaMemcpy(&calls, c->dev.calls, 8, cudaMemcpyDeviceToHost));
+  const uint32_t epoch = (uint32_t)(calls / (uint64_t)c->dev.decay_calls);
+  std::vector<uint32_t> cnt(K), ep(K, epoch);
+  for (size_t i = 0; i < K; ++i) cnt[i] = h_counts[i] < kFreqCap ? h_counts[i] : kFreqCap;
+  MOE_CUDA(cudaMemcpy(c->dev.freq, cnt.data(), K * 4, cudaMemcpyHostToDevice));
+  MOE_CUDA(cudaMemcpy(c->dev.freq_epoch, ep.data(), K * 4, cudaMemcpyHostToDevice));
+  return MOE_OK;
+}
+
+moe_status moe_cache_export_frequency(moe_cache* c, uint32_t* h_counts, uint32_t* h_epochs, uint64_t* h_calls) {
+  clear_error();
+  MOE_ARG(c != nullptr && h_counts && h_epochs && h_calls, "null argument");
+  const size_t K = (size_t)c->L * c->E;
+  MOE_CUDA(cudaDeviceSynchronize());
+  MOE_CUDA(cudaMemcpy(h_counts, c->dev.freq, K * 4, cudaMemcpyDeviceToHost));
+  MOE_CUDA(cudaMemcpy(h_epochs, c->dev.freq_epoch, K * 4, cudaMemcpyDeviceToHost));
+  MOE_CUDA(cudaMemcpy(h_calls, c->dev.calls, 8, cudaMemcpyDeviceToHost));
   return MOE_OK;
 }
 

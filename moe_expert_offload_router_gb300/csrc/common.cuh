@@ -12,6 +12,9 @@
 
 namespace moe {
 
+constexpr uint32_t kFreqCap = (1u << 20) - 1;  // LFU count cap (20 bits of the eviction order key)
+
+
 moe_status fail(moe_status s, const char* fmt, ...);
 moe_status cuda_fail(cudaError_t e, const char* what);
 void clear_error();
@@ -46,7 +49,12 @@ struct CacheDev {
   uint64_t* slot_stamp;  // [S] recency stamp (unique among occupied slots)
   int32_t* key_to_slot;  // [L*E] slot of a key, -1 = not resident
   uint64_t* clock;       // [1]
+  uint32_t* freq;        // [L*E] LFU count of a key
+  uint32_t* freq_epoch;  // [L*E] epoch in which the count was last written
+  uint64_t* calls;       // [1] ensure calls that returned (LFU epochs)
   int S, L, E;
+  int policy;            // MOE_EVICT_LRU or MOE_EVICT_LFU
+  int decay_calls;       // LFU: counts halve once per this many calls
 };
 
 }  // namespace moe

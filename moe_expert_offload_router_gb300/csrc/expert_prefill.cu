@@ -392,8 +392,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         q[mt][0] = *reinterpret_cast<const uint4*>(src);
         q[mt][1] = *reinterpret_cast<const uint4*>(src + 16);
       }
-      mbar_arrive(&rawe[rs]);
-      if (rnd > 0 && !(ok = mbar_wait_fast(&empty[s], (rnd - 1) & 1, a.err))) break;
+      if (rnd > 0 && !(ok = mbar_wait_fast(&empty[s], (rnd - 1) & 1, a.err))) {
+        mbar_arrive(&rawe[rs]);
+        break;
+      }
 #pragma unroll
       for (int mt = 0; mt < kPfMT; ++mt) {
         uint8_t* arow = sm + C::kOffA + s * kAStage + mt * kATile + r * 128;
@@ -426,6 +428,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(&full[s]);
+      // the raw stage is released only now: its codes have been used, so the
+      // shared-memory loads are complete before the next TMA can overwrite it
+      // (an arrive right after issuing the loads let the refill overtake them)
+      mbar_arrive(&rawe[rs]);
     }
   }
 

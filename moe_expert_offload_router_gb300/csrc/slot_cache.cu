@@ -179,6 +179,18 @@ __device__ int chunk_tokens(const PassSmem& s, const Entries& en, int dtotal, in
   return n_rel;
 }
 
+// Eviction order of an occupied slot among the candidates (smaller goes
+// first): its stamp under LRU; under LFU the worth of its key (count halved
+// once per epoch since it was written) above the stamp's low 44 bits, so equal
+// worths fall back to the stamp order.
+__device__ __forceinline__ uint64_t evict_order(const CacheDev& c, int slot, uint32_t epoch) {
+  const uint64_t st = c.slot_stamp[slot];
+  if (c.policy != MOE_EVICT_LFU) return st;
+  const int key = c.slot_key[slot];
+  const uint32_t sh = min(31u, epoch - c.freq_epoch[key]);
+  return ((uint64_t)(c.freq[key] >> sh) << 44) | (st & ((1ull << 44) - 1));
+}
+
 // Steps 3-5 for the D distinct experts found by analyze(): resolve hits,
 // place misses (FETCH), stamp.  Leaves the final slot (or -1) of every
 // first-appearance order in slot_of_ord.  Returns the number of misses.
@@ -186,6 +198,9 @@ __device__ int resolve(const PassSmem& s, CacheDev c, int layer, int D, int mode
                        int32_t* miss_key, int32_t* miss_slot) {
   const int tid = threadIdx.x, NT = blockDim.x;
   const int E = s.E;
+  const bool lfu = c.policy == MOE_EVICT_LFU;
+  const unsigned long long calls0 = lfu ? *c.calls : 0ull;  // read by all before thread 0 writes it back
+  const uint32_t epoch = lfu ? (uint32_t)(calls0 / (unsigned long long)c.decay_calls) : 0u;
   if (tid == 0) *s.clock0 = *c.clock;
   for (int q = tid; q < D; q += NT) s.slot_of_ord[q] = c.key_to_slot[layer * E + s.key_by_ord[q]];
   __syncthreads();
@@ -227,7 +242,7 @@ __device__ int resolve(const PassSmem& s, CacheDev c, int layer, int D, int mode
             const int key = c.slot_key[i];
             const bool pinned = key >= 0 && key / E == layer && s.ord_of[key % E] < D;
             if (key >= 0 && !pinned) {
-              s.cand_stamp[cpos] = c.slot_stamp[i];
+              s.cand_stamp[cpos] = evict_order(c, i, epoch);
               s.cand_slot[cpos] = i;
               ++cpos;
             }
@@ -236,13 +251,14 @@ __device__ int resolve(const PassSmem& s, CacheDev c, int layer, int D, int mode
           // r_lru-th smallest stamp by binary search over stamp values, then
           // keep exactly the r_lru candidates at or below it (stamps are unique)
           unsigned long long lo = 0, hi = *s.clock0;
+          if (lfu) hi |= (unsigned long long)kFreqCap << 44;
           while (lo < hi) {
             const unsigned long long mid = lo + (hi - lo) / 2;
             int cnt = 0;
             for (int i = s0; i < s1; ++i) {
               const int key = c.slot_key[i];
               const bool pinned = key >= 0 && key / E == layer && s.ord_of[key % E] < D;
-              cnt += (key >= 0 && !pinned && c.slot_stamp[i] <= mid);
+              cnt += (key >= 0 && !pinned && evict_order(c, i, epoch) <= mid);
             }
             const int tot = block_sum(cnt, s.ws);
             if (tot >= r_lru)
@@ -254,14 +270,14 @@ __device__ int resolve(const PassSmem& s, CacheDev c, int layer, int D, int mode
           for (int i = s0; i < s1; ++i) {
             const int key = c.slot_key[i];
             const bool pinned = key >= 0 && key / E == layer && s.ord_of[key % E] < D;
-            nk += (key >= 0 && !pinned && c.slot_stamp[i] <= lo);
+            nk += (key >= 0 && !pinned && evict_order(c, i, epoch) <= lo);
           }
           int kpos = block_exclusive_scan(nk, s.ws, &C);
           for (int i = s0; i < s1; ++i) {
             const int key = c.slot_key[i];
             const bool pinned = key >= 0 && key / E == layer && s.ord_of[key % E] < D;
-            if (key >= 0 && !pinned && c.slot_stamp[i] <= lo) {
-              s.cand_stamp[kpos] = c.slot_stamp[i];
+            if (key >= 0 && !pinned && evict_order(c, i, epoch) <= lo) {
+              s.cand_stamp[kpos] = evict_order(c, i, epoch);
               s.cand_slot[kpos] = i;
               ++kpos;
             }
@@ -296,9 +312,19 @@ __device__ int resolve(const PassSmem& s, CacheDev c, int layer, int D, int mode
   for (int q = tid; q < D; q += NT) {
     const int sl = s.slot_of_ord[q];
     if (sl >= 0) c.slot_stamp[sl] = clk + (unsigned long long)q;
+    if (lfu) {
+      // every distinct key of the call, resident or not: worth + 1, capped
+      const int key = layer * E + s.key_by_ord[q];
+      const uint32_t sh = min(31u, epoch - c.freq_epoch[key]);
+      c.freq[key] = min((c.freq[key] >> sh) + 1u, kFreqCap);
+      c.freq_epoch[key] = epoch;
+    }
   }
   __syncthreads();
-  if (tid == 0) *c.clock = clk + (unsigned long long)D;
+  if (tid == 0) {
+    *c.clock = clk + (unsigned long long)D;
+    if (lfu) *c.calls = calls0 + 1;
+  }
   return M;
 }
 
@@ -653,6 +679,7 @@ extern "C" moe_status moe_ladder_classify(moe_cache* c4, moe_cache* c2, int laye
   clear_error();
   MOE_ARG(c4 && c2, "cache is null");
   MOE_ARG(c4->E == c2->E && c4->L == c2->L, "the two caches must have the same L and E");
+  MOE_ARG(c4->dev.policy == MOE_EVICT_LRU && c2->dev.policy == MOE_EVICT_LRU, "the ladder needs LRU caches");
   MOE_ARG(layer_id >= 0 && layer_id < c4->L, "layer_id out of range");
   MOE_ARG(T >= 0 && k >= 1 && k <= 64, "need T >= 0 and 1 <= k <= 64");
   MOE_ARG(1 <= a && a <= b && b <= k, "need 1 <= a <= b <= k");
