@@ -439,7 +439,8 @@ def run_other(args):
             s2 = torch.empty(wl.S2 * B2, dtype=torch.uint8, device=dev)
             c2 = M.moe_cache(wl.S2, 1, E, B2, s2, bank2)
         views = M.make_views(H, I, slots, wl.S, s2, wl.S2 if s2 is not None else 0, None)
-        runner = M.DecodeLayerRunner(cache, views, E, k, T, dev, int2_cache=c2, ladder=wl.ladder)
+        runner = M.DecodeLayerRunner(cache, views, E, k, T, dev, int2_cache=c2, ladder=wl.ladder,
+                                     copy=args.copy)
         n = args.warmup + args.steps
         nsteps = max(wl.steps, 1)
         lg = [torch.from_numpy(gen.router_logits(wl, 0, s % nsteps, T)).to(dev) for s in range(n)]
@@ -448,11 +449,13 @@ def run_other(args):
         for s in range(args.warmup):
             runner.run(0, lg[s], xs[s], y)
         torch.cuda.synchronize()
+        runner.check()
         m0 = runner.stats["misses"]
         M.moe_profile_enable(True)
         clocks.start()
         ms = timed(lambda i: runner.run(0, lg[args.warmup + i], xs[args.warmup + i], y), args.steps)
         ck = clocks.stop()
+        runner.check()
         kt = {M.KERNEL_NAMES[kid]: M.moe_profile_query(kid) for kid in range(M.MOE_K_COUNT)}
         M.moe_profile_enable(False)
         out.update({"value": T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "clocks": ck,

@@ -25,6 +25,10 @@ With ``overlap=True`` (device copy only) the copy kernel runs on a side stream
 with a small grid while ``moe_expert_forward_overlap`` computes the pairs of
 resident experts and the shared expert; only the pairs of missed experts wait
 for the copies.  ``overlap="auto"`` does so from 256 pairs per call.
+
+The precision ladder takes ``copy="device"`` too: when a batch cannot need more
+distinct experts of either rank range than its pool has slots, classify, the
+copies of both pools and the forward are enqueued without a host wait.
 """
 from __future__ import annotations
 
@@ -71,8 +75,8 @@ class DecodeLayerRunner:
         self.done = torch.cuda.Event()
         if copy not in ("engine", "device"):
             raise ValueError("copy must be 'engine' or 'device'")
-        if copy == "device" and ladder is not None:
-            raise ValueError("copy='device' serves the FP4-only path")
+        if copy == "device" and ladder is not None and overlap:
+            raise ValueError("the ladder takes copy='device' without overlap")
         self.copy = copy
         if overlap not in (False, True, "auto"):
             raise ValueError("overlap must be False, True or 'auto'")
@@ -104,10 +108,11 @@ class DecodeLayerRunner:
         self.pending = None
         self.status_ev.synchronize()
         n4, done = int(self.status_h[0]), int(self.status_h[1])
-        if n4 < 0:
-            raise L.MoeError(-n4, f"slot ensure failed on the device (layer {layer_id})")
-        self.stats["misses"] += n4
-        self.stats["bytes_copied"] += n4 * self.cache.B
+        n2 = int(self.status_h[2]) if self.ladder is not None else 0
+        if n4 < 0 or n2 < 0:
+            raise L.MoeError(-min(n4, n2), f"slot ensure failed on the device (layer {layer_id})")
+        self.stats["misses"] += n4 + n2
+        self.stats["bytes_copied"] += n4 * self.cache.B + (n2 * self.c2.B if n2 else 0)
         if done != T:
             raise L.MoeError(L.MOE_ERR_CAPACITY, f"layer {layer_id}: single chunk expected, got {done}/{T}")
 
@@ -149,6 +154,28 @@ class DecodeLayerRunner:
             tb = done
         return y
 
+    def _ladder_single_chunk(self, T):
+        a, b = self.ladder
+        return (min(self.E, T * a) <= self.cache.S and min(self.E, T * (b - a)) <= self.c2.S)
+
+    def _run_device_ladder(self, layer_id, T, ids, w, slots, x, y, stream):
+        """Ladder chunk that fits both pools by construction: classify, both
+        pools' misses copied by kernels, forward; no host wait."""
+        v = self._views(T)
+        a, b = self.ladder
+        tags, wuse = self.tags[:T], self.w2[:T]
+        L.moe_ladder_classify(self.cache, self.c2, layer_id, ids, w, a, b, 0, slots, tags, wuse, v["keys4"],
+                              v["slots4"], v["count4"], v["keys2"], v["slots2"], v["count2"], v["done"], stream)
+        with torch.cuda.stream(stream):
+            self.status_h.copy_(self.info[0:4], non_blocking=True)
+        self.status_ev.record(stream)
+        L.moe_copy_missing_device(self.cache, v["keys4"], v["slots4"], v["count4"], stream)
+        L.moe_copy_missing_device(self.c2, v["keys2"], v["slots2"], v["count2"], stream)
+        self.stats["chunks"] += 1
+        L.moe_expert_forward(self.views, x, slots, tags, wuse, y, self.ws, self.err, stream)
+        self.pending = (layer_id, T)
+        return y
+
     def run(self, layer_id: int, logits, x, y, stream=None):
         """y[T, H] (bf16 bits) = the MoE layer applied to x[T, H] with router logits [T, E]."""
         T = logits.shape[0]
@@ -159,8 +186,12 @@ class DecodeLayerRunner:
         ids, w, slots = self.ids[:T], self.w[:T], self.slots[:T]
         L.moe_router_topk(logits, k, True, ids, w, stream)
         if self.copy == "device" and not self.assume_resident:
-            self.stats["calls"] += 1
-            return self._run_device(layer_id, T, ids, w, slots, x, y, stream)
+            if self.ladder is None:
+                self.stats["calls"] += 1
+                return self._run_device(layer_id, T, ids, w, slots, x, y, stream)
+            if self._ladder_single_chunk(T):
+                self.stats["calls"] += 1
+                return self._run_device_ladder(layer_id, T, ids, w, slots, x, y, stream)
         v = self._views(T)
         tb = 0
         self.stats["calls"] += 1

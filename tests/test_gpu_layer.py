@@ -152,3 +152,46 @@ def test_stack_all_resident_no_sync():
         M.moe_rms_carry(y, 1e-6, nxt)
         xin = nxt
     assert runner.stats["misses"] == 0
+
+
+def test_layer_ladder_device_copy():
+    # the ladder chunk fits both pools by construction (T*a <= S4, T*(b-a) <= S2):
+    # classify, both pools' copies by kernels and the forward run with no host wait
+    M = load_lib()
+    wl = configs.scaled(configs.LADDER, H=256, I=128, T=8, S=20, S2=30)
+    bank4, B4 = pinned_fp4_bank(wl, (0,))
+    B2 = M.moe_int2_expert_bytes(wl.H, wl.I)
+    bank2 = torch.empty(wl.E * B2, dtype=torch.uint8, pin_memory=True)
+    for e in range(wl.E):
+        bank2[e * B2:(e + 1) * B2] = torch.from_numpy(gen.int2_expert(wl, 0, e))
+    s4 = torch.empty(wl.S * B4, dtype=torch.uint8, device="cuda")
+    s2 = torch.empty(wl.S2 * B2, dtype=torch.uint8, device="cuda")
+    c4 = M.moe_cache(wl.S, 1, wl.E, B4, s4, bank4)
+    c2 = M.moe_cache(wl.S2, 1, wl.E, B2, s2, bank2)
+    views = M.make_views(wl.H, wl.I, s4, wl.S, s2, wl.S2, None)
+    runner = M.DecodeLayerRunner(c4, views, wl.E, wl.k, wl.T, int2_cache=c2, ladder=wl.ladder, copy="device")
+    assert runner._ladder_single_chunk(wl.T)
+    r4, r2 = SlotCacheLRU(wl.S, 1, wl.E), SlotCacheLRU(wl.S2, 1, wl.E)
+    b4, b2 = bank4.numpy(), bank2.numpy()
+
+    def dec(e, tag):
+        if tag == 0:
+            return F.decode_fp4_expert(b4[e * B4:(e + 1) * B4], wl.H, wl.I)
+        return F.decode_int2_expert(b2[e * B2:(e + 1) * B2], wl.H, wl.I)
+
+    for step in range(10):
+        lg = gen.router_logits(wl, 0, step)
+        x = gen.activations(wl, 0, step)
+        y = torch.empty((wl.T, wl.H), dtype=torch.int16, device="cuda")
+        runner.run(0, torch.from_numpy(lg).cuda(), torch.from_numpy(x.view(np.int16)).cuda(), y)
+        torch.cuda.synchronize()
+        ids, w = router_topk(lg, wl.k)
+        w32 = w.astype(np.float32).astype(np.float64)
+        _, tg, wo, _, _, end = ladder_classify(r4, r2, 0, ids, w32, *wl.ladder, 0)
+        assert end == wl.T
+        ref = moe_layer(x, np.where(tg == 2, -1, ids), wo, dec, tags=tg)
+        assert bf16_rel_err(y.cpu().numpy(), ref) <= TOL
+        assert np.array_equal(c4.export()[0], r4.state()[0])
+        assert np.array_equal(c2.export()[0], r2.state()[0])
+    runner.check()
+    assert runner.stats["misses"] > 0 and runner.stats["chunks"] == runner.stats["calls"]
