@@ -40,7 +40,7 @@ def test_prefill_full_size_repeatable():
         assert torch.equal(y, outs[0])
 
 
-@pytest.mark.parametrize("T", [16, 64])
+@pytest.mark.parametrize("T", [1, 2, 16, 64])
 def test_decode_forward_repeatable(T):
     M = load_lib()
     wl = configs.DECODE

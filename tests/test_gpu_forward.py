@@ -154,7 +154,7 @@ def test_forward_reports_bad_slot():
     assert err == M.MOE_ERR_INVALID
 
 
-@pytest.mark.parametrize("T", [1, 4, 16, 64])
+@pytest.mark.parametrize("T", [1, 2, 4, 16, 64])
 def test_forward_decode_full_size_sampled(T):
     M = load_lib()
     wl = configs.DECODE
