@@ -210,3 +210,64 @@ class SlotCacheLFU(SlotCacheLRU):
             self.count[key] = min(self.worth(key) + 1, self.CAP)
             self.count_epoch[key] = e
         self.calls += 1
+
+
+class StagingRing:
+    """Staging ring for predicted experts, beside a slot cache.
+
+    "An elephant through a straw", section "Guessing the router two layers
+    ahead": predicted experts are copied into a small round-robin region
+    appended to the same slot buffer, so a guess never evicts a resident
+    expert; a wrong guess is overwritten by a later prediction, a right one is
+    already in GPU memory when the router asks for it.  Readings:
+
+    * the ring has R slots, numbered S .. S+R-1 in the slot buffer;
+    * prefetch(layer, experts) takes the predicted experts in order, skips
+      negative ids, ids already seen in this call, keys resident in the cache
+      and keys already staged; each remaining key takes ring position
+      pos % R (pos then advances), displacing the key staged there; the call
+      returns the (key, slot) copy list;
+    * the cache's own state is never changed by prefetching; when ensure
+      later lists a staged key as a miss, the miss is filled from its staging
+      slot instead of the host bank (same bytes), and the key stays staged.
+    """
+
+    def __init__(self, cache: SlotCacheLRU, num_stage: int):
+        if num_stage < 1:
+            raise ValueError("num_stage must be >= 1")
+        self.c = cache
+        self.R = num_stage
+        self.stage_key = [-1] * num_stage
+        self.pos = 0
+
+    def staged_slot(self, key):
+        for j, kk in enumerate(self.stage_key):
+            if kk == key:
+                return self.c.S + j
+        return -1
+
+    def prefetch(self, layer: int, experts):
+        c = self.c
+        if not (0 <= layer < c.L):
+            raise ValueError("layer out of range")
+        out, seen = [], set()
+        for e in experts:
+            e = int(e)
+            if e < 0 or e in seen:
+                continue
+            if e >= c.E:
+                raise ValueError("expert id >= E")
+            seen.add(e)
+            key = layer * c.E + e
+            if c.key_to_slot[key] >= 0 or self.staged_slot(key) >= 0:
+                continue
+            j = self.pos % self.R
+            self.pos += 1
+            self.stage_key[j] = key
+            out.append((key, c.S + j))
+        return out
+
+    def miss_source(self, key):
+        """Where a miss of `key` is copied from: ('stage', slot) or ('bank', key)."""
+        s = self.staged_slot(key)
+        return ("stage", s) if s >= 0 else ("bank", key)
