@@ -226,7 +226,8 @@ class StagingRing:
       negative ids, ids already seen in this call, keys resident in the cache
       and keys already staged; each remaining key takes ring position
       pos % R (pos then advances), displacing the key staged there; the call
-      returns the (key, slot) copy list;
+      returns the (key, slot) copy list, without the guesses that a later
+      guess of the same call displaced (only the last R assignments);
     * the cache's own state is never changed by prefetching; when ensure
       later lists a staged key as a miss, the miss is filled from its staging
       slot instead of the host bank (same bytes), and the key stays staged.
@@ -265,7 +266,7 @@ class StagingRing:
             self.pos += 1
             self.stage_key[j] = key
             out.append((key, c.S + j))
-        return out
+        return out[-self.R:]
 
     def miss_source(self, key):
         """Where a miss of `key` is copied from: ('stage', slot) or ('bank', key)."""

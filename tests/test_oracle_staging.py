@@ -23,6 +23,20 @@ def test_hand_worked_ring():
     assert [r.miss_source(k) for k in mk] == [("stage", 3), ("stage", 4)]
 
 
+def test_ring_wrap_within_one_call():
+    # more new guesses than ring slots: a guess displaced by a later guess of the
+    # same call is not copied (worked by hand: ring of 3, state [7, 5, 6], pos 4)
+    c = SlotCacheLRU(2, 1, 8)
+    r = StagingRing(c, 3)
+    c.ensure(0, np.array([[0, 1]]), 0, 2, FETCH, 0)
+    r.prefetch(0, [4, 5, 6])
+    r.prefetch(0, [7])
+    assert r.stage_key == [7, 5, 6] and r.pos == 4
+    # 2 -> ring 1 (slot 3), 3 -> ring 2 (slot 4), 4 -> ring 0 (slot 2), 5 -> ring 1 (slot 3, displacing 2)
+    assert r.prefetch(0, [2, 3, 4, 5]) == [(3, 4), (4, 2), (5, 3)]
+    assert r.stage_key == [4, 5, 3] and r.pos == 8
+
+
 @pytest.mark.parametrize("seed", [0, 1])
 def test_prefetch_never_changes_cache_state(seed):
     wl = configs.scaled(configs.DECODE, T=4, seed=seed + 10)
