@@ -197,6 +197,43 @@ moe_status moe_cache_export_frequency(moe_cache* cache, uint32_t* h_counts, uint
                                       uint64_t* h_calls);
 
 /* ---------------------------------------------------------------------------
+ * Staging ring for predicted experts.  "An elephant through a straw", section
+ * "Guessing the router two layers ahead": predicted experts are copied into a
+ * small round-robin region appended to the slot buffer, so a guess never
+ * evicts a resident expert; a wrong guess is overwritten by a later
+ * prediction; a right one is in GPU memory when the router asks for it.
+ *
+ * moe_cache_set_staging(cache, R): ring slots S .. S+R-1 of the caller's slot
+ * buffer (which must then hold S + R experts); allocates and clears the ring
+ * state (0 removes it).  Synchronous.
+ *
+ * moe_prefetch(cache, layer, d_experts[n], ...): device int32 expert ids of
+ * `layer`, in order.  Negative ids, ids repeated in the call, keys resident in
+ * the cache and keys already staged are skipped; every other key takes ring
+ * position pos % R (pos advances), displacing the key staged there.  Writes
+ * the copy list (key, ring slot) of the guesses that still hold their slot
+ * at the end of the call (the last min(new keys, R)) and its length to the
+ * device arrays d_list_* (room for min(n, R) entries), to be copied by
+ * moe_copy_missing_device.  An id >= E
+ * makes the call a no-op with *d_list_count = -MOE_ERR_INVALID.  The cache's
+ * own state (slots, stamps, counts) is never changed.
+ *
+ * When moe_slot_ensure later lists a staged key as a miss, moe_copy_missing_
+ * device fills the cache slot from the key's staging slot (a device copy)
+ * instead of the host bank.  Order the copies on one stream (or with events)
+ * so that a staging slot's prefetch copy has landed before it is read and is
+ * not overwritten while it is read.  moe_copy_missing (host lists, copy
+ * engine) always copies from the bank.  moe_cache_reset clears the ring.
+ * ------------------------------------------------------------------------- */
+moe_status moe_cache_set_staging(moe_cache* cache, int num_stage);
+moe_status moe_prefetch(moe_cache* cache, int layer_id, const int32_t* d_experts, int n,
+                        int32_t* d_list_key, int32_t* d_list_slot, int32_t* d_list_count,
+                        cudaStream_t stream);
+/* Copies the ring to the host: the key staged in each ring slot (-1 = none)
+ * and the next ring position.  Synchronous. */
+moe_status moe_cache_export_staging(moe_cache* cache, int32_t* h_stage_key, uint32_t* h_pos);
+
+/* ---------------------------------------------------------------------------
  * copy_missing driven from the device: reads the miss list and count written
  * by moe_slot_ensure (device int32 arrays) and copies every miss with GPU
  * loads of the pinned bank over the host-device link, stream-ordered on

@@ -65,6 +65,9 @@ _SIGS = {
     "moe_cache_set_policy": (i32, [vp, i32, i32]),
     "moe_cache_seed_frequency": (i32, [vp, vp]),
     "moe_cache_export_frequency": (i32, [vp, vp, vp, vp]),
+    "moe_cache_set_staging": (i32, [vp, i32]),
+    "moe_prefetch": (i32, [vp, i32, vp, i32, vp, vp, vp, vp]),
+    "moe_cache_export_staging": (i32, [vp, vp, vp]),
     "moe_ladder_classify": (i32, [vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp,
                                   vp, vp, vp, vp, vp, vp, vp, vp]),
     "moe_group_pairs": (i32, [vp, i32, i32, i32, vp, vp, vp, vp]),
@@ -161,6 +164,7 @@ class moe_cache:
                                      _p(h_bank), C.byref(h)))
         self.handle = h
         self.S, self.L, self.E, self.B = num_slots, num_layers, num_experts, expert_bytes
+        self.R = 0
         self._keep = (d_slots, h_bank)
 
     def close(self):
@@ -219,6 +223,26 @@ def moe_cache_export_frequency(cache: moe_cache):
     calls = np.empty(1, dtype=np.uint64)
     _check(_lib.moe_cache_export_frequency(cache.handle, cnt.ctypes.data, ep.ctypes.data, calls.ctypes.data))
     return cnt, ep, int(calls[0])
+
+
+def moe_cache_set_staging(cache: moe_cache, num_stage: int):
+    _check(_lib.moe_cache_set_staging(cache.handle, num_stage))
+    cache.R = num_stage
+
+
+def moe_prefetch(cache: moe_cache, layer_id: int, d_experts, d_list_key, d_list_slot, d_list_count, stream=None):
+    n = d_experts.numel()
+    _check(_lib.moe_prefetch(cache.handle, layer_id, _p(d_experts), n, _p(d_list_key), _p(d_list_slot),
+                             _p(d_list_count), _s(stream)))
+
+
+def moe_cache_export_staging(cache: moe_cache):
+    """(stage_key [R] int32, next ring position)."""
+    import numpy as np
+    key = np.empty(cache.R, dtype=np.int32)
+    pos = np.empty(1, dtype=np.uint32)
+    _check(_lib.moe_cache_export_staging(cache.handle, key.ctypes.data, pos.ctypes.data))
+    return key, int(pos[0])
 
 
 def moe_slot_ensure(cache: moe_cache, layer_id: int, ids, slots_out, rank_lo: int, rank_hi: int,

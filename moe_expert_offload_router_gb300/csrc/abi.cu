@@ -98,10 +98,59 @@ __global__ void cache_reset_kernel(CacheDev c) {
     c.freq[i] = 0;
     c.freq_epoch[i] = 0;
   }
+  if (c.R > 0) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) c.stage_of[i] = -1;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < c.R; i += gridDim.x * blockDim.x) c.stage_key[i] = -1;
+  }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     *c.clock = 0;
     *c.calls = 0;
+    if (c.R > 0) *c.stage_pos = 0;
   }
+}
+
+// Staging ring: predicted experts that are neither resident nor staged take
+// ring slots round-robin (displacing older guesses, never a resident expert);
+// the copy list (key, S + j) of the guesses that keep their slot is written
+// for moe_copy_missing_device.  Ids are
+// checked first; any id >= E makes the call a no-op with count -MOE_ERR_INVALID.
+__global__ void prefetch_kernel(CacheDev c, int layer, const int32_t* experts, int n, int32_t* list_key,
+                                int32_t* list_slot, int32_t* list_count) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  for (int i = 0; i < n; ++i)
+    if (experts[i] >= c.E) {
+      *list_count = -MOE_ERR_INVALID;
+      return;
+    }
+  int m = 0;
+  for (int i = 0; i < n; ++i) {
+    const int e = experts[i];
+    if (e < 0) continue;
+    bool dup = false;
+    for (int q = 0; q < i; ++q) dup = dup || experts[q] == e;
+    if (dup) continue;
+    const int key = layer * c.E + e;
+    if (c.key_to_slot[key] >= 0 || c.stage_of[key] >= 0) continue;
+    const uint32_t p = *c.stage_pos;
+    const int j = (int)(p % (uint32_t)c.R);
+    *c.stage_pos = p + 1;
+    const int old = c.stage_key[j];
+    if (old >= 0) c.stage_of[old] = -1;
+    c.stage_key[j] = key;
+    c.stage_of[key] = j;
+    list_key[m] = key;
+    list_slot[m] = c.S + j;
+    ++m;
+  }
+  // assignments are round-robin, so only the last R of the call still hold
+  // their ring slot: earlier ones were displaced within the call and are not
+  // copied (two copies into one slot would race in the copy kernel)
+  const int keep = m < c.R ? m : c.R;
+  for (int q = 0; q < keep; ++q) {
+    list_key[q] = list_key[m - keep + q];
+    list_slot[q] = list_slot[m - keep + q];
+  }
+  *list_count = keep;
 }
 
 __global__ void cache_mark_empty_kernel(CacheDev c, int slot) {
@@ -131,8 +180,11 @@ __device__ __forceinline__ void copy_units(const CacheDev& c, const uint8_t* ban
         const int m = (int)(u / per);
         const size_t off = (size_t)(u - (Idx)m * per) * 16;
         const int key = miss_key[m], sl = miss_slot[m];
-        if (key >= 0 && key < K && sl >= 0 && sl < c.S) {
-          v[j] = __ldcs(reinterpret_cast<const uint4*>(bank + (size_t)key * B + off));
+        if (key >= 0 && key < K && sl >= 0 && sl < c.S + c.R) {
+          // a cache slot filled with a staged key copies from its staging slot
+          const int st = (c.R > 0 && sl < c.S) ? c.stage_of[key] : -1;
+          const uint8_t* src = st >= 0 ? slots + (size_t)(c.S + st) * B : bank + (size_t)key * B;
+          v[j] = __ldcs(reinterpret_cast<const uint4*>(src + off));
           dst[j] = (size_t)sl * B + off;
         }
       }
@@ -250,6 +302,11 @@ moe_status moe_cache_create(int num_slots, int num_layers, int num_experts, size
   c->dev.calls = (uint64_t*)(((uintptr_t)p + 7) & ~(uintptr_t)7);
   c->dev.policy = MOE_EVICT_LRU;
   c->dev.decay_calls = 1;
+  c->dev.R = 0;
+  c->dev.stage_key = nullptr;
+  c->dev.stage_of = nullptr;
+  c->dev.stage_pos = nullptr;
+  c->d_stage = nullptr;
   c->dev.S = num_slots;
   c->dev.L = num_layers;
   c->dev.E = num_experts;
@@ -269,6 +326,7 @@ moe_status moe_cache_destroy(moe_cache* c) {
   clear_error();
   if (c == nullptr) return MOE_OK;
   cudaError_t e = cudaFree(c->d_state);
+  if (c->d_stage) cudaFree(c->d_stage);
   delete c;
   if (e != cudaSuccess) return cuda_fail(e, "cudaFree(cache state)");
   return MOE_OK;
@@ -362,6 +420,59 @@ moe_status moe_cache_export_frequency(moe_cache* c, uint32_t* h_counts, uint32_t
   MOE_CUDA(cudaMemcpy(h_counts, c->dev.freq, K * 4, cudaMemcpyDeviceToHost));
   MOE_CUDA(cudaMemcpy(h_epochs, c->dev.freq_epoch, K * 4, cudaMemcpyDeviceToHost));
   MOE_CUDA(cudaMemcpy(h_calls, c->dev.calls, 8, cudaMemcpyDeviceToHost));
+  return MOE_OK;
+}
+
+moe_status moe_cache_set_staging(moe_cache* c, int num_stage) {
+  clear_error();
+  MOE_ARG(c != nullptr, "cache is null");
+  MOE_ARG(num_stage >= 0 && num_stage <= 65536, "num_stage out of [0, 65536]");
+  MOE_CUDA(cudaDeviceSynchronize());
+  if (c->d_stage) {
+    MOE_CUDA(cudaFree(c->d_stage));
+    c->d_stage = nullptr;
+  }
+  c->dev.R = 0;
+  c->dev.stage_key = c->dev.stage_of = nullptr;
+  c->dev.stage_pos = nullptr;
+  if (num_stage == 0) return MOE_OK;
+  const size_t K = (size_t)c->L * c->E;
+  const size_t bytes = (size_t)num_stage * 4 + K * 4 + 16;
+  void* p = nullptr;
+  cudaError_t e = cudaMalloc(&p, bytes);
+  if (e != cudaSuccess) return fail(MOE_ERR_NOMEM, "cudaMalloc of %zu bytes of staging state: %s", bytes,
+                                    cudaGetErrorString(e));
+  c->d_stage = p;
+  c->dev.R = num_stage;
+  c->dev.stage_key = (int32_t*)p;
+  c->dev.stage_of = (int32_t*)p + num_stage;
+  c->dev.stage_pos = (uint32_t*)((int32_t*)p + num_stage + K);
+  MOE_CUDA(cudaMemset(c->dev.stage_key, 0xff, (size_t)num_stage * 4));
+  MOE_CUDA(cudaMemset(c->dev.stage_of, 0xff, K * 4));
+  MOE_CUDA(cudaMemset(c->dev.stage_pos, 0, 4));
+  MOE_CUDA(cudaDeviceSynchronize());
+  return MOE_OK;
+}
+
+moe_status moe_prefetch(moe_cache* c, int layer_id, const int32_t* d_experts, int n, int32_t* d_list_key,
+                        int32_t* d_list_slot, int32_t* d_list_count, cudaStream_t stream) {
+  clear_error();
+  MOE_ARG(c != nullptr, "cache is null");
+  MOE_ARG(c->dev.R > 0, "the cache has no staging ring (moe_cache_set_staging)");
+  MOE_ARG(layer_id >= 0 && layer_id < c->L, "layer_id %d out of [0, %d)", layer_id, c->L);
+  MOE_ARG(n >= 0 && n <= 4096, "n out of [0, 4096]");
+  MOE_ARG(d_list_count && (n == 0 || (d_experts && d_list_key && d_list_slot)), "null pointer");
+  prefetch_kernel<<<1, 32, 0, stream>>>(c->dev, layer_id, d_experts, n, d_list_key, d_list_slot, d_list_count);
+  return check_launch("prefetch_kernel");
+}
+
+moe_status moe_cache_export_staging(moe_cache* c, int32_t* h_stage_key, uint32_t* h_pos) {
+  clear_error();
+  MOE_ARG(c != nullptr && h_stage_key && h_pos, "null argument");
+  MOE_ARG(c->dev.R > 0, "the cache has no staging ring");
+  MOE_CUDA(cudaDeviceSynchronize());
+  MOE_CUDA(cudaMemcpy(h_stage_key, c->dev.stage_key, (size_t)c->dev.R * 4, cudaMemcpyDeviceToHost));
+  MOE_CUDA(cudaMemcpy(h_pos, c->dev.stage_pos, 4, cudaMemcpyDeviceToHost));
   return MOE_OK;
 }
 

@@ -55,6 +55,10 @@ struct CacheDev {
   int S, L, E;
   int policy;            // MOE_EVICT_LRU or MOE_EVICT_LFU
   int decay_calls;       // LFU: counts halve once per this many calls
+  int R;                 // staging-ring slots after the S cache slots (0 = none)
+  int32_t* stage_key;    // [R] key staged in ring slot j, -1 = none
+  int32_t* stage_of;     // [L*E] ring slot holding a key, -1 = not staged
+  uint32_t* stage_pos;   // [1] next ring position (mod R)
 };
 
 }  // namespace moe
@@ -69,6 +73,7 @@ struct moe_cache {
   int device;
   int fail_copy_index;    // host-side fault injection for moe_copy_missing (-1 = off)
   const uint8_t* bank_dev;  // device-side address of h_bank (null if not mapped)
+  void* d_stage;            // library-owned staging-ring state (null if none)
 };
 
 #define MOE_ARG(cond, ...)                                   \

@@ -88,6 +88,14 @@ class DecodeLayerRunner:
         self.status_h = torch.zeros(4, dtype=torch.int32, pin_memory=True)
         self.status_ev = torch.cuda.Event()
         self.pending = None   # (layer_id, T) whose status is still to be read
+        # staging-ring prefetch (moe_cache_set_staging on the cache)
+        npf = 4096
+        self.pf_key = torch.empty(npf, dtype=torch.int32, device=dev)
+        self.pf_slot = torch.empty(npf, dtype=torch.int32, device=dev)
+        self.pf_cnt = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.pf_ready = torch.cuda.Event()
+        self.pf_done = torch.cuda.Event()
+        self.pf_pending = False
         self.assume_resident = assume_resident
         if assume_resident and cache.S < cache.L * cache.E:
             raise ValueError("assume_resident needs a cache with a slot for every key")
@@ -99,6 +107,24 @@ class DecodeLayerRunner:
         return dict(count4=i[0:1], done=i[1:2], count2=i[2:3], keys4=i[4:4 + m4],
                     slots4=i[4 + m4:4 + 2 * m4], keys2=i[4 + 2 * m4:4 + 2 * m4 + m2],
                     slots2=i[4 + 2 * m4 + m2:4 + 2 * m4 + 2 * m2])
+
+    def prefetch(self, layer_id: int, d_experts, stream=None):
+        """Stages predicted experts of `layer_id` (device int32 ids) in the cache's
+        ring: the assignment runs on `stream` after everything enqueued there,
+        the copies on the side stream after the copies already queued on it."""
+        stream = stream or torch.cuda.current_stream(self.dev)
+        L.moe_prefetch(self.cache, layer_id, d_experts, self.pf_key, self.pf_slot, self.pf_cnt, stream)
+        self.pf_ready.record(stream)
+        self.copy_stream.wait_event(self.pf_ready)
+        L.moe_copy_missing_device(self.cache, self.pf_key, self.pf_slot, self.pf_cnt, self.copy_stream,
+                                  self.copy_ctas)
+        self.pf_done.record(self.copy_stream)
+        self.pf_pending = True
+
+    def _wait_prefetch(self, stream):
+        # a staged expert promoted by a copy on `stream` must have landed
+        if self.pf_pending:
+            stream.wait_event(self.pf_done)
 
     def check(self):
         """Reads the status of the last device-mode layer whose check was deferred."""
@@ -116,7 +142,7 @@ class DecodeLayerRunner:
         if done != T:
             raise L.MoeError(L.MOE_ERR_CAPACITY, f"layer {layer_id}: single chunk expected, got {done}/{T}")
 
-    def _run_device(self, layer_id, T, ids, w, slots, x, y, stream):
+    def _run_device(self, layer_id, T, ids, w, slots, x, y, stream, prefetch=None):
         v = self._views(T)
         k = self.k
         single = min(self.E, T * k) <= self.cache.S
@@ -135,11 +161,18 @@ class DecodeLayerRunner:
                 L.moe_copy_missing_device(self.cache, v["keys4"], v["slots4"], v["count4"], self.copy_stream,
                                           self.copy_ctas)
                 self.done.record(self.copy_stream)
+                if prefetch is not None:   # after this chunk's own copies on the side stream
+                    self.prefetch(*prefetch, stream=stream)
+                    prefetch = None
                 L.moe_expert_forward_overlap(self.views, x[tb:T], slots[tb:T], w[tb:T], v["slots4"],
                                              v["count4"], self.m4, self.done, y[tb:T], self.ws_ov, self.err,
                                              stream)
             else:
+                self._wait_prefetch(stream)
                 L.moe_copy_missing_device(self.cache, v["keys4"], v["slots4"], v["count4"], stream)
+                if prefetch is not None:
+                    self.prefetch(*prefetch, stream=stream)
+                    prefetch = None
                 L.moe_expert_forward(self.views, x[tb:T], slots[tb:T], None, w[tb:T], y[tb:T], self.ws,
                                      self.err, stream)
             if single:
@@ -169,6 +202,7 @@ class DecodeLayerRunner:
         with torch.cuda.stream(stream):
             self.status_h.copy_(self.info[0:4], non_blocking=True)
         self.status_ev.record(stream)
+        self._wait_prefetch(stream)
         L.moe_copy_missing_device(self.cache, v["keys4"], v["slots4"], v["count4"], stream)
         L.moe_copy_missing_device(self.c2, v["keys2"], v["slots2"], v["count2"], stream)
         self.stats["chunks"] += 1
@@ -176,8 +210,11 @@ class DecodeLayerRunner:
         self.pending = (layer_id, T)
         return y
 
-    def run(self, layer_id: int, logits, x, y, stream=None):
-        """y[T, H] (bf16 bits) = the MoE layer applied to x[T, H] with router logits [T, E]."""
+    def run(self, layer_id: int, logits, x, y, stream=None, prefetch=None):
+        """y[T, H] (bf16 bits) = the MoE layer applied to x[T, H] with router logits [T, E].
+
+        prefetch=(layer, d_experts): predicted experts to stage once this layer's
+        own miss copies are queued (device-copy mode; the cache needs a ring)."""
         T = logits.shape[0]
         assert T <= self.T_max
         stream = stream or torch.cuda.current_stream(self.dev)
@@ -188,10 +225,12 @@ class DecodeLayerRunner:
         if self.copy == "device" and not self.assume_resident:
             if self.ladder is None:
                 self.stats["calls"] += 1
-                return self._run_device(layer_id, T, ids, w, slots, x, y, stream)
+                return self._run_device(layer_id, T, ids, w, slots, x, y, stream, prefetch)
             if self._ladder_single_chunk(T):
                 self.stats["calls"] += 1
                 return self._run_device_ladder(layer_id, T, ids, w, slots, x, y, stream)
+        if prefetch is not None:
+            raise ValueError("prefetch needs copy='device' (the copy engine copies from the bank)")
         v = self._views(T)
         tb = 0
         self.stats["calls"] += 1
