@@ -47,6 +47,10 @@ def _args():
     p.add_argument("--evict", default="lru", choices=["lru", "lfu"],
                    help="decode: slot eviction policy (lfu: counts seeded from a disjoint stretch of the trace)")
     p.add_argument("--lfu-decay", type=int, default=64, help="decode, lfu: ensure calls per count halving")
+    p.add_argument("--prefetch", type=int, default=0,
+                   help="decode: staging-ring slots for predicted experts of the next step (0 = off)")
+    p.add_argument("--pf-recall", type=float, default=0.75,
+                   help="decode prefetch: share of the next step's experts the synthetic predictor includes")
     p.add_argument("--no-overlap", action="store_true",
                    help="device copy: run the forward after the copies instead of beside them")
     return p.parse_args()
@@ -198,9 +202,11 @@ def run_ours(args):
     bank = torch.empty(E * Bx, dtype=torch.uint8, pin_memory=True)
     for e in range(E):
         bank[e * Bx:(e + 1) * Bx].copy_(gen.fp4_expert(base, 0, e, device=dev))
-    slots = torch.empty(S * Bx, dtype=torch.uint8, device=dev)
+    slots = torch.empty((S + args.prefetch) * Bx, dtype=torch.uint8, device=dev)
     shared = torch.from_numpy(gen.shared_expert(base, 0)).to(dev)
     cache = M.moe_cache(S, 1, E, Bx, slots, bank)
+    if args.prefetch:
+        M.moe_cache_set_staging(cache, args.prefetch)
     views = M.make_views(H, I, slots, S, None, 0, shared)
     if args.evict == "lfu":
         # seed: how often each expert was routed over 64 steps of the trace that the timed steps do not replay
@@ -221,10 +227,28 @@ def run_ours(args):
 
     def inputs(T):
         wl = configs.scaled(base, T=T)
-        lg = [torch.from_numpy(gen.router_logits(wl, 0, s % base.steps, T)).to(dev) for s in range(n_steps)]
+        lg_np = [gen.router_logits(wl, 0, s % base.steps, T) for s in range(n_steps + 1)]
+        lg = [torch.from_numpy(v).to(dev) for v in lg_np[:n_steps]]
         xs = [torch.from_numpy(gen.activations(wl, 0, s % base.steps, T).view(np.int16)).to(dev)
               for s in range(n_steps)]
-        return lg, xs
+        return lg, xs, predictions(lg_np)
+
+    def predictions(lg_np):
+        """Synthetic predictor (the pages' trained predictor is out of scope): for
+        step s, each expert that step s+1 routes to is included with probability
+        pf_recall, plus a quarter as many experts it does not route to."""
+        if not args.prefetch:
+            return None
+        rng = np.random.default_rng(17)
+        out = []
+        for s in range(n_steps):
+            nxt = np.unique(np.argsort(-lg_np[s + 1], axis=1, kind="stable")[:, :k])
+            keep = nxt[rng.random(nxt.size) < args.pf_recall]
+            others = np.setdiff1d(np.arange(E), nxt)
+            fp = rng.choice(others, size=max(1, keep.size // 4), replace=False)
+            guess = rng.permutation(np.concatenate([keep, fp])).astype(np.int32)
+            out.append((0, torch.from_numpy(guess).to(dev)))
+        return out
 
     gu_expert = 2 * (I * H // 2 + I * H // 32)             # w1 + w3 bytes of one FP4 expert
     gu_shared = 2 * (I * H + I * 4)                          # w1 + w3 of the FP8 shared expert
@@ -235,10 +259,10 @@ def run_ours(args):
         torch.cuda.synchronize()
         if lfu_seed is not None:
             M.moe_cache_seed_frequency(cache, lfu_seed)
-        lg, xs = inputs(T)
+        lg, xs, pf = inputs(T)
         y = torch.empty((T, H), dtype=torch.int16, device=dev)
         for s in range(args.warmup):
-            runner.run(0, lg[s], xs[s], y)
+            runner.run(0, lg[s], xs[s], y, prefetch=pf[s] if pf else None)
         torch.cuda.synchronize()
         runner.check()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -255,7 +279,7 @@ def run_ours(args):
             s = args.warmup + i
             flush.zero_()
             ev[i][0].record(stream)
-            runner.run(0, lg[s], xs[s], y)
+            runner.run(0, lg[s], xs[s], y, prefetch=pf[s] if pf else None)
             ev[i][1].record(stream)
             # accounting (outside the events): distinct experts per forward chunk
             ids = runner.ids[:T]
@@ -300,7 +324,7 @@ def run_ours(args):
     def measure_e2e(T):
         """Same steps through the public API with host buffers: inputs copied in
         from pinned memory and the output read back, every step."""
-        lg, xs = inputs(T)
+        lg, xs, pf = inputs(T)
         h_lg = [t.cpu().pin_memory() for t in lg]
         h_x = [t.cpu().pin_memory() for t in xs]
         d_lg = torch.empty_like(lg[0])
@@ -314,7 +338,7 @@ def run_ours(args):
         for s in range(args.warmup):
             d_lg.copy_(h_lg[s], non_blocking=True)
             d_x.copy_(h_x[s], non_blocking=True)
-            runner.run(0, d_lg, d_x, y)
+            runner.run(0, d_lg, d_x, y, prefetch=pf[s] if pf else None)
             h_y.copy_(y, non_blocking=True)
         torch.cuda.synchronize()
         tot = 0.0
@@ -325,7 +349,7 @@ def run_ours(args):
             a.record(stream)
             d_lg.copy_(h_lg[s], non_blocking=True)
             d_x.copy_(h_x[s], non_blocking=True)
-            runner.run(0, d_lg, d_x, y)
+            runner.run(0, d_lg, d_x, y, prefetch=pf[s] if pf else None)
             h_y.copy_(y, non_blocking=True)
             b.record(stream)
             b.synchronize()
@@ -352,6 +376,8 @@ def run_ours(args):
             "config": {"workload": f"decode layer H=4096 I=2048 E=256 top_k=8 + FP8 shared, 64-slot cache over a pinned "
                                    f"256-expert bank, Zipf(1.1) routing trace, T={args.T}",
                        "T": args.T, "copy": args.copy, "overlap": overlap,
+                       "prefetch": (f"{args.prefetch} staging slots, synthetic predictor of the next step "
+                                    f"(recall {args.pf_recall})") if args.prefetch else None,
                        "evict": args.evict if args.evict == "lru" else f"lfu (decay every {args.lfu_decay} calls, "
                                                                         "seeded from 64 other trace steps)",
                        "parallelism": "replicas" if world > 1 else "single GPU",
