@@ -44,6 +44,8 @@ def _args():
     p.add_argument("--prefill-experts", type=int, default=0,
                    help="prefill workload with this many experts (all resident), for profiling a smaller case")
     p.add_argument("--prefill-tokens", type=int, default=0, help="prefill workload with this many tokens")
+    p.add_argument("--stream-layers", type=int, default=0,
+                   help="prefill: stream this many layers whole from the pinned bank (nothing resident)")
     p.add_argument("--evict", default="lru", choices=["lru", "lfu"],
                    help="decode: slot eviction policy (lfu: counts seeded from a disjoint stretch of the trace)")
     p.add_argument("--lfu-decay", type=int, default=64, help="decode, lfu: ensure calls per count halving")
@@ -450,6 +452,45 @@ def run_other(args):
         wl = configs.scaled(wl, E=e, S=e, T=args.prefill_tokens or wl.T)
     H, I, E, k, T = wl.H, wl.I, wl.E, wl.k, wl.T
     Bx = M.moe_fp4_expert_bytes(H, I)
+    if args.workload == "prefill" and args.stream_layers > 0:
+        # whole-layer streaming: every layer's experts cross the host link each pass
+        nl = args.stream_layers
+        bank = torch.empty(nl * E * Bx, dtype=torch.uint8, pin_memory=True)
+        for layer in range(nl):
+            for e in range(E):
+                o = (layer * E + e) * Bx
+                bank[o:o + Bx].copy_(gen.fp4_expert(wl, layer, e, device=dev))
+        st = M.PrefillStreamer(bank, nl, E, H, I, k, T, dev)
+        lg = [torch.from_numpy(gen.router_logits(wl, layer, 0, T)).to(dev) for layer in range(nl)]
+        xs = [torch.from_numpy(gen.activations(wl, layer, 0, T).view(np.int16)).to(dev) for layer in range(nl)]
+        y = torch.empty((T, H), dtype=torch.int16, device=dev)
+
+        def one_pass(_):
+            st.begin(0)
+            for layer in range(nl):
+                st.run_layer(layer, lg[layer], xs[layer], y)
+        for _ in range(args.warmup):
+            one_pass(0)
+        torch.cuda.synchronize()
+        M.moe_profile_enable(True)
+        clocks.start()
+        ms = timed(one_pass, args.steps)
+        ck = clocks.stop()
+        kt = {M.KERNEL_NAMES[kid]: M.moe_profile_query(kid) for kid in range(M.MOE_K_COUNT)}
+        M.moe_profile_enable(False)
+        per_layer = ms / nl
+        out.update({"value": T / (per_layer / 1e3), "unit": UNIT, "ms_per_step": ms, "clocks": ck,
+                    "gpu_launches": sum(v[1] for v in kt.values()),
+                    "kernel_ms_per_step": {nm: round(v[0] / args.steps, 4) for nm, v in kt.items() if v[1]},
+                    "dtype": "bf16 MMA (fp32 accumulate) on exactly decoded MXFP4 weights",
+                    "config": {"workload": f"whole-layer streaming prefill: {nl} layers x (E={E} MXFP4 experts, "
+                                           f"H={H} I={I} top_k={k}), T={T} per layer, every layer streamed from "
+                                           "the pinned bank through two layer buffers", "T": T, "layers": nl},
+                    "ms_per_layer": per_layer,
+                    "host_link_gbs": E * Bx / (per_layer / 1e3) / 1e9,
+                    "roofline": None})
+        print(json.dumps(out))
+        return
     if args.workload in ("prefill", "ladder"):
         bank = torch.empty(E * Bx, dtype=torch.uint8, pin_memory=True)
         for e in range(E):

@@ -248,6 +248,22 @@ moe_status moe_copy_missing_device(moe_cache* cache, const int32_t* d_miss_key,
                                    const int32_t* d_miss_slot, const int32_t* d_miss_count,
                                    int max_ctas, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Whole-layer streaming for prefill past the crossover.  "Running DeepSeek-
+ * V4-Flash across four free GPUs", section "What the expert cache actually
+ * does": above T * top_k >= num_experts prefill streams whole expert layers
+ * instead of fetching slots, because a chunk touches most of the layer anyway;
+ * section "Step 7" ("moe_cache_size=128 is too small"): with prefill overlap
+ * two full expert-layer buffers are in use.  Copies all num_experts experts of
+ * layer `layer_id` (bytes layer_id * E * B .. +E * B of the key-major pinned
+ * bank) into the device buffer d_buf (E * B bytes) with one cudaMemcpyAsync
+ * on `stream` (the copy engine: no SM time taken from the compute).  The
+ * buffer then serves as an E-slot pool whose slot e holds expert e, for
+ * moe_expert_prefill.  The slot cache is not involved.
+ * ------------------------------------------------------------------------- */
+moe_status moe_copy_layer(const void* h_bank, int layer_id, int num_experts, size_t expert_bytes,
+                          void* d_buf, cudaStream_t stream);
+
 /* Test hook: make the copy with list index `index` of later moe_copy_missing
  * calls fail on the host, as if cudaMemcpyAsync had returned an error
  * (index < 0 disarms).  Nothing is issued to the device for a failed copy. */

@@ -14,8 +14,8 @@ _SUBMODULES = ("build", "layer", "_lib")
 def __getattr__(name):
     if name in _SUBMODULES or name.startswith("__"):
         raise AttributeError(name)   # the import system then loads the submodule
-    if name == "DecodeLayerRunner":
-        return importlib.import_module(__name__ + ".layer").DecodeLayerRunner
+    if name in ("DecodeLayerRunner", "PrefillStreamer"):
+        return getattr(importlib.import_module(__name__ + ".layer"), name)
     lib = importlib.import_module(__name__ + "._lib")
     try:
         return getattr(lib, name)

@@ -61,6 +61,7 @@ _SIGS = {
     "moe_slot_ensure": (i32, [vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp]),
     "moe_copy_missing": (i32, [vp, vp, vp, i32, vp, vp, vp]),
     "moe_debug_fail_copy": (i32, [vp, i32]),
+    "moe_copy_layer": (i32, [vp, i32, i32, sz, vp, vp]),
     "moe_copy_missing_device": (i32, [vp, vp, vp, vp, i32, vp]),
     "moe_cache_set_policy": (i32, [vp, i32, i32]),
     "moe_cache_seed_frequency": (i32, [vp, vp]),
@@ -269,6 +270,10 @@ def moe_copy_missing_device(cache: moe_cache, d_miss_key, d_miss_slot, d_miss_co
                             max_ctas: int = 0):
     _check(_lib.moe_copy_missing_device(cache.handle, _p(d_miss_key), _p(d_miss_slot), _p(d_miss_count),
                                         max_ctas, _s(stream)))
+
+
+def moe_copy_layer(h_bank, layer_id: int, num_experts: int, expert_bytes: int, d_buf, stream=None):
+    _check(_lib.moe_copy_layer(_p(h_bank), layer_id, num_experts, expert_bytes, _p(d_buf), _s(stream)))
 
 
 def moe_debug_fail_copy(cache: moe_cache, index: int):

@@ -494,6 +494,20 @@ moe_status moe_copy_missing_device(moe_cache* c, const int32_t* d_miss_key, cons
   return check_launch("copy_missing_kernel");
 }
 
+moe_status moe_copy_layer(const void* h_bank, int layer_id, int num_experts, size_t expert_bytes, void* d_buf,
+                          cudaStream_t stream) {
+  clear_error();
+  MOE_ARG(h_bank && d_buf, "null pointer");
+  MOE_ARG(layer_id >= 0 && num_experts >= 1 && expert_bytes > 0, "bad layer, expert count or size");
+  cudaPointerAttributes hb;
+  MOE_CUDA(cudaPointerGetAttributes(&hb, h_bank));
+  MOE_ARG(hb.type == cudaMemoryTypeHost, "h_bank is not page-locked host memory");
+  const size_t bytes = (size_t)num_experts * expert_bytes;
+  const uint8_t* src = (const uint8_t*)h_bank + (size_t)layer_id * bytes;
+  MOE_CUDA(cudaMemcpyAsync(d_buf, src, bytes, cudaMemcpyHostToDevice, stream));
+  return MOE_OK;
+}
+
 moe_status moe_debug_fail_copy(moe_cache* c, int index) {
   clear_error();
   MOE_ARG(c != nullptr, "cache is null");

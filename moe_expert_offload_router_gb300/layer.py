@@ -278,3 +278,62 @@ class DecodeLayerRunner:
                                  self.ws, self.err, stream)
             tb = done
         return y
+
+
+class PrefillStreamer:
+    """Whole-layer streaming prefill with two layer buffers.
+
+    Past the crossover T * top_k >= E a prefill chunk touches most of a layer's
+    experts, so the layer is streamed whole ("Running DeepSeek-V4-Flash across
+    four free GPUs", section "What the expert cache actually does") into one of
+    two device buffers of E experts each (section "Step 7": with overlap, two
+    full expert-layer buffers): while layer l computes from one buffer, layer
+    l + 1 streams into the other on the copy engine.  Each layer: router top-k
+    (the expert id is the buffer slot), wait for the layer's copy, grouped-GEMM
+    prefill; the buffer is then refilled with layer l + 2.
+    """
+
+    def __init__(self, h_bank, num_layers: int, E: int, H: int, I: int, k: int, T_max: int, device=None):
+        self.bank, self.L, self.E, self.H, self.I, self.k = h_bank, num_layers, E, H, I, k
+        self.dev = torch.device(device or "cuda")
+        self.B = L.moe_fp4_expert_bytes(H, I)
+        self.bufs = [torch.empty(E * self.B, dtype=torch.uint8, device=self.dev) for _ in range(2)]
+        self.views = [L.make_views(H, I, b, E) for b in self.bufs]
+        self.ids = torch.empty((T_max, k), dtype=torch.int32, device=self.dev)
+        self.w = torch.empty((T_max, k), dtype=torch.float32, device=self.dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=self.dev)
+        self.ws = torch.empty(L.moe_expert_prefill_workspace(self.views[0], T_max, k), dtype=torch.uint8,
+                              device=self.dev)
+        self.copy_stream = torch.cuda.Stream(device=self.dev)
+        self.loaded = [torch.cuda.Event(), torch.cuda.Event()]
+        self.freed = [torch.cuda.Event(), torch.cuda.Event()]
+        self.layer_in = [-1, -1]
+
+    def _load(self, layer: int, stream):
+        b = layer % 2
+        self.freed[b].record(stream)               # the last compute reading this buffer is enqueued
+        self.copy_stream.wait_event(self.freed[b])
+        L.moe_copy_layer(self.bank, layer, self.E, self.B, self.bufs[b], self.copy_stream)
+        self.loaded[b].record(self.copy_stream)
+        self.layer_in[b] = layer
+
+    def begin(self, first_layer: int = 0, stream=None):
+        """Starts streaming the first two layers."""
+        stream = stream or torch.cuda.current_stream(self.dev)
+        for layer in range(first_layer, min(first_layer + 2, self.L)):
+            self._load(layer, stream)
+
+    def run_layer(self, layer: int, logits, x, y, stream=None):
+        """y[T, H] = the MoE layer `layer` on x[T, H] with router logits [T, E]."""
+        stream = stream or torch.cuda.current_stream(self.dev)
+        b = layer % 2
+        if self.layer_in[b] != layer:
+            self._load(layer, stream)
+        T = logits.shape[0]
+        ids, w = self.ids[:T], self.w[:T]
+        L.moe_router_topk(logits, self.k, True, ids, w, stream)
+        stream.wait_event(self.loaded[b])
+        L.moe_expert_prefill(self.views[b], x, ids, w, y, self.ws, self.err, stream)
+        if layer + 2 < self.L:
+            self._load(layer + 2, stream)
+        return y
