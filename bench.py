@@ -362,12 +362,44 @@ def run_ours(args):
         return {"value": world * T / (ms / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": T * E * 4 + T * H * 2, "d2h_bytes_per_step": T * H * 2}
 
+    def measure_graph(T):
+        """The same steps with each layer step replayed as one CUDA graph (batches
+        that are one chunk by construction); no per-kernel profiling."""
+        grunner = M.DecodeLayerRunner(cache, views, E, k, T, dev, copy=args.copy, graph=True)
+        cache.reset()
+        torch.cuda.synchronize()
+        if lfu_seed is not None:
+            M.moe_cache_seed_frequency(cache, lfu_seed)
+        lg, xs, _ = inputs(T)
+        y = torch.empty((T, H), dtype=torch.int16, device=dev)
+        for s in range(args.warmup):
+            grunner.run(0, lg[s], xs[s], y)
+        torch.cuda.synchronize()
+        grunner.check()
+        tot = 0.0
+        for i in range(args.steps):
+            s = args.warmup + i
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            grunner.run(0, lg[s], xs[s], y)
+            b.record(stream)
+            b.synchronize()
+            tot += a.elapsed_time(b)
+        grunner.check()
+        ms = tot / args.steps
+        return {"graph_ms_per_step": ms, "graph_tokens_per_s": T / (ms / 1e3)}
+
     clocks = Clocks(local)
     results = {}
     clocks.start()
     for T in Ts:
         results[T] = measure(T)
     ck = clocks.stop()
+    if args.copy == "device" and not args.prefetch:
+        for T in Ts:
+            if min(E, T * k) <= S:
+                results[T].update(measure_graph(T))
     head = results[args.T]
     e2e = measure_e2e(args.T)
     cpu = cpu_baseline(args.cpu_sample_tokens) if (rank == 0 and world == 1) else None

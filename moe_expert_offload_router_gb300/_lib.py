@@ -369,8 +369,17 @@ def moe_selftest():
     _check(_lib.moe_selftest())
 
 
+_PROFILING = [False]
+
+
 def moe_profile_enable(enable: bool = True):
     _check(_lib.moe_profile_enable(int(bool(enable))))
+    _PROFILING[0] = bool(enable)
+
+
+def moe_profile_active() -> bool:
+    """Whether moe_profile_enable(True) is in effect (kernel timing events are recorded)."""
+    return _PROFILING[0]
 
 
 def moe_profile_query(kernel: int):

@@ -21,6 +21,11 @@ batch cannot need more distinct experts than there are slots
 does not wait at all: the status of each layer is checked on the next call
 (or by :meth:`check`).
 
+With ``graph=True`` (device copy, no ladder) a layer step whose batch is one
+chunk by construction is captured once as a CUDA graph (router, ensure,
+status read-back, copies, forward) and replayed on static buffers, which
+removes the per-launch host cost of small batches.
+
 With ``overlap=True`` (device copy only) the copy kernel runs on a side stream
 with a small grid while ``moe_expert_forward_overlap`` computes the pairs of
 resident experts and the shared expert; only the pairs of missed experts wait
@@ -49,7 +54,7 @@ class DecodeLayerRunner:
     def __init__(self, cache: L.moe_cache, views: L.moe_expert_views, E: int, k: int,
                  T_max: int, device=None, int2_cache: Optional[L.moe_cache] = None,
                  ladder=None, assume_resident: bool = False, copy: str = "engine",
-                 overlap=False, copy_ctas: int = 64):
+                 overlap=False, copy_ctas: int = 64, graph: bool = False):
         self.cache, self.views, self.E, self.k, self.T_max = cache, views, E, k, T_max
         self.dev = torch.device(device or "cuda")
         self.c2, self.ladder = int2_cache, ladder
@@ -96,6 +101,10 @@ class DecodeLayerRunner:
         self.pf_ready = torch.cuda.Event()
         self.pf_done = torch.cuda.Event()
         self.pf_pending = False
+        # CUDA graphs of whole single-chunk device-copy layer steps, per (layer, T)
+        self.graph = graph
+        self.graphs = {}
+        self._capturing = False
         self.assume_resident = assume_resident
         if assume_resident and cache.S < cache.L * cache.E:
             raise ValueError("assume_resident needs a cache with a slot for every key")
@@ -152,7 +161,8 @@ class DecodeLayerRunner:
                               v["keys4"], v["slots4"], v["count4"], v["done"], stream)
             with torch.cuda.stream(stream):
                 self.status_h.copy_(self.info[0:4], non_blocking=True)
-            self.status_ev.record(stream)
+            if not self._capturing:      # a replayed graph records it after the replay
+                self.status_ev.record(stream)
             self.stats["chunks"] += 1
             if self.overlap is True or (self.overlap == "auto" and T * k >= self.OVERLAP_MIN_PAIRS):
                 # copies on the side stream; resident experts' pairs compute meanwhile
@@ -210,6 +220,49 @@ class DecodeLayerRunner:
         self.pending = (layer_id, T)
         return y
 
+    def _graph_ok(self, T, prefetch):
+        return (self.graph and self.copy == "device" and self.ladder is None and not self.assume_resident
+                and prefetch is None and min(self.E, T * self.k) <= self.cache.S and not L.moe_profile_active())
+
+    def _replay(self, layer_id, logits, x, y, stream):
+        """Whole layer step as one CUDA graph: router, ensure, status read-back,
+        device copies and the forward, replayed on static input and output buffers."""
+        T = logits.shape[0]
+        key = (layer_id, T)
+        if key not in self.graphs:
+            return False
+        g, lg, xb, yb = self.graphs[key]
+        with torch.cuda.stream(stream):
+            lg.copy_(logits, non_blocking=True)
+            xb.copy_(x, non_blocking=True)
+            g.replay()
+            y.copy_(yb, non_blocking=True)
+        self.status_ev.record(stream)
+        self.pending = (layer_id, T)
+        self.stats["calls"] += 1
+        self.stats["chunks"] += 1
+        return True
+
+    def _capture(self, layer_id, T):
+        g = torch.cuda.CUDAGraph()
+        H = self.views.H
+        lg = torch.empty((T, self.E), dtype=torch.float32, device=self.dev)
+        xb = torch.empty((T, H), dtype=torch.int16, device=self.dev)
+        yb = torch.empty((T, H), dtype=torch.int16, device=self.dev)
+        calls, chunks = self.stats["calls"], self.stats["chunks"]
+        self._capturing = True
+        try:
+            with torch.cuda.graph(g):
+                s = torch.cuda.current_stream(self.dev)
+                ids, w, slots = self.ids[:T], self.w[:T], self.slots[:T]
+                L.moe_router_topk(lg, self.k, True, ids, w, s)
+                self._run_device(layer_id, T, ids, w, slots, xb, yb, s)
+        finally:
+            self._capturing = False
+            self.pending = None
+            self.stats["calls"], self.stats["chunks"] = calls, chunks
+        self.graphs[(layer_id, T)] = (g, lg, xb, yb)
+
     def run(self, layer_id: int, logits, x, y, stream=None, prefetch=None):
         """y[T, H] (bf16 bits) = the MoE layer applied to x[T, H] with router logits [T, E].
 
@@ -220,12 +273,26 @@ class DecodeLayerRunner:
         stream = stream or torch.cuda.current_stream(self.dev)
         k = self.k
         self.check()
+        if self._graph_ok(T, prefetch):
+            if self._replay(layer_id, logits, x, y, stream):
+                return y
+            # first call of this (layer, T): run it eagerly below, then capture the
+            # step for the next calls (capturing executes nothing)
+            capture_after = True
+        else:
+            capture_after = False
         ids, w, slots = self.ids[:T], self.w[:T], self.slots[:T]
         L.moe_router_topk(logits, k, True, ids, w, stream)
         if self.copy == "device" and not self.assume_resident:
             if self.ladder is None:
                 self.stats["calls"] += 1
-                return self._run_device(layer_id, T, ids, w, slots, x, y, stream, prefetch)
+                out = self._run_device(layer_id, T, ids, w, slots, x, y, stream, prefetch)
+                if capture_after:
+                    torch.cuda.synchronize(self.dev)
+                    pending = self.pending
+                    self._capture(layer_id, T)
+                    self.pending = pending
+                return out
             if self._ladder_single_chunk(T):
                 self.stats["calls"] += 1
                 return self._run_device_ladder(layer_id, T, ids, w, slots, x, y, stream)
