@@ -131,26 +131,33 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Two E2M1 codes -> bf16x2 (element 2j low) times the block scale, exact.
-__device__ __forceinline__ uint32_t fp4x2_to_bf16x2(uint32_t byte, uint32_t scale2) {
-  uint32_t h, r;
-  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(h) : "r"(byte));
+// Eight E2M1 codes (one 32-bit word, element 2j in the low nibble of byte j)
+// -> four 16-bit pairs times the block scale: the word is split into its four
+// bytes by one mov, each byte converted by cvt.rn.f16x2.e2m1x2.
+__device__ __forceinline__ void fp4x8_to_f16(uint32_t w, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+      : "r"(w));
+}
+
+// fp16 pair times the block scale 2^(e-127) given as fp16x2: exact when e is
+// within [kF16ScaleLo, kF16ScaleHi].
+__device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t s) {
+  __half2 v = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<const __half2*>(&s));
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// fp16 pair (exact E2M1 values) -> bf16 pair times the block scale: exact for
+// every E8M0 scale.
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2_scaled(uint32_t h, uint32_t scale2) {
+  uint32_t r;
   asm("{\n\t.reg .b16 l, u, bl, bu;\n\tmov.b32 {l, u}, %1;\n\tcvt.rn.bf16.f16 bl, l;\n\tcvt.rn.bf16.f16 bu, u;\n\t"
       "mov.b32 %0, {bl, bu};\n\t}"
       : "=r"(r)
       : "r"(h));
-  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&r);
-  const __nv_bfloat162 s = *reinterpret_cast<const __nv_bfloat162*>(&scale2);
-  v = __hmul2(v, s);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// Two E2M1 codes -> fp16x2 times the block scale 2^(e-127) given as fp16x2;
-// exact when e is within [kF16ScaleLo, kF16ScaleHi].
-__device__ __forceinline__ uint32_t fp4x2_to_f16x2(uint32_t byte, uint32_t scale2) {
-  uint32_t h;
-  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(h) : "r"(byte));
-  __half2 v = __hmul2(*reinterpret_cast<__half2*>(&h), *reinterpret_cast<const __half2*>(&scale2));
+  __nv_bfloat162 v = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&r), *reinterpret_cast<const __nv_bfloat162*>(&scale2));
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
@@ -408,18 +415,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const uint32_t w4[4] = {q[mt][c].x, q[mt][c].y, q[mt][c].z, q[mt][c].w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const uint32_t wv = w4[u];
             uint4 o;
+            fp4x8_to_f16(w4[u], o.x, o.y, o.z, o.w);
             if (f16) {
-              o.x = fp4x2_to_f16x2(wv & 0xff, sc2);
-              o.y = fp4x2_to_f16x2((wv >> 8) & 0xff, sc2);
-              o.z = fp4x2_to_f16x2((wv >> 16) & 0xff, sc2);
-              o.w = fp4x2_to_f16x2(wv >> 24, sc2);
+              o.x = hmul2_f16(o.x, sc2);
+              o.y = hmul2_f16(o.y, sc2);
+              o.z = hmul2_f16(o.z, sc2);
+              o.w = hmul2_f16(o.w, sc2);
             } else {
-              o.x = fp4x2_to_bf16x2(wv & 0xff, sc2);
-              o.y = fp4x2_to_bf16x2((wv >> 8) & 0xff, sc2);
-              o.z = fp4x2_to_bf16x2((wv >> 16) & 0xff, sc2);
-              o.w = fp4x2_to_bf16x2(wv >> 24, sc2);
+              o.x = f16x2_to_bf16x2_scaled(o.x, sc2);
+              o.y = f16x2_to_bf16x2_scaled(o.y, sc2);
+              o.z = f16x2_to_bf16x2_scaled(o.z, sc2);
+              o.w = f16x2_to_bf16x2_scaled(o.w, sc2);
             }
             const int unit = c * 4 + u;
             *reinterpret_cast<uint4*>(arow + ((unit ^ (r & 7)) << 4)) = o;
