@@ -17,14 +17,14 @@
 //             epilogue o[pair][feature] in fp32
 //   combine   y_t = sum_j w_tj o_tj in rank order -> bf16
 //
-// GEMM CTA (384 threads): warp 8 lane 0 streams the raw FP4 codes of the A
-// tiles by TMA into a staging ring, as far ahead as the ring allows; warp 10
+// GEMM CTA (512 threads): warp 12 lane 0 streams the raw FP4 codes of the A
+// tiles by TMA into a staging ring, as far ahead as the ring allows; warp 14
 // lane 0 loads the B tile by TMA straight into its 128-byte swizzled K-major
-// layout, one stage per free operand slot; warps 0-7 decode the raw codes to
+// layout, one stage per free operand slot; warps 0-11 decode the raw codes to
 // 16-bit with the E8M0 scale folded in (exact) and store them in the same
-// swizzled layout; warp 9 lane 0 issues tcgen05.mma.kind::f16 (M = 128,
+// swizzled layout; warp 13 lane 0 issues tcgen05.mma.kind::f16 (M = 128,
 // N = rows of the item rounded to 16, K = 16 per instruction) into two TMEM
-// accumulators and commits each stage back to the producers; all 12 warps
+// accumulators and commits each stage back to the producers; all 16 warps
 // read TMEM with tcgen05.ld for the epilogue.  Every mbarrier wait gives up
 // after one second and records MOE_ERR_TIMEOUT.
 #include <cuda.h>
@@ -39,17 +39,22 @@
 
 namespace moe {
 
-constexpr int kPfThreads = 384;
+constexpr int kPfThreads = 512;   // 16 warps: 12 converters, raw producer, MMA, B producer, spare
 constexpr int kPfStages = 3;      // A/B operand stages
 constexpr int kPfMT = 2;          // 128-row weight tiles per CTA (two TMEM accumulators)
 constexpr int kPfNMax = 256;      // rows per item (MMA N) of the item list
 constexpr int kPfKStep = 64;      // K elements per stage (128 bytes of bf16: one swizzle row)
 constexpr int kPfBox = 64;        // rows per TMA box of the B operand
-// Converter warps 0-7 form two groups of 128 threads; group g converts the
-// K steps ks with ks % 2 == g, one A row per thread.  Each group then has two
-// steps' time per wait round, which halves the wait overhead per step.
-constexpr int kPfConvGroups = 2;
+// Converter warps 0-11 form three groups of 128 threads; group g converts the
+// K steps ks with ks % 3 == g, one A row per thread.  The converters' instruction
+// stream bounds a K step, so three warps per scheduler keep more of it issuing.
+constexpr int kPfConvGroups = 3;
 constexpr int kPfConvThreads = 128;
+constexpr int kPfConvWarps = kPfConvGroups * kPfConvThreads / 32;  // 12
+constexpr int kWarpRaw = kPfConvWarps;       // raw FP4 code producer
+constexpr int kWarpMma = kPfConvWarps + 1;   // TMEM allocation, MMA issue
+constexpr int kWarpB = kPfConvWarps + 2;     // activation (B) producer
+constexpr int kPfWarps = kPfThreads / 32;
 
 // shared memory layout (offsets from a 1024-aligned base)
 constexpr int kATile = 128 * 128;                 // 16 KB per 128-row tile
@@ -237,7 +242,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     *f16_flag = (a.mode == 0 && a.allow_f16) ? 1 : 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
                  "r"(512));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -255,7 +260,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   // tile keeps the scaled E2M1 values exact in fp16 (gate/up only).  The vote
   // runs in every warp but the raw-code producer, which starts streaming at once.
   bool f16 = false;
-  if (warp != 8) {
+  if (warp != kWarpRaw) {
     if (a.mode == 0 && a.allow_f16 && warp < 8) {
       const int r = threadIdx.x >> 1, c = threadIdx.x & 1;
       const int g = r & 1, i = r >> 1;
@@ -290,7 +295,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     f16 = *(volatile int*)f16_flag != 0;
   }
 
-  if (warp == 8) {
+  if (warp == kWarpRaw) {
     // weight codes: as far ahead as the raw ring allows, independent of MMA progress
     if (lane == 0) {
       bool ok = true;
@@ -313,7 +318,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       }
     }
-  } else if (warp == 10) {
+  } else if (warp == kWarpB) {
     // activation tiles: one stage per free operand slot
     if (lane == 0) {
       bool ok = true;
@@ -332,7 +337,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kWarpMma) {
     if (lane == 0) {
       const uint32_t idesc = idesc_16bit(n_mma, !f16);
       bool ok = true;
@@ -354,10 +359,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       mma_commit(done);  // fires when every issued MMA has completed
     }
-  } else if (warp < 8) {
-    // converters: group cg takes the K steps of its parity; thread -> row r
+  } else if (warp < kPfConvWarps) {
+    // converters: group cg takes the K steps ks = cg (mod 3); thread -> row r
     // of both 128 x 64 A tiles (two 32-weight halves each)
-    const int cg = warp >> 2;
+    const int cg = warp / (kPfConvThreads / 32);
     const int r = threadIdx.x & (kPfConvThreads - 1);
     const int g = r & 1, i = r >> 1;  // mode 0: gate/up interleaved rows
     int raw_off[kPfMT];
@@ -380,14 +385,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       snext[mt] = sbytes > 16 ? __ldg(reinterpret_cast<const uint4*>(srow[mt] + 16)) : scur[mt];
     }
     bool ok = true;
+    int chunk = 0;  // scur holds the scale bytes of K steps 8 * chunk .. 8 * chunk + 7
     for (int ks = cg; ks < nk && ok; ks += kPfConvGroups) {
       const int rs = ks % C::kRaw, rr = ks / C::kRaw;
       const int s = ks % kPfStages, rnd = ks / kPfStages;
-      if ((ks & 7) == cg && ks >= 8) {
+      if (ks / 8 != chunk) {  // a stride below 8 moves on by one chunk at a time
+        ++chunk;
 #pragma unroll
         for (int mt = 0; mt < kPfMT; ++mt) {
           scur[mt] = snext[mt];
-          const int nxt = (ks / 8 + 1) * 16;
+          const int nxt = (chunk + 1) * 16;
           if (nxt < sbytes) snext[mt] = __ldg(reinterpret_cast<const uint4*>(srow[mt] + nxt));
         }
       }
@@ -442,20 +449,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
   }
 
-  // epilogue: all 12 warps.  Warp w reads TMEM lane quadrant w % 4 and takes
-  // every third 16-column chunk (w / 4 picks which), over both accumulators.
+  // epilogue: all 16 warps.  Warp w reads TMEM lane quadrant w % 4 and takes
+  // every fourth 16-column chunk (w / 4 picks which), over both accumulators.
   {
     __syncwarp();
     bool ok = mbar_wait(done, 0, a.err);
     ok = __all_sync(0xffffffffu, ok);
     __syncwarp();
     tc_fence_after();
-    if (warp == 8) f16 = *(volatile int*)f16_flag != 0;  // final: every converter has passed the vote
+    if (warp == kWarpRaw) f16 = *(volatile int*)f16_flag != 0;  // final: every converter has passed the vote
     const int q = warp & 3, part = warp >> 2;
     const int row = q * 32 + lane;  // D row = A tile row
     const int nchunks = n_mma / 16;
     if (ok) {
-      for (int cc = part; cc < kPfMT * nchunks; cc += 3) {
+      for (int cc = part; cc < kPfMT * nchunks; cc += kPfWarps / 4) {
         const int mt = cc / nchunks, c0 = (cc % nchunks) * 16;
         uint32_t v[16];
         tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(mt * 256 + c0), v);
@@ -489,7 +496,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
   }
