@@ -114,15 +114,33 @@ __device__ __forceinline__ uint32_t idesc_16bit(int n, bool bf16) {
   return (1u << 4) | (t << 7) | (t << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// One 64-wide K step of both accumulators, issued by one elected lane of a
+// converged warp: four K = 16 MMAs per 128-row A tile (descriptor start
+// addresses advance 32 bytes per slice inside the 128-byte swizzled rows),
+// then a commit that arrives on `bar` once they complete.  `acc` = 0 starts
+// the accumulators (first K step only).
+__device__ __forceinline__ void mma_kstep_2x4(uint32_t d0, uint32_t d1, uint64_t a0, uint64_t a1, uint64_t b,
+                                              uint32_t idesc, uint32_t acc, uint64_t* bar) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+      "{\n\t.reg .pred p, t, e;\n\t.reg .b64 a, bb;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %5, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %4, %6, p;\n\t"
+      "add.s64 a, %2, 2;\n\tadd.s64 bb, %4, 2;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, bb, %6, t;\n\t"
+      "add.s64 a, %2, 4;\n\tadd.s64 bb, %4, 4;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, bb, %6, t;\n\t"
+      "add.s64 a, %2, 6;\n\tadd.s64 bb, %4, 6;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, bb, %6, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%1], %3, %4, %6, p;\n\t"
+      "add.s64 a, %3, 2;\n\tadd.s64 bb, %4, 2;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], a, bb, %6, t;\n\t"
+      "add.s64 a, %3, 4;\n\tadd.s64 bb, %4, 4;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], a, bb, %6, t;\n\t"
+      "add.s64 a, %3, 6;\n\tadd.s64 bb, %4, 6;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%1], a, bb, %6, t;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t}" ::"r"(d0),
+      "r"(d1), "l"(a0), "l"(a1), "l"(b), "r"(acc), "r"(idesc), "r"(su32(bar))
+      : "memory");
 }
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
-               : "memory");
+__device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(su32(bar))
+      : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -338,27 +356,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
     }
   } else if (warp == kWarpMma) {
-    if (lane == 0) {
-      const uint32_t idesc = idesc_16bit(n_mma, !f16);
-      bool ok = true;
-      for (int ks = 0; ks < nk && ok; ++ks) {
-        const int s = ks % kPfStages, r = ks / kPfStages;
-        ok = mbar_wait_fast(&full[s], r & 1, a.err);
-        if (!ok) break;
-        tc_fence_after();
-        const uint64_t bd = umma_desc_sw128(su32(sm + C::kOffB + s * C::kBTile));
-#pragma unroll
-        for (int mt = 0; mt < kPfMT; ++mt) {
-          const uint64_t ad = umma_desc_sw128(su32(sm + C::kOffA + s * kAStage + mt * kATile));
-#pragma unroll
-          for (int kk = 0; kk < kPfKStep / 16; ++kk)
-            mma_bf16(tmem + (uint32_t)(mt * 256), ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
-                     (ks | kk) != 0);
-        }
-        mma_commit(&empty[s]);
-      }
-      mma_commit(done);  // fires when every issued MMA has completed
+    // the whole warp runs the loop and one elected lane issues: operands stay
+    // warp-uniform, and a K step's MMAs and commit go out as one block
+    const uint32_t idesc = idesc_16bit(n_mma, !f16);
+    bool ok = true;
+    for (int ks = 0; ks < nk && ok; ++ks) {
+      const int s = ks % kPfStages, r = ks / kPfStages;
+      ok = __all_sync(0xffffffffu, mbar_wait_fast(&full[s], r & 1, a.err));
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t bd = umma_desc_sw128(su32(sm + C::kOffB + s * C::kBTile));
+      const uint64_t a0 = umma_desc_sw128(su32(sm + C::kOffA + s * kAStage));
+      const uint64_t a1 = umma_desc_sw128(su32(sm + C::kOffA + s * kAStage + kATile));
+      static_assert(kPfMT == 2 && kPfKStep == 64, "mma_kstep_2x4 covers two tiles x four K = 16 slices");
+      mma_kstep_2x4(tmem, tmem + 256u, a0, a1, bd, idesc, ks != 0, &empty[s]);
     }
+    mma_commit_elect(done);  // fires when every issued MMA has completed
   } else if (warp < kPfConvWarps) {
     // converters: group cg takes the K steps ks = cg (mod 3); thread -> row r
     // of both 128 x 64 A tiles (two 32-weight halves each)
