@@ -11,8 +11,10 @@
 //   group     pairs sorted by slot (stable counting sort, moe_group_pairs)
 //   items     per slot, tiles of <= 256 rows of its pairs
 //   gather    Xg[i] = x[token of the i-th sorted pair] (bf16 rows, 16-byte copies)
-//   GEMM1     per (item, 64-feature tile): D[128, n] = [W1;W3 interleaved] . Xg^T
-//             over K = H; epilogue h = SiLU(gate) * up -> bf16 rows of Hs
+//   GEMM1     per (item, 128-feature tile): D0[128, n] = W1 . Xg^T and
+//             D1[128, n] = W3 . Xg^T over K = H (same rows of both, so a
+//             thread's TMEM lane holds gate and up of one feature); epilogue
+//             h = SiLU(gate) * up -> bf16 rows of Hs
 //   GEMM2     per (item, 128-feature tile): D[128, n] = W2 . Hs^T over K = I;
 //             epilogue o[pair][feature] in fp32
 //   combine   y_t = sum_j w_tj o_tj in rank order -> bf16
@@ -270,8 +272,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // first weight row of this CTA: mode 0 -> feature f0 of w1 and of w3 (128
-  // features = 2 tiles of 64 gate/up pairs); mode 1 -> row f0 of w2 (256 rows)
+  // first weight row of this CTA: mode 0 -> feature f0 of w1 (tile 0) and of
+  // w3 (tile 1), 128 features each; mode 1 -> row f0 of w2 (256 rows)
   const int f0 = a.mode == 0 ? tile * 128 : tile * 256;
 
   // fp16 or bf16 operands for this tile: fp16 when every block scale of the
@@ -377,14 +379,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // of both 128 x 64 A tiles (two 32-weight halves each)
     const int cg = warp / (kPfConvThreads / 32);
     const int r = threadIdx.x & (kPfConvThreads - 1);
-    const int g = r & 1, i = r >> 1;  // mode 0: gate/up interleaved rows
     int raw_off[kPfMT];
     const uint8_t* srow[kPfMT];
 #pragma unroll
     for (int mt = 0; mt < kPfMT; ++mt) {
-      if (a.mode == 0) {
-        raw_off[mt] = g * (128 * 32) + (64 * mt + i) * 32;
-        srow[mt] = (g ? a.sc1 : a.sc0) + (size_t)it.slot * a.B + (size_t)(f0 + 64 * mt + i) * sbytes;
+      if (a.mode == 0) {  // tile 0: w1 row f0 + r (gate), tile 1: w3 row f0 + r (up)
+        raw_off[mt] = mt * (128 * 32) + r * 32;
+        srow[mt] = (mt ? a.sc1 : a.sc0) + (size_t)it.slot * a.B + (size_t)(f0 + r) * sbytes;
       } else {
         raw_off[mt] = (128 * mt + r) * 32;
         srow[mt] = a.sc0 + (size_t)it.slot * a.B + (size_t)(f0 + 128 * mt + r) * sbytes;
@@ -463,7 +464,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   }
 
   // epilogue: all 16 warps.  Warp w reads TMEM lane quadrant w % 4 and takes
-  // every fourth 16-column chunk (w / 4 picks which), over both accumulators.
+  // every fourth 16-column chunk (w / 4 picks which): gate/up reads the same
+  // chunk of both accumulators (gate and up of feature f0 + row), down each
+  // accumulator's chunks in turn.
   {
     __syncwarp();
     bool ok = mbar_wait(done, 0, a.err);
@@ -474,35 +477,39 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int q = warp & 3, part = warp >> 2;
     const int row = q * 32 + lane;  // D row = A tile row
     const int nchunks = n_mma / 16;
-    if (ok) {
+    const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+    if (ok && a.mode == 0) {
+      const int feat = f0 + row;
+      for (int c0 = part * 16; c0 < n_mma; c0 += kPfWarps / 4 * 16) {
+        uint32_t vg[16], vu[16];
+        tmem_ld16(tq + (uint32_t)c0, vg);
+        tmem_ld16(tq + (uint32_t)(256 + c0), vu);
+        // lane j < 16 holds column c0 + j's power-of-two rescale of the fp16 activation copy
+        const int cl = c0 + (lane & 15);
+        const int sgl = (f16 && cl < it.count) ? a.xsig[it.row0 + cl] : 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int col = c0 + j;
+          const float sc = __uint_as_float((uint32_t)(127 + __shfl_sync(0xffffffffu, sgl, j)) << 23);
+          if (col < it.count) {
+            const float gt = __uint_as_float(vg[j]) * sc, up = __uint_as_float(vu[j]) * sc;
+            const float hv = __fdividef(gt, 1.f + __expf(-gt)) * up;
+            a.hs[(size_t)(it.row0 + col) * a.I + feat] = __float2bfloat16_rn(hv);
+          }
+        }
+      }
+    } else if (ok) {
       for (int cc = part; cc < kPfMT * nchunks; cc += kPfWarps / 4) {
         const int mt = cc / nchunks, c0 = (cc % nchunks) * 16;
         uint32_t v[16];
-        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(mt * 256 + c0), v);
-        if (a.mode == 0) {
-          const int feat = f0 + 64 * mt + (row >> 1);
+        tmem_ld16(tq + (uint32_t)(mt * 256 + c0), v);
+        const int feat = f0 + 128 * mt + row;
+        const int cl = c0 + (lane & 15);
+        const int pl = cl < it.count ? a.perm[it.row0 + cl] : 0;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = c0 + j;
-            // exact power-of-two rescale of the fp16 activation copy
-            const int sg = (f16 && col < it.count) ? a.xsig[it.row0 + col] : 0;
-            const float mine = __uint_as_float(v[j]) * __uint_as_float((uint32_t)(127 + sg) << 23);
-            const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-            if ((row & 1) == 0 && col < it.count) {
-              const float hv = __fdividef(mine, 1.f + __expf(-mine)) * other;
-              a.hs[(size_t)(it.row0 + col) * a.I + feat] = __float2bfloat16_rn(hv);
-            }
-          }
-        } else {
-          const int feat = f0 + 128 * mt + row;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = c0 + j;
-            if (col < it.count) {
-              const int p = a.perm[it.row0 + col];
-              a.o[(size_t)p * a.H + feat] = __uint_as_float(v[j]);
-            }
-          }
+        for (int j = 0; j < 16; ++j) {
+          const int p = __shfl_sync(0xffffffffu, pl, j);
+          if (c0 + j < it.count) a.o[(size_t)p * a.H + feat] = __uint_as_float(v[j]);
         }
       }
     }
@@ -744,7 +751,7 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
     else
       prefill_gemm_kernel<PfBig><<<max_items * pa.tiles, kPfThreads, PfBig::kSmem, stream>>>(a0, a1, bm, bm16, pa);
   };
-  // GEMM1: gate/up, 128 features (two tiles of 64 gate/up pairs) per CTA
+  // GEMM1: gate/up, 128 features (their w1 rows and their w3 rows) per CTA
   pa.mode = 0;
   pa.K = H;
   pa.tiles = I / 128;
