@@ -260,22 +260,25 @@ def run_ours(args):
     layer_shared = M.moe_fp8_expert_bytes(H, I)
 
     def measure(T):
-        cache.reset()
-        torch.cuda.synchronize()
-        if lfu_seed is not None:
-            M.moe_cache_seed_frequency(cache, lfu_seed)
         lg, xs, pf = inputs(T)
         y = torch.empty((T, H), dtype=torch.int16, device=dev)
-        for s in range(args.warmup):
-            runner.run(0, lg[s], xs[s], y, prefetch=pf[s] if pf else None)
-        torch.cuda.synchronize()
-        runner.check()
+
+        def fresh():
+            cache.reset()
+            torch.cuda.synchronize()
+            if lfu_seed is not None:
+                M.moe_cache_seed_frequency(cache, lfu_seed)
+            for s in range(args.warmup):
+                runner.run(0, lg[s], xs[s], y, prefetch=pf[s] if pf else None)
+            torch.cuda.synchronize()
+            runner.check()
+
+        # timed pass: no per-kernel events inside the timed steps
+        fresh()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
-        acct_gu_bytes, acct_layer_bytes, acct_gemm_bytes = 0, 0, 0
         misses0, bytes0 = runner.stats["misses"], runner.stats["bytes_copied"]
-        pairs_hit = 0
-        M.moe_profile_enable(True)
+        ids_seen = []
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
@@ -286,20 +289,34 @@ def run_ours(args):
             ev[i][0].record(stream)
             runner.run(0, lg[s], xs[s], y, prefetch=pf[s] if pf else None)
             ev[i][1].record(stream)
-            # accounting (outside the events): distinct experts per forward chunk
-            ids = runner.ids[:T]
-            d = int(torch.unique(ids).numel())
-            acct_gemm_bytes += d * gu_expert + T * H * 2 + T * k * I * 2
-            # the routed pairs take the grouped GEMM from 256 pairs per call on
-            acct_gu_bytes += gu_shared + T * H * 2 + T * I * 4 + (0 if T * k >= 256 else
-                                                                   d * gu_expert + T * k * I * 4)
-            acct_layer_bytes += d * Bx + layer_shared + 2 * T * H * 2
+            ids_seen.append(runner.ids[:T].clone())
         torch.cuda.synchronize()
         runner.check()
         if world > 1:
             dist.barrier()
         wall = time.perf_counter() - t0
         step_ms = [a.elapsed_time(b) for a, b in ev]
+        misses = runner.stats["misses"] - misses0
+        copied = runner.stats["bytes_copied"] - bytes0
+        # accounting: distinct experts per step
+        acct_gu_bytes, acct_layer_bytes, acct_gemm_bytes = 0, 0, 0
+        for ids in ids_seen:
+            d = int(torch.unique(ids).numel())
+            acct_gemm_bytes += d * gu_expert + T * H * 2 + T * k * I * 2
+            # the routed pairs take the grouped GEMM from 256 pairs per call on
+            acct_gu_bytes += gu_shared + T * H * 2 + T * I * 4 + (0 if T * k >= 256 else
+                                                                   d * gu_expert + T * k * I * 4)
+            acct_layer_bytes += d * Bx + layer_shared + 2 * T * H * 2
+        # profiled pass: the same steps again from the same cache state, each
+        # kernel bracketed by the library's events (for the breakdown only)
+        fresh()
+        M.moe_profile_enable(True)
+        for i in range(args.steps):
+            s = args.warmup + i
+            flush.zero_()
+            runner.run(0, lg[s], xs[s], y, prefetch=pf[s] if pf else None)
+        torch.cuda.synchronize()
+        runner.check()
         kt = {M.KERNEL_NAMES[kid]: M.moe_profile_query(kid) for kid in range(M.MOE_K_COUNT)}
         M.moe_profile_enable(False)
         ms, tps = aggregate(sum(step_ms) / len(step_ms), T, world, dev)
@@ -319,10 +336,10 @@ def run_ours(args):
             "gateup_ms": gu_ms / max(gu_n, 1), "gateup_launches": gu_n,
             "gateup_gbs": (acct_gu_bytes / max(gu_n, 1)) / (gu_ms / max(gu_n, 1) / 1e3) / 1e9,
             "gateup_bytes_per_launch": acct_gu_bytes / max(gu_n, 1),
-            "misses_per_step": (runner.stats["misses"] - misses0) / args.steps,
-            "host_link_gbs": ((runner.stats["bytes_copied"] - bytes0) / args.steps / (kt["copy_device"][0] / args.steps / 1e3)
+            "misses_per_step": misses / args.steps,
+            "host_link_gbs": (copied / args.steps / (kt["copy_device"][0] / args.steps / 1e3)
                               / 1e9 if kt["copy_device"][1] else None),
-            "h2d_gb_per_step": (runner.stats["bytes_copied"] - bytes0) / args.steps / 1e9,
+            "h2d_gb_per_step": copied / args.steps / 1e9,
             "kernel_ms": {n: round(v[0] / args.steps, 4) for n, v in kt.items() if v[1]},
             "launches": sum(v[1] for v in kt.values()),
             "wall_s": wall,
@@ -489,6 +506,18 @@ def run_other(args):
         torch.cuda.synchronize()
         return sum(a.elapsed_time(b) for a, b in ev) / n
 
+    def profiled(step_fn, n):
+        """Per-kernel totals of n more steps run with the library's kernel events
+        on (kept out of the timed steps)."""
+        M.moe_profile_enable(True)
+        for i in range(n):
+            flush.zero_()
+            step_fn(i)
+        torch.cuda.synchronize()
+        kt = {M.KERNEL_NAMES[kid]: M.moe_profile_query(kid) for kid in range(M.MOE_K_COUNT)}
+        M.moe_profile_enable(False)
+        return kt
+
     wl = {"prefill": configs.PREFILL, "ladder": configs.LADDER, "stack": configs.STACK}[args.workload]
     if args.workload == "prefill" and (args.prefill_experts or args.prefill_tokens):
         e = args.prefill_experts or wl.E
@@ -515,12 +544,10 @@ def run_other(args):
         for _ in range(args.warmup):
             one_pass(0)
         torch.cuda.synchronize()
-        M.moe_profile_enable(True)
         clocks.start()
         ms = timed(one_pass, args.steps)
         ck = clocks.stop()
-        kt = {M.KERNEL_NAMES[kid]: M.moe_profile_query(kid) for kid in range(M.MOE_K_COUNT)}
-        M.moe_profile_enable(False)
+        kt = profiled(one_pass, args.steps)
         per_layer = ms / nl
         out.update({"value": T / (per_layer / 1e3), "unit": UNIT, "ms_per_step": ms, "clocks": ck,
                     "gpu_launches": sum(v[1] for v in kt.values()),
@@ -561,17 +588,24 @@ def run_other(args):
         torch.cuda.synchronize()
         runner.check()
         m0 = runner.stats["misses"]
-        M.moe_profile_enable(True)
         clocks.start()
         ms = timed(lambda i: runner.run(0, lg[args.warmup + i], xs[args.warmup + i], y), args.steps)
         ck = clocks.stop()
         runner.check()
-        kt = {M.KERNEL_NAMES[kid]: M.moe_profile_query(kid) for kid in range(M.MOE_K_COUNT)}
-        M.moe_profile_enable(False)
+        m1 = runner.stats["misses"]
+        # the breakdown replays the same steps from the same cache state
+        cache.reset()
+        if c2 is not None:
+            c2.reset()
+        torch.cuda.synchronize()
+        for s in range(args.warmup):
+            runner.run(0, lg[s], xs[s], y)
+        kt = profiled(lambda i: runner.run(0, lg[args.warmup + i], xs[args.warmup + i], y), args.steps)
+        runner.check()
         out.update({"value": T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "clocks": ck,
                     "gpu_launches": sum(v[1] for v in kt.values()),
                     "kernel_ms_per_step": {nm: round(v[0] / args.steps, 4) for nm, v in kt.items() if v[1]},
-                    "misses_per_step": (runner.stats["misses"] - m0) / args.steps})
+                    "misses_per_step": (m1 - m0) / args.steps})
         if args.workload == "prefill":
             P = T * k
             flops = 6.0 * P * H * I
@@ -625,12 +659,10 @@ def run_other(args):
         for s in range(args.warmup):
             step(s)
         torch.cuda.synchronize()
-        M.moe_profile_enable(True)
         clocks.start()
         ms = timed(lambda i: step(args.warmup + i), args.steps)
         ck = clocks.stop()
-        kt = {M.KERNEL_NAMES[kid]: M.moe_profile_query(kid) for kid in range(M.MOE_K_COUNT)}
-        M.moe_profile_enable(False)
+        kt = profiled(lambda i: step(args.warmup + i), args.steps)
         # touched bytes per step: distinct experts per layer
         tb = 0
         for s in range(args.warmup, n):

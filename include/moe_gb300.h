@@ -425,6 +425,12 @@ moe_status moe_rms_carry(const uint16_t* y, int T, int H, float eps, uint16_t* x
  * moe_profile_enable(1) clears the record and starts collecting; (0) stops.
  * moe_profile_query synchronises on the recorded events and returns, for one
  * kernel id, the summed elapsed milliseconds and the number of launches.
+ * moe_profile_timeline synchronises likewise and writes, in recording order,
+ * up to `max` records (host arrays of length >= max): the kernel id and the
+ * start and stop times in milliseconds relative to the start of the first
+ * record, whatever stream each was launched on; *n receives the number of
+ * records held (which may exceed max).  MOE_ERR_ARG on a null pointer or
+ * max < 0.
  * ------------------------------------------------------------------------- */
 enum {
   MOE_K_ROUTER = 0, MOE_K_ENSURE, MOE_K_LADDER, MOE_K_GROUP, MOE_K_PLAN, MOE_K_GATEUP,
@@ -432,6 +438,7 @@ enum {
 };
 moe_status moe_profile_enable(int enable);
 moe_status moe_profile_query(int kernel, double* total_ms, int* launches);
+moe_status moe_profile_timeline(int max, int32_t* kernel, double* start_ms, double* stop_ms, int* n);
 
 /* Test hook for failure detection without a fault: launches one thread that
  * waits on an mbarrier nothing arrives on, with the library's bounded wait and

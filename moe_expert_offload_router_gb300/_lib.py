@@ -87,6 +87,7 @@ _SIGS = {
     "moe_debug_timeout_probe": (i32, [C.c_int64, vp, vp]),
     "moe_profile_enable": (i32, [i32]),
     "moe_profile_query": (i32, [i32, C.POINTER(C.c_double), C.POINTER(C.c_int)]),
+    "moe_profile_timeline": (i32, [i32, C.c_void_p, C.c_void_p, C.c_void_p, C.POINTER(C.c_int)]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -387,3 +388,15 @@ def moe_profile_query(kernel: int):
     ms, n = C.c_double(), C.c_int()
     _check(_lib.moe_profile_query(kernel, C.byref(ms), C.byref(n)))
     return ms.value, n.value
+
+
+def moe_profile_timeline():
+    """Every record since profiling was enabled, in recording order, as a list of
+    (kernel id, start ms, stop ms) relative to the first record's start."""
+    n = C.c_int()
+    z = (C.c_int32 * 1)(), (C.c_double * 1)(), (C.c_double * 1)()
+    _check(_lib.moe_profile_timeline(0, C.addressof(z[0]), C.addressof(z[1]), C.addressof(z[2]), C.byref(n)))
+    m = max(n.value, 1)
+    k, t0, t1 = (C.c_int32 * m)(), (C.c_double * m)(), (C.c_double * m)()
+    _check(_lib.moe_profile_timeline(m, C.addressof(k), C.addressof(t0), C.addressof(t1), C.byref(n)))
+    return [(int(k[i]), float(t0[i]), float(t1[i])) for i in range(min(m, n.value))]

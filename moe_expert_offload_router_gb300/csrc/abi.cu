@@ -591,6 +591,24 @@ moe_status moe_profile_query(int kernel, double* total_ms, int* launches) {
   return MOE_OK;
 }
 
+moe_status moe_profile_timeline(int max, int32_t* kernel, double* start_ms, double* stop_ms, int* n) {
+  clear_error();
+  MOE_ARG(max >= 0 && kernel && start_ms && stop_ms && n, "bad arguments");
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  *n = (int)g_prof.size();
+  for (int i = 0; i < (int)g_prof.size() && i < max; ++i) {
+    const ProfRec& r = g_prof[i];
+    MOE_CUDA(cudaEventSynchronize(r.stop));
+    float a = 0.f, b = 0.f;
+    MOE_CUDA(cudaEventElapsedTime(&a, g_prof[0].start, r.start));
+    MOE_CUDA(cudaEventElapsedTime(&b, g_prof[0].start, r.stop));
+    kernel[i] = r.kernel;
+    start_ms[i] = a;
+    stop_ms[i] = b;
+  }
+  return MOE_OK;
+}
+
 moe_status moe_debug_timeout_probe(int64_t limit_ns, int32_t* d_status, cudaStream_t stream) {
   clear_error();
   MOE_ARG(d_status != nullptr, "d_status is null");

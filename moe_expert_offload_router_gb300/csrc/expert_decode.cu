@@ -1119,15 +1119,20 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
     gb.o = a.o;
     if ((st = grouped_gemm_fp4(v, x, T, k, slots, gb, d_error, stream)) != MOE_OK) return st;
   }
-  const size_t plan_smem = (size_t)kMaxPlanPairs * 12 + 64 * 4;
-  if ((st = set_smem(plan_kernel, plan_smem)) != MOE_OK) return st;
-  {
-    ProfScope ps(MOE_K_PLAN, stream);
-    plan_kernel<<<1 + T, 1024, plan_smem, stream>>>(a);
-  }
-  if ((st = check_launch("plan_kernel")) != MOE_OK) return st;
-
+  // the plan groups the pairs and prepares the fp16 activations for the GEMV
+  // kernels; a routed-GEMM pass without the shared expert runs none of them
+  // (the grouping kernels of the GEMM check the slots)
   const bool gemv = !a.routed_gemm || a.shared != nullptr;
+  if (gemv) {
+    const size_t plan_smem = (size_t)kMaxPlanPairs * 12 + 64 * 4;
+    if ((st = set_smem(plan_kernel, plan_smem)) != MOE_OK) return st;
+    {
+      ProfScope ps(MOE_K_PLAN, stream);
+      plan_kernel<<<1 + T, 1024, plan_smem, stream>>>(a);
+    }
+    if ((st = check_launch("plan_kernel")) != MOE_OK) return st;
+  }
+
   const long long max_groups = (long long)T * k + (T + kG - 1) / kG + 1;
   const size_t gu_smem = (size_t)kG * v->H * 2 + 2 * kG * 4;
   const long long gu_items = max_groups * ((v->I + kRowsGateUp - 1) / kRowsGateUp);

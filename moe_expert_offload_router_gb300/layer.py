@@ -54,7 +54,7 @@ class DecodeLayerRunner:
     def __init__(self, cache: L.moe_cache, views: L.moe_expert_views, E: int, k: int,
                  T_max: int, device=None, int2_cache: Optional[L.moe_cache] = None,
                  ladder=None, assume_resident: bool = False, copy: str = "engine",
-                 overlap=False, copy_ctas: int = 64, graph: bool = False):
+                 overlap=False, copy_ctas: int = 32, graph: bool = False):
         self.cache, self.views, self.E, self.k, self.T_max = cache, views, E, k, T_max
         self.dev = torch.device(device or "cuda")
         self.c2, self.ladder = int2_cache, ladder
