@@ -248,6 +248,18 @@ moe_status moe_copy_missing_device(moe_cache* cache, const int32_t* d_miss_key,
                                    const int32_t* d_miss_slot, const int32_t* d_miss_count,
                                    int max_ctas, cudaStream_t stream);
 
+/* The same copy for one part of the list: with n = *d_miss_count, part p of
+ * n_parts copies the entries [n * p / n_parts, n * (p + 1) / n_parts) (integer
+ * division; a part may be empty).  Launching parts 0..n_parts-1 in order with
+ * an event after each lets moe_expert_forward_overlap_parts compute each
+ * part's pairs as soon as that part has landed.  1 <= n_parts <=
+ * MOE_MAX_COPY_PARTS, else MOE_ERR_INVALID.  moe_copy_missing_device is part 0
+ * of 1. */
+#define MOE_MAX_COPY_PARTS 4
+moe_status moe_copy_missing_device_part(moe_cache* cache, const int32_t* d_miss_key,
+                                        const int32_t* d_miss_slot, const int32_t* d_miss_count,
+                                        int part, int n_parts, int max_ctas, cudaStream_t stream);
+
 /* ---------------------------------------------------------------------------
  * Whole-layer streaming for prefill past the crossover.  "Running DeepSeek-
  * V4-Flash across four free GPUs", section "What the expert cache actually
@@ -363,6 +375,14 @@ moe_status moe_expert_forward(const moe_expert_views* v, const uint16_t* x, int 
  *   d_error         as moe_expert_forward (cleared by the call)
  * The result equals moe_expert_forward's for the same slots (one combine over
  * all pairs in rank order).  Limits: T * k <= 4096, FP4 pool, no tags.
+ *
+ * moe_expert_forward_overlap_parts splits the missed pairs further by the part
+ * of the miss list (as moe_copy_missing_device_part divides it) their slot is
+ * in: after the first pass the stream waits on parts_done[p] and computes
+ * part p's pairs, for p = 0..n_parts-1, so only the last part's pairs follow
+ * the last copy.  parts_done: host array of n_parts events (NULL entries:
+ * already complete); 1 <= n_parts <= MOE_MAX_COPY_PARTS.  The workspace size
+ * covers every n_parts; the result is the same as moe_expert_forward's.
  * ------------------------------------------------------------------------- */
 size_t moe_expert_forward_overlap_workspace(const moe_expert_views* v, int T, int k);
 moe_status moe_expert_forward_overlap(const moe_expert_views* v, const uint16_t* x, int T, int k,
@@ -370,6 +390,11 @@ moe_status moe_expert_forward_overlap(const moe_expert_views* v, const uint16_t*
                                       const int32_t* d_miss_count, int max_miss, cudaEvent_t copies_done,
                                       uint16_t* y, void* workspace, size_t workspace_bytes,
                                       int32_t* d_error, cudaStream_t stream);
+moe_status moe_expert_forward_overlap_parts(const moe_expert_views* v, const uint16_t* x, int T, int k,
+                                            const int32_t* slots, const float* w, const int32_t* d_miss_slot,
+                                            const int32_t* d_miss_count, int max_miss, int n_parts,
+                                            const cudaEvent_t* parts_done, uint16_t* y, void* workspace,
+                                            size_t workspace_bytes, int32_t* d_error, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Grouped-GEMM expert MLP for prefill-sized batches ("Running DeepSeek-V4-

@@ -63,6 +63,7 @@ _SIGS = {
     "moe_debug_fail_copy": (i32, [vp, i32]),
     "moe_copy_layer": (i32, [vp, i32, i32, sz, vp, vp]),
     "moe_copy_missing_device": (i32, [vp, vp, vp, vp, i32, vp]),
+    "moe_copy_missing_device_part": (i32, [vp, vp, vp, vp, i32, i32, i32, vp]),
     "moe_cache_set_policy": (i32, [vp, i32, i32]),
     "moe_cache_seed_frequency": (i32, [vp, vp]),
     "moe_cache_export_frequency": (i32, [vp, vp, vp, vp]),
@@ -79,6 +80,8 @@ _SIGS = {
     "moe_expert_forward_overlap_workspace": (sz, [C.POINTER(moe_expert_views), i32, i32]),
     "moe_expert_forward_overlap": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, i32, vp,
                                          vp, vp, sz, vp, vp]),
+    "moe_expert_forward_overlap_parts": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, i32,
+                                               i32, vp, vp, vp, sz, vp, vp]),
     "moe_expert_forward_noalloc": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, vp, vp]),
     "moe_expert_prefill_workspace": (sz, [C.POINTER(moe_expert_views), i32, i32]),
     "moe_expert_prefill": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, sz, vp, vp]),
@@ -273,6 +276,15 @@ def moe_copy_missing_device(cache: moe_cache, d_miss_key, d_miss_slot, d_miss_co
                                         max_ctas, _s(stream)))
 
 
+MOE_MAX_COPY_PARTS = 4
+
+
+def moe_copy_missing_device_part(cache: moe_cache, d_miss_key, d_miss_slot, d_miss_count, part: int,
+                                 n_parts: int, stream=None, max_ctas: int = 0):
+    _check(_lib.moe_copy_missing_device_part(cache.handle, _p(d_miss_key), _p(d_miss_slot), _p(d_miss_count),
+                                             part, n_parts, max_ctas, _s(stream)))
+
+
 def moe_copy_layer(h_bank, layer_id: int, num_experts: int, expert_bytes: int, d_buf, stream=None):
     _check(_lib.moe_copy_layer(_p(h_bank), layer_id, num_experts, expert_bytes, _p(d_buf), _s(stream)))
 
@@ -334,6 +346,18 @@ def moe_expert_forward_overlap(views: moe_expert_views, x, slots, w, d_miss_slot
                                            _p(d_miss_count), max_miss, _e(copies_done), _p(y), _p(workspace),
                                            workspace.numel() * workspace.element_size(), _p(d_error),
                                            _s(stream)))
+
+
+def moe_expert_forward_overlap_parts(views: moe_expert_views, x, slots, w, d_miss_slot, d_miss_count,
+                                     max_miss: int, parts_done, y, workspace, d_error=None, stream=None):
+    """parts_done: one event (or None) per part of the miss list, in part order."""
+    T, k = slots.shape
+    n = len(parts_done)
+    evs = (C.c_void_p * max(n, 1))(*[_e(e) for e in parts_done])
+    _check(_lib.moe_expert_forward_overlap_parts(C.byref(views), _p(x), T, k, _p(slots), _p(w), _p(d_miss_slot),
+                                                 _p(d_miss_count), max_miss, n, C.addressof(evs), _p(y),
+                                                 _p(workspace), workspace.numel() * workspace.element_size(),
+                                                 _p(d_error), _s(stream)))
 
 
 def moe_expert_forward_noalloc(views: moe_expert_views, x, slots, tags, w, y, d_error=None, stream=None):

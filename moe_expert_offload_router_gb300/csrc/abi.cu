@@ -199,16 +199,20 @@ __device__ __forceinline__ void copy_units(const CacheDev& c, const uint8_t* ban
 // host-device link) and stores into the slots; reads the miss list and count
 // on the device, so it needs no host round trip.  16-byte units, four loads in
 // flight per thread before their stores.
+// Part `part` of `parts` takes the list entries [n * part / parts, n * (part + 1) / parts).
 __global__ void __launch_bounds__(256) copy_missing_kernel(CacheDev c, const uint8_t* bank, uint8_t* slots,
                                                            size_t B, const int32_t* miss_key,
-                                                           const int32_t* miss_slot, const int32_t* miss_count) {
+                                                           const int32_t* miss_slot, const int32_t* miss_count,
+                                                           int part, int parts) {
   const int n = *miss_count;
   if (n <= 0) return;
-  const size_t total = (size_t)n * (B / 16);
+  const int m0 = (int)((long long)n * part / parts), m1 = (int)((long long)n * (part + 1) / parts);
+  if (m1 <= m0) return;
+  const size_t total = (size_t)(m1 - m0) * (B / 16);
   if (total < 0xFFFFFFFFull)
-    copy_units<uint32_t>(c, bank, slots, B, miss_key, miss_slot, (uint32_t)total);
+    copy_units<uint32_t>(c, bank, slots, B, miss_key + m0, miss_slot + m0, (uint32_t)total);
   else
-    copy_units<size_t>(c, bank, slots, B, miss_key, miss_slot, total);
+    copy_units<size_t>(c, bank, slots, B, miss_key + m0, miss_slot + m0, total);
 }
 
 // One thread waits on an mbarrier that nothing arrives on; the bounded wait
@@ -476,22 +480,30 @@ moe_status moe_cache_export_staging(moe_cache* c, int32_t* h_stage_key, uint32_t
   return MOE_OK;
 }
 
-moe_status moe_copy_missing_device(moe_cache* c, const int32_t* d_miss_key, const int32_t* d_miss_slot,
-                                   const int32_t* d_miss_count, int max_ctas, cudaStream_t stream) {
+moe_status moe_copy_missing_device_part(moe_cache* c, const int32_t* d_miss_key, const int32_t* d_miss_slot,
+                                        const int32_t* d_miss_count, int part, int n_parts, int max_ctas,
+                                        cudaStream_t stream) {
   clear_error();
   MOE_ARG(c != nullptr, "cache is null");
   MOE_ARG(d_miss_key && d_miss_slot && d_miss_count, "null miss list");
   MOE_ARG(c->bank_dev != nullptr, "the host bank is not mapped into the device address space");
   MOE_ARG(c->B % 16 == 0, "expert bytes %zu not a multiple of 16", c->B);
+  MOE_ARG(n_parts >= 1 && n_parts <= MOE_MAX_COPY_PARTS && part >= 0 && part < n_parts,
+          "part %d of %d: need 0 <= part < n_parts <= %d", part, n_parts, MOE_MAX_COPY_PARTS);
+  MOE_ARG(max_ctas >= 0, "max_ctas < 0");
   int dev = 0, sms = 1;
   MOE_CUDA(cudaGetDevice(&dev));
   MOE_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   ProfScope ps(MOE_K_COPY, stream);
-  MOE_ARG(max_ctas >= 0, "max_ctas < 0");
   const int grid = max_ctas > 0 && max_ctas < sms * 4 ? max_ctas : sms * 4;
   copy_missing_kernel<<<grid, 256, 0, stream>>>(c->dev, c->bank_dev, c->d_slots, c->B, d_miss_key, d_miss_slot,
-                                                  d_miss_count);
+                                                  d_miss_count, part, n_parts);
   return check_launch("copy_missing_kernel");
+}
+
+moe_status moe_copy_missing_device(moe_cache* c, const int32_t* d_miss_key, const int32_t* d_miss_slot,
+                                   const int32_t* d_miss_count, int max_ctas, cudaStream_t stream) {
+  return moe_copy_missing_device_part(c, d_miss_key, d_miss_slot, d_miss_count, 0, 1, max_ctas, stream);
 }
 
 moe_status moe_copy_layer(const void* h_bank, int layer_id, int num_experts, size_t expert_bytes, void* d_buf,

@@ -1169,33 +1169,36 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
   return check_launch("combine_kernel");
 }
 
-// Splits the pairs of a chunk by whether their slot is on the miss list:
-// hit[p] keeps the slot of pairs whose expert was resident, miss[p] the slot
-// of pairs whose expert is being copied in (every other entry -1).
+// Splits the pairs of a chunk by whether their slot is on the miss list, and
+// the missed ones by the part of the list (as the part-wise copy divides it:
+// part q holds entries [n * q / parts, n * (q + 1) / parts)): hit[p] keeps the
+// slot of pairs whose expert was resident, miss[q * P + p] the slot of pairs
+// whose expert is copied in with part q (every other entry -1).
 __global__ void __launch_bounds__(1024) split_miss_kernel(const int32_t* slots, int P, const int32_t* miss_slot,
                                                           const int32_t* miss_count, int max_miss, int S,
-                                                          int32_t* hit, int32_t* miss) {
-  extern __shared__ uint32_t bits[];
-  const int nw = (S + 31) >> 5;
-  for (int i = threadIdx.x; i < nw; i += blockDim.x) bits[i] = 0;
+                                                          int parts, int32_t* hit, int32_t* miss) {
+  extern __shared__ int8_t part_of[];  // [S]: part of the slot's miss, -1 if not missed
+  for (int i = threadIdx.x; i < S; i += blockDim.x) part_of[i] = -1;
   __syncthreads();
   const int n = min(max(*miss_count, 0), max_miss);
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const int sl = miss_slot[i];
-    if (sl >= 0 && sl < S) atomicOr(&bits[sl >> 5], 1u << (sl & 31));
+    int q = 0;
+    while (q + 1 < parts && (long long)n * (q + 1) / parts <= i) ++q;
+    if (sl >= 0 && sl < S) part_of[sl] = (int8_t)q;
   }
   __syncthreads();
   for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < P; p += gridDim.x * blockDim.x) {
     const int sl = slots[p];
-    const bool m = sl >= 0 && sl < S && ((bits[sl >> 5] >> (sl & 31)) & 1u);
-    hit[p] = m ? -1 : sl;
-    miss[p] = m ? sl : -1;
+    const int q = (sl >= 0 && sl < S) ? part_of[sl] : -1;
+    hit[p] = q >= 0 ? -1 : sl;
+    for (int r = 0; r < parts; ++r) miss[(size_t)r * P + p] = q == r ? sl : -1;
   }
 }
 
 static size_t overlap_extra(const moe_expert_views* v, int T, int k, const FwdLayout& L) {
   const size_t P = (size_t)T * k;
-  size_t b = 2 * align256(P * 4);
+  size_t b = align256(P * 4) + align256((size_t)MOE_MAX_COPY_PARTS * P * 4);
   if (L.gemm) b += align256(P * v->H * 4 + P * v->I * 2);
   return b;
 }
@@ -1233,19 +1236,22 @@ extern "C" size_t moe_expert_forward_overlap_workspace(const moe_expert_views* v
   return L.total + overlap_extra(v, T, k, L);
 }
 
-extern "C" moe_status moe_expert_forward_overlap(const moe_expert_views* v, const uint16_t* x, int T, int k,
-                                                 const int32_t* slots, const float* w, const int32_t* d_miss_slot,
-                                                 const int32_t* d_miss_count, int max_miss,
-                                                 cudaEvent_t copies_done, uint16_t* y, void* workspace,
-                                                 size_t workspace_bytes, int32_t* d_error, cudaStream_t stream) {
+extern "C" moe_status moe_expert_forward_overlap_parts(const moe_expert_views* v, const uint16_t* x, int T, int k,
+                                                       const int32_t* slots, const float* w,
+                                                       const int32_t* d_miss_slot, const int32_t* d_miss_count,
+                                                       int max_miss, int n_parts, const cudaEvent_t* parts_done,
+                                                       uint16_t* y, void* workspace, size_t workspace_bytes,
+                                                       int32_t* d_error, cudaStream_t stream) {
   clear_error();
   moe_status st = validate_views(v);
   if (st != MOE_OK) return st;
   MOE_ARG(T >= 0 && k >= 1 && k <= 64, "need T >= 0 and 1 <= k <= 64");
+  MOE_ARG(n_parts >= 1 && n_parts <= MOE_MAX_COPY_PARTS, "n_parts %d outside [1, %d]", n_parts,
+          MOE_MAX_COPY_PARTS);
   if (T == 0) return MOE_OK;
   MOE_ARG((long long)T * k <= kMaxPlanPairs, "T * k = %lld above the %d pairs of one overlapped call",
           (long long)T * k, kMaxPlanPairs);
-  MOE_ARG(x && slots && w && y && workspace && d_miss_slot && d_miss_count, "null pointer");
+  MOE_ARG(x && slots && w && y && workspace && d_miss_slot && d_miss_count && parts_done, "null pointer");
   MOE_ARG(v->fp4_slots != nullptr, "no FP4 pool");
   MOE_ARG(max_miss >= 0, "max_miss < 0");
   MOE_ARG(((uintptr_t)workspace & 255) == 0, "workspace must be 256-byte aligned");
@@ -1256,26 +1262,32 @@ extern "C" moe_status moe_expert_forward_overlap(const moe_expert_views* v, cons
   const size_t P = (size_t)T * k;
   int32_t* hit = (int32_t*)(base + L.total);
   int32_t* miss = (int32_t*)(base + L.total + align256(P * 4));
-  uint8_t* gemm_bufs = L.gemm ? base + L.total + 2 * align256(P * 4) : nullptr;
+  uint8_t* gemm_bufs =
+      L.gemm ? base + L.total + align256(P * 4) + align256((size_t)MOE_MAX_COPY_PARTS * P * 4) : nullptr;
   if (d_error) MOE_CUDA(cudaMemsetAsync(d_error, 0, sizeof(int32_t), stream));
   const int S = v->fp4_num_slots;
-  const size_t bits = (size_t)((S + 31) / 32) * 4;
-  if ((st = set_smem(split_miss_kernel, bits)) != MOE_OK) return st;
-  split_miss_kernel<<<(int)((P + 1023) / 1024), 1024, bits, stream>>>(slots, (int)P, d_miss_slot, d_miss_count,
-                                                                      max_miss, S, hit, miss);
+  if ((st = set_smem(split_miss_kernel, (size_t)S)) != MOE_OK) return st;
+  split_miss_kernel<<<(int)((P + 1023) / 1024), 1024, (size_t)S, stream>>>(slots, (int)P, d_miss_slot,
+                                                                          d_miss_count, max_miss, S, n_parts,
+                                                                          hit, miss);
   if ((st = check_launch("split_miss_kernel")) != MOE_OK) return st;
   // pass 1: pairs whose experts were resident, and the shared expert, while
   // the misses are still being copied
   FwdPass p1;
   p1.combine = false;
   if ((st = forward_pass(v, x, T, k, hit, nullptr, w, y, base, L, d_error, stream, p1)) != MOE_OK) return st;
-  if (copies_done) MOE_CUDA(cudaStreamWaitEvent(stream, copies_done, 0));
-  // pass 2: the pairs whose experts have just been copied in
-  FwdPass p2;
-  p2.shared = false;
-  p2.combine = false;
-  p2.gemm_bufs = gemm_bufs;
-  if ((st = forward_pass(v, x, T, k, miss, nullptr, w, y, base, L, d_error, stream, p2)) != MOE_OK) return st;
+  // then each part's pairs once that part's copies have landed; the passes
+  // run in order on the stream, so they can share the GEMM's buffers
+  for (int q = 0; q < n_parts; ++q) {
+    if (parts_done[q]) MOE_CUDA(cudaStreamWaitEvent(stream, parts_done[q], 0));
+    FwdPass p2;
+    p2.shared = false;
+    p2.combine = false;
+    p2.gemm_bufs = gemm_bufs;
+    if ((st = forward_pass(v, x, T, k, miss + (size_t)q * P, nullptr, w, y, base, L, d_error, stream, p2)) !=
+        MOE_OK)
+      return st;
+  }
   // one combine over every pair of the chunk
   FwdArgs a{};
   a.H = v->H;
@@ -1295,6 +1307,15 @@ extern "C" moe_status moe_expert_forward_overlap(const moe_expert_views* v, cons
   ProfScope ps(MOE_K_COMBINE, stream);
   combine_kernel<<<cg, 256, 0, stream>>>(a);
   return check_launch("combine_kernel");
+}
+
+extern "C" moe_status moe_expert_forward_overlap(const moe_expert_views* v, const uint16_t* x, int T, int k,
+                                                 const int32_t* slots, const float* w, const int32_t* d_miss_slot,
+                                                 const int32_t* d_miss_count, int max_miss,
+                                                 cudaEvent_t copies_done, uint16_t* y, void* workspace,
+                                                 size_t workspace_bytes, int32_t* d_error, cudaStream_t stream) {
+  return moe_expert_forward_overlap_parts(v, x, T, k, slots, w, d_miss_slot, d_miss_count, max_miss, 1,
+                                          &copies_done, y, workspace, workspace_bytes, d_error, stream);
 }
 
 // ------------------------------------------------------ allocation-free entry --

@@ -54,7 +54,7 @@ class DecodeLayerRunner:
     def __init__(self, cache: L.moe_cache, views: L.moe_expert_views, E: int, k: int,
                  T_max: int, device=None, int2_cache: Optional[L.moe_cache] = None,
                  ladder=None, assume_resident: bool = False, copy: str = "engine",
-                 overlap=False, copy_ctas: int = 32, graph: bool = False):
+                 overlap=False, copy_ctas: int = 32, graph: bool = False, copy_parts: int = 1):
         self.cache, self.views, self.E, self.k, self.T_max = cache, views, E, k, T_max
         self.dev = torch.device(device or "cuda")
         self.c2, self.ladder = int2_cache, ladder
@@ -88,6 +88,10 @@ class DecodeLayerRunner:
         if overlap and copy != "device":
             raise ValueError("overlap needs copy='device'")
         self.overlap, self.copy_ctas = overlap, copy_ctas
+        if not 1 <= copy_parts <= L.MOE_MAX_COPY_PARTS:
+            raise ValueError(f"copy_parts must be in [1, {L.MOE_MAX_COPY_PARTS}]")
+        self.copy_parts = copy_parts
+        self.part_done = [torch.cuda.Event() for _ in range(copy_parts)]
         self.ws_ov = (torch.empty(L.moe_expert_forward_overlap_workspace(views, T_max, k), dtype=torch.uint8,
                                   device=dev) if overlap else None)
         self.status_h = torch.zeros(4, dtype=torch.int32, pin_memory=True)
@@ -108,14 +112,18 @@ class DecodeLayerRunner:
         self.assume_resident = assume_resident
         if assume_resident and cache.S < cache.L * cache.E:
             raise ValueError("assume_resident needs a cache with a slot for every key")
+        self._vcache = None   # views into self.info, built on first use
         self.stats = {"misses": 0, "hits_pairs": 0, "calls": 0, "bytes_copied": 0, "chunks": 0}
 
     def _views(self, t):
+        if self._vcache is not None:
+            return self._vcache
         i = self.info
         m4, m2 = self.m4, self.m2
-        return dict(count4=i[0:1], done=i[1:2], count2=i[2:3], keys4=i[4:4 + m4],
+        self._vcache = dict(count4=i[0:1], done=i[1:2], count2=i[2:3], keys4=i[4:4 + m4],
                     slots4=i[4 + m4:4 + 2 * m4], keys2=i[4 + 2 * m4:4 + 2 * m4 + m2],
                     slots2=i[4 + 2 * m4 + m2:4 + 2 * m4 + 2 * m2])
+        return self._vcache
 
     def prefetch(self, layer_id: int, d_experts, stream=None):
         """Stages predicted experts of `layer_id` (device int32 ids) in the cache's
@@ -159,24 +167,30 @@ class DecodeLayerRunner:
         while tb < T:
             L.moe_slot_ensure(self.cache, layer_id, ids, slots, 0, k, L.MOE_FETCH_MARK_REST, tb,
                               v["keys4"], v["slots4"], v["count4"], v["done"], stream)
+            overlap = self.overlap is True or (self.overlap == "auto" and T * k >= self.OVERLAP_MIN_PAIRS)
+            if overlap:
+                # copies on the side stream, in parts, launched first: they are
+                # the step's critical path
+                self.ready.record(stream)
+                self.copy_stream.wait_event(self.ready)
+                for q, ev in enumerate(self.part_done):
+                    L.moe_copy_missing_device_part(self.cache, v["keys4"], v["slots4"], v["count4"], q,
+                                                   self.copy_parts, self.copy_stream, self.copy_ctas)
+                    ev.record(self.copy_stream)
             with torch.cuda.stream(stream):
                 self.status_h.copy_(self.info[0:4], non_blocking=True)
             if not self._capturing:      # a replayed graph records it after the replay
                 self.status_ev.record(stream)
             self.stats["chunks"] += 1
-            if self.overlap is True or (self.overlap == "auto" and T * k >= self.OVERLAP_MIN_PAIRS):
-                # copies on the side stream; resident experts' pairs compute meanwhile
-                self.ready.record(stream)
-                self.copy_stream.wait_event(self.ready)
-                L.moe_copy_missing_device(self.cache, v["keys4"], v["slots4"], v["count4"], self.copy_stream,
-                                          self.copy_ctas)
-                self.done.record(self.copy_stream)
+            if overlap:
+                # resident experts' pairs compute meanwhile, then each part's
+                # pairs once it has landed
                 if prefetch is not None:   # after this chunk's own copies on the side stream
                     self.prefetch(*prefetch, stream=stream)
                     prefetch = None
-                L.moe_expert_forward_overlap(self.views, x[tb:T], slots[tb:T], w[tb:T], v["slots4"],
-                                             v["count4"], self.m4, self.done, y[tb:T], self.ws_ov, self.err,
-                                             stream)
+                L.moe_expert_forward_overlap_parts(self.views, x[tb:T], slots[tb:T], w[tb:T], v["slots4"],
+                                                   v["count4"], self.m4, self.part_done, y[tb:T], self.ws_ov,
+                                                   self.err, stream)
             else:
                 self._wait_prefetch(stream)
                 L.moe_copy_missing_device(self.cache, v["keys4"], v["slots4"], v["count4"], stream)

@@ -50,6 +50,37 @@ def test_copy_missing_device_bytes():
     cache.close()
 
 
+@pytest.mark.parametrize("n", [0, 1, 2, 5, 7])
+def test_copy_missing_device_parts(n):
+    # part q of n_parts copies list entries [n q / n_parts, n (q + 1) / n_parts)
+    M = load_lib()
+    wl = configs.scaled(configs.TINY, E=16)
+    bank, B, slots, cache = _cache(M, wl, 8)
+    b = bank.numpy().reshape(wl.E, B)
+    rng = np.random.default_rng(40 + n)
+    keys_np = rng.choice(wl.E, size=n, replace=False).astype(np.int32)
+    sl_np = rng.choice(8, size=n, replace=False).astype(np.int32)
+    keys = torch.from_numpy(np.concatenate([keys_np, [0]]).astype(np.int32)).cuda()
+    sl = torch.from_numpy(np.concatenate([sl_np, [0]]).astype(np.int32)).cuda()
+    cnt = torch.tensor([n], dtype=torch.int32, device="cuda")
+    for parts in (1, 2, 3, 4):
+        for q in range(parts):
+            slots.zero_()
+            M.moe_copy_missing_device_part(cache, keys, sl, cnt, q, parts)
+            torch.cuda.synchronize()
+            got = slots.cpu().numpy().reshape(8, B)
+            mine = set(range(n * q // parts, n * (q + 1) // parts))
+            for i in range(n):
+                if i in mine:
+                    assert np.array_equal(got[sl_np[i]], b[keys_np[i]])
+                else:
+                    assert not got[sl_np[i]].any()
+    for bad in ((0, 0), (1, 1), (0, M.MOE_MAX_COPY_PARTS + 1), (-1, 2)):
+        with pytest.raises(M.MoeError):
+            M.moe_copy_missing_device_part(cache, keys, sl, cnt, *bad)
+    cache.close()
+
+
 def test_copy_missing_device_full_size_expert():
     M = load_lib()
     wl = configs.scaled(configs.DECODE, E=4)

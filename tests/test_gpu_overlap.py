@@ -20,17 +20,19 @@ pytestmark = pytest.mark.gpu
 TOL = 2e-2
 
 
-def _overlap(M, P, x_bits, slots, w, miss_slots, event=None):
+def _overlap(M, P, x_bits, slots, w, miss_slots, event=None, parts=None):
     T, k = slots.shape
     y = torch.empty((T, P.wl.H), dtype=torch.int16, device="cuda")
     ws = torch.empty(M.moe_expert_forward_overlap_workspace(P.views, T, k), dtype=torch.uint8, device="cuda")
     err = torch.full((1,), -5, dtype=torch.int32, device="cuda")
     ms = torch.tensor(list(miss_slots) + [0], dtype=torch.int32, device="cuda")
     cnt = torch.tensor([len(miss_slots)], dtype=torch.int32, device="cuda")
-    M.moe_expert_forward_overlap(P.views, torch.from_numpy(x_bits.view(np.int16)).cuda(),
-                                 torch.from_numpy(slots.astype(np.int32)).cuda(),
-                                 torch.from_numpy(w.astype(np.float32)).cuda(), ms, cnt, len(miss_slots) + 1,
-                                 event, y, ws, err)
+    args = (P.views, torch.from_numpy(x_bits.view(np.int16)).cuda(), torch.from_numpy(slots.astype(np.int32)).cuda(),
+            torch.from_numpy(w.astype(np.float32)).cuda(), ms, cnt, len(miss_slots) + 1)
+    if parts is None:
+        M.moe_expert_forward_overlap(*args, event, y, ws, err)
+    else:
+        M.moe_expert_forward_overlap_parts(*args, [event] * parts, y, ws, err)
     torch.cuda.synchronize()
     return y.cpu().numpy(), int(err)
 
@@ -53,6 +55,37 @@ def test_overlap_equals_forward_decode_shape(T, nmiss):
     assert np.array_equal(y0, y1)
     sample = sorted({0, T // 2, T - 1})
     assert bf16_rel_err(y1[sample], P.reference(x, slots, None, w, tokens=sample)) <= TOL
+
+
+@pytest.mark.parametrize("T,nmiss,parts", [(64, 9, 2), (64, 9, 4), (64, 1, 3), (64, 64, 3), (16, 5, 2),
+                                           (64, 0, 2)])
+def test_overlap_parts_equal_forward(T, nmiss, parts):
+    # misses split into parts as the part-wise copy divides the list (a part
+    # may be empty); every pair is still computed exactly once
+    M = load_lib()
+    wl = configs.DECODE
+    S = 64
+    P = Pools(M, wl, S, shared=True)
+    rng = np.random.default_rng(700 + T + nmiss + parts)
+    slots, w = _route(rng, T, wl.k, S)
+    misses = rng.choice(S, size=nmiss, replace=False) if nmiss < S else rng.permutation(S)
+    x = gen.activations(wl, 0, 9, T)
+    y0, e0 = P.forward(x, slots, None, w)
+    y1, e1 = _overlap(M, P, x, slots, w, misses, parts=parts)
+    assert e0 == 0 and e1 == 0
+    assert np.array_equal(y0, y1)
+
+
+def test_overlap_parts_rejects_bad_count():
+    M = load_lib()
+    wl = configs.TINY
+    P = Pools(M, wl, 4, shared=True)
+    x = gen.activations(wl, 0, 1, 2)
+    slots = np.array([[0, 1], [2, 3]])
+    w = np.full((2, 2), 0.5, np.float32)
+    for parts in (0, M.MOE_MAX_COPY_PARTS + 1):
+        with pytest.raises(M.MoeError):
+            _overlap(M, P, x, slots, w, [1], parts=parts)
 
 
 def test_overlap_small_all_tokens_and_error_clearing():
@@ -95,19 +128,20 @@ def _decoder(bank_np, B, wl):
     return f
 
 
-@pytest.mark.parametrize("wl,S,steps,full", [
-    (configs.TINY, 4, 6, True),                                   # chunked
-    (configs.scaled(configs.DECODE, T=4), 64, 4, False),          # single chunk, CUDA-core path
-    (configs.scaled(configs.DECODE, T=64), 40, 3, False),         # chunked, grouped GEMM
+@pytest.mark.parametrize("wl,S,steps,full,parts", [
+    (configs.TINY, 4, 6, True, 2),                                   # chunked
+    (configs.scaled(configs.DECODE, T=4), 64, 4, False, 1),          # single chunk, CUDA-core path
+    (configs.scaled(configs.DECODE, T=64), 40, 3, False, 2),         # chunked, grouped GEMM
+    (configs.scaled(configs.DECODE, T=64), 64, 3, False, 3),         # grouped GEMM, three copy parts
 ])
-def test_layer_overlapped_copy(wl, S, steps, full):
+def test_layer_overlapped_copy(wl, S, steps, full, parts):
     M = load_lib()
     bank, B = pinned_fp4_bank(wl, (0,))
     slots = torch.empty(S * B, dtype=torch.uint8, device="cuda")
     cache = M.moe_cache(S, 1, wl.E, B, slots, bank)
     sh = torch.from_numpy(gen.shared_expert(wl, 0)).cuda() if wl.shared else None
     views = M.make_views(wl.H, wl.I, slots, S, None, 0, sh)
-    runner = M.DecodeLayerRunner(cache, views, wl.E, wl.k, wl.T, copy="device", overlap=True)
+    runner = M.DecodeLayerRunner(cache, views, wl.E, wl.k, wl.T, copy="device", overlap=True, copy_parts=parts)
     ref = SlotCacheLRU(S, 1, wl.E)
     dec = _decoder(bank.numpy(), B, wl)
     shw = F.decode_fp8_expert(gen.shared_expert(wl, 0), wl.H, wl.I) if wl.shared else None
