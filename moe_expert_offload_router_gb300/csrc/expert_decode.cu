@@ -1122,8 +1122,10 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
   // the plan groups the pairs and prepares the fp16 activations for the GEMV
   // kernels; a routed-GEMM pass without the shared expert runs none of them
   // (the grouping kernels of the GEMM check the slots)
-  const bool gemv = !a.routed_gemm || a.shared != nullptr;
-  if (gemv) {
+  // the shared expert takes the tensor cores too when the routed pairs do
+  const bool shared_gemm = a.routed_gemm && a.shared != nullptr;
+  const bool gemv = !a.routed_gemm;
+  if (gemv || shared_gemm) {
     const size_t plan_smem = (size_t)kMaxPlanPairs * 12 + 64 * 4;
     if ((st = set_smem(plan_kernel, plan_smem)) != MOE_OK) return st;
     {
@@ -1131,6 +1133,11 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
       plan_kernel<<<1 + T, 1024, plan_smem, stream>>>(a);
     }
     if ((st = check_launch("plan_kernel")) != MOE_OK) return st;
+  }
+  if (shared_gemm) {
+    // SwiGLU scratch in the shared expert's rows of h; output rows P .. P + T - 1 of o
+    __nv_bfloat16* hs_sh = reinterpret_cast<__nv_bfloat16*>(a.h + (size_t)a.P * a.I);
+    if ((st = grouped_gemm_shared_fp8(v, a.xs, a.xsig, T, hs_sh, a.o, a.P, d_error, stream)) != MOE_OK) return st;
   }
 
   const long long max_groups = (long long)T * k + (T + kG - 1) / kG + 1;

@@ -172,6 +172,24 @@ __device__ __forceinline__ void fp4x8_to_f16(uint32_t w, uint32_t& r0, uint32_t&
       : "r"(w));
 }
 
+// Four E4M3 codes (one 32-bit word, element j in byte j) -> two fp16 pairs (exact).
+__device__ __forceinline__ void fp8x4_to_f16(uint32_t w, uint32_t& r0, uint32_t& r1) {
+  asm("{\n\t.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, h0;\n\tcvt.rn.f16x2.e4m3x2 %1, h1;\n\t}"
+      : "=r"(r0), "=r"(r1)
+      : "r"(w));
+}
+
+// fp16 pair -> bf16 pair (exact for values with at most 8 significant bits)
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 l, u, bl, bu;\n\tmov.b32 {l, u}, %1;\n\tcvt.rn.bf16.f16 bl, l;\n\tcvt.rn.bf16.f16 bu, u;\n\t"
+      "mov.b32 %0, {bl, bu};\n\t}"
+      : "=r"(r)
+      : "r"(h));
+  return r;
+}
+
 // fp16 pair times the block scale 2^(e-127) given as fp16x2: exact when e is
 // within [kF16ScaleLo, kF16ScaleHi].
 __device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t s) {
@@ -221,9 +239,21 @@ struct PfArgs {
   __nv_bfloat16* hs;  // mode 0 output [P, I]
   float* o;           // mode 1 output [P, H] by pair
   int* err;
+  // row-scaled FP8 weights (the shared expert): per-row fp32 scales of w1 and
+  // w3 (mode 0) or w2 (mode 1); items are the row ranges [64 i, 64 i + 64) of
+  // `rows` rows, and mode 1 writes row r of the output at o[(o_row0 + r) * H]
+  const float* rs0;
+  const float* rs1;
+  int rows;
+  int o_row0;
 };
 
-template <class C>
+// FP8 = false: MXFP4 experts of the slot pool (E2M1 codes with E8M0 block
+// scales), items from the grouped pair list.  FP8 = true: one row-scaled E4M3
+// matrix pair (the shared expert) over all tokens: codes are read 64 bytes
+// per row per K step, decoded exactly to fp16 (mode 0) or bf16 (mode 1), and
+// the row scales are applied to the fp32 accumulators.
+template <class C, bool FP8>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
                         const __grid_constant__ CUtensorMap mB, const __grid_constant__ CUtensorMap mB16,
@@ -238,11 +268,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint64_t* done = rawe + C::kRaw;
   uint32_t* tmem_slot = (uint32_t*)(done + 1);
   int* f16_flag = (int*)(tmem_slot + 1);
+  // raw-code ring: FP8 rows take twice the bytes per K step, in half as many stages
+  constexpr int kRT = FP8 ? 2 * kRawTile : kRawTile;
+  constexpr int kRing = FP8 ? C::kRaw / 2 : C::kRaw;
+  constexpr int kRowB = FP8 ? 64 : 32;  // code bytes per weight row per K step
 
   const int item_idx = blockIdx.x / a.tiles;
   const int tile = blockIdx.x % a.tiles;
-  if (item_idx >= *a.n_items) return;
-  const PfItem it = a.items[item_idx];
+  PfItem it;
+  if (FP8) {
+    it.slot = 0;
+    it.row0 = item_idx * C::kNMax;
+    it.count = min(C::kNMax, a.rows - it.row0);
+    it.pad = 0;
+    if (it.count < 1) return;
+  } else {
+    if (item_idx >= *a.n_items) return;
+    it = a.items[item_idx];
+  }
   if (it.count > C::kNMax || it.count < 1) {  // the host picks the shape from T; never expected
     if (threadIdx.x == 0) atomicCAS(a.err, 0, MOE_ERR_INVALID);
     return;
@@ -259,12 +302,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_init(&full[s], kPfConvThreads + 1);
       mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < C::kRaw; ++s) {
+    for (int s = 0; s < kRing; ++s) {
       mbar_init(&rawf[s], 1);
       mbar_init(&rawe[s], kPfConvThreads);
     }
     mbar_init(done, 1);
-    *f16_flag = (a.mode == 0 && a.allow_f16) ? 1 : 0;
+    // E4M3 values are exact in fp16 (gate/up runs against the fp16 activation copy)
+    *f16_flag = (a.mode == 0 && (FP8 || a.allow_f16)) ? 1 : 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kWarpMma) {
@@ -286,7 +330,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   // runs in every warp but the raw-code producer, which starts streaming at once.
   bool f16 = false;
   if (warp != kWarpRaw) {
-    if (a.mode == 0 && a.allow_f16 && warp < 8) {
+    if (!FP8 && a.mode == 0 && a.allow_f16 && warp < 8) {
       const int r = threadIdx.x >> 1, c = threadIdx.x & 1;
       const int g = r & 1, i = r >> 1;
       uint4 q[kPfMT][4];
@@ -325,12 +369,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (lane == 0) {
       bool ok = true;
       for (int rk = 0; rk < nk && ok; ++rk) {
-        const int rs = rk % C::kRaw, rr = rk / C::kRaw;
+        const int rs = rk % kRing, rr = rk / kRing;
         if (rr > 0) ok = mbar_wait_fast(&rawe[rs], (rr - 1) & 1, a.err);
         if (!ok) break;
-        uint8_t* dst = sm + C::kOffRaw + rs * kRawTile;
-        mbar_expect_tx(&rawf[rs], kRawTile);
-        if (a.mode == 0) {
+        uint8_t* dst = sm + C::kOffRaw + rs * kRT;
+        mbar_expect_tx(&rawf[rs], kRT);
+        if (FP8) {  // 2-D maps over one matrix: (row bytes, rows)
+          if (a.mode == 0) {
+            tma_2d(dst, &mA0, rk * 64, f0, &rawf[rs]);
+            tma_2d(dst + 128 * 64, &mA1, rk * 64, f0, &rawf[rs]);
+          } else {
+            tma_2d(dst, &mA0, rk * 64, f0, &rawf[rs]);
+          }
+        } else if (a.mode == 0) {
           tma_3d(dst, &mA0, rk * 32, f0, it.slot, &rawf[rs]);
           tma_3d(dst + 128 * 32, &mA1, rk * 32, f0, it.slot, &rawf[rs]);
         } else {
@@ -389,26 +440,30 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
     for (int mt = 0; mt < kPfMT; ++mt) {
       if (a.mode == 0) {  // tile 0: w1 row f0 + r (gate), tile 1: w3 row f0 + r (up)
-        raw_off[mt] = mt * (128 * 32) + r * 32;
-        srow[mt] = (mt ? a.sc1 : a.sc0) + (size_t)it.slot * a.B + (size_t)(f0 + r) * sbytes;
+        raw_off[mt] = mt * (128 * kRowB) + r * kRowB;
+        srow[mt] = FP8 ? nullptr : (mt ? a.sc1 : a.sc0) + (size_t)it.slot * a.B + (size_t)(f0 + r) * sbytes;
       } else {
-        raw_off[mt] = (128 * mt + r) * 32;
-        srow[mt] = a.sc0 + (size_t)it.slot * a.B + (size_t)(f0 + 128 * mt + r) * sbytes;
+        raw_off[mt] = (128 * mt + r) * kRowB;
+        srow[mt] = FP8 ? nullptr : a.sc0 + (size_t)it.slot * a.B + (size_t)(f0 + 128 * mt + r) * sbytes;
       }
     }
     // scale bytes: 16 at a time (8 K steps), loaded one group ahead
     uint4 scur[kPfMT], snext[kPfMT];
 #pragma unroll
     for (int mt = 0; mt < kPfMT; ++mt) {
-      scur[mt] = __ldg(reinterpret_cast<const uint4*>(srow[mt]));
-      snext[mt] = sbytes > 16 ? __ldg(reinterpret_cast<const uint4*>(srow[mt] + 16)) : scur[mt];
+      if (FP8) {
+        scur[mt] = snext[mt] = make_uint4(0, 0, 0, 0);
+      } else {
+        scur[mt] = __ldg(reinterpret_cast<const uint4*>(srow[mt]));
+        snext[mt] = sbytes > 16 ? __ldg(reinterpret_cast<const uint4*>(srow[mt] + 16)) : scur[mt];
+      }
     }
     bool ok = true;
     int chunk = 0;  // scur holds the scale bytes of K steps 8 * chunk .. 8 * chunk + 7
     for (int ks = cg; ks < nk && ok; ks += kPfConvGroups) {
-      const int rs = ks % C::kRaw, rr = ks / C::kRaw;
+      const int rs = ks % kRing, rr = ks / kRing;
       const int s = ks % kPfStages, rnd = ks / kPfStages;
-      if (ks / 8 != chunk) {  // a stride below 8 moves on by one chunk at a time
+      if (!FP8 && ks / 8 != chunk) {  // a stride below 8 moves on by one chunk at a time
         ++chunk;
 #pragma unroll
         for (int mt = 0; mt < kPfMT; ++mt) {
@@ -418,10 +473,42 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       }
       if (!(ok = mbar_wait_fast(&rawf[rs], rr & 1, a.err))) break;
+      if (FP8) {
+        // 64 E4M3 codes per row: exact 16-bit values, no block scale
+        uint4 q8[kPfMT][4];
+#pragma unroll
+        for (int mt = 0; mt < kPfMT; ++mt)
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            q8[mt][c] = *reinterpret_cast<const uint4*>(sm + C::kOffRaw + rs * kRT + raw_off[mt] + 16 * c);
+        if (rnd > 0 && !(ok = mbar_wait_fast(&empty[s], (rnd - 1) & 1, a.err))) {
+          mbar_arrive(&rawe[rs]);
+          break;
+        }
+#pragma unroll
+        for (int mt = 0; mt < kPfMT; ++mt) {
+          uint8_t* arow = sm + C::kOffA + s * kAStage + mt * kATile + r * 128;
+#pragma unroll
+          for (int unit = 0; unit < 8; ++unit) {  // 8 weights = two code words
+            const uint4 v = q8[mt][unit >> 1];
+            const uint32_t w0 = (unit & 1) ? v.z : v.x, w1 = (unit & 1) ? v.w : v.y;
+            uint4 o;
+            fp8x4_to_f16(w0, o.x, o.y);
+            fp8x4_to_f16(w1, o.z, o.w);
+            if (!f16) {
+              o.x = f16x2_to_bf16x2(o.x);
+              o.y = f16x2_to_bf16x2(o.y);
+              o.z = f16x2_to_bf16x2(o.z);
+              o.w = f16x2_to_bf16x2(o.w);
+            }
+            *reinterpret_cast<uint4*>(arow + ((unit ^ (r & 7)) << 4)) = o;
+          }
+        }
+      } else {
       uint4 q[kPfMT][2];
 #pragma unroll
       for (int mt = 0; mt < kPfMT; ++mt) {
-        const uint8_t* src = sm + C::kOffRaw + rs * kRawTile + raw_off[mt];
+        const uint8_t* src = sm + C::kOffRaw + rs * kRT + raw_off[mt];
         q[mt][0] = *reinterpret_cast<const uint4*>(src);
         q[mt][1] = *reinterpret_cast<const uint4*>(src + 16);
       }
@@ -459,6 +546,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
         }
       }
+      }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(&full[s]);
       // the raw stage is released only now: its codes have been used, so the
@@ -485,6 +573,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
     if (ok && a.mode == 0) {
       const int feat = f0 + row;
+      const float rg = FP8 ? a.rs0[feat] : 1.f, ru = FP8 ? a.rs1[feat] : 1.f;
       for (int c0 = part * 16; c0 < n_mma; c0 += kPfWarps / 4 * 16) {
         uint32_t vg[16], vu[16];
         tmem_ld16(tq + (uint32_t)c0, vg);
@@ -499,7 +588,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           if (col < it.count) {
             // SiLU(g) = g * sigmoid(g) with sigmoid(g) = (1 + tanh(g / 2)) / 2: one
             // hardware tanh (relative error ~2^-11, below h's bf16 rounding)
-            const float hg = 0.5f * __uint_as_float(vg[j]) * sc, up = __uint_as_float(vu[j]) * sc;
+            const float hg = 0.5f * __uint_as_float(vg[j]) * (sc * rg), up = __uint_as_float(vu[j]) * (sc * ru);
             const float hv = fmaf(hg, tanh_approx(hg), hg) * up;
             a.hs[(size_t)(it.row0 + col) * a.I + feat] = __float2bfloat16_rn(hv);
           }
@@ -511,12 +600,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         uint32_t v[16];
         tmem_ld16(tq + (uint32_t)(mt * 256 + c0), v);
         const int feat = f0 + 128 * mt + row;
+        const float rw = FP8 ? a.rs0[feat] : 1.f;
         const int cl = c0 + (lane & 15);
-        const int pl = cl < it.count ? a.perm[it.row0 + cl] : 0;
+        const int pl = cl < it.count ? (FP8 ? a.o_row0 + it.row0 + cl : a.perm[it.row0 + cl]) : 0;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int p = __shfl_sync(0xffffffffu, pl, j);
-          if (c0 + j < it.count) a.o[(size_t)p * a.H + feat] = __uint_as_float(v[j]);
+          if (c0 + j < it.count) a.o[(size_t)p * a.H + feat] = __uint_as_float(v[j]) * rw;
         }
       }
     }
@@ -730,9 +820,9 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
   const bool small = T <= PfSmall::kNMax;
   static bool smem_set[2] = {false, false};
   if (!smem_set[small]) {
-    cudaError_t e = small ? cudaFuncSetAttribute(prefill_gemm_kernel<PfSmall>,
+    cudaError_t e = small ? cudaFuncSetAttribute(prefill_gemm_kernel<PfSmall, false>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, PfSmall::kSmem)
-                          : cudaFuncSetAttribute(prefill_gemm_kernel<PfBig>,
+                          : cudaFuncSetAttribute(prefill_gemm_kernel<PfBig, false>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, PfBig::kSmem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_gemm_kernel)");
     smem_set[small] = true;
@@ -754,9 +844,9 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
   pa.xsig = b.xsig;
   auto launch = [&](const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& bm, const CUtensorMap& bm16) {
     if (small)
-      prefill_gemm_kernel<PfSmall><<<max_items * pa.tiles, kPfThreads, PfSmall::kSmem, stream>>>(a0, a1, bm, bm16, pa);
+      prefill_gemm_kernel<PfSmall, false><<<max_items * pa.tiles, kPfThreads, PfSmall::kSmem, stream>>>(a0, a1, bm, bm16, pa);
     else
-      prefill_gemm_kernel<PfBig><<<max_items * pa.tiles, kPfThreads, PfBig::kSmem, stream>>>(a0, a1, bm, bm16, pa);
+      prefill_gemm_kernel<PfBig, false><<<max_items * pa.tiles, kPfThreads, PfBig::kSmem, stream>>>(a0, a1, bm, bm16, pa);
   };
   // GEMM1: gate/up, 128 features (their w1 rows and their w3 rows) per CTA
   pa.mode = 0;
@@ -782,6 +872,82 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
     launch(m2c, m2c, mh, mh);
   }
   return check_launch("prefill_gemm_kernel (down)");
+}
+
+// rank-2 byte map: (x: row bytes, y: rows)
+static moe_status map_bytes2(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_x,
+                             uint32_t box_y) {
+  auto fn = encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_x, box_y};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (shared weights) failed: %d", (int)r);
+  return MOE_OK;
+}
+
+moe_status grouped_gemm_shared_fp8(const moe_expert_views* v, const __half* xs, const int* xsig, int T,
+                                   __nv_bfloat16* hs, float* o, int o_row0, int32_t* d_error,
+                                   cudaStream_t stream) {
+  using C = PfSmall;
+  const int H = v->H, I = v->I;
+  // FP8 expert layout: w1 codes [I, H] + fp32 row scales [I], w3 likewise, w2 codes [H, I] + scales [H]
+  const size_t hi = (size_t)H * I;
+  const uint8_t* w1 = v->shared;
+  const uint8_t* w3 = w1 + hi + (size_t)I * 4;
+  const uint8_t* w2 = w3 + hi + (size_t)I * 4;
+  CUtensorMap m1, m3, m2, mx16, mh;
+  moe_status st;
+  if ((st = map_bytes2(&m1, w1, H, I, 64, 128)) != MOE_OK) return st;
+  if ((st = map_bytes2(&m3, w3, H, I, 64, 128)) != MOE_OK) return st;
+  if ((st = map_bytes2(&m2, w2, I, H, 64, 256)) != MOE_OK) return st;
+  if ((st = map_bf16_rows(&mx16, xs, H, T, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != MOE_OK) return st;
+  if ((st = map_bf16_rows(&mh, hs, I, T)) != MOE_OK) return st;
+  static bool smem_set = false;
+  if (!smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel<C, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_gemm_kernel, FP8)");
+    smem_set = true;
+  }
+  const int items = (T + C::kNMax - 1) / C::kNMax;
+  PfArgs pa{};
+  pa.H = H;
+  pa.I = I;
+  pa.k = 1;
+  pa.S = 1;
+  pa.xsig = xsig;
+  pa.hs = hs;
+  pa.o = o;
+  pa.err = d_error;
+  pa.rows = T;
+  pa.o_row0 = o_row0;
+  // gate/up: 128 features (their w1 and w3 rows) per CTA
+  pa.mode = 0;
+  pa.K = H;
+  pa.tiles = I / 128;
+  pa.rs0 = reinterpret_cast<const float*>(w1 + hi);
+  pa.rs1 = reinterpret_cast<const float*>(w3 + hi);
+  {
+    ProfScope ps(MOE_K_GATEUP, stream);
+    prefill_gemm_kernel<C, true><<<items * pa.tiles, kPfThreads, C::kSmem, stream>>>(m1, m3, mx16, mx16, pa);
+  }
+  if ((st = check_launch("prefill_gemm_kernel (shared gate/up)")) != MOE_OK) return st;
+  // down: 256 output features per CTA
+  pa.mode = 1;
+  pa.K = I;
+  pa.tiles = H / 256;
+  pa.rs0 = reinterpret_cast<const float*>(w2 + hi);
+  pa.rs1 = pa.rs0;
+  {
+    ProfScope ps(MOE_K_DOWN, stream);
+    prefill_gemm_kernel<C, true><<<items * pa.tiles, kPfThreads, C::kSmem, stream>>>(m2, m2, mh, mh, pa);
+  }
+  return check_launch("prefill_gemm_kernel (shared down)");
 }
 
 struct PfLayout {

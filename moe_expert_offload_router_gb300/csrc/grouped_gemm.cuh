@@ -33,5 +33,11 @@ void gg_carve_index(uint8_t* base, int T, int k, int S, GgBufs* b);
 // Writes o rows of every pair with 0 <= slot < S; other rows are untouched.
 moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T, int k, const int32_t* slots,
                             const GgBufs& b, int32_t* d_error, cudaStream_t stream);
+// The FP8 shared expert (v->shared) over all T tokens on the tensor cores:
+// xs = fp16 activations [T, H], row t scaled by 2^-xsig[t]; hs = bf16 SwiGLU
+// scratch [T, I]; writes o rows o_row0 .. o_row0 + T - 1 (fp32 [., H]).
+moe_status grouped_gemm_shared_fp8(const moe_expert_views* v, const __half* xs, const int* xsig, int T,
+                                   __nv_bfloat16* hs, float* o, int o_row0, int32_t* d_error,
+                                   cudaStream_t stream);
 
 }  // namespace moe
