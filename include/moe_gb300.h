@@ -248,6 +248,15 @@ moe_status moe_copy_missing_device(moe_cache* cache, const int32_t* d_miss_key,
                                    const int32_t* d_miss_slot, const int32_t* d_miss_count,
                                    int max_ctas, cudaStream_t stream);
 
+/* Reads one 16-byte word of every 4 KB page of the cache's mapped host bank
+ * (all num_layers * num_experts experts), stream-ordered on `stream`.  The
+ * first GPU read of a page of pinned host memory runs far below the link's
+ * rate (measured: 25-100 GB/s for an expert's first copy against ~170 GB/s
+ * for later ones), so a server primes the bank once at setup and every miss
+ * copy then runs at the link rate.  The bank is not modified.
+ * MOE_ERR_INVALID if the bank is not mapped. */
+moe_status moe_cache_prime_bank(moe_cache* cache, cudaStream_t stream);
+
 /* The same copy for one part of the list: with n = *d_miss_count, part p of
  * n_parts copies the entries [n * p / n_parts, n * (p + 1) / n_parts) (integer
  * division; a part may be empty).  Launching parts 0..n_parts-1 in order with

@@ -64,6 +64,7 @@ _SIGS = {
     "moe_copy_layer": (i32, [vp, i32, i32, sz, vp, vp]),
     "moe_copy_missing_device": (i32, [vp, vp, vp, vp, i32, vp]),
     "moe_copy_missing_device_part": (i32, [vp, vp, vp, vp, i32, i32, i32, vp]),
+    "moe_cache_prime_bank": (i32, [vp, vp]),
     "moe_cache_set_policy": (i32, [vp, i32, i32]),
     "moe_cache_seed_frequency": (i32, [vp, vp]),
     "moe_cache_export_frequency": (i32, [vp, vp, vp, vp]),
@@ -171,6 +172,14 @@ class moe_cache:
         self.S, self.L, self.E, self.B = num_slots, num_layers, num_experts, expert_bytes
         self.R = 0
         self._keep = (d_slots, h_bank)
+        self.has_bank = h_bank is not None
+        self.primed = False
+
+    def prime_bank(self, stream=None):
+        """moe_cache_prime_bank once per cache (later calls do nothing)."""
+        if self.has_bank and not self.primed:
+            moe_cache_prime_bank(self, stream)
+            self.primed = True
 
     def close(self):
         if self.handle:
@@ -277,6 +286,12 @@ def moe_copy_missing_device(cache: moe_cache, d_miss_key, d_miss_slot, d_miss_co
 
 
 MOE_MAX_COPY_PARTS = 4
+
+
+def moe_cache_prime_bank(cache: moe_cache, stream=None):
+    """Reads one word of every 4 KB page of the cache's pinned bank from the GPU
+    (address translations warmed before the first miss copy)."""
+    _check(_lib.moe_cache_prime_bank(cache.handle, _s(stream)))
 
 
 def moe_copy_missing_device_part(cache: moe_cache, d_miss_key, d_miss_slot, d_miss_count, part: int,

@@ -215,6 +215,20 @@ __global__ void __launch_bounds__(256) copy_missing_kernel(CacheDev c, const uin
     copy_units<size_t>(c, bank, slots, B, miss_key + m0, miss_slot + m0, total);
 }
 
+// One 16-byte load per `stride` bytes of the mapped bank (a page of it), so
+// the GPU has translated every page before a miss copy reads it.  The loads
+// bypass the caches; their xor feeds a store the compiler cannot drop.
+__device__ uint32_t g_prime_sink;
+__global__ void __launch_bounds__(256) prime_bank_kernel(const uint8_t* bank, size_t bytes, size_t stride) {
+  uint32_t acc = 0;
+  const size_t n = bytes / stride;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const uint4 v = __ldcv(reinterpret_cast<const uint4*>(bank + i * stride));
+    acc ^= v.x ^ v.y ^ v.z ^ v.w;
+  }
+  if (acc == 0x9e3779b9u) g_prime_sink = acc;  // rarely taken; keeps the loads
+}
+
 // One thread waits on an mbarrier that nothing arrives on; the bounded wait
 // gives up after limit_ns and reports MOE_ERR_TIMEOUT (the same wait every
 // pipelined kernel of this library uses).
@@ -499,6 +513,18 @@ moe_status moe_copy_missing_device_part(moe_cache* c, const int32_t* d_miss_key,
   copy_missing_kernel<<<grid, 256, 0, stream>>>(c->dev, c->bank_dev, c->d_slots, c->B, d_miss_key, d_miss_slot,
                                                   d_miss_count, part, n_parts);
   return check_launch("copy_missing_kernel");
+}
+
+moe_status moe_cache_prime_bank(moe_cache* c, cudaStream_t stream) {
+  clear_error();
+  MOE_ARG(c != nullptr, "cache is null");
+  MOE_ARG(c->bank_dev != nullptr, "the host bank is not mapped into the device address space");
+  const size_t bytes = (size_t)c->L * c->E * c->B;
+  int dev = 0, sms = 1;
+  MOE_CUDA(cudaGetDevice(&dev));
+  MOE_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  prime_bank_kernel<<<sms * 4, 256, 0, stream>>>(c->bank_dev, bytes, 4096);
+  return check_launch("prime_bank_kernel");
 }
 
 moe_status moe_copy_missing_device(moe_cache* c, const int32_t* d_miss_key, const int32_t* d_miss_slot,

@@ -75,7 +75,9 @@ class DecodeLayerRunner:
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.ws = torch.empty(L.moe_expert_forward_workspace(views, T_max, k), dtype=torch.uint8,
                               device=dev)
-        self.copy_stream = torch.cuda.Stream(device=dev)
+        # high priority: a copy launched while the compute stream's GEMM still has
+        # CTAs waiting for SMs gets the next free SMs instead of queueing behind them
+        self.copy_stream = torch.cuda.Stream(device=dev, priority=-1)
         self.ready = torch.cuda.Event()
         self.done = torch.cuda.Event()
         if copy not in ("engine", "device"):
@@ -105,6 +107,11 @@ class DecodeLayerRunner:
         self.pf_ready = torch.cuda.Event()
         self.pf_done = torch.cuda.Event()
         self.pf_pending = False
+        if copy == "device" and not assume_resident:
+            # the first GPU read of a bank page is slow: translate every page now
+            for c in (cache, int2_cache):
+                if c is not None:
+                    c.prime_bank()
         # CUDA graphs of whole single-chunk device-copy layer steps, per (layer, T)
         self.graph = graph
         self.graphs = {}
