@@ -269,6 +269,17 @@ moe_status moe_copy_missing_device_part(moe_cache* cache, const int32_t* d_miss_
                                         const int32_t* d_miss_slot, const int32_t* d_miss_count,
                                         int part, int n_parts, int max_ctas, cudaStream_t stream);
 
+/* The same copy restricted to the bytes [byte_begin, byte_end) of every listed
+ * expert (both multiples of 16, byte_end <= the expert size, else
+ * MOE_ERR_INVALID).  With the FP4 layout, [0, 2 * (H*I/2 + H*I/32)) holds w1
+ * and w3 (gate/up) and the rest w2 (down): copying the gate/up range first lets
+ * moe_expert_forward_overlap_staged start the missed experts' gate/up work
+ * while their down matrices are still crossing the link. */
+moe_status moe_copy_missing_device_range(moe_cache* cache, const int32_t* d_miss_key,
+                                         const int32_t* d_miss_slot, const int32_t* d_miss_count,
+                                         size_t byte_begin, size_t byte_end, int max_ctas,
+                                         cudaStream_t stream);
+
 /* ---------------------------------------------------------------------------
  * Whole-layer streaming for prefill past the crossover.  "Running DeepSeek-
  * V4-Flash across four free GPUs", section "What the expert cache actually
@@ -392,6 +403,12 @@ moe_status moe_expert_forward(const moe_expert_views* v, const uint16_t* x, int 
  * the last copy.  parts_done: host array of n_parts events (NULL entries:
  * already complete); 1 <= n_parts <= MOE_MAX_COPY_PARTS.  The workspace size
  * covers every n_parts; the result is the same as moe_expert_forward's.
+ *
+ * moe_expert_forward_overlap_staged: the missed experts arrive in two stages,
+ * their gate/up matrices (event gateup_ready) and then their down matrices
+ * (event down_ready); the missed pairs' gate/up work waits only for the
+ * first, their down work for the second.  NULL events: already complete.
+ * Same workspace and result as moe_expert_forward_overlap.
  * ------------------------------------------------------------------------- */
 size_t moe_expert_forward_overlap_workspace(const moe_expert_views* v, int T, int k);
 moe_status moe_expert_forward_overlap(const moe_expert_views* v, const uint16_t* x, int T, int k,
@@ -399,6 +416,11 @@ moe_status moe_expert_forward_overlap(const moe_expert_views* v, const uint16_t*
                                       const int32_t* d_miss_count, int max_miss, cudaEvent_t copies_done,
                                       uint16_t* y, void* workspace, size_t workspace_bytes,
                                       int32_t* d_error, cudaStream_t stream);
+moe_status moe_expert_forward_overlap_staged(const moe_expert_views* v, const uint16_t* x, int T, int k,
+                                             const int32_t* slots, const float* w, const int32_t* d_miss_slot,
+                                             const int32_t* d_miss_count, int max_miss, cudaEvent_t gateup_ready,
+                                             cudaEvent_t down_ready, uint16_t* y, void* workspace,
+                                             size_t workspace_bytes, int32_t* d_error, cudaStream_t stream);
 moe_status moe_expert_forward_overlap_parts(const moe_expert_views* v, const uint16_t* x, int T, int k,
                                             const int32_t* slots, const float* w, const int32_t* d_miss_slot,
                                             const int32_t* d_miss_count, int max_miss, int n_parts,

@@ -163,10 +163,11 @@ __global__ void cache_mark_empty_kernel(CacheDev c, int slot) {
 // host-device link) and stores into the slots; reads the miss list and count
 // on the device, so it needs no host round trip.  16-byte units, four loads in
 // flight per thread before their stores.
+// Bytes [b0, b0 + 16 * per) of each listed expert, one 16-byte unit per step.
 template <typename Idx>
 __device__ __forceinline__ void copy_units(const CacheDev& c, const uint8_t* bank, uint8_t* slots, size_t B,
-                                           const int32_t* miss_key, const int32_t* miss_slot, Idx total) {
-  const Idx per = (Idx)(B / 16);
+                                           size_t b0, Idx per, const int32_t* miss_key, const int32_t* miss_slot,
+                                           Idx total) {
   const Idx stride = (Idx)gridDim.x * blockDim.x;
   const int K = c.L * c.E;
   for (Idx u0 = (Idx)blockIdx.x * blockDim.x + threadIdx.x; u0 < total; u0 += 4 * stride) {
@@ -178,7 +179,7 @@ __device__ __forceinline__ void copy_units(const CacheDev& c, const uint8_t* ban
       dst[j] = (size_t)-1;
       if (u < total) {
         const int m = (int)(u / per);
-        const size_t off = (size_t)(u - (Idx)m * per) * 16;
+        const size_t off = b0 + (size_t)(u - (Idx)m * per) * 16;
         const int key = miss_key[m], sl = miss_slot[m];
         if (key >= 0 && key < K && sl >= 0 && sl < c.S + c.R) {
           // a cache slot filled with a staged key copies from its staging slot
@@ -199,20 +200,22 @@ __device__ __forceinline__ void copy_units(const CacheDev& c, const uint8_t* ban
 // host-device link) and stores into the slots; reads the miss list and count
 // on the device, so it needs no host round trip.  16-byte units, four loads in
 // flight per thread before their stores.
-// Part `part` of `parts` takes the list entries [n * part / parts, n * (part + 1) / parts).
+// Part `part` of `parts` takes the list entries [n * part / parts, n * (part + 1) / parts),
+// and of each expert the bytes [b0, b1) (16-byte multiples).
 __global__ void __launch_bounds__(256) copy_missing_kernel(CacheDev c, const uint8_t* bank, uint8_t* slots,
                                                            size_t B, const int32_t* miss_key,
                                                            const int32_t* miss_slot, const int32_t* miss_count,
-                                                           int part, int parts) {
+                                                           int part, int parts, size_t b0, size_t b1) {
   const int n = *miss_count;
   if (n <= 0) return;
   const int m0 = (int)((long long)n * part / parts), m1 = (int)((long long)n * (part + 1) / parts);
   if (m1 <= m0) return;
-  const size_t total = (size_t)(m1 - m0) * (B / 16);
+  const size_t per = (b1 - b0) / 16;
+  const size_t total = (size_t)(m1 - m0) * per;
   if (total < 0xFFFFFFFFull)
-    copy_units<uint32_t>(c, bank, slots, B, miss_key + m0, miss_slot + m0, (uint32_t)total);
+    copy_units<uint32_t>(c, bank, slots, B, b0, (uint32_t)per, miss_key + m0, miss_slot + m0, (uint32_t)total);
   else
-    copy_units<size_t>(c, bank, slots, B, miss_key + m0, miss_slot + m0, total);
+    copy_units<size_t>(c, bank, slots, B, b0, per, miss_key + m0, miss_slot + m0, total);
 }
 
 // One 16-byte load per `stride` bytes of the mapped bank (a page of it), so
@@ -494,27 +497,6 @@ moe_status moe_cache_export_staging(moe_cache* c, int32_t* h_stage_key, uint32_t
   return MOE_OK;
 }
 
-moe_status moe_copy_missing_device_part(moe_cache* c, const int32_t* d_miss_key, const int32_t* d_miss_slot,
-                                        const int32_t* d_miss_count, int part, int n_parts, int max_ctas,
-                                        cudaStream_t stream) {
-  clear_error();
-  MOE_ARG(c != nullptr, "cache is null");
-  MOE_ARG(d_miss_key && d_miss_slot && d_miss_count, "null miss list");
-  MOE_ARG(c->bank_dev != nullptr, "the host bank is not mapped into the device address space");
-  MOE_ARG(c->B % 16 == 0, "expert bytes %zu not a multiple of 16", c->B);
-  MOE_ARG(n_parts >= 1 && n_parts <= MOE_MAX_COPY_PARTS && part >= 0 && part < n_parts,
-          "part %d of %d: need 0 <= part < n_parts <= %d", part, n_parts, MOE_MAX_COPY_PARTS);
-  MOE_ARG(max_ctas >= 0, "max_ctas < 0");
-  int dev = 0, sms = 1;
-  MOE_CUDA(cudaGetDevice(&dev));
-  MOE_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  ProfScope ps(MOE_K_COPY, stream);
-  const int grid = max_ctas > 0 && max_ctas < sms * 4 ? max_ctas : sms * 4;
-  copy_missing_kernel<<<grid, 256, 0, stream>>>(c->dev, c->bank_dev, c->d_slots, c->B, d_miss_key, d_miss_slot,
-                                                  d_miss_count, part, n_parts);
-  return check_launch("copy_missing_kernel");
-}
-
 moe_status moe_cache_prime_bank(moe_cache* c, cudaStream_t stream) {
   clear_error();
   MOE_ARG(c != nullptr, "cache is null");
@@ -527,9 +509,49 @@ moe_status moe_cache_prime_bank(moe_cache* c, cudaStream_t stream) {
   return check_launch("prime_bank_kernel");
 }
 
+static moe_status copy_missing_launch(moe_cache* c, const int32_t* d_miss_key, const int32_t* d_miss_slot,
+                                      const int32_t* d_miss_count, int part, int n_parts, size_t b0, size_t b1,
+                                      int max_ctas, cudaStream_t stream) {
+  MOE_ARG(c != nullptr, "cache is null");
+  MOE_ARG(d_miss_key && d_miss_slot && d_miss_count, "null miss list");
+  MOE_ARG(c->bank_dev != nullptr, "the host bank is not mapped into the device address space");
+  MOE_ARG(c->B % 16 == 0, "expert bytes %zu not a multiple of 16", c->B);
+  MOE_ARG(n_parts >= 1 && n_parts <= MOE_MAX_COPY_PARTS && part >= 0 && part < n_parts,
+          "part %d of %d: need 0 <= part < n_parts <= %d", part, n_parts, MOE_MAX_COPY_PARTS);
+  MOE_ARG(b0 < b1 && b1 <= c->B && b0 % 16 == 0 && b1 % 16 == 0,
+          "byte range [%zu, %zu) not within [0, %zu) in 16-byte units", b0, b1, c->B);
+  MOE_ARG(max_ctas >= 0, "max_ctas < 0");
+  int dev = 0, sms = 1;
+  MOE_CUDA(cudaGetDevice(&dev));
+  MOE_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  ProfScope ps(MOE_K_COPY, stream);
+  const int grid = max_ctas > 0 && max_ctas < sms * 4 ? max_ctas : sms * 4;
+  copy_missing_kernel<<<grid, 256, 0, stream>>>(c->dev, c->bank_dev, c->d_slots, c->B, d_miss_key, d_miss_slot,
+                                                  d_miss_count, part, n_parts, b0, b1);
+  return check_launch("copy_missing_kernel");
+}
+
+moe_status moe_copy_missing_device_part(moe_cache* c, const int32_t* d_miss_key, const int32_t* d_miss_slot,
+                                        const int32_t* d_miss_count, int part, int n_parts, int max_ctas,
+                                        cudaStream_t stream) {
+  clear_error();
+  MOE_ARG(c != nullptr, "cache is null");
+  return copy_missing_launch(c, d_miss_key, d_miss_slot, d_miss_count, part, n_parts, 0, c->B, max_ctas, stream);
+}
+
+moe_status moe_copy_missing_device_range(moe_cache* c, const int32_t* d_miss_key, const int32_t* d_miss_slot,
+                                         const int32_t* d_miss_count, size_t byte_begin, size_t byte_end,
+                                         int max_ctas, cudaStream_t stream) {
+  clear_error();
+  return copy_missing_launch(c, d_miss_key, d_miss_slot, d_miss_count, 0, 1, byte_begin, byte_end, max_ctas,
+                             stream);
+}
+
 moe_status moe_copy_missing_device(moe_cache* c, const int32_t* d_miss_key, const int32_t* d_miss_slot,
                                    const int32_t* d_miss_count, int max_ctas, cudaStream_t stream) {
-  return moe_copy_missing_device_part(c, d_miss_key, d_miss_slot, d_miss_count, 0, 1, max_ctas, stream);
+  clear_error();
+  MOE_ARG(c != nullptr, "cache is null");
+  return copy_missing_launch(c, d_miss_key, d_miss_slot, d_miss_count, 0, 1, 0, c->B, max_ctas, stream);
 }
 
 moe_status moe_copy_layer(const void* h_bank, int layer_id, int num_experts, size_t expert_bytes, void* d_buf,

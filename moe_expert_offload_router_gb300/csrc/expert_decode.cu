@@ -1064,6 +1064,7 @@ struct FwdPass {
   bool shared = true;            // include the shared expert
   bool combine = true;           // finish with the router-weighted combine into y
   uint8_t* gemm_bufs = nullptr;  // grouped GEMM activation / h copies (else aliased into o / h)
+  cudaEvent_t down_wait = nullptr;  // the stream waits on it before the down matrices are read
 };
 
 static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int T, int k, const int32_t* slots,
@@ -1117,7 +1118,7 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
       gb.hs = (__nv_bfloat16*)a.h;
     }
     gb.o = a.o;
-    if ((st = grouped_gemm_fp4(v, x, T, k, slots, gb, d_error, stream)) != MOE_OK) return st;
+    if ((st = grouped_gemm_fp4(v, x, T, k, slots, gb, d_error, stream, pass.down_wait)) != MOE_OK) return st;
   }
   // the plan groups the pairs and prepares the fp16 activations for the GEMV
   // kernels; a routed-GEMM pass without the shared expert runs none of them
@@ -1155,6 +1156,7 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
   }
   if ((st = check_launch("gateup_kernel")) != MOE_OK) return st;
 
+  if (gemv && pass.down_wait) MOE_CUDA(cudaStreamWaitEvent(stream, pass.down_wait, 0));
   const size_t dn_smem = (size_t)kG * v->I * 4 + 2 * kG * 4;
   const long long dn_items = max_groups * ((v->H + kRowsDown - 1) / kRowsDown);
   if (!gemv) {
@@ -1296,6 +1298,71 @@ extern "C" moe_status moe_expert_forward_overlap_parts(const moe_expert_views* v
       return st;
   }
   // one combine over every pair of the chunk
+  FwdArgs a{};
+  a.H = v->H;
+  a.I = v->I;
+  a.T = T;
+  a.k = k;
+  a.P = (int)P;
+  a.n4 = v->fp4_num_slots;
+  a.n2 = 0;
+  a.shared = v->shared;
+  a.slots = slots;
+  a.tags = nullptr;
+  a.w = w;
+  a.y = y;
+  a.o = (float*)(base + L.o);
+  dim3 cg((v->H + 1023) / 1024, T);
+  ProfScope ps(MOE_K_COMBINE, stream);
+  combine_kernel<<<cg, 256, 0, stream>>>(a);
+  return check_launch("combine_kernel");
+}
+
+extern "C" moe_status moe_expert_forward_overlap_staged(const moe_expert_views* v, const uint16_t* x, int T, int k,
+                                                        const int32_t* slots, const float* w,
+                                                        const int32_t* d_miss_slot, const int32_t* d_miss_count,
+                                                        int max_miss, cudaEvent_t gateup_ready,
+                                                        cudaEvent_t down_ready, uint16_t* y, void* workspace,
+                                                        size_t workspace_bytes, int32_t* d_error,
+                                                        cudaStream_t stream) {
+  clear_error();
+  moe_status st = validate_views(v);
+  if (st != MOE_OK) return st;
+  MOE_ARG(T >= 0 && k >= 1 && k <= 64, "need T >= 0 and 1 <= k <= 64");
+  if (T == 0) return MOE_OK;
+  MOE_ARG((long long)T * k <= kMaxPlanPairs, "T * k = %lld above the %d pairs of one overlapped call",
+          (long long)T * k, kMaxPlanPairs);
+  MOE_ARG(x && slots && w && y && workspace && d_miss_slot && d_miss_count, "null pointer");
+  MOE_ARG(v->fp4_slots != nullptr, "no FP4 pool");
+  MOE_ARG(max_miss >= 0, "max_miss < 0");
+  MOE_ARG(((uintptr_t)workspace & 255) == 0, "workspace must be 256-byte aligned");
+  const FwdLayout L = fwd_layout(v, T, k);
+  const size_t need = L.total + overlap_extra(v, T, k, L);
+  MOE_ARG(workspace_bytes >= need, "workspace too small: %zu < %zu", workspace_bytes, need);
+  uint8_t* base = (uint8_t*)workspace;
+  const size_t P = (size_t)T * k;
+  int32_t* hit = (int32_t*)(base + L.total);
+  int32_t* miss = (int32_t*)(base + L.total + align256(P * 4));
+  uint8_t* gemm_bufs =
+      L.gemm ? base + L.total + align256(P * 4) + align256((size_t)MOE_MAX_COPY_PARTS * P * 4) : nullptr;
+  if (d_error) MOE_CUDA(cudaMemsetAsync(d_error, 0, sizeof(int32_t), stream));
+  const int S = v->fp4_num_slots;
+  if ((st = set_smem(split_miss_kernel, (size_t)S)) != MOE_OK) return st;
+  split_miss_kernel<<<(int)((P + 1023) / 1024), 1024, (size_t)S, stream>>>(slots, (int)P, d_miss_slot,
+                                                                          d_miss_count, max_miss, S, 1, hit, miss);
+  if ((st = check_launch("split_miss_kernel")) != MOE_OK) return st;
+  FwdPass p1;
+  p1.combine = false;
+  if ((st = forward_pass(v, x, T, k, hit, nullptr, w, y, base, L, d_error, stream, p1)) != MOE_OK) return st;
+  // the missed experts' gate/up matrices have landed: their pairs' first
+  // GEMM runs while the down matrices are still on the way
+  if (gateup_ready) MOE_CUDA(cudaStreamWaitEvent(stream, gateup_ready, 0));
+  FwdPass p2;
+  p2.shared = false;
+  p2.combine = false;
+  p2.gemm_bufs = gemm_bufs;
+  p2.down_wait = down_ready;
+  if ((st = forward_pass(v, x, T, k, miss, nullptr, w, y, base, L, d_error, stream, p2)) != MOE_OK) return st;
   FwdArgs a{};
   a.H = v->H;
   a.I = v->I;

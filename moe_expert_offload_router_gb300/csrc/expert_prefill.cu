@@ -785,7 +785,7 @@ void gg_carve_index(uint8_t* base, int T, int k, int S, GgBufs* b) {
 }
 
 moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T, int k, const int32_t* slots,
-                            const GgBufs& b, int32_t* d_error, cudaStream_t stream) {
+                            const GgBufs& b, int32_t* d_error, cudaStream_t stream, cudaEvent_t before_down) {
   const int H = v->H, I = v->I, S = v->fp4_num_slots;
   const size_t P = (size_t)T * k;
   moe_status st = group_pairs_multi(slots, (int)P, S, b.offsets, b.perm, d_error, b.cnt, stream);
@@ -860,6 +860,7 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
     launch(m1c, m3c, mx, mx16);
   }
   if ((st = check_launch("prefill_gemm_kernel (gate/up)")) != MOE_OK) return st;
+  if (before_down) MOE_CUDA(cudaStreamWaitEvent(stream, before_down, 0));
   // GEMM2: down, 256 output features (two tiles of 128) per CTA
   pa.mode = 1;
   pa.K = I;

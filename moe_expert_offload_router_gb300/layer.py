@@ -94,6 +94,9 @@ class DecodeLayerRunner:
             raise ValueError(f"copy_parts must be in [1, {L.MOE_MAX_COPY_PARTS}]")
         self.copy_parts = copy_parts
         self.part_done = [torch.cuda.Event() for _ in range(copy_parts)]
+        self.gu_done = torch.cuda.Event()
+        # bytes of one FP4 matrix (codes + E8M0 scales); w1 and w3 come first in an expert
+        self.gu_half = views.H * views.I // 2 + views.H * views.I // 32
         self.ws_ov = (torch.empty(L.moe_expert_forward_overlap_workspace(views, T_max, k), dtype=torch.uint8,
                                   device=dev) if overlap else None)
         self.status_h = torch.zeros(4, dtype=torch.int32, pin_memory=True)
@@ -180,10 +183,20 @@ class DecodeLayerRunner:
                 # the step's critical path
                 self.ready.record(stream)
                 self.copy_stream.wait_event(self.ready)
-                for q, ev in enumerate(self.part_done):
-                    L.moe_copy_missing_device_part(self.cache, v["keys4"], v["slots4"], v["count4"], q,
-                                                   self.copy_parts, self.copy_stream, self.copy_ctas)
-                    ev.record(self.copy_stream)
+                if self.copy_parts == 1:
+                    # every miss's gate/up matrices first, then their down matrices
+                    gu = 2 * self.gu_half
+                    L.moe_copy_missing_device_range(self.cache, v["keys4"], v["slots4"], v["count4"], 0, gu,
+                                                    self.copy_stream, self.copy_ctas)
+                    self.gu_done.record(self.copy_stream)
+                    L.moe_copy_missing_device_range(self.cache, v["keys4"], v["slots4"], v["count4"], gu,
+                                                    self.cache.B, self.copy_stream, self.copy_ctas)
+                    self.part_done[0].record(self.copy_stream)
+                else:
+                    for q, ev in enumerate(self.part_done):
+                        L.moe_copy_missing_device_part(self.cache, v["keys4"], v["slots4"], v["count4"], q,
+                                                       self.copy_parts, self.copy_stream, self.copy_ctas)
+                        ev.record(self.copy_stream)
             with torch.cuda.stream(stream):
                 self.status_h.copy_(self.info[0:4], non_blocking=True)
             if not self._capturing:      # a replayed graph records it after the replay
@@ -195,9 +208,14 @@ class DecodeLayerRunner:
                 if prefetch is not None:   # after this chunk's own copies on the side stream
                     self.prefetch(*prefetch, stream=stream)
                     prefetch = None
-                L.moe_expert_forward_overlap_parts(self.views, x[tb:T], slots[tb:T], w[tb:T], v["slots4"],
-                                                   v["count4"], self.m4, self.part_done, y[tb:T], self.ws_ov,
-                                                   self.err, stream)
+                if self.copy_parts == 1:
+                    L.moe_expert_forward_overlap_staged(self.views, x[tb:T], slots[tb:T], w[tb:T], v["slots4"],
+                                                        v["count4"], self.m4, self.gu_done, self.part_done[0],
+                                                        y[tb:T], self.ws_ov, self.err, stream)
+                else:
+                    L.moe_expert_forward_overlap_parts(self.views, x[tb:T], slots[tb:T], w[tb:T], v["slots4"],
+                                                       v["count4"], self.m4, self.part_done, y[tb:T], self.ws_ov,
+                                                       self.err, stream)
             else:
                 self._wait_prefetch(stream)
                 L.moe_copy_missing_device(self.cache, v["keys4"], v["slots4"], v["count4"], stream)

@@ -81,6 +81,30 @@ def test_copy_missing_device_parts(n):
     cache.close()
 
 
+def test_copy_missing_device_range():
+    # [b0, b1) of every listed expert; the rest of each slot untouched
+    M = load_lib()
+    wl = configs.scaled(configs.TINY, E=16)
+    bank, B, slots, cache = _cache(M, wl, 8)
+    b = bank.numpy().reshape(wl.E, B)
+    keys = torch.tensor([3, 15, 0], dtype=torch.int32, device="cuda")
+    sl = torch.tensor([5, 0, 7], dtype=torch.int32, device="cuda")
+    cnt = torch.tensor([3], dtype=torch.int32, device="cuda")
+    gu = 2 * (wl.H * wl.I // 2 + wl.H * wl.I // 32)
+    for b0, b1 in ((0, gu), (gu, B), (16, 48), (0, B)):
+        slots.zero_()
+        M.moe_copy_missing_device_range(cache, keys, sl, cnt, b0, b1)
+        torch.cuda.synchronize()
+        got = slots.cpu().numpy().reshape(8, B)
+        for key, s in [(3, 5), (15, 0), (0, 7)]:
+            assert np.array_equal(got[s, b0:b1], b[key, b0:b1])
+            assert not got[s, :b0].any() and not got[s, b1:].any()
+    for b0, b1 in ((0, 0), (8, 32), (0, B + 16), (32, 16)):
+        with pytest.raises(M.MoeError):
+            M.moe_copy_missing_device_range(cache, keys, sl, cnt, b0, b1)
+    cache.close()
+
+
 def test_copy_missing_device_full_size_expert():
     M = load_lib()
     wl = configs.scaled(configs.DECODE, E=4)

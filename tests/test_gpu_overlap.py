@@ -31,6 +31,8 @@ def _overlap(M, P, x_bits, slots, w, miss_slots, event=None, parts=None):
             torch.from_numpy(w.astype(np.float32)).cuda(), ms, cnt, len(miss_slots) + 1)
     if parts is None:
         M.moe_expert_forward_overlap(*args, event, y, ws, err)
+    elif parts == "staged":
+        M.moe_expert_forward_overlap_staged(*args, event, event, y, ws, err)
     else:
         M.moe_expert_forward_overlap_parts(*args, [event] * parts, y, ws, err)
     torch.cuda.synchronize()
@@ -58,7 +60,7 @@ def test_overlap_equals_forward_decode_shape(T, nmiss):
 
 
 @pytest.mark.parametrize("T,nmiss,parts", [(64, 9, 2), (64, 9, 4), (64, 1, 3), (64, 64, 3), (16, 5, 2),
-                                           (64, 0, 2)])
+                                           (64, 0, 2), (64, 9, "staged"), (16, 5, "staged"), (64, 64, "staged")])
 def test_overlap_parts_equal_forward(T, nmiss, parts):
     # misses split into parts as the part-wise copy divides the list (a part
     # may be empty); every pair is still computed exactly once
@@ -66,7 +68,7 @@ def test_overlap_parts_equal_forward(T, nmiss, parts):
     wl = configs.DECODE
     S = 64
     P = Pools(M, wl, S, shared=True)
-    rng = np.random.default_rng(700 + T + nmiss + parts)
+    rng = np.random.default_rng(700 + T + nmiss + (parts if isinstance(parts, int) else 7))
     slots, w = _route(rng, T, wl.k, S)
     misses = rng.choice(S, size=nmiss, replace=False) if nmiss < S else rng.permutation(S)
     x = gen.activations(wl, 0, 9, T)
@@ -131,7 +133,8 @@ def _decoder(bank_np, B, wl):
 @pytest.mark.parametrize("wl,S,steps,full,parts", [
     (configs.TINY, 4, 6, True, 2),                                   # chunked
     (configs.scaled(configs.DECODE, T=4), 64, 4, False, 1),          # single chunk, CUDA-core path
-    (configs.scaled(configs.DECODE, T=64), 40, 3, False, 2),         # chunked, grouped GEMM
+    (configs.scaled(configs.DECODE, T=64), 40, 3, False, 1),         # chunked, grouped GEMM, staged copies
+    (configs.scaled(configs.DECODE, T=64), 40, 3, False, 2),         # chunked, grouped GEMM, two parts
     (configs.scaled(configs.DECODE, T=64), 64, 3, False, 3),         # grouped GEMM, three copy parts
 ])
 def test_layer_overlapped_copy(wl, S, steps, full, parts):
