@@ -900,6 +900,8 @@ __global__ void __launch_bounds__(kFwdThreads, 2) down_kernel(FwdArgs a) {
 
 // ------------------------------------------------------------ combine kernel --
 
+// Four consecutive outputs per thread (16-byte loads of o, all k issued before
+// use); per element the same fmaf chain in rank order as one element at a time.
 __global__ void __launch_bounds__(256) combine_kernel(FwdArgs a) {
   const int t = blockIdx.y;
   __shared__ float wk[64];
@@ -914,12 +916,39 @@ __global__ void __launch_bounds__(256) combine_kernel(FwdArgs a) {
     pk[threadIdx.x] = keep ? p : -1;
   }
   __syncthreads();
-  for (int n = blockIdx.x * blockDim.x + threadIdx.x; n < a.H; n += gridDim.x * blockDim.x) {
-    float acc = 0.f;
-    for (int j = 0; j < a.k; ++j)
-      if (pk[j] >= 0) acc = fmaf(wk[j], a.o[(size_t)pk[j] * a.H + n], acc);
-    if (a.shared) acc += a.o[(size_t)(a.P + t) * a.H + n];
-    a.y[(size_t)t * a.H + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+  for (int n = 4 * (blockIdx.x * blockDim.x + threadIdx.x); n < a.H; n += 4 * gridDim.x * blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int j = 0; j < a.k; ++j) {
+      if (pk[j] < 0) continue;
+      const float4 v = *reinterpret_cast<const float4*>(a.o + (size_t)pk[j] * a.H + n);
+      const float wj = wk[j];
+      acc.x = fmaf(wj, v.x, acc.x);
+      acc.y = fmaf(wj, v.y, acc.y);
+      acc.z = fmaf(wj, v.z, acc.z);
+      acc.w = fmaf(wj, v.w, acc.w);
+    }
+    if (a.shared) {
+      const float4 v = *reinterpret_cast<const float4*>(a.o + (size_t)(a.P + t) * a.H + n);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    uint2 out;
+    out.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.x)) |
+            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.y)) << 16);
+    out.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.z)) |
+            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.w)) << 16);
+    uint16_t* dst = a.y + (size_t)t * a.H + n;
+    if (((uintptr_t)dst & 7) == 0) {
+      *reinterpret_cast<uint2*>(dst) = out;
+    } else {  // a caller's y need only be 2-byte aligned
+      dst[0] = (uint16_t)out.x;
+      dst[1] = (uint16_t)(out.x >> 16);
+      dst[2] = (uint16_t)out.y;
+      dst[3] = (uint16_t)(out.y >> 16);
+    }
   }
 }
 
@@ -1172,7 +1201,7 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
   if ((st = check_launch("down_kernel")) != MOE_OK) return st;
   if (!pass.combine) return MOE_OK;
 
-  dim3 cg((v->H + 1023) / 1024, T);
+  dim3 cg((v->H / 4 + 255) / 256, T);
   ProfScope ps(MOE_K_COMBINE, stream);
   combine_kernel<<<cg, 256, 0, stream>>>(a);
   return check_launch("combine_kernel");
@@ -1312,7 +1341,7 @@ extern "C" moe_status moe_expert_forward_overlap_parts(const moe_expert_views* v
   a.w = w;
   a.y = y;
   a.o = (float*)(base + L.o);
-  dim3 cg((v->H + 1023) / 1024, T);
+  dim3 cg((v->H / 4 + 255) / 256, T);
   ProfScope ps(MOE_K_COMBINE, stream);
   combine_kernel<<<cg, 256, 0, stream>>>(a);
   return check_launch("combine_kernel");
@@ -1377,7 +1406,7 @@ extern "C" moe_status moe_expert_forward_overlap_staged(const moe_expert_views* 
   a.w = w;
   a.y = y;
   a.o = (float*)(base + L.o);
-  dim3 cg((v->H + 1023) / 1024, T);
+  dim3 cg((v->H / 4 + 255) / 256, T);
   ProfScope ps(MOE_K_COMBINE, stream);
   combine_kernel<<<cg, 256, 0, stream>>>(a);
   return check_launch("combine_kernel");

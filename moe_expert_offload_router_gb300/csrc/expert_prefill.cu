@@ -687,17 +687,39 @@ __global__ void gather_rows_kernel(const uint16_t* x, int H, int k, const int* p
   }
 }
 
-__global__ void prefill_combine_kernel(const float* o, const int32_t* slots, const float* w, int T, int k, int H,
-                                       int S, uint16_t* y) {
+// Four consecutive outputs per thread (16-byte loads of o, all k issued before
+// use); per element the same fmaf chain in rank order.
+__global__ void __launch_bounds__(256) prefill_combine_kernel(const float* o, const int32_t* slots, const float* w,
+                                                              int T, int k, int H, int S, uint16_t* y) {
   const int t = blockIdx.y;
-  for (int n = blockIdx.x * blockDim.x + threadIdx.x; n < H; n += gridDim.x * blockDim.x) {
-    float acc = 0.f;
+  for (int n = 4 * (blockIdx.x * blockDim.x + threadIdx.x); n < H; n += 4 * gridDim.x * blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
     for (int j = 0; j < k; ++j) {
       const int p = t * k + j;
       const int sl = slots[p];
-      if (sl >= 0 && sl < S) acc = fmaf(w[p], o[(size_t)p * H + n], acc);
+      if (sl < 0 || sl >= S) continue;
+      const float4 v = *reinterpret_cast<const float4*>(o + (size_t)p * H + n);
+      const float wj = w[p];
+      acc.x = fmaf(wj, v.x, acc.x);
+      acc.y = fmaf(wj, v.y, acc.y);
+      acc.z = fmaf(wj, v.z, acc.z);
+      acc.w = fmaf(wj, v.w, acc.w);
     }
-    y[(size_t)t * H + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+    uint2 out;
+    out.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.x)) |
+            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.y)) << 16);
+    out.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.z)) |
+            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.w)) << 16);
+    uint16_t* dst = y + (size_t)t * H + n;
+    if (((uintptr_t)dst & 7) == 0) {
+      *reinterpret_cast<uint2*>(dst) = out;
+    } else {  // a caller's y need only be 2-byte aligned
+      dst[0] = (uint16_t)out.x;
+      dst[1] = (uint16_t)(out.x >> 16);
+      dst[2] = (uint16_t)out.y;
+      dst[3] = (uint16_t)(out.y >> 16);
+    }
   }
 }
 
@@ -1000,7 +1022,7 @@ moe_status prefill_forward(const moe_expert_views* v, const uint16_t* x, int T, 
   if (st != MOE_OK) return st;
   {
     ProfScope ps(MOE_K_COMBINE, stream);
-    dim3 cg((H + 1023) / 1024, T);
+    dim3 cg((H / 4 + 255) / 256, T);
     prefill_combine_kernel<<<cg, 256, 0, stream>>>(b.o, slots, w, T, k, H, S, y);
   }
   return check_launch("prefill_combine_kernel");
