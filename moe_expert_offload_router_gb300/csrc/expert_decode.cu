@@ -483,7 +483,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(FwdArgs a) {
     if (threadIdx.x == 0) a.xsig[t] = sg;
     return;
   }
-  // block 0: group kept pairs by (pool, slot)
+  // block 0: group kept pairs by (pool, slot); a routed-GEMM pass has no GEMV
+  // groups (its grouping kernels check the slots), only the activation prep
+  if (a.routed_gemm) return;
   unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem_raw);
   int* ws = reinterpret_cast<int*>(keys + kMaxPlanPairs);
   int* scal = ws + 34;

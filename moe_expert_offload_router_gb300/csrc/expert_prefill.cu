@@ -42,7 +42,6 @@
 namespace moe {
 
 constexpr int kPfThreads = 512;   // 16 warps: 12 converters, raw producer, MMA, B producer, spare
-constexpr int kPfStages = 3;      // A/B operand stages
 constexpr int kPfMT = 2;          // 128-row weight tiles per CTA (two TMEM accumulators)
 constexpr int kPfNMax = 256;      // rows per item (MMA N) of the item list
 constexpr int kPfKStep = 64;      // K elements per stage (128 bytes of bf16: one swizzle row)
@@ -63,25 +62,30 @@ constexpr int kATile = 128 * 128;                 // 16 KB per 128-row tile
 constexpr int kAStage = kPfMT * kATile;           // 32 KB
 constexpr int kRawTile = kPfMT * 128 * 32;        // 8 KB of packed codes per stage
 
-// Two shapes of the GEMM CTA: items of up to 256 rows with a 4-deep raw-code
-// ring (prefill: tensor-bound), or items of up to 64 rows, whose smaller B
-// stages leave room for a 12-deep ring (decode batches: the weight stream is
-// the bound, and one CTA per SM needs ~100 KB in flight to cover HBM latency).
-template <int NMAX, int RAW>
+// Shapes of the GEMM CTA: items of up to 256 rows with three operand stages
+// and a 4-deep raw-code ring (prefill: tensor-bound), or items of up to 64
+// rows, whose smaller B stages leave room for four operand stages and an
+// 8-deep ring (decode batches: a fourth stage lengthens the reuse distance of
+// each A stage, which bounds a K step at small N; 64 KB of codes in flight per
+// SM).  The FP8 shared expert keeps three stages and a 12-deep ring of 8 KB
+// (six of its 16 KB stages).
+template <int NMAX, int RAW, int STAGES>
 struct PfCfg {
   static constexpr int kNMax = NMAX;
   static constexpr int kRaw = RAW;
+  static constexpr int kStages = STAGES;  // A/B operand stages
   static constexpr int kBTile = NMAX * 128;
   static constexpr int kOffA = 0;
-  static constexpr int kOffB = kOffA + kPfStages * kAStage;
-  static constexpr int kOffRaw = kOffB + kPfStages * kBTile;
+  static constexpr int kOffB = kOffA + STAGES * kAStage;
+  static constexpr int kOffRaw = kOffB + STAGES * kBTile;
   static constexpr int kOffBar = kOffRaw + RAW * kRawTile;
   static constexpr int kSmem = kOffBar + 512 + 1024;  // barriers + alignment slack
-  static_assert((2 * kPfStages + 2 * RAW + 1) * 8 + 8 <= 512, "barrier area");
+  static_assert((2 * STAGES + 2 * RAW + 1) * 8 + 8 <= 512, "barrier area");
   static_assert(kSmem <= 232448, "shared memory per CTA");
 };
-using PfBig = PfCfg<256, 4>;
-using PfSmall = PfCfg<64, 12>;
+using PfBig = PfCfg<256, 4, 3>;
+using PfSmall = PfCfg<64, 8, 4>;
+using PfShared = PfCfg<64, 12, 3>;  // FP8 shared expert: 16 KB raw stages, so a deeper ring
 
 __device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
   asm volatile(
@@ -261,9 +265,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bar = (uint64_t*)(sm + C::kOffBar);
-  uint64_t* full = bar;                  // [kPfStages]
-  uint64_t* empty = bar + kPfStages;     // [kPfStages]
-  uint64_t* rawf = bar + 2 * kPfStages;  // [C::kRaw]
+  uint64_t* full = bar;                    // [C::kStages]
+  uint64_t* empty = bar + C::kStages;      // [C::kStages]
+  uint64_t* rawf = bar + 2 * C::kStages;   // [C::kRaw]
   uint64_t* rawe = rawf + C::kRaw;       // [C::kRaw]
   uint64_t* done = rawe + C::kRaw;
   uint32_t* tmem_slot = (uint32_t*)(done + 1);
@@ -298,7 +302,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const uint32_t b_bytes = (uint32_t)n_box * kPfBox * 128;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kPfStages; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], kPfConvThreads + 1);
       mbar_init(&empty[s], 1);
     }
@@ -399,7 +403,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (lane == 0) {
       bool ok = true;
       for (int ks = 0; ks < nk && ok; ++ks) {
-        const int s = ks % kPfStages, r = ks / kPfStages;
+        const int s = ks % C::kStages, r = ks / C::kStages;
         if (r > 0) ok = mbar_wait_fast(&empty[s], (r - 1) & 1, a.err);
         if (!ok) break;
         uint8_t* bdst = sm + C::kOffB + s * C::kBTile;
@@ -419,7 +423,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t idesc = idesc_16bit(n_mma, !f16);
     bool ok = true;
     for (int ks = 0; ks < nk && ok; ++ks) {
-      const int s = ks % kPfStages, r = ks / kPfStages;
+      const int s = ks % C::kStages, r = ks / C::kStages;
       ok = __all_sync(0xffffffffu, mbar_wait_fast(&full[s], r & 1, a.err));
       if (!ok) break;
       tc_fence_after();
@@ -462,7 +466,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     int chunk = 0;  // scur holds the scale bytes of K steps 8 * chunk .. 8 * chunk + 7
     for (int ks = cg; ks < nk && ok; ks += kPfConvGroups) {
       const int rs = ks % kRing, rr = ks / kRing;
-      const int s = ks % kPfStages, rnd = ks / kPfStages;
+      const int s = ks % C::kStages, rnd = ks / C::kStages;
       if (!FP8 && ks / 8 != chunk) {  // a stride below 8 moves on by one chunk at a time
         ++chunk;
 #pragma unroll
@@ -916,7 +920,7 @@ static moe_status map_bytes2(CUtensorMap* m, const void* base, uint64_t row_byte
 moe_status grouped_gemm_shared_fp8(const moe_expert_views* v, const __half* xs, const int* xsig, int T,
                                    __nv_bfloat16* hs, float* o, int o_row0, int32_t* d_error,
                                    cudaStream_t stream) {
-  using C = PfSmall;
+  using C = PfShared;
   const int H = v->H, I = v->I;
   // FP8 expert layout: w1 codes [I, H] + fp32 row scales [I], w3 likewise, w2 codes [H, I] + scales [H]
   const size_t hi = (size_t)H * I;
