@@ -22,7 +22,11 @@ Functions and what pins each one (see the ``-m "not gpu"`` tests):
                    forms.
 * ``permute``    - grouping of (token, rank) pairs by expert.  Pinned by a
                    brute-force bucket construction.
+* ``mxquant``    - OCP MX quantisation of activations to MXFP4 (the
+                   A-quantised prefill mode).  Pinned by hand-worked blocks
+                   (grid values, every tie, saturation, zero and tiny blocks)
+                   and a brute-force nearest-grid-point search.
 * Model quality of the ladder and of the 2-bit level values: parity
   unpinned (needs trained weights and text).
 """
-from . import formats, router, slot_cache, ladder, mlp, permute  # noqa: F401
+from . import formats, router, slot_cache, ladder, mlp, permute, mxquant  # noqa: F401

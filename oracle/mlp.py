@@ -25,20 +25,29 @@ def silu(z: np.ndarray) -> np.ndarray:
         return z / (1.0 + np.exp(-z))
 
 
-def expert_mlp(x: np.ndarray, W: dict) -> np.ndarray:
-    """x fp64 [n, H]; W = {'w1': [I,H], 'w3': [I,H], 'w2': [H,I]} fp64 -> [n, H]."""
+def expert_mlp(x: np.ndarray, W: dict, quant=None) -> np.ndarray:
+    """x fp64 [n, H]; W = {'w1': [I,H], 'w3': [I,H], 'w2': [H,I]} fp64 -> [n, H].
+
+    ``quant`` (e.g. ``mxquant.mx_round``) is applied to x and to h before
+    their products when the activations are quantised."""
+    if quant is not None:
+        x = quant(x)
     g = x @ W["w1"].T
     u = x @ W["w3"].T
-    return (silu(g) * u) @ W["w2"].T
+    h = silu(g) * u
+    if quant is not None:
+        h = quant(h)
+    return h @ W["w2"].T
 
 
 def moe_layer(x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray, expert_weights,
               shared: dict | None = None, tags: np.ndarray | None = None,
-              tokens=None) -> np.ndarray:
+              tokens=None, quant=None) -> np.ndarray:
     """y fp64 [len(tokens), H].
 
     ``expert_weights(expert, tag) -> W`` decodes a routed expert (tag 0 FP4,
     1 the 2-bit copy); pairs with tag 2 (dropped) or a negative id are skipped.
+    ``quant``: activation quantiser of the routed experts' x and h (None: W4A16).
     """
     x = bf16_to_f64(x_bits)
     T, k = ids.shape
@@ -55,7 +64,7 @@ def moe_layer(x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray, expert_weights
     o = {}
     for (e, tag), pairs in groups.items():
         W = expert_weights(e, tag)
-        out = expert_mlp(x[[t for t, _ in pairs]], W)
+        out = expert_mlp(x[[t for t, _ in pairs]], W, quant)
         for (t, j), row in zip(pairs, out):
             o[(t, j)] = row
     y = np.zeros((len(tokens), H), dtype=np.float64)
