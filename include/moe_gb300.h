@@ -445,6 +445,33 @@ moe_status moe_expert_prefill(const moe_expert_views* v, const uint16_t* x, int 
                               const int32_t* slots, const float* w, uint16_t* y, void* workspace,
                               size_t workspace_bytes, int32_t* d_error, cudaStream_t stream);
 
+/* moe_expert_prefill with a precision mode.  MOE_PREC_W4A16 (the pages'
+ * semantics, = moe_expert_prefill): activations bf16.  MOE_PREC_A_MXFP4 (not on
+ * the pages; the tensor cores' block-scaled FP4 format): x, per token along H,
+ * and h, per routed pair along I, are quantised to MXFP4 by the OCP MX rule of
+ * moe_mx_quantize before their products, which then run on the exact
+ * quantised values (bf16 MMA, fp32 accumulate).  Same workspace; an unknown
+ * mode gives MOE_ERR_INVALID. */
+#define MOE_PREC_W4A16 0
+#define MOE_PREC_A_MXFP4 1
+moe_status moe_expert_prefill_prec(const moe_expert_views* v, const uint16_t* x, int T, int k,
+                                   const int32_t* slots, const float* w, int prec_mode, uint16_t* y,
+                                   void* workspace, size_t workspace_bytes, int32_t* d_error,
+                                   cudaStream_t stream);
+
+/* OCP MX quantisation (OCP Microscaling Formats (MX) Specification v1.0) of a
+ * bf16 matrix to MXFP4, the activation step of MOE_PREC_A_MXFP4:
+ *   x       device bf16 [rows, K], row-major, 16-byte aligned; K % 32 == 0
+ *   codes   device uint8 [rows, K/2] out, 16-byte aligned: element 2j in the
+ *           low nibble of byte j (E2M1 codes)
+ *   scales  device uint8 [rows, K/32] out: one E8M0 byte per 32-element block
+ * Per block: X = 2^(floor(log2 amax) - 2) (byte clamped to [0, 254]; an
+ * all-zero block takes 2^-127), element = E2M1 value nearest to v / X with
+ * ties to the even code, saturated at 6, zero magnitudes as +0.  Stream-
+ * ordered; MOE_ERR_INVALID on bad sizes, null or misaligned pointers. */
+moe_status moe_mx_quantize(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* scales,
+                           cudaStream_t stream);
+
 /* ---------------------------------------------------------------------------
  * moe_expert_forward without a caller-provided workspace.  The pages have no
  * counterpart; this serves callers that cannot allocate device memory: hosts

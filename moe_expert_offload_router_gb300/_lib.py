@@ -89,6 +89,9 @@ _SIGS = {
     "moe_expert_forward_noalloc": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, vp, vp]),
     "moe_expert_prefill_workspace": (sz, [C.POINTER(moe_expert_views), i32, i32]),
     "moe_expert_prefill": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, sz, vp, vp]),
+    "moe_expert_prefill_prec": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, i32, vp, vp, sz, vp,
+                                      vp]),
+    "moe_mx_quantize": (i32, [vp, i32, i32, vp, vp, vp]),
     "moe_rms_carry": (i32, [vp, i32, i32, f32, vp, vp]),
     "moe_selftest": (i32, []),
     "moe_debug_timeout_probe": (i32, [C.c_int64, vp, vp]),
@@ -409,6 +412,23 @@ def moe_expert_prefill(views: moe_expert_views, x, slots, w, y, workspace, d_err
     T, k = slots.shape
     _check(_lib.moe_expert_prefill(C.byref(views), _p(x), T, k, _p(slots), _p(w), _p(y), _p(workspace),
                                    workspace.numel() * workspace.element_size(), _p(d_error), _s(stream)))
+
+
+MOE_PREC_W4A16, MOE_PREC_A_MXFP4 = 0, 1
+
+
+def moe_expert_prefill_prec(views: moe_expert_views, x, slots, w, prec_mode: int, y, workspace, d_error,
+                            stream=None):
+    T, k = slots.shape
+    _check(_lib.moe_expert_prefill_prec(C.byref(views), _p(x), T, k, _p(slots), _p(w), prec_mode, _p(y),
+                                        _p(workspace), workspace.numel() * workspace.element_size(), _p(d_error),
+                                        _s(stream)))
+
+
+def moe_mx_quantize(x, codes, scales, stream=None):
+    """x device bf16 bits [rows, K] -> codes uint8 [rows, K/2], scales uint8 [rows, K/32]."""
+    rows, K = x.shape
+    _check(_lib.moe_mx_quantize(_p(x), rows, K, _p(codes), _p(scales), _s(stream)))
 
 
 def moe_dequant_debug(views: moe_expert_views, pool: int, slot: int, matrix: int, out, stream=None):

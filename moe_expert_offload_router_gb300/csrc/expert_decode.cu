@@ -1077,7 +1077,7 @@ namespace moe {
 size_t prefill_workspace(int H, int I, int T, int k, int S);
 moe_status prefill_forward(const moe_expert_views* v, const uint16_t* x, int T, int k, const int32_t* slots,
                            const float* w, uint16_t* y, void* workspace, size_t ws_bytes, int32_t* d_error,
-                           cudaStream_t stream);
+                           cudaStream_t stream, int prec_mode = MOE_PREC_W4A16);
 }  // namespace moe
 
 using namespace moe;

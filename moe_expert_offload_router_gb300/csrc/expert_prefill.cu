@@ -38,6 +38,7 @@
 
 #include "common.cuh"
 #include "grouped_gemm.cuh"
+#include "mx.cuh"
 
 namespace moe {
 
@@ -250,6 +251,7 @@ struct PfArgs {
   const float* rs1;
   int rows;
   int o_row0;
+  int mx;             // mode 0: h quantised to MXFP4 along I (blocks of 32 features) before the store
 };
 
 // FP8 = false: MXFP4 experts of the slot pool (E2M1 codes with E8M0 block
@@ -593,7 +595,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             // SiLU(g) = g * sigmoid(g) with sigmoid(g) = (1 + tanh(g / 2)) / 2: one
             // hardware tanh (relative error ~2^-11, below h's bf16 rounding)
             const float hg = 0.5f * __uint_as_float(vg[j]) * (sc * rg), up = __uint_as_float(vu[j]) * (sc * ru);
-            const float hv = fmaf(hg, tanh_approx(hg), hg) * up;
+            float hv = fmaf(hg, tanh_approx(hg), hg) * up;
+            if (a.mx) {
+              // the warp's 32 lanes hold 32 consecutive features of this column: one MX block
+              const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv)));
+              const uint32_t sb = mx_scale_byte(__uint_as_float(amax));
+              hv = mx_value(mx_code(hv, mx_inv_scale(sb)), mx_scale(sb));
+            }
             a.hs[(size_t)(it.row0 + col) * a.I + feat] = __float2bfloat16_rn(hv);
           }
         }
@@ -649,8 +657,10 @@ __global__ void prefill_items_kernel(const int* offsets, int S, PfItem* items, i
 
 // One warp per sorted row: copy the token's bf16 row, and an fp16 copy scaled
 // by the power of two that brings its largest magnitude into [1, 2).
+// mx != 0: each 32-element block of the row is replaced by its MXFP4
+// quantisation (exact in bf16); the fp16 copy is not written (bf16 MMAs only).
 __global__ void gather_rows_kernel(const uint16_t* x, int H, int k, const int* perm, const int* offsets, int S,
-                                   uint16_t* xg, __half* xg16, int* xsig) {
+                                   uint16_t* xg, __half* xg16, int* xsig, int mx) {
   const int n = offsets[S];
   const int lane = threadIdx.x & 31;
   const int units = H / 8;
@@ -659,6 +669,37 @@ __global__ void gather_rows_kernel(const uint16_t* x, int H, int k, const int* p
     const int tok = perm[i] / k;
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)tok * H);
     uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)i * H);
+    if (mx) {
+      // units 4b .. 4b + 3 (one 32-element block) sit in four consecutive lanes;
+      // H is a multiple of 256, so every lane takes part in every step
+      for (int c = lane; c < units; c += 32) {
+        const uint4 v = src[c];
+        float f[8];
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          f[2 * q] = __uint_as_float(w4[q] << 16);
+          f[2 * q + 1] = __uint_as_float(w4[q] & 0xffff0000u);
+        }
+        float am = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) am = fmaxf(am, fabsf(f[q]));
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+        const uint32_t sb = mx_scale_byte(am);
+        const float inv = mx_inv_scale(sb), xs = mx_scale(sb);
+        uint32_t o4[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(mx_value(mx_code(f[2 * q], inv), xs)));
+          const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(mx_value(mx_code(f[2 * q + 1], inv), xs)));
+          o4[q] = lo | (hi << 16);
+        }
+        dst[c] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+      }
+      if (lane == 0) xsig[i] = 0;
+      continue;
+    }
     float m = 0.f;
     for (int c = lane; c < units; c += 32) {
       const uint4 v = src[c];
@@ -811,7 +852,8 @@ void gg_carve_index(uint8_t* base, int T, int k, int S, GgBufs* b) {
 }
 
 moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T, int k, const int32_t* slots,
-                            const GgBufs& b, int32_t* d_error, cudaStream_t stream, cudaEvent_t before_down) {
+                            const GgBufs& b, int32_t* d_error, cudaStream_t stream, cudaEvent_t before_down,
+                            int mx_act) {
   const int H = v->H, I = v->I, S = v->fp4_num_slots;
   const size_t P = (size_t)T * k;
   moe_status st = group_pairs_multi(slots, (int)P, S, b.offsets, b.perm, d_error, b.cnt, stream);
@@ -820,7 +862,7 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
   if ((st = check_launch("prefill_items_kernel")) != MOE_OK) return st;
   {
     const int blocks = (int)std::min<size_t>((P + 7) / 8, 152 * 16);
-    gather_rows_kernel<<<blocks, 256, 0, stream>>>(x, H, k, b.perm, b.offsets, S, b.xg, b.xg16, b.xsig);
+    gather_rows_kernel<<<blocks, 256, 0, stream>>>(x, H, k, b.perm, b.offsets, S, b.xg, b.xg16, b.xsig, mx_act);
     if ((st = check_launch("gather_rows_kernel")) != MOE_OK) return st;
   }
   // weight maps over the whole pool: dims (row bytes, rows, slots)
@@ -855,11 +897,12 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
   }
   // items: at most one per used slot, plus one per 256 further rows (wide shape)
   const int max_items = (int)std::min<size_t>((size_t)S, P) + (small ? 0 : (int)(P / kPfNMax) + 1);
-  PfArgs pa;
+  PfArgs pa{};
   pa.H = H;
   pa.I = I;
   pa.k = k;
   pa.S = S;
+  pa.mx = mx_act;
   pa.items = b.items;
   pa.n_items = b.nitems;
   pa.perm = b.perm;
@@ -880,7 +923,7 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
   pa.tiles = I / 128;
   pa.sc0 = w1s;
   pa.sc1 = w3s;
-  pa.allow_f16 = 1;
+  pa.allow_f16 = mx_act ? 0 : 1;  // MXFP4 activations run as bf16 products (exact values)
   {
     ProfScope ps(MOE_K_GEMM_GATEUP, stream);
     launch(m1c, m3c, mx, mx16);
@@ -1003,7 +1046,7 @@ size_t prefill_workspace(int H, int I, int T, int k, int S) { return pf_layout(H
 
 moe_status prefill_forward(const moe_expert_views* v, const uint16_t* x, int T, int k, const int32_t* slots,
                            const float* w, uint16_t* y, void* workspace, size_t ws_bytes, int32_t* d_error,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, int prec_mode) {
   const int H = v->H, I = v->I, S = v->fp4_num_slots;
   MOE_ARG(v->fp4_slots && S >= 1, "the grouped GEMM path needs the FP4 pool");
   MOE_ARG(v->int2_slots == nullptr && v->shared == nullptr,
@@ -1022,7 +1065,8 @@ moe_status prefill_forward(const moe_expert_views* v, const uint16_t* x, int T, 
   b.hs = (__nv_bfloat16*)(base + L.hs);
   b.o = (float*)(base + L.o);
   MOE_CUDA(cudaMemsetAsync(d_error, 0, sizeof(int32_t), stream));
-  moe_status st = grouped_gemm_fp4(v, x, T, k, slots, b, d_error, stream);
+  moe_status st = grouped_gemm_fp4(v, x, T, k, slots, b, d_error, stream, nullptr,
+                                   prec_mode == MOE_PREC_A_MXFP4 ? 1 : 0);
   if (st != MOE_OK) return st;
   {
     ProfScope ps(MOE_K_COMBINE, stream);
@@ -1039,15 +1083,73 @@ extern "C" size_t moe_expert_prefill_workspace(const moe_expert_views* v, int T,
   return moe::prefill_workspace(v->H, v->I, T, k, v->fp4_num_slots);
 }
 
-extern "C" moe_status moe_expert_prefill(const moe_expert_views* v, const uint16_t* x, int T, int k,
-                                         const int32_t* slots, const float* w, uint16_t* y, void* workspace,
-                                         size_t workspace_bytes, int32_t* d_error, cudaStream_t stream) {
+extern "C" moe_status moe_expert_prefill_prec(const moe_expert_views* v, const uint16_t* x, int T, int k,
+                                              const int32_t* slots, const float* w, int prec_mode, uint16_t* y,
+                                              void* workspace, size_t workspace_bytes, int32_t* d_error,
+                                              cudaStream_t stream) {
   moe::clear_error();
   MOE_ARG(v != nullptr, "views is null");
   MOE_ARG(T >= 0 && k >= 1 && k <= 64, "need T >= 0 and 1 <= k <= 64");
+  MOE_ARG(prec_mode == MOE_PREC_W4A16 || prec_mode == MOE_PREC_A_MXFP4, "unknown precision mode %d", prec_mode);
   if (T == 0) return MOE_OK;
   MOE_ARG(x && slots && w && y && workspace, "null pointer");
   MOE_ARG(((uintptr_t)workspace & 255) == 0, "workspace must be 256-byte aligned");
   MOE_ARG(((uintptr_t)x & 15) == 0, "x must be 16-byte aligned");
-  return moe::prefill_forward(v, x, T, k, slots, w, y, workspace, workspace_bytes, d_error, stream);
+  return moe::prefill_forward(v, x, T, k, slots, w, y, workspace, workspace_bytes, d_error, stream, prec_mode);
+}
+
+extern "C" moe_status moe_expert_prefill(const moe_expert_views* v, const uint16_t* x, int T, int k,
+                                         const int32_t* slots, const float* w, uint16_t* y, void* workspace,
+                                         size_t workspace_bytes, int32_t* d_error, cudaStream_t stream) {
+  return moe_expert_prefill_prec(v, x, T, k, slots, w, MOE_PREC_W4A16, y, workspace, workspace_bytes, d_error,
+                                 stream);
+}
+
+namespace moe {
+// One thread per 32-element block: its 16 code bytes and its scale byte.
+__global__ void mx_quantize_kernel(const uint16_t* x, long long blocks, uint8_t* codes, uint8_t* scales) {
+  for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < blocks;
+       b += (long long)gridDim.x * blockDim.x) {
+    float f[32];
+    const uint4* src = reinterpret_cast<const uint4*>(x + b * 32);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint4 v = src[u];
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        f[8 * u + 2 * q] = __uint_as_float(w4[q] << 16);
+        f[8 * u + 2 * q + 1] = __uint_as_float(w4[q] & 0xffff0000u);
+      }
+    }
+    float am = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) am = fmaxf(am, fabsf(f[i]));
+    const uint32_t sb = mx_scale_byte(am);
+    const float inv = mx_inv_scale(sb);
+    uint32_t o[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) word |= mx_code(f[8 * w + i], inv) << (4 * i);
+      o[w] = word;
+    }
+    reinterpret_cast<uint4*>(codes)[b] = make_uint4(o[0], o[1], o[2], o[3]);
+    scales[b] = (uint8_t)sb;
+  }
+}
+}  // namespace moe
+
+extern "C" moe_status moe_mx_quantize(const uint16_t* x, int rows, int K, uint8_t* codes, uint8_t* scales,
+                                      cudaStream_t stream) {
+  moe::clear_error();
+  MOE_ARG(rows >= 0 && K >= 0 && K % 32 == 0, "need rows >= 0 and K a multiple of 32");
+  if (rows == 0 || K == 0) return MOE_OK;
+  MOE_ARG(x && codes && scales, "null pointer");
+  MOE_ARG(((uintptr_t)x & 15) == 0 && ((uintptr_t)codes & 15) == 0, "x and codes must be 16-byte aligned");
+  const long long blocks = (long long)rows * (K / 32);
+  const int grid = (int)std::min<long long>((blocks + 255) / 256, 152LL * 8);
+  moe::mx_quantize_kernel<<<grid, 256, 0, stream>>>(x, blocks, codes, scales);
+  return moe::check_launch("mx_quantize_kernel");
 }
