@@ -279,6 +279,12 @@ moe_status moe_copy_missing_device_range(moe_cache* cache, const int32_t* d_miss
                                          const int32_t* d_miss_slot, const int32_t* d_miss_count,
                                          size_t byte_begin, size_t byte_end, int max_ctas,
                                          cudaStream_t stream);
+/* Both at once: part `part` of n_parts of the list (as moe_copy_missing_device_
+ * part divides it), bytes [byte_begin, byte_end) of each of its experts. */
+moe_status moe_copy_missing_device_slice(moe_cache* cache, const int32_t* d_miss_key,
+                                         const int32_t* d_miss_slot, const int32_t* d_miss_count, int part,
+                                         int n_parts, size_t byte_begin, size_t byte_end, int max_ctas,
+                                         cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Whole-layer streaming for prefill past the crossover.  "Running DeepSeek-
@@ -404,11 +410,14 @@ moe_status moe_expert_forward(const moe_expert_views* v, const uint16_t* x, int 
  * already complete); 1 <= n_parts <= MOE_MAX_COPY_PARTS.  The workspace size
  * covers every n_parts; the result is the same as moe_expert_forward's.
  *
- * moe_expert_forward_overlap_staged: the missed experts arrive in two stages,
- * their gate/up matrices (event gateup_ready) and then their down matrices
- * (event down_ready); the missed pairs' gate/up work waits only for the
- * first, their down work for the second.  NULL events: already complete.
- * Same workspace and result as moe_expert_forward_overlap.
+ * moe_expert_forward_overlap_staged: the missed experts arrive in stages,
+ * their gate/up matrices (event gateup_ready) and then their down matrices in
+ * n_down_parts parts of the miss list (events down_ready[0..n_down_parts-1],
+ * as moe_copy_missing_device_slice divides the list); the missed pairs'
+ * gate/up work waits only for the first event, the down work of the pairs of
+ * part q for down_ready[q] (the CUDA-core path waits for the last).  NULL
+ * events: already complete; 1 <= n_down_parts <= MOE_MAX_COPY_PARTS.  Same
+ * workspace and result as moe_expert_forward_overlap.
  * ------------------------------------------------------------------------- */
 size_t moe_expert_forward_overlap_workspace(const moe_expert_views* v, int T, int k);
 moe_status moe_expert_forward_overlap(const moe_expert_views* v, const uint16_t* x, int T, int k,
@@ -419,8 +428,9 @@ moe_status moe_expert_forward_overlap(const moe_expert_views* v, const uint16_t*
 moe_status moe_expert_forward_overlap_staged(const moe_expert_views* v, const uint16_t* x, int T, int k,
                                              const int32_t* slots, const float* w, const int32_t* d_miss_slot,
                                              const int32_t* d_miss_count, int max_miss, cudaEvent_t gateup_ready,
-                                             cudaEvent_t down_ready, uint16_t* y, void* workspace,
-                                             size_t workspace_bytes, int32_t* d_error, cudaStream_t stream);
+                                             int n_down_parts, const cudaEvent_t* down_ready, uint16_t* y,
+                                             void* workspace, size_t workspace_bytes, int32_t* d_error,
+                                             cudaStream_t stream);
 moe_status moe_expert_forward_overlap_parts(const moe_expert_views* v, const uint16_t* x, int T, int k,
                                             const int32_t* slots, const float* w, const int32_t* d_miss_slot,
                                             const int32_t* d_miss_count, int max_miss, int n_parts,

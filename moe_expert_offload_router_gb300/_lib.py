@@ -66,6 +66,7 @@ _SIGS = {
     "moe_copy_missing_device_part": (i32, [vp, vp, vp, vp, i32, i32, i32, vp]),
     "moe_cache_prime_bank": (i32, [vp, vp]),
     "moe_copy_missing_device_range": (i32, [vp, vp, vp, vp, sz, sz, i32, vp]),
+    "moe_copy_missing_device_slice": (i32, [vp, vp, vp, vp, i32, i32, sz, sz, i32, vp]),
     "moe_cache_set_policy": (i32, [vp, i32, i32]),
     "moe_cache_seed_frequency": (i32, [vp, vp]),
     "moe_cache_export_frequency": (i32, [vp, vp, vp, vp]),
@@ -83,7 +84,7 @@ _SIGS = {
     "moe_expert_forward_overlap": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, i32, vp,
                                          vp, vp, sz, vp, vp]),
     "moe_expert_forward_overlap_staged": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, i32,
-                                                vp, vp, vp, vp, sz, vp, vp]),
+                                                vp, i32, vp, vp, vp, sz, vp, vp]),
     "moe_expert_forward_overlap_parts": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, i32,
                                                i32, vp, vp, vp, sz, vp, vp]),
     "moe_expert_forward_noalloc": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, vp, vp]),
@@ -300,6 +301,12 @@ def moe_copy_missing_device_range(cache: moe_cache, d_miss_key, d_miss_slot, d_m
                                               byte_begin, byte_end, max_ctas, _s(stream)))
 
 
+def moe_copy_missing_device_slice(cache: moe_cache, d_miss_key, d_miss_slot, d_miss_count, part: int, n_parts: int,
+                                  byte_begin: int, byte_end: int, stream=None, max_ctas: int = 0):
+    _check(_lib.moe_copy_missing_device_slice(cache.handle, _p(d_miss_key), _p(d_miss_slot), _p(d_miss_count),
+                                              part, n_parts, byte_begin, byte_end, max_ctas, _s(stream)))
+
+
 def moe_cache_prime_bank(cache: moe_cache, stream=None):
     """Reads one word of every 4 KB page of the cache's pinned bank from the GPU
     (address translations warmed before the first miss copy)."""
@@ -378,11 +385,15 @@ def moe_expert_forward_overlap(views: moe_expert_views, x, slots, w, d_miss_slot
 def moe_expert_forward_overlap_staged(views: moe_expert_views, x, slots, w, d_miss_slot, d_miss_count,
                                       max_miss: int, gateup_ready, down_ready, y, workspace, d_error=None,
                                       stream=None):
+    """down_ready: one event (or None) per part of the miss list's down matrices, in part order."""
     T, k = slots.shape
+    n = len(down_ready)
+    evs = (C.c_void_p * max(n, 1))(*[_e(e) for e in down_ready])
     _check(_lib.moe_expert_forward_overlap_staged(C.byref(views), _p(x), T, k, _p(slots), _p(w), _p(d_miss_slot),
-                                                  _p(d_miss_count), max_miss, _e(gateup_ready), _e(down_ready),
-                                                  _p(y), _p(workspace), workspace.numel() * workspace.element_size(),
-                                                  _p(d_error), _s(stream)))
+                                                  _p(d_miss_count), max_miss, _e(gateup_ready), n,
+                                                  C.addressof(evs), _p(y), _p(workspace),
+                                                  workspace.numel() * workspace.element_size(), _p(d_error),
+                                                  _s(stream)))
 
 
 def moe_expert_forward_overlap_parts(views: moe_expert_views, x, slots, w, d_miss_slot, d_miss_count,

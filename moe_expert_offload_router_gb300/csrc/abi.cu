@@ -539,6 +539,14 @@ moe_status moe_copy_missing_device_part(moe_cache* c, const int32_t* d_miss_key,
   return copy_missing_launch(c, d_miss_key, d_miss_slot, d_miss_count, part, n_parts, 0, c->B, max_ctas, stream);
 }
 
+moe_status moe_copy_missing_device_slice(moe_cache* c, const int32_t* d_miss_key, const int32_t* d_miss_slot,
+                                         const int32_t* d_miss_count, int part, int n_parts, size_t byte_begin,
+                                         size_t byte_end, int max_ctas, cudaStream_t stream) {
+  clear_error();
+  return copy_missing_launch(c, d_miss_key, d_miss_slot, d_miss_count, part, n_parts, byte_begin, byte_end,
+                             max_ctas, stream);
+}
+
 moe_status moe_copy_missing_device_range(moe_cache* c, const int32_t* d_miss_key, const int32_t* d_miss_slot,
                                          const int32_t* d_miss_count, size_t byte_begin, size_t byte_end,
                                          int max_ctas, cudaStream_t stream) {

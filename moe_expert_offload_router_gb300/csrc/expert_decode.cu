@@ -1095,7 +1095,7 @@ struct FwdPass {
   bool shared = true;            // include the shared expert
   bool combine = true;           // finish with the router-weighted combine into y
   uint8_t* gemm_bufs = nullptr;  // grouped GEMM activation / h copies (else aliased into o / h)
-  cudaEvent_t down_wait = nullptr;  // the stream waits on it before the down matrices are read
+  DownParts down;                // waits before the down matrices are read (per part of the slots)
 };
 
 static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int T, int k, const int32_t* slots,
@@ -1149,7 +1149,7 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
       gb.hs = (__nv_bfloat16*)a.h;
     }
     gb.o = a.o;
-    if ((st = grouped_gemm_fp4(v, x, T, k, slots, gb, d_error, stream, pass.down_wait)) != MOE_OK) return st;
+    if ((st = grouped_gemm_fp4(v, x, T, k, slots, gb, d_error, stream, pass.down)) != MOE_OK) return st;
   }
   // the plan groups the pairs and prepares the fp16 activations for the GEMV
   // kernels; a routed-GEMM pass without the shared expert runs none of them
@@ -1187,7 +1187,9 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
   }
   if ((st = check_launch("gateup_kernel")) != MOE_OK) return st;
 
-  if (gemv && pass.down_wait) MOE_CUDA(cudaStreamWaitEvent(stream, pass.down_wait, 0));
+  // the GEMV down kernel reads every slot's matrices: it waits for the last part
+  if (gemv && pass.down.n >= 1 && pass.down.ready && pass.down.ready[pass.down.n - 1])
+    MOE_CUDA(cudaStreamWaitEvent(stream, pass.down.ready[pass.down.n - 1], 0));
   const size_t dn_smem = (size_t)kG * v->I * 4 + 2 * kG * 4;
   const long long dn_items = max_groups * ((v->H + kRowsDown - 1) / kRowsDown);
   if (!gemv) {
@@ -1216,29 +1218,37 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
 // whose expert is copied in with part q (every other entry -1).
 __global__ void __launch_bounds__(1024) split_miss_kernel(const int32_t* slots, int P, const int32_t* miss_slot,
                                                           const int32_t* miss_count, int max_miss, int S,
-                                                          int parts, int32_t* hit, int32_t* miss) {
+                                                          int parts, int32_t* hit, int32_t* miss,
+                                                          int slot_parts, int8_t* slot_part) {
   extern __shared__ int8_t part_of[];  // [S]: part of the slot's miss, -1 if not missed
   for (int i = threadIdx.x; i < S; i += blockDim.x) part_of[i] = -1;
   __syncthreads();
   const int n = min(max(*miss_count, 0), max_miss);
+  const int np = parts > 1 ? parts : slot_parts;  // the partition the arrays or the slot index follow
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const int sl = miss_slot[i];
     int q = 0;
-    while (q + 1 < parts && (long long)n * (q + 1) / parts <= i) ++q;
+    while (q + 1 < np && (long long)n * (q + 1) / np <= i) ++q;
     if (sl >= 0 && sl < S) part_of[sl] = (int8_t)q;
   }
   __syncthreads();
+  if (slot_part && blockIdx.x == 0)
+    for (int i = threadIdx.x; i < S; i += blockDim.x) slot_part[i] = part_of[i];
   for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < P; p += gridDim.x * blockDim.x) {
     const int sl = slots[p];
     const int q = (sl >= 0 && sl < S) ? part_of[sl] : -1;
     hit[p] = q >= 0 ? -1 : sl;
-    for (int r = 0; r < parts; ++r) miss[(size_t)r * P + p] = q == r ? sl : -1;
+    if (parts > 1) {
+      for (int r = 0; r < parts; ++r) miss[(size_t)r * P + p] = q == r ? sl : -1;
+    } else {
+      miss[p] = q >= 0 ? sl : -1;
+    }
   }
 }
 
 static size_t overlap_extra(const moe_expert_views* v, int T, int k, const FwdLayout& L) {
   const size_t P = (size_t)T * k;
-  size_t b = align256(P * 4) + align256((size_t)MOE_MAX_COPY_PARTS * P * 4);
+  size_t b = align256(P * 4) + align256((size_t)MOE_MAX_COPY_PARTS * P * 4) + align256((size_t)v->fp4_num_slots);
   if (L.gemm) b += align256(P * v->H * 4 + P * v->I * 2);
   return b;
 }
@@ -1303,13 +1313,15 @@ extern "C" moe_status moe_expert_forward_overlap_parts(const moe_expert_views* v
   int32_t* hit = (int32_t*)(base + L.total);
   int32_t* miss = (int32_t*)(base + L.total + align256(P * 4));
   uint8_t* gemm_bufs =
-      L.gemm ? base + L.total + align256(P * 4) + align256((size_t)MOE_MAX_COPY_PARTS * P * 4) : nullptr;
+      L.gemm ? base + L.total + align256(P * 4) + align256((size_t)MOE_MAX_COPY_PARTS * P * 4) +
+                   align256((size_t)v->fp4_num_slots)
+             : nullptr;
   if (d_error) MOE_CUDA(cudaMemsetAsync(d_error, 0, sizeof(int32_t), stream));
   const int S = v->fp4_num_slots;
   if ((st = set_smem(split_miss_kernel, (size_t)S)) != MOE_OK) return st;
   split_miss_kernel<<<(int)((P + 1023) / 1024), 1024, (size_t)S, stream>>>(slots, (int)P, d_miss_slot,
                                                                           d_miss_count, max_miss, S, n_parts,
-                                                                          hit, miss);
+                                                                          hit, miss, 1, nullptr);
   if ((st = check_launch("split_miss_kernel")) != MOE_OK) return st;
   // pass 1: pairs whose experts were resident, and the shared expert, while
   // the misses are still being copied
@@ -1352,9 +1364,9 @@ extern "C" moe_status moe_expert_forward_overlap_parts(const moe_expert_views* v
 extern "C" moe_status moe_expert_forward_overlap_staged(const moe_expert_views* v, const uint16_t* x, int T, int k,
                                                         const int32_t* slots, const float* w,
                                                         const int32_t* d_miss_slot, const int32_t* d_miss_count,
-                                                        int max_miss, cudaEvent_t gateup_ready,
-                                                        cudaEvent_t down_ready, uint16_t* y, void* workspace,
-                                                        size_t workspace_bytes, int32_t* d_error,
+                                                        int max_miss, cudaEvent_t gateup_ready, int n_down_parts,
+                                                        const cudaEvent_t* down_ready, uint16_t* y,
+                                                        void* workspace, size_t workspace_bytes, int32_t* d_error,
                                                         cudaStream_t stream) {
   clear_error();
   moe_status st = validate_views(v);
@@ -1363,7 +1375,9 @@ extern "C" moe_status moe_expert_forward_overlap_staged(const moe_expert_views* 
   if (T == 0) return MOE_OK;
   MOE_ARG((long long)T * k <= kMaxPlanPairs, "T * k = %lld above the %d pairs of one overlapped call",
           (long long)T * k, kMaxPlanPairs);
-  MOE_ARG(x && slots && w && y && workspace && d_miss_slot && d_miss_count, "null pointer");
+  MOE_ARG(x && slots && w && y && workspace && d_miss_slot && d_miss_count && down_ready, "null pointer");
+  MOE_ARG(n_down_parts >= 1 && n_down_parts <= MOE_MAX_COPY_PARTS, "n_down_parts %d outside [1, %d]", n_down_parts,
+          MOE_MAX_COPY_PARTS);
   MOE_ARG(v->fp4_slots != nullptr, "no FP4 pool");
   MOE_ARG(max_miss >= 0, "max_miss < 0");
   MOE_ARG(((uintptr_t)workspace & 255) == 0, "workspace must be 256-byte aligned");
@@ -1375,12 +1389,16 @@ extern "C" moe_status moe_expert_forward_overlap_staged(const moe_expert_views* 
   int32_t* hit = (int32_t*)(base + L.total);
   int32_t* miss = (int32_t*)(base + L.total + align256(P * 4));
   uint8_t* gemm_bufs =
-      L.gemm ? base + L.total + align256(P * 4) + align256((size_t)MOE_MAX_COPY_PARTS * P * 4) : nullptr;
+      L.gemm ? base + L.total + align256(P * 4) + align256((size_t)MOE_MAX_COPY_PARTS * P * 4) +
+                   align256((size_t)v->fp4_num_slots)
+             : nullptr;
+  int8_t* slot_part = (int8_t*)(base + L.total + align256(P * 4) + align256((size_t)MOE_MAX_COPY_PARTS * P * 4));
   if (d_error) MOE_CUDA(cudaMemsetAsync(d_error, 0, sizeof(int32_t), stream));
   const int S = v->fp4_num_slots;
   if ((st = set_smem(split_miss_kernel, (size_t)S)) != MOE_OK) return st;
   split_miss_kernel<<<(int)((P + 1023) / 1024), 1024, (size_t)S, stream>>>(slots, (int)P, d_miss_slot,
-                                                                          d_miss_count, max_miss, S, 1, hit, miss);
+                                                                          d_miss_count, max_miss, S, 1, hit, miss,
+                                                                          n_down_parts, slot_part);
   if ((st = check_launch("split_miss_kernel")) != MOE_OK) return st;
   FwdPass p1;
   p1.combine = false;
@@ -1392,7 +1410,9 @@ extern "C" moe_status moe_expert_forward_overlap_staged(const moe_expert_views* 
   p2.shared = false;
   p2.combine = false;
   p2.gemm_bufs = gemm_bufs;
-  p2.down_wait = down_ready;
+  p2.down.n = n_down_parts;
+  p2.down.ready = down_ready;
+  p2.down.slot_part = slot_part;
   if ((st = forward_pass(v, x, T, k, miss, nullptr, w, y, base, L, d_error, stream, p2)) != MOE_OK) return st;
   FwdArgs a{};
   a.H = v->H;

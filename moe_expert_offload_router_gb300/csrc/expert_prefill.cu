@@ -252,6 +252,8 @@ struct PfArgs {
   int rows;
   int o_row0;
   int mx;             // mode 0: h quantised to MXFP4 along I (blocks of 32 features) before the store
+  const int8_t* slot_part;  // non-null: only items whose slot_part[slot] == part_sel run
+  int part_sel;
 };
 
 // FP8 = false: MXFP4 experts of the slot pool (E2M1 codes with E8M0 block
@@ -291,6 +293,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   } else {
     if (item_idx >= *a.n_items) return;
     it = a.items[item_idx];
+    if (a.slot_part && (it.slot < 0 || it.slot >= a.S || a.slot_part[it.slot] != a.part_sel)) return;
   }
   if (it.count > C::kNMax || it.count < 1) {  // the host picks the shape from T; never expected
     if (threadIdx.x == 0) atomicCAS(a.err, 0, MOE_ERR_INVALID);
@@ -852,7 +855,7 @@ void gg_carve_index(uint8_t* base, int T, int k, int S, GgBufs* b) {
 }
 
 moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T, int k, const int32_t* slots,
-                            const GgBufs& b, int32_t* d_error, cudaStream_t stream, cudaEvent_t before_down,
+                            const GgBufs& b, int32_t* d_error, cudaStream_t stream, const DownParts& down,
                             int mx_act) {
   const int H = v->H, I = v->I, S = v->fp4_num_slots;
   const size_t P = (size_t)T * k;
@@ -929,19 +932,27 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
     launch(m1c, m3c, mx, mx16);
   }
   if ((st = check_launch("prefill_gemm_kernel (gate/up)")) != MOE_OK) return st;
-  if (before_down) MOE_CUDA(cudaStreamWaitEvent(stream, before_down, 0));
-  // GEMM2: down, 256 output features (two tiles of 128) per CTA
+  // GEMM2: down, 256 output features (two tiles of 128) per CTA; with parts,
+  // one launch per part of the slots once that part's down matrices are in
   pa.mode = 1;
   pa.K = I;
   pa.tiles = H / 256;
   pa.sc0 = w2s;
   pa.sc1 = w2s;
   pa.allow_f16 = 0;
-  {
-    ProfScope ps(MOE_K_GEMM_DOWN, stream);
-    launch(m2c, m2c, mh, mh);
+  const int np = down.n > 1 && down.slot_part ? down.n : 1;
+  for (int q = 0; q < np; ++q) {
+    const cudaEvent_t ev = down.n >= 1 && down.ready ? down.ready[np == 1 ? down.n - 1 : q] : nullptr;
+    if (ev) MOE_CUDA(cudaStreamWaitEvent(stream, ev, 0));
+    pa.slot_part = np > 1 ? down.slot_part : nullptr;
+    pa.part_sel = q;
+    {
+      ProfScope ps(MOE_K_GEMM_DOWN, stream);
+      launch(m2c, m2c, mh, mh);
+    }
+    if ((st = check_launch("prefill_gemm_kernel (down)")) != MOE_OK) return st;
   }
-  return check_launch("prefill_gemm_kernel (down)");
+  return MOE_OK;
 }
 
 // rank-2 byte map: (x: row bytes, y: rows)
@@ -1065,7 +1076,7 @@ moe_status prefill_forward(const moe_expert_views* v, const uint16_t* x, int T, 
   b.hs = (__nv_bfloat16*)(base + L.hs);
   b.o = (float*)(base + L.o);
   MOE_CUDA(cudaMemsetAsync(d_error, 0, sizeof(int32_t), stream));
-  moe_status st = grouped_gemm_fp4(v, x, T, k, slots, b, d_error, stream, nullptr,
+  moe_status st = grouped_gemm_fp4(v, x, T, k, slots, b, d_error, stream, DownParts(),
                                    prec_mode == MOE_PREC_A_MXFP4 ? 1 : 0);
   if (st != MOE_OK) return st;
   {

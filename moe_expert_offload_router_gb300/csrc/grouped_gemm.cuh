@@ -31,13 +31,20 @@ bool grouped_gemm_supported(const moe_expert_views* v);
 size_t gg_index_bytes(int T, int k, int S);                   // offsets .. cnt, 256-aligned pieces
 void gg_carve_index(uint8_t* base, int T, int k, int S, GgBufs* b);
 // Writes o rows of every pair with 0 <= slot < S; other rows are untouched.
-// before_down (may be null): the stream waits on it between the gate/up and
-// down GEMMs (the down matrices of some slots may still be landing).
+// Waits before the down GEMM, whose matrices may still be landing: with n
+// events and a per-slot part index (device int8 [S], -1 = none), the down GEMM
+// runs once per part q after ready[q], over the items of the slots of part q;
+// with one event (or no part index) it waits on the last and runs once.
+struct DownParts {
+  int n = 0;
+  const cudaEvent_t* ready = nullptr;
+  const int8_t* slot_part = nullptr;
+};
 // mx_act != 0: x and h are quantised to MXFP4 (OCP MX, blocks of 32 along K) and
 // the products run on their exact values.
 moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T, int k, const int32_t* slots,
                             const GgBufs& b, int32_t* d_error, cudaStream_t stream,
-                            cudaEvent_t before_down = nullptr, int mx_act = 0);
+                            const DownParts& down = DownParts(), int mx_act = 0);
 // The FP8 shared expert (v->shared) over all T tokens on the tensor cores:
 // xs = fp16 activations [T, H], row t scaled by 2^-xsig[t]; hs = bf16 SwiGLU
 // scratch [T, I]; writes o rows o_row0 .. o_row0 + T - 1 (fp32 [., H]).

@@ -54,7 +54,8 @@ class DecodeLayerRunner:
     def __init__(self, cache: L.moe_cache, views: L.moe_expert_views, E: int, k: int,
                  T_max: int, device=None, int2_cache: Optional[L.moe_cache] = None,
                  ladder=None, assume_resident: bool = False, copy: str = "engine",
-                 overlap=False, copy_ctas: int = 32, graph: bool = False, copy_parts: int = 1):
+                 overlap=False, copy_ctas: int = 32, graph: bool = False, copy_parts: int = 1,
+                 down_parts: int = 1):
         self.cache, self.views, self.E, self.k, self.T_max = cache, views, E, k, T_max
         self.dev = torch.device(device or "cuda")
         self.c2, self.ladder = int2_cache, ladder
@@ -95,6 +96,9 @@ class DecodeLayerRunner:
         self.copy_parts = copy_parts
         self.part_done = [torch.cuda.Event() for _ in range(copy_parts)]
         self.gu_done = torch.cuda.Event()
+        if not 1 <= down_parts <= L.MOE_MAX_COPY_PARTS:
+            raise ValueError(f"down_parts must be in [1, {L.MOE_MAX_COPY_PARTS}]")
+        self.down_done = [torch.cuda.Event() for _ in range(down_parts)]
         # bytes of one FP4 matrix (codes + E8M0 scales); w1 and w3 come first in an expert
         self.gu_half = views.H * views.I // 2 + views.H * views.I // 32
         self.ws_ov = (torch.empty(L.moe_expert_forward_overlap_workspace(views, T_max, k), dtype=torch.uint8,
@@ -184,14 +188,17 @@ class DecodeLayerRunner:
                 self.ready.record(stream)
                 self.copy_stream.wait_event(self.ready)
                 if self.copy_parts == 1:
-                    # every miss's gate/up matrices first, then their down matrices
+                    # every miss's gate/up matrices first, then their down
+                    # matrices in parts of the miss list
                     gu = 2 * self.gu_half
                     L.moe_copy_missing_device_range(self.cache, v["keys4"], v["slots4"], v["count4"], 0, gu,
                                                     self.copy_stream, self.copy_ctas)
                     self.gu_done.record(self.copy_stream)
-                    L.moe_copy_missing_device_range(self.cache, v["keys4"], v["slots4"], v["count4"], gu,
-                                                    self.cache.B, self.copy_stream, self.copy_ctas)
-                    self.part_done[0].record(self.copy_stream)
+                    nd = len(self.down_done)
+                    for q, ev in enumerate(self.down_done):
+                        L.moe_copy_missing_device_slice(self.cache, v["keys4"], v["slots4"], v["count4"], q, nd,
+                                                        gu, self.cache.B, self.copy_stream, self.copy_ctas)
+                        ev.record(self.copy_stream)
                 else:
                     for q, ev in enumerate(self.part_done):
                         L.moe_copy_missing_device_part(self.cache, v["keys4"], v["slots4"], v["count4"], q,
@@ -210,7 +217,7 @@ class DecodeLayerRunner:
                     prefetch = None
                 if self.copy_parts == 1:
                     L.moe_expert_forward_overlap_staged(self.views, x[tb:T], slots[tb:T], w[tb:T], v["slots4"],
-                                                        v["count4"], self.m4, self.gu_done, self.part_done[0],
+                                                        v["count4"], self.m4, self.gu_done, self.down_done,
                                                         y[tb:T], self.ws_ov, self.err, stream)
                 else:
                     L.moe_expert_forward_overlap_parts(self.views, x[tb:T], slots[tb:T], w[tb:T], v["slots4"],

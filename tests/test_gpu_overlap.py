@@ -32,7 +32,9 @@ def _overlap(M, P, x_bits, slots, w, miss_slots, event=None, parts=None):
     if parts is None:
         M.moe_expert_forward_overlap(*args, event, y, ws, err)
     elif parts == "staged":
-        M.moe_expert_forward_overlap_staged(*args, event, event, y, ws, err)
+        M.moe_expert_forward_overlap_staged(*args, event, [event], y, ws, err)
+    elif parts == "staged3":
+        M.moe_expert_forward_overlap_staged(*args, event, [event] * 3, y, ws, err)
     else:
         M.moe_expert_forward_overlap_parts(*args, [event] * parts, y, ws, err)
     torch.cuda.synchronize()
@@ -60,7 +62,8 @@ def test_overlap_equals_forward_decode_shape(T, nmiss):
 
 
 @pytest.mark.parametrize("T,nmiss,parts", [(64, 9, 2), (64, 9, 4), (64, 1, 3), (64, 64, 3), (16, 5, 2),
-                                           (64, 0, 2), (64, 9, "staged"), (16, 5, "staged"), (64, 64, "staged")])
+                                           (64, 0, 2), (64, 9, "staged"), (16, 5, "staged"), (64, 64, "staged"),
+                                           (64, 9, "staged3"), (64, 1, "staged3"), (16, 5, "staged3")])
 def test_overlap_parts_equal_forward(T, nmiss, parts):
     # misses split into parts as the part-wise copy divides the list (a part
     # may be empty); every pair is still computed exactly once
@@ -134,6 +137,8 @@ def _decoder(bank_np, B, wl):
     (configs.TINY, 4, 6, True, 2),                                   # chunked
     (configs.scaled(configs.DECODE, T=4), 64, 4, False, 1),          # single chunk, CUDA-core path
     (configs.scaled(configs.DECODE, T=64), 40, 3, False, 1),         # chunked, grouped GEMM, staged copies
+    (configs.scaled(configs.DECODE, T=64), 64, 3, False, (1, 2)),    # staged, down matrices in two parts
+    (configs.scaled(configs.DECODE, T=64), 64, 3, False, (1, 3)),    # staged, down matrices in three parts
     (configs.scaled(configs.DECODE, T=64), 40, 3, False, 2),         # chunked, grouped GEMM, two parts
     (configs.scaled(configs.DECODE, T=64), 64, 3, False, 3),         # grouped GEMM, three copy parts
 ])
@@ -144,7 +149,9 @@ def test_layer_overlapped_copy(wl, S, steps, full, parts):
     cache = M.moe_cache(S, 1, wl.E, B, slots, bank)
     sh = torch.from_numpy(gen.shared_expert(wl, 0)).cuda() if wl.shared else None
     views = M.make_views(wl.H, wl.I, slots, S, None, 0, sh)
-    runner = M.DecodeLayerRunner(cache, views, wl.E, wl.k, wl.T, copy="device", overlap=True, copy_parts=parts)
+    cp, dp = parts if isinstance(parts, tuple) else (parts, 1)
+    runner = M.DecodeLayerRunner(cache, views, wl.E, wl.k, wl.T, copy="device", overlap=True, copy_parts=cp,
+                                 down_parts=dp)
     ref = SlotCacheLRU(S, 1, wl.E)
     dec = _decoder(bank.numpy(), B, wl)
     shw = F.decode_fp8_expert(gen.shared_expert(wl, 0), wl.H, wl.I) if wl.shared else None
