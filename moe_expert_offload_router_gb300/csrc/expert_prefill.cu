@@ -887,7 +887,7 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
   if ((st = map_bf16_rows(&mh, b.hs, I, P)) != MOE_OK) return st;
 
   // items hold at most T rows (each token routes to a slot once): up to 64
-  // tokens take the deep-ring shape
+  // tokens take the small shape (four operand stages)
   const bool small = T <= PfSmall::kNMax;
   static bool smem_set[2] = {false, false};
   if (!smem_set[small]) {
