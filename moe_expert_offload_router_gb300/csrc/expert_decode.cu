@@ -1286,59 +1286,79 @@ extern "C" size_t moe_expert_forward_overlap_workspace(const moe_expert_views* v
   return L.total + overlap_extra(v, T, k, L);
 }
 
-extern "C" moe_status moe_expert_forward_overlap_parts(const moe_expert_views* v, const uint16_t* x, int T, int k,
-                                                       const int32_t* slots, const float* w,
-                                                       const int32_t* d_miss_slot, const int32_t* d_miss_count,
-                                                       int max_miss, int n_parts, const cudaEvent_t* parts_done,
-                                                       uint16_t* y, void* workspace, size_t workspace_bytes,
-                                                       int32_t* d_error, cudaStream_t stream) {
-  clear_error();
+namespace moe {
+
+// How the missed pairs follow their copies: `parts` passes over parts of the
+// miss list, pass q after parts_done[q]; or (parts == 0, staged) one pass
+// whose gate/up waits for gateup_ready and whose down work waits for
+// down_ready[q] per part q of the slots (down_parts of them).
+struct OverlapPlan {
+  int parts = 1;
+  const cudaEvent_t* parts_done = nullptr;
+  cudaEvent_t gateup_ready = nullptr;
+  int down_parts = 1;
+  const cudaEvent_t* down_ready = nullptr;
+};
+
+static moe_status forward_overlap(const moe_expert_views* v, const uint16_t* x, int T, int k, const int32_t* slots,
+                                  const float* w, const int32_t* d_miss_slot, const int32_t* d_miss_count,
+                                  int max_miss, const OverlapPlan& plan, uint16_t* y, void* workspace,
+                                  size_t workspace_bytes, int32_t* d_error, cudaStream_t stream) {
   moe_status st = validate_views(v);
   if (st != MOE_OK) return st;
   MOE_ARG(T >= 0 && k >= 1 && k <= 64, "need T >= 0 and 1 <= k <= 64");
-  MOE_ARG(n_parts >= 1 && n_parts <= MOE_MAX_COPY_PARTS, "n_parts %d outside [1, %d]", n_parts,
-          MOE_MAX_COPY_PARTS);
   if (T == 0) return MOE_OK;
   MOE_ARG((long long)T * k <= kMaxPlanPairs, "T * k = %lld above the %d pairs of one overlapped call",
           (long long)T * k, kMaxPlanPairs);
-  MOE_ARG(x && slots && w && y && workspace && d_miss_slot && d_miss_count && parts_done, "null pointer");
+  MOE_ARG(x && slots && w && y && workspace && d_miss_slot && d_miss_count, "null pointer");
   MOE_ARG(v->fp4_slots != nullptr, "no FP4 pool");
   MOE_ARG(max_miss >= 0, "max_miss < 0");
   MOE_ARG(((uintptr_t)workspace & 255) == 0, "workspace must be 256-byte aligned");
   const FwdLayout L = fwd_layout(v, T, k);
   const size_t need = L.total + overlap_extra(v, T, k, L);
   MOE_ARG(workspace_bytes >= need, "workspace too small: %zu < %zu", workspace_bytes, need);
+  // workspace past the forward's own: hit slots [P], miss slots [parts][P],
+  // the slots' part index [S], then the miss pass's GEMM buffers
   uint8_t* base = (uint8_t*)workspace;
   const size_t P = (size_t)T * k;
+  const int S = v->fp4_num_slots;
   int32_t* hit = (int32_t*)(base + L.total);
   int32_t* miss = (int32_t*)(base + L.total + align256(P * 4));
-  uint8_t* gemm_bufs =
-      L.gemm ? base + L.total + align256(P * 4) + align256((size_t)MOE_MAX_COPY_PARTS * P * 4) +
-                   align256((size_t)v->fp4_num_slots)
-             : nullptr;
+  int8_t* slot_part = (int8_t*)(base + L.total + align256(P * 4) + align256((size_t)MOE_MAX_COPY_PARTS * P * 4));
+  uint8_t* gemm_bufs = L.gemm ? (uint8_t*)slot_part + align256((size_t)S) : nullptr;
+  const bool staged = plan.parts == 0;
   if (d_error) MOE_CUDA(cudaMemsetAsync(d_error, 0, sizeof(int32_t), stream));
-  const int S = v->fp4_num_slots;
   if ((st = set_smem(split_miss_kernel, (size_t)S)) != MOE_OK) return st;
-  split_miss_kernel<<<(int)((P + 1023) / 1024), 1024, (size_t)S, stream>>>(slots, (int)P, d_miss_slot,
-                                                                          d_miss_count, max_miss, S, n_parts,
-                                                                          hit, miss, 1, nullptr);
+  split_miss_kernel<<<(int)((P + 1023) / 1024), 1024, (size_t)S, stream>>>(
+      slots, (int)P, d_miss_slot, d_miss_count, max_miss, S, staged ? 1 : plan.parts, hit, miss,
+      staged ? plan.down_parts : 1, staged ? slot_part : nullptr);
   if ((st = check_launch("split_miss_kernel")) != MOE_OK) return st;
   // pass 1: pairs whose experts were resident, and the shared expert, while
   // the misses are still being copied
   FwdPass p1;
   p1.combine = false;
   if ((st = forward_pass(v, x, T, k, hit, nullptr, w, y, base, L, d_error, stream, p1)) != MOE_OK) return st;
-  // then each part's pairs once that part's copies have landed; the passes
-  // run in order on the stream, so they can share the GEMM's buffers
-  for (int q = 0; q < n_parts; ++q) {
-    if (parts_done[q]) MOE_CUDA(cudaStreamWaitEvent(stream, parts_done[q], 0));
-    FwdPass p2;
-    p2.shared = false;
-    p2.combine = false;
-    p2.gemm_bufs = gemm_bufs;
-    if ((st = forward_pass(v, x, T, k, miss + (size_t)q * P, nullptr, w, y, base, L, d_error, stream, p2)) !=
-        MOE_OK)
-      return st;
+  // then the missed pairs as their bytes land; the passes run in order on the
+  // stream, so they can share the GEMM's buffers
+  FwdPass p2;
+  p2.shared = false;
+  p2.combine = false;
+  p2.gemm_bufs = gemm_bufs;
+  if (staged) {
+    // the gate/up matrices have landed: the first GEMM runs while the down
+    // matrices are still on the way
+    if (plan.gateup_ready) MOE_CUDA(cudaStreamWaitEvent(stream, plan.gateup_ready, 0));
+    p2.down.n = plan.down_parts;
+    p2.down.ready = plan.down_ready;
+    p2.down.slot_part = slot_part;
+    if ((st = forward_pass(v, x, T, k, miss, nullptr, w, y, base, L, d_error, stream, p2)) != MOE_OK) return st;
+  } else {
+    for (int q = 0; q < plan.parts; ++q) {
+      if (plan.parts_done[q]) MOE_CUDA(cudaStreamWaitEvent(stream, plan.parts_done[q], 0));
+      if ((st = forward_pass(v, x, T, k, miss + (size_t)q * P, nullptr, w, y, base, L, d_error, stream, p2)) !=
+          MOE_OK)
+        return st;
+    }
   }
   // one combine over every pair of the chunk
   FwdArgs a{};
@@ -1347,7 +1367,7 @@ extern "C" moe_status moe_expert_forward_overlap_parts(const moe_expert_views* v
   a.T = T;
   a.k = k;
   a.P = (int)P;
-  a.n4 = v->fp4_num_slots;
+  a.n4 = S;
   a.n2 = 0;
   a.shared = v->shared;
   a.slots = slots;
@@ -1361,6 +1381,25 @@ extern "C" moe_status moe_expert_forward_overlap_parts(const moe_expert_views* v
   return check_launch("combine_kernel");
 }
 
+}  // namespace moe
+
+extern "C" moe_status moe_expert_forward_overlap_parts(const moe_expert_views* v, const uint16_t* x, int T, int k,
+                                                       const int32_t* slots, const float* w,
+                                                       const int32_t* d_miss_slot, const int32_t* d_miss_count,
+                                                       int max_miss, int n_parts, const cudaEvent_t* parts_done,
+                                                       uint16_t* y, void* workspace, size_t workspace_bytes,
+                                                       int32_t* d_error, cudaStream_t stream) {
+  clear_error();
+  MOE_ARG(n_parts >= 1 && n_parts <= MOE_MAX_COPY_PARTS, "n_parts %d outside [1, %d]", n_parts,
+          MOE_MAX_COPY_PARTS);
+  MOE_ARG(parts_done != nullptr, "null pointer");
+  OverlapPlan plan;
+  plan.parts = n_parts;
+  plan.parts_done = parts_done;
+  return forward_overlap(v, x, T, k, slots, w, d_miss_slot, d_miss_count, max_miss, plan, y, workspace,
+                         workspace_bytes, d_error, stream);
+}
+
 extern "C" moe_status moe_expert_forward_overlap_staged(const moe_expert_views* v, const uint16_t* x, int T, int k,
                                                         const int32_t* slots, const float* w,
                                                         const int32_t* d_miss_slot, const int32_t* d_miss_count,
@@ -1369,69 +1408,16 @@ extern "C" moe_status moe_expert_forward_overlap_staged(const moe_expert_views* 
                                                         void* workspace, size_t workspace_bytes, int32_t* d_error,
                                                         cudaStream_t stream) {
   clear_error();
-  moe_status st = validate_views(v);
-  if (st != MOE_OK) return st;
-  MOE_ARG(T >= 0 && k >= 1 && k <= 64, "need T >= 0 and 1 <= k <= 64");
-  if (T == 0) return MOE_OK;
-  MOE_ARG((long long)T * k <= kMaxPlanPairs, "T * k = %lld above the %d pairs of one overlapped call",
-          (long long)T * k, kMaxPlanPairs);
-  MOE_ARG(x && slots && w && y && workspace && d_miss_slot && d_miss_count && down_ready, "null pointer");
   MOE_ARG(n_down_parts >= 1 && n_down_parts <= MOE_MAX_COPY_PARTS, "n_down_parts %d outside [1, %d]", n_down_parts,
           MOE_MAX_COPY_PARTS);
-  MOE_ARG(v->fp4_slots != nullptr, "no FP4 pool");
-  MOE_ARG(max_miss >= 0, "max_miss < 0");
-  MOE_ARG(((uintptr_t)workspace & 255) == 0, "workspace must be 256-byte aligned");
-  const FwdLayout L = fwd_layout(v, T, k);
-  const size_t need = L.total + overlap_extra(v, T, k, L);
-  MOE_ARG(workspace_bytes >= need, "workspace too small: %zu < %zu", workspace_bytes, need);
-  uint8_t* base = (uint8_t*)workspace;
-  const size_t P = (size_t)T * k;
-  int32_t* hit = (int32_t*)(base + L.total);
-  int32_t* miss = (int32_t*)(base + L.total + align256(P * 4));
-  uint8_t* gemm_bufs =
-      L.gemm ? base + L.total + align256(P * 4) + align256((size_t)MOE_MAX_COPY_PARTS * P * 4) +
-                   align256((size_t)v->fp4_num_slots)
-             : nullptr;
-  int8_t* slot_part = (int8_t*)(base + L.total + align256(P * 4) + align256((size_t)MOE_MAX_COPY_PARTS * P * 4));
-  if (d_error) MOE_CUDA(cudaMemsetAsync(d_error, 0, sizeof(int32_t), stream));
-  const int S = v->fp4_num_slots;
-  if ((st = set_smem(split_miss_kernel, (size_t)S)) != MOE_OK) return st;
-  split_miss_kernel<<<(int)((P + 1023) / 1024), 1024, (size_t)S, stream>>>(slots, (int)P, d_miss_slot,
-                                                                          d_miss_count, max_miss, S, 1, hit, miss,
-                                                                          n_down_parts, slot_part);
-  if ((st = check_launch("split_miss_kernel")) != MOE_OK) return st;
-  FwdPass p1;
-  p1.combine = false;
-  if ((st = forward_pass(v, x, T, k, hit, nullptr, w, y, base, L, d_error, stream, p1)) != MOE_OK) return st;
-  // the missed experts' gate/up matrices have landed: their pairs' first
-  // GEMM runs while the down matrices are still on the way
-  if (gateup_ready) MOE_CUDA(cudaStreamWaitEvent(stream, gateup_ready, 0));
-  FwdPass p2;
-  p2.shared = false;
-  p2.combine = false;
-  p2.gemm_bufs = gemm_bufs;
-  p2.down.n = n_down_parts;
-  p2.down.ready = down_ready;
-  p2.down.slot_part = slot_part;
-  if ((st = forward_pass(v, x, T, k, miss, nullptr, w, y, base, L, d_error, stream, p2)) != MOE_OK) return st;
-  FwdArgs a{};
-  a.H = v->H;
-  a.I = v->I;
-  a.T = T;
-  a.k = k;
-  a.P = (int)P;
-  a.n4 = v->fp4_num_slots;
-  a.n2 = 0;
-  a.shared = v->shared;
-  a.slots = slots;
-  a.tags = nullptr;
-  a.w = w;
-  a.y = y;
-  a.o = (float*)(base + L.o);
-  dim3 cg((v->H / 4 + 255) / 256, T);
-  ProfScope ps(MOE_K_COMBINE, stream);
-  combine_kernel<<<cg, 256, 0, stream>>>(a);
-  return check_launch("combine_kernel");
+  MOE_ARG(down_ready != nullptr, "null pointer");
+  OverlapPlan plan;
+  plan.parts = 0;
+  plan.gateup_ready = gateup_ready;
+  plan.down_parts = n_down_parts;
+  plan.down_ready = down_ready;
+  return forward_overlap(v, x, T, k, slots, w, d_miss_slot, d_miss_count, max_miss, plan, y, workspace,
+                         workspace_bytes, d_error, stream);
 }
 
 extern "C" moe_status moe_expert_forward_overlap(const moe_expert_views* v, const uint16_t* x, int T, int k,
