@@ -1030,15 +1030,12 @@ __global__ void __launch_bounds__(256) rms_carry_kernel(const uint16_t* y, int H
 
 // ------------------------------------------------------------------- host --
 
+// SM count of the current device.
 static int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
-  }
-  return n;
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
 }
 
 template <typename K>

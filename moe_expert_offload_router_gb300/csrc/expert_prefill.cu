@@ -889,14 +889,13 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
   // items hold at most T rows (each token routes to a slot once): up to 64
   // tokens take the small shape (four operand stages)
   const bool small = T <= PfSmall::kNMax;
-  static bool smem_set[2] = {false, false};
-  if (!smem_set[small]) {
+  {
+    // a function attribute holds per device: set it on every call
     cudaError_t e = small ? cudaFuncSetAttribute(prefill_gemm_kernel<PfSmall, false>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, PfSmall::kSmem)
                           : cudaFuncSetAttribute(prefill_gemm_kernel<PfBig, false>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, PfBig::kSmem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_gemm_kernel)");
-    smem_set[small] = true;
   }
   // items: at most one per used slot, plus one per 256 further rows (wide shape)
   const int max_items = (int)std::min<size_t>((size_t)S, P) + (small ? 0 : (int)(P / kPfNMax) + 1);
@@ -988,12 +987,10 @@ moe_status grouped_gemm_shared_fp8(const moe_expert_views* v, const __half* xs, 
   if ((st = map_bytes2(&m2, w2, I, H, 64, 256)) != MOE_OK) return st;
   if ((st = map_bf16_rows(&mx16, xs, H, T, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != MOE_OK) return st;
   if ((st = map_bf16_rows(&mh, hs, I, T)) != MOE_OK) return st;
-  static bool smem_set = false;
-  if (!smem_set) {
+  {
     cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel<C, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_gemm_kernel, FP8)");
-    smem_set = true;
   }
   const int items = (T + C::kNMax - 1) / C::kNMax;
   PfArgs pa{};
