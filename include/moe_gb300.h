@@ -239,8 +239,9 @@ moe_status moe_cache_export_staging(moe_cache* cache, int32_t* h_stage_key, uint
  * loads of the pinned bank over the host-device link, stream-ordered on
  * `stream` -- no host synchronisation between ensure and the forward.  The
  * bank must be mapped into the device address space (true for pinned memory
- * on systems with unified addressing); otherwise MOE_ERR_INVALID.  Entries
- * with an out-of-range key or slot are skipped.  max_ctas bounds the grid
+ * on systems with unified addressing) and 16-byte aligned, as must be the
+ * slot pool; otherwise MOE_ERR_INVALID.  Entries with an out-of-range key or
+ * slot are skipped.  max_ctas bounds the grid
  * (0: four CTAs of 256 threads per SM); a small grid leaves the SMs to
  * kernels that run concurrently, such as moe_expert_forward_overlap.
  * ------------------------------------------------------------------------- */
@@ -254,7 +255,7 @@ moe_status moe_copy_missing_device(moe_cache* cache, const int32_t* d_miss_key,
  * rate (measured: 25-100 GB/s for an expert's first copy against ~170 GB/s
  * for later ones), so a server primes the bank once at setup and every miss
  * copy then runs at the link rate.  The bank is not modified.
- * MOE_ERR_INVALID if the bank is not mapped. */
+ * MOE_ERR_INVALID if the bank is not mapped or not 16-byte aligned. */
 moe_status moe_cache_prime_bank(moe_cache* cache, cudaStream_t stream);
 
 /* The same copy for one part of the list: with n = *d_miss_count, part p of

@@ -501,6 +501,7 @@ moe_status moe_cache_prime_bank(moe_cache* c, cudaStream_t stream) {
   clear_error();
   MOE_ARG(c != nullptr, "cache is null");
   MOE_ARG(c->bank_dev != nullptr, "the host bank is not mapped into the device address space");
+  MOE_ARG(((uintptr_t)c->bank_dev & 15) == 0, "the host bank must be 16-byte aligned");
   const size_t bytes = (size_t)c->L * c->E * c->B;
   int dev = 0, sms = 1;
   MOE_CUDA(cudaGetDevice(&dev));
@@ -516,6 +517,8 @@ static moe_status copy_missing_launch(moe_cache* c, const int32_t* d_miss_key, c
   MOE_ARG(d_miss_key && d_miss_slot && d_miss_count, "null miss list");
   MOE_ARG(c->bank_dev != nullptr, "the host bank is not mapped into the device address space");
   MOE_ARG(c->B % 16 == 0, "expert bytes %zu not a multiple of 16", c->B);
+  MOE_ARG(((uintptr_t)c->bank_dev & 15) == 0 && ((uintptr_t)c->d_slots & 15) == 0,
+          "the host bank and the slot pool must be 16-byte aligned");
   MOE_ARG(n_parts >= 1 && n_parts <= MOE_MAX_COPY_PARTS && part >= 0 && part < n_parts,
           "part %d of %d: need 0 <= part < n_parts <= %d", part, n_parts, MOE_MAX_COPY_PARTS);
   MOE_ARG(b0 < b1 && b1 <= c->B && b0 % 16 == 0 && b1 % 16 == 0,
