@@ -1128,6 +1128,9 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
   a.o = (float*)(base + L.o);
 
   if (a.routed_gemm) {
+    // the gather reads x rows with 16-byte loads
+    MOE_ARG(((uintptr_t)x & 15) == 0, "x must be 16-byte aligned for the grouped-GEMM path (T * k >= %d)",
+            kGemmMinPairs);
     // FP4 routed pairs on the tensor cores; its 16-bit buffers (two activation
     // copies of P x H each, h of P x I) reuse the routed rows of the fp32 o and
     // h buffers, which the CUDA-core kernels do not touch in this mode, unless
