@@ -40,7 +40,8 @@ def _args():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--T", type=int, default=64, help="decode batch of the headline line")
     p.add_argument("--sweep", default="1,4,16,64", help="decode batches also measured (comma list, '' for none)")
-    p.add_argument("--cpu-sample-tokens", type=int, default=4)
+    p.add_argument("--cpu-sample-tokens", type=int, default=12,
+                   help="tokens of the decode workload the oracle is timed on (about 10 s of host time)")
     p.add_argument("--workload", default="decode", choices=["decode", "prefill", "ladder", "stack"])
     p.add_argument("--copy", default="device", choices=["engine", "device"],
                    help="miss copies: copy engine after one host sync, or a kernel reading the miss list")
