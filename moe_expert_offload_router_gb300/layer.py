@@ -45,7 +45,27 @@ from . import _lib as L
 
 
 class DecodeLayerRunner:
-    """Buffers and streams for running layers of one model shape on one cache."""
+    """Buffers and streams for running layers of one model shape on one cache.
+
+    ``run(layer_id, logits, x, y)`` performs one layer step: router, slot
+    ensure, miss copies, expert MLP and combine.
+
+    * ``copy``: "engine" (one host read of the miss list, then copy-engine
+      copies) or "device" (a kernel copies the misses straight from the miss
+      list on the device; no host wait when the batch is one chunk).
+    * ``overlap`` (device copies): True, False or "auto" (from
+      OVERLAP_MIN_PAIRS pairs): pairs of resident experts compute while the
+      misses are copied.  With ``copy_parts`` 1 the copies are staged: every
+      miss's gate/up matrices first, then its down matrices in ``down_parts``
+      parts of the miss list; ``copy_parts`` > 1 instead splits the miss list
+      into that many parts, each with its own pass.
+    * ``copy_ctas``: the copy kernel's grid (each CTA keeps an SM from the
+      grouped GEMM).
+    * ``graph``: replay single-chunk device-copy steps as CUDA graphs.
+    * ``assume_resident``: every key has its slot (a cache of L * E slots);
+      no copies, no host waits.
+    * ``int2_cache`` and ``ladder`` = (a, b): the precision ladder.
+    """
 
     # overlap="auto" overlaps copies and compute from this many pairs per call:
     # below it the second forward pass costs more than the short copies hide
