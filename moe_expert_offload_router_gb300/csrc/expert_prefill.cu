@@ -279,6 +279,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   // raw-code ring: FP8 rows take twice the bytes per K step, in half as many stages
   constexpr int kRT = FP8 ? 2 * kRawTile : kRawTile;
   constexpr int kRing = FP8 ? C::kRaw / 2 : C::kRaw;
+  // TMA fills may land out of order.  A group's own earlier waits imply that
+  // the previous fill of a raw slot (step ks - kRing) has landed when kRing is
+  // a multiple of the group count (the group converted it itself) or when
+  // kRing >= kStages + groups (its previous step waited for the MMA of step
+  // ks - 3 - kStages, which needed step ks - kRing converted); otherwise it
+  // first waits for that fill's conversion on rawe, so that rawf's parity
+  // cannot pass on the older phase.
+  constexpr bool kRawGuard = kRing % kPfConvGroups != 0 && kRing < C::kStages + kPfConvGroups;
   constexpr int kRowB = FP8 ? 64 : 32;  // code bytes per weight row per K step
 
   const int item_idx = blockIdx.x / a.tiles;
@@ -481,6 +489,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           if (nxt < sbytes) snext[mt] = __ldg(reinterpret_cast<const uint4*>(srow[mt] + nxt));
         }
       }
+      if (kRawGuard && rr > 0 && !(ok = mbar_wait_fast(&rawe[rs], (rr - 1) & 1, a.err))) break;
       if (!(ok = mbar_wait_fast(&rawf[rs], rr & 1, a.err))) break;
       if (FP8) {
         // 64 E4M3 codes per row: exact 16-bit values, no block scale
