@@ -523,47 +523,47 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
         }
       } else {
-      uint4 q[kPfMT][2];
+        uint4 q[kPfMT][2];
 #pragma unroll
-      for (int mt = 0; mt < kPfMT; ++mt) {
-        const uint8_t* src = sm + C::kOffRaw + rs * kRT + raw_off[mt];
-        q[mt][0] = *reinterpret_cast<const uint4*>(src);
-        q[mt][1] = *reinterpret_cast<const uint4*>(src + 16);
-      }
-      if (rnd > 0 && !(ok = mbar_wait_fast(&empty[s], (rnd - 1) & 1, a.err))) {
-        mbar_arrive(&rawe[rs]);
-        break;
-      }
+        for (int mt = 0; mt < kPfMT; ++mt) {
+          const uint8_t* src = sm + C::kOffRaw + rs * kRT + raw_off[mt];
+          q[mt][0] = *reinterpret_cast<const uint4*>(src);
+          q[mt][1] = *reinterpret_cast<const uint4*>(src + 16);
+        }
+        if (rnd > 0 && !(ok = mbar_wait_fast(&empty[s], (rnd - 1) & 1, a.err))) {
+          mbar_arrive(&rawe[rs]);
+          break;
+        }
 #pragma unroll
-      for (int mt = 0; mt < kPfMT; ++mt) {
-        uint8_t* arow = sm + C::kOffA + s * kAStage + mt * kATile + r * 128;
+        for (int mt = 0; mt < kPfMT; ++mt) {
+          uint8_t* arow = sm + C::kOffA + s * kAStage + mt * kATile + r * 128;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int sb = (ks & 7) * 2 + c;  // scale byte within the 16 loaded
-          const uint32_t sw = sb < 4 ? scur[mt].x : sb < 8 ? scur[mt].y : sb < 12 ? scur[mt].z : scur[mt].w;
-          const uint32_t e8 = (sw >> (8 * (sb & 3))) & 0xff;
-          const uint32_t sc2 = f16 ? e8m0_f16x2(e8) : e8m0_bf16x2(e8);
-          const uint32_t w4[4] = {q[mt][c].x, q[mt][c].y, q[mt][c].z, q[mt][c].w};
+          for (int c = 0; c < 2; ++c) {
+            const int sb = (ks & 7) * 2 + c;  // scale byte within the 16 loaded
+            const uint32_t sw = sb < 4 ? scur[mt].x : sb < 8 ? scur[mt].y : sb < 12 ? scur[mt].z : scur[mt].w;
+            const uint32_t e8 = (sw >> (8 * (sb & 3))) & 0xff;
+            const uint32_t sc2 = f16 ? e8m0_f16x2(e8) : e8m0_bf16x2(e8);
+            const uint32_t w4[4] = {q[mt][c].x, q[mt][c].y, q[mt][c].z, q[mt][c].w};
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            uint4 o;
-            fp4x8_to_f16(w4[u], o.x, o.y, o.z, o.w);
-            if (f16) {
-              o.x = hmul2_f16(o.x, sc2);
-              o.y = hmul2_f16(o.y, sc2);
-              o.z = hmul2_f16(o.z, sc2);
-              o.w = hmul2_f16(o.w, sc2);
-            } else {
-              o.x = f16x2_to_bf16x2_scaled(o.x, sc2);
-              o.y = f16x2_to_bf16x2_scaled(o.y, sc2);
-              o.z = f16x2_to_bf16x2_scaled(o.z, sc2);
-              o.w = f16x2_to_bf16x2_scaled(o.w, sc2);
+            for (int u = 0; u < 4; ++u) {
+              uint4 o;
+              fp4x8_to_f16(w4[u], o.x, o.y, o.z, o.w);
+              if (f16) {
+                o.x = hmul2_f16(o.x, sc2);
+                o.y = hmul2_f16(o.y, sc2);
+                o.z = hmul2_f16(o.z, sc2);
+                o.w = hmul2_f16(o.w, sc2);
+              } else {
+                o.x = f16x2_to_bf16x2_scaled(o.x, sc2);
+                o.y = f16x2_to_bf16x2_scaled(o.y, sc2);
+                o.z = f16x2_to_bf16x2_scaled(o.z, sc2);
+                o.w = f16x2_to_bf16x2_scaled(o.w, sc2);
+              }
+              const int unit = c * 4 + u;
+              *reinterpret_cast<uint4*>(arow + ((unit ^ (r & 7)) << 4)) = o;
             }
-            const int unit = c * 4 + u;
-            *reinterpret_cast<uint4*>(arow + ((unit ^ (r & 7)) << 4)) = o;
           }
         }
-      }
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(&full[s]);
