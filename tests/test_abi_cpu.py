@@ -1,4 +1,5 @@
-"""The C-ABI library builds, loads and exports every symbol its header declares (CPU only)."""
+"""The C-ABI library builds, loads and exports every symbol its header declares, and the binding
+agrees with every declared signature (CPU only)."""
 import ctypes
 import os
 import re
@@ -62,3 +63,57 @@ def test_oracle_not_imported_by_product_code():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 txt = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in txt and "from oracle" not in txt, f
+
+
+def _prototypes():
+    """(return type, name, [parameter types]) of every function the header declares."""
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    out = []
+    for ret, name, params in re.findall(r"([A-Za-z_][A-Za-z0-9_ \*]*?)\b(moe_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;",
+                                        src, flags=re.S):
+        ps = [" ".join(p.split()) for p in params.split(",")]
+        ps = [] if ps == ["void"] else [re.sub(r"\s*\b[A-Za-z_][A-Za-z0-9_]*$", "", p) if not p.endswith("*")
+                                        else p for p in ps]
+        out.append((" ".join(ret.split()), name, ps))
+    return out
+
+
+def _c_class(t):
+    """The ctypes class a C parameter or return type of the header must be bound as."""
+    t = t.replace("const ", "").strip()
+    if t.endswith("*") or t in ("cudaStream_t", "cudaEvent_t"):
+        return "pointer"
+    return {"int": ctypes.c_int, "int32_t": ctypes.c_int, "moe_status": ctypes.c_int,
+            "size_t": ctypes.c_size_t, "uint64_t": ctypes.c_uint64, "int64_t": ctypes.c_int64,
+            "float": ctypes.c_float, "double": ctypes.c_double}[t]
+
+
+def _is_pointer(ct):
+    return ct in (ctypes.c_void_p, ctypes.c_char_p) or (isinstance(ct, type) and issubclass(ct, ctypes._Pointer))
+
+
+def test_binding_signatures_match_header(lib):
+    # a parameter added, dropped or retyped on one side only is undefined
+    # behaviour at the call: every declared function's binding must agree in
+    # arity and in the class of every parameter and of the result
+    from moe_expert_offload_router_gb300 import _lib as L
+    protos = _prototypes()
+    assert len(protos) == len(_declared())
+    for ret, name, params in protos:
+        assert name in L._SIGS, name
+        res, args = L._SIGS[name]
+        assert len(args) == len(params), (name, params, args)
+        for p, a in zip(params, args):
+            want = _c_class(p)
+            if want == "pointer":
+                assert _is_pointer(a), (name, p, a)
+            else:
+                assert a is want or ctypes.sizeof(a) == ctypes.sizeof(want) and a._type_ == want._type_, \
+                    (name, p, a)
+        want = _c_class(ret)
+        if want == "pointer":
+            assert _is_pointer(res), (name, ret, res)
+        else:
+            assert res is want or ctypes.sizeof(res) == ctypes.sizeof(want), (name, ret, res)
