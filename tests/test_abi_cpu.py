@@ -117,3 +117,30 @@ def test_binding_signatures_match_header(lib):
             assert _is_pointer(res), (name, ret, res)
         else:
             assert res is want or ctypes.sizeof(res) == ctypes.sizeof(want), (name, ret, res)
+
+
+def test_views_struct_matches_header(lib):
+    # moe_expert_views crosses the boundary by pointer: field order, types and
+    # offsets of the ctypes mirror must be the header's
+    from moe_expert_offload_router_gb300 import _lib as L
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef\s+struct\s*\w*\s*\{([^}]*)\}\s*moe_expert_views\s*;", src, flags=re.S).group(1)
+    fields = []
+    for decl in body.split(";"):
+        decl = " ".join(decl.split())
+        if decl:   # "int H, I" declares two fields of the base type
+            first, *more = decl.split(",")
+            typ, name = re.match(r"(.*?)\s*\b([A-Za-z_][A-Za-z0-9_]*)$", first.strip()).groups()
+            fields.append((name, typ))
+            base = typ.rstrip("* ")
+            for d in more:
+                d = d.strip()
+                fields.append((d.lstrip("* "), base + "*" * d.count("*")))
+    mirror = L.moe_expert_views._fields_
+    assert [n for n, _ in fields] == [n for n, _ in mirror]
+    for (name, typ), (_, ct) in zip(fields, mirror):
+        want = _c_class(typ)
+        if want == "pointer":
+            assert _is_pointer(ct), (name, typ, ct)
+        else:
+            assert ct is want, (name, typ, ct)
