@@ -118,7 +118,11 @@ moe_status moe_cache_import(moe_cache* cache, const int32_t* h_slot_key,
 /* ---------------------------------------------------------------------------
  * ensure_experts: remap expert ids of tokens [token_begin, T) and ranks
  * [rank_lo, rank_hi) onto slots, in first-appearance order (token-major,
- * then rank).  Entries holding a negative id are skipped.
+ * then rank).  Entries holding a negative id are skipped.  ("Running
+ * DeepSeek-V4-Flash across four free GPUs", section "What the expert cache
+ * actually does": ids remapped in place onto cache slots before the expert
+ * GEMM; its section "Step 7: Errors you will actually hit" for a cache too
+ * small for one batch's experts, read here as the token-prefix chunking.)
  *   ids        device int32 [T, k] expert ids (< num_experts)
  *   slots_out  device int32 [T, k]; may alias ids (in-place remap, as the
  *              pages' ensure_experts).  Only the processed entries are written.
@@ -156,7 +160,11 @@ moe_status moe_slot_ensure(moe_cache* cache, int layer_id, const int32_t* ids, i
 /* ---------------------------------------------------------------------------
  * copy_missing: for each listed miss, copy expert_bytes from
  * h_bank + key * expert_bytes to d_slots + slot * expert_bytes with one
- * cudaMemcpyAsync on copy_stream, in list order.  ready (may be NULL) is
+ * cudaMemcpyAsync on copy_stream, in list order.  ("Running DeepSeek-V4-Flash
+ * across four free GPUs", section "What the expert cache actually does": only
+ * the misses cross from the pinned host bank; "An elephant through a straw",
+ * section "43 graphs, 43 syncs": one host synchronisation per layer reads the
+ * miss list.)  ready (may be NULL) is
  * waited on by copy_stream first; done (may be NULL) is recorded on
  * copy_stream after the last copy, for the compute stream to wait on.
  *   h_miss_key, h_miss_slot  host int32 [n_miss] (the lists read back after
@@ -351,6 +359,10 @@ moe_status moe_group_pairs(const int32_t* ids, int T, int k, int E, int32_t* off
  * Grouped expert MLP + combine.  For every kept pair (t, j):
  * h = SiLU(W1 x_t) * (W3 x_t), o = W2 h, and
  * y_t = sum_j w[t,j] * o[t,j] + shared(x_t), rounded to bf16.
+ * ("Running DeepSeek-V4-Flash across four free GPUs", sections "The model"
+ * and "What the expert cache actually does": MXFP4 routed experts run as a
+ * grouped GEMM over the cache slots; "An elephant through a straw", opening
+ * section: MXFP4 experts of 13,369,344 bytes and the 2-bit copy.)
  * ------------------------------------------------------------------------- */
 typedef struct {
   int H, I;                    /* hidden and intermediate sizes, multiples of 32 */
