@@ -535,7 +535,7 @@ moe_status moe_rms_carry(const uint16_t* y, int T, int H, float eps, uint16_t* x
  * up to `max` records (host arrays of length >= max): the kernel id and the
  * start and stop times in milliseconds relative to the start of the first
  * record, whatever stream each was launched on; *n receives the number of
- * records held (which may exceed max).  MOE_ERR_ARG on a null pointer or
+ * records held (which may exceed max).  MOE_ERR_INVALID on a null pointer or
  * max < 0.
  * ------------------------------------------------------------------------- */
 enum {
