@@ -144,3 +144,14 @@ def test_views_struct_matches_header(lib):
             assert _is_pointer(ct), (name, typ, ct)
         else:
             assert ct is want, (name, typ, ct)
+
+
+def test_header_comments_name_only_defined_constants():
+    # a status or constant named in the documentation must exist in the header
+    src = open(HEADER).read()
+    comments = " ".join(re.findall(r"/\*.*?\*/", src, flags=re.S))
+    code = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    used = set(re.findall(r"\bMOE_[A-Z0-9_]+\b", comments))
+    defined = set(re.findall(r"#define\s+(MOE_[A-Z0-9_]+)", code)) | \
+        set(re.findall(r"\b(MOE_[A-Z0-9_]+)\s*(?:=|,|\})", code))
+    assert used and not used - defined, sorted(used - defined)
