@@ -155,3 +155,28 @@ def test_header_comments_name_only_defined_constants():
     defined = set(re.findall(r"#define\s+(MOE_[A-Z0-9_]+)", code)) | \
         set(re.findall(r"\b(MOE_[A-Z0-9_]+)\s*(?:=|,|\})", code))
     assert used and not used - defined, sorted(used - defined)
+
+
+def _header_constants():
+    code = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    vals = {}
+    for body in re.findall(r"enum\s*\w*\s*\{([^}]*)\}", code, flags=re.S):
+        cur = -1
+        for item in (i.strip() for i in body.split(",")):
+            if item:
+                name, expr = re.match(r"(MOE_[A-Z0-9_]+)\s*(?:=\s*(.+))?$", item).groups()
+                cur = int(eval(expr, {}, dict(vals))) if expr else cur + 1
+                vals[name] = cur
+    for m in re.finditer(r"#define\s+(MOE_[A-Z0-9_]+)\s+\(?(-?\d+)\)?", code):
+        vals[m.group(1)] = int(m.group(2))
+    return vals
+
+
+def test_binding_constants_match_header(lib):
+    from moe_expert_offload_router_gb300 import _lib as L
+    vals = _header_constants()
+    assert len(vals) > 20
+    for name, v in vals.items():
+        assert hasattr(L, name), name
+        assert getattr(L, name) == v, (name, getattr(L, name), v)
+    assert L.KERNEL_NAMES and len(L.KERNEL_NAMES) == vals["MOE_K_COUNT"]
