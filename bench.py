@@ -231,6 +231,25 @@ def run_ours(args):
     runner = M.DecodeLayerRunner(cache, views, E, k, Tmax, dev, copy=args.copy, overlap=overlap)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)     # > 129 MB L2
     hbm_peak, peak_kind = _peaks()
+
+    def link_probe():
+        """Copy-engine bandwidth from the pinned bank to the device (one
+        cudaMemcpyAsync of 128 MB, median of 5 after one untimed), the
+        reference that host_link_gbs is reported against; None if it fails."""
+        try:
+            n = min(128 << 20, bank.numel(), flush.numel())
+            src, dst = bank[:n], flush[:n]
+            rates = []
+            for _ in range(6):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                dst.copy_(src, non_blocking=True)
+                b.record(stream)
+                b.synchronize()
+                rates.append(n / (a.elapsed_time(b) / 1e3) / 1e9)
+            return statistics.median(rates[1:])
+        except Exception:
+            return None
     stream = torch.cuda.current_stream(dev)
     n_steps = args.warmup + args.steps
 
@@ -304,8 +323,10 @@ def run_ours(args):
         copied = runner.stats["bytes_copied"] - bytes0
         # accounting: distinct experts per step
         acct_gu_bytes, acct_layer_bytes, acct_gemm_bytes = 0, 0, 0
+        distinct = 0
         for ids in ids_seen:
             d = int(torch.unique(ids).numel())
+            distinct += d
             acct_gemm_bytes += d * gu_expert + T * H * 2 + T * k * I * 2
             # the routed pairs take the grouped GEMM from 256 pairs per call on
             acct_gu_bytes += gu_shared + T * H * 2 + T * I * 4 + (0 if T * k >= 256 else
@@ -341,6 +362,8 @@ def run_ours(args):
             "gateup_gbs": (acct_gu_bytes / max(gu_n, 1)) / (gu_ms / max(gu_n, 1) / 1e3) / 1e9,
             "gateup_bytes_per_launch": acct_gu_bytes / max(gu_n, 1),
             "misses_per_step": misses / args.steps,
+            # distinct experts of a step found resident (capacity chunks that re-fetch count as misses)
+            "hit_rate": 1.0 - misses / max(distinct, 1),
             "host_link_gbs": (copied / args.steps / (kt["copy_device"][0] / args.steps / 1e3)
                               / 1e9 if kt["copy_device"][1] else None),
             "h2d_gb_per_step": copied / args.steps / 1e9,
@@ -461,6 +484,7 @@ def run_ours(args):
     head = results[args.T]
     compute_only = measure_compute_only(args.T)
     e2e = measure_e2e(args.T)
+    link_gbs = link_probe() if args.copy == "device" else None
     cpu = cpu_baseline(args.cpu_sample_tokens) if (rank == 0 and world == 1) else None
     cpu_all = (cpu_baseline(args.cpu_sample_tokens, threads=os.cpu_count() or 1)
                if (rank == 0 and world == 1) else None)
@@ -496,6 +520,10 @@ def run_ours(args):
             "misses_per_step": head["misses_per_step"],
             "h2d_gb_per_step": head["h2d_gb_per_step"],
             "host_link_gbs": head["host_link_gbs"],
+            "host_link_probe_gbs": link_gbs,
+            "host_link_frac_of_probe": (head["host_link_gbs"] / link_gbs
+                                        if head["host_link_gbs"] and link_gbs else None),
+            "hit_rate": head["hit_rate"],
             "kernel_ms_per_step": head["kernel_ms"],
             "sweep": {str(T): {kk: (round(v, 4) if isinstance(v, float) else v) for kk, v in r.items()
                                if kk not in ("kernel_ms",)} for T, r in results.items()},
