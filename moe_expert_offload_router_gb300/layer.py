@@ -164,6 +164,9 @@ class DecodeLayerRunner:
         ring: the assignment runs on `stream` after everything enqueued there,
         the copies on the side stream after the copies already queued on it."""
         stream = stream or torch.cuda.current_stream(self.dev)
+        # the previous prefetch's copy kernel (side stream) still reads the key /
+        # slot lists and its ring slots: the assignment that rewrites them waits
+        self._wait_prefetch(stream)
         L.moe_prefetch(self.cache, layer_id, d_experts, self.pf_key, self.pf_slot, self.pf_cnt, stream)
         self.pf_ready.record(stream)
         self.copy_stream.wait_event(self.pf_ready)

@@ -105,8 +105,12 @@ def test_promotion_copies_from_the_staging_slot():
     assert srcs == [("bank", 6), ("bank", 7)]
 
 
-@pytest.mark.parametrize("T,overlap", [(4, False), (64, True)])
-def test_layer_outputs_identical_with_prefetch(T, overlap):
+@pytest.mark.parametrize("T,overlap,sync", [(4, False, True), (64, True, True), (64, True, False),
+                                             (4, False, False)])
+def test_layer_outputs_identical_with_prefetch(T, overlap, sync):
+    # sync=False enqueues every step back to back: a step's prefetch copy is
+    # still running on the side stream when the next step assigns new ring
+    # slots, so the assignment must wait for it
     M = load_lib()
     wl = configs.scaled(configs.DECODE, T=T)
     S, R = 48, 12
@@ -125,12 +129,17 @@ def test_layer_outputs_identical_with_prefetch(T, overlap):
             lg = gen.router_logits(wl, 0, step, T)
             x = gen.activations(wl, 0, step, T)
             nxt = router_topk(gen.router_logits(wl, 0, step + 1, T), wl.k)[0]
-            guess = np.unique(nxt)[::2]                   # half of the next step's experts
+            # half of the next step's experts; unsynchronised steps stage a full
+            # ring of guesses so that the copy is long
+            guess = np.unique(nxt)[::2] if sync else np.unique(np.concatenate([nxt.ravel(), np.arange(R) * 7]))
             pf = (0, torch.from_numpy(guess.astype(np.int32)).cuda()) if use_pf else None
             y = torch.empty((T, wl.H), dtype=torch.int16, device="cuda")
             runner.run(0, torch.from_numpy(lg).cuda(), torch.from_numpy(x.view(np.int16)).cuda(), y, prefetch=pf)
-            torch.cuda.synchronize()
-            ys.append(y.cpu().numpy())
+            if sync:
+                torch.cuda.synchronize()
+            ys.append(y)
+        torch.cuda.synchronize()
+        ys = [y.cpu().numpy() for y in ys]
         runner.check()
         outs.append((ys, cache.export()[0], runner.stats["misses"]))
         cache.close()
