@@ -6,15 +6,21 @@ import numpy as np
 import pytest
 import torch
 
+from oracle import formats as F
+from oracle.mlp import moe_layer
 from oracle.router import router_topk
 from synth import configs, gen
-from tests.helpers import load_lib
+from tests.helpers import bf16_rel_err, load_lib
 from tests.test_gpu_forward import Pools, _route
 
 pytestmark = pytest.mark.gpu
 
 
-def test_prefill_full_size_repeatable():
+def test_prefill_full_size_repeatable_and_oracle_rows():
+    # the full prefill workload (T = 8192, top-6, all 256 experts resident):
+    # four identical calls give identical bits, and sampled rows match the
+    # oracle -- the first and last tokens and a token of the largest and of
+    # the smallest expert group (items of 256 rows at K = H and K = I)
     M = load_lib()
     wl = configs.PREFILL
     H, I, E = wl.H, wl.I, wl.E
@@ -38,6 +44,15 @@ def test_prefill_full_size_repeatable():
         outs.append(y)
     for y in outs[1:]:
         assert torch.equal(y, outs[0])
+    counts = np.bincount(ids.ravel(), minlength=E)
+    big, small = int(np.argmax(counts)), int(np.argmin(np.where(counts > 0, counts, 1 << 30)))
+    sample = sorted({0, wl.T - 1, int(np.nonzero((ids == big).any(1))[0][0]),
+                     int(np.nonzero((ids == small).any(1))[0][-1])})
+    xb = gen.activations(wl, 0, 0)
+    ref = moe_layer(xb, ids, w.astype(np.float32).astype(np.float64),
+                    lambda e, tag: F.decode_fp4_expert(gen.fp4_expert(wl, 0, e), H, I), tokens=sample)
+    got = outs[0].cpu().numpy()[sample]
+    assert bf16_rel_err(got, ref) <= 2e-2
 
 
 @pytest.mark.parametrize("T", [1, 2, 16, 64])

@@ -195,3 +195,63 @@ def test_layer_ladder_device_copy():
         assert np.array_equal(c2.export()[0], r2.state()[0])
     runner.check()
     assert runner.stats["misses"] > 0 and runner.stats["chunks"] == runner.stats["calls"]
+
+
+def test_stack_full_size_sample_4_layers_x_4_steps():
+    # the 43-layer stack workload at full size (H=4096, I=2048, E=256, top-8
+    # plus the FP8 shared expert, T=16, 70% step-to-step reuse): a seeded
+    # sample of 4 of its layers and 4 of its 64 steps, every expert of the
+    # sampled layers resident; each step carries x from layer to layer on the
+    # GPU (moe_rms_carry) and each layer is checked against the oracle from
+    # the GPU's own bf16 input to that layer, on two sampled tokens
+    M = load_lib()
+    wl = configs.STACK
+    H, I, E, k, T = wl.H, wl.I, wl.E, wl.k, wl.T
+    rng = np.random.default_rng(wl.seed)
+    layers = sorted(int(v) for v in rng.choice(wl.layers, size=4, replace=False))
+    steps = sorted(int(v) for v in rng.choice(wl.steps, size=4, replace=False))
+    B = M.moe_fp4_expert_bytes(H, I)
+    S = len(layers) * E
+    pool = torch.empty(S * B, dtype=torch.uint8, device="cuda")
+    for li, layer in enumerate(layers):
+        for e in range(E):
+            key = li * E + e
+            pool[key * B:(key + 1) * B] = gen.fp4_expert(wl, layer, e, device="cuda")
+    cache = M.moe_cache(S, len(layers), E, B, pool, None)
+    cache.import_(np.arange(S, dtype=np.int32), np.arange(S, dtype=np.uint64), S)
+    shared_np = [gen.shared_expert(wl, layer) for layer in layers]
+    shared = [torch.from_numpy(b).cuda() for b in shared_np]
+    runners = [M.DecodeLayerRunner(cache, M.make_views(H, I, pool, S, None, 0, shared[li]), E, k, T,
+                                   assume_resident=True) for li in range(len(layers))]
+    record = {}      # (layer index, step) -> (x bits, logits, y bits)
+    for step in steps:
+        x = torch.from_numpy(gen.activations(wl, 0, step).view(np.int16)).cuda()
+        for li, layer in enumerate(layers):
+            lg = gen.router_logits(wl, layer, step)
+            y = torch.empty((T, H), dtype=torch.int16, device="cuda")
+            runners[li].run(li, torch.from_numpy(lg).cuda(), x, y)
+            record[(li, step)] = (x.cpu().numpy().view(np.uint16), lg, y)
+            nxt = torch.empty_like(y)
+            M.moe_rms_carry(y, 1e-6, nxt)
+            x = nxt
+    torch.cuda.synchronize()
+    for r in runners:
+        r.check()
+    assert all(r.stats["misses"] == 0 for r in runners)
+    for li, layer in enumerate(layers):
+        memo = {}      # decoded experts kept in float32 (exact for these scales) across the steps
+
+        def dec(e, tag, layer=layer, memo=memo):
+            if e not in memo:
+                memo[e] = {m: v.astype(np.float32) for m, v in
+                           F.decode_fp4_expert(gen.fp4_expert(wl, layer, e), H, I).items()}
+            return {m: v.astype(np.float64) for m, v in memo[e].items()}
+        shw = F.decode_fp8_expert(shared_np[li], H, I)
+        for step in steps:
+            xb, lg, y = record[(li, step)]
+            ids, w = router_topk(lg, k)
+            # the same two tokens at every step: their experts recur (70% reuse)
+            tokens = sorted(int(v) for v in np.random.default_rng(1000 + layer).choice(T, 2, replace=False))
+            ref = moe_layer(xb, ids, w, dec, shared=shw, tokens=tokens)
+            assert bf16_rel_err(y.cpu().numpy()[tokens], ref) <= TOL, (layer, step)
+    cache.close()
