@@ -47,7 +47,9 @@ typedef enum {
   MOE_ERR_INVALID = 1,   /* bad argument (null pointer, size, range, alignment) */
   MOE_ERR_CAPACITY = 2,  /* a single token needs more experts than the pool has slots */
   MOE_ERR_CUDA = 3,      /* a CUDA runtime call failed (message has the CUDA error) */
-  MOE_ERR_TIMEOUT = 4,   /* reserved: no call in this library waits on the device */
+  MOE_ERR_TIMEOUT = 4,   /* a kernel's bounded wait gave up (grouped-GEMM mbarrier waits stop
+                            after 1 s); reported through the call's d_error, the call itself
+                            having returned MOE_OK when it was enqueued */
   MOE_ERR_NOMEM = 5      /* library-owned allocation failed */
 } moe_status;
 
@@ -248,14 +250,16 @@ moe_status moe_cache_export_staging(moe_cache* cache, int32_t* h_stage_key, uint
  * `stream` -- no host synchronisation between ensure and the forward.  The
  * bank must be mapped into the device address space (true for pinned memory
  * on systems with unified addressing) and 16-byte aligned, as must be the
- * slot pool; otherwise MOE_ERR_INVALID.  Entries with an out-of-range key or
- * slot are skipped.  max_ctas bounds the grid
+ * slot pool; otherwise MOE_ERR_INVALID.  An entry with an out-of-range key or
+ * slot is not copied and, when d_error (device int32, may be null) is given,
+ * sets *d_error to MOE_ERR_INVALID if it holds 0 (the caller clears it; the
+ * slot that entry named keeps stale bytes).  max_ctas bounds the grid
  * (0: four CTAs of 256 threads per SM); a small grid leaves the SMs to
  * kernels that run concurrently, such as moe_expert_forward_overlap.
  * ------------------------------------------------------------------------- */
 moe_status moe_copy_missing_device(moe_cache* cache, const int32_t* d_miss_key,
                                    const int32_t* d_miss_slot, const int32_t* d_miss_count,
-                                   int max_ctas, cudaStream_t stream);
+                                   int max_ctas, int32_t* d_error, cudaStream_t stream);
 
 /* Reads one 16-byte word of every 4 KB page of the cache's mapped host bank
  * (all num_layers * num_experts experts), stream-ordered on `stream`.  The
@@ -276,7 +280,8 @@ moe_status moe_cache_prime_bank(moe_cache* cache, cudaStream_t stream);
 #define MOE_MAX_COPY_PARTS 4
 moe_status moe_copy_missing_device_part(moe_cache* cache, const int32_t* d_miss_key,
                                         const int32_t* d_miss_slot, const int32_t* d_miss_count,
-                                        int part, int n_parts, int max_ctas, cudaStream_t stream);
+                                        int part, int n_parts, int max_ctas, int32_t* d_error,
+                                        cudaStream_t stream);
 
 /* The same copy restricted to the bytes [byte_begin, byte_end) of every listed
  * expert (both multiples of 16, byte_end <= the expert size, else
@@ -287,13 +292,13 @@ moe_status moe_copy_missing_device_part(moe_cache* cache, const int32_t* d_miss_
 moe_status moe_copy_missing_device_range(moe_cache* cache, const int32_t* d_miss_key,
                                          const int32_t* d_miss_slot, const int32_t* d_miss_count,
                                          size_t byte_begin, size_t byte_end, int max_ctas,
-                                         cudaStream_t stream);
+                                         int32_t* d_error, cudaStream_t stream);
 /* Both at once: part `part` of n_parts of the list (as moe_copy_missing_device_
  * part divides it), bytes [byte_begin, byte_end) of each of its experts. */
 moe_status moe_copy_missing_device_slice(moe_cache* cache, const int32_t* d_miss_key,
                                          const int32_t* d_miss_slot, const int32_t* d_miss_count, int part,
                                          int n_parts, size_t byte_begin, size_t byte_end, int max_ctas,
-                                         cudaStream_t stream);
+                                         int32_t* d_error, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Whole-layer streaming for prefill past the crossover.  "Running DeepSeek-
@@ -386,8 +391,13 @@ size_t moe_expert_forward_workspace(const moe_expert_views* v, int T, int k);
  *   d_error  device int32 [1] out: 0, or MOE_ERR_INVALID if a slot >= the
  *            pool's slot count (the pair is then skipped)
  * Numerics: weights are decoded exactly; activations are held in fp16 with a
- * per-token power-of-two scale; 32-weight partial sums accumulate in fp16 and
- * are scaled and summed in fp32; the combine runs in fp32 in rank order.
+ * per-token power-of-two scale.  On the warp-level tensor-core path (see
+ * moe_set_option) products accumulate in fp32 (bf16 operands for a 128-weight
+ * chunk whose E8M0 scales leave [2^-12, 2^13]); on the CUDA-core path
+ * 32-weight partial sums accumulate in fp16 and are scaled and summed in fp32;
+ * from 256 pairs above that path's token limit the tcgen05 grouped GEMM runs
+ * (fp16 or bf16 operands, fp32 accumulate, h in bf16).  The combine runs in
+ * fp32 in rank order.
  * Above 4096 pairs per call the grouped-GEMM path of moe_expert_prefill is
  * taken (FP4 pool only, tags must be NULL). */
 moe_status moe_expert_forward(const moe_expert_views* v, const uint16_t* x, int T, int k,
@@ -510,11 +520,26 @@ moe_status moe_mx_quantize(const uint16_t* x, int rows, int K, uint8_t* codes, u
  * call before any stream capture.  The call allocates nothing.  All calls
  * share the one scratch, which keeps the last call's contents (nothing in it
  * needs to start at zero): calls that overlap on the GPU race, so issue them
- * on one stream or order them.
+ * on one stream or order them.  The looked-up address is kept for the life of
+ * the process: after cudaDeviceReset (or any teardown of the device's primary
+ * context) it no longer names the scratch, so do not call this entry point on
+ * that device again in the same process.
  * ------------------------------------------------------------------------- */
 moe_status moe_expert_forward_noalloc(const moe_expert_views* v, const uint16_t* x, int T, int k,
                                       const int32_t* slots, const int8_t* tags, const float* w,
                                       uint16_t* y, int32_t* d_error, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Process-wide tuning option (not on the pages).  MOE_OPT_MMA_MAX_TOKENS:
+ * decode calls of 2 up to this many tokens run their FP4 and shared-expert
+ * pairs on the warp-level tensor-core kernels (default 32; 0 = never); larger
+ * ones take the tcgen05 grouped GEMM from 256 pairs, and the CUDA-core GEMV
+ * below that (and at one token).  The previous value goes to *old_value (may be null).
+ * MOE_ERR_INVALID for an unknown option or a negative value.  Set it between
+ * calls, not while another thread issues forward calls.
+ * ------------------------------------------------------------------------- */
+enum { MOE_OPT_MMA_MAX_TOKENS = 0 };
+moe_status moe_set_option(int option, int value, int* old_value);
 
 /* Decode one matrix of one slot to fp32 [N, K] (test hook; values are exact). */
 moe_status moe_dequant_debug(const moe_expert_views* v, int pool, int slot, int matrix,

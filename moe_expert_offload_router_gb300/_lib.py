@@ -62,11 +62,11 @@ _SIGS = {
     "moe_copy_missing": (i32, [vp, vp, vp, i32, vp, vp, vp]),
     "moe_debug_fail_copy": (i32, [vp, i32]),
     "moe_copy_layer": (i32, [vp, i32, i32, sz, vp, vp]),
-    "moe_copy_missing_device": (i32, [vp, vp, vp, vp, i32, vp]),
-    "moe_copy_missing_device_part": (i32, [vp, vp, vp, vp, i32, i32, i32, vp]),
+    "moe_copy_missing_device": (i32, [vp, vp, vp, vp, i32, vp, vp]),
+    "moe_copy_missing_device_part": (i32, [vp, vp, vp, vp, i32, i32, i32, vp, vp]),
     "moe_cache_prime_bank": (i32, [vp, vp]),
-    "moe_copy_missing_device_range": (i32, [vp, vp, vp, vp, sz, sz, i32, vp]),
-    "moe_copy_missing_device_slice": (i32, [vp, vp, vp, vp, i32, i32, sz, sz, i32, vp]),
+    "moe_copy_missing_device_range": (i32, [vp, vp, vp, vp, sz, sz, i32, vp, vp]),
+    "moe_copy_missing_device_slice": (i32, [vp, vp, vp, vp, i32, i32, sz, sz, i32, vp, vp]),
     "moe_cache_set_policy": (i32, [vp, i32, i32]),
     "moe_cache_seed_frequency": (i32, [vp, vp]),
     "moe_cache_export_frequency": (i32, [vp, vp, vp, vp]),
@@ -80,6 +80,7 @@ _SIGS = {
     "moe_expert_forward": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, vp,
                                  sz, vp, vp]),
     "moe_dequant_debug": (i32, [C.POINTER(moe_expert_views), i32, i32, i32, vp, vp]),
+    "moe_set_option": (i32, [i32, i32, vp]),
     "moe_expert_forward_overlap_workspace": (sz, [C.POINTER(moe_expert_views), i32, i32]),
     "moe_expert_forward_overlap": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, i32, vp,
                                          vp, vp, sz, vp, vp]),
@@ -287,24 +288,26 @@ def moe_copy_missing(cache: moe_cache, h_miss_key, h_miss_slot, n_miss: int, cop
 
 
 def moe_copy_missing_device(cache: moe_cache, d_miss_key, d_miss_slot, d_miss_count, stream=None,
-                            max_ctas: int = 0):
+                            max_ctas: int = 0, d_error=None):
     _check(_lib.moe_copy_missing_device(cache.handle, _p(d_miss_key), _p(d_miss_slot), _p(d_miss_count),
-                                        max_ctas, _s(stream)))
+                                        max_ctas, _p(d_error), _s(stream)))
 
 
 MOE_MAX_COPY_PARTS = 4
 
 
 def moe_copy_missing_device_range(cache: moe_cache, d_miss_key, d_miss_slot, d_miss_count, byte_begin: int,
-                                  byte_end: int, stream=None, max_ctas: int = 0):
+                                  byte_end: int, stream=None, max_ctas: int = 0, d_error=None):
     _check(_lib.moe_copy_missing_device_range(cache.handle, _p(d_miss_key), _p(d_miss_slot), _p(d_miss_count),
-                                              byte_begin, byte_end, max_ctas, _s(stream)))
+                                              byte_begin, byte_end, max_ctas, _p(d_error), _s(stream)))
 
 
 def moe_copy_missing_device_slice(cache: moe_cache, d_miss_key, d_miss_slot, d_miss_count, part: int, n_parts: int,
-                                  byte_begin: int, byte_end: int, stream=None, max_ctas: int = 0):
+                                  byte_begin: int, byte_end: int, stream=None, max_ctas: int = 0,
+                                  d_error=None):
     _check(_lib.moe_copy_missing_device_slice(cache.handle, _p(d_miss_key), _p(d_miss_slot), _p(d_miss_count),
-                                              part, n_parts, byte_begin, byte_end, max_ctas, _s(stream)))
+                                              part, n_parts, byte_begin, byte_end, max_ctas, _p(d_error),
+                                              _s(stream)))
 
 
 def moe_cache_prime_bank(cache: moe_cache, stream=None):
@@ -314,9 +317,9 @@ def moe_cache_prime_bank(cache: moe_cache, stream=None):
 
 
 def moe_copy_missing_device_part(cache: moe_cache, d_miss_key, d_miss_slot, d_miss_count, part: int,
-                                 n_parts: int, stream=None, max_ctas: int = 0):
+                                 n_parts: int, stream=None, max_ctas: int = 0, d_error=None):
     _check(_lib.moe_copy_missing_device_part(cache.handle, _p(d_miss_key), _p(d_miss_slot), _p(d_miss_count),
-                                             part, n_parts, max_ctas, _s(stream)))
+                                             part, n_parts, max_ctas, _p(d_error), _s(stream)))
 
 
 def moe_copy_layer(h_bank, layer_id: int, num_experts: int, expert_bytes: int, d_buf, stream=None):
@@ -440,6 +443,16 @@ def moe_mx_quantize(x, codes, scales, stream=None):
     """x device bf16 bits [rows, K] -> codes uint8 [rows, K/2], scales uint8 [rows, K/32]."""
     rows, K = x.shape
     _check(_lib.moe_mx_quantize(_p(x), rows, K, _p(codes), _p(scales), _s(stream)))
+
+
+MOE_OPT_MMA_MAX_TOKENS = 0
+
+
+def moe_set_option(option: int, value: int) -> int:
+    """Sets a process-wide tuning option; returns its previous value."""
+    old = C.c_int(0)
+    _check(_lib.moe_set_option(option, value, C.byref(old)))
+    return old.value
 
 
 def moe_dequant_debug(views: moe_expert_views, pool: int, slot: int, matrix: int, out, stream=None):

@@ -167,7 +167,7 @@ __global__ void cache_mark_empty_kernel(CacheDev c, int slot) {
 template <typename Idx>
 __device__ __forceinline__ void copy_units(const CacheDev& c, const uint8_t* bank, uint8_t* slots, size_t B,
                                            size_t b0, Idx per, const int32_t* miss_key, const int32_t* miss_slot,
-                                           Idx total) {
+                                           Idx total, int32_t* err) {
   const Idx stride = (Idx)gridDim.x * blockDim.x;
   const int K = c.L * c.E;
   for (Idx u0 = (Idx)blockIdx.x * blockDim.x + threadIdx.x; u0 < total; u0 += 4 * stride) {
@@ -187,6 +187,10 @@ __device__ __forceinline__ void copy_units(const CacheDev& c, const uint8_t* ban
           const uint8_t* src = st >= 0 ? slots + (size_t)(c.S + st) * B : bank + (size_t)key * B;
           v[j] = __ldcs(reinterpret_cast<const uint4*>(src + off));
           dst[j] = (size_t)sl * B + off;
+        } else if (err && u - (Idx)m * per == 0) {
+          // an entry that names no key or no slot is not copied; the slot it
+          // was meant for holds stale bytes, so the call's status says so
+          atomicCAS(err, 0, MOE_ERR_INVALID);
         }
       }
     }
@@ -205,7 +209,7 @@ __device__ __forceinline__ void copy_units(const CacheDev& c, const uint8_t* ban
 __global__ void __launch_bounds__(256) copy_missing_kernel(CacheDev c, const uint8_t* bank, uint8_t* slots,
                                                            size_t B, const int32_t* miss_key,
                                                            const int32_t* miss_slot, const int32_t* miss_count,
-                                                           int part, int parts, size_t b0, size_t b1) {
+                                                           int part, int parts, size_t b0, size_t b1, int32_t* err) {
   const int n = *miss_count;
   if (n <= 0) return;
   const int m0 = (int)((long long)n * part / parts), m1 = (int)((long long)n * (part + 1) / parts);
@@ -213,9 +217,10 @@ __global__ void __launch_bounds__(256) copy_missing_kernel(CacheDev c, const uin
   const size_t per = (b1 - b0) / 16;
   const size_t total = (size_t)(m1 - m0) * per;
   if (total < 0xFFFFFFFFull)
-    copy_units<uint32_t>(c, bank, slots, B, b0, (uint32_t)per, miss_key + m0, miss_slot + m0, (uint32_t)total);
+    copy_units<uint32_t>(c, bank, slots, B, b0, (uint32_t)per, miss_key + m0, miss_slot + m0, (uint32_t)total,
+                         err);
   else
-    copy_units<size_t>(c, bank, slots, B, b0, per, miss_key + m0, miss_slot + m0, total);
+    copy_units<size_t>(c, bank, slots, B, b0, per, miss_key + m0, miss_slot + m0, total, err);
 }
 
 // One 16-byte load per `stride` bytes of the mapped bank (a page of it), so
@@ -512,7 +517,7 @@ moe_status moe_cache_prime_bank(moe_cache* c, cudaStream_t stream) {
 
 static moe_status copy_missing_launch(moe_cache* c, const int32_t* d_miss_key, const int32_t* d_miss_slot,
                                       const int32_t* d_miss_count, int part, int n_parts, size_t b0, size_t b1,
-                                      int max_ctas, cudaStream_t stream) {
+                                      int max_ctas, int32_t* d_error, cudaStream_t stream) {
   MOE_ARG(c != nullptr, "cache is null");
   MOE_ARG(d_miss_key && d_miss_slot && d_miss_count, "null miss list");
   MOE_ARG(c->bank_dev != nullptr, "the host bank is not mapped into the device address space");
@@ -530,39 +535,41 @@ static moe_status copy_missing_launch(moe_cache* c, const int32_t* d_miss_key, c
   ProfScope ps(MOE_K_COPY, stream);
   const int grid = max_ctas > 0 && max_ctas < sms * 4 ? max_ctas : sms * 4;
   copy_missing_kernel<<<grid, 256, 0, stream>>>(c->dev, c->bank_dev, c->d_slots, c->B, d_miss_key, d_miss_slot,
-                                                  d_miss_count, part, n_parts, b0, b1);
+                                                  d_miss_count, part, n_parts, b0, b1, d_error);
   return check_launch("copy_missing_kernel");
 }
 
 moe_status moe_copy_missing_device_part(moe_cache* c, const int32_t* d_miss_key, const int32_t* d_miss_slot,
                                         const int32_t* d_miss_count, int part, int n_parts, int max_ctas,
-                                        cudaStream_t stream) {
+                                        int32_t* d_error, cudaStream_t stream) {
   clear_error();
   MOE_ARG(c != nullptr, "cache is null");
-  return copy_missing_launch(c, d_miss_key, d_miss_slot, d_miss_count, part, n_parts, 0, c->B, max_ctas, stream);
+  return copy_missing_launch(c, d_miss_key, d_miss_slot, d_miss_count, part, n_parts, 0, c->B, max_ctas, d_error,
+                             stream);
 }
 
 moe_status moe_copy_missing_device_slice(moe_cache* c, const int32_t* d_miss_key, const int32_t* d_miss_slot,
                                          const int32_t* d_miss_count, int part, int n_parts, size_t byte_begin,
-                                         size_t byte_end, int max_ctas, cudaStream_t stream) {
+                                         size_t byte_end, int max_ctas, int32_t* d_error, cudaStream_t stream) {
   clear_error();
   return copy_missing_launch(c, d_miss_key, d_miss_slot, d_miss_count, part, n_parts, byte_begin, byte_end,
-                             max_ctas, stream);
+                             max_ctas, d_error, stream);
 }
 
 moe_status moe_copy_missing_device_range(moe_cache* c, const int32_t* d_miss_key, const int32_t* d_miss_slot,
                                          const int32_t* d_miss_count, size_t byte_begin, size_t byte_end,
-                                         int max_ctas, cudaStream_t stream) {
+                                         int max_ctas, int32_t* d_error, cudaStream_t stream) {
   clear_error();
   return copy_missing_launch(c, d_miss_key, d_miss_slot, d_miss_count, 0, 1, byte_begin, byte_end, max_ctas,
-                             stream);
+                             d_error, stream);
 }
 
 moe_status moe_copy_missing_device(moe_cache* c, const int32_t* d_miss_key, const int32_t* d_miss_slot,
-                                   const int32_t* d_miss_count, int max_ctas, cudaStream_t stream) {
+                                   const int32_t* d_miss_count, int max_ctas, int32_t* d_error,
+                                   cudaStream_t stream) {
   clear_error();
   MOE_ARG(c != nullptr, "cache is null");
-  return copy_missing_launch(c, d_miss_key, d_miss_slot, d_miss_count, 0, 1, 0, c->B, max_ctas, stream);
+  return copy_missing_launch(c, d_miss_key, d_miss_slot, d_miss_count, 0, 1, 0, c->B, max_ctas, d_error, stream);
 }
 
 moe_status moe_copy_layer(const void* h_bank, int layer_id, int num_experts, size_t expert_bytes, void* d_buf,

@@ -94,6 +94,7 @@ struct FwdArgs {
   uint16_t* y;
   int32_t* err;
   int routed_gemm;  // routed pairs are computed by the grouped GEMM, not by these kernels
+  int gemv_skip;    // bit per pool: groups of these pools are left to the warp-MMA kernels
   // workspace
   int* hdr;
   int* perm;
@@ -742,6 +743,7 @@ __global__ void __launch_bounds__(kFwdThreads, 2) gateup_kernel(FwdArgs a) {
     const int gi = (int)(item / tiles);
     const int tile = (int)(item % tiles);
     const Group g = a.groups[gi];
+    if (g.pool >= 0 && g.pool < 31 && ((a.gemv_skip >> g.pool) & 1)) continue;
     if (!group_ok(a, g)) {
       if (threadIdx.x == 0 && a.err) *a.err = MOE_ERR_INVALID;
       continue;
@@ -859,6 +861,7 @@ __global__ void __launch_bounds__(kFwdThreads, 2) down_kernel(FwdArgs a) {
     const int gi = (int)(item / tiles);
     const int tile = (int)(item % tiles);
     const Group g = a.groups[gi];
+    if (g.pool >= 0 && g.pool < 31 && ((a.gemv_skip >> g.pool) & 1)) continue;
     if (!group_ok(a, g)) {
       if (threadIdx.x == 0 && a.err) *a.err = MOE_ERR_INVALID;
       continue;
@@ -899,6 +902,12 @@ __global__ void __launch_bounds__(kFwdThreads, 2) down_kernel(FwdArgs a) {
     }
   }
 }
+
+}  // namespace moe
+
+#include "decode_mma.cuh"
+
+namespace moe {
 
 // ------------------------------------------------------------ combine kernel --
 
@@ -1057,6 +1066,28 @@ static int persistent_grid(K kernel, size_t smem, long long max_items) {
   return (int)(g < 1 ? 1 : g);
 }
 
+template <typename K>
+static int mma_grid(K kernel, size_t smem, long long max_items) {
+  int per_sm = 1;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kMmaThreads, smem);
+  if (per_sm < 1) per_sm = 1;
+  long long g = (long long)sm_count() * per_sm;
+  if (max_items < g) g = max_items;
+  return (int)(g < 1 ? 1 : g);
+}
+
+// Shapes the warp-MMA kernels take: K of every matrix a multiple of 256 (FP4
+// steps of two 128-element chunks), whole gate/up and down tiles.
+static bool mma_supported(const moe_expert_views* v) {
+  return v->H % 512 == 0 && v->I % 512 == 0 && v->I % kMmaFeat == 0 && v->H % kMmaRowsDown == 0;
+}
+
+// Decode batches of at most this many tokens take the warp-MMA kernels for their
+// FP4 and shared-expert groups (0: never); larger ones from kGemmMinPairs pairs
+// take the tcgen05 grouped GEMM (moe_set_option).
+static int g_mma_max_tokens = 32;
+constexpr int kMmaMinTokens = 2;
+
 static moe_status validate_views(const moe_expert_views* v) {
   MOE_ARG(v != nullptr, "views is null");
   MOE_ARG(v->H > 0 && v->I > 0 && v->H % 32 == 0 && v->I % 32 == 0, "H and I must be positive multiples of 32");
@@ -1118,7 +1149,12 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
   a.w = w;
   a.y = y;
   a.err = d_error;
-  a.routed_gemm = L.gemm && tags == nullptr && d_error != nullptr;
+  a.routed_gemm = L.gemm && tags == nullptr && d_error != nullptr && T > g_mma_max_tokens;
+  // the warp-MMA kernels take the FP4 and shared-expert groups of decode batches
+  // from two tokens on (a single token gives too few work items to fill the GPU;
+  // the CUDA-core kernels keep more bytes in flight there)
+  const bool mma = !a.routed_gemm && T >= kMmaMinTokens && T <= g_mma_max_tokens && mma_supported(v);
+  a.gemv_skip = mma ? kMmaPoolMask : 0;
   a.hdr = (int*)(base + L.hdr);
   a.perm = (int*)(base + L.perm);
   a.groups = (Group*)(base + L.groups);
@@ -1173,9 +1209,19 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
   }
 
   const long long max_groups = (long long)T * k + (T + kG - 1) / kG + 1;
+  if (mma) {
+    const size_t smem = (size_t)kG * mma_rs_fp4(v->H) + 2 * kG * 4;
+    if ((st = set_smem(mma_gateup_kernel, smem)) != MOE_OK) return st;
+    ProfScope ps(MOE_K_GATEUP, stream);
+    mma_gateup_kernel<<<mma_grid(mma_gateup_kernel, smem, max_groups * (v->I / kMmaFeat)), kMmaThreads, smem,
+                        stream>>>(a);
+  }
+  if ((st = check_launch("mma_gateup_kernel")) != MOE_OK) return st;
+  // the CUDA-core kernels: every group, or only the 2-bit ones beside the MMA kernels
+  const bool gemv_run = gemv && (!mma || tags != nullptr);
   const size_t gu_smem = (size_t)kG * v->H * 2 + 2 * kG * 4;
   const long long gu_items = max_groups * ((v->I + kRowsGateUp - 1) / kRowsGateUp);
-  if (!gemv) {
+  if (!gemv_run) {
   } else if (v->H == 4096) {
     if ((st = set_smem(gateup_kernel<4096>, gu_smem)) != MOE_OK) return st;
     ProfScope ps(MOE_K_GATEUP, stream);
@@ -1187,12 +1233,20 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
   }
   if ((st = check_launch("gateup_kernel")) != MOE_OK) return st;
 
-  // the GEMV down kernel reads every slot's matrices: it waits for the last part
+  // the down kernels read every slot's matrices: they wait for the last part
   if (gemv && pass.down.n >= 1 && pass.down.ready && pass.down.ready[pass.down.n - 1])
     MOE_CUDA(cudaStreamWaitEvent(stream, pass.down.ready[pass.down.n - 1], 0));
+  if (mma) {
+    const size_t smem = (size_t)kG * mma_rs_fp4(v->I) + 2 * kG * 4;
+    if ((st = set_smem(mma_down_kernel, smem)) != MOE_OK) return st;
+    ProfScope ps(MOE_K_DOWN, stream);
+    mma_down_kernel<<<mma_grid(mma_down_kernel, smem, max_groups * (v->H / kMmaRowsDown)), kMmaThreads, smem,
+                      stream>>>(a);
+  }
+  if ((st = check_launch("mma_down_kernel")) != MOE_OK) return st;
   const size_t dn_smem = (size_t)kG * v->I * 4 + 2 * kG * 4;
   const long long dn_items = max_groups * ((v->H + kRowsDown - 1) / kRowsDown);
-  if (!gemv) {
+  if (!gemv_run) {
   } else if (v->I == 2048) {
     if ((st = set_smem(down_kernel<2048>, dn_smem)) != MOE_OK) return st;
     ProfScope ps(MOE_K_DOWN, stream);
@@ -1474,6 +1528,15 @@ extern "C" moe_status moe_expert_forward_noalloc(const moe_expert_views* v, cons
   // nothing in the scratch has to start at zero: every region is written
   // by an earlier kernel of the same call before it is read
   return moe_expert_forward(v, x, T, k, slots, tags, w, y, scratch, kNoAllocScratchBytes, d_error, stream);
+}
+
+extern "C" moe_status moe_set_option(int option, int value, int* old_value) {
+  clear_error();
+  MOE_ARG(option == MOE_OPT_MMA_MAX_TOKENS, "unknown option %d", option);
+  MOE_ARG(value >= 0, "option value must be >= 0");
+  if (old_value) *old_value = g_mma_max_tokens;
+  g_mma_max_tokens = value;
+  return MOE_OK;
 }
 
 extern "C" moe_status moe_dequant_debug(const moe_expert_views* v, int pool, int slot, int matrix,

@@ -27,11 +27,12 @@ def test_mx_quantize_needs_k_multiple_of_32(lib):
 
 
 def test_copy_entry_points_need_a_cache(lib):
-    _invalid(lib, lib.moe_copy_missing_device(None, None, None, None, 0, None))
-    _invalid(lib, lib.moe_copy_missing_device_part(None, None, None, None, 0, 2, 0, None))
-    _invalid(lib, lib.moe_copy_missing_device_range(None, None, None, None, C.c_size_t(0), C.c_size_t(16), 0, None))
+    _invalid(lib, lib.moe_copy_missing_device(None, None, None, None, 0, None, None))
+    _invalid(lib, lib.moe_copy_missing_device_part(None, None, None, None, 0, 2, 0, None, None))
+    _invalid(lib, lib.moe_copy_missing_device_range(None, None, None, None, C.c_size_t(0), C.c_size_t(16), 0,
+                                                    None, None))
     _invalid(lib, lib.moe_copy_missing_device_slice(None, None, None, None, 0, 1, C.c_size_t(0), C.c_size_t(16),
-                                                    0, None))
+                                                    0, None, None))
     _invalid(lib, lib.moe_cache_prime_bank(None, None))
 
 
