@@ -42,7 +42,9 @@ def _args():
     p.add_argument("--sweep", default="1,4,16,64", help="decode batches also measured (comma list, '' for none)")
     p.add_argument("--cpu-sample-tokens", type=int, default=12,
                    help="tokens of the decode workload the oracle is timed on (about 10 s of host time)")
-    p.add_argument("--workload", default="decode", choices=["decode", "prefill", "ladder", "stack"])
+    p.add_argument("--workload", default="decode", choices=["decode", "prefill", "ladder", "stack", "forward"],
+                   help="forward: the decode layer's compute alone (router, ensure, expert MLP) on all 256 "
+                        "experts resident, no copies and no CPU baseline (a small case for profiling)")
     p.add_argument("--copy", default="device", choices=["engine", "device"],
                    help="miss copies: copy engine after one host sync, or a kernel reading the miss list")
     p.add_argument("--prefill-experts", type=int, default=0,
@@ -59,6 +61,9 @@ def _args():
                    help="decode prefetch: share of the next step's experts the synthetic predictor includes")
     p.add_argument("--no-overlap", action="store_true",
                    help="device copy: run the forward after the copies instead of beside them")
+    p.add_argument("--mma-max-tokens", type=int, default=None,
+                   help="decode batches of 2 up to this many tokens take the warp-MMA kernels (library default "
+                        "if omitted; 0 = never)")
     return p.parse_args()
 
 
@@ -198,6 +203,8 @@ def run_ours(args):
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
+    if args.mma_max_tokens is not None:
+        M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, args.mma_max_tokens)
     dev = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
@@ -252,6 +259,8 @@ def run_ours(args):
             return None
     stream = torch.cuda.current_stream(dev)
     n_steps = args.warmup + args.steps
+    mma_max = M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, 0)
+    M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, mma_max)
 
     def inputs(T):
         wl = configs.scaled(base, T=T)
@@ -328,9 +337,7 @@ def run_ours(args):
             d = int(torch.unique(ids).numel())
             distinct += d
             acct_gemm_bytes += d * gu_expert + T * H * 2 + T * k * I * 2
-            # the routed pairs take the grouped GEMM from 256 pairs per call on
-            acct_gu_bytes += gu_shared + T * H * 2 + T * I * 4 + (0 if T * k >= 256 else
-                                                                   d * gu_expert + T * k * I * 4)
+            acct_gu_bytes += gu_shared + T * H * 2 + T * I * 4 + d * gu_expert + T * k * I * 4
             acct_layer_bytes += d * Bx + layer_shared + 2 * T * H * 2
         # profiled pass: the same steps again from the same cache state, each
         # kernel bracketed by the library's events (for the breakdown only)
@@ -350,7 +357,9 @@ def run_ours(args):
         if gg_n and gg_ms >= gu_ms:   # the tcgen05 grouped GEMM dominates this batch size
             dom, dms, dn, dbytes = "prefill_gemm_kernel (gate/up)", gg_ms, gg_n, acct_gemm_bytes
         else:
-            dom, dms, dn, dbytes = "gateup_kernel", gu_ms, gu_n, acct_gu_bytes
+            # the routed experts' bytes count only where this kernel computed them
+            dbytes = acct_gu_bytes if not gg_n else acct_gu_bytes - acct_gemm_bytes + T * H * 2
+            dom, dms, dn = ("mma_gateup_kernel" if 2 <= T <= mma_max else "gateup_kernel"), gu_ms, gu_n
         gu_ms, gu_n, acct_gu_bytes = dms, dn, dbytes
         compute_ms = sum(v[0] for n, v in kt.items() if n != "copy_device") / args.steps
         return {
@@ -749,6 +758,65 @@ def run_other(args):
     print(json.dumps(out))
 
 
+def run_forward(args):
+    """Router + ensure + expert forward of the decode layer at T = args.T with every
+    expert resident (3.4 GB on the device), L2 flushed between steps."""
+    import numpy as np
+    import torch
+
+    from moe_expert_offload_router_gb300 import build as B
+    B.build()
+    import moe_expert_offload_router_gb300 as M
+    from synth import configs, gen
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if args.mma_max_tokens is not None:
+        M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, args.mma_max_tokens)
+    wl = configs.scaled(configs.DECODE, T=args.T)
+    H, I, E, k, T = wl.H, wl.I, wl.E, wl.k, wl.T
+    Bx = M.moe_fp4_expert_bytes(H, I)
+    pool = torch.empty(E * Bx, dtype=torch.uint8, device=dev)
+    for e in range(E):
+        pool[e * Bx:(e + 1) * Bx] = gen.fp4_expert(wl, 0, e, device=dev)
+    cache = M.moe_cache(E, 1, E, Bx, pool, None)
+    cache.import_(np.arange(E, dtype=np.int32), np.arange(E, dtype=np.uint64), E)
+    shared = torch.from_numpy(gen.shared_expert(wl, 0)).to(dev)
+    views = M.make_views(H, I, pool, E, None, 0, shared)
+    runner = M.DecodeLayerRunner(cache, views, E, k, T, dev, assume_resident=True)
+    n = args.warmup + args.steps
+    lg = [torch.from_numpy(gen.router_logits(wl, 0, s % wl.steps, T)).to(dev) for s in range(n)]
+    xs = [torch.from_numpy(gen.activations(wl, 0, s % wl.steps, T).view(np.int16)).to(dev) for s in range(n)]
+    y = torch.empty((T, H), dtype=torch.int16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for s in range(args.warmup):
+        runner.run(0, lg[s], xs[s], y)
+    torch.cuda.synchronize()
+    ev, seen = [], []
+    for i in range(args.steps):
+        s = args.warmup + i
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        runner.run(0, lg[s], xs[s], y)
+        b.record(stream)
+        ev.append((a, b))
+        seen.append(runner.ids[:T].clone())
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    nbytes = sum(int(torch.unique(ids).numel()) * Bx + M.moe_fp8_expert_bytes(H, I) + 2 * T * H * 2 for ids in seen)
+    gbs = nbytes / args.steps / (ms / 1e3) / 1e9
+    hbm_peak, _ = _peaks()
+    cache.close()
+    print(json.dumps({"metric": METRIC, "value": T / (ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+                      "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                      "vs_baseline": None, "data": "synthetic (seeded generator; no checkpoint weights)",
+                      "config": {"workload": f"decode layer compute alone (router, ensure, expert MLP), all {E} "
+                                             f"experts resident, T={T}", "T": T},
+                      "layer_hbm_gbs": gbs, "frac_of_hbm": gbs / hbm_peak}))
+
+
 def run_reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -782,5 +850,7 @@ if __name__ == "__main__":
         run_reference(a)
     elif a.workload == "decode":
         run_ours(a)
+    elif a.workload == "forward":
+        run_forward(a)
     else:
         run_other(a)

@@ -510,7 +510,7 @@ moe_status moe_mx_quantize(const uint16_t* x, int rows, int K, uint8_t* codes, u
  * counterpart; this serves callers that cannot allocate device memory: hosts
  * that hand a module a stream but own the device-memory budget, and serving
  * loops that forbid cudaMalloc after start-up (it can synchronise the device
- * and fail once memory is committed).  The scratch is a fixed 16 MiB array in
+ * and fail once memory is committed).  The scratch is a fixed 32 MiB array in
  * the library's device memory (held by every GPU that loads the library until
  * the process exits), enough for T = 64 tokens of top-8 at H = 4096,
  * I = 2048; larger calls return MOE_ERR_INVALID.  The caller still passes the
@@ -532,7 +532,7 @@ moe_status moe_expert_forward_noalloc(const moe_expert_views* v, const uint16_t*
 /* ---------------------------------------------------------------------------
  * Process-wide tuning option (not on the pages).  MOE_OPT_MMA_MAX_TOKENS:
  * decode calls of 2 up to this many tokens run their FP4 and shared-expert
- * pairs on the warp-level tensor-core kernels (default 32; 0 = never); larger
+ * pairs on the warp-level tensor-core kernels (default 64; 0 = never); larger
  * ones take the tcgen05 grouped GEMM from 256 pairs, and the CUDA-core GEMV
  * below that (and at one token).  The previous value goes to *old_value (may be null).
  * MOE_ERR_INVALID for an unknown option or a negative value.  Set it between

@@ -27,6 +27,7 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -46,7 +47,7 @@ struct Group {
 };
 
 struct FwdLayout {
-  size_t hdr, perm, groups, xsig, xs, h, o, gg, total;
+  size_t hdr, perm, groups, xsig, xs, h, o, hs16, hsig, gg, total;
   bool gemm;  // the FP4 routed pairs may take the grouped GEMM
 };
 
@@ -72,6 +73,10 @@ static FwdLayout fwd_layout(const moe_expert_views* v, int T, int k) {
   off = align256(off + (P + T) * (size_t)I * 4);
   L.o = off;
   off = align256(off + (P + T) * (size_t)H * 4);
+  L.hs16 = off;  // fp16 copy of h for the warp-MMA down kernel
+  off = align256(off + (P + T) * (size_t)I * 2);
+  L.hsig = off;
+  off = align256(off + (P + T) * 4);
   L.gemm = (long long)P >= kGemmMinPairs && grouped_gemm_supported(v);
   L.gg = off;
   if (L.gemm) off = align256(off + gg_index_bytes(T, k, v->fp4_num_slots));
@@ -95,6 +100,7 @@ struct FwdArgs {
   int32_t* err;
   int routed_gemm;  // routed pairs are computed by the grouped GEMM, not by these kernels
   int gemv_skip;    // bit per pool: groups of these pools are left to the warp-MMA kernels
+  int mma_group;    // tokens per group of those pools (kG for the others)
   // workspace
   int* hdr;
   int* perm;
@@ -103,6 +109,8 @@ struct FwdArgs {
   __half* xs;
   float* h;
   float* o;
+  __half* hs16;  // h in fp16, row r scaled by 2^-hsig[r] (warp-MMA down kernel)
+  int* hsig;
 };
 
 // ------------------------------------------------------------------ decode --
@@ -467,6 +475,11 @@ __device__ __forceinline__ int pow2_exponent(float amax) {
   return e - 1;
 }
 
+// Tokens per group: the warp-MMA kernels' pools take a.mma_group, the others kG.
+__device__ __forceinline__ int group_size(const FwdArgs& a, int pool) {
+  return (a.mma_group > 0 && pool >= 0 && pool < 31 && ((a.gemv_skip >> pool) & 1)) ? a.mma_group : kG;
+}
+
 __global__ void __launch_bounds__(1024) plan_kernel(FwdArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   if (blockIdx.x > 0) {
@@ -559,38 +572,44 @@ __global__ void __launch_bounds__(1024) plan_kernel(FwdArgs a) {
     }
     return lo;
   };
+  // runs of a pool the warp-MMA kernels take are cut every a.mma_group pairs
+  auto gsize = [&](unsigned long long key) { return group_size(a, (int)(key >> 62)); };
   int ng = 0;
-  for (int i = i0; i < min(i1, V); ++i) ng += ((i - starts[run_of(i)]) % kG) == 0;
+  for (int i = i0; i < min(i1, V); ++i) ng += ((i - starts[run_of(i)]) % gsize(keys[i])) == 0;
   int ngroups;
   int gi = block_exclusive_scan(ng, ws, &ngroups);
   for (int i = i0; i < min(i1, V); ++i) {
     const unsigned long long key = keys[i];
     a.perm[i] = (int)(key & 0xffffffffu);
     const int r = run_of(i);
-    if ((i - starts[r]) % kG) continue;
+    const int gs = gsize(key);
+    if ((i - starts[r]) % gs) continue;
     const int run_end = r + 1 < NS ? starts[r + 1] : V;
     Group g;
     g.pool = (int)(key >> 62);
     g.slot = (int)((key >> 32) & 0x3fffffffu);
     g.begin = i;
-    g.count = min(kG, run_end - i);
+    g.count = min(gs, run_end - i);
     a.groups[gi++] = g;
   }
   __syncthreads();
   if (tid == 0) {
     int n = ngroups;
     if (a.shared) {
-      for (int t0 = 0; t0 < a.T; t0 += kG) {
+      const int gs = group_size(a, MOE_POOL_SHARED);
+      for (int t0 = 0; t0 < a.T; t0 += gs) {
         Group g;
         g.pool = MOE_POOL_SHARED;
         g.slot = 0;
         g.begin = t0;
-        g.count = min(kG, a.T - t0);
+        g.count = min(gs, a.T - t0);
         a.groups[n++] = g;
       }
     }
     a.hdr[0] = n;
     a.hdr[1] = ngroups;
+    a.hdr[2] = 0;  // work counters of the warp-MMA gate/up and down kernels
+    a.hdr[3] = 0;
     if (a.err && scal[0]) atomicCAS(a.err, 0, MOE_ERR_INVALID);  // the caller's call cleared it
   }
 }
@@ -600,7 +619,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(FwdArgs a) {
 // A work item's group is checked against the buffers it indexes before any
 // access; a bad group (which the plan never produces) is skipped and flagged.
 __device__ __forceinline__ bool group_ok(const FwdArgs& a, const Group& g) {
-  if (g.count < 1 || g.count > kG) return false;
+  if (g.pool < 0 || g.pool > 2 || g.count < 1 || g.count > group_size(a, g.pool)) return false;
   if (g.pool == MOE_POOL_SHARED) return a.shared != nullptr && g.begin >= 0 && g.begin + g.count <= a.T;
   const int npool = g.pool == MOE_POOL_FP4 ? a.n4 : (g.pool == MOE_POOL_INT2 ? a.n2 : 0);
   return g.slot >= 0 && g.slot < npool && g.begin >= 0 && g.begin + g.count <= a.P;
@@ -1085,7 +1104,7 @@ static bool mma_supported(const moe_expert_views* v) {
 // Decode batches of at most this many tokens take the warp-MMA kernels for their
 // FP4 and shared-expert groups (0: never); larger ones from kGemmMinPairs pairs
 // take the tcgen05 grouped GEMM (moe_set_option).
-static int g_mma_max_tokens = 32;
+static int g_mma_max_tokens = 64;
 constexpr int kMmaMinTokens = 2;
 
 static moe_status validate_views(const moe_expert_views* v) {
@@ -1155,6 +1174,10 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
   // the CUDA-core kernels keep more bytes in flight there)
   const bool mma = !a.routed_gemm && T >= kMmaMinTokens && T <= g_mma_max_tokens && mma_supported(v);
   a.gemv_skip = mma ? kMmaPoolMask : 0;
+  // token tiles per group: one up to 8 tokens, else two (with four tiles per
+  // group only two chunk buffers fit the registers, which measured slower)
+  const int mma_nb = T <= 8 ? 1 : 2;
+  a.mma_group = mma ? 8 * mma_nb : 0;
   a.hdr = (int*)(base + L.hdr);
   a.perm = (int*)(base + L.perm);
   a.groups = (Group*)(base + L.groups);
@@ -1162,6 +1185,8 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
   a.xs = (__half*)(base + L.xs);
   a.h = (float*)(base + L.h);
   a.o = (float*)(base + L.o);
+  a.hs16 = (__half*)(base + L.hs16);
+  a.hsig = (int*)(base + L.hsig);
 
   if (a.routed_gemm) {
     // the gather reads x rows with 16-byte loads
@@ -1210,11 +1235,15 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
 
   const long long max_groups = (long long)T * k + (T + kG - 1) / kG + 1;
   if (mma) {
-    const size_t smem = (size_t)kG * mma_rs_fp4(v->H) + 2 * kG * 4;
-    if ((st = set_smem(mma_gateup_kernel, smem)) != MOE_OK) return st;
-    ProfScope ps(MOE_K_GATEUP, stream);
-    mma_gateup_kernel<<<mma_grid(mma_gateup_kernel, smem, max_groups * (v->I / kMmaFeat)), kMmaThreads, smem,
-                        stream>>>(a);
+    auto launch = [&](auto kernel) -> moe_status {
+      moe_status s2 = set_smem(kernel, kMmaSmem);
+      if (s2 != MOE_OK) return s2;
+      ProfScope ps(MOE_K_GATEUP, stream);
+      kernel<<<mma_grid(kernel, kMmaSmem, max_groups * (v->I / kMmaFeat)), kMmaThreads, kMmaSmem, stream>>>(a);
+      return MOE_OK;
+    };
+    st = mma_nb == 1 ? launch(mma_gateup_kernel<1>) : launch(mma_gateup_kernel<2>);
+    if (st != MOE_OK) return st;
   }
   if ((st = check_launch("mma_gateup_kernel")) != MOE_OK) return st;
   // the CUDA-core kernels: every group, or only the 2-bit ones beside the MMA kernels
@@ -1237,11 +1266,23 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
   if (gemv && pass.down.n >= 1 && pass.down.ready && pass.down.ready[pass.down.n - 1])
     MOE_CUDA(cudaStreamWaitEvent(stream, pass.down.ready[pass.down.n - 1], 0));
   if (mma) {
-    const size_t smem = (size_t)kG * mma_rs_fp4(v->I) + 2 * kG * 4;
-    if ((st = set_smem(mma_down_kernel, smem)) != MOE_OK) return st;
-    ProfScope ps(MOE_K_DOWN, stream);
-    mma_down_kernel<<<mma_grid(mma_down_kernel, smem, max_groups * (v->H / kMmaRowsDown)), kMmaThreads, smem,
-                      stream>>>(a);
+    {
+      // h rows in fp16 with a power-of-two scale each (routed pairs and shared rows)
+      const int rows = a.P + (a.shared ? T : 0);
+      ProfScope ps(MOE_K_DOWN, stream);
+      mma_hprep_kernel<<<std::min((rows + 7) / 8, sm_count() * 8), 256, 0, stream>>>(a.h, rows, a.I, a.hs16,
+                                                                                      a.hsig);
+    }
+    if ((st = check_launch("mma_hprep_kernel")) != MOE_OK) return st;
+    auto launch = [&](auto kernel) -> moe_status {
+      moe_status s2 = set_smem(kernel, kMmaSmem);
+      if (s2 != MOE_OK) return s2;
+      ProfScope ps(MOE_K_DOWN, stream);
+      kernel<<<mma_grid(kernel, kMmaSmem, max_groups * (v->H / kMmaRowsDown)), kMmaThreads, kMmaSmem, stream>>>(a);
+      return MOE_OK;
+    };
+    st = mma_nb == 1 ? launch(mma_down_kernel<1>) : launch(mma_down_kernel<2>);
+    if (st != MOE_OK) return st;
   }
   if ((st = check_launch("mma_down_kernel")) != MOE_OK) return st;
   const size_t dn_smem = (size_t)kG * v->I * 4 + 2 * kG * 4;
@@ -1488,7 +1529,7 @@ extern "C" moe_status moe_expert_forward_overlap(const moe_expert_views* v, cons
 // every GPU loading this library holds until the process exits.  Host code
 // cannot pass the array's name to a kernel (on the host it names a stand-in,
 // not device memory), so its device address is looked up once per device.
-constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;
+constexpr size_t kNoAllocScratchBytes = (size_t)32 << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 static std::mutex g_noalloc_mu;
