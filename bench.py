@@ -61,6 +61,12 @@ def _args():
                    help="decode prefetch: share of the next step's experts the synthetic predictor includes")
     p.add_argument("--no-overlap", action="store_true",
                    help="device copy: run the forward after the copies instead of beside them")
+    p.add_argument("--window-start", type=int, default=128,
+                   help="decode: first trace step of the timed window; the steps before it are replayed untimed "
+                        "(the warm-up steps are the last of them), so the window sits at the trace's steady state")
+    p.add_argument("--extras", default="prefill,ladder,stack",
+                   help="decode: other workloads measured in the same run and reported under their own keys "
+                        "(comma list of prefill, ladder, stack; '' for none)")
     p.add_argument("--mma-max-tokens", type=int, default=None,
                    help="decode batches of 2 up to this many tokens take the warp-MMA kernels (library default "
                         "if omitted; 0 = never)")
@@ -74,6 +80,35 @@ def _peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+# DRAM bytes (read + write) of one launch of a kernel from an ncu capture of
+# the same workload (profiles/), with the algorithmic bytes of that same
+# launch: a bench line scales the ratio to its own launches.  An entry is
+# removed when its kernel changes.
+NCU_TRAFFIC = {
+    ("mma_gateup_kernel", "decode"): {
+        "dram_bytes": 446_307_328 + 3_269_120, "algorithmic_bytes": 449_855_488,
+        "capture": "ncu dram__bytes_read/write.sum of mma_gateup_kernel<2>, bench.py --workload forward --T 64 "
+                   "(trace step 5: 48 experts + shared), profiles/mma_gateup_kernel_decode_forward_T64.md"},
+    ("prefill_gemm_kernel (gate/up)", "prefill"): {
+        "dram_bytes": 675_437_824 + 44_954_624, "algorithmic_bytes": 721_420_288,
+        "capture": "ncu dram__bytes_read/write.sum of prefill_gemm_kernel gate/up, bench.py --workload prefill "
+                   "--prefill-experts 64 --prefill-tokens 2048, profiles/prefill_gemm_kernel_prefill_E64_T2048.md"},
+}
+
+
+def ncu_traffic(kernel, workload, bytes_per_launch):
+    t = NCU_TRAFFIC.get((kernel, workload))
+    return (t["dram_bytes"] / t["algorithmic_bytes"] * bytes_per_launch, t["capture"]) if t else (None, None)
+
+
+def roofline_hbm(kernel, achieved, bytes_per_launch, ms_per_launch, peak, peak_kind, note, workload=None):
+    traffic, src = ncu_traffic(kernel, workload, bytes_per_launch)
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": traffic, "traffic_source": src,
+            "kernel": kernel, "peak_kind": peak_kind + " (copy bandwidth)",
+            "bytes_per_launch": bytes_per_launch, "ms_per_launch": ms_per_launch, "note": note}
 
 
 class Clocks:
@@ -189,7 +224,8 @@ def cpu_baseline(T: int, steps: int = 1, threads: int = 1):
 # GPU arm
 # ----------------------------------------------------------------------------
 
-def run_ours(args):
+def decode_line(args):
+    """The decode workload's contract line (rank 0; None elsewhere)."""
     import numpy as np
     import torch
     import torch.distributed as dist
@@ -258,9 +294,13 @@ def run_ours(args):
         except Exception:
             return None
     stream = torch.cuda.current_stream(dev)
-    n_steps = args.warmup + args.steps
     mma_max = M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, 0)
     M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, mma_max)
+    # trace steps: [0, start - warmup) replayed untimed from an empty cache, then
+    # [start - warmup, start) as warm-up, then the timed window [start, start + steps)
+    start = max(args.window_start, args.warmup)
+    n_steps = start + args.steps
+    first_warm = start - args.warmup
 
     def inputs(T):
         wl = configs.scaled(base, T=T)
@@ -300,7 +340,7 @@ def run_ours(args):
             torch.cuda.synchronize()
             if lfu_seed is not None:
                 M.moe_cache_seed_frequency(cache, lfu_seed)
-            for s in range(args.warmup):
+            for s in range(start):      # replay, then warm-up: the cache reaches the window's state
                 runner.run(0, lg[s], xs[s], y, prefetch=pf[s] if pf else None)
             torch.cuda.synchronize()
             runner.check()
@@ -316,7 +356,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for i in range(args.steps):
-            s = args.warmup + i
+            s = start + i
             flush.zero_()
             ev[i][0].record(stream)
             runner.run(0, lg[s], xs[s], y, prefetch=pf[s] if pf else None)
@@ -344,7 +384,7 @@ def run_ours(args):
         fresh()
         M.moe_profile_enable(True)
         for i in range(args.steps):
-            s = args.warmup + i
+            s = start + i
             flush.zero_()
             runner.run(0, lg[s], xs[s], y, prefetch=pf[s] if pf else None)
         torch.cuda.synchronize()
@@ -385,17 +425,19 @@ def run_ours(args):
         """Same steps through the public API with host buffers: inputs copied in
         from pinned memory and the output read back, every step."""
         lg, xs, pf = inputs(T)
-        h_lg = [t.cpu().pin_memory() for t in lg]
-        h_x = [t.cpu().pin_memory() for t in xs]
+        h_lg = {s: lg[s].cpu().pin_memory() for s in range(first_warm, n_steps)}
+        h_x = {s: xs[s].cpu().pin_memory() for s in range(first_warm, n_steps)}
         d_lg = torch.empty_like(lg[0])
         d_x = torch.empty_like(xs[0])
         y = torch.empty((T, H), dtype=torch.int16, device=dev)
         h_y = torch.empty((T, H), dtype=torch.int16, pin_memory=True)
         cache.reset()
+        torch.cuda.synchronize()
         if lfu_seed is not None:
-            torch.cuda.synchronize()
             M.moe_cache_seed_frequency(cache, lfu_seed)
-        for s in range(args.warmup):
+        for s in range(first_warm):          # untimed replay to the window's cache state
+            runner.run(0, lg[s], xs[s], y, prefetch=pf[s] if pf else None)
+        for s in range(first_warm, start):
             d_lg.copy_(h_lg[s], non_blocking=True)
             d_x.copy_(h_x[s], non_blocking=True)
             runner.run(0, d_lg, d_x, y, prefetch=pf[s] if pf else None)
@@ -403,7 +445,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         tot = 0.0
         for i in range(args.steps):
-            s = args.warmup + i
+            s = start + i
             flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -429,28 +471,76 @@ def run_ours(args):
         frunner = M.DecodeLayerRunner(fcache, fviews, E, k, T, dev, assume_resident=True)
         lg, xs, _ = inputs(T)
         y = torch.empty((T, H), dtype=torch.int16, device=dev)
-        for s in range(args.warmup):
+        for s in range(first_warm, start):
             frunner.run(0, lg[s], xs[s], y)
         torch.cuda.synchronize()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
         seen = []
         for i in range(args.steps):
-            s = args.warmup + i
+            s = start + i
             flush.zero_()
             ev[i][0].record(stream)
             frunner.run(0, lg[s], xs[s], y)
             ev[i][1].record(stream)
             seen.append(frunner.ids[:T].clone())
         torch.cuda.synchronize()
-        nbytes = sum(int(torch.unique(ids).numel()) * Bx + layer_shared + 2 * T * H * 2 for ids in seen)
         ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+        # the same steps again with the library's per-kernel events: the
+        # dominant kernel's launch time (kept out of the step timing above)
+        M.moe_profile_enable(True)
+        for i in range(args.steps):
+            s = start + i
+            flush.zero_()
+            frunner.run(0, lg[s], xs[s], y)
+        torch.cuda.synchronize()
+        kt = {M.KERNEL_NAMES[kid]: M.moe_profile_query(kid) for kid in range(M.MOE_K_COUNT)}
+        M.moe_profile_enable(False)
         fcache.close()
         del full
+        dsum = [int(torch.unique(ids).numel()) for ids in seen]
+        nbytes = sum(d * Bx + layer_shared + 2 * T * H * 2 for d in dsum)
         gbs = nbytes / args.steps / (ms / 1e3) / 1e9
+        # gate/up launch: the routed experts' w1/w3 (or only the shared expert's when
+        # the tcgen05 grouped GEMM took the routed pairs), x and h
+        gg_ms, gg_n = kt["gemm_gateup"]
+        gu_ms, gu_n = kt["gateup"]
+        P = T * k
+        if gg_n:
+            kname, kms, kn = "prefill_gemm_kernel (gate/up)", gg_ms, gg_n
+            kbytes = sum(d * gu_expert + T * H * 2 + P * I * 2 for d in dsum) / kn
+        else:
+            kname = "mma_gateup_kernel" if 2 <= T <= mma_max else "gateup_kernel"
+            kms, kn = gu_ms, gu_n
+            kbytes = sum(d * gu_expert + gu_shared + T * H * 2 + (P + T) * I * 4 for d in dsum) / kn
+        kgbs = kbytes / (kms / kn / 1e3) / 1e9
         return {"ms_per_step": ms, "tokens_per_s": T / (ms / 1e3), "layer_hbm_gbs": gbs,
-                "frac_of_hbm": gbs / hbm_peak,
+                "frac_of_hbm": gbs / hbm_peak, "kernel": kname, "kernel_ms_per_launch": kms / kn,
+                "kernel_bytes_per_launch": kbytes, "kernel_gbs": kgbs,
+                "kernel_ms_per_step": {n: round(v[0] / args.steps, 4) for n, v in kt.items() if v[1]},
                 "note": "router + ensure + forward, all 256 experts resident, same trace steps, L2 flushed"}
+
+    def measure_trace(T):
+        """Misses over the whole seeded trace (every step from an empty cache), beside
+        the timed window's figures."""
+        wl = configs.scaled(base, T=T)
+        y = torch.empty((T, H), dtype=torch.int16, device=dev)
+        cache.reset()
+        torch.cuda.synchronize()
+        if lfu_seed is not None:
+            M.moe_cache_seed_frequency(cache, lfu_seed)
+        m0 = runner.stats["misses"]
+        distinct = 0
+        for s in range(base.steps):
+            lg_s = torch.from_numpy(gen.router_logits(wl, 0, s, T)).to(dev)
+            x_s = torch.from_numpy(gen.activations(wl, 0, s, T).view(np.int16)).to(dev)
+            runner.run(0, lg_s, x_s, y)
+            distinct += int(torch.unique(runner.ids[:T]).numel())
+        torch.cuda.synchronize()
+        runner.check()
+        misses = runner.stats["misses"] - m0
+        return {"steps": base.steps, "misses_per_step": misses / base.steps,
+                "hit_rate": 1.0 - misses / max(distinct, 1)}
 
     def measure_graph(T):
         """The same steps with each layer step replayed as one CUDA graph (batches
@@ -462,13 +552,13 @@ def run_ours(args):
             M.moe_cache_seed_frequency(cache, lfu_seed)
         lg, xs, _ = inputs(T)
         y = torch.empty((T, H), dtype=torch.int16, device=dev)
-        for s in range(args.warmup):
+        for s in range(start):
             grunner.run(0, lg[s], xs[s], y)
         torch.cuda.synchronize()
         grunner.check()
         tot = 0.0
         for i in range(args.steps):
-            s = args.warmup + i
+            s = start + i
             flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -493,6 +583,7 @@ def run_ours(args):
     head = results[args.T]
     compute_only = measure_compute_only(args.T)
     e2e = measure_e2e(args.T)
+    trace = measure_trace(args.T)
     link_gbs = link_probe() if args.copy == "device" else None
     cpu = cpu_baseline(args.cpu_sample_tokens) if (rank == 0 and world == 1) else None
     cpu_all = (cpu_baseline(args.cpu_sample_tokens, threads=os.cpu_count() or 1)
@@ -512,12 +603,17 @@ def run_ours(args):
                                                                         "seeded from 64 other trace steps)",
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "l2": "flushed (256 MB write) before every timed step"},
-            "roofline": {"bound": "hbm", "achieved": head["gateup_gbs"], "peak": hbm_peak, "unit": "GB/s",
-                         "frac": head["gateup_gbs"] / hbm_peak, "traffic": None,
-                         "kernel": head["dominant"], "peak_kind": peak_kind + " (copy bandwidth)",
-                         "bytes_per_launch": head["gateup_bytes_per_launch"], "ms_per_launch": head["gateup_ms"],
-                         "note": "timed inside the step; with overlapped copies its first pass shares the SMs "
-                                 "with the copy kernel"},
+            "roofline": roofline_hbm(compute_only["kernel"], compute_only["kernel_gbs"],
+                                     compute_only["kernel_bytes_per_launch"], compute_only["kernel_ms_per_launch"],
+                                     hbm_peak, peak_kind,
+                                     "dominant kernel of the decode layer's compute (all experts resident, the "
+                                     "timed window's steps, one launch per step); inside the copy-bound step it "
+                                     "runs as two passes beside the copy kernel: see roofline_in_step",
+                                     workload="decode"),
+            "roofline_in_step": {"kernel": head["dominant"], "achieved": head["gateup_gbs"],
+                                 "frac": head["gateup_gbs"] / hbm_peak, "unit": "GB/s",
+                                 "bytes_per_launch": head["gateup_bytes_per_launch"],
+                                 "ms_per_launch": head["gateup_ms"], "launches": head["gateup_launches"]},
             "cpu_baseline": cpu,
             "cpu_baseline_all_cores": cpu_all,
             "e2e": e2e,
@@ -533,10 +629,29 @@ def run_ours(args):
             "host_link_frac_of_probe": (head["host_link_gbs"] / link_gbs
                                         if head["host_link_gbs"] and link_gbs else None),
             "hit_rate": head["hit_rate"],
+            "trace_window": {"timed_steps": [start, start + args.steps], "warmup_steps": [first_warm, start],
+                             "replayed_untimed": [0, first_warm], "full_trace": trace},
             "kernel_ms_per_step": head["kernel_ms"],
             "sweep": {str(T): {kk: (round(v, 4) if isinstance(v, float) else v) for kk, v in r.items()
                                if kk not in ("kernel_ms",)} for T, r in results.items()},
         }
+        return line
+    return None
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    line = decode_line(args)
+    torch.cuda.empty_cache()
+    # the other workloads, each under its own key (single GPU, rank 0 only)
+    if rank == 0 and world == 1:
+        for name in [w.strip() for w in args.extras.split(",") if w.strip()]:
+            line[name] = other_entry(args, name)
+            torch.cuda.empty_cache()
+    if rank == 0:
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
@@ -551,8 +666,92 @@ def _tensor_peak():
         return 1900.0, "fallback"
 
 
-def run_other(args):
-    """Prefill grouped GEMM, precision-ladder decode, or the 43-layer stack."""
+# Oracle timings of the other workloads on bounded samples (fp64 NumPy, one host
+# core): the prefill's first tokens, one ladder step of a few tokens from empty
+# pools, one token of one stack layer.
+_CPU_OTHER = {
+    "prefill": r"""
+wl = configs.PREFILL
+ids, w = router_topk(gen.router_logits(wl, 0, 0), wl.k)
+x = gen.activations(wl, 0, 0)
+t0 = time.perf_counter()
+moe_layer(x, ids, w, lambda e, tag: F.decode_fp4_expert(gen.fp4_expert(wl, 0, e), wl.H, wl.I),
+          tokens=list(range(NTOK)))
+dt = time.perf_counter() - t0
+print(json.dumps({"tokens": NTOK, "seconds": dt}))
+""",
+    "ladder": r"""
+wl = configs.scaled(configs.LADDER, T=NTOK)
+lg = gen.router_logits(wl, 0, 0, NTOK)
+x = gen.activations(wl, 0, 0, NTOK)
+t0 = time.perf_counter()
+ids, w = router_topk(lg, wl.k)
+c4, c2 = SlotCacheLRU(wl.S, 1, wl.E), SlotCacheLRU(wl.S2, 1, wl.E)
+_, tags, wout, _, _, end = ladder_classify(c4, c2, 0, ids, w, *wl.ladder, 0)
+def dec(e, tag):
+    if tag == 0:
+        return F.decode_fp4_expert(gen.fp4_expert(wl, 0, e), wl.H, wl.I)
+    return F.decode_int2_expert(gen.int2_expert(wl, 0, e), wl.H, wl.I)
+moe_layer(x, np.where(tags == 2, -1, ids), wout, dec, tags=tags, tokens=list(range(end)))
+dt = time.perf_counter() - t0
+print(json.dumps({"tokens": end, "seconds": dt}))
+""",
+    "stack": r"""
+wl = configs.STACK
+lg = gen.router_logits(wl, 0, 0)
+x = gen.activations(wl, 0, 0)
+t0 = time.perf_counter()
+ids, w = router_topk(lg, wl.k)
+shw = F.decode_fp8_expert(gen.shared_expert(wl, 0), wl.H, wl.I)
+moe_layer(x, ids, w, lambda e, tag: F.decode_fp4_expert(gen.fp4_expert(wl, 0, e), wl.H, wl.I), shared=shw,
+          tokens=list(range(NTOK)))
+dt = time.perf_counter() - t0
+print(json.dumps({"tokens": NTOK, "seconds": dt}))
+""",
+}
+_CPU_HEAD = r"""
+import json, sys, time
+sys.path.insert(0, ROOT)
+import numpy as np
+from oracle import formats as F
+from oracle.ladder import ladder_classify
+from oracle.mlp import moe_layer
+from oracle.router import router_topk
+from oracle.slot_cache import SlotCacheLRU
+from synth import configs, gen
+"""
+
+
+def cpu_baseline_other(name: str, ntok: int):
+    """The oracle on a bounded sample of workload `name`, single-threaded."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = _CPU_HEAD.replace("ROOT", repr(ROOT)) + _CPU_OTHER[name].replace("NTOK", str(ntok))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": "failed: " + (r.stderr.strip().splitlines()[-1][:200] if r.stderr else "")}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    what = {"prefill": f"the first {d['tokens']} tokens of the prefill batch (their experts decoded)",
+            "ladder": f"one ladder step of {d['tokens']} tokens from empty pools (classify + MLP)",
+            "stack": f"{d['tokens']} token(s) of one stack layer with the shared expert"}[name]
+    out = {"value": d["tokens"] / d["seconds"], "unit": UNIT, "cores": 1, "kind": "oracle",
+           "sample": f"{what}, fp64 NumPy, {d['seconds']:.1f} s single-threaded"}
+    if name == "stack":
+        # the line's unit is tokens per 43-layer step: the oracle's per-layer rate / 43
+        out["value"] = d["tokens"] / d["seconds"] / configs_layers()
+        out["sample"] += " (tokens/s of one layer divided by the 43 layers of a step)"
+    return out
+
+
+def configs_layers():
+    from synth import configs
+    return configs.STACK.layers
+
+
+def other_entry(args, name):
+    """Prefill grouped GEMM, precision-ladder decode, or the 43-layer stack: one
+    contract-shaped entry (timed steps, per-kernel breakdown, roofline, oracle
+    baseline)."""
     import numpy as np
     import torch
 
@@ -563,6 +762,10 @@ def run_other(args):
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
+    if args.mma_max_tokens is not None:
+        M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, args.mma_max_tokens)
+    mma_max = M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, 0)
+    M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, mma_max)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     hbm_peak, hbm_kind = _peaks()
@@ -595,13 +798,14 @@ def run_other(args):
         M.moe_profile_enable(False)
         return kt
 
-    wl = {"prefill": configs.PREFILL, "ladder": configs.LADDER, "stack": configs.STACK}[args.workload]
-    if args.workload == "prefill" and (args.prefill_experts or args.prefill_tokens):
+    wl = {"prefill": configs.PREFILL, "ladder": configs.LADDER, "stack": configs.STACK}[name]
+    if name == "prefill" and (args.prefill_experts or args.prefill_tokens):
         e = args.prefill_experts or wl.E
         wl = configs.scaled(wl, E=e, S=e, T=args.prefill_tokens or wl.T)
     H, I, E, k, T = wl.H, wl.I, wl.E, wl.k, wl.T
     Bx = M.moe_fp4_expert_bytes(H, I)
-    if args.workload == "prefill" and args.stream_layers > 0:
+    gu4 = 2 * (I * H // 2 + I * H // 32)     # w1 + w3 bytes of an FP4 expert
+    if name == "prefill" and args.stream_layers > 0:
         # whole-layer streaming: every layer's experts cross the host link each pass
         nl = args.stream_layers
         bank = torch.empty(nl * E * Bx, dtype=torch.uint8, pin_memory=True)
@@ -636,16 +840,15 @@ def run_other(args):
                     "ms_per_layer": per_layer,
                     "host_link_gbs": E * Bx / (per_layer / 1e3) / 1e9,
                     "roofline": None})
-        print(json.dumps(out))
-        return
-    if args.workload in ("prefill", "ladder"):
+        return out
+    if name in ("prefill", "ladder"):
         bank = torch.empty(E * Bx, dtype=torch.uint8, pin_memory=True)
         for e in range(E):
             bank[e * Bx:(e + 1) * Bx].copy_(gen.fp4_expert(wl, 0, e, device=dev))
         slots = torch.empty(wl.S * Bx, dtype=torch.uint8, device=dev)
         cache = M.moe_cache(wl.S, 1, E, Bx, slots, bank)
         c2, s2 = None, None
-        if args.workload == "ladder":
+        if name == "ladder":
             B2 = M.moe_int2_expert_bytes(H, I)
             bank2 = torch.empty(E * B2, dtype=torch.uint8, pin_memory=True)
             for e in range(E):
@@ -655,107 +858,161 @@ def run_other(args):
         views = M.make_views(H, I, slots, wl.S, s2, wl.S2 if s2 is not None else 0, None)
         runner = M.DecodeLayerRunner(cache, views, E, k, T, dev, int2_cache=c2, ladder=wl.ladder,
                                      copy=args.copy)
-        n = args.warmup + args.steps
+        # ladder: steady state as in the decode workload (untimed replay of the
+        # steps before the window); prefill: one batch, all experts resident
         nsteps = max(wl.steps, 1)
+        start = min(max(args.window_start, args.warmup), max(nsteps - args.steps, args.warmup)) \
+            if name == "ladder" else args.warmup
+        n = start + args.steps
         lg = [torch.from_numpy(gen.router_logits(wl, 0, s % nsteps, T)).to(dev) for s in range(n)]
         xs = [torch.from_numpy(gen.activations(wl, 0, s % nsteps, T).view(np.int16)).to(dev) for s in range(n)]
         y = torch.empty((T, H), dtype=torch.int16, device=dev)
-        for s in range(args.warmup):
-            runner.run(0, lg[s], xs[s], y)
-        torch.cuda.synchronize()
-        runner.check()
+
+        def fresh():
+            cache.reset()
+            if c2 is not None:
+                c2.reset()
+            torch.cuda.synchronize()
+            for s in range(start):
+                runner.run(0, lg[s], xs[s], y)
+            torch.cuda.synchronize()
+            runner.check()
+
+        fresh()
         m0 = runner.stats["misses"]
+        seen = []
+
+        def step(i):
+            runner.run(0, lg[start + i], xs[start + i], y)
+            seen.append((runner.slots[:T].clone(), runner.tags[:T].clone()) if name == "ladder" else None)
         clocks.start()
-        ms = timed(lambda i: runner.run(0, lg[args.warmup + i], xs[args.warmup + i], y), args.steps)
+        ms = timed(step, args.steps)
         ck = clocks.stop()
         runner.check()
         m1 = runner.stats["misses"]
-        # the breakdown replays the same steps from the same cache state
-        cache.reset()
-        if c2 is not None:
-            c2.reset()
-        torch.cuda.synchronize()
-        for s in range(args.warmup):
-            runner.run(0, lg[s], xs[s], y)
-        kt = profiled(lambda i: runner.run(0, lg[args.warmup + i], xs[args.warmup + i], y), args.steps)
+        fresh()
+        kt = profiled(lambda i: runner.run(0, lg[start + i], xs[start + i], y), args.steps)
         runner.check()
         out.update({"value": T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "clocks": ck,
                     "gpu_launches": sum(v[1] for v in kt.values()),
                     "kernel_ms_per_step": {nm: round(v[0] / args.steps, 4) for nm, v in kt.items() if v[1]},
                     "misses_per_step": (m1 - m0) / args.steps})
-        if args.workload == "prefill":
+        if name == "prefill":
             P = T * k
-            flops = 6.0 * P * H * I
             gu_ms = kt["gemm_gateup"][0] / max(kt["gemm_gateup"][1], 1)
             dn_ms = kt["gemm_down"][0] / max(kt["gemm_down"][1], 1)
             gu_tf = 4.0 * P * H * I / (gu_ms / 1e3) / 1e12
             peak, kind = _tensor_peak()
-            out["dtype"] = "bf16 MMA (fp32 accumulate) on exactly decoded MXFP4 weights"
+            floor_ms = 3 * E * (H * I // 2 + H * I // 32) / (hbm_peak * 1e6)
+            out["dtype"] = "bf16/fp16 MMA (fp32 accumulate) on exactly decoded MXFP4 weights (W4A16)"
             out["config"] = {"workload": f"prefill grouped GEMM H=4096 I=2048 E={E} top_k=6 T={T}, all {E} "
-                                         "experts resident", "T": T}
-            out["grouped_gemm_tflops"] = flops / ((gu_ms + dn_ms) / 1e3) / 1e12
+                                         "experts resident, W4A16", "T": T}
+            out["grouped_gemm_tflops"] = 6.0 * P * H * I / ((gu_ms + dn_ms) / 1e3) / 1e12
+            gu_bytes = E * gu4 + P * H * 2 + P * I * 2
+            traffic, src = ncu_traffic("prefill_gemm_kernel (gate/up)", "prefill", gu_bytes)
             out["roofline"] = {"bound": "tensor", "achieved": gu_tf, "peak": peak, "unit": "TFLOP/s",
-                               "frac": gu_tf / peak, "traffic": None, "kernel": "prefill_gemm_kernel (gate/up)",
-                               "peak_kind": kind, "ms_per_launch": gu_ms,
-                               "hbm_floor_ms_weights": 3 * E * (H * I // 2 + H * I // 32) / (hbm_peak * 1e6)}
+                               "frac": gu_tf / peak, "traffic": traffic, "traffic_source": src,
+                               "bytes_per_launch": gu_bytes, "kernel": "prefill_gemm_kernel (gate/up)",
+                               "peak_kind": kind, "ms_per_launch": gu_ms, "flops_per_launch": 4.0 * P * H * I,
+                               "hbm_floor_ms_weights": floor_ms,
+                               "step_frac_of_hbm_floor": floor_ms / ms}
+            out["cpu_baseline"] = cpu_baseline_other("prefill", 3)
         else:
-            out["dtype"] = "e2m1/e8m0 + 2-bit/e4m3 weights, f16 dot, f32 accumulate"
+            # touched bytes of the timed steps: each pool's distinct slots of kept pairs
+            B2 = M.moe_int2_expert_bytes(H, I)
+            gu2 = 2 * (I * H // 4 + I * H // 32)
+            lay_b, gu_b = 0, 0
+            for sl, tg in seen:
+                sl, tg = sl.cpu().numpy(), tg.cpu().numpy()
+                d4 = len(np.unique(sl[(tg == 0) & (sl >= 0)]))
+                d2 = len(np.unique(sl[(tg == 1) & (sl >= 0)]))
+                lay_b += d4 * Bx + d2 * B2 + 2 * T * H * 2
+                gu_b += d4 * gu4 + d2 * gu2 + T * H * 2 + T * k * I * 4
+            gu_ms, gu_n = kt["gateup"]
+            gu_bytes = gu_b / max(gu_n, 1)
+            gu_gbs = gu_bytes / (gu_ms / max(gu_n, 1) / 1e3) / 1e9
+            out["dtype"] = "e2m1/e8m0 and 2-bit/e4m3 weights, fp16 products, fp32 accumulate"
             out["config"] = {"workload": "ladder (2,4) decode H=4096 I=2048 E=256 top_k=6 T=32, 96 FP4 + "
-                                         "192 2-bit slots, Zipf(1.1) trace", "T": T}
-    else:
-        # 43-layer stack, every expert resident, no host sync per layer
-        L = wl.layers
-        S = L * E
-        pool = torch.empty(S * Bx, dtype=torch.uint8, device=dev)
+                                         "192 2-bit slots, Zipf(1.1) trace", "T": T,
+                             "timed_steps": [start, start + args.steps]}
+            out["layer_gbs"] = lay_b / args.steps / (ms / 1e3) / 1e9
+            # every launch of the gate/up scope (the warp-MMA kernel for the FP4
+            # pairs and the CUDA-core kernel for the 2-bit ones share it)
+            out["roofline"] = roofline_hbm("gateup (mma_gateup_kernel + gateup_kernel)", gu_gbs, gu_bytes,
+                                           gu_ms / max(gu_n, 1), hbm_peak, hbm_kind,
+                                           "the gate/up kernels of the ladder's steps: touched FP4 and 2-bit "
+                                           "experts' w1/w3, x and h")
+            out["cpu_baseline"] = cpu_baseline_other("ladder", 4)
+        return out
+    # 43-layer stack, every expert resident, no host sync per layer
+    L = wl.layers
+    S = L * E
+    pool = torch.empty(S * Bx, dtype=torch.uint8, device=dev)
+    for layer in range(L):
+        for e in range(E):
+            key = layer * E + e
+            pool[key * Bx:(key + 1) * Bx] = gen.fp4_expert(wl, layer, e, device=dev)
+    cache = M.moe_cache(S, L, E, Bx, pool, None)
+    cache.import_(np.arange(S, dtype=np.int32), np.arange(S, dtype=np.uint64), S)
+    shared = [torch.from_numpy(gen.shared_expert(wl, layer)).to(dev) for layer in range(L)]
+    views = [M.make_views(H, I, pool, S, None, 0, shared[layer]) for layer in range(L)]
+    runners = [M.DecodeLayerRunner(cache, views[layer], E, k, T, dev, assume_resident=True)
+               for layer in range(L)]
+    for r in runners[1:]:
+        r.ws = runners[0].ws
+    n = args.warmup + args.steps
+    lg = [[torch.from_numpy(gen.router_logits(wl, layer, s % wl.steps, T)).to(dev) for layer in range(L)]
+          for s in range(n)]
+    x0 = torch.from_numpy(gen.activations(wl, 0, 0, T).view(np.int16)).to(dev)
+    ya = torch.empty((T, H), dtype=torch.int16, device=dev)
+    xb = torch.empty((T, H), dtype=torch.int16, device=dev)
+
+    def step(s):
+        x = x0
         for layer in range(L):
-            for e in range(E):
-                key = layer * E + e
-                pool[key * Bx:(key + 1) * Bx] = gen.fp4_expert(wl, layer, e, device=dev)
-        cache = M.moe_cache(S, L, E, Bx, pool, None)
-        cache.import_(np.arange(S, dtype=np.int32), np.arange(S, dtype=np.uint64), S)
-        shared = [torch.from_numpy(gen.shared_expert(wl, layer)).to(dev) for layer in range(L)]
-        views = [M.make_views(H, I, pool, S, None, 0, shared[layer]) for layer in range(L)]
-        runners = [M.DecodeLayerRunner(cache, views[layer], E, k, T, dev, assume_resident=True)
-                   for layer in range(L)]
-        for r in runners[1:]:
-            r.ws = runners[0].ws
-        n = args.warmup + args.steps
-        lg = [[torch.from_numpy(gen.router_logits(wl, layer, s % wl.steps, T)).to(dev) for layer in range(L)]
-              for s in range(n)]
-        x0 = torch.from_numpy(gen.activations(wl, 0, 0, T).view(np.int16)).to(dev)
-        ya = torch.empty((T, H), dtype=torch.int16, device=dev)
-        xb = torch.empty((T, H), dtype=torch.int16, device=dev)
+            runners[layer].run(layer, lg[s][layer], x, ya)
+            M.moe_rms_carry(ya, 1e-6, xb)
+            x = xb
 
-        def step(s):
-            x = x0
-            for layer in range(L):
-                runners[layer].run(layer, lg[s][layer], x, ya)
-                M.moe_rms_carry(ya, 1e-6, xb)
-                x = xb
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+    clocks.start()
+    ms = timed(lambda i: step(args.warmup + i), args.steps)
+    ck = clocks.stop()
+    kt = profiled(lambda i: step(args.warmup + i), args.steps)
+    # touched bytes per step: distinct experts per layer
+    tb, gub = 0, 0
+    fp8 = M.moe_fp8_expert_bytes(H, I)
+    gu8 = 2 * (I * H + I * 4)
+    for s in range(args.warmup, n):
+        for layer in range(L):
+            ids, _ = M.moe_router_topk(lg[s][layer], k)
+            d = int(torch.unique(ids).numel())
+            tb += d * Bx + fp8
+            gub += d * gu4 + gu8 + T * H * 2 + (T * k + T) * I * 4
+    gbs = tb / args.steps / (ms / 1e3) / 1e9
+    gu_ms, gu_n = kt["gateup"]
+    gu_bytes = gub / max(gu_n, 1)
+    gu_gbs = gu_bytes / (gu_ms / max(gu_n, 1) / 1e3) / 1e9
+    out.update({"value": T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "clocks": ck,
+                "dtype": "e2m1/e8m0 weights, fp16 products, fp32 accumulate",
+                "config": {"workload": "43-layer stack decode, 256 FP4 experts + FP8 shared per layer, all "
+                                       "resident (148 GB), T=16, 70% step-to-step reuse", "T": T, "layers": L},
+                "stack_hbm_gbs": gbs, "hbm_frac_of_step": gbs / hbm_peak,
+                "gpu_launches": sum(v[1] for v in kt.values()),
+                "kernel_ms_per_step": {nm: round(v[0] / args.steps, 4) for nm, v in kt.items() if v[1]},
+                "roofline": roofline_hbm("mma_gateup_kernel" if 2 <= T <= mma_max else "gateup_kernel", gu_gbs,
+                                         gu_bytes, gu_ms / max(gu_n, 1), hbm_peak, hbm_kind,
+                                         "gate/up kernel of each layer: touched experts' w1/w3, the shared "
+                                         "expert's, x and h"),
+                "cpu_baseline": cpu_baseline_other("stack", 1)})
+    del pool
+    return out
 
-        for s in range(args.warmup):
-            step(s)
-        torch.cuda.synchronize()
-        clocks.start()
-        ms = timed(lambda i: step(args.warmup + i), args.steps)
-        ck = clocks.stop()
-        kt = profiled(lambda i: step(args.warmup + i), args.steps)
-        # touched bytes per step: distinct experts per layer
-        tb = 0
-        for s in range(args.warmup, n):
-            for layer in range(L):
-                ids, _ = M.moe_router_topk(lg[s][layer], k)
-                tb += int(torch.unique(ids).numel()) * Bx + M.moe_fp8_expert_bytes(H, I)
-        gbs = tb / args.steps / (ms / 1e3) / 1e9
-        gu_ms, gu_n = kt["gateup"]
-        out.update({"value": T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "clocks": ck,
-                    "dtype": "e2m1/e8m0 weights, f16 dot, f32 accumulate",
-                    "config": {"workload": "43-layer stack decode, 256 FP4 experts + FP8 shared per layer, all "
-                                           "resident (148 GB), T=16, 70% step-to-step reuse", "T": T, "layers": L},
-                    "stack_hbm_gbs": gbs, "hbm_frac_of_step": gbs / hbm_peak,
-                    "gpu_launches": sum(v[1] for v in kt.values()),
-                    "kernel_ms_per_step": {nm: round(v[0] / args.steps, 4) for nm, v in kt.items() if v[1]}})
-    print(json.dumps(out))
+
+def run_other(args):
+    print(json.dumps(other_entry(args, args.workload)))
 
 
 def run_forward(args):
