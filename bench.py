@@ -917,6 +917,42 @@ def other_entry(args, name):
                                "hbm_floor_ms_weights": floor_ms,
                                "step_frac_of_hbm_floor": floor_ms / ms}
             out["cpu_baseline"] = cpu_baseline_other("prefill", 3)
+            # the A-quantised mode on the block-scaled FP4 MMA, on the same batch
+            # (the runner's slots and router weights of its last step)
+            sl, ww = runner.slots[:T].clone(), runner.w[:T].clone()
+            ws_mx = torch.empty(M.moe_expert_prefill_workspace(views, T, k), dtype=torch.uint8, device=dev)
+            err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+            def mx_step(i):
+                M.moe_expert_prefill_prec(views, xs[start], sl, ww, M.MOE_PREC_A_MXFP4, y, ws_mx, err)
+            for _ in range(args.warmup):
+                mx_step(0)
+            torch.cuda.synchronize()
+            ms_mx = timed(mx_step, args.steps)
+            kmx = profiled(mx_step, args.steps)
+            if int(err.item()) != 0:
+                raise RuntimeError(f"A-quantised prefill reported status {int(err.item())}")
+            fp4_peak = M.moe_fp4_mma_peak(4096)
+            mgu = kmx["gemm_gateup"][0] / max(kmx["gemm_gateup"][1], 1)
+            mdn = kmx["gemm_down"][0] / max(kmx["gemm_down"][1], 1)
+            mgu_tf = 4.0 * P * H * I / (mgu / 1e3) / 1e12
+            mdn_tf = 2.0 * P * H * I / (mdn / 1e3) / 1e12
+            out["a_mxfp4"] = {
+                "ms_per_step": ms_mx, "tokens_per_s": T / (ms_mx / 1e3),
+                "note": "activations x and h quantised to MXFP4 (OCP MX, blocks of 32) and multiplied on "
+                        "tcgen05.mma.kind::mxf4.block_scale; the expert forward only (the batch's slots given)",
+                "kernel_ms_per_step": {nm: round(v[0] / args.steps, 4) for nm, v in kmx.items() if v[1]},
+                "gemm_gateup_tflops": mgu_tf, "gemm_down_tflops": mdn_tf,
+                "grouped_gemm_tflops": 6.0 * P * H * I / ((mgu + mdn) / 1e3) / 1e12,
+                "fp4_peak_tflops": fp4_peak,
+                "fp4_peak_kind": "measured in this run: back-to-back kind::mxf4 MMAs (M=128, N=256, K=64) from "
+                                 "shared memory on every SM (moe_fp4_mma_peak)",
+                "step_frac_of_hbm_floor": floor_ms / ms_mx,
+            }
+            out["roofline_fp4"] = {"bound": "tensor", "achieved": mgu_tf, "peak": fp4_peak, "unit": "TFLOP/s",
+                                   "frac": mgu_tf / fp4_peak, "traffic": None,
+                                   "kernel": "mxf4_gemm_kernel (gate/up)", "peak_kind": out["a_mxfp4"]["fp4_peak_kind"],
+                                   "ms_per_launch": mgu, "flops_per_launch": 4.0 * P * H * I}
         else:
             # touched bytes of the timed steps: each pool's distinct slots of kept pairs
             B2 = M.moe_int2_expert_bytes(H, I)

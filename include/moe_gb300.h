@@ -541,6 +541,16 @@ moe_status moe_expert_forward_noalloc(const moe_expert_views* v, const uint16_t*
 enum { MOE_OPT_MMA_MAX_TOKENS = 0 };
 moe_status moe_set_option(int option, int value, int* old_value);
 
+/* Diagnostic (not on the pages): the block-scaled FP4 tensor rate of this GPU.
+ * One CTA per SM issues `iters` groups of four tcgen05.mma.kind::mxf4 (M = 128,
+ * N = 256, K = 64, E8M0 unit scales) from shared memory into one tensor-memory
+ * accumulator, with no data movement; *tflops receives the dense TFLOP/s
+ * (2 M N K per MMA) measured with CUDA events on `stream`.  The call
+ * synchronises the stream (and allocates 4 bytes of device memory for its
+ * status).  iters a positive multiple of 64, else MOE_ERR_INVALID;
+ * MOE_ERR_TIMEOUT if the completion wait gave up. */
+moe_status moe_fp4_mma_peak(int iters, double* tflops, cudaStream_t stream);
+
 /* Decode one matrix of one slot to fp32 [N, K] (test hook; values are exact). */
 moe_status moe_dequant_debug(const moe_expert_views* v, int pool, int slot, int matrix,
                              float* out, cudaStream_t stream);
@@ -577,8 +587,10 @@ moe_status moe_profile_timeline(int max, int32_t* kernel, double* start_ms, doub
  * MOE_ERR_TIMEOUT when the wait gives up.  The context stays usable. */
 moe_status moe_debug_timeout_probe(int64_t limit_ns, int32_t* d_status, cudaStream_t stream);
 
-/* Runs a tiny router + cache + copy round trip on the current device and
- * checks it (synchronous).  MOE_OK means the library executes here. */
+/* Runs a tiny router + cache + copy round trip and a tiny expert forward
+ * (H = 64, I = 32, two all-ones FP4 experts, x = 1: every output exactly 2^17)
+ * on the current device and checks them (synchronous).  MOE_OK means the
+ * library executes here. */
 moe_status moe_selftest(void);
 
 #ifdef __cplusplus

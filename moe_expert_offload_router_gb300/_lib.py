@@ -81,6 +81,7 @@ _SIGS = {
                                  sz, vp, vp]),
     "moe_dequant_debug": (i32, [C.POINTER(moe_expert_views), i32, i32, i32, vp, vp]),
     "moe_set_option": (i32, [i32, i32, vp]),
+    "moe_fp4_mma_peak": (i32, [i32, vp, vp]),
     "moe_expert_forward_overlap_workspace": (sz, [C.POINTER(moe_expert_views), i32, i32]),
     "moe_expert_forward_overlap": (i32, [C.POINTER(moe_expert_views), vp, i32, i32, vp, vp, vp, vp, i32, vp,
                                          vp, vp, sz, vp, vp]),
@@ -453,6 +454,13 @@ def moe_set_option(option: int, value: int) -> int:
     old = C.c_int(0)
     _check(_lib.moe_set_option(option, value, C.byref(old)))
     return old.value
+
+
+def moe_fp4_mma_peak(iters: int = 4096, stream=None) -> float:
+    """Dense block-scaled FP4 tensor rate of this GPU (TFLOP/s), measured."""
+    v = C.c_double(0.0)
+    _check(_lib.moe_fp4_mma_peak(iters, C.byref(v), _s(stream)))
+    return v.value
 
 
 def moe_dequant_debug(views: moe_expert_views, pool: int, slot: int, matrix: int, out, stream=None):

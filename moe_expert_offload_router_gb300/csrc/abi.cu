@@ -740,8 +740,79 @@ moe_status moe_selftest(void) {
   }
   if ((st = moe_copy_missing(c, h_i + 4, h_i + 6, h_i[8], 0, nullptr, nullptr)) != MOE_OK) goto out;
   ST_CUDA(cudaMemcpy(h_slot_bytes, d_slots, S * B, cudaMemcpyDeviceToHost));
-  if (memcmp(h_slot_bytes, h_bank + 2 * B, B) != 0 || memcmp(h_slot_bytes + B, h_bank, B) != 0)
+  if (memcmp(h_slot_bytes, h_bank + 2 * B, B) != 0 || memcmp(h_slot_bytes + B, h_bank, B) != 0) {
     st = fail(MOE_ERR_CUDA, "selftest: copied slot bytes differ from the bank");
+    goto out;
+  }
+  {
+    // a tiny layer: H = 64, I = 32, two FP4 experts whose codes are all 1.0 with
+    // unit E8M0 scales, x = 1, router weights 1/4 and 3/4.  gate = up = 64 for
+    // every feature, h = SiLU(64) * 64 = 4096 (SiLU(64) rounds to 64 in fp32),
+    // every output 32 * 4096 = 2^17, exact at every step and in bf16.
+    const int FH = 64, FI = 32, FT = 1, FK = 2;
+    const size_t EB = fp4_bytes(FH, FI);
+    std::vector<uint8_t> ex(2 * EB);
+    size_t off = 0;
+    for (int m = 0; m < 3; ++m) {
+      const size_t n = (m == 2) ? FH : FI, kk = (m == 2) ? FI : FH;
+      for (size_t i = 0; i < n * kk / 2; ++i) ex[off + i] = 0x22;          // E2M1 1.0, both nibbles
+      for (size_t i = 0; i < n * kk / 32; ++i) ex[off + n * kk / 2 + i] = 127;  // E8M0 2^0
+      off += n * kk / 2 + n * kk / 32;
+    }
+    memcpy(ex.data() + EB, ex.data(), EB);
+    std::vector<uint16_t> xv(FH, (uint16_t)0x3f80);  // bf16 1.0
+    const int32_t hslots[FK] = {0, 1};
+    const float hw[FK] = {0.25f, 0.75f};
+    moe_expert_views v{};
+    v.H = FH;
+    v.I = FI;
+    v.fp4_num_slots = 2;
+    const size_t wsb = moe_expert_forward_workspace(&v, FT, FK);
+    uint8_t* d_ex = nullptr;
+    uint8_t* d_ws = nullptr;
+    uint16_t* d_x = nullptr;
+    uint16_t* d_y = nullptr;
+    int32_t* d_sl = nullptr;
+    float* d_fw = nullptr;
+    int32_t* d_err = nullptr;
+    uint16_t hy[FH];
+    int32_t herr = -1;
+    cudaError_t e = cudaMalloc(&d_ex, 2 * EB);
+    if (e == cudaSuccess) e = cudaMalloc(&d_ws, wsb);
+    if (e == cudaSuccess) e = cudaMalloc(&d_x, FH * 2);
+    if (e == cudaSuccess) e = cudaMalloc(&d_y, FH * 2);
+    if (e == cudaSuccess) e = cudaMalloc(&d_sl, sizeof hslots);
+    if (e == cudaSuccess) e = cudaMalloc(&d_fw, sizeof hw);
+    if (e == cudaSuccess) e = cudaMalloc(&d_err, sizeof herr);
+    if (e == cudaSuccess) e = cudaMemcpy(d_ex, ex.data(), 2 * EB, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(d_x, xv.data(), FH * 2, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(d_sl, hslots, sizeof hslots, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(d_fw, hw, sizeof hw, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+      st = cuda_fail(e, "selftest: forward buffers");
+    } else {
+      v.fp4_slots = d_ex;
+      st = moe_expert_forward(&v, d_x, FT, FK, d_sl, nullptr, d_fw, d_y, d_ws, wsb, d_err, 0);
+      if (st == MOE_OK) {
+        e = cudaMemcpy(hy, d_y, FH * 2, cudaMemcpyDeviceToHost);
+        if (e == cudaSuccess) e = cudaMemcpy(&herr, d_err, sizeof herr, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) {
+          st = cuda_fail(e, "selftest: forward read-back");
+        } else {
+          bool good = herr == 0;
+          for (int i = 0; i < FH; ++i) good = good && hy[i] == 0x4800;  // bf16 2^17
+          if (!good) st = fail(MOE_ERR_CUDA, "selftest: the tiny layer's output differs from 2^17");
+        }
+      }
+    }
+    cudaFree(d_ex);
+    cudaFree(d_ws);
+    cudaFree(d_x);
+    cudaFree(d_y);
+    cudaFree(d_sl);
+    cudaFree(d_fw);
+    cudaFree(d_err);
+  }
 out:
 #undef ST_CUDA
   if (c) moe_cache_destroy(c);

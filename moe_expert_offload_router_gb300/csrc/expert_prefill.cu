@@ -45,6 +45,7 @@ namespace moe {
 constexpr int kPfThreads = 512;   // 16 warps: 12 converters, raw producer, MMA, B producer, spare
 constexpr int kPfMT = 2;          // 128-row weight tiles per CTA (two TMEM accumulators)
 constexpr int kPfNMax = 256;      // rows per item (MMA N) of the item list
+constexpr int kMxNMax = 224;      // rows per item of the block-scaled FP4 path (two 224-column accumulators)
 constexpr int kPfKStep = 64;      // K elements per stage (128 bytes of bf16: one swizzle row)
 constexpr int kPfBox = 64;        // rows per TMA box of the B operand
 // Converter warps 0-11 form three groups of 128 threads; group g converts the
@@ -643,23 +644,371 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   }
 }
 
-// items: per slot, tiles of <= kPfNMax sorted rows
-__global__ void prefill_items_kernel(const int* offsets, int S, PfItem* items, int* n_items) {
+// ------------------------------------------- block-scaled FP4 (kind::mxf4) --
+// The A-quantised mode (activations quantised to MXFP4 by the OCP MX rule, as
+// the weights are): both operands are E2M1 codes with one E8M0 scale per 32
+// elements, multiplied by tcgen05.mma.kind::mxf4.block_scale.  The packed codes
+// go from global memory to shared memory by TMA (128-byte swizzle, 256 codes per
+// row and stage) with no conversion; the scale factors go to tensor memory.
+//
+// Tensor-memory layout of the scale factors (measured with a one-MMA probe on
+// sm_103a): the tensor core computes D rows 32 q .. 32 q + 31 in lane quadrant
+// q and takes their scales from that quadrant's lanes.  Per 128-K window (four
+// 32-element blocks, two K = 64 MMAs with scale-factor IDs 0 and 2) a 4-column
+// group holds, for A, row m's four block scales (bytes 0..3) in lane m, column
+// group + m / 32; for B, row n's in lane 32 q + n % 32, column group + n / 32 of
+// every quadrant q.
+constexpr int kMxThreads = 256;   // warp 0 TMA, warp 1 MMA, warps 4-7 scale factors; all 8 the epilogue
+constexpr int kMxStages = 3;      // shared-memory stages of codes
+constexpr int kMxSfSlots = 2;     // tensor-memory slots of scale factors (stage ks in slot ks % 2)
+constexpr int kMxKStage = 256;    // K elements per stage: one 128-byte row of packed codes
+constexpr int kMxATile = 128 * 128;
+constexpr int kMxAStage = 2 * kMxATile;
+constexpr int kMxBStage = 256 * 128;  // up to four 64-row boxes
+constexpr int kMxOffB = kMxStages * kMxAStage;
+constexpr int kMxOffBar = kMxOffB + kMxStages * kMxBStage;
+constexpr int kMxSmem = kMxOffBar + 256 + 1024;
+constexpr int kMxSfBase = 2 * kMxNMax;  // first scale-factor column (after the two accumulators)
+// per scale slot, 32 columns at kMxSfBase + 32 slot: A tile 0 (windows 0, 1) +0,
+// +4; A tile 1 +8, +12; B window 0 +16 .. +22, window 1 +24 .. +30
+static_assert(kMxSfBase + 32 * kMxSfSlots <= 512, "tensor memory columns");
+static_assert(kMxNMax % 32 == 0 && kMxNMax / 32 <= 8 && kMxNMax <= 256, "B scale columns per window");
+static_assert((2 * kMxStages + 1) * 8 + 8 <= 256, "barrier area");
+
+struct MxArgs {
+  int mode;            // 0: gate/up + SwiGLU, h quantised to MXFP4; 1: down
+  int K;               // reduction length (H or I)
+  int tiles;           // feature tiles per item
+  int H, I, S, P;
+  size_t B;            // bytes per expert
+  const uint8_t* sc0;  // E8M0 scales of w1 (mode 0) or w2 (mode 1) of slot 0 (slot s at + s * B)
+  const uint8_t* sc1;  // w3 scales (mode 0)
+  const uint8_t* bsc;  // E8M0 scales of the activation rows [P][K / 32] (sorted order)
+  const PfItem* items;
+  const int* n_items;
+  const int* perm;     // sorted position -> pair index (mode 1 output rows)
+  uint8_t* hq;         // mode 0 out: h codes [P][I / 2]
+  uint8_t* hsc;        // mode 0 out: h scales [P][I / 32]
+  float* o;            // mode 1 out: [P][H] by pair
+  int* err;
+};
+
+// One stage (K = 256) of both tiles: four K = 64 MMAs per tile, scale windows
+// 0 (IDs 0, 2) then 1 (IDs 0, 2); descriptors advance 32 bytes (+2) per MMA.
+__device__ __forceinline__ void mma_mx_stage(uint32_t d0, uint32_t d1, uint64_t a0, uint64_t a1, uint64_t b,
+                                             uint32_t id0, uint32_t id2, uint32_t sf, uint32_t acc, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b64 a, bb;\n\t.reg .b32 sa0, sa1, sb;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %8, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      // window 0
+      "add.u32 sa0, %7, 0;\n\tadd.u32 sa1, %7, 8;\n\tadd.u32 sb, %7, 16;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.block32 [%0], %2, %4, %5, [sa0], [sb], p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.block32 [%1], %3, %4, %5, [sa1], [sb], p;\n\t"
+      "add.s64 a, %2, 2;\n\tadd.s64 bb, %4, 2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.block32 [%0], a, bb, %6, [sa0], [sb], t;\n\t"
+      "add.s64 a, %3, 2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.block32 [%1], a, bb, %6, [sa1], [sb], t;\n\t"
+      // window 1
+      "add.u32 sa0, %7, 4;\n\tadd.u32 sa1, %7, 12;\n\tadd.u32 sb, %7, 24;\n\t"
+      "add.s64 a, %2, 4;\n\tadd.s64 bb, %4, 4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.block32 [%0], a, bb, %5, [sa0], [sb], t;\n\t"
+      "add.s64 a, %3, 4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.block32 [%1], a, bb, %5, [sa1], [sb], t;\n\t"
+      "add.s64 a, %2, 6;\n\tadd.s64 bb, %4, 6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.block32 [%0], a, bb, %6, [sa0], [sb], t;\n\t"
+      "add.s64 a, %3, 6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.block32 [%1], a, bb, %6, [sa1], [sb], t;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%9];\n\t}" ::"r"(d0),
+      "r"(d1), "l"(a0), "l"(a1), "l"(b), "r"(id0), "r"(id2), "r"(sf), "r"(acc), "r"(su32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+// Block-scaled FP4 grouped GEMM of one (item, feature tile): mode 0 computes
+// 128 features' gate (w1) and up (w3) rows over K = H and writes h = SiLU(gate)
+// * up quantised to MXFP4 along I; mode 1 computes 256 rows of w2 over K = I and
+// writes fp32 outputs per pair.
+__global__ void __launch_bounds__(kMxThreads, 1)
+    mxf4_gemm_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
+                     const __grid_constant__ CUtensorMap mB, MxArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* full = (uint64_t*)(sm + kMxOffBar);  // [kMxStages]: TMA bytes + four scale-factor warps
+  uint64_t* empty = full + kMxStages;             // [kMxStages]: the stage's MMAs completed
+  uint64_t* done = empty + kMxStages;
+  uint32_t* tmem_slot = (uint32_t*)(done + 1);
+  const int item_idx = blockIdx.x / a.tiles, tile = blockIdx.x % a.tiles;
+  if (item_idx >= *a.n_items) return;
+  const PfItem it = a.items[item_idx];
+  if (it.count < 1 || it.count > kMxNMax || it.slot < 0 || it.slot >= a.S || it.row0 < 0 ||
+      it.row0 + it.count > a.P) {  // the item kernel never produces these
+    if (threadIdx.x == 0) atomicCAS(a.err, 0, MOE_ERR_INVALID);
+    return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nk = a.K / kMxKStage;
+  const int sbytes = a.K / 32;  // scale bytes per row
+  const int n_mma = (it.count + 15) & ~15;
+  const int n_box = (it.count + 63) / 64;
+  const uint32_t b_bytes = (uint32_t)n_box * 64 * 128;
+  const int f0 = a.mode == 0 ? tile * 128 : tile * 256;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMxStages; ++s) {
+      mbar_init(&full[s], 1 + 4);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                 "r"(512));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      bool ok = true;
+      for (int ks = 0; ks < nk && ok; ++ks) {
+        const int s = ks % kMxStages, r = ks / kMxStages;
+        if (r > 0 && !(ok = mbar_wait_fast(&empty[s], (r - 1) & 1, a.err))) break;
+        uint8_t* ad = sm + s * kMxAStage;
+        uint8_t* bd = sm + kMxOffB + s * kMxBStage;
+        mbar_expect_tx(&full[s], kMxAStage + b_bytes);
+        const int x = ks * 128;  // byte column of the stage's codes (a multiple of 16)
+        if (a.mode == 0) {
+          tma_3d(ad, &mA0, x, f0, it.slot, &full[s]);
+          tma_3d(ad + kMxATile, &mA1, x, f0, it.slot, &full[s]);
+        } else {
+          tma_3d(ad, &mA0, x, f0, it.slot, &full[s]);
+          tma_3d(ad + kMxATile, &mA0, x, f0 + 128, it.slot, &full[s]);
+        }
+        for (int bx = 0; bx < n_box; ++bx) tma_2d(bd + bx * 64 * 128, &mB, x, it.row0 + bx * 64, &full[s]);
+      }
+      if (!ok) {  // let copies already issued land before the CTA can exit
+        const uint64_t t0 = gtimer();
+        while (gtimer() - t0 < 2000000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // MXF4 x MXF4 -> fp32, M = 128, N = n_mma, both operands K-major; scale
+    // factors E8M0; IDs 0 and 2 pick bytes 0-1 and 2-3 of a window's columns
+    const uint32_t idesc = (1u << 7) | (1u << 10) | ((uint32_t)(n_mma >> 3) << 17) | (1u << 23) |
+                           ((uint32_t)(128 >> 4) << 24);
+    const uint32_t id0 = idesc, id2 = idesc | (2u << 4) | (2u << 29);
+    bool ok = true;
+    for (int ks = 0; ks < nk && ok; ++ks) {
+      const int s = ks % kMxStages, r = ks / kMxStages;
+      ok = __all_sync(0xffffffffu, mbar_wait_fast(&full[s], r & 1, a.err));
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t ad0 = umma_desc_sw128(su32(sm + s * kMxAStage));
+      const uint64_t ad1 = umma_desc_sw128(su32(sm + s * kMxAStage + kMxATile));
+      const uint64_t bd = umma_desc_sw128(su32(sm + kMxOffB + s * kMxBStage));
+      mma_mx_stage(tmem, tmem + kMxNMax, ad0, ad1, bd, id0, id2, tmem + kMxSfBase + 32 * (ks % kMxSfSlots),
+                   ks != 0, &empty[s]);
+    }
+    mma_commit_elect(done);
+  } else if (warp >= 4) {
+    // scale factors: this warp's lane quadrant q (warp 4 + q may write only lanes 32 q .. 32 q + 31)
+    const int q = warp - 4;
+    const uint8_t* base_a = a.sc0 + (size_t)it.slot * a.B;
+    const uint8_t* sa0 = base_a + (size_t)(f0 + 32 * q + lane) * sbytes;
+    const uint8_t* sa1 = a.mode == 0 ? a.sc1 + (size_t)it.slot * a.B + (size_t)(f0 + 32 * q + lane) * sbytes
+                                     : base_a + (size_t)(f0 + 128 + 32 * q + lane) * sbytes;
+    const uint8_t* sb[kMxNMax / 32];
+#pragma unroll
+    for (int c = 0; c < kMxNMax / 32; ++c) {
+      const int n = 32 * c + lane;
+      sb[c] = a.bsc + (size_t)(it.row0 + (n < it.count ? n : 0)) * sbytes;  // rows past the item: any valid row
+    }
+    // a stage's scale words (per K window: A tile 0, A tile 1, B rows 32 c + lane)
+    // are loaded two stages ahead of their tensor-memory writes, through a ring
+    // of three register sets, so the loads' latency is off the per-stage path
+    struct Sf {
+      uint2 a0, a1, b[kMxNMax / 32];
+    };
+    auto load = [&](int ks, Sf& w) {
+      w.a0 = __ldg(reinterpret_cast<const uint2*>(sa0 + 8 * ks));  // x: window 0, y: window 1
+      w.a1 = __ldg(reinterpret_cast<const uint2*>(sa1 + 8 * ks));
+#pragma unroll
+      for (int c = 0; c < kMxNMax / 32; ++c) w.b[c] = __ldg(reinterpret_cast<const uint2*>(sb[c] + 8 * ks));
+    };
+    auto store = [&](int ks, const Sf& w) -> bool {
+      // the scale slot's previous stage (ks - kMxSfSlots) must have finished its
+      // MMAs, whose commit arrived on that stage's "empty" barrier.  This warp
+      // writes stage ks - 1's scales before stage ks's, and the MMAs of a stage
+      // wait for its scales, so that barrier is at most one phase behind.
+      const int p = ks - kMxSfSlots;
+      if (p >= 0 && !__all_sync(0xffffffffu, mbar_wait_fast(&empty[p % kMxStages], (p / kMxStages) & 1, a.err)))
+        return false;
+      uint32_t bw0[8], bw1[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        bw0[c] = c < kMxNMax / 32 ? w.b[c < kMxNMax / 32 ? c : 0].x : 0u;
+        bw1[c] = c < kMxNMax / 32 ? w.b[c < kMxNMax / 32 ? c : 0].y : 0u;
+      }
+      const uint32_t col = tmem + ((uint32_t)(32 * q) << 16) + kMxSfBase + 32 * (ks % kMxSfSlots);
+      tmem_st1(col + 0 + q, w.a0.x);
+      tmem_st1(col + 4 + q, w.a0.y);
+      tmem_st1(col + 8 + q, w.a1.x);
+      tmem_st1(col + 12 + q, w.a1.y);
+      tmem_st8(col + 16, bw0);
+      tmem_st8(col + 24, bw1);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[ks % kMxStages]);
+      return true;
+    };
+    Sf ring[3];
+    load(0, ring[0]);
+    if (nk > 1) load(1, ring[1]);
+    bool ok = true;
+    for (int k0 = 0; k0 < nk && ok; k0 += 3) {
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        const int ks = k0 + j;
+        if (ks >= nk || !ok) break;
+        if (ks + 2 < nk) load(ks + 2, ring[(j + 2) % 3]);
+        ok = store(ks, ring[j]);
+      }
+    }
+  }
+
+  // epilogue: all 8 warps.  Warp w reads TMEM lane quadrant w % 4 and the
+  // columns [64 (w / 4), 64 (w / 4) + 64) of each accumulator.
+  {
+    __syncwarp();
+    bool ok = mbar_wait(done, 0, a.err);
+    ok = __all_sync(0xffffffffu, ok);
+    __syncwarp();
+    tc_fence_after();
+    const int q = warp & 3, half = warp >> 2;
+    const int row = q * 32 + lane;
+    const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+    const int cb = half * (kMxNMax / 2), ce = min(cb + kMxNMax / 2, n_mma);
+    if (ok && a.mode == 0) {
+      // lane = feature f0 + row: gate (w1 row) in tile 0, up (w3 row) in tile 1
+      for (int c0 = cb; c0 < ce; c0 += 16) {
+        uint32_t vg[16], vu[16];
+        tmem_ld16(tq + (uint32_t)c0, vg);
+        tmem_ld16(tq + (uint32_t)(kMxNMax + c0), vu);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int col = c0 + j;
+          if (col >= it.count) break;  // the same for every lane of the warp
+          const float hg = 0.5f * __uint_as_float(vg[j]), up = __uint_as_float(vu[j]);
+          const float hv = fmaf(hg, tanh_approx(hg), hg) * up;
+          // the warp's 32 lanes hold 32 consecutive features of this column: one MX block
+          const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv)));
+          const uint32_t sbyte = mx_scale_byte(__uint_as_float(amax));
+          const uint32_t code = mx_code(hv, mx_inv_scale(sbyte));
+          // pack: byte b of the block = codes of lanes 2b (low nibble) and 2b + 1
+          const uint32_t pair = code | (__shfl_down_sync(0xffffffffu, code, 1) << 4);
+          const uint32_t b1 = __shfl_down_sync(0xffffffffu, pair, 2), b2 = __shfl_down_sync(0xffffffffu, pair, 4),
+                         b3 = __shfl_down_sync(0xffffffffu, pair, 6);
+          const size_t prow = (size_t)(it.row0 + col);
+          if ((lane & 7) == 0) {
+            const uint32_t word = (pair & 0xffu) | ((b1 & 0xffu) << 8) | ((b2 & 0xffu) << 16) | ((b3 & 0xffu) << 24);
+            *reinterpret_cast<uint32_t*>(a.hq + prow * (a.I / 2) + (f0 + 32 * q) / 2 + lane / 2) = word;
+          }
+          if (lane == 0) a.hsc[prow * (a.I / 32) + (f0 + 32 * q) / 32] = (uint8_t)sbyte;
+        }
+      }
+    } else if (ok) {
+      for (int mt = 0; mt < 2; ++mt) {
+        const int feat = f0 + 128 * mt + row;
+        for (int c0 = cb; c0 < ce; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tq + (uint32_t)(mt * kMxNMax + c0), v);
+          const int cl = c0 + (lane & 15);
+          const int pl = cl < it.count ? a.perm[it.row0 + cl] : 0;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int p = __shfl_sync(0xffffffffu, pl, j);
+            if (c0 + j < it.count) a.o[(size_t)p * a.H + feat] = __uint_as_float(v[j]);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
+  }
+}
+
+// One warp per sorted row: x of the pair's token quantised to MXFP4 (OCP MX,
+// 32-element blocks along H): packed codes (element 2j in the low nibble of
+// byte j) and one E8M0 scale byte per block.  Four lanes hold a block; H is a
+// multiple of 256, so every lane takes part in every step.
+__global__ void gather_mxq_kernel(const uint16_t* x, int H, int k, const int* perm, const int* offsets, int S,
+                                  uint8_t* xq, uint8_t* xsc) {
+  const int n = offsets[S];
+  const int lane = threadIdx.x & 31;
+  const int units = H / 8;
+  for (int i = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5); i < n;
+       i += (int)((gridDim.x * (size_t)blockDim.x) >> 5)) {
+    const int tok = perm[i] / k;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)tok * H);
+    for (int c = lane; c < units; c += 32) {
+      const uint4 v = src[c];
+      float f[8];
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        f[2 * qq] = __uint_as_float(w4[qq] << 16);
+        f[2 * qq + 1] = __uint_as_float(w4[qq] & 0xffff0000u);
+      }
+      float am = 0.f;
+#pragma unroll
+      for (int qq = 0; qq < 8; ++qq) am = fmaxf(am, fabsf(f[qq]));
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+      const uint32_t sbyte = mx_scale_byte(am);
+      const float inv = mx_inv_scale(sbyte);
+      uint32_t word = 0;
+#pragma unroll
+      for (int qq = 0; qq < 8; ++qq) word |= mx_code(f[qq], inv) << (4 * qq);
+      reinterpret_cast<uint32_t*>(xq + (size_t)i * (H / 2))[c] = word;
+      if ((lane & 3) == 0) xsc[(size_t)i * (H / 32) + c / 4] = (uint8_t)sbyte;
+    }
+  }
+}
+
+// items: per slot, tiles of <= nmax sorted rows
+__global__ void prefill_items_kernel(const int* offsets, int S, int nmax, PfItem* items, int* n_items) {
   __shared__ int ws[34];
   const int tid = threadIdx.x, NT = blockDim.x;
   const int per = (S + NT - 1) / NT;
   const int s0 = min(S, tid * per), s1 = min(S, s0 + per);
   int local = 0;
-  for (int s = s0; s < s1; ++s) local += (offsets[s + 1] - offsets[s] + kPfNMax - 1) / kPfNMax;
+  for (int s = s0; s < s1; ++s) local += (offsets[s + 1] - offsets[s] + nmax - 1) / nmax;
   int total;
   int pos = block_exclusive_scan(local, ws, &total);
   for (int s = s0; s < s1; ++s) {
     const int b = offsets[s], cnt = offsets[s + 1] - b;
-    for (int t = 0; t * kPfNMax < cnt; ++t) {
+    for (int t = 0; t * nmax < cnt; ++t) {
       PfItem itm;
       itm.slot = s;
-      itm.row0 = b + t * kPfNMax;
-      itm.count = min(kPfNMax, cnt - t * kPfNMax);
+      itm.row0 = b + t * nmax;
+      itm.count = min(nmax, cnt - t * nmax);
       itm.pad = 0;
       items[pos++] = itm;
     }
@@ -828,6 +1177,24 @@ static moe_status map_bf16_rows(CUtensorMap* m, const void* base, uint64_t cols,
   return MOE_OK;
 }
 
+// Byte maps with 128-byte swizzle for packed FP4 codes: box of 128 bytes (256
+// codes) by box_y rows.  Rank 3: (row bytes, rows, slots); rank 2: (row bytes, rows).
+static moe_status map_codes_sw128(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows,
+                                  uint64_t slots, uint64_t slot_stride, uint32_t box_y) {
+  auto fn = encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint32_t rank = slots ? 3 : 2;
+  cuuint64_t dims[3] = {row_bytes, rows, slots ? slots : 1};
+  cuuint64_t strides[2] = {row_bytes, slot_stride};
+  cuuint32_t box[3] = {128, box_y, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (FP4 codes) failed: %d", (int)r);
+  return MOE_OK;
+}
+
 moe_status group_pairs_multi(const int32_t* ids, int P, int E, int32_t* offsets, int32_t* perm, int32_t* d_error,
                              int* cnt_ws, cudaStream_t stream);
 size_t group_pairs_multi_ws(int P, int E);
@@ -841,14 +1208,14 @@ bool grouped_gemm_supported(const moe_expert_views* v) {
 
 size_t gg_index_bytes(int T, int k, int S) {
   const size_t P = (size_t)T * k;
-  const size_t max_items = (size_t)S + P / kPfNMax + 1;
+  const size_t max_items = (size_t)S + P / kMxNMax + 1;  // the smaller items (block-scaled FP4 path)
   return a256((S + 1) * 4) + a256(P * 4) + a256(max_items * sizeof(PfItem)) + a256(16) +
          a256(group_pairs_multi_ws((int)P, S)) + a256(P * 4);
 }
 
 void gg_carve_index(uint8_t* base, int T, int k, int S, GgBufs* b) {
   const size_t P = (size_t)T * k;
-  const size_t max_items = (size_t)S + P / kPfNMax + 1;
+  const size_t max_items = (size_t)S + P / kMxNMax + 1;
   size_t off = 0;
   b->offsets = (int*)(base + off);
   off += a256((S + 1) * 4);
@@ -870,7 +1237,7 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
   const size_t P = (size_t)T * k;
   moe_status st = group_pairs_multi(slots, (int)P, S, b.offsets, b.perm, d_error, b.cnt, stream);
   if (st != MOE_OK) return st;
-  prefill_items_kernel<<<1, 1024, 0, stream>>>(b.offsets, S, b.items, b.nitems);
+  prefill_items_kernel<<<1, 1024, 0, stream>>>(b.offsets, S, kPfNMax, b.items, b.nitems);
   if ((st = check_launch("prefill_items_kernel")) != MOE_OK) return st;
   {
     const int blocks = (int)std::min<size_t>((P + 7) / 8, 152 * 16);
@@ -961,6 +1328,86 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
     if ((st = check_launch("prefill_gemm_kernel (down)")) != MOE_OK) return st;
   }
   return MOE_OK;
+}
+
+// The A-quantised mode on the block-scaled FP4 MMA: x and h quantised to MXFP4
+// (OCP MX), codes and E8M0 scales straight into kind::mxf4.  Buffers: b.xg holds
+// the packed x codes [P][H/2], b.xg16 their scales [P][H/32], b.hs the packed h
+// codes [P][I/2] followed (256-aligned) by their scales [P][I/32].
+moe_status grouped_gemm_mxf4(const moe_expert_views* v, const uint16_t* x, int T, int k, const int32_t* slots,
+                             const GgBufs& b, int32_t* d_error, cudaStream_t stream) {
+  const int H = v->H, I = v->I, S = v->fp4_num_slots;
+  const size_t P = (size_t)T * k;
+  moe_status st = group_pairs_multi(slots, (int)P, S, b.offsets, b.perm, d_error, b.cnt, stream);
+  if (st != MOE_OK) return st;
+  prefill_items_kernel<<<1, 1024, 0, stream>>>(b.offsets, S, kMxNMax, b.items, b.nitems);
+  if ((st = check_launch("prefill_items_kernel")) != MOE_OK) return st;
+  uint8_t* xq = reinterpret_cast<uint8_t*>(b.xg);
+  uint8_t* xsc = reinterpret_cast<uint8_t*>(b.xg16);
+  uint8_t* hq = reinterpret_cast<uint8_t*>(b.hs);
+  uint8_t* hsc = hq + a256(P * (size_t)I / 2);
+  {
+    const int blocks = (int)std::min<size_t>((P + 7) / 8, 152 * 16);
+    gather_mxq_kernel<<<blocks, 256, 0, stream>>>(x, H, k, b.perm, b.offsets, S, xq, xsc);
+    if ((st = check_launch("gather_mxq_kernel")) != MOE_OK) return st;
+  }
+  const size_t B = fp4_bytes(H, I);
+  const uint8_t* pool = v->fp4_slots;
+  const size_t hi = (size_t)H * I;
+  const uint8_t* w1c = pool;
+  const uint8_t* w1s = pool + hi / 2;
+  const uint8_t* w3c = pool + (hi / 2 + hi / 32);
+  const uint8_t* w3s = w3c + hi / 2;
+  const uint8_t* w2c = pool + 2 * (hi / 2 + hi / 32);
+  const uint8_t* w2s = w2c + hi / 2;
+  CUtensorMap m1, m3, m2, mx, mh;
+  if ((st = map_codes_sw128(&m1, w1c, H / 2, I, S, B, 128)) != MOE_OK) return st;
+  if ((st = map_codes_sw128(&m3, w3c, H / 2, I, S, B, 128)) != MOE_OK) return st;
+  if ((st = map_codes_sw128(&m2, w2c, I / 2, H, S, B, 128)) != MOE_OK) return st;
+  if ((st = map_codes_sw128(&mx, xq, H / 2, P, 0, 0, 64)) != MOE_OK) return st;
+  if ((st = map_codes_sw128(&mh, hq, I / 2, P, 0, 0, 64)) != MOE_OK) return st;
+  {
+    cudaError_t e = cudaFuncSetAttribute(mxf4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(mxf4_gemm_kernel)");
+  }
+  const int max_items = (int)std::min<size_t>((size_t)S, P) + (int)(P / kMxNMax) + 1;
+  MxArgs ma{};
+  ma.H = H;
+  ma.I = I;
+  ma.S = S;
+  ma.P = (int)P;
+  ma.B = B;
+  ma.items = b.items;
+  ma.n_items = b.nitems;
+  ma.perm = b.perm;
+  ma.hq = hq;
+  ma.hsc = hsc;
+  ma.o = b.o;
+  ma.err = d_error;
+  // GEMM1: gate/up over K = H, 128 features (their w1 and w3 rows) per CTA
+  ma.mode = 0;
+  ma.K = H;
+  ma.tiles = I / 128;
+  ma.sc0 = w1s;
+  ma.sc1 = w3s;
+  ma.bsc = xsc;
+  {
+    ProfScope ps(MOE_K_GEMM_GATEUP, stream);
+    mxf4_gemm_kernel<<<max_items * ma.tiles, kMxThreads, kMxSmem, stream>>>(m1, m3, mx, ma);
+  }
+  if ((st = check_launch("mxf4_gemm_kernel (gate/up)")) != MOE_OK) return st;
+  // GEMM2: down over K = I, 256 output features per CTA
+  ma.mode = 1;
+  ma.K = I;
+  ma.tiles = H / 256;
+  ma.sc0 = w2s;
+  ma.sc1 = w2s;
+  ma.bsc = hsc;
+  {
+    ProfScope ps(MOE_K_GEMM_DOWN, stream);
+    mxf4_gemm_kernel<<<max_items * ma.tiles, kMxThreads, kMxSmem, stream>>>(m2, m2, mh, ma);
+  }
+  return check_launch("mxf4_gemm_kernel (down)");
 }
 
 // rank-2 byte map: (x: row bytes, y: rows)
@@ -1082,8 +1529,8 @@ moe_status prefill_forward(const moe_expert_views* v, const uint16_t* x, int T, 
   b.hs = (__nv_bfloat16*)(base + L.hs);
   b.o = (float*)(base + L.o);
   MOE_CUDA(cudaMemsetAsync(d_error, 0, sizeof(int32_t), stream));
-  moe_status st = grouped_gemm_fp4(v, x, T, k, slots, b, d_error, stream, DownParts(),
-                                   prec_mode == MOE_PREC_A_MXFP4 ? 1 : 0);
+  moe_status st = prec_mode == MOE_PREC_A_MXFP4 ? grouped_gemm_mxf4(v, x, T, k, slots, b, d_error, stream)
+                                                : grouped_gemm_fp4(v, x, T, k, slots, b, d_error, stream);
   if (st != MOE_OK) return st;
   {
     ProfScope ps(MOE_K_COMBINE, stream);
@@ -1094,6 +1541,120 @@ moe_status prefill_forward(const moe_expert_views* v, const uint16_t* x, int T, 
 }
 
 }  // namespace moe
+
+namespace moe {
+// Back-to-back kind::mxf4 MMAs (M = 128, N = 256, K = 64) from shared memory,
+// one CTA per SM, `iters` groups of four per CTA into one accumulator: the
+// block-scaled FP4 tensor rate this GPU sustains with no data movement.
+// Operands are E2M1 1.0 codes with unit scales; the one wait is bounded.
+__global__ void __launch_bounds__(128, 1) fp4_peak_kernel(int iters, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* A = sm;                // 128 rows x 128 bytes
+  uint8_t* Bm = sm + 128 * 128;   // 256 rows x 128 bytes
+  uint64_t* bar = (uint64_t*)(Bm + 256 * 128);
+  uint32_t* tslot = (uint32_t*)(bar + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < (128 + 256) * 128 / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(sm)[i] = make_uint4(0x22222222u, 0x22222222u, 0x22222222u, 0x22222222u);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tslot)), "r"(512));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  // unit scales (127) in the scale columns 256 .. 279 of every lane
+  {
+    const uint32_t u = 0x7f7f7f7fu;
+    const uint32_t v[8] = {u, u, u, u, u, u, u, u};
+    const uint32_t col = tmem + ((uint32_t)(32 * warp) << 16) + 256;
+    tmem_st8(col, v);
+    tmem_st8(col + 8, v);
+    tmem_st8(col + 16, v);
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) {
+    const uint32_t idesc = (1u << 7) | (1u << 10) | ((uint32_t)(256 >> 3) << 17) | (1u << 23) |
+                           ((uint32_t)(128 >> 4) << 24);
+    const uint32_t id2 = idesc | (2u << 4) | (2u << 29);
+    const uint64_t ad = umma_desc_sw128(su32(A)), bd = umma_desc_sw128(su32(Bm));
+    const uint32_t sf = tmem + 256;
+    for (int i = 0; i < iters; ++i) {
+      // four K = 64 MMAs into one accumulator (a K = 256 stage), no commit: the
+      // issue queue applies back-pressure
+      asm volatile(
+          "{\n\t.reg .pred e, t;\n\t.reg .b64 a, bb;\n\t.reg .b32 sb;\n\t"
+          "elect.sync _|e, 0xffffffff;\n\tsetp.eq.b32 t, 0, 0;\n\tadd.u32 sb, %4, 16;\n\t"
+          "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.block32 [%0], %1, %2, %5, [%4], [sb], t;\n\t"
+          "add.s64 a, %1, 2;\n\tadd.s64 bb, %2, 2;\n\t"
+          "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.block32 [%0], a, bb, %3, [%4], [sb], t;\n\t"
+          "add.s64 a, %1, 4;\n\tadd.s64 bb, %2, 4;\n\t"
+          "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.block32 [%0], a, bb, %5, [%4], [sb], t;\n\t"
+          "add.s64 a, %1, 6;\n\tadd.s64 bb, %2, 6;\n\t"
+          "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.block32 [%0], a, bb, %3, [%4], [sb], t;\n\t}" ::"r"(tmem),
+          "l"(ad), "l"(bd), "r"(id2), "r"(sf), "r"(idesc)
+          : "memory");
+    }
+    mma_commit_elect(bar);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, 0, err));
+    (void)ok;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
+  }
+  (void)lane;
+}
+}  // namespace moe
+
+extern "C" moe_status moe_fp4_mma_peak(int iters, double* tflops, cudaStream_t stream) {
+  moe::clear_error();
+  MOE_ARG(iters >= 64 && iters % 64 == 0 && tflops, "need iters a positive multiple of 64 and tflops non-null");
+  int dev = 0, sms = 0;
+  MOE_CUDA(cudaGetDevice(&dev));
+  MOE_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const size_t smem = (128 + 256) * 128 + 64 + 1024;
+  MOE_CUDA(cudaFuncSetAttribute(moe::fp4_peak_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  int* err = nullptr;
+  MOE_CUDA(cudaMallocAsync((void**)&err, sizeof(int), stream));
+  MOE_CUDA(cudaMemsetAsync(err, 0, sizeof(int), stream));
+  cudaEvent_t e0, e1;
+  MOE_CUDA(cudaEventCreate(&e0));
+  MOE_CUDA(cudaEventCreate(&e1));
+  moe::fp4_peak_kernel<<<sms, 128, smem, stream>>>(iters / 8, err);  // warm-up
+  MOE_CUDA(cudaEventRecord(e0, stream));
+  moe::fp4_peak_kernel<<<sms, 128, smem, stream>>>(iters, err);
+  MOE_CUDA(cudaEventRecord(e1, stream));
+  moe_status st = moe::check_launch("fp4_peak_kernel");
+  int h_err = 0;
+  if (st == MOE_OK) {
+    cudaError_t e = cudaEventSynchronize(e1);
+    if (e != cudaSuccess) st = moe::cuda_fail(e, "cudaEventSynchronize");
+  }
+  float ms = 0.f;
+  if (st == MOE_OK) cudaEventElapsedTime(&ms, e0, e1);
+  if (st == MOE_OK) cudaMemcpy(&h_err, err, sizeof(int), cudaMemcpyDeviceToHost);
+  cudaFreeAsync(err, stream);
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (st != MOE_OK) return st;
+  if (h_err) return moe::fail(MOE_ERR_TIMEOUT, "fp4 peak probe: a commit wait gave up");
+  // 4 MMAs of 2 * 128 * 256 * 64 flops per iteration and CTA
+  *tflops = (double)sms * iters * 4.0 * 2.0 * 128 * 256 * 64 / (ms * 1e-3) / 1e12;
+  return MOE_OK;
+}
 
 extern "C" size_t moe_expert_prefill_workspace(const moe_expert_views* v, int T, int k) {
   if (!v || T < 0 || k < 1) return 0;

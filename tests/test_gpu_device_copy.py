@@ -211,3 +211,30 @@ def test_layer_device_copy(wl, S, steps, full):
     else:
         assert ref_chunks == steps
     cache.close()
+
+
+def test_copy_missing_device_reports_bad_entries():
+    # an entry naming no key or no slot is not copied and sets d_error; the
+    # others are copied
+    M = load_lib()
+    S, L, E, B = 6, 1, 10, 4096
+    slots = torch.zeros(S * B, dtype=torch.uint8, device="cuda")
+    bank = torch.arange(L * E * B, dtype=torch.int64).remainder(253).to(torch.uint8).pin_memory()
+    cache = M.moe_cache(S, L, E, B, slots, bank)
+    keys = torch.tensor([3, E + 5, 7, 2], dtype=torch.int32, device="cuda")
+    sl = torch.tensor([0, 1, S + 3, 4], dtype=torch.int32, device="cuda")
+    cnt = torch.tensor([4], dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    M.moe_copy_missing_device(cache, keys, sl, cnt, d_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == M.MOE_ERR_INVALID
+    got = slots.cpu().numpy().reshape(S, B)
+    ref = bank.numpy().reshape(L * E, B)
+    assert np.array_equal(got[0], ref[3]) and np.array_equal(got[4], ref[2])
+    assert not got[1].any()                       # the entry with key E + 5 was skipped
+    err.zero_()
+    M.moe_copy_missing_device(cache, keys[:1], sl[:1], torch.ones(1, dtype=torch.int32, device="cuda"),
+                              d_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    cache.close()

@@ -199,3 +199,30 @@ def test_rms_carry():
     ref = rms_carry(F.bf16_to_f64(yb))
     got = F.bf16_to_f64(out.cpu().numpy().view(np.uint16))
     assert np.max(np.abs(got - ref) / np.abs(ref).clip(1e-30)) <= 2 ** -8
+
+
+@pytest.mark.parametrize("T", [4, 16, 64])
+def test_decode_paths_both_match_oracle(T):
+    # the warp-MMA kernels (the default up to 64 tokens) and, with them switched
+    # off, the CUDA-core GEMV (below 256 pairs) or the tcgen05 grouped GEMM
+    M = load_lib()
+    wl = configs.DECODE
+    P = Pools(M, wl, 24, shared=True)
+    rng = np.random.default_rng(300 + T)
+    slots, w = _route(rng, T, wl.k, 24)
+    x = gen.activations(wl, 0, 8, T)
+    sample = sorted(set([0, T - 1, T // 3]))
+    ref = P.reference(x, slots, None, w, tokens=sample)
+    old = M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, 64)
+    try:
+        y_mma, err = P.forward(x, slots, None, w)
+        assert err == 0
+        M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, 0)
+        y_other, err = P.forward(x, slots, None, w)
+        assert err == 0
+    finally:
+        M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, old)
+    assert bf16_rel_err(y_mma[sample], ref) <= TOL
+    assert bf16_rel_err(y_other[sample], ref) <= TOL
+    with pytest.raises(M.MoeError):
+        M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, -1)

@@ -114,3 +114,13 @@ def test_prefill_mxfp4_mode_full_size_sampled():
     rows = [0, 1, 350, 699]
     ref = moe_layer(x, slots, w.astype(np.float64), weights, tokens=rows, quant=mx_round)
     assert bf16_rel_err(y[rows], ref) <= TOL
+
+
+def test_fp4_mma_peak_probe():
+    # back-to-back kind::mxf4 MMAs: a dense block-scaled FP4 rate well above the
+    # bf16 tensor rate of the same GPU
+    M = load_lib()
+    tf = M.moe_fp4_mma_peak(1024)
+    assert 2000.0 < tf < 30000.0
+    with pytest.raises(M.MoeError):
+        M.moe_fp4_mma_peak(100)
