@@ -189,3 +189,37 @@ def test_model_catches_an_unguarded_short_ring():
     assert hits > 0
     for seed in range(20):
         run_model(32, stages, ring, True, seed, "lifo")
+
+
+@pytest.mark.parametrize("stages,ring", [(3, 4), (3, 6)])
+def test_four_converter_groups_lap_a_three_stage_operand_ring(stages, ring):
+    # A 20-warp variant of the kernel (four converter groups) faulted the GPU on
+    # the wide shape (three operand stages).  The model shows why: with four
+    # groups over three stages a stage is filled by a different group each
+    # round, so a fast group reaches its next step on a stage while the group
+    # of the round in between has not filled it yet; its parity wait on that
+    # stage's "empty" barrier passes a round early, it overwrites operands the
+    # MMA has not read and arrives on "full" in the wrong phase.  With three
+    # groups (each group always fills the same stage) every wait is exact.
+    hits = 0
+    for nk in (8, 32, 64):
+        for seed in range(10):
+            for strategy in ("uniform", "starve"):
+                try:
+                    run_model(nk, stages, ring, ring % 4 != 0 and ring < stages + 4, seed, strategy, groups=4)
+                except ProtocolError as e:
+                    assert "empty" in str(e) and "early" in str(e)
+                    hits += 1
+    assert hits > 0
+    for nk in (8, 32, 64):
+        for seed in range(4):
+            run_model(nk, stages, ring, _kernel_guard(ring, stages), seed, "starve", groups=3)
+
+
+@pytest.mark.parametrize("stages,ring", [(4, 4), (4, 8)])
+def test_four_converter_groups_with_four_stages_are_exact(stages, ring):
+    # as many operand stages as groups: each group owns its stage again
+    for nk in (1, 5, 32, 64):
+        for seed in range(4):
+            for strategy in ("uniform", "lifo", "starve"):
+                run_model(nk, stages, ring, ring % 4 != 0 and ring < stages + 4, seed, strategy, groups=4)
