@@ -902,31 +902,43 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
     const int cb = half * (kMxNMax / 2), ce = min(cb + kMxNMax / 2, n_mma);
     if (ok && a.mode == 0) {
-      // lane = feature f0 + row: gate (w1 row) in tile 0, up (w3 row) in tile 1
+      // lane = feature f0 + row: gate (w1 row) in tile 0, up (w3 row) in tile 1.
+      // The 16 columns of a chunk go through each step together (independent
+      // warp reductions and shuffles), so their latencies overlap.
+      uint8_t* hq_base = a.hq + (size_t)(f0 + 32 * q) / 2 + lane / 2;
+      uint8_t* hsc_base = a.hsc + (size_t)(f0 + 32 * q) / 32;
       for (int c0 = cb; c0 < ce; c0 += 16) {
         uint32_t vg[16], vu[16];
         tmem_ld16(tq + (uint32_t)c0, vg);
         tmem_ld16(tq + (uint32_t)(kMxNMax + c0), vu);
+        float hv[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float hg = 0.5f * __uint_as_float(vg[j]), up = __uint_as_float(vu[j]);
+          hv[j] = fmaf(hg, tanh_approx(hg), hg) * up;
+        }
+        // the warp's 32 lanes hold 32 consecutive features of a column: one MX block
+        uint32_t am[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) am[j] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv[j])));
+        uint32_t code[16], sbyte[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          sbyte[j] = mx_scale_byte(__uint_as_float(am[j]));
+          code[j] = mx_code(hv[j], mx_inv_scale(sbyte[j]));
+        }
+        uint32_t hi[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) hi[j] = __shfl_down_sync(0xffffffffu, code[j], 1);
+        // byte b of the block = codes of lanes 2b (low nibble) and 2b + 1
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int col = c0 + j;
-          if (col >= it.count) break;  // the same for every lane of the warp
-          const float hg = 0.5f * __uint_as_float(vg[j]), up = __uint_as_float(vu[j]);
-          const float hv = fmaf(hg, tanh_approx(hg), hg) * up;
-          // the warp's 32 lanes hold 32 consecutive features of this column: one MX block
-          const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv)));
-          const uint32_t sbyte = mx_scale_byte(__uint_as_float(amax));
-          const uint32_t code = mx_code(hv, mx_inv_scale(sbyte));
-          // pack: byte b of the block = codes of lanes 2b (low nibble) and 2b + 1
-          const uint32_t pair = code | (__shfl_down_sync(0xffffffffu, code, 1) << 4);
-          const uint32_t b1 = __shfl_down_sync(0xffffffffu, pair, 2), b2 = __shfl_down_sync(0xffffffffu, pair, 4),
-                         b3 = __shfl_down_sync(0xffffffffu, pair, 6);
-          const size_t prow = (size_t)(it.row0 + col);
-          if ((lane & 7) == 0) {
-            const uint32_t word = (pair & 0xffu) | ((b1 & 0xffu) << 8) | ((b2 & 0xffu) << 16) | ((b3 & 0xffu) << 24);
-            *reinterpret_cast<uint32_t*>(a.hq + prow * (a.I / 2) + (f0 + 32 * q) / 2 + lane / 2) = word;
+          if (col < it.count) {
+            const size_t prow = (size_t)(it.row0 + col);
+            if ((lane & 1) == 0) hq_base[prow * (a.I / 2)] = (uint8_t)(code[j] | (hi[j] << 4));
+            if (lane == 0) hsc_base[prow * (a.I / 32)] = (uint8_t)sbyte[j];
           }
-          if (lane == 0) a.hsc[prow * (a.I / 32) + (f0 + 32 * q) / 32] = (uint8_t)sbyte;
         }
       }
     } else if (ok) {
