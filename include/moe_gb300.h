@@ -530,15 +530,23 @@ moe_status moe_expert_forward_noalloc(const moe_expert_views* v, const uint16_t*
                                       uint16_t* y, int32_t* d_error, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
- * Process-wide tuning option (not on the pages).  MOE_OPT_MMA_MAX_TOKENS:
+ * Process-wide tuning options (not on the pages).  MOE_OPT_MMA_MAX_TOKENS:
  * decode calls of 2 up to this many tokens run their FP4 and shared-expert
- * pairs on the warp-level tensor-core kernels (default 64; 0 = never); larger
- * ones take the tcgen05 grouped GEMM from 256 pairs, and the CUDA-core GEMV
- * below that (and at one token).  The previous value goes to *old_value (may be null).
- * MOE_ERR_INVALID for an unknown option or a negative value.  Set it between
- * calls, not while another thread issues forward calls.
+ * pairs on the tensor cores in decode-sized groups (default 64; 0 = never);
+ * larger ones take the tcgen05 grouped GEMM from 256 pairs, and the CUDA-core
+ * GEMV below that (and at one token).  MOE_OPT_MX8_MIN_TOKENS: of those
+ * calls, the ones with at least this many tokens use the block-scaled
+ * tcgen05 GEMM (tcgen05.mma.kind::mxf8f6f4: E2M1 weights as stored, the
+ * activations and h split into two E4M3 terms with a power-of-two scale per
+ * 32 elements, which holds a bf16 value exactly but for subnormal low terms),
+ * the others the warp-level kernels (mma.sync); 0 = never.  It needs H a
+ * multiple of 256, I of 128, fp4_slots 32-byte and x 8-byte aligned, and
+ * falls back to the warp-level kernels otherwise.  The previous value goes to
+ * *old_value (may be null).  MOE_ERR_INVALID for an unknown option or a
+ * negative value.  Set them between calls, not while another thread issues
+ * forward calls.
  * ------------------------------------------------------------------------- */
-enum { MOE_OPT_MMA_MAX_TOKENS = 0 };
+enum { MOE_OPT_MMA_MAX_TOKENS = 0, MOE_OPT_MX8_MIN_TOKENS = 1 };
 moe_status moe_set_option(int option, int value, int* old_value);
 
 /* Diagnostic (not on the pages): the block-scaled FP4 tensor rate of this GPU.

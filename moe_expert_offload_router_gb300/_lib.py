@@ -447,6 +447,7 @@ def moe_mx_quantize(x, codes, scales, stream=None):
 
 
 MOE_OPT_MMA_MAX_TOKENS = 0
+MOE_OPT_MX8_MIN_TOKENS = 1
 
 
 def moe_set_option(option: int, value: int) -> int:

@@ -1,0 +1,618 @@
+// Block-scaled tensor-core GEMMs of the decode forward: the grouped expert
+// MLP of decode batches (up to 64 tokens per expert) on
+// tcgen05.mma.kind::mxf8f6f4 with no weight conversion at all.
+//
+// "Running DeepSeek-V4-Flash across four free GPUs", section "What the expert
+// cache actually does" (the grouped expert GEMM over the slot views); "An
+// elephant through a straw", section "Rig, model & methodology" (MXFP4
+// experts: E2M1 codes with one E8M0 scale per 32 weights; one FP8 shared
+// expert).
+//
+// The A operand is the expert's weight rows as stored in the slot pool: TMA
+// copies the packed E2M1 codes with the 16U4_ALIGN16B element type, which
+// lays 16 codes into each 16-byte unit of shared memory (8 bytes of codes, 8
+// bytes of gap), the operand layout the tensor core reads E2M1 from, and the
+// rows' E8M0 block scales go to tensor memory as the MMA's A scale factors.
+// The FP8 shared expert's E4M3 rows load as bytes with a unit A scale; its
+// per-row fp32 scales multiply the accumulators.  The B operand is the
+// activations, each 32-element block along K scaled by a power of two and
+// carried as two E4M3 terms hi + lo (mx.cuh); a bf16 input is held exactly in
+// all but subnormal-lo cases, so the products are those of the bf16 path.
+// For items of up to 48 tokens the hi and lo rows of a stage stack into one
+// B operand of 2n rows (one MMA per K slice, the accumulator's two halves
+// added in the epilogue); larger items issue an MMA for each.
+//
+// Persistent CTA (384 threads, one per SM), items = (token group, feature
+// tile) drawn in a fixed stride, tensor-memory accumulators double-buffered
+// so an item's epilogue overlaps the next item's main loop:
+//   warp 0      TMA producer: two 128-row A tiles and the group's hi/lo rows
+//               per 128-element K stage, four stages deep
+//   warp 1      TMEM allocation; MMA issue (one elected lane, one asm block
+//               per stage), commits to the stage's "empty" barrier and, after
+//               the item's last stage, to the accumulator's "full" barrier
+//   warps 4-7   scale factors: each writes its TMEM lane quadrant's A and B
+//               scale words of a stage, two stages of loads ahead
+//   warps 8-11  epilogue: gate/up -> h = SiLU(gate) * up, itself split into
+//               E4M3 hi/lo with a scale per 32 features (the down GEMM's B
+//               operand, in the same sorted row order); down -> fp32 rows of
+//               o per pair for the router-weighted combine
+// Every mbarrier wait gives up after one second and records MOE_ERR_TIMEOUT.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "grouped_gemm.cuh"
+#include "mx.cuh"
+#include "tcgen05.cuh"
+
+namespace moe {
+
+constexpr int kM8Threads = 384;
+constexpr int kM8Stages = 4;
+constexpr int kM8KStage = 128;                  // K elements per stage: one 128-byte swizzled row
+constexpr int kM8ATile = 128 * 128;             // one 128-row A tile of a stage in shared memory
+constexpr int kM8BBytes = 2 * kMx8MaxRows * 128;  // hi rows, then lo rows
+constexpr int kM8Stage = 2 * kM8ATile + kM8BBytes;
+constexpr int kM8OffBar = kM8Stages * kM8Stage;
+constexpr int kM8Smem = kM8OffBar + 256 + 1024;
+constexpr int kM8StackMax = 48;                 // items up to this many rows stack hi and lo in one B operand
+constexpr int kM8AccCols = 96;                  // TMEM columns per accumulator (2 * 48, or 64 unstacked)
+constexpr int kM8SfBase = 4 * kM8AccCols;       // two buffers of two accumulators, then the scale factors
+constexpr int kM8SfCols = 16;                   // per stage: A tile 0 +0..3, A tile 1 +4..7, B +8..10
+static_assert(kM8SfBase + kM8Stages * kM8SfCols <= 512, "tensor memory columns");
+static_assert(kM8Smem <= 232448, "shared memory per CTA");
+static_assert(2 * kM8StackMax <= kM8AccCols && kMx8MaxRows <= kM8AccCols, "accumulator width");
+static_assert((2 * kM8Stages + 4) * 8 + 8 <= 256, "barrier area");
+
+struct Mx8Args {
+  int mode;          // 0: gate/up + SwiGLU -> h hi/lo; 1: down -> o
+  int K;             // H (mode 0) or I (mode 1)
+  int H, I, T, P;
+  int tiles;         // feature tiles per group: I / 128 (mode 0) or H / 256 (mode 1)
+  int max_groups;    // capacity of the group list
+  const uint8_t* fp4;
+  int n4;
+  size_t b4;         // bytes per FP4 expert
+  size_t sc0, sc1;   // byte offsets of the A tiles' E8M0 scales in an expert (mode 0: w1, w3; mode 1: w2)
+  const uint8_t* shared;
+  const float* rs0;  // shared expert row scales: w1 (mode 0) or w2 (mode 1)
+  const float* rs1;  // w3 (mode 0)
+  const uint8_t* bsc;  // B scale bytes [P + T][K / 32]
+  const int* hdr;      // [0] groups, [1] routed groups (the shared expert's follow)
+  const Group* groups;
+  const int* perm;     // sorted position -> pair index
+  uint8_t* hhi;        // mode 0 out: [P + T][I] E4M3 hi, lo, and scale bytes [P + T][I / 32]
+  uint8_t* hlo;
+  uint8_t* hsc;
+  float* o;            // mode 1 out: [P + T][H] (row = pair index, or P + token for the shared expert)
+  int* err;
+};
+
+struct M8Item {
+  bool run;          // a group this kernel computes
+  bool fp8;          // the shared expert
+  int slot, begin, count, brow0, f0, n16;
+};
+
+// Item it of the list: groups in the order shared expert first, then routed;
+// tile fastest.  2-bit groups belong to the CUDA-core kernels and are skipped;
+// a group the plan never produces is skipped and flagged (by warp 1 only).
+__device__ __forceinline__ M8Item m8_item(const Mx8Args& a, int it, int ng, int nr, bool flag) {
+  M8Item r;
+  r.run = false;
+  const int gi = it / a.tiles, tile = it % a.tiles;
+  const Group g = a.groups[(nr + gi) % ng];
+  r.fp8 = g.pool == MOE_POOL_SHARED;
+  r.slot = g.slot;
+  r.begin = g.begin;
+  r.count = g.count;
+  r.f0 = a.mode == 0 ? tile * 128 : tile * 256;
+  r.n16 = (g.count + 15) & ~15;
+  if (g.pool == MOE_POOL_INT2) return r;
+  bool ok = g.count >= 1 && g.count <= kMx8MaxRows && g.begin >= 0;
+  if (r.fp8) {
+    ok = ok && a.shared != nullptr && g.begin + g.count <= a.T;
+    r.brow0 = a.P + g.begin;
+  } else {
+    ok = ok && g.pool == MOE_POOL_FP4 && g.slot >= 0 && g.slot < a.n4 && g.begin + g.count <= a.P;
+    r.brow0 = g.begin;
+  }
+  if (!ok) {
+    if (flag) atomicCAS(a.err, 0, MOE_ERR_INVALID);
+    return r;
+  }
+  r.run = true;
+  return r;
+}
+
+// Four K = 32 slices of one stage for both accumulators, from one elected
+// lane: with STACK one MMA per slice and tile (B = hi rows then lo rows),
+// else two (hi, then lo into the same accumulator).  Slice j advances the
+// descriptors 32 bytes and selects byte j of the scale-factor words (the
+// A and B scale-factor IDs of the instruction descriptor).
+template <bool STACK>
+__device__ __forceinline__ void m8_stage(uint32_t d0, uint32_t d1, uint64_t a0, uint64_t a1, uint64_t bh,
+                                         uint64_t bl, uint32_t idesc, uint32_t sfa0, uint32_t sfa1, uint32_t sfb,
+                                         uint32_t acc, uint64_t* bar) {
+#define M8_MMA(D, A, B, ID, SFA, P) \
+  "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.block32 [" D "], " A ", " B ", " ID ", [" SFA "], [%9], " P ";\n\t"
+#define M8_SLICE(OFF, IDOFF, P)                                                                              \
+  "add.s64 a, %2, " OFF ";\n\tadd.s64 c, %3, " OFF ";\n\tadd.s64 bb, %4, " OFF ";\n\tadd.s64 bo, %5, " OFF \
+  ";\n\tadd.u32 id, %6, " IDOFF ";\n\t" M8_MMA("%0", "a", "bb", "id", "%7", P)                              \
+  M8_LO("%0", "a", "%7") M8_MMA("%1", "c", "bb", "id", "%8", P) M8_LO("%1", "c", "%8")
+  if (STACK) {
+#define M8_LO(D, A, SFA) ""
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b64 a, c, bb, bo;\n\t.reg .b32 id;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %10, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t" M8_SLICE("0", "0", "p")
+            M8_SLICE("2", "536870928", "t") M8_SLICE("4", "1073741856", "t") M8_SLICE("6", "1610612784", "t")
+                "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%11];\n\t}" ::"r"(d0),
+        "r"(d1), "l"(a0), "l"(a1), "l"(bh), "l"(bl), "r"(idesc), "r"(sfa0), "r"(sfa1), "r"(sfb), "r"(acc),
+        "r"(su32(bar))
+        : "memory");
+#undef M8_LO
+  } else {
+#define M8_LO(D, A, SFA) M8_MMA(D, A, "bo", "id", SFA, "t")
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b64 a, c, bb, bo;\n\t.reg .b32 id;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %10, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t" M8_SLICE("0", "0", "p")
+            M8_SLICE("2", "536870928", "t") M8_SLICE("4", "1073741856", "t") M8_SLICE("6", "1610612784", "t")
+                "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%11];\n\t}" ::"r"(d0),
+        "r"(d1), "l"(a0), "l"(a1), "l"(bh), "l"(bl), "r"(idesc), "r"(sfa0), "r"(sfa1), "r"(sfb), "r"(acc),
+        "r"(su32(bar))
+        : "memory");
+#undef M8_LO
+  }
+#undef M8_SLICE
+#undef M8_MMA
+}
+// The immediates above are j * (2^29 + 2^4) for j = 1, 2, 3: the A scale-factor
+// ID (bits 29-30) and the B scale-factor ID (bits 4-5) both set to j.
+static_assert(536870928u == (1u << 29) + (1u << 4) && 1610612784u == 3u * ((1u << 29) + (1u << 4)),
+              "scale-factor ID immediates");
+
+__device__ __forceinline__ uint32_t ldg_u32(const uint8_t* p) { return __ldg(reinterpret_cast<const uint32_t*>(p)); }
+
+__global__ void __launch_bounds__(kM8Threads, 1)
+    mx8_gemm_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
+                    const __grid_constant__ CUtensorMap mS0, const __grid_constant__ CUtensorMap mS1,
+                    const __grid_constant__ CUtensorMap mBh, const __grid_constant__ CUtensorMap mBl, Mx8Args a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* full = (uint64_t*)(sm + kM8OffBar);  // [kM8Stages]: TMA bytes + the four scale-factor warps
+  uint64_t* empty = full + kM8Stages;             // [kM8Stages]: the stage's MMAs completed
+  uint64_t* accf = empty + kM8Stages;             // [2]: an accumulator's item finished
+  uint64_t* acce = accf + 2;                      // [2]: the epilogue has read an accumulator
+  uint64_t* drain = acce + 2;
+  uint32_t* tmem_slot = (uint32_t*)(drain + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nk = a.K / kM8KStage;
+
+  int ng = a.hdr[0], nr = a.hdr[1];
+  if (ng < 0 || ng > a.max_groups || nr < 0 || nr > ng) {
+    if (threadIdx.x == 0) atomicCAS(a.err, 0, MOE_ERR_INVALID);
+    ng = 0;
+  }
+  const int n_items = ng * a.tiles;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kM8Stages; ++s) {
+      mbar_init(&full[s], 1 + 4);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf[b], 1);
+      mbar_init(&acce[b], 4);
+    }
+    mbar_init(drain, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                 "r"(512));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      bool ok = true;
+      uint32_t gs = 0;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const M8Item m = m8_item(a, it, ng, nr, false);
+        if (!m.run) continue;
+        const int nbx = m.n16 / 16;
+        const uint32_t bytes = (m.fp8 ? 2u * kM8ATile : (uint32_t)kM8ATile) + 2u * (uint32_t)nbx * 2048u;
+        const int row1 = a.mode == 0 ? m.f0 : m.f0 + 128;
+        for (int ks = 0; ks < nk; ++ks, ++gs) {
+          const int s = gs % kM8Stages;
+          const uint32_t r = gs / kM8Stages;
+          if (r > 0 && !(ok = mbar_wait_fast(&empty[s], (r - 1) & 1, a.err))) break;
+          uint8_t* st = sm + s * kM8Stage;
+          mbar_expect_tx(&full[s], bytes);
+          const int x = ks * kM8KStage;  // element coordinate: 64 (FP4) or 128 (E4M3) bytes, 16-byte multiples
+          if (m.fp8) {
+            tma_2d(st, &mS0, x, m.f0, &full[s]);
+            tma_2d(st + kM8ATile, &mS1, x, row1, &full[s]);
+          } else {
+            tma_3d(st, &mA0, x, m.f0, m.slot, &full[s]);
+            tma_3d(st + kM8ATile, &mA1, x, row1, m.slot, &full[s]);
+          }
+          uint8_t* bd = st + 2 * kM8ATile;
+          for (int bx = 0; bx < nbx; ++bx) {
+            tma_2d(bd + bx * 2048, &mBh, x, m.brow0 + 16 * bx, &full[s]);
+            tma_2d(bd + (nbx + bx) * 2048, &mBl, x, m.brow0 + 16 * bx, &full[s]);
+          }
+        }
+      }
+      if (!ok) {  // let copies already issued land before the CTA can exit
+        const uint64_t t0 = gtimer();
+        while (gtimer() - t0 < 2000000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    bool ok = true;
+    uint32_t gs = 0, i = 0;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const M8Item m = m8_item(a, it, ng, nr, true);
+      if (!m.run) continue;
+      const int b = i & 1;
+      const uint32_t u = i >> 1;
+      ++i;
+      if (u > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait_fast(&acce[b], (u - 1) & 1, a.err)))) break;
+      tc_fence_after();
+      const bool stack = m.n16 <= kM8StackMax;
+      const int n_mma = stack ? 2 * m.n16 : m.n16;
+      // E2M1 (5) or E4M3 (0) A, E4M3 B, fp32 D, K-major both, E8M0 scales, M = 128
+      const uint32_t idesc = ((m.fp8 ? 0u : 5u) << 7) | ((uint32_t)(n_mma >> 3) << 17) | (1u << 23) |
+                             ((uint32_t)(128 >> 4) << 24);
+      const uint32_t d0 = tmem + (uint32_t)(b * 2 * kM8AccCols), d1 = d0 + kM8AccCols;
+      for (int ks = 0; ks < nk; ++ks, ++gs) {
+        const int s = gs % kM8Stages;
+        const uint32_t r = gs / kM8Stages;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait_fast(&full[s], r & 1, a.err)))) break;
+        tc_fence_after();
+        uint8_t* st = sm + s * kM8Stage;
+        const uint64_t ad0 = umma_desc_sw128(su32(st)), ad1 = umma_desc_sw128(su32(st + kM8ATile));
+        const uint64_t bh = umma_desc_sw128(su32(st + 2 * kM8ATile));
+        const uint64_t bl = umma_desc_sw128(su32(st + 2 * kM8ATile + m.n16 * 128));
+        const uint32_t sf = tmem + kM8SfBase + kM8SfCols * s;
+        if (stack)
+          m8_stage<true>(d0, d1, ad0, ad1, bh, bl, idesc, sf, sf + 4, sf + 8, ks != 0, &empty[s]);
+        else
+          m8_stage<false>(d0, d1, ad0, ad1, bh, bl, idesc, sf, sf + 4, sf + 8, ks != 0, &empty[s]);
+      }
+      if (ok) mma_commit_elect(&accf[b]);
+    }
+    // every MMA this warp issued has completed before tensor memory is freed
+    mma_commit_elect(drain);
+    __syncwarp();
+    mbar_wait(drain, 0, a.err);
+  } else if (warp >= 4 && warp < 8) {
+    // scale factors of lane quadrant q: A row 32 q + lane of each tile at
+    // column +q of its 4-column group; B rows 32 c + lane at column +8 + c
+    const int q = warp - 4;
+    const int sbytes = a.K / 32;
+    bool ok = true;
+    uint32_t gs = 0;
+    struct Sf {
+      uint32_t a0, a1, b[3];
+    };
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const M8Item m = m8_item(a, it, ng, nr, false);
+      if (!m.run) continue;
+      const bool stack = m.n16 <= kM8StackMax;
+      const uint8_t* sa0 = nullptr;
+      const uint8_t* sa1 = nullptr;
+      if (!m.fp8) {
+        const uint8_t* e = a.fp4 + (size_t)m.slot * a.b4;
+        const int r0 = m.f0 + 32 * q + lane, r1 = (a.mode == 0 ? m.f0 : m.f0 + 128) + 32 * q + lane;
+        sa0 = e + a.sc0 + (size_t)r0 * sbytes;
+        sa1 = e + a.sc1 + (size_t)r1 * sbytes;
+      }
+      const uint8_t* sb[3];
+#pragma unroll
+      for (int c = 0; c < 3; ++c) {
+        int tk = 32 * c + lane;
+        if (stack && tk >= m.n16) tk -= m.n16;
+        if (tk >= m.count) tk = 0;  // columns past the group: any valid row
+        sb[c] = a.bsc + (size_t)(m.brow0 + tk) * sbytes;
+      }
+      auto load = [&](int ks, Sf& w) {
+        w.a0 = m.fp8 ? 0x7f7f7f7fu : ldg_u32(sa0 + 4 * ks);
+        w.a1 = m.fp8 ? 0x7f7f7f7fu : ldg_u32(sa1 + 4 * ks);
+#pragma unroll
+        for (int c = 0; c < 3; ++c) w.b[c] = ldg_u32(sb[c] + 4 * ks);
+      };
+      auto store = [&](const Sf& w) -> bool {
+        const int s = gs % kM8Stages;
+        const uint32_t r = gs / kM8Stages;
+        // the slot's previous stage (gs - kM8Stages) must have finished its MMAs
+        if (r > 0 && !__all_sync(0xffffffffu, mbar_wait_fast(&empty[s], (r - 1) & 1, a.err))) return false;
+        const uint32_t col = tmem + ((uint32_t)(32 * q) << 16) + kM8SfBase + kM8SfCols * s;
+        tmem_st1(col + q, w.a0);
+        tmem_st1(col + 4 + q, w.a1);
+        tmem_st1(col + 8, w.b[0]);
+        tmem_st1(col + 9, w.b[1]);
+        tmem_st1(col + 10, w.b[2]);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
+        ++gs;
+        return true;
+      };
+      Sf ring[3];
+      load(0, ring[0]);
+      if (nk > 1) load(1, ring[1]);
+      for (int k0 = 0; k0 < nk && ok; k0 += 3) {
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+          const int ks = k0 + j;
+          if (ks >= nk || !ok) break;
+          if (ks + 2 < nk) load(ks + 2, ring[(j + 2) % 3]);
+          ok = store(ring[j]);
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    const int q = warp - 8;
+    bool ok = true;
+    uint32_t i = 0;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const M8Item m = m8_item(a, it, ng, nr, false);
+      if (!m.run) continue;
+      const int b = i & 1;
+      const uint32_t u = i >> 1;
+      ++i;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait_fast(&accf[b], u & 1, a.err)))) break;
+      tc_fence_after();
+      const bool stack = m.n16 <= kM8StackMax;
+      const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 2 * kM8AccCols);
+      const uint32_t lo_off = stack ? (uint32_t)m.n16 : 0u;
+      // accumulator columns c0 .. c0 + 15 of tile t (hi + lo halves when stacked)
+      auto acc16 = [&](int t, int c0, float* v) {
+        uint32_t r[16];
+        tmem_ld16(tq + (uint32_t)(t * kM8AccCols + c0), r);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+        if (stack) {
+          tmem_ld16(tq + (uint32_t)(t * kM8AccCols + c0) + lo_off, r);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(r[j]);
+        }
+      };
+      if (a.mode == 0) {
+        const int f = m.f0 + 32 * q + lane;  // this lane's feature
+        const float rg = m.fp8 ? a.rs0[f] : 1.f, ru = m.fp8 ? a.rs1[f] : 1.f;
+        uint8_t* hi_base = a.hhi + f;
+        uint8_t* lo_base = a.hlo + f;
+        uint8_t* sc_base = a.hsc + (m.f0 + 32 * q) / 32;
+        for (int c0 = 0; c0 < m.n16; c0 += 16) {
+          float g[16], up[16];
+          acc16(0, c0, g);
+          acc16(1, c0, up);
+          float hv[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float hg = 0.5f * (g[j] * rg);
+            hv[j] = fmaf(hg, tanh_approx(hg), hg) * (up[j] * ru);
+          }
+          // a warp's 32 lanes are 32 consecutive features: one scale block of h
+          uint32_t sbyte[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const uint32_t am = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv[j])));
+            sbyte[j] = mx8_scale_byte(__uint_as_float(am));
+            hv[j] *= __uint_as_float((254u - sbyte[j]) << 23);
+          }
+#pragma unroll
+          for (int j = 0; j < 16; j += 2) {
+            uint32_t hi, lo;
+            mx8_split2(hv[j], hv[j + 1], hi, lo);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int col = c0 + j + e;
+              if (col < m.count) {
+                const size_t row = (size_t)(m.brow0 + col);
+                hi_base[row * a.I] = (uint8_t)(hi >> (8 * e));
+                lo_base[row * a.I] = (uint8_t)(lo >> (8 * e));
+                if (lane == 0) sc_base[row * (a.I / 32)] = (uint8_t)sbyte[j + e];
+              }
+            }
+          }
+        }
+      } else {
+        const int fa = m.f0 + 32 * q + lane, fb = fa + 128;
+        const float ra = m.fp8 ? a.rs0[fa] : 1.f, rb = m.fp8 ? a.rs0[fb] : 1.f;
+        for (int c0 = 0; c0 < m.n16; c0 += 16) {
+          float v0[16], v1[16];
+          acc16(0, c0, v0);
+          acc16(1, c0, v1);
+          const int cl = c0 + (lane & 15);
+          const int pl = cl < m.count ? (m.fp8 ? a.P + m.begin + cl : a.perm[m.begin + cl]) : 0;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int p = __shfl_sync(0xffffffffu, pl, j);
+            if (c0 + j < m.count) {
+              float* orow = a.o + (size_t)p * a.H;
+              orow[fa] = v0[j] * ra;
+              orow[fb] = v1[j] * rb;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce[b]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
+  }
+}
+
+// ------------------------------------------------------------------- host --
+
+// Packed E2M1 codes of one matrix over every slot: (x: K codes, y: rows,
+// z: slots), 16U4_ALIGN16B (16 codes per 16 bytes of shared memory), 128-byte
+// swizzle, box of 128 codes by 128 rows.
+static moe_status map_fp4_rows(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint64_t slots,
+                               uint64_t slot_stride) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[3] = {K, rows, slots};
+  cuuint64_t strides[2] = {K / 2, slot_stride};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (FP4 rows) failed: %d", (int)r);
+  return MOE_OK;
+}
+
+// Byte rows (E4M3): (x: K bytes, y: rows), 128-byte swizzle, box of 128 bytes by box_rows.
+static moe_status map_u8_rows(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint32_t box_rows) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[2] = {K, rows};
+  cuuint64_t strides[1] = {K};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (E4M3 rows) failed: %d", (int)r);
+  return MOE_OK;
+}
+
+static int mx8_sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+bool mx8_supported(const moe_expert_views* v) {
+  // 128-element K stages and feature tiles; 256-row down tiles; the 16U4
+  // element type needs 32-byte aligned bases and row strides
+  if (v->H % 256 != 0 || v->I % 128 != 0) return false;
+  const bool fp4 = v->fp4_slots != nullptr && v->fp4_num_slots > 0;
+  if (fp4 && ((uintptr_t)v->fp4_slots & 31) != 0) return false;
+  if (v->shared && ((uintptr_t)v->shared & 15) != 0) return false;
+  return fp4 || v->shared != nullptr;
+}
+
+size_t mx8_bytes(int H, int I, int rows) {
+  auto a = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  return 2 * a((size_t)rows * H) + a((size_t)rows * H / 32) + 2 * a((size_t)rows * I) + a((size_t)rows * I / 32);
+}
+
+void mx8_carve(uint8_t* base, int H, int I, int rows, Mx8Bufs* b) {
+  auto a = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  size_t off = 0;
+  b->xhi = base + off;
+  off += a((size_t)rows * H);
+  b->xlo = base + off;
+  off += a((size_t)rows * H);
+  b->xsc = base + off;
+  off += a((size_t)rows * H / 32);
+  b->hhi = base + off;
+  off += a((size_t)rows * I);
+  b->hlo = base + off;
+  off += a((size_t)rows * I);
+  b->hsc = base + off;
+}
+
+moe_status mx8_gemm(const moe_expert_views* v, int mode, int T, int k, bool shared, int max_groups,
+                    const int* hdr, const Group* groups, const int* perm, const Mx8Bufs& b, float* o,
+                    int32_t* d_error, cudaStream_t stream) {
+  const int H = v->H, I = v->I, P = T * k;
+  const size_t b4 = fp4_bytes(H, I);
+  const size_t codes_hi = (size_t)I * H / 2, scales_hi = (size_t)I * H / 32;  // one w1 or w3 matrix
+  const size_t off_w3 = codes_hi + scales_hi, off_w2 = 2 * off_w3;
+  const size_t f8_mat = (size_t)I * H + (size_t)I * 4;  // one shared w1 or w3 matrix (codes + row scales)
+  const uint8_t* sh = shared ? v->shared : nullptr;
+  const int rows = P + T;
+  Mx8Args a;
+  a.mode = mode;
+  a.K = mode == 0 ? H : I;
+  a.H = H;
+  a.I = I;
+  a.T = T;
+  a.P = P;
+  a.tiles = mode == 0 ? I / 128 : H / 256;
+  a.max_groups = max_groups;
+  a.fp4 = v->fp4_slots;
+  a.n4 = v->fp4_slots ? v->fp4_num_slots : 0;
+  a.b4 = b4;
+  a.sc0 = mode == 0 ? codes_hi : off_w2 + (size_t)H * I / 2;
+  a.sc1 = mode == 0 ? off_w3 + codes_hi : a.sc0;
+  a.shared = sh;
+  a.rs0 = sh ? reinterpret_cast<const float*>(sh + (mode == 0 ? (size_t)I * H : 2 * f8_mat + (size_t)H * I))
+             : nullptr;
+  a.rs1 = sh ? reinterpret_cast<const float*>(sh + f8_mat + (size_t)I * H) : nullptr;
+  a.bsc = mode == 0 ? b.xsc : b.hsc;
+  a.hdr = hdr;
+  a.groups = groups;
+  a.perm = perm;
+  a.hhi = b.hhi;
+  a.hlo = b.hlo;
+  a.hsc = b.hsc;
+  a.o = o;
+  a.err = d_error;
+
+  CUtensorMap mA0, mA1, mS0, mS1, mBh, mBl;
+  moe_status st;
+  const int S = a.n4;
+  if (a.fp4 && S > 0) {
+    if (mode == 0) {
+      if ((st = map_fp4_rows(&mA0, a.fp4, H, I, S, b4)) != MOE_OK) return st;
+      if ((st = map_fp4_rows(&mA1, a.fp4 + off_w3, H, I, S, b4)) != MOE_OK) return st;
+    } else {
+      if ((st = map_fp4_rows(&mA0, a.fp4 + off_w2, I, H, S, b4)) != MOE_OK) return st;
+      mA1 = mA0;
+    }
+  }
+  if (sh) {
+    if (mode == 0) {
+      if ((st = map_u8_rows(&mS0, sh, H, I, 128)) != MOE_OK) return st;
+      if ((st = map_u8_rows(&mS1, sh + f8_mat, H, I, 128)) != MOE_OK) return st;
+    } else {
+      if ((st = map_u8_rows(&mS0, sh + 2 * f8_mat, I, H, 128)) != MOE_OK) return st;
+      mS1 = mS0;
+    }
+  }
+  if (!a.fp4 || S == 0) {
+    mA0 = mS0;
+    mA1 = mS1;
+  }
+  if (!sh) {
+    mS0 = mA0;
+    mS1 = mA1;
+  }
+  if ((st = map_u8_rows(&mBh, mode == 0 ? b.xhi : b.hhi, a.K, rows, 16)) != MOE_OK) return st;
+  if ((st = map_u8_rows(&mBl, mode == 0 ? b.xlo : b.hlo, a.K, rows, 16)) != MOE_OK) return st;
+
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(mx8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kM8Smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(mx8_gemm_kernel)");
+    attr_set = true;
+  }
+  const long long items = (long long)max_groups * a.tiles;
+  const int grid = (int)std::max(1LL, std::min<long long>(mx8_sm_count(), items));
+  mx8_gemm_kernel<<<grid, kM8Threads, kM8Smem, stream>>>(mA0, mA1, mS0, mS1, mBh, mBl, a);
+  return check_launch(mode == 0 ? "mx8_gemm_kernel (gate/up)" : "mx8_gemm_kernel (down)");
+}
+
+}  // namespace moe

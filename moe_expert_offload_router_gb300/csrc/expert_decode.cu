@@ -32,6 +32,7 @@
 
 #include "common.cuh"
 #include "grouped_gemm.cuh"
+#include "mx.cuh"
 
 namespace moe {
 
@@ -42,13 +43,10 @@ constexpr int kRowsDown = 64;     // rows of w2 per down work item
 constexpr int kMaxPlanPairs = 4096;
 constexpr int kGemmMinPairs = 256;  // from here on the FP4 routed pairs take the tcgen05 grouped GEMM
 
-struct Group {
-  int pool, slot, begin, count;
-};
-
 struct FwdLayout {
-  size_t hdr, perm, groups, xsig, xs, h, o, hs16, hsig, gg, total;
-  bool gemm;  // the FP4 routed pairs may take the grouped GEMM
+  size_t hdr, perm, groups, xsig, xs, h, o, hs16, hsig, gg, mx8, total;
+  bool gemm;     // the FP4 routed pairs may take the grouped GEMM
+  bool mx8_ok;   // room for the block-scaled decode GEMM's operands
 };
 
 static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -80,6 +78,9 @@ static FwdLayout fwd_layout(const moe_expert_views* v, int T, int k) {
   L.gemm = (long long)P >= kGemmMinPairs && grouped_gemm_supported(v);
   L.gg = off;
   if (L.gemm) off = align256(off + gg_index_bytes(T, k, v->fp4_num_slots));
+  L.mx8_ok = T >= 2 && T <= kMx8MaxRows && mx8_supported(v);
+  L.mx8 = off;
+  if (L.mx8_ok) off = align256(off + mx8_bytes(H, I, (int)P + T));
   L.total = off;
   return L;
 }
@@ -111,6 +112,11 @@ struct FwdArgs {
   float* o;
   __half* hs16;  // h in fp16, row r scaled by 2^-hsig[r] (warp-MMA down kernel)
   int* hsig;
+  // block-scaled decode GEMM: E4M3 hi/lo activation rows in sorted order and
+  // their scale bytes, written by the plan (null: not this path)
+  uint8_t* xhi;
+  uint8_t* xlo;
+  uint8_t* xsc;
 };
 
 // ------------------------------------------------------------------ decode --
@@ -480,8 +486,69 @@ __device__ __forceinline__ int group_size(const FwdArgs& a, int pool) {
   return (a.mma_group > 0 && pool >= 0 && pool < 31 && ((a.gemv_skip >> pool) & 1)) ? a.mma_group : kG;
 }
 
+// Sort key of pair p: (pool, slot, p) for a pair the kernels compute, ~0 for
+// one they leave out (slot < 0 or a dropped tag), ~0 - 1 for a bad slot or tag.
+__device__ __forceinline__ unsigned long long plan_key(const FwdArgs& a, int p) {
+  const int sl = a.slots[p];
+  const int tag = a.tags ? (int)a.tags[p] : MOE_TAG_FP4;
+  if (sl < 0 || tag == MOE_TAG_DROP) return ~0ull;
+  const int pool = tag == MOE_TAG_INT2 ? MOE_POOL_INT2 : MOE_POOL_FP4;
+  const int npool = pool == MOE_POOL_FP4 ? a.n4 : a.n2;
+  if ((tag == MOE_TAG_FP4 || tag == MOE_TAG_INT2) && sl < npool)
+    return ((unsigned long long)((unsigned)pool << 30 | (unsigned)sl) << 32) | (unsigned)p;
+  return ~0ull - 1;
+}
+
+// Token t's activations as E4M3 hi/lo with a power-of-two scale per 32
+// elements (mx.cuh), written to the rows of its FP4 pairs in the sorted order
+// (a pair's row is the number of kept keys below its own, the position the
+// sort of block 0 gives it) and to row P + t for the shared expert.
+__device__ void plan_mx8_rows(const FwdArgs& a, int t, int* dst) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int j = warp; j < a.k; j += (int)(blockDim.x >> 5)) {
+    const int p = t * a.k + j;
+    const unsigned long long key = plan_key(a, p);
+    int below = 0;
+    for (int q = lane; q < a.P; q += 32) below += plan_key(a, q) < key;
+    below = __reduce_add_sync(0xffffffffu, below);
+    if (lane == 0) dst[j] = (key < ~0ull - 1 && (key >> 62) == MOE_POOL_FP4) ? below : -1;
+  }
+  if (threadIdx.x == 0) dst[a.k] = a.shared ? a.P + t : -1;
+  __syncthreads();
+  const uint16_t* xr = a.x + (size_t)t * a.H;
+  // 8 threads per 32-element block, 4 elements each (H is a multiple of 256,
+  // so every warp is either whole or idle in each pass)
+  for (int e0 = 4 * threadIdx.x; e0 < a.H; e0 += 4 * blockDim.x) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(xr + e0);
+    float f[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u), __uint_as_float(raw.y << 16),
+                  __uint_as_float(raw.y & 0xffff0000u)};
+    float am = fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3])));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
+    const uint32_t sb = mx8_scale_byte(am);
+    const float inv = __uint_as_float((254u - sb) << 23);
+    uint32_t h01, l01, h23, l23;
+    mx8_split2(f[0] * inv, f[1] * inv, h01, l01);
+    mx8_split2(f[2] * inv, f[3] * inv, h23, l23);
+    const uint32_t hw = h01 | (h23 << 16), lw = l01 | (l23 << 16);
+    for (int d = 0; d <= a.k; ++d) {
+      const int row = dst[d];
+      if (row < 0) continue;
+      *reinterpret_cast<uint32_t*>(a.xhi + (size_t)row * a.H + e0) = hw;
+      *reinterpret_cast<uint32_t*>(a.xlo + (size_t)row * a.H + e0) = lw;
+      if ((threadIdx.x & 7) == 0) a.xsc[(size_t)row * (a.H / 32) + e0 / 32] = (uint8_t)sb;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(1024) plan_kernel(FwdArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
+  if (blockIdx.x > 0 && a.xhi) {
+    plan_mx8_rows(a, blockIdx.x - 1, reinterpret_cast<int*>(smem_raw + 256));
+    if (!a.tags) return;  // the fp16 copy below serves only the 2-bit pairs' CUDA-core kernels then
+    __syncthreads();
+  }
   if (blockIdx.x > 0) {
     // activation prep for token t
     float* red = reinterpret_cast<float*>(smem_raw);
@@ -510,20 +577,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(FwdArgs a) {
   if (tid == 0) scal[0] = 0;
   __syncthreads();
   for (int p = tid; p < NP; p += NT) {
-    unsigned long long key = ~0ull;
-    if (p < P) {
-      const int sl = a.slots[p];
-      const int tag = a.tags ? (int)a.tags[p] : MOE_TAG_FP4;
-      if (sl >= 0 && tag != MOE_TAG_DROP) {
-        const int pool = tag == MOE_TAG_INT2 ? MOE_POOL_INT2 : MOE_POOL_FP4;
-        const int npool = pool == MOE_POOL_FP4 ? a.n4 : a.n2;
-        if ((tag == MOE_TAG_FP4 || tag == MOE_TAG_INT2) && sl < npool) {
-          if (!a.routed_gemm)
-            key = ((unsigned long long)((unsigned)pool << 30 | (unsigned)sl) << 32) | (unsigned)p;
-        } else {
-          scal[0] = 1;
-        }
-      }
+    unsigned long long key = p < P ? plan_key(a, p) : ~0ull;
+    if (key == ~0ull - 1) {
+      scal[0] = 1;
+      key = ~0ull;
     }
     keys[p] = key;
   }
@@ -1106,6 +1163,9 @@ static bool mma_supported(const moe_expert_views* v) {
 // take the tcgen05 grouped GEMM (moe_set_option).
 static int g_mma_max_tokens = 64;
 constexpr int kMmaMinTokens = 2;
+// Of those, batches from this many tokens take the block-scaled tcgen05 GEMM
+// (decode_mx8.cu) instead of the warp-MMA kernels (moe_set_option).
+static int g_mx8_min_tokens = 2;
 
 static moe_status validate_views(const moe_expert_views* v) {
   MOE_ARG(v != nullptr, "views is null");
@@ -1177,7 +1237,15 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
   // token tiles per group: one up to 8 tokens, else two (with four tiles per
   // group only two chunk buffers fit the registers, which measured slower)
   const int mma_nb = T <= 8 ? 1 : 2;
-  a.mma_group = mma ? 8 * mma_nb : 0;
+  // the block-scaled tcgen05 GEMM: groups of up to 64 tokens (one per expert
+  // at these batch sizes); the plan reads x rows with 8-byte loads
+  const bool mx8 = mma && L.mx8_ok && g_mx8_min_tokens > 0 && T >= g_mx8_min_tokens && ((uintptr_t)x & 7) == 0;
+  a.mma_group = mma ? (mx8 ? kMx8MaxRows : 8 * mma_nb) : 0;
+  Mx8Bufs mb{};
+  if (mx8) mx8_carve(base + L.mx8, v->H, v->I, a.P + T, &mb);
+  a.xhi = mx8 ? mb.xhi : nullptr;
+  a.xlo = mx8 ? mb.xlo : nullptr;
+  a.xsc = mx8 ? mb.xsc : nullptr;
   a.hdr = (int*)(base + L.hdr);
   a.perm = (int*)(base + L.perm);
   a.groups = (Group*)(base + L.groups);
@@ -1234,7 +1302,12 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
   }
 
   const long long max_groups = (long long)T * k + (T + kG - 1) / kG + 1;
-  if (mma) {
+  if (mx8) {
+    ProfScope ps(MOE_K_GATEUP, stream);
+    if ((st = mx8_gemm(v, 0, T, k, a.shared != nullptr, (int)max_groups, a.hdr, a.groups, a.perm, mb, a.o, d_error,
+                       stream)) != MOE_OK)
+      return st;
+  } else if (mma) {
     auto launch = [&](auto kernel) -> moe_status {
       moe_status s2 = set_smem(kernel, kMmaSmem);
       if (s2 != MOE_OK) return s2;
@@ -1265,7 +1338,12 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
   // the down kernels read every slot's matrices: they wait for the last part
   if (gemv && pass.down.n >= 1 && pass.down.ready && pass.down.ready[pass.down.n - 1])
     MOE_CUDA(cudaStreamWaitEvent(stream, pass.down.ready[pass.down.n - 1], 0));
-  if (mma) {
+  if (mx8) {
+    ProfScope ps(MOE_K_DOWN, stream);
+    if ((st = mx8_gemm(v, 1, T, k, a.shared != nullptr, (int)max_groups, a.hdr, a.groups, a.perm, mb, a.o, d_error,
+                       stream)) != MOE_OK)
+      return st;
+  } else if (mma) {
     {
       // h rows in fp16 with a power-of-two scale each (routed pairs and shared rows)
       const int rows = a.P + (a.shared ? T : 0);
@@ -1573,10 +1651,11 @@ extern "C" moe_status moe_expert_forward_noalloc(const moe_expert_views* v, cons
 
 extern "C" moe_status moe_set_option(int option, int value, int* old_value) {
   clear_error();
-  MOE_ARG(option == MOE_OPT_MMA_MAX_TOKENS, "unknown option %d", option);
+  MOE_ARG(option == MOE_OPT_MMA_MAX_TOKENS || option == MOE_OPT_MX8_MIN_TOKENS, "unknown option %d", option);
   MOE_ARG(value >= 0, "option value must be >= 0");
-  if (old_value) *old_value = g_mma_max_tokens;
-  g_mma_max_tokens = value;
+  int& slot = option == MOE_OPT_MMA_MAX_TOKENS ? g_mma_max_tokens : g_mx8_min_tokens;
+  if (old_value) *old_value = slot;
+  slot = value;
   return MOE_OK;
 }
 

@@ -38,6 +38,7 @@
 
 #include "common.cuh"
 #include "grouped_gemm.cuh"
+#include "tcgen05.cuh"
 #include "mx.cuh"
 
 namespace moe {
@@ -89,32 +90,6 @@ using PfBig = PfCfg<256, 4, 3>;
 using PfSmall = PfCfg<64, 8, 4>;
 using PfShared = PfCfg<64, 12, 3>;  // FP8 shared expert: 16 KB raw stages, so a deeper ring
 
-__device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-      "[%5];" ::"r"(su32(dst)),
-      "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(su32(bar))
-      : "memory");
-}
-__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          su32(dst)),
-      "l"((uint64_t)map), "r"(x), "r"(y), "r"(su32(bar))
-      : "memory");
-}
-
-// UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row atoms 1024 B apart.
-__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
-  d |= (uint64_t)1 << 16;                  // leading byte offset (unused for swizzled K-major)
-  d |= (uint64_t)(1024 >> 4) << 32;        // stride byte offset
-  d |= (uint64_t)1 << 46;                  // descriptor version
-  d |= (uint64_t)2 << 61;                  // 128-byte swizzle
-  return d;
-}
-
 // kind::f16 instruction descriptor: D fp32, A and B both bf16 (or both fp16),
 // both K-major, M = 128.
 __device__ __forceinline__ uint32_t idesc_16bit(int n, bool bf16) {
@@ -144,29 +119,6 @@ __device__ __forceinline__ void mma_kstep_2x4(uint32_t d0, uint32_t d1, uint64_t
       "r"(d1), "l"(a0), "l"(a1), "l"(b), "r"(acc), "r"(idesc), "r"(su32(bar))
       : "memory");
 }
-__device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(su32(bar))
-      : "memory");
-}
-__device__ __forceinline__ float tanh_approx(float x) {
-  float y;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 // Eight E2M1 codes (one 32-bit word, element 2j in the low nibble of byte j)
 // -> four 16-bit pairs times the block scale: the word is split into its four
 // bytes by one mov, each byte converted by cvt.rn.f16x2.e2m1x2.
@@ -723,15 +675,6 @@ __device__ __forceinline__ void mma_mx_stage(uint32_t d0, uint32_t d1, uint64_t 
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
-}
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
-               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-               : "memory");
-}
-
 // Block-scaled FP4 grouped GEMM of one (item, feature tile): mode 0 computes
 // 128 features' gate (w1) and up (w3) rows over K = H and writes h = SiLU(gate)
 // * up quantised to MXFP4 along I; mode 1 computes 256 rows of w2 over K = I and
@@ -1143,7 +1086,7 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const float* o, co
 
 // ------------------------------------------------------------------- host --
 
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -1160,7 +1103,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // rank-3 byte map: (x: row bytes, y: rows, z: slots)
 static moe_status map_bytes3(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint64_t slots,
                              uint64_t slot_stride, uint32_t box_x, uint32_t box_y) {
-  auto fn = encode_fn();
+  auto fn = tensor_map_encoder();
   if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   cuuint64_t dims[3] = {row_bytes, rows, slots};
   cuuint64_t strides[2] = {row_bytes, slot_stride};
@@ -1176,7 +1119,7 @@ static moe_status map_bytes3(CUtensorMap* m, const void* base, uint64_t row_byte
 // rank-2 16-bit map (bf16 or fp16) with 128-byte swizzle, box 64 x kPfBox
 static moe_status map_bf16_rows(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
                                 CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
-  auto fn = encode_fn();
+  auto fn = tensor_map_encoder();
   if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
@@ -1193,7 +1136,7 @@ static moe_status map_bf16_rows(CUtensorMap* m, const void* base, uint64_t cols,
 // codes) by box_y rows.  Rank 3: (row bytes, rows, slots); rank 2: (row bytes, rows).
 static moe_status map_codes_sw128(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows,
                                   uint64_t slots, uint64_t slot_stride, uint32_t box_y) {
-  auto fn = encode_fn();
+  auto fn = tensor_map_encoder();
   if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   const cuuint32_t rank = slots ? 3 : 2;
   cuuint64_t dims[3] = {row_bytes, rows, slots ? slots : 1};
@@ -1425,7 +1368,7 @@ moe_status grouped_gemm_mxf4(const moe_expert_views* v, const uint16_t* x, int T
 // rank-2 byte map: (x: row bytes, y: rows)
 static moe_status map_bytes2(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_x,
                              uint32_t box_y) {
-  auto fn = encode_fn();
+  auto fn = tensor_map_encoder();
   if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   cuuint64_t dims[2] = {row_bytes, rows};
   cuuint64_t strides[1] = {row_bytes};

@@ -9,6 +9,12 @@
 
 namespace moe {
 
+// A run of one slot's (or the shared expert's) pairs in the decode forward's
+// sorted order: begin is the first sorted position (routed) or token (shared).
+struct Group {
+  int pool, slot, begin, count;
+};
+
 struct PfItem {
   int slot, row0, count, pad;
 };
@@ -51,5 +57,31 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
 moe_status grouped_gemm_shared_fp8(const moe_expert_views* v, const __half* xs, const int* xsig, int T,
                                    __nv_bfloat16* hs, float* o, int o_row0, int32_t* d_error,
                                    cudaStream_t stream);
+
+// ------------------------------------------------ block-scaled decode GEMM --
+// Decode batches on tcgen05.mma.kind::mxf8f6f4 (decode_mx8.cu): E2M1 weights
+// straight from the slot pool, activations as E4M3 hi + lo with a power-of-two
+// scale per 32 elements.  Groups of up to kMx8MaxRows tokens.
+constexpr int kMx8MaxRows = 64;
+
+// Activation and h operands, rows in the plan's sorted order (routed pairs at
+// their sorted position, the shared expert's tokens at P + t).
+struct Mx8Bufs {
+  uint8_t* xhi;  // [rows][H] E4M3
+  uint8_t* xlo;
+  uint8_t* xsc;  // [rows][H / 32] E8M0
+  uint8_t* hhi;  // [rows][I]
+  uint8_t* hlo;
+  uint8_t* hsc;  // [rows][I / 32]
+};
+
+bool mx8_supported(const moe_expert_views* v);
+size_t mx8_bytes(int H, int I, int rows);
+void mx8_carve(uint8_t* base, int H, int I, int rows, Mx8Bufs* b);
+// mode 0: gate/up over the plan's groups (hdr, groups, perm) -> h operands in b;
+// mode 1: down -> o rows (pair index, or P + token for the shared expert).
+moe_status mx8_gemm(const moe_expert_views* v, int mode, int T, int k, bool shared, int max_groups,
+                    const int* hdr, const Group* groups, const int* perm, const Mx8Bufs& b, float* o,
+                    int32_t* d_error, cudaStream_t stream);
 
 }  // namespace moe
