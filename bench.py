@@ -68,8 +68,11 @@ def _args():
                    help="decode: other workloads measured in the same run and reported under their own keys "
                         "(comma list of prefill, ladder, stack; '' for none)")
     p.add_argument("--mma-max-tokens", type=int, default=None,
-                   help="decode batches of 2 up to this many tokens take the warp-MMA kernels (library default "
-                        "if omitted; 0 = never)")
+                   help="decode batches of 2 up to this many tokens take the tensor-core decode kernels (library "
+                        "default if omitted; 0 = never)")
+    p.add_argument("--mx8-min-tokens", type=int, default=None,
+                   help="of those, batches from this many tokens take the block-scaled tcgen05 GEMM, the others "
+                        "the warp-MMA kernels (library default if omitted; 0 = never)")
     return p.parse_args()
 
 
@@ -87,15 +90,47 @@ def _peaks():
 # launch: a bench line scales the ratio to its own launches.  An entry is
 # removed when its kernel changes.
 NCU_TRAFFIC = {
-    ("mma_gateup_kernel", "decode"): {
-        "dram_bytes": 446_307_328 + 3_269_120, "algorithmic_bytes": 449_855_488,
-        "capture": "ncu dram__bytes_read/write.sum of mma_gateup_kernel<2>, bench.py --workload forward --T 64 "
-                   "(trace step 5: 48 experts + shared), profiles/mma_gateup_kernel_decode_forward_T64.md"},
     ("prefill_gemm_kernel (gate/up)", "prefill"): {
         "dram_bytes": 675_437_824 + 44_954_624, "algorithmic_bytes": 721_420_288,
         "capture": "ncu dram__bytes_read/write.sum of prefill_gemm_kernel gate/up, bench.py --workload prefill "
                    "--prefill-experts 64 --prefill-tokens 2048, profiles/prefill_gemm_kernel_prefill_E64_T2048.md"},
 }
+
+
+def apply_options(M, args):
+    """Sets the library's decode-path options from the command line; returns
+    (mma_max, mx8_min) as they stand."""
+    if args.mma_max_tokens is not None:
+        M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, args.mma_max_tokens)
+    if getattr(args, "mx8_min_tokens", None) is not None:
+        M.moe_set_option(M.MOE_OPT_MX8_MIN_TOKENS, args.mx8_min_tokens)
+    mma_max = M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, 0)
+    M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, mma_max)
+    mx8_min = M.moe_set_option(M.MOE_OPT_MX8_MIN_TOKENS, 0)
+    M.moe_set_option(M.MOE_OPT_MX8_MIN_TOKENS, mx8_min)
+    return mma_max, mx8_min
+
+
+def gateup_kernel(T, mma_max, mx8_min):
+    """Name of the kernel that runs a decode batch's gate/up (below the grouped-GEMM size)."""
+    if 2 <= T <= mma_max:
+        return "mx8_gemm_kernel (gate/up)" if 0 < mx8_min <= T else "mma_gateup_kernel"
+    return "gateup_kernel"
+
+
+def gateup_io_bytes(kernel, T, k, H, I):
+    """Activation and h bytes one gate/up launch moves for a batch of T tokens
+    (k pairs each, plus the shared expert's T rows): bf16 x and fp32 h for the
+    CUDA-core and warp-MMA kernels; E4M3 hi/lo rows with a scale byte per 32
+    elements, read and written, for the block-scaled GEMM."""
+    rows = T * k + T
+    if kernel.startswith("mx8"):
+        return rows * (2 * H + H // 32) + rows * (2 * I + I // 32)
+    return T * H * 2 + rows * I * 4
+
+
+DTYPE_MX8 = ("e2m1/e8m0 weights x e4m3 hi+lo activations (tcgen05.mma.kind::mxf8f6f4), fp32 accumulate")
+DTYPE_MMA = "e2m1/e8m0 weights, fp16 products, fp32 accumulate"
 
 
 def ncu_traffic(kernel, workload, bytes_per_launch):
@@ -239,8 +274,7 @@ def decode_line(args):
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
-    if args.mma_max_tokens is not None:
-        M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, args.mma_max_tokens)
+    apply_options(M, args)
     dev = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
@@ -294,8 +328,7 @@ def decode_line(args):
         except Exception:
             return None
     stream = torch.cuda.current_stream(dev)
-    mma_max = M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, 0)
-    M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, mma_max)
+    mma_max, mx8_min = apply_options(M, args)
     # trace steps: [0, start - warmup) replayed untimed from an empty cache, then
     # [start - warmup, start) as warm-up, then the timed window [start, start + steps)
     start = max(args.window_start, args.warmup)
@@ -371,13 +404,14 @@ def decode_line(args):
         misses = runner.stats["misses"] - misses0
         copied = runner.stats["bytes_copied"] - bytes0
         # accounting: distinct experts per step
+        gu_name = gateup_kernel(T, mma_max, mx8_min)
         acct_gu_bytes, acct_layer_bytes, acct_gemm_bytes = 0, 0, 0
         distinct = 0
         for ids in ids_seen:
             d = int(torch.unique(ids).numel())
             distinct += d
             acct_gemm_bytes += d * gu_expert + T * H * 2 + T * k * I * 2
-            acct_gu_bytes += gu_shared + T * H * 2 + T * I * 4 + d * gu_expert + T * k * I * 4
+            acct_gu_bytes += gu_shared + d * gu_expert + gateup_io_bytes(gu_name, T, k, H, I)
             acct_layer_bytes += d * Bx + layer_shared + 2 * T * H * 2
         # profiled pass: the same steps again from the same cache state, each
         # kernel bracketed by the library's events (for the breakdown only)
@@ -399,7 +433,7 @@ def decode_line(args):
         else:
             # the routed experts' bytes count only where this kernel computed them
             dbytes = acct_gu_bytes if not gg_n else acct_gu_bytes - acct_gemm_bytes + T * H * 2
-            dom, dms, dn = ("mma_gateup_kernel" if 2 <= T <= mma_max else "gateup_kernel"), gu_ms, gu_n
+            dom, dms, dn = gu_name, gu_ms, gu_n
         gu_ms, gu_n, acct_gu_bytes = dms, dn, dbytes
         compute_ms = sum(v[0] for n, v in kt.items() if n != "copy_device") / args.steps
         return {
@@ -510,9 +544,9 @@ def decode_line(args):
             kname, kms, kn = "prefill_gemm_kernel (gate/up)", gg_ms, gg_n
             kbytes = sum(d * gu_expert + T * H * 2 + P * I * 2 for d in dsum) / kn
         else:
-            kname = "mma_gateup_kernel" if 2 <= T <= mma_max else "gateup_kernel"
+            kname = gateup_kernel(T, mma_max, mx8_min)
             kms, kn = gu_ms, gu_n
-            kbytes = sum(d * gu_expert + gu_shared + T * H * 2 + (P + T) * I * 4 for d in dsum) / kn
+            kbytes = sum(d * gu_expert + gu_shared + gateup_io_bytes(kname, T, k, H, I) for d in dsum) / kn
         kgbs = kbytes / (kms / kn / 1e3) / 1e9
         return {"ms_per_step": ms, "tokens_per_s": T / (ms / 1e3), "layer_hbm_gbs": gbs,
                 "frac_of_hbm": gbs / hbm_peak, "kernel": kname, "kernel_ms_per_launch": kms / kn,
@@ -592,7 +626,8 @@ def decode_line(args):
         line = {
             "metric": METRIC, "value": head["tokens_per_s"], "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e2m1/e8m0 weights, f16 dot, f32 accumulate",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": DTYPE_MX8 if gateup_kernel(args.T, mma_max, mx8_min).startswith("mx8") else DTYPE_MMA,
             "data": "synthetic (seeded generator; no checkpoint weights)",
             "config": {"workload": f"decode layer H=4096 I=2048 E=256 top_k=8 + FP8 shared, 64-slot cache over a pinned "
                                    f"256-expert bank, Zipf(1.1) routing trace, T={args.T}",
@@ -762,10 +797,7 @@ def other_entry(args, name):
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    if args.mma_max_tokens is not None:
-        M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, args.mma_max_tokens)
-    mma_max = M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, 0)
-    M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, mma_max)
+    mma_max, mx8_min = apply_options(M, args)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     hbm_peak, hbm_kind = _peaks()
@@ -958,23 +990,25 @@ def other_entry(args, name):
             B2 = M.moe_int2_expert_bytes(H, I)
             gu2 = 2 * (I * H // 4 + I * H // 32)
             lay_b, gu_b = 0, 0
+            kname = gateup_kernel(T, mma_max, mx8_min)
             for sl, tg in seen:
                 sl, tg = sl.cpu().numpy(), tg.cpu().numpy()
                 d4 = len(np.unique(sl[(tg == 0) & (sl >= 0)]))
                 d2 = len(np.unique(sl[(tg == 1) & (sl >= 0)]))
                 lay_b += d4 * Bx + d2 * B2 + 2 * T * H * 2
-                gu_b += d4 * gu4 + d2 * gu2 + T * H * 2 + T * k * I * 4
+                gu_b += d4 * gu4 + d2 * gu2 + gateup_io_bytes(kname, T, k, H, I)
             gu_ms, gu_n = kt["gateup"]
             gu_bytes = gu_b / max(gu_n, 1)
             gu_gbs = gu_bytes / (gu_ms / max(gu_n, 1) / 1e3) / 1e9
-            out["dtype"] = "e2m1/e8m0 and 2-bit/e4m3 weights, fp16 products, fp32 accumulate"
+            out["dtype"] = ("FP4 pairs: " + (DTYPE_MX8 if kname.startswith("mx8") else DTYPE_MMA) +
+                            "; 2-bit pairs: e4m3-scaled 2-bit weights, fp16 products, fp32 accumulate")
             out["config"] = {"workload": "ladder (2,4) decode H=4096 I=2048 E=256 top_k=6 T=32, 96 FP4 + "
                                          "192 2-bit slots, Zipf(1.1) trace", "T": T,
                              "timed_steps": [start, start + args.steps]}
             out["layer_gbs"] = lay_b / args.steps / (ms / 1e3) / 1e9
             # every launch of the gate/up scope (the warp-MMA kernel for the FP4
             # pairs and the CUDA-core kernel for the 2-bit ones share it)
-            out["roofline"] = roofline_hbm("gateup (mma_gateup_kernel + gateup_kernel)", gu_gbs, gu_bytes,
+            out["roofline"] = roofline_hbm(f"gateup ({kname} + gateup_kernel)", gu_gbs, gu_bytes,
                                            gu_ms / max(gu_n, 1), hbm_peak, hbm_kind,
                                            "the gate/up kernels of the ladder's steps: touched FP4 and 2-bit "
                                            "experts' w1/w3, x and h")
@@ -1019,6 +1053,7 @@ def other_entry(args, name):
     kt = profiled(lambda i: step(args.warmup + i), args.steps)
     # touched bytes per step: distinct experts per layer
     tb, gub = 0, 0
+    kname = gateup_kernel(T, mma_max, mx8_min)
     fp8 = M.moe_fp8_expert_bytes(H, I)
     gu8 = 2 * (I * H + I * 4)
     for s in range(args.warmup, n):
@@ -1026,19 +1061,19 @@ def other_entry(args, name):
             ids, _ = M.moe_router_topk(lg[s][layer], k)
             d = int(torch.unique(ids).numel())
             tb += d * Bx + fp8
-            gub += d * gu4 + gu8 + T * H * 2 + (T * k + T) * I * 4
+            gub += d * gu4 + gu8 + gateup_io_bytes(kname, T, k, H, I)
     gbs = tb / args.steps / (ms / 1e3) / 1e9
     gu_ms, gu_n = kt["gateup"]
     gu_bytes = gub / max(gu_n, 1)
     gu_gbs = gu_bytes / (gu_ms / max(gu_n, 1) / 1e3) / 1e9
     out.update({"value": T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "clocks": ck,
-                "dtype": "e2m1/e8m0 weights, fp16 products, fp32 accumulate",
+                "dtype": DTYPE_MX8 if kname.startswith("mx8") else DTYPE_MMA,
                 "config": {"workload": "43-layer stack decode, 256 FP4 experts + FP8 shared per layer, all "
                                        "resident (148 GB), T=16, 70% step-to-step reuse", "T": T, "layers": L},
                 "stack_hbm_gbs": gbs, "hbm_frac_of_step": gbs / hbm_peak,
                 "gpu_launches": sum(v[1] for v in kt.values()),
                 "kernel_ms_per_step": {nm: round(v[0] / args.steps, 4) for nm, v in kt.items() if v[1]},
-                "roofline": roofline_hbm("mma_gateup_kernel" if 2 <= T <= mma_max else "gateup_kernel", gu_gbs,
+                "roofline": roofline_hbm(kname, gu_gbs,
                                          gu_bytes, gu_ms / max(gu_n, 1), hbm_peak, hbm_kind,
                                          "gate/up kernel of each layer: touched experts' w1/w3, the shared "
                                          "expert's, x and h"),
@@ -1064,8 +1099,7 @@ def run_forward(args):
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    if args.mma_max_tokens is not None:
-        M.moe_set_option(M.MOE_OPT_MMA_MAX_TOKENS, args.mma_max_tokens)
+    apply_options(M, args)
     wl = configs.scaled(configs.DECODE, T=args.T)
     H, I, E, k, T = wl.H, wl.I, wl.E, wl.k, wl.T
     Bx = M.moe_fp4_expert_bytes(H, I)

@@ -539,9 +539,9 @@ moe_status moe_expert_forward_noalloc(const moe_expert_views* v, const uint16_t*
  * tcgen05 GEMM (tcgen05.mma.kind::mxf8f6f4: E2M1 weights as stored, the
  * activations and h split into two E4M3 terms with a power-of-two scale per
  * 32 elements, which holds a bf16 value exactly but for subnormal low terms),
- * the others the warp-level kernels (mma.sync); 0 = never.  It needs H a
- * multiple of 256, I of 128, fp4_slots 32-byte and x 8-byte aligned, and
- * falls back to the warp-level kernels otherwise.  The previous value goes to
+ * the others the warp-level kernels (mma.sync); 0 = never.  It needs at most
+ * 64 tokens, H and I multiples of 512 up to 4096, fp4_slots 32-byte and x
+ * 8-byte aligned, and falls back to the warp-level kernels otherwise.  The previous value goes to
  * *old_value (may be null).  MOE_ERR_INVALID for an unknown option or a
  * negative value.  Set them between calls, not while another thread issues
  * forward calls.

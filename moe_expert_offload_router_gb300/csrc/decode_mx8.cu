@@ -18,21 +18,26 @@
 // activations, each 32-element block along K scaled by a power of two and
 // carried as two E4M3 terms hi + lo (mx.cuh); a bf16 input is held exactly in
 // all but subnormal-lo cases, so the products are those of the bf16 path.
-// For items of up to 48 tokens the hi and lo rows of a stage stack into one
-// B operand of 2n rows (one MMA per K slice, the accumulator's two halves
-// added in the epilogue); larger items issue an MMA for each.
+// Groups hold up to 48 tokens; the hi and lo rows of a stage stack into one
+// B operand of 2n rows (one MMA per K slice and tile), and the epilogue adds
+// the accumulator's two halves.
 //
-// Persistent CTA (384 threads, one per SM), items = (token group, feature
-// tile) drawn in a fixed stride, tensor-memory accumulators double-buffered
-// so an item's epilogue overlaps the next item's main loop:
-//   warp 0      TMA producer: two 128-row A tiles and the group's hi/lo rows
-//               per 128-element K stage, four stages deep
+// Persistent CTAs, two per SM (192 threads, 90 KB of shared memory and 256
+// tensor-memory columns each): one CTA's TMA engine moves the 64-byte rows of
+// the packed E2M1 tiles at about two thirds of an SM's share of HBM, two
+// together at the full rate, and one CTA streams while the other runs its
+// epilogue.  Items = (token group, feature tile): CTA c starts with item c and
+// draws the next from a global counter, published to the other warps through
+// a small queue in shared memory (the tail is at most about one item):
+//   warp 0      TMA: two 128-row A tiles and the group's hi/lo rows per
+//               128-element K stage, two stages deep; draws the items and
+//               prefetches each next item's A scale rows into L2
 //   warp 1      TMEM allocation; MMA issue (one elected lane, one asm block
 //               per stage), commits to the stage's "empty" barrier and, after
-//               the item's last stage, to the accumulator's "full" barrier
-//   warps 4-7   scale factors: each writes its TMEM lane quadrant's A and B
-//               scale words of a stage, two stages of loads ahead
-//   warps 8-11  epilogue: gate/up -> h = SiLU(gate) * up, itself split into
+//               the item's last stage, to the accumulators' "full" barrier
+//   warps 2-5   per item: the A and B scale words of every stage into their
+//               TMEM lane quadrant (two stages of loads ahead), then the
+//               epilogue: gate/up -> h = SiLU(gate) * up, itself split into
 //               E4M3 hi/lo with a scale per 32 features (the down GEMM's B
 //               operand, in the same sorted row order); down -> fp32 rows of
 //               o per pair for the router-weighted combine
@@ -49,22 +54,26 @@
 
 namespace moe {
 
-constexpr int kM8Threads = 384;
-constexpr int kM8Stages = 4;
+constexpr int kM8Threads = 192;                 // 6 warps: TMA, MMA, four scale-factor / epilogue warps
+constexpr int kM8CtasPerSm = 2;                 // two CTAs stream each SM's share of HBM
+constexpr int kM8Stages = 2;
 constexpr int kM8KStage = 128;                  // K elements per stage: one 128-byte swizzled row
 constexpr int kM8ATile = 128 * 128;             // one 128-row A tile of a stage in shared memory
 constexpr int kM8BBytes = 2 * kMx8MaxRows * 128;  // hi rows, then lo rows
 constexpr int kM8Stage = 2 * kM8ATile + kM8BBytes;
 constexpr int kM8OffBar = kM8Stages * kM8Stage;
-constexpr int kM8Smem = kM8OffBar + 256 + 1024;
-constexpr int kM8StackMax = 48;                 // items up to this many rows stack hi and lo in one B operand
-constexpr int kM8AccCols = 96;                  // TMEM columns per accumulator (2 * 48, or 64 unstacked)
-constexpr int kM8SfBase = 4 * kM8AccCols;       // two buffers of two accumulators, then the scale factors
+constexpr int kM8OffSB = kM8OffBar + 256;       // the group's B scale rows, padded by 16 bytes
+constexpr int kM8SBBytes = kMx8MaxRows * (4096 / 32 + 16);  // K up to 4096
+constexpr int kM8Smem = kM8OffSB + kM8SBBytes + 1024;
+constexpr int kM8AccCols = 2 * kMx8MaxRows;     // TMEM columns per accumulator (hi and lo halves)
+constexpr int kM8SfBase = 2 * kM8AccCols;       // the two accumulators, then the scale factors
 constexpr int kM8SfCols = 16;                   // per stage: A tile 0 +0..3, A tile 1 +4..7, B +8..10
-static_assert(kM8SfBase + kM8Stages * kM8SfCols <= 512, "tensor memory columns");
-static_assert(kM8Smem <= 232448, "shared memory per CTA");
-static_assert(2 * kM8StackMax <= kM8AccCols && kMx8MaxRows <= kM8AccCols, "accumulator width");
-static_assert((2 * kM8Stages + 4) * 8 + 8 <= 256, "barrier area");
+constexpr int kM8TmemCols = 256;                // half of an SM's tensor memory
+static_assert(kM8SfBase + kM8Stages * kM8SfCols <= kM8TmemCols, "tensor memory columns");
+static_assert(kM8CtasPerSm * (kM8Smem + 1024) <= 228 * 1024, "shared memory of two CTAs per SM");
+static_assert(kM8AccCols % 32 == 0 && kM8AccCols <= 96, "accumulator width (three B scale columns)");
+constexpr int kM8Queue = 4;                     // items published ahead to the consumer warps
+static_assert((2 * kM8Stages + 4 + 2 * kM8Queue) * 8 + 8 + 4 * kM8Queue <= 256, "barrier area");
 
 struct Mx8Args {
   int mode;          // 0: gate/up + SwiGLU -> h hi/lo; 1: down -> o
@@ -81,6 +90,7 @@ struct Mx8Args {
   const float* rs1;  // w3 (mode 0)
   const uint8_t* bsc;  // B scale bytes [P + T][K / 32]
   const int* hdr;      // [0] groups, [1] routed groups (the shared expert's follow)
+  int* ctr;            // item counter (zeroed by the plan): items past the first gridDim.x are drawn from it
   const Group* groups;
   const int* perm;     // sorted position -> pair index
   uint8_t* hhi;        // mode 0 out: [P + T][I] E4M3 hi, lo, and scale bytes [P + T][I / 32]
@@ -128,43 +138,25 @@ __device__ __forceinline__ M8Item m8_item(const Mx8Args& a, int it, int ng, int 
 }
 
 // Four K = 32 slices of one stage for both accumulators, from one elected
-// lane: with STACK one MMA per slice and tile (B = hi rows then lo rows),
-// else two (hi, then lo into the same accumulator).  Slice j advances the
-// descriptors 32 bytes and selects byte j of the scale-factor words (the
-// A and B scale-factor IDs of the instruction descriptor).
-template <bool STACK>
-__device__ __forceinline__ void m8_stage(uint32_t d0, uint32_t d1, uint64_t a0, uint64_t a1, uint64_t bh,
-                                         uint64_t bl, uint32_t idesc, uint32_t sfa0, uint32_t sfa1, uint32_t sfb,
-                                         uint32_t acc, uint64_t* bar) {
-#define M8_MMA(D, A, B, ID, SFA, P) \
-  "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.block32 [" D "], " A ", " B ", " ID ", [" SFA "], [%9], " P ";\n\t"
-#define M8_SLICE(OFF, IDOFF, P)                                                                              \
-  "add.s64 a, %2, " OFF ";\n\tadd.s64 c, %3, " OFF ";\n\tadd.s64 bb, %4, " OFF ";\n\tadd.s64 bo, %5, " OFF \
-  ";\n\tadd.u32 id, %6, " IDOFF ";\n\t" M8_MMA("%0", "a", "bb", "id", "%7", P)                              \
-  M8_LO("%0", "a", "%7") M8_MMA("%1", "c", "bb", "id", "%8", P) M8_LO("%1", "c", "%8")
-  if (STACK) {
-#define M8_LO(D, A, SFA) ""
-    asm volatile(
-        "{\n\t.reg .pred e, p, t;\n\t.reg .b64 a, c, bb, bo;\n\t.reg .b32 id;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %10, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t" M8_SLICE("0", "0", "p")
-            M8_SLICE("2", "536870928", "t") M8_SLICE("4", "1073741856", "t") M8_SLICE("6", "1610612784", "t")
-                "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%11];\n\t}" ::"r"(d0),
-        "r"(d1), "l"(a0), "l"(a1), "l"(bh), "l"(bl), "r"(idesc), "r"(sfa0), "r"(sfa1), "r"(sfb), "r"(acc),
-        "r"(su32(bar))
-        : "memory");
-#undef M8_LO
-  } else {
-#define M8_LO(D, A, SFA) M8_MMA(D, A, "bo", "id", SFA, "t")
-    asm volatile(
-        "{\n\t.reg .pred e, p, t;\n\t.reg .b64 a, c, bb, bo;\n\t.reg .b32 id;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %10, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t" M8_SLICE("0", "0", "p")
-            M8_SLICE("2", "536870928", "t") M8_SLICE("4", "1073741856", "t") M8_SLICE("6", "1610612784", "t")
-                "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%11];\n\t}" ::"r"(d0),
-        "r"(d1), "l"(a0), "l"(a1), "l"(bh), "l"(bl), "r"(idesc), "r"(sfa0), "r"(sfa1), "r"(sfb), "r"(acc),
-        "r"(su32(bar))
-        : "memory");
-#undef M8_LO
-  }
+// lane: one MMA per slice and tile, B = the stage's hi rows then its lo rows
+// (N = 2 n).  Slice j advances the descriptors 32 bytes and selects byte j of
+// the scale-factor words (the A and B scale-factor IDs of the instruction
+// descriptor).
+__device__ __forceinline__ void m8_stage(uint32_t d0, uint32_t d1, uint64_t a0, uint64_t a1, uint64_t b,
+                                         uint32_t idesc, uint32_t sfa0, uint32_t sfa1, uint32_t sfb, uint32_t acc,
+                                         uint64_t* bar) {
+#define M8_MMA(D, A, SFA, P) \
+  "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.block32 [" D "], " A ", bb, id, [" SFA "], [%8], " P ";\n\t"
+#define M8_SLICE(OFF, IDOFF, P)                                                                             \
+  "add.s64 a, %2, " OFF ";\n\tadd.s64 c, %3, " OFF ";\n\tadd.s64 bb, %4, " OFF ";\n\tadd.u32 id, %5, " IDOFF \
+  ";\n\t" M8_MMA("%0", "a", "%6", P) M8_MMA("%1", "c", "%7", P)
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b64 a, c, bb;\n\t.reg .b32 id;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %9, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t" M8_SLICE("0", "0", "p")
+          M8_SLICE("2", "536870928", "t") M8_SLICE("4", "1073741856", "t") M8_SLICE("6", "1610612784", "t")
+              "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%10];\n\t}" ::"r"(d0),
+      "r"(d1), "l"(a0), "l"(a1), "l"(b), "r"(idesc), "r"(sfa0), "r"(sfa1), "r"(sfb), "r"(acc), "r"(su32(bar))
+      : "memory");
 #undef M8_SLICE
 #undef M8_MMA
 }
@@ -173,9 +165,23 @@ __device__ __forceinline__ void m8_stage(uint32_t d0, uint32_t d1, uint64_t a0, 
 static_assert(536870928u == (1u << 29) + (1u << 4) && 1610612784u == 3u * ((1u << 29) + (1u << 4)),
               "scale-factor ID immediates");
 
-__device__ __forceinline__ uint32_t ldg_u32(const uint8_t* p) { return __ldg(reinterpret_cast<const uint32_t*>(p)); }
+__device__ __forceinline__ uint4 ldg_u128(const uint8_t* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
 
-__global__ void __launch_bounds__(kM8Threads, 1)
+
+// L2 prefetch of an FP4 item's A scale rows (two runs of 128 rows x K / 32
+// bytes, contiguous in the expert), so the scale-factor warps' loads hit L2.
+__device__ __forceinline__ void m8_prefetch_scales(const Mx8Args& a, const M8Item& m) {
+  if (!m.run || m.fp8) return;
+  const uint32_t sbytes = (uint32_t)a.K / 32;
+  const uint8_t* e = a.fp4 + (size_t)m.slot * a.b4;
+  const int row1 = a.mode == 0 ? m.f0 : m.f0 + 128;
+  const uint8_t* p0 = e + a.sc0 + (size_t)m.f0 * sbytes;
+  const uint8_t* p1 = e + a.sc1 + (size_t)row1 * sbytes;
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p0), "r"(128u * sbytes) : "memory");
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p1), "r"(128u * sbytes) : "memory");
+}
+
+__global__ void __launch_bounds__(kM8Threads, kM8CtasPerSm)
     mx8_gemm_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
                     const __grid_constant__ CUtensorMap mS0, const __grid_constant__ CUtensorMap mS1,
                     const __grid_constant__ CUtensorMap mBh, const __grid_constant__ CUtensorMap mBl, Mx8Args a) {
@@ -183,10 +189,14 @@ __global__ void __launch_bounds__(kM8Threads, 1)
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* full = (uint64_t*)(sm + kM8OffBar);  // [kM8Stages]: TMA bytes + the four scale-factor warps
   uint64_t* empty = full + kM8Stages;             // [kM8Stages]: the stage's MMAs completed
-  uint64_t* accf = empty + kM8Stages;             // [2]: an accumulator's item finished
-  uint64_t* acce = accf + 2;                      // [2]: the epilogue has read an accumulator
-  uint64_t* drain = acce + 2;
-  uint32_t* tmem_slot = (uint32_t*)(drain + 1);
+  uint64_t* accf = empty + kM8Stages;             // the item's MMAs completed
+  uint64_t* acce = accf + 1;                      // the epilogue has read the accumulators
+  uint64_t* drain = acce + 1;
+  uint64_t* qfull = drain + 1;                    // [kM8Queue]: an item index published
+  uint64_t* qempty = qfull + kM8Queue;            // [kM8Queue]: the five consumer warps have read it
+  uint64_t* sbar = qempty + kM8Queue;             // the four scale-factor warps (copy of the B scale rows)
+  uint32_t* tmem_slot = (uint32_t*)(sbar + 1);
+  volatile int* itq = (volatile int*)(tmem_slot + 1);  // [kM8Queue] item indices, -1 = no more
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = a.K / kM8KStage;
 
@@ -198,32 +208,61 @@ __global__ void __launch_bounds__(kM8Threads, 1)
   const int n_items = ng * a.tiles;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kM8Stages; ++s) {
-      mbar_init(&full[s], 1 + 4);
+      mbar_init(&full[s], 1 + 4);  // the TMA thread's expect_tx arrival + the scale-factor warps
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&accf[b], 1);
-      mbar_init(&acce[b], 4);
-    }
+    mbar_init(accf, 1);
+    mbar_init(acce, 4);
     mbar_init(drain, 1);
+    for (int j = 0; j < kM8Queue; ++j) {
+      mbar_init(&qfull[j], 1);
+      mbar_init(&qempty[j], 1 + 4);  // the MMA warp and the four scale-factor / epilogue warps
+    }
+    mbar_init(sbar, 4);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
-                 "r"(512));
+                 "r"(kM8TmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // q-th item of this CTA for a consumer warp (whole warp): false on timeout
+  auto next_item = [&](uint32_t q, int& it) -> bool {
+    const int j = q % kM8Queue;
+    if (!__all_sync(0xffffffffu, mbar_wait_fast(&qfull[j], (q / kM8Queue) & 1, a.err))) return false;
+    it = itq[j];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&qempty[j]);
+    return true;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
       bool ok = true;
-      uint32_t gs = 0;
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const M8Item m = m8_item(a, it, ng, nr, false);
+      uint32_t gs = 0, q = 0;
+      auto publish = [&](int it) -> bool {
+        const int j = q % kM8Queue;
+        const uint32_t r = q / kM8Queue;
+        if (r > 0 && !mbar_wait_fast(&qempty[j], (r - 1) & 1, a.err)) return false;
+        itq[j] = it;
+        mbar_arrive(&qfull[j]);  // release: the index is visible to the warps that wait on it
+        ++q;
+        return true;
+      };
+      int cur = (int)blockIdx.x < n_items ? (int)blockIdx.x : -1;
+      ok = publish(cur);
+      if (cur >= 0) m8_prefetch_scales(a, m8_item(a, cur, ng, nr, false));
+      while (ok && cur >= 0) {
+        int nxt = atomicAdd(a.ctr, 1) + (int)gridDim.x;
+        if (nxt >= n_items) nxt = -1;
+        if (!(ok = publish(nxt))) break;
+        if (nxt >= 0) m8_prefetch_scales(a, m8_item(a, nxt, ng, nr, false));
+        const M8Item m = m8_item(a, cur, ng, nr, false);
+        cur = nxt;
         if (!m.run) continue;
         const int nbx = m.n16 / 16;
         const uint32_t bytes = (m.fp8 ? 2u * kM8ATile : (uint32_t)kM8ATile) + 2u * (uint32_t)nbx * 2048u;
@@ -258,20 +297,19 @@ __global__ void __launch_bounds__(kM8Threads, 1)
   } else if (warp == 1) {
     bool ok = true;
     uint32_t gs = 0, i = 0;
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+    for (uint32_t qi = 0; ok; ++qi) {
+      int it;
+      if (!(ok = next_item(qi, it)) || it < 0) break;
       const M8Item m = m8_item(a, it, ng, nr, true);
       if (!m.run) continue;
-      const int b = i & 1;
-      const uint32_t u = i >> 1;
+      // the epilogue of the previous item has read the accumulators
+      if (i > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait_fast(acce, (i - 1) & 1, a.err)))) break;
       ++i;
-      if (u > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait_fast(&acce[b], (u - 1) & 1, a.err)))) break;
       tc_fence_after();
-      const bool stack = m.n16 <= kM8StackMax;
-      const int n_mma = stack ? 2 * m.n16 : m.n16;
-      // E2M1 (5) or E4M3 (0) A, E4M3 B, fp32 D, K-major both, E8M0 scales, M = 128
-      const uint32_t idesc = ((m.fp8 ? 0u : 5u) << 7) | ((uint32_t)(n_mma >> 3) << 17) | (1u << 23) |
+      // E2M1 (5) or E4M3 (0) A, E4M3 B, fp32 D, K-major both, E8M0 scales, M = 128, N = 2 n16
+      const uint32_t idesc = ((m.fp8 ? 0u : 5u) << 7) | ((uint32_t)(2 * m.n16 >> 3) << 17) | (1u << 23) |
                              ((uint32_t)(128 >> 4) << 24);
-      const uint32_t d0 = tmem + (uint32_t)(b * 2 * kM8AccCols), d1 = d0 + kM8AccCols;
+      const uint32_t d0 = tmem, d1 = tmem + kM8AccCols;
       for (int ks = 0; ks < nk; ++ks, ++gs) {
         const int s = gs % kM8Stages;
         const uint32_t r = gs / kM8Stages;
@@ -279,34 +317,54 @@ __global__ void __launch_bounds__(kM8Threads, 1)
         tc_fence_after();
         uint8_t* st = sm + s * kM8Stage;
         const uint64_t ad0 = umma_desc_sw128(su32(st)), ad1 = umma_desc_sw128(su32(st + kM8ATile));
-        const uint64_t bh = umma_desc_sw128(su32(st + 2 * kM8ATile));
-        const uint64_t bl = umma_desc_sw128(su32(st + 2 * kM8ATile + m.n16 * 128));
+        const uint64_t bd = umma_desc_sw128(su32(st + 2 * kM8ATile));
         const uint32_t sf = tmem + kM8SfBase + kM8SfCols * s;
-        if (stack)
-          m8_stage<true>(d0, d1, ad0, ad1, bh, bl, idesc, sf, sf + 4, sf + 8, ks != 0, &empty[s]);
-        else
-          m8_stage<false>(d0, d1, ad0, ad1, bh, bl, idesc, sf, sf + 4, sf + 8, ks != 0, &empty[s]);
+        m8_stage(d0, d1, ad0, ad1, bd, idesc, sf, sf + 4, sf + 8, ks != 0, &empty[s]);
       }
-      if (ok) mma_commit_elect(&accf[b]);
+      if (ok) mma_commit_elect(accf);
     }
     // every MMA this warp issued has completed before tensor memory is freed
     mma_commit_elect(drain);
     __syncwarp();
     mbar_wait(drain, 0, a.err);
-  } else if (warp >= 4 && warp < 8) {
-    // scale factors of lane quadrant q: A row 32 q + lane of each tile at
-    // column +q of its 4-column group; B rows 32 c + lane at column +8 + c
-    const int q = warp - 4;
+  } else {
+    // warps 2-5: lane quadrant q = warp % 4 of tensor memory.  Per item, the
+    // scale factors of every stage (A row 32 q + lane of each tile at column
+    // +q of its 4-column group; B rows 32 c + lane at column +8 + c), then
+    // the epilogue once the item's MMAs have completed.  The scale rows are
+    // read whole, once per item: each lane keeps its two A rows' words in
+    // registers (up to 32 stages at a time, one load per 16 bytes, the rest of
+    // each line from L1), and the group's B rows go to shared memory in one
+    // coalesced copy by the four warps; scattered 4-byte loads per stage cost
+    // about as many L2 requests as the TMA's own and slowed it down.
+    const int q = warp & 3;
+    const int tid = threadIdx.x - 64;  // 0 .. 127 over the four warps
     const int sbytes = a.K / 32;
+    const int srow = sbytes + 16;      // padded row of the B scale copy (4-way bank conflicts at most)
+    uint8_t* sB = sm + kM8OffSB;
     bool ok = true;
-    uint32_t gs = 0;
-    struct Sf {
-      uint32_t a0, a1, b[3];
+    uint32_t gs = 0, i = 0, nsync = 0;
+    // the four warps meet (an mbarrier with a bounded wait, so a warp that gave
+    // up cannot leave the others waiting)
+    auto group_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sbar);
+      return __all_sync(0xffffffffu, mbar_wait_fast(sbar, (nsync++) & 1, a.err));
     };
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+    for (uint32_t qi = 0; ok; ++qi) {
+      int it;
+      if (!(ok = next_item(qi, it)) || it < 0) break;
       const M8Item m = m8_item(a, it, ng, nr, false);
       if (!m.run) continue;
-      const bool stack = m.n16 <= kM8StackMax;
+      // the group's B scale rows (contiguous in global memory) -> shared memory
+      if (!(ok = group_sync())) break;  // every warp is done with the previous item's copy
+      {
+        const uint8_t* gB = a.bsc + (size_t)m.brow0 * sbytes;
+        const int cpr = sbytes / 16, n = m.count * cpr;
+        for (int c = tid; c < n; c += 128)
+          *reinterpret_cast<uint4*>(sB + (c / cpr) * srow + 16 * (c % cpr)) = ldg_u128(gB + 16 * c);
+      }
+      if (!(ok = group_sync())) break;
       const uint8_t* sa0 = nullptr;
       const uint8_t* sa1 = nullptr;
       if (!m.fp8) {
@@ -315,31 +373,25 @@ __global__ void __launch_bounds__(kM8Threads, 1)
         sa0 = e + a.sc0 + (size_t)r0 * sbytes;
         sa1 = e + a.sc1 + (size_t)r1 * sbytes;
       }
-      const uint8_t* sb[3];
+      const uint32_t* sbw[3];  // this lane's B rows in the shared copy
 #pragma unroll
       for (int c = 0; c < 3; ++c) {
         int tk = 32 * c + lane;
-        if (stack && tk >= m.n16) tk -= m.n16;
-        if (tk >= m.count) tk = 0;  // columns past the group: any valid row
-        sb[c] = a.bsc + (size_t)(m.brow0 + tk) * sbytes;
+        if (tk >= m.n16) tk -= m.n16;  // B rows n16 .. 2 n16 - 1 are the lo terms
+        if (tk >= m.count) tk = 0;     // columns past the group: any valid row
+        sbw[c] = reinterpret_cast<const uint32_t*>(sB + tk * srow);
       }
-      auto load = [&](int ks, Sf& w) {
-        w.a0 = m.fp8 ? 0x7f7f7f7fu : ldg_u32(sa0 + 4 * ks);
-        w.a1 = m.fp8 ? 0x7f7f7f7fu : ldg_u32(sa1 + 4 * ks);
-#pragma unroll
-        for (int c = 0; c < 3; ++c) w.b[c] = ldg_u32(sb[c] + 4 * ks);
-      };
-      auto store = [&](const Sf& w) -> bool {
+      auto store = [&](uint32_t wa0, uint32_t wa1, int ks) -> bool {
         const int s = gs % kM8Stages;
         const uint32_t r = gs / kM8Stages;
         // the slot's previous stage (gs - kM8Stages) must have finished its MMAs
         if (r > 0 && !__all_sync(0xffffffffu, mbar_wait_fast(&empty[s], (r - 1) & 1, a.err))) return false;
         const uint32_t col = tmem + ((uint32_t)(32 * q) << 16) + kM8SfBase + kM8SfCols * s;
-        tmem_st1(col + q, w.a0);
-        tmem_st1(col + 4 + q, w.a1);
-        tmem_st1(col + 8, w.b[0]);
-        tmem_st1(col + 9, w.b[1]);
-        tmem_st1(col + 10, w.b[2]);
+        tmem_st1(col + q, wa0);
+        tmem_st1(col + 4 + q, wa1);
+        tmem_st1(col + 8, sbw[0][ks]);
+        tmem_st1(col + 9, sbw[1][ks]);
+        tmem_st1(col + 10, sbw[2][ks]);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         __syncwarp();
@@ -347,45 +399,42 @@ __global__ void __launch_bounds__(kM8Threads, 1)
         ++gs;
         return true;
       };
-      Sf ring[3];
-      load(0, ring[0]);
-      if (nk > 1) load(1, ring[1]);
-      for (int k0 = 0; k0 < nk && ok; k0 += 3) {
+      // nk is a multiple of 4 (K a multiple of 512)
+      for (int kc = 0; kc < nk && ok; kc += 32) {
+        uint4 ra0[8], ra1[8];
+        const uint4 unit = make_uint4(0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
 #pragma unroll
-        for (int j = 0; j < 3; ++j) {
-          const int ks = k0 + j;
-          if (ks >= nk || !ok) break;
-          if (ks + 2 < nk) load(ks + 2, ring[(j + 2) % 3]);
-          ok = store(ring[j]);
+        for (int g = 0; g < 8; ++g) {
+          const bool in = kc + 4 * g < nk;
+          ra0[g] = (m.fp8 || !in) ? unit : ldg_u128(sa0 + 4 * kc + 16 * g);
+          ra1[g] = (m.fp8 || !in) ? unit : ldg_u128(sa1 + 4 * kc + 16 * g);
+        }
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          if (kc + 4 * g >= nk || !ok) break;
+          if (ok) ok = store(ra0[g].x, ra1[g].x, kc + 4 * g);
+          if (ok) ok = store(ra0[g].y, ra1[g].y, kc + 4 * g + 1);
+          if (ok) ok = store(ra0[g].z, ra1[g].z, kc + 4 * g + 2);
+          if (ok) ok = store(ra0[g].w, ra1[g].w, kc + 4 * g + 3);
         }
       }
-    }
-  } else if (warp >= 8) {
-    const int q = warp - 8;
-    bool ok = true;
-    uint32_t i = 0;
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      const M8Item m = m8_item(a, it, ng, nr, false);
-      if (!m.run) continue;
-      const int b = i & 1;
-      const uint32_t u = i >> 1;
+      if (!ok) break;
+
+      // epilogue
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait_fast(accf, i & 1, a.err)))) break;
       ++i;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait_fast(&accf[b], u & 1, a.err)))) break;
       tc_fence_after();
-      const bool stack = m.n16 <= kM8StackMax;
-      const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 2 * kM8AccCols);
-      const uint32_t lo_off = stack ? (uint32_t)m.n16 : 0u;
-      // accumulator columns c0 .. c0 + 15 of tile t (hi + lo halves when stacked)
+      const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
+      const uint32_t lo_off = (uint32_t)m.n16;
+      // accumulator columns c0 .. c0 + 15 of tile t: hi half plus lo half
       auto acc16 = [&](int t, int c0, float* v) {
         uint32_t r[16];
         tmem_ld16(tq + (uint32_t)(t * kM8AccCols + c0), r);
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-        if (stack) {
-          tmem_ld16(tq + (uint32_t)(t * kM8AccCols + c0) + lo_off, r);
+        tmem_ld16(tq + (uint32_t)(t * kM8AccCols + c0) + lo_off, r);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(r[j]);
-        }
+        for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(r[j]);
       };
       if (a.mode == 0) {
         const int f = m.f0 + 32 * q + lane;  // this lane's feature
@@ -449,14 +498,14 @@ __global__ void __launch_bounds__(kM8Threads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acce[b]);
+      if (lane == 0) mbar_arrive(acce);
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kM8TmemCols));
   }
 }
 
@@ -464,7 +513,7 @@ __global__ void __launch_bounds__(kM8Threads, 1)
 
 // Packed E2M1 codes of one matrix over every slot: (x: K codes, y: rows,
 // z: slots), 16U4_ALIGN16B (16 codes per 16 bytes of shared memory), 128-byte
-// swizzle, box of 128 codes by 128 rows.
+// swizzle, box of 128 codes by 128 rows (an A tile).
 static moe_status map_fp4_rows(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint64_t slots,
                                uint64_t slot_stride) {
   auto fn = tensor_map_encoder();
@@ -503,9 +552,11 @@ static int mx8_sm_count() {
 }
 
 bool mx8_supported(const moe_expert_views* v) {
-  // 128-element K stages and feature tiles; 256-row down tiles; the 16U4
-  // element type needs 32-byte aligned bases and row strides
-  if (v->H % 256 != 0 || v->I % 128 != 0) return false;
+  // K stages of 128 elements whose scale words go four stages to a 16-byte
+  // load (H, I multiples of 512); the B scale rows' shared copy holds K up to
+  // 4096; 256-row down tiles; the 16U4 element type needs 32-byte aligned
+  // bases and row strides
+  if (v->H % 512 != 0 || v->I % 512 != 0 || v->H > 4096 || v->I > 4096) return false;
   const bool fp4 = v->fp4_slots != nullptr && v->fp4_num_slots > 0;
   if (fp4 && ((uintptr_t)v->fp4_slots & 31) != 0) return false;
   if (v->shared && ((uintptr_t)v->shared & 15) != 0) return false;
@@ -534,7 +585,7 @@ void mx8_carve(uint8_t* base, int H, int I, int rows, Mx8Bufs* b) {
 }
 
 moe_status mx8_gemm(const moe_expert_views* v, int mode, int T, int k, bool shared, int max_groups,
-                    const int* hdr, const Group* groups, const int* perm, const Mx8Bufs& b, float* o,
+                    int* hdr, const Group* groups, const int* perm, const Mx8Bufs& b, float* o,
                     int32_t* d_error, cudaStream_t stream) {
   const int H = v->H, I = v->I, P = T * k;
   const size_t b4 = fp4_bytes(H, I);
@@ -563,6 +614,7 @@ moe_status mx8_gemm(const moe_expert_views* v, int mode, int T, int k, bool shar
   a.rs1 = sh ? reinterpret_cast<const float*>(sh + f8_mat + (size_t)I * H) : nullptr;
   a.bsc = mode == 0 ? b.xsc : b.hsc;
   a.hdr = hdr;
+  a.ctr = hdr + 2 + mode;  // zeroed by the plan kernel
   a.groups = groups;
   a.perm = perm;
   a.hhi = b.hhi;
@@ -607,10 +659,13 @@ moe_status mx8_gemm(const moe_expert_views* v, int mode, int T, int k, bool shar
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(mx8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kM8Smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(mx8_gemm_kernel)");
+    // all of the unified L1 / shared memory as shared memory, so two CTAs fit an SM
+    e = cudaFuncSetAttribute(mx8_gemm_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(mx8_gemm_kernel carveout)");
     attr_set = true;
   }
   const long long items = (long long)max_groups * a.tiles;
-  const int grid = (int)std::max(1LL, std::min<long long>(mx8_sm_count(), items));
+  const int grid = (int)std::max(1LL, std::min<long long>((long long)kM8CtasPerSm * mx8_sm_count(), items));
   mx8_gemm_kernel<<<grid, kM8Threads, kM8Smem, stream>>>(mA0, mA1, mS0, mS1, mBh, mBl, a);
   return check_launch(mode == 0 ? "mx8_gemm_kernel (gate/up)" : "mx8_gemm_kernel (down)");
 }

@@ -43,6 +43,11 @@ constexpr int kRowsDown = 64;     // rows of w2 per down work item
 constexpr int kMaxPlanPairs = 4096;
 constexpr int kGemmMinPairs = 256;  // from here on the FP4 routed pairs take the tcgen05 grouped GEMM
 
+// Decode batches up to this many tokens get the block-scaled GEMM's operand
+// buffers in their workspace (its groups are cut at kMx8MaxRows rows, so any
+// batch size works; the bound keeps the workspace of larger calls small).
+constexpr int kMx8MaxTokens = 64;
+
 struct FwdLayout {
   size_t hdr, perm, groups, xsig, xs, h, o, hs16, hsig, gg, mx8, total;
   bool gemm;     // the FP4 routed pairs may take the grouped GEMM
@@ -78,7 +83,7 @@ static FwdLayout fwd_layout(const moe_expert_views* v, int T, int k) {
   L.gemm = (long long)P >= kGemmMinPairs && grouped_gemm_supported(v);
   L.gg = off;
   if (L.gemm) off = align256(off + gg_index_bytes(T, k, v->fp4_num_slots));
-  L.mx8_ok = T >= 2 && T <= kMx8MaxRows && mx8_supported(v);
+  L.mx8_ok = T >= 2 && T <= kMx8MaxTokens && mx8_supported(v);
   L.mx8 = off;
   if (L.mx8_ok) off = align256(off + mx8_bytes(H, I, (int)P + T));
   L.total = off;

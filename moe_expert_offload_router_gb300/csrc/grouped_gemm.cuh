@@ -62,7 +62,7 @@ moe_status grouped_gemm_shared_fp8(const moe_expert_views* v, const __half* xs, 
 // Decode batches on tcgen05.mma.kind::mxf8f6f4 (decode_mx8.cu): E2M1 weights
 // straight from the slot pool, activations as E4M3 hi + lo with a power-of-two
 // scale per 32 elements.  Groups of up to kMx8MaxRows tokens.
-constexpr int kMx8MaxRows = 64;
+constexpr int kMx8MaxRows = 48;
 
 // Activation and h operands, rows in the plan's sorted order (routed pairs at
 // their sorted position, the shared expert's tokens at P + t).
@@ -78,10 +78,11 @@ struct Mx8Bufs {
 bool mx8_supported(const moe_expert_views* v);
 size_t mx8_bytes(int H, int I, int rows);
 void mx8_carve(uint8_t* base, int H, int I, int rows, Mx8Bufs* b);
-// mode 0: gate/up over the plan's groups (hdr, groups, perm) -> h operands in b;
+// mode 0: gate/up over the plan's groups (hdr, groups, perm; hdr[2 + mode] is the
+// item counter, zeroed by the plan) -> h operands in b;
 // mode 1: down -> o rows (pair index, or P + token for the shared expert).
 moe_status mx8_gemm(const moe_expert_views* v, int mode, int T, int k, bool shared, int max_groups,
-                    const int* hdr, const Group* groups, const int* perm, const Mx8Bufs& b, float* o,
+                    int* hdr, const Group* groups, const int* perm, const Mx8Bufs& b, float* o,
                     int32_t* d_error, cudaStream_t stream);
 
 }  // namespace moe

@@ -2,11 +2,12 @@
 stored, activations and h as two E4M3 terms with a power-of-two scale per 32
 elements) against the oracle, and against the warp-level kernels it replaces.
 
-Cases: items that stack the hi and lo rows into one B operand (up to 48 rows
-per group) and items that issue an MMA for each (49..64 rows); groups cut at
-64 rows when one slot takes more pairs than that; the tiny and a generic
-shape; every token of a full-size batch; FP8 shared expert on and off;
-run-to-run bit equality.  Layer outputs within max |err| <= 2e-2 * RMS of the
+Cases: groups of 1..48 rows (the hi and lo rows stack into one B operand of
+up to 96 rows) and slots with more pairs than that, cut into groups of 48;
+a generic shape (H = 1024, I = 512); the tiny shape, which the path does not
+take (H, I not multiples of 512: the CUDA-core kernels run it); every token
+of a full-size batch; FP8 shared expert on and off; run-to-run bit
+equality.  Layer outputs within max |err| <= 2e-2 * RMS of the
 oracle row.
 """
 import numpy as np
@@ -51,9 +52,9 @@ def test_full_size_every_token(mx8_on, T):
 
 
 @pytest.mark.parametrize("n_hot", [47, 48, 49, 64])
-def test_stacked_and_split_items(mx8_on, n_hot):
-    # slot 0 takes n_hot tokens: 48 rows stack hi and lo (N = 96), 49 and 64
-    # issue two MMAs per slice (N = 64); the rest spread over the other slots
+def test_groups_at_the_48_row_cut(mx8_on, n_hot):
+    # slot 0 takes n_hot tokens: one group of 47 or 48 rows (N = 96), or a
+    # group of 48 and one of 1 or 16; the rest spread over the other slots
     M = mx8_on
     wl = configs.scaled(configs.DECODE, H=1024, I=512)
     P = Pools(M, wl, 10, shared=True)
@@ -71,11 +72,11 @@ def test_stacked_and_split_items(mx8_on, n_hot):
     assert bf16_rel_err(y[sorted(set(tokens))], ref) <= TOL
 
 
-def test_groups_cut_at_64_rows(mx8_on):
+def test_slot_with_more_pairs_than_tokens(mx8_on):
     # a token's pairs may name one slot twice: slot 0 takes two pairs of every
-    # token (128 or more pairs), so its run is cut into groups of 64 rows
+    # token (128 or more pairs), cut into groups of 48 rows
     M = mx8_on
-    wl = configs.scaled(configs.DECODE, H=512, I=256)
+    wl = configs.scaled(configs.DECODE, H=1024, I=512)
     P = Pools(M, wl, 3, shared=False)
     rng = np.random.default_rng(5)
     T, k = 64, 4
