@@ -199,13 +199,14 @@ __global__ void __launch_bounds__(kM8Threads, kM8CtasPerSm)
   volatile int* itq = (volatile int*)(tmem_slot + 1);  // [kM8Queue] item indices, -1 = no more
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = a.K / kM8KStage;
-
-  int ng = a.hdr[0], nr = a.hdr[1];
-  if (ng < 0 || ng > a.max_groups || nr < 0 || nr > ng) {
-    if (threadIdx.x == 0) atomicCAS(a.err, 0, MOE_ERR_INVALID);
-    ng = 0;
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    for (const CUtensorMap* m : {&mA0, &mA1, &mS0, &mS1, &mBh, &mBl})
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
   }
-  const int n_items = ng * a.tiles;
+  // the barriers and the tensor memory above do not depend on the previous
+  // kernel (the plan, or the gate/up GEMM): set them up before waiting for it
+  int ng = 0, nr = 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kM8Stages; ++s) {
       mbar_init(&full[s], 1 + 4);  // the TMA thread's expect_tx arrival + the scale-factor warps
@@ -230,6 +231,14 @@ __global__ void __launch_bounds__(kM8Threads, kM8CtasPerSm)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();
+  ng = a.hdr[0];
+  nr = a.hdr[1];
+  if (ng < 0 || ng > a.max_groups || nr < 0 || nr > ng) {
+    if (threadIdx.x == 0) atomicCAS(a.err, 0, MOE_ERR_INVALID);
+    ng = 0;
+  }
+  const int n_items = ng * a.tiles;
   // q-th item of this CTA for a consumer warp (whole warp): false on timeout
   auto next_item = [&](uint32_t q, int& it) -> bool {
     const int j = q % kM8Queue;
@@ -257,36 +266,40 @@ __global__ void __launch_bounds__(kM8Threads, kM8CtasPerSm)
       ok = publish(cur);
       if (cur >= 0) m8_prefetch_scales(a, m8_item(a, cur, ng, nr, false));
       while (ok && cur >= 0) {
-        int nxt = atomicAdd(a.ctr, 1) + (int)gridDim.x;
+        // the next item's ticket: its latency overlaps this item's loads
+        const int ticket = atomicAdd(a.ctr, 1);
+        const M8Item m = m8_item(a, cur, ng, nr, false);
+        if (m.run) {
+          const int nbx = m.n16 / 16;
+          const uint32_t bytes = (m.fp8 ? 2u * kM8ATile : (uint32_t)kM8ATile) + 2u * (uint32_t)nbx * 2048u;
+          const int row1 = a.mode == 0 ? m.f0 : m.f0 + 128;
+          for (int ks = 0; ks < nk; ++ks, ++gs) {
+            const int s = gs % kM8Stages;
+            const uint32_t r = gs / kM8Stages;
+            if (r > 0 && !(ok = mbar_wait_fast(&empty[s], (r - 1) & 1, a.err))) break;
+            uint8_t* st = sm + s * kM8Stage;
+            mbar_expect_tx(&full[s], bytes);
+            const int x = ks * kM8KStage;  // element coordinate: 64 (FP4) or 128 (E4M3) bytes, 16-byte multiples
+            if (m.fp8) {
+              tma_2d(st, &mS0, x, m.f0, &full[s]);
+              tma_2d(st + kM8ATile, &mS1, x, row1, &full[s]);
+            } else {
+              tma_3d(st, &mA0, x, m.f0, m.slot, &full[s]);
+              tma_3d(st + kM8ATile, &mA1, x, row1, m.slot, &full[s]);
+            }
+            uint8_t* bd = st + 2 * kM8ATile;
+            for (int bx = 0; bx < nbx; ++bx) {
+              tma_2d(bd + bx * 2048, &mBh, x, m.brow0 + 16 * bx, &full[s]);
+              tma_2d(bd + (nbx + bx) * 2048, &mBl, x, m.brow0 + 16 * bx, &full[s]);
+            }
+          }
+        }
+        if (!ok) break;
+        int nxt = ticket + (int)gridDim.x;
         if (nxt >= n_items) nxt = -1;
         if (!(ok = publish(nxt))) break;
         if (nxt >= 0) m8_prefetch_scales(a, m8_item(a, nxt, ng, nr, false));
-        const M8Item m = m8_item(a, cur, ng, nr, false);
         cur = nxt;
-        if (!m.run) continue;
-        const int nbx = m.n16 / 16;
-        const uint32_t bytes = (m.fp8 ? 2u * kM8ATile : (uint32_t)kM8ATile) + 2u * (uint32_t)nbx * 2048u;
-        const int row1 = a.mode == 0 ? m.f0 : m.f0 + 128;
-        for (int ks = 0; ks < nk; ++ks, ++gs) {
-          const int s = gs % kM8Stages;
-          const uint32_t r = gs / kM8Stages;
-          if (r > 0 && !(ok = mbar_wait_fast(&empty[s], (r - 1) & 1, a.err))) break;
-          uint8_t* st = sm + s * kM8Stage;
-          mbar_expect_tx(&full[s], bytes);
-          const int x = ks * kM8KStage;  // element coordinate: 64 (FP4) or 128 (E4M3) bytes, 16-byte multiples
-          if (m.fp8) {
-            tma_2d(st, &mS0, x, m.f0, &full[s]);
-            tma_2d(st + kM8ATile, &mS1, x, row1, &full[s]);
-          } else {
-            tma_3d(st, &mA0, x, m.f0, m.slot, &full[s]);
-            tma_3d(st + kM8ATile, &mA1, x, row1, m.slot, &full[s]);
-          }
-          uint8_t* bd = st + 2 * kM8ATile;
-          for (int bx = 0; bx < nbx; ++bx) {
-            tma_2d(bd + bx * 2048, &mBh, x, m.brow0 + 16 * bx, &full[s]);
-            tma_2d(bd + (nbx + bx) * 2048, &mBl, x, m.brow0 + 16 * bx, &full[s]);
-          }
-        }
       }
       if (!ok) {  // let copies already issued land before the CTA can exit
         const uint64_t t0 = gtimer();
@@ -666,7 +679,9 @@ moe_status mx8_gemm(const moe_expert_views* v, int mode, int T, int k, bool shar
   }
   const long long items = (long long)max_groups * a.tiles;
   const int grid = (int)std::max(1LL, std::min<long long>((long long)kM8CtasPerSm * mx8_sm_count(), items));
-  mx8_gemm_kernel<<<grid, kM8Threads, kM8Smem, stream>>>(mA0, mA1, mS0, mS1, mBh, mBl, a);
+  cudaError_t le = launch_pdl(mx8_gemm_kernel, dim3(grid), dim3(kM8Threads), (size_t)kM8Smem, stream, mA0, mA1, mS0,
+                              mS1, mBh, mBl, a);
+  if (le != cudaSuccess) return cuda_fail(le, mode == 0 ? "mx8_gemm_kernel (gate/up)" : "mx8_gemm_kernel (down)");
   return check_launch(mode == 0 ? "mx8_gemm_kernel (gate/up)" : "mx8_gemm_kernel (down)");
 }
 

@@ -549,6 +549,7 @@ __device__ void plan_mx8_rows(const FwdArgs& a, int t, int* dst) {
 
 __global__ void __launch_bounds__(1024) plan_kernel(FwdArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
+  pdl_launch_dependents();  // the block-scaled GEMM sets itself up meanwhile
   if (blockIdx.x > 0 && a.xhi) {
     plan_mx8_rows(a, blockIdx.x - 1, reinterpret_cast<int*>(smem_raw + 256));
     if (!a.tags) return;  // the fp16 copy below serves only the 2-bit pairs' CUDA-core kernels then
@@ -995,6 +996,7 @@ namespace moe {
 // Four consecutive outputs per thread (16-byte loads of o, all k issued before
 // use); per element the same fmaf chain in rank order as one element at a time.
 __global__ void __launch_bounds__(256) combine_kernel(FwdArgs a) {
+  pdl_wait();  // launched early behind the block-scaled down GEMM
   const int t = blockIdx.y;
   __shared__ float wk[64];
   __shared__ int pk[64];
@@ -1385,7 +1387,12 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
 
   dim3 cg((v->H / 4 + 255) / 256, T);
   ProfScope ps(MOE_K_COMBINE, stream);
-  combine_kernel<<<cg, 256, 0, stream>>>(a);
+  if (mx8) {
+    cudaError_t le = launch_pdl(combine_kernel, cg, dim3(256), 0, stream, a);
+    if (le != cudaSuccess) return cuda_fail(le, "combine_kernel");
+  } else {
+    combine_kernel<<<cg, 256, 0, stream>>>(a);
+  }
   return check_launch("combine_kernel");
 }
 
