@@ -90,6 +90,10 @@ def _peaks():
 # launch: a bench line scales the ratio to its own launches.  An entry is
 # removed when its kernel changes.
 NCU_TRAFFIC = {
+    ("mx8_gemm_kernel (gate/up)", "decode"): {
+        "dram_bytes": 503_352_064 + 4_839_936, "algorithmic_bytes": 505_278_464,
+        "capture": "ncu dram__bytes_read/write.sum of mx8_gemm_kernel gate/up, bench.py --workload forward --T 64 "
+                   "(trace step 3: 54 experts + shared), profiles/mx8_gemm_kernel_decode_forward_T64.md"},
     ("prefill_gemm_kernel (gate/up)", "prefill"): {
         "dram_bytes": 675_437_824 + 44_954_624, "algorithmic_bytes": 721_420_288,
         "capture": "ncu dram__bytes_read/write.sum of prefill_gemm_kernel gate/up, bench.py --workload prefill "

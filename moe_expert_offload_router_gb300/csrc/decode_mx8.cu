@@ -597,7 +597,7 @@ void mx8_carve(uint8_t* base, int H, int I, int rows, Mx8Bufs* b) {
   b->hsc = base + off;
 }
 
-moe_status mx8_gemm(const moe_expert_views* v, int mode, int T, int k, bool shared, int max_groups,
+moe_status mx8_gemm(const moe_expert_views* v, int mode, int T, int k, bool shared, int max_groups, int rows,
                     int* hdr, const Group* groups, const int* perm, const Mx8Bufs& b, float* o,
                     int32_t* d_error, cudaStream_t stream) {
   const int H = v->H, I = v->I, P = T * k;
@@ -606,7 +606,6 @@ moe_status mx8_gemm(const moe_expert_views* v, int mode, int T, int k, bool shar
   const size_t off_w3 = codes_hi + scales_hi, off_w2 = 2 * off_w3;
   const size_t f8_mat = (size_t)I * H + (size_t)I * 4;  // one shared w1 or w3 matrix (codes + row scales)
   const uint8_t* sh = shared ? v->shared : nullptr;
-  const int rows = P + T;
   Mx8Args a;
   a.mode = mode;
   a.K = mode == 0 ? H : I;

@@ -1311,8 +1311,8 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
   const long long max_groups = (long long)T * k + (T + kG - 1) / kG + 1;
   if (mx8) {
     ProfScope ps(MOE_K_GATEUP, stream);
-    if ((st = mx8_gemm(v, 0, T, k, a.shared != nullptr, (int)max_groups, a.hdr, a.groups, a.perm, mb, a.o, d_error,
-                       stream)) != MOE_OK)
+    if ((st = mx8_gemm(v, 0, T, k, a.shared != nullptr, (int)max_groups, a.P + T, a.hdr, a.groups, a.perm, mb,
+                       a.o, d_error, stream)) != MOE_OK)
       return st;
   } else if (mma) {
     auto launch = [&](auto kernel) -> moe_status {
@@ -1347,8 +1347,8 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
     MOE_CUDA(cudaStreamWaitEvent(stream, pass.down.ready[pass.down.n - 1], 0));
   if (mx8) {
     ProfScope ps(MOE_K_DOWN, stream);
-    if ((st = mx8_gemm(v, 1, T, k, a.shared != nullptr, (int)max_groups, a.hdr, a.groups, a.perm, mb, a.o, d_error,
-                       stream)) != MOE_OK)
+    if ((st = mx8_gemm(v, 1, T, k, a.shared != nullptr, (int)max_groups, a.P + T, a.hdr, a.groups, a.perm, mb,
+                       a.o, d_error, stream)) != MOE_OK)
       return st;
   } else if (mma) {
     {

@@ -78,10 +78,11 @@ struct Mx8Bufs {
 bool mx8_supported(const moe_expert_views* v);
 size_t mx8_bytes(int H, int I, int rows);
 void mx8_carve(uint8_t* base, int H, int I, int rows, Mx8Bufs* b);
+// rows: the operand buffers' rows (P + T with the shared expert's, else P).
 // mode 0: gate/up over the plan's groups (hdr, groups, perm; hdr[2 + mode] is the
 // item counter, zeroed by the plan) -> h operands in b;
 // mode 1: down -> o rows (pair index, or P + token for the shared expert).
-moe_status mx8_gemm(const moe_expert_views* v, int mode, int T, int k, bool shared, int max_groups,
+moe_status mx8_gemm(const moe_expert_views* v, int mode, int T, int k, bool shared, int max_groups, int rows,
                     int* hdr, const Group* groups, const int* perm, const Mx8Bufs& b, float* o,
                     int32_t* d_error, cudaStream_t stream);
 
