@@ -550,6 +550,7 @@ __device__ void plan_mx8_rows(const FwdArgs& a, int t, int* dst) {
 __global__ void __launch_bounds__(1024) plan_kernel(FwdArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   pdl_launch_dependents();  // the block-scaled GEMM sets itself up meanwhile
+  pdl_wait();               // launched early behind the slot ensure
   if (blockIdx.x > 0 && a.xhi) {
     plan_mx8_rows(a, blockIdx.x - 1, reinterpret_cast<int*>(smem_raw + 256));
     if (!a.tags) return;  // the fp16 copy below serves only the 2-bit pairs' CUDA-core kernels then
@@ -1298,7 +1299,8 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
     if ((st = set_smem(plan_kernel, plan_smem)) != MOE_OK) return st;
     {
       ProfScope ps(MOE_K_PLAN, stream);
-      plan_kernel<<<1 + T, 1024, plan_smem, stream>>>(a);
+      cudaError_t le = launch_pdl(plan_kernel, dim3(1 + T), dim3(1024), plan_smem, stream, a);
+      if (le != cudaSuccess) return cuda_fail(le, "plan_kernel");
     }
     if ((st = check_launch("plan_kernel")) != MOE_OK) return st;
   }

@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
                                                           int E, int k, int renorm,
                                                           int32_t* __restrict__ ids,
                                                           float* __restrict__ w) {
+  pdl_launch_dependents();  // the slot ensure may set up meanwhile
+  pdl_wait();               // launched early: the logits come from the previous work on the stream
   const int warp = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (warp >= T) return;
@@ -87,7 +89,8 @@ static moe_status launch_router(const float* logits, int T, int E, int k, int re
   const int tpb = 256, tok_per_block = tpb / 32;
   const int blocks = (T + tok_per_block - 1) / tok_per_block;
   ProfScope ps(MOE_K_ROUTER, s);
-  router_topk_kernel<VPL><<<blocks, tpb, 0, s>>>(logits, T, E, k, renorm, ids, w);
+  cudaError_t e = launch_pdl(router_topk_kernel<VPL>, dim3(blocks), dim3(tpb), 0, s, logits, T, E, k, renorm, ids, w);
+  if (e != cudaSuccess) return cuda_fail(e, "router_topk_kernel");
   return check_launch("router_topk_kernel");
 }
 

@@ -348,6 +348,8 @@ __global__ void __launch_bounds__(kEnsureThreads)
                        int lo, int hi, int mode, int tb, int32_t* miss_key, int32_t* miss_slot,
                        int32_t* miss_count, int32_t* tokens_done, int W, int CMAX) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
+  pdl_launch_dependents();  // the forward's plan may set up meanwhile
+  pdl_wait();               // launched early behind the router
   PassSmem s = carve(smem_raw, c.E, W, CMAX);
   Entries en{ids, nullptr, k, lo, hi, tb, max(T, tb)};
   const bool mark_rest = mode == MOE_FETCH_MARK_REST;
@@ -663,10 +665,11 @@ extern "C" moe_status moe_slot_ensure(moe_cache* cache, int layer_id, const int3
   moe_status st = prepare_smem((const void*)slot_ensure_kernel, smem);
   if (st != MOE_OK) return st;
   ProfScope ps(MOE_K_ENSURE, stream);
-  slot_ensure_kernel<<<1, kEnsureThreads, smem, stream>>>(
-      cache->dev, layer_id, ids, slots_out, T, k, rank_lo, rank_hi, mode, token_begin,
-      d_miss_key ? d_miss_key : d_miss_count, d_miss_slot ? d_miss_slot : d_miss_count,
-      d_miss_count, d_tokens_done, W, CMAX);
+  cudaError_t e = launch_pdl(slot_ensure_kernel, dim3(1), dim3(kEnsureThreads), smem, stream, cache->dev, layer_id,
+                             ids, slots_out, T, k, rank_lo, rank_hi, mode, token_begin,
+                             d_miss_key ? d_miss_key : d_miss_count, d_miss_slot ? d_miss_slot : d_miss_count,
+                             d_miss_count, d_tokens_done, W, CMAX);
+  if (e != cudaSuccess) return cuda_fail(e, "slot_ensure_kernel");
   return check_launch("slot_ensure_kernel");
 }
 
