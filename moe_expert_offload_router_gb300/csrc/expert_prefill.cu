@@ -610,7 +610,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 // group holds, for A, row m's four block scales (bytes 0..3) in lane m, column
 // group + m / 32; for B, row n's in lane 32 q + n % 32, column group + n / 32 of
 // every quadrant q.
-constexpr int kMxThreads = 256;   // warp 0 TMA, warp 1 MMA, warps 4-7 scale factors; all 8 the epilogue
+constexpr int kMxThreads = 384;   // warp 0 TMA, warp 1 MMA, warps 4-7 scale factors, warps 4-11 the epilogue
+constexpr int kMxQueue = 4;       // work indices published ahead to the consumer warps
 constexpr int kMxStages = 3;      // shared-memory stages of codes
 constexpr int kMxSfSlots = 2;     // tensor-memory slots of scale factors (stage ks in slot ks % 2)
 constexpr int kMxKStage = 256;    // K elements per stage: one 128-byte row of packed codes
@@ -625,7 +626,7 @@ constexpr int kMxSfBase = 2 * kMxNMax;  // first scale-factor column (after the 
 // +4; A tile 1 +8, +12; B window 0 +16 .. +22, window 1 +24 .. +30
 static_assert(kMxSfBase + 32 * kMxSfSlots <= 512, "tensor memory columns");
 static_assert(kMxNMax % 32 == 0 && kMxNMax / 32 <= 8 && kMxNMax <= 256, "B scale columns per window");
-static_assert((2 * kMxStages + 1) * 8 + 8 <= 256, "barrier area");
+static_assert((2 * kMxStages + 3 + 2 * kMxQueue) * 8 + 8 + 4 * kMxQueue <= 256, "barrier area");
 
 struct MxArgs {
   int mode;            // 0: gate/up + SwiGLU, h quantised to MXFP4; 1: down
@@ -638,6 +639,8 @@ struct MxArgs {
   const uint8_t* bsc;  // E8M0 scales of the activation rows [P][K / 32] (sorted order)
   const PfItem* items;
   const int* n_items;
+  int max_items;       // capacity of the item list
+  int* ctr;            // work counter (zeroed by the item kernel): work past the first gridDim.x is drawn from it
   const int* perm;     // sorted position -> pair index (mode 1 output rows)
   uint8_t* hq;         // mode 0 out: h codes [P][I / 2]
   uint8_t* hsc;        // mode 0 out: h scales [P][I / 32]
@@ -686,29 +689,28 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* full = (uint64_t*)(sm + kMxOffBar);  // [kMxStages]: TMA bytes + four scale-factor warps
   uint64_t* empty = full + kMxStages;             // [kMxStages]: the stage's MMAs completed
-  uint64_t* done = empty + kMxStages;
-  uint32_t* tmem_slot = (uint32_t*)(done + 1);
-  const int item_idx = blockIdx.x / a.tiles, tile = blockIdx.x % a.tiles;
-  if (item_idx >= *a.n_items) return;
-  const PfItem it = a.items[item_idx];
-  if (it.count < 1 || it.count > kMxNMax || it.slot < 0 || it.slot >= a.S || it.row0 < 0 ||
-      it.row0 + it.count > a.P) {  // the item kernel never produces these
-    if (threadIdx.x == 0) atomicCAS(a.err, 0, MOE_ERR_INVALID);
-    return;
-  }
+  uint64_t* accf = empty + kMxStages;             // the item's MMAs completed
+  uint64_t* acce = accf + 1;                      // the eight epilogue warps have read the accumulators
+  uint64_t* drain = acce + 1;
+  uint64_t* qfull = drain + 1;                    // [kMxQueue]: an item index published
+  uint64_t* qempty = qfull + kMxQueue;            // [kMxQueue]: the nine consumer warps have read it
+  uint32_t* tmem_slot = (uint32_t*)(qempty + kMxQueue);
+  volatile int* itq = (volatile int*)(tmem_slot + 1);  // [kMxQueue] work indices, -1 = no more
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = a.K / kMxKStage;
   const int sbytes = a.K / 32;  // scale bytes per row
-  const int n_mma = (it.count + 15) & ~15;
-  const int n_box = (it.count + 63) / 64;
-  const uint32_t b_bytes = (uint32_t)n_box * 64 * 128;
-  const int f0 = a.mode == 0 ? tile * 128 : tile * 256;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMxStages; ++s) {
       mbar_init(&full[s], 1 + 4);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(done, 1);
+    mbar_init(accf, 1);
+    mbar_init(acce, 8);
+    mbar_init(drain, 1);
+    for (int j = 0; j < kMxQueue; ++j) {
+      mbar_init(&qfull[j], 1);
+      mbar_init(&qempty[j], 1 + 8);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -720,25 +722,84 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  int n_it = *a.n_items;
+  if (n_it < 0 || n_it > a.max_items) {
+    if (threadIdx.x == 0) atomicCAS(a.err, 0, MOE_ERR_INVALID);
+    n_it = 0;
+  }
+  const int n_work = n_it * a.tiles;
+  // work index -> (item, feature tile); an item the item kernel never produces
+  // is skipped by every role (and flagged by the MMA warp)
+  struct Work {
+    PfItem it;
+    int f0, n_mma, n_box;
+    bool run;
+  };
+  auto work = [&](int w, bool flag) -> Work {
+    Work r;
+    r.it = a.items[w / a.tiles];
+    const int tile = w % a.tiles;
+    r.run = !(r.it.count < 1 || r.it.count > kMxNMax || r.it.slot < 0 || r.it.slot >= a.S || r.it.row0 < 0 ||
+              r.it.row0 + r.it.count > a.P);
+    if (!r.run && flag) atomicCAS(a.err, 0, MOE_ERR_INVALID);
+    r.f0 = a.mode == 0 ? tile * 128 : tile * 256;
+    r.n_mma = (r.it.count + 15) & ~15;
+    r.n_box = (r.it.count + 63) / 64;
+    return r;
+  };
+  // q-th work index of this CTA for a consumer warp (whole warp): false on timeout
+  auto next_work = [&](uint32_t q, int& w) -> bool {
+    const int j = q % kMxQueue;
+    if (!__all_sync(0xffffffffu, mbar_wait_fast(&qfull[j], (q / kMxQueue) & 1, a.err))) return false;
+    w = itq[j];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&qempty[j]);
+    return true;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
       bool ok = true;
-      for (int ks = 0; ks < nk && ok; ++ks) {
-        const int s = ks % kMxStages, r = ks / kMxStages;
-        if (r > 0 && !(ok = mbar_wait_fast(&empty[s], (r - 1) & 1, a.err))) break;
-        uint8_t* ad = sm + s * kMxAStage;
-        uint8_t* bd = sm + kMxOffB + s * kMxBStage;
-        mbar_expect_tx(&full[s], kMxAStage + b_bytes);
-        const int x = ks * 128;  // byte column of the stage's codes (a multiple of 16)
-        if (a.mode == 0) {
-          tma_3d(ad, &mA0, x, f0, it.slot, &full[s]);
-          tma_3d(ad + kMxATile, &mA1, x, f0, it.slot, &full[s]);
-        } else {
-          tma_3d(ad, &mA0, x, f0, it.slot, &full[s]);
-          tma_3d(ad + kMxATile, &mA0, x, f0 + 128, it.slot, &full[s]);
+      uint32_t gs = 0, q = 0;
+      auto publish = [&](int w) -> bool {
+        const int j = q % kMxQueue;
+        const uint32_t r = q / kMxQueue;
+        if (r > 0 && !mbar_wait_fast(&qempty[j], (r - 1) & 1, a.err)) return false;
+        itq[j] = w;
+        mbar_arrive(&qfull[j]);  // release: the index is visible to the warps that wait on it
+        ++q;
+        return true;
+      };
+      int cur = (int)blockIdx.x < n_work ? (int)blockIdx.x : -1;
+      ok = publish(cur);
+      while (ok && cur >= 0) {
+        const int ticket = atomicAdd(a.ctr, 1);  // the next work index; its latency overlaps these loads
+        const Work m = work(cur, false);
+        if (m.run) {
+          const uint32_t b_bytes = (uint32_t)m.n_box * 64 * 128;
+          for (int ks = 0; ks < nk; ++ks, ++gs) {
+            const int s = gs % kMxStages;
+            const uint32_t r = gs / kMxStages;
+            if (r > 0 && !(ok = mbar_wait_fast(&empty[s], (r - 1) & 1, a.err))) break;
+            uint8_t* ad = sm + s * kMxAStage;
+            uint8_t* bd = sm + kMxOffB + s * kMxBStage;
+            mbar_expect_tx(&full[s], kMxAStage + b_bytes);
+            const int x = ks * 128;  // byte column of the stage's codes (a multiple of 16)
+            if (a.mode == 0) {
+              tma_3d(ad, &mA0, x, m.f0, m.it.slot, &full[s]);
+              tma_3d(ad + kMxATile, &mA1, x, m.f0, m.it.slot, &full[s]);
+            } else {
+              tma_3d(ad, &mA0, x, m.f0, m.it.slot, &full[s]);
+              tma_3d(ad + kMxATile, &mA0, x, m.f0 + 128, m.it.slot, &full[s]);
+            }
+            for (int bx = 0; bx < m.n_box; ++bx) tma_2d(bd + bx * 64 * 128, &mB, x, m.it.row0 + bx * 64, &full[s]);
+          }
         }
-        for (int bx = 0; bx < n_box; ++bx) tma_2d(bd + bx * 64 * 128, &mB, x, it.row0 + bx * 64, &full[s]);
+        if (!ok) break;
+        int nxt = ticket + (int)gridDim.x;
+        if (nxt >= n_work) nxt = -1;
+        if (!(ok = publish(nxt))) break;
+        cur = nxt;
       }
       if (!ok) {  // let copies already issued land before the CTA can exit
         const uint64_t t0 = gtimer();
@@ -747,158 +808,185 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // MXF4 x MXF4 -> fp32, M = 128, N = n_mma, both operands K-major; scale
-    // factors E8M0; IDs 0 and 2 pick bytes 0-1 and 2-3 of a window's columns
-    const uint32_t idesc = (1u << 7) | (1u << 10) | ((uint32_t)(n_mma >> 3) << 17) | (1u << 23) |
-                           ((uint32_t)(128 >> 4) << 24);
-    const uint32_t id0 = idesc, id2 = idesc | (2u << 4) | (2u << 29);
     bool ok = true;
-    for (int ks = 0; ks < nk && ok; ++ks) {
-      const int s = ks % kMxStages, r = ks / kMxStages;
-      ok = __all_sync(0xffffffffu, mbar_wait_fast(&full[s], r & 1, a.err));
-      if (!ok) break;
+    uint32_t gs = 0, i = 0;
+    for (uint32_t qi = 0; ok; ++qi) {
+      int w;
+      if (!(ok = next_work(qi, w)) || w < 0) break;
+      const Work m = work(w, true);
+      if (!m.run) continue;
+      // the epilogue of the previous item has read the accumulators
+      if (i > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait_fast(acce, (i - 1) & 1, a.err)))) break;
+      ++i;
       tc_fence_after();
-      const uint64_t ad0 = umma_desc_sw128(su32(sm + s * kMxAStage));
-      const uint64_t ad1 = umma_desc_sw128(su32(sm + s * kMxAStage + kMxATile));
-      const uint64_t bd = umma_desc_sw128(su32(sm + kMxOffB + s * kMxBStage));
-      mma_mx_stage(tmem, tmem + kMxNMax, ad0, ad1, bd, id0, id2, tmem + kMxSfBase + 32 * (ks % kMxSfSlots),
-                   ks != 0, &empty[s]);
+      // MXF4 x MXF4 -> fp32, M = 128, N = n_mma, both operands K-major; scale
+      // factors E8M0; IDs 0 and 2 pick bytes 0-1 and 2-3 of a window's columns
+      const uint32_t idesc = (1u << 7) | (1u << 10) | ((uint32_t)(m.n_mma >> 3) << 17) | (1u << 23) |
+                             ((uint32_t)(128 >> 4) << 24);
+      const uint32_t id0 = idesc, id2 = idesc | (2u << 4) | (2u << 29);
+      for (int ks = 0; ks < nk; ++ks, ++gs) {
+        const int s = gs % kMxStages;
+        const uint32_t r = gs / kMxStages;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait_fast(&full[s], r & 1, a.err)))) break;
+        tc_fence_after();
+        const uint64_t ad0 = umma_desc_sw128(su32(sm + s * kMxAStage));
+        const uint64_t ad1 = umma_desc_sw128(su32(sm + s * kMxAStage + kMxATile));
+        const uint64_t bd = umma_desc_sw128(su32(sm + kMxOffB + s * kMxBStage));
+        mma_mx_stage(tmem, tmem + kMxNMax, ad0, ad1, bd, id0, id2, tmem + kMxSfBase + 32 * (gs % kMxSfSlots),
+                     ks != 0, &empty[s]);
+      }
+      if (ok) mma_commit_elect(accf);
     }
-    mma_commit_elect(done);
+    // every MMA this warp issued has completed before tensor memory is freed
+    mma_commit_elect(drain);
+    __syncwarp();
+    mbar_wait(drain, 0, a.err);
   } else if (warp >= 4) {
-    // scale factors: this warp's lane quadrant q (warp 4 + q may write only lanes 32 q .. 32 q + 31)
-    const int q = warp - 4;
-    const uint8_t* base_a = a.sc0 + (size_t)it.slot * a.B;
-    const uint8_t* sa0 = base_a + (size_t)(f0 + 32 * q + lane) * sbytes;
-    const uint8_t* sa1 = a.mode == 0 ? a.sc1 + (size_t)it.slot * a.B + (size_t)(f0 + 32 * q + lane) * sbytes
-                                     : base_a + (size_t)(f0 + 128 + 32 * q + lane) * sbytes;
-    const uint8_t* sb[kMxNMax / 32];
-#pragma unroll
-    for (int c = 0; c < kMxNMax / 32; ++c) {
-      const int n = 32 * c + lane;
-      sb[c] = a.bsc + (size_t)(it.row0 + (n < it.count ? n : 0)) * sbytes;  // rows past the item: any valid row
-    }
-    // a stage's scale words (per K window: A tile 0, A tile 1, B rows 32 c + lane)
-    // are loaded two stages ahead of their tensor-memory writes, through a ring
-    // of three register sets, so the loads' latency is off the per-stage path
-    struct Sf {
-      uint2 a0, a1, b[kMxNMax / 32];
-    };
-    auto load = [&](int ks, Sf& w) {
-      w.a0 = __ldg(reinterpret_cast<const uint2*>(sa0 + 8 * ks));  // x: window 0, y: window 1
-      w.a1 = __ldg(reinterpret_cast<const uint2*>(sa1 + 8 * ks));
-#pragma unroll
-      for (int c = 0; c < kMxNMax / 32; ++c) w.b[c] = __ldg(reinterpret_cast<const uint2*>(sb[c] + 8 * ks));
-    };
-    auto store = [&](int ks, const Sf& w) -> bool {
-      // the scale slot's previous stage (ks - kMxSfSlots) must have finished its
-      // MMAs, whose commit arrived on that stage's "empty" barrier.  This warp
-      // writes stage ks - 1's scales before stage ks's, and the MMAs of a stage
-      // wait for its scales, so that barrier is at most one phase behind.
-      const int p = ks - kMxSfSlots;
-      if (p >= 0 && !__all_sync(0xffffffffu, mbar_wait_fast(&empty[p % kMxStages], (p / kMxStages) & 1, a.err)))
-        return false;
-      uint32_t bw0[8], bw1[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        bw0[c] = c < kMxNMax / 32 ? w.b[c < kMxNMax / 32 ? c : 0].x : 0u;
-        bw1[c] = c < kMxNMax / 32 ? w.b[c < kMxNMax / 32 ? c : 0].y : 0u;
-      }
-      const uint32_t col = tmem + ((uint32_t)(32 * q) << 16) + kMxSfBase + 32 * (ks % kMxSfSlots);
-      tmem_st1(col + 0 + q, w.a0.x);
-      tmem_st1(col + 4 + q, w.a0.y);
-      tmem_st1(col + 8 + q, w.a1.x);
-      tmem_st1(col + 12 + q, w.a1.y);
-      tmem_st8(col + 16, bw0);
-      tmem_st8(col + 24, bw1);
-      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&full[ks % kMxStages]);
-      return true;
-    };
-    Sf ring[3];
-    load(0, ring[0]);
-    if (nk > 1) load(1, ring[1]);
+    // warps 4-7: per item the scale factors of every stage into lane quadrant
+    // q (warp 4 + q may write only lanes 32 q .. 32 q + 31), then half 0 of the
+    // epilogue; warps 8-11: half 1 of the epilogue
+    const int q = warp & 3, half = (warp - 4) >> 2;
     bool ok = true;
-    for (int k0 = 0; k0 < nk && ok; k0 += 3) {
+    uint32_t gs = 0, i = 0;
+    for (uint32_t qi = 0; ok; ++qi) {
+      int w;
+      if (!(ok = next_work(qi, w)) || w < 0) break;
+      const Work m = work(w, false);
+      if (!m.run) continue;
+      const PfItem it = m.it;
+      const int f0 = m.f0, n_mma = m.n_mma;
+      if (half == 0) {
+        const uint8_t* base_a = a.sc0 + (size_t)it.slot * a.B;
+        const uint8_t* sa0 = base_a + (size_t)(f0 + 32 * q + lane) * sbytes;
+        const uint8_t* sa1 = a.mode == 0 ? a.sc1 + (size_t)it.slot * a.B + (size_t)(f0 + 32 * q + lane) * sbytes
+                                         : base_a + (size_t)(f0 + 128 + 32 * q + lane) * sbytes;
+        const uint8_t* sb[kMxNMax / 32];
 #pragma unroll
-      for (int j = 0; j < 3; ++j) {
-        const int ks = k0 + j;
-        if (ks >= nk || !ok) break;
-        if (ks + 2 < nk) load(ks + 2, ring[(j + 2) % 3]);
-        ok = store(ks, ring[j]);
-      }
-    }
-  }
-
-  // epilogue: all 8 warps.  Warp w reads TMEM lane quadrant w % 4 and the
-  // columns [64 (w / 4), 64 (w / 4) + 64) of each accumulator.
-  {
-    __syncwarp();
-    bool ok = mbar_wait(done, 0, a.err);
-    ok = __all_sync(0xffffffffu, ok);
-    __syncwarp();
-    tc_fence_after();
-    const int q = warp & 3, half = warp >> 2;
-    const int row = q * 32 + lane;
-    const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
-    const int cb = half * (kMxNMax / 2), ce = min(cb + kMxNMax / 2, n_mma);
-    if (ok && a.mode == 0) {
-      // lane = feature f0 + row: gate (w1 row) in tile 0, up (w3 row) in tile 1.
-      // The 16 columns of a chunk go through each step together (independent
-      // warp reductions and shuffles), so their latencies overlap.
-      uint8_t* hq_base = a.hq + (size_t)(f0 + 32 * q) / 2 + lane / 2;
-      uint8_t* hsc_base = a.hsc + (size_t)(f0 + 32 * q) / 32;
-      for (int c0 = cb; c0 < ce; c0 += 16) {
-        uint32_t vg[16], vu[16];
-        tmem_ld16(tq + (uint32_t)c0, vg);
-        tmem_ld16(tq + (uint32_t)(kMxNMax + c0), vu);
-        float hv[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float hg = 0.5f * __uint_as_float(vg[j]), up = __uint_as_float(vu[j]);
-          hv[j] = fmaf(hg, tanh_approx(hg), hg) * up;
+        for (int c = 0; c < kMxNMax / 32; ++c) {
+          const int n = 32 * c + lane;
+          sb[c] = a.bsc + (size_t)(it.row0 + (n < it.count ? n : 0)) * sbytes;  // rows past the item: any valid row
         }
-        // the warp's 32 lanes hold 32 consecutive features of a column: one MX block
-        uint32_t am[16];
+        // a stage's scale words (per K window: A tile 0, A tile 1, B rows 32 c +
+        // lane) are loaded two stages ahead of their tensor-memory writes,
+        // through a ring of three register sets
+        struct Sf {
+          uint2 a0, a1, b[kMxNMax / 32];
+        };
+        auto load = [&](int ks, Sf& sf) {
+          sf.a0 = __ldg(reinterpret_cast<const uint2*>(sa0 + 8 * ks));  // x: window 0, y: window 1
+          sf.a1 = __ldg(reinterpret_cast<const uint2*>(sa1 + 8 * ks));
 #pragma unroll
-        for (int j = 0; j < 16; ++j) am[j] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv[j])));
-        uint32_t code[16], sbyte[16];
+          for (int c = 0; c < kMxNMax / 32; ++c) sf.b[c] = __ldg(reinterpret_cast<const uint2*>(sb[c] + 8 * ks));
+        };
+        auto store = [&](const Sf& sf) -> bool {
+          // the scale slot's previous stage (gs - kMxSfSlots) must have finished
+          // its MMAs, whose commit arrived on that stage's "empty" barrier.  This
+          // warp writes stage gs - 1's scales before stage gs's, and the MMAs of
+          // a stage wait for its scales, so that barrier is at most one phase behind.
+          const int p = (int)gs - kMxSfSlots;
+          if (p >= 0 && !__all_sync(0xffffffffu, mbar_wait_fast(&empty[p % kMxStages], (p / kMxStages) & 1, a.err)))
+            return false;
+          uint32_t bw0[8], bw1[8];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          sbyte[j] = mx_scale_byte(__uint_as_float(am[j]));
-          code[j] = mx_code(hv[j], mx_inv_scale(sbyte[j]));
-        }
-        uint32_t hi[16];
+          for (int c = 0; c < 8; ++c) {
+            bw0[c] = c < kMxNMax / 32 ? sf.b[c < kMxNMax / 32 ? c : 0].x : 0u;
+            bw1[c] = c < kMxNMax / 32 ? sf.b[c < kMxNMax / 32 ? c : 0].y : 0u;
+          }
+          const uint32_t col = tmem + ((uint32_t)(32 * q) << 16) + kMxSfBase + 32 * (gs % kMxSfSlots);
+          tmem_st1(col + 0 + q, sf.a0.x);
+          tmem_st1(col + 4 + q, sf.a0.y);
+          tmem_st1(col + 8 + q, sf.a1.x);
+          tmem_st1(col + 12 + q, sf.a1.y);
+          tmem_st8(col + 16, bw0);
+          tmem_st8(col + 24, bw1);
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[gs % kMxStages]);
+          ++gs;
+          return true;
+        };
+        Sf ring[3];
+        load(0, ring[0]);
+        if (nk > 1) load(1, ring[1]);
+        for (int k0 = 0; k0 < nk && ok; k0 += 3) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) hi[j] = __shfl_down_sync(0xffffffffu, code[j], 1);
-        // byte b of the block = codes of lanes 2b (low nibble) and 2b + 1
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int col = c0 + j;
-          if (col < it.count) {
-            const size_t prow = (size_t)(it.row0 + col);
-            if ((lane & 1) == 0) hq_base[prow * (a.I / 2)] = (uint8_t)(code[j] | (hi[j] << 4));
-            if (lane == 0) hsc_base[prow * (a.I / 32)] = (uint8_t)sbyte[j];
+          for (int j = 0; j < 3; ++j) {
+            const int ks = k0 + j;
+            if (ks >= nk || !ok) break;
+            if (ks + 2 < nk) load(ks + 2, ring[(j + 2) % 3]);
+            ok = store(ring[j]);
           }
         }
+        if (!ok) break;
       }
-    } else if (ok) {
-      for (int mt = 0; mt < 2; ++mt) {
-        const int feat = f0 + 128 * mt + row;
+      // epilogue: warp w reads TMEM lane quadrant w % 4 and the columns
+      // [112 half, 112 half + 112) of each accumulator
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait_fast(accf, i & 1, a.err)))) break;
+      ++i;
+      tc_fence_after();
+      const int row = q * 32 + lane;
+      const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+      const int cb = half * (kMxNMax / 2), ce = min(cb + kMxNMax / 2, n_mma);
+      if (a.mode == 0) {
+        // lane = feature f0 + row: gate (w1 row) in tile 0, up (w3 row) in tile 1.
+        // The 16 columns of a chunk go through each step together (independent
+        // warp reductions and shuffles), so their latencies overlap.
+        uint8_t* hq_base = a.hq + (size_t)(f0 + 32 * q) / 2 + lane / 2;
+        uint8_t* hsc_base = a.hsc + (size_t)(f0 + 32 * q) / 32;
         for (int c0 = cb; c0 < ce; c0 += 16) {
-          uint32_t v[16];
-          tmem_ld16(tq + (uint32_t)(mt * kMxNMax + c0), v);
-          const int cl = c0 + (lane & 15);
-          const int pl = cl < it.count ? a.perm[it.row0 + cl] : 0;
+          uint32_t vg[16], vu[16];
+          tmem_ld16(tq + (uint32_t)c0, vg);
+          tmem_ld16(tq + (uint32_t)(kMxNMax + c0), vu);
+          float hv[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const int p = __shfl_sync(0xffffffffu, pl, j);
-            if (c0 + j < it.count) a.o[(size_t)p * a.H + feat] = __uint_as_float(v[j]);
+            const float hg = 0.5f * __uint_as_float(vg[j]), up = __uint_as_float(vu[j]);
+            hv[j] = fmaf(hg, tanh_approx(hg), hg) * up;
+          }
+          // the warp's 32 lanes hold 32 consecutive features of a column: one MX block
+          uint32_t am[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) am[j] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv[j])));
+          uint32_t code[16], sbyte[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            sbyte[j] = mx_scale_byte(__uint_as_float(am[j]));
+            code[j] = mx_code(hv[j], mx_inv_scale(sbyte[j]));
+          }
+          uint32_t hi[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) hi[j] = __shfl_down_sync(0xffffffffu, code[j], 1);
+          // byte b of the block = codes of lanes 2b (low nibble) and 2b + 1
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int col = c0 + j;
+            if (col < it.count) {
+              const size_t prow = (size_t)(it.row0 + col);
+              if ((lane & 1) == 0) hq_base[prow * (a.I / 2)] = (uint8_t)(code[j] | (hi[j] << 4));
+              if (lane == 0) hsc_base[prow * (a.I / 32)] = (uint8_t)sbyte[j];
+            }
+          }
+        }
+      } else {
+        for (int mt = 0; mt < 2; ++mt) {
+          const int feat = f0 + 128 * mt + row;
+          for (int c0 = cb; c0 < ce; c0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(tq + (uint32_t)(mt * kMxNMax + c0), v);
+            const int cl = c0 + (lane & 15);
+            const int pl = cl < it.count ? a.perm[it.row0 + cl] : 0;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int p = __shfl_sync(0xffffffffu, pl, j);
+              if (c0 + j < it.count) a.o[(size_t)p * a.H + feat] = __uint_as_float(v[j]);
+            }
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce);
     }
   }
   tc_fence_before();
@@ -968,7 +1056,11 @@ __global__ void prefill_items_kernel(const int* offsets, int S, int nmax, PfItem
       items[pos++] = itm;
     }
   }
-  if (tid == 0) *n_items = total;
+  if (tid == 0) {
+    n_items[0] = total;
+    n_items[1] = 0;  // work counters of the persistent block-scaled GEMMs (gate/up, down)
+    n_items[2] = 0;
+  }
 }
 
 // One warp per sorted row: copy the token's bf16 row, and an fp16 copy scaled
@@ -1289,6 +1381,13 @@ moe_status grouped_gemm_fp4(const moe_expert_views* v, const uint16_t* x, int T,
 // (OCP MX), codes and E8M0 scales straight into kind::mxf4.  Buffers: b.xg holds
 // the packed x codes [P][H/2], b.xg16 their scales [P][H/32], b.hs the packed h
 // codes [P][I/2] followed (256-aligned) by their scales [P][I/32].
+static int sm_count_prefill() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
 moe_status grouped_gemm_mxf4(const moe_expert_views* v, const uint16_t* x, int T, int k, const int32_t* slots,
                              const GgBufs& b, int32_t* d_error, cudaStream_t stream) {
   const int H = v->H, I = v->I, S = v->fp4_num_slots;
@@ -1334,6 +1433,7 @@ moe_status grouped_gemm_mxf4(const moe_expert_views* v, const uint16_t* x, int T
   ma.B = B;
   ma.items = b.items;
   ma.n_items = b.nitems;
+  ma.max_items = max_items;
   ma.perm = b.perm;
   ma.hq = hq;
   ma.hsc = hsc;
@@ -1346,9 +1446,12 @@ moe_status grouped_gemm_mxf4(const moe_expert_views* v, const uint16_t* x, int T
   ma.sc0 = w1s;
   ma.sc1 = w3s;
   ma.bsc = xsc;
+  ma.ctr = b.nitems + 1;
+  // persistent: one CTA per SM (its tensor memory is the SM's 512 columns)
+  const int grid = (int)std::min<long long>(sm_count_prefill(), (long long)max_items * (I / 128));
   {
     ProfScope ps(MOE_K_GEMM_GATEUP, stream);
-    mxf4_gemm_kernel<<<max_items * ma.tiles, kMxThreads, kMxSmem, stream>>>(m1, m3, mx, ma);
+    mxf4_gemm_kernel<<<grid, kMxThreads, kMxSmem, stream>>>(m1, m3, mx, ma);
   }
   if ((st = check_launch("mxf4_gemm_kernel (gate/up)")) != MOE_OK) return st;
   // GEMM2: down over K = I, 256 output features per CTA
@@ -1358,9 +1461,10 @@ moe_status grouped_gemm_mxf4(const moe_expert_views* v, const uint16_t* x, int T
   ma.sc0 = w2s;
   ma.sc1 = w2s;
   ma.bsc = hsc;
+  ma.ctr = b.nitems + 2;
   {
     ProfScope ps(MOE_K_GEMM_DOWN, stream);
-    mxf4_gemm_kernel<<<max_items * ma.tiles, kMxThreads, kMxSmem, stream>>>(m2, m2, mh, ma);
+    mxf4_gemm_kernel<<<grid, kMxThreads, kMxSmem, stream>>>(m2, m2, mh, ma);
   }
   return check_launch("mxf4_gemm_kernel (down)");
 }
