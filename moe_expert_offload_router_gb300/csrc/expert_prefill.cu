@@ -699,7 +699,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = a.K / kMxKStage;
   const int sbytes = a.K / 32;  // scale bytes per row
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
+    for (const CUtensorMap* m : {&mA0, &mA1, &mB})
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
     for (int s = 0; s < kMxStages; ++s) {
       mbar_init(&full[s], 1 + 4);
       mbar_init(&empty[s], 1);
@@ -722,6 +725,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // launched early: the items, activations and counters come from the kernels before
   int n_it = *a.n_items;
   if (n_it < 0 || n_it > a.max_items) {
     if (threadIdx.x == 0) atomicCAS(a.err, 0, MOE_ERR_INVALID);
@@ -1003,6 +1007,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 // multiple of 256, so every lane takes part in every step.
 __global__ void gather_mxq_kernel(const uint16_t* x, int H, int k, const int* perm, const int* offsets, int S,
                                   uint8_t* xq, uint8_t* xsc) {
+  pdl_launch_dependents();  // the block-scaled GEMM sets itself up meanwhile
   const int n = offsets[S];
   const int lane = threadIdx.x & 31;
   const int units = H / 8;
@@ -1451,7 +1456,8 @@ moe_status grouped_gemm_mxf4(const moe_expert_views* v, const uint16_t* x, int T
   const int grid = (int)std::min<long long>(sm_count_prefill(), (long long)max_items * (I / 128));
   {
     ProfScope ps(MOE_K_GEMM_GATEUP, stream);
-    mxf4_gemm_kernel<<<grid, kMxThreads, kMxSmem, stream>>>(m1, m3, mx, ma);
+    cudaError_t le = launch_pdl(mxf4_gemm_kernel, dim3(grid), dim3(kMxThreads), (size_t)kMxSmem, stream, m1, m3, mx, ma);
+    if (le != cudaSuccess) return cuda_fail(le, "mxf4_gemm_kernel (gate/up)");
   }
   if ((st = check_launch("mxf4_gemm_kernel (gate/up)")) != MOE_OK) return st;
   // GEMM2: down over K = I, 256 output features per CTA
@@ -1464,7 +1470,8 @@ moe_status grouped_gemm_mxf4(const moe_expert_views* v, const uint16_t* x, int T
   ma.ctr = b.nitems + 2;
   {
     ProfScope ps(MOE_K_GEMM_DOWN, stream);
-    mxf4_gemm_kernel<<<grid, kMxThreads, kMxSmem, stream>>>(m2, m2, mh, ma);
+    cudaError_t le = launch_pdl(mxf4_gemm_kernel, dim3(grid), dim3(kMxThreads), (size_t)kMxSmem, stream, m2, m2, mh, ma);
+    if (le != cudaSuccess) return cuda_fail(le, "mxf4_gemm_kernel (down)");
   }
   return check_launch("mxf4_gemm_kernel (down)");
 }
