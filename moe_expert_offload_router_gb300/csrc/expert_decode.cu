@@ -508,13 +508,16 @@ __device__ __forceinline__ unsigned long long plan_key(const FwdArgs& a, int p) 
 // elements (mx.cuh), written to the rows of its FP4 pairs in the sorted order
 // (a pair's row is the number of kept keys below its own, the position the
 // sort of block 0 gives it) and to row P + t for the shared expert.
-__device__ void plan_mx8_rows(const FwdArgs& a, int t, int* dst) {
+__device__ void plan_mx8_rows(const FwdArgs& a, int t, int* dst, unsigned long long* keys) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // every pair's key, staged once in shared memory for the counts below
+  for (int q = threadIdx.x; q < a.P; q += blockDim.x) keys[q] = plan_key(a, q);
+  __syncthreads();
   for (int j = warp; j < a.k; j += (int)(blockDim.x >> 5)) {
     const int p = t * a.k + j;
-    const unsigned long long key = plan_key(a, p);
+    const unsigned long long key = keys[p];
     int below = 0;
-    for (int q = lane; q < a.P; q += 32) below += plan_key(a, q) < key;
+    for (int q = lane; q < a.P; q += 32) below += keys[q] < key;
     below = __reduce_add_sync(0xffffffffu, below);
     if (lane == 0) dst[j] = (key < ~0ull - 1 && (key >> 62) == MOE_POOL_FP4) ? below : -1;
   }
@@ -552,7 +555,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(FwdArgs a) {
   pdl_launch_dependents();  // the block-scaled GEMM sets itself up meanwhile
   pdl_wait();               // launched early behind the slot ensure
   if (blockIdx.x > 0 && a.xhi) {
-    plan_mx8_rows(a, blockIdx.x - 1, reinterpret_cast<int*>(smem_raw + 256));
+    plan_mx8_rows(a, blockIdx.x - 1, reinterpret_cast<int*>(smem_raw + 256),
+                  reinterpret_cast<unsigned long long*>(smem_raw + 1024));
     if (!a.tags) return;  // the fp16 copy below serves only the 2-bit pairs' CUDA-core kernels then
     __syncthreads();
   }
