@@ -620,13 +620,17 @@ constexpr int kMxAStage = 2 * kMxATile;
 constexpr int kMxBStage = 256 * 128;  // up to four 64-row boxes
 constexpr int kMxOffB = kMxStages * kMxAStage;
 constexpr int kMxOffBar = kMxOffB + kMxStages * kMxBStage;
-constexpr int kMxSmem = kMxOffBar + 256 + 1024;
+constexpr int kMxOffH = kMxOffBar + 256;          // gate/up: an item's h codes and scales before they go out
+constexpr int kMxHRow = 80;                        // per row: 128 features' codes, their 4 scale bytes, pad to 16 B
+static_assert(kMxHRow % 16 == 0 && kMxHRow >= 64 + 4, "staged h rows are read 16 bytes at a time");
+constexpr int kMxSmem = kMxOffH + kMxNMax * kMxHRow + 1024;
+static_assert(kMxSmem <= 232448, "shared memory per CTA");
 constexpr int kMxSfBase = 2 * kMxNMax;  // first scale-factor column (after the two accumulators)
 // per scale slot, 32 columns at kMxSfBase + 32 slot: A tile 0 (windows 0, 1) +0,
 // +4; A tile 1 +8, +12; B window 0 +16 .. +22, window 1 +24 .. +30
 static_assert(kMxSfBase + 32 * kMxSfSlots <= 512, "tensor memory columns");
 static_assert(kMxNMax % 32 == 0 && kMxNMax / 32 <= 8 && kMxNMax <= 256, "B scale columns per window");
-static_assert((2 * kMxStages + 3 + 2 * kMxQueue) * 8 + 8 + 4 * kMxQueue <= 256, "barrier area");
+static_assert((2 * kMxStages + 4 + 2 * kMxQueue) * 8 + 8 + 4 * kMxQueue <= 256, "barrier area");
 
 struct MxArgs {
   int mode;            // 0: gate/up + SwiGLU, h quantised to MXFP4; 1: down
@@ -694,7 +698,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   uint64_t* drain = acce + 1;
   uint64_t* qfull = drain + 1;                    // [kMxQueue]: an item index published
   uint64_t* qempty = qfull + kMxQueue;            // [kMxQueue]: the nine consumer warps have read it
-  uint32_t* tmem_slot = (uint32_t*)(qempty + kMxQueue);
+  uint64_t* esync = qempty + kMxQueue;            // the eight epilogue warps meet (h staging)
+  uint32_t* tmem_slot = (uint32_t*)(esync + 1);
   volatile int* itq = (volatile int*)(tmem_slot + 1);  // [kMxQueue] work indices, -1 = no more
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = a.K / kMxKStage;
@@ -714,6 +719,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       mbar_init(&qfull[j], 1);
       mbar_init(&qempty[j], 1 + 8);
     }
+    mbar_init(esync, 8);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -851,7 +857,14 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     // epilogue; warps 8-11: half 1 of the epilogue
     const int q = warp & 3, half = (warp - 4) >> 2;
     bool ok = true;
-    uint32_t gs = 0, i = 0;
+    uint32_t gs = 0, i = 0, nsync = 0;
+    // the eight epilogue warps meet (bounded, so a warp that gave up cannot
+    // leave the others waiting)
+    auto epi_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(esync);
+      return __all_sync(0xffffffffu, mbar_wait_fast(esync, (nsync++) & 1, a.err));
+    };
     for (uint32_t qi = 0; ok; ++qi) {
       int w;
       if (!(ok = next_work(qi, w)) || w < 0) break;
@@ -935,13 +948,18 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       if (a.mode == 0) {
         // lane = feature f0 + row: gate (w1 row) in tile 0, up (w3 row) in tile 1.
         // The 16 columns of a chunk go through each step together (independent
-        // warp reductions and shuffles), so their latencies overlap.
-        uint8_t* hq_base = a.hq + (size_t)(f0 + 32 * q) / 2 + lane / 2;
-        uint8_t* hsc_base = a.hsc + (size_t)(f0 + 32 * q) / 32;
+        // warp reductions and shuffles), so their latencies overlap.  The codes
+        // and scales collect in shared memory (a row per token: 64 code bytes,
+        // 4 scale bytes) and leave in 16-byte stores once every warp is done:
+        // one narrow store per column and warp cost half the epilogue.
+        uint8_t* hs = sm + kMxOffH;
+        if (!(ok = epi_sync())) break;  // the previous item's rows have left
         for (int c0 = cb; c0 < ce; c0 += 16) {
           uint32_t vg[16], vu[16];
-          tmem_ld16(tq + (uint32_t)c0, vg);
-          tmem_ld16(tq + (uint32_t)(kMxNMax + c0), vu);
+          tmem_ld16_nw(tq + (uint32_t)c0, vg);  // both loads in flight, one wait
+          tmem_ld16_nw(tq + (uint32_t)(kMxNMax + c0), vu);
+          tmem_ld_wait16(vg);
+          tmem_ld_fence16(vu);
           float hv[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -964,14 +982,26 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           // byte b of the block = codes of lanes 2b (low nibble) and 2b + 1
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const int col = c0 + j;
-            if (col < it.count) {
-              const size_t prow = (size_t)(it.row0 + col);
-              if ((lane & 1) == 0) hq_base[prow * (a.I / 2)] = (uint8_t)(code[j] | (hi[j] << 4));
-              if (lane == 0) hsc_base[prow * (a.I / 32)] = (uint8_t)sbyte[j];
-            }
+            uint8_t* hr = hs + (c0 + j) * kMxHRow;
+            if ((lane & 1) == 0) hr[16 * q + lane / 2] = (uint8_t)(code[j] | (hi[j] << 4));
+            if (lane == 0) hr[64 + q] = (uint8_t)sbyte[j];
           }
         }
+        // the accumulators are read: the next item's MMAs may start
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce);
+        if (!(ok = epi_sync())) break;
+        const int et = threadIdx.x - 128;  // 0 .. 255 over the eight epilogue warps
+        for (int e = et; e < it.count * 4; e += 256) {
+          const int r = e >> 2, part = e & 3;
+          *reinterpret_cast<uint4*>(a.hq + (size_t)(it.row0 + r) * (a.I / 2) + f0 / 2 + 16 * part) =
+              *reinterpret_cast<const uint4*>(hs + r * kMxHRow + 16 * part);
+        }
+        for (int r = et; r < it.count; r += 256)
+          *reinterpret_cast<uint32_t*>(a.hsc + (size_t)(it.row0 + r) * (a.I / 32) + f0 / 32) =
+              *reinterpret_cast<const uint32_t*>(hs + r * kMxHRow + 64);
+        continue;
       } else {
         for (int mt = 0; mt < 2; ++mt) {
           const int feat = f0 + 128 * mt + row;
