@@ -94,6 +94,10 @@ NCU_TRAFFIC = {
         "dram_bytes": 503_352_064 + 4_839_936, "algorithmic_bytes": 505_278_464,
         "capture": "ncu dram__bytes_read/write.sum of mx8_gemm_kernel gate/up, bench.py --workload forward --T 64 "
                    "(trace step 3: 54 experts + shared), profiles/mx8_gemm_kernel_decode_forward_T64.md"},
+    ("mxf4_gemm_kernel (gate/up)", "prefill"): {
+        "dram_bytes": 597_573_888 + 12_905_216, "algorithmic_bytes": 610_533_376,
+        "capture": "ncu dram__bytes_read/write.sum of mxf4_gemm_kernel gate/up, bench.py --workload prefill "
+                   "--prefill-experts 64 --prefill-tokens 2048, profiles/mxf4_gemm_kernel_prefill_E64_T2048.md"},
     ("prefill_gemm_kernel (gate/up)", "prefill"): {
         "dram_bytes": 675_437_824 + 44_954_624, "algorithmic_bytes": 721_420_288,
         "capture": "ncu dram__bytes_read/write.sum of prefill_gemm_kernel gate/up, bench.py --workload prefill "
@@ -985,8 +989,13 @@ def other_entry(args, name):
                                  "shared memory on every SM (moe_fp4_mma_peak)",
                 "step_frac_of_hbm_floor": floor_ms / ms_mx,
             }
+            # algorithmic bytes of the launch: the experts' w1 + w3 codes and scales,
+            # x's MXFP4 codes and scales read, h's written
+            mx_bytes = E * gu4 + P * (H // 2 + H // 32) + P * (I // 2 + I // 32)
+            mx_traffic, mx_src = ncu_traffic("mxf4_gemm_kernel (gate/up)", "prefill", mx_bytes)
             out["roofline_fp4"] = {"bound": "tensor", "achieved": mgu_tf, "peak": fp4_peak, "unit": "TFLOP/s",
-                                   "frac": mgu_tf / fp4_peak, "traffic": None,
+                                   "frac": mgu_tf / fp4_peak, "traffic": mx_traffic, "traffic_source": mx_src,
+                                   "bytes_per_launch": mx_bytes,
                                    "kernel": "mxf4_gemm_kernel (gate/up)", "peak_kind": out["a_mxfp4"]["fp4_peak_kind"],
                                    "ms_per_launch": mgu, "flops_per_launch": 4.0 * P * H * I}
         else:
