@@ -22,7 +22,7 @@
 // B operand of 2n rows (one MMA per K slice and tile), and the epilogue adds
 // the accumulator's two halves.
 //
-// Persistent CTAs, two per SM (192 threads, 90 KB of shared memory and 256
+// Persistent CTAs, two per SM (192 threads, 98 KB of shared memory and 256
 // tensor-memory columns each): one CTA's TMA engine moves the 64-byte rows of
 // the packed E2M1 tiles at about two thirds of an SM's share of HBM, two
 // together at the full rate, and one CTA streams while the other runs its
@@ -36,12 +36,15 @@
 //               per stage), commits to the stage's "empty" barrier and, after
 //               the item's last stage, to the accumulators' "full" barrier
 //   warps 2-5   per item: the A and B scale words of every stage into their
-//               TMEM lane quadrant (two stages of loads ahead), then the
+//               TMEM lane quadrant (A rows read 16 bytes per four stages, the
+//               group's B scale rows copied to shared memory once), then the
 //               epilogue: gate/up -> h = SiLU(gate) * up, itself split into
 //               E4M3 hi/lo with a scale per 32 features (the down GEMM's B
 //               operand, in the same sorted row order); down -> fp32 rows of
 //               o per pair for the router-weighted combine
-// Every mbarrier wait gives up after one second and records MOE_ERR_TIMEOUT.
+// Launched with programmatic stream serialization: barriers, tensor memory and
+// tensor-map prefetches are set up while the previous kernel finishes.  Every
+// mbarrier wait gives up after one second and records MOE_ERR_TIMEOUT.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
