@@ -682,10 +682,13 @@ __device__ __forceinline__ void mma_mx_stage(uint32_t d0, uint32_t d1, uint64_t 
       : "memory");
 }
 
-// Block-scaled FP4 grouped GEMM of one (item, feature tile): mode 0 computes
-// 128 features' gate (w1) and up (w3) rows over K = H and writes h = SiLU(gate)
-// * up quantised to MXFP4 along I; mode 1 computes 256 rows of w2 over K = I and
-// writes fp32 outputs per pair.
+// Block-scaled FP4 grouped GEMM, persistent (one CTA per SM): each work unit
+// (item, feature tile) of mode 0 computes 128 features' gate (w1) and up (w3)
+// rows over K = H and writes h = SiLU(gate) * up quantised to MXFP4 along I;
+// of mode 1, 256 rows of w2 over K = I, written as fp32 outputs per pair.  CTA c
+// starts with unit c and draws the next from a counter the item kernel zeroes;
+// warp 0 publishes each to the other warps through a queue in shared memory and
+// loads the next unit's stages while the current one's epilogue runs.
 __global__ void __launch_bounds__(kMxThreads, 1)
     mxf4_gemm_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
                      const __grid_constant__ CUtensorMap mB, MxArgs a) {
