@@ -478,12 +478,14 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   return r;
 }
 
-// Power-of-two exponent s with amax * 2^-s in [1, 2) (0 when amax is 0).
+// Power-of-two exponent s with amax * 2^-s in [1, 2) (0 when amax is 0),
+// at least -126 so that 2^s is a normal float for the epilogues that multiply
+// it back (a smaller amax is scaled up by 2^126 only).
 __device__ __forceinline__ int pow2_exponent(float amax) {
   if (!(amax > 0.f)) return 0;
   int e;
   frexpf(amax, &e);
-  return e - 1;
+  return max(-126, e - 1);
 }
 
 // Tokens per group: the warp-MMA kernels' pools take a.mma_group, the others kG.

@@ -533,29 +533,53 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   // accumulator's chunks in turn.
   {
     __syncwarp();
-    bool ok = mbar_wait(done, 0, a.err);
-    ok = __all_sync(0xffffffffu, ok);
-    __syncwarp();
-    tc_fence_after();
-    if (warp == kWarpRaw) f16 = *(volatile int*)f16_flag != 0;  // final: every converter has passed the vote
+    // the raw-code producer warp did not take part in the vote: it reads the
+    // result once the MMAs are done; the other warps load the per-column
+    // values of their chunks (the activation copy's row exponents, or the
+    // pair of each column) before they wait
+    bool ok = true;
+    if (warp == kWarpRaw) {
+      ok = __all_sync(0xffffffffu, mbar_wait(done, 0, a.err));
+      __syncwarp();
+      f16 = *(volatile int*)f16_flag != 0;
+    }
     const int q = warp & 3, part = warp >> 2;
     const int row = q * 32 + lane;  // D row = A tile row
     const int nchunks = n_mma / 16;
     const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
-    if (ok && a.mode == 0) {
+    constexpr int kParts = kPfWarps / 4;
+    if (a.mode == 0) {
+      constexpr int kMaxChunks = (C::kNMax / 16 + kParts - 1) / kParts;
+      static_assert(kMaxChunks <= 4, "one word of packed exponents");
       const int feat = f0 + row;
       const float rg = FP8 ? a.rs0[feat] : 1.f, ru = FP8 ? a.rs1[feat] : 1.f;
-      for (int c0 = part * 16; c0 < n_mma; c0 += kPfWarps / 4 * 16) {
+      // chunk i's exponent (|e| < 128) for column c0 + j in byte i of lane j
+      uint32_t sgw = 0;
+#pragma unroll
+      for (int i = 0; i < kMaxChunks; ++i) {
+        const int cl = part * 16 + i * kParts * 16 + (lane & 15);
+        const uint32_t e = (f16 && cl < it.count) ? ((uint32_t)a.xsig[it.row0 + cl] & 0xffu) : 0u;
+        sgw |= e << (8 * i);
+      }
+      if (warp != kWarpRaw) {
+        ok = __all_sync(0xffffffffu, mbar_wait(done, 0, a.err));
+        __syncwarp();
+      }
+      tc_fence_after();
+#pragma unroll 1
+      for (int i = 0; ok && i < kMaxChunks; ++i) {
+        const int c0 = part * 16 + i * kParts * 16;
+        if (c0 >= n_mma) break;
+        const int sg = (int)(sgw << (24 - 8 * i)) >> 24;
         uint32_t vg[16], vu[16];
-        tmem_ld16(tq + (uint32_t)c0, vg);
-        tmem_ld16(tq + (uint32_t)(256 + c0), vu);
-        // lane j < 16 holds column c0 + j's power-of-two rescale of the fp16 activation copy
-        const int cl = c0 + (lane & 15);
-        const int sgl = (f16 && cl < it.count) ? a.xsig[it.row0 + cl] : 0;
+        tmem_ld16_nw(tq + (uint32_t)c0, vg);
+        tmem_ld16_nw(tq + (uint32_t)(256 + c0), vu);
+        tmem_ld_wait16(vg);
+        tmem_ld_fence16(vu);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int col = c0 + j;
-          const float sc = __uint_as_float((uint32_t)(127 + __shfl_sync(0xffffffffu, sgl, j)) << 23);
+          const float sc = __uint_as_float((uint32_t)(127 + __shfl_sync(0xffffffffu, sg, j)) << 23);
           if (col < it.count) {
             // SiLU(g) = g * sigmoid(g) with sigmoid(g) = (1 + tanh(g / 2)) / 2: one
             // hardware tanh (relative error ~2^-11, below h's bf16 rounding)
@@ -571,19 +595,34 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
         }
       }
-    } else if (ok) {
-      for (int cc = part; cc < kPfMT * nchunks; cc += kPfWarps / 4) {
+    } else {
+      constexpr int kMaxChunks = (kPfMT * C::kNMax / 16 + kParts - 1) / kParts;
+      static_assert(kPfMT == 2, "two row scales");
+      const float rw0 = FP8 ? a.rs0[f0 + row] : 1.f, rw1 = FP8 ? a.rs0[f0 + 128 + row] : 1.f;
+      int plv[kMaxChunks];  // lane j < 16: the output row of column c0 + j of chunk i
+#pragma unroll
+      for (int i = 0; i < kMaxChunks; ++i) {
+        const int cc = part + i * kParts;
+        const int cl = (nchunks > 0 ? cc % nchunks : 0) * 16 + (lane & 15);
+        plv[i] = (cc < kPfMT * nchunks && cl < it.count) ? (FP8 ? a.o_row0 + it.row0 + cl : a.perm[it.row0 + cl]) : 0;
+      }
+      if (warp != kWarpRaw) {
+        ok = __all_sync(0xffffffffu, mbar_wait(done, 0, a.err));
+        __syncwarp();
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int i = 0; i < kMaxChunks; ++i) {
+        const int cc = part + i * kParts;
+        if (!ok || cc >= kPfMT * nchunks) break;
         const int mt = cc / nchunks, c0 = (cc % nchunks) * 16;
         uint32_t v[16];
         tmem_ld16(tq + (uint32_t)(mt * 256 + c0), v);
         const int feat = f0 + 128 * mt + row;
-        const float rw = FP8 ? a.rs0[feat] : 1.f;
-        const int cl = c0 + (lane & 15);
-        const int pl = cl < it.count ? (FP8 ? a.o_row0 + it.row0 + cl : a.perm[it.row0 + cl]) : 0;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const int p = __shfl_sync(0xffffffffu, pl, j);
-          if (c0 + j < it.count) a.o[(size_t)p * a.H + feat] = __uint_as_float(v[j]) * rw;
+          const int p = __shfl_sync(0xffffffffu, plv[i], j);
+          if (c0 + j < it.count) a.o[(size_t)p * a.H + feat] = __uint_as_float(v[j]) * (mt ? rw1 : rw0);
         }
       }
     }
