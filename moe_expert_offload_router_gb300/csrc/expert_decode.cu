@@ -41,6 +41,7 @@ constexpr int kFwdThreads = 256;  // 8 warps
 constexpr int kRowsGateUp = 32;   // rows of w1/w3 per gate/up work item
 constexpr int kRowsDown = 64;     // rows of w2 per down work item
 constexpr int kMaxPlanPairs = 4096;
+constexpr int kPlanBins = 4096;  // (pool, slot) bins of the plan's counting sort (FP4 slots, then 2-bit)
 constexpr int kGemmMinPairs = 256;  // from here on the FP4 routed pairs take the tcgen05 grouped GEMM
 
 // Decode batches up to this many tokens get the block-scaled GEMM's operand
@@ -552,6 +553,105 @@ __device__ void plan_mx8_rows(const FwdArgs& a, int t, int* dst, unsigned long l
   }
 }
 
+// After the routed groups: the shared expert's groups (runs of its group
+// size over the tokens) and the header (one thread).
+__device__ void plan_finish(const FwdArgs& a, int ngroups, bool bad) {
+  int n = ngroups;
+  if (a.shared) {
+    const int gs = group_size(a, MOE_POOL_SHARED);
+    for (int t0 = 0; t0 < a.T; t0 += gs) {
+      Group g;
+      g.pool = MOE_POOL_SHARED;
+      g.slot = 0;
+      g.begin = t0;
+      g.count = min(gs, a.T - t0);
+      a.groups[n++] = g;
+    }
+  }
+  a.hdr[0] = n;
+  a.hdr[1] = ngroups;
+  a.hdr[2] = 0;  // work counters of the warp-MMA gate/up and down kernels
+  a.hdr[3] = 0;
+  if (a.err && bad) atomicCAS(a.err, 0, MOE_ERR_INVALID);  // the caller's call cleared it
+}
+
+// Block 0 of the plan when the (pool, slot) bins fit in shared memory: a
+// stable counting sort.  Bin of a kept pair = its FP4 slot, or n4 + its 2-bit
+// slot, so bin order is the (pool, slot) order; the bins' counts give each
+// bin's first sorted position and its groups (runs cut every group-size
+// pairs) directly, and one warp places the pairs 32 at a time in pair order
+// (rank among equal bins by __match_any_sync), so that each bin keeps its
+// pairs in increasing pair index: the order a sort on (pool, slot, pair)
+// gives.
+__device__ void plan_groups_counting(const FwdArgs& a, uint8_t* smem_raw) {
+  int* cnt = reinterpret_cast<int*>(smem_raw);  // [kPlanBins] pairs per bin
+  int* cur = cnt + kPlanBins;                   // [kPlanBins] next sorted position of each bin
+  int* binv = cur + kPlanBins;                  // [kMaxPlanPairs] bin of each pair, -1 if left out
+  int* ws = binv + kMaxPlanPairs;               // [34] scan workspace
+  int* scal = ws + 34;
+  const int P = a.P, nb = a.n4 + a.n2;
+  const int tid = threadIdx.x, NT = blockDim.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int b = tid; b < nb; b += NT) cnt[b] = 0;
+  if (tid == 0) scal[0] = 0;
+  __syncthreads();
+  for (int p = tid; p < P; p += NT) {
+    const unsigned long long key = plan_key(a, p);
+    int b = -1;
+    if (key == ~0ull - 1) {
+      scal[0] = 1;
+    } else if (key != ~0ull) {
+      const int slot = (int)((key >> 32) & 0x3fffffffu);
+      b = (key >> 62) == MOE_POOL_FP4 ? slot : a.n4 + slot;
+      atomicAdd(&cnt[b], 1);
+    }
+    binv[p] = b;
+  }
+  __syncthreads();
+  // each thread takes a run of bins: their pairs and groups, scanned over the block
+  const int per = (nb + NT - 1) / NT;
+  const int b0 = min(nb, tid * per), b1 = min(nb, b0 + per);
+  auto gsize = [&](int b) { return group_size(a, b < a.n4 ? MOE_POOL_FP4 : MOE_POOL_INT2); };
+  int np = 0, ng = 0;
+  for (int b = b0; b < b1; ++b) {
+    np += cnt[b];
+    ng += (cnt[b] + gsize(b) - 1) / gsize(b);
+  }
+  int V, ngroups;
+  int pos = block_exclusive_scan(np, ws, &V);
+  int gi = block_exclusive_scan(ng, ws, &ngroups);
+  for (int b = b0; b < b1; ++b) {
+    cur[b] = pos;
+    const int gs = gsize(b);
+    for (int j = 0; j < cnt[b]; j += gs) {
+      Group g;
+      g.pool = b < a.n4 ? MOE_POOL_FP4 : MOE_POOL_INT2;
+      g.slot = b < a.n4 ? b : b - a.n4;
+      g.begin = pos + j;
+      g.count = min(gs, cnt[b] - j);
+      a.groups[gi++] = g;
+    }
+    pos += cnt[b];
+  }
+  __syncthreads();
+  if (warp == 0) {
+    for (int c0 = 0; c0 < P; c0 += 32) {
+      const int p = c0 + lane;
+      const int b = p < P ? binv[p] : -1;
+      const unsigned m = __match_any_sync(0xffffffffu, b);
+      const int base = b >= 0 ? cur[b] : 0;
+      __syncwarp();
+      if (b >= 0) {
+        a.perm[base + __popc(m & ((1u << lane) - 1u))] = p;
+        if (lane == __ffs(m) - 1) cur[b] = base + __popc(m);
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  if (tid == 0) plan_finish(a, ngroups, scal[0] != 0);
+}
+
 __global__ void __launch_bounds__(1024) plan_kernel(FwdArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   pdl_launch_dependents();  // the block-scaled GEMM sets itself up meanwhile
@@ -580,6 +680,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(FwdArgs a) {
   // block 0: group kept pairs by (pool, slot); a routed-GEMM pass has no GEMV
   // groups (its grouping kernels check the slots), only the activation prep
   if (a.routed_gemm) return;
+  if (a.n4 + a.n2 <= kPlanBins) return plan_groups_counting(a, smem_raw);
   unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem_raw);
   int* ws = reinterpret_cast<int*>(keys + kMaxPlanPairs);
   int* scal = ws + 34;
@@ -663,25 +764,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(FwdArgs a) {
     a.groups[gi++] = g;
   }
   __syncthreads();
-  if (tid == 0) {
-    int n = ngroups;
-    if (a.shared) {
-      const int gs = group_size(a, MOE_POOL_SHARED);
-      for (int t0 = 0; t0 < a.T; t0 += gs) {
-        Group g;
-        g.pool = MOE_POOL_SHARED;
-        g.slot = 0;
-        g.begin = t0;
-        g.count = min(gs, a.T - t0);
-        a.groups[n++] = g;
-      }
-    }
-    a.hdr[0] = n;
-    a.hdr[1] = ngroups;
-    a.hdr[2] = 0;  // work counters of the warp-MMA gate/up and down kernels
-    a.hdr[3] = 0;
-    if (a.err && scal[0]) atomicCAS(a.err, 0, MOE_ERR_INVALID);  // the caller's call cleared it
-  }
+  if (tid == 0) plan_finish(a, ngroups, scal[0] != 0);
 }
 
 // ---------------------------------------------------------- gate/up kernel --
@@ -1301,7 +1384,8 @@ static moe_status forward_pass(const moe_expert_views* v, const uint16_t* x, int
   const bool shared_gemm = a.routed_gemm && a.shared != nullptr;
   const bool gemv = !a.routed_gemm;
   if (gemv || shared_gemm) {
-    const size_t plan_smem = (size_t)kMaxPlanPairs * 12 + 64 * 4;
+    const size_t plan_smem = std::max((size_t)kMaxPlanPairs * 12 + 64 * 4,
+                                      (size_t)(2 * kPlanBins + kMaxPlanPairs + 64) * 4);
     if ((st = set_smem(plan_kernel, plan_smem)) != MOE_OK) return st;
     {
       ProfScope ps(MOE_K_PLAN, stream);
