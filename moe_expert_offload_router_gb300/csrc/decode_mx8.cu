@@ -37,7 +37,8 @@
 //               the item's last stage, to the accumulators' "full" barrier
 //   warps 2-5   per item: the A and B scale words of every stage into their
 //               TMEM lane quadrant (A rows read 16 bytes per four stages, the
-//               group's B scale rows copied to shared memory once), then the
+//               group's B scale rows copied to shared memory once, one item
+//               ahead), then the
 //               epilogue: gate/up -> h = SiLU(gate) * up, itself split into
 //               E4M3 hi/lo with a scale per 32 features (the down GEMM's B
 //               operand, in the same sorted row order); down -> fp32 rows of
@@ -67,7 +68,7 @@ constexpr int kM8Stage = 2 * kM8ATile + kM8BBytes;
 constexpr int kM8OffBar = kM8Stages * kM8Stage;
 constexpr int kM8OffSB = kM8OffBar + 256;       // the group's B scale rows, padded by 16 bytes
 constexpr int kM8SBBytes = kMx8MaxRows * (4096 / 32 + 16);  // K up to 4096
-constexpr int kM8Smem = kM8OffSB + kM8SBBytes + 1024;
+constexpr int kM8Smem = kM8OffSB + 2 * kM8SBBytes + 1024;  // two B scale buffers (this item, the next)
 constexpr int kM8AccCols = 2 * kMx8MaxRows;     // TMEM columns per accumulator (hi and lo halves)
 constexpr int kM8SfBase = 2 * kM8AccCols;       // the two accumulators, then the scale factors
 constexpr int kM8SfCols = 16;                   // per stage: A tile 0 +0..3, A tile 1 +4..7, B +8..10
@@ -352,7 +353,10 @@ __global__ void __launch_bounds__(kM8Threads, kM8CtasPerSm)
     // registers (up to 32 stages at a time, one load per 16 bytes, the rest of
     // each line from L1), and the group's B rows go to shared memory in one
     // coalesced copy by the four warps; scattered 4-byte loads per stage cost
-    // about as many L2 requests as the TMA's own and slowed it down.
+    // about as many L2 requests as the TMA's own and slowed it down.  The B
+    // rows have two buffers: the next item's are copied right after the
+    // current item's last scale-factor store, while its last MMAs complete,
+    // so the next item's first stage does not wait for the copy.
     const int q = warp & 3;
     const int tid = threadIdx.x - 64;  // 0 .. 127 over the four warps
     const int sbytes = a.K / 32;
@@ -367,20 +371,36 @@ __global__ void __launch_bounds__(kM8Threads, kM8CtasPerSm)
       if (lane == 0) mbar_arrive(sbar);
       return __all_sync(0xffffffffu, mbar_wait_fast(sbar, (nsync++) & 1, a.err));
     };
-    for (uint32_t qi = 0; ok; ++qi) {
-      int it;
-      if (!(ok = next_item(qi, it)) || it < 0) break;
-      const M8Item m = m8_item(a, it, ng, nr, false);
-      if (!m.run) continue;
-      // the group's B scale rows (contiguous in global memory) -> shared memory
-      if (!(ok = group_sync())) break;  // every warp is done with the previous item's copy
-      {
-        const uint8_t* gB = a.bsc + (size_t)m.brow0 * sbytes;
-        const int cpr = sbytes / 16, n = m.count * cpr;
-        for (int c = tid; c < n; c += 128)
-          *reinterpret_cast<uint4*>(sB + (c / cpr) * srow + 16 * (c % cpr)) = ldg_u128(gB + 16 * c);
+    uint32_t qi = 0;
+    // the next item that runs (items no role computes are skipped): its
+    // index, -1 at the end of the list, -2 on a timeout
+    auto take_run = [&](M8Item& mm) -> int {
+      for (;;) {
+        int it;
+        if (!next_item(qi++, it)) return -2;
+        if (it < 0) return -1;
+        mm = m8_item(a, it, ng, nr, false);
+        if (mm.run) return it;
       }
+    };
+    // an item's B scale rows (contiguous in global memory) -> shared buffer b
+    auto copy_b = [&](const M8Item& mm, int b) {
+      uint8_t* dst = sB + b * kM8SBBytes;
+      const uint8_t* gB = a.bsc + (size_t)mm.brow0 * sbytes;
+      const int cpr = sbytes / 16, n = mm.count * cpr;
+      for (int c = tid; c < n; c += 128)
+        *reinterpret_cast<uint4*>(dst + (c / cpr) * srow + 16 * (c % cpr)) = ldg_u128(gB + 16 * c);
+    };
+    M8Item m;
+    int it = take_run(m);
+    ok = it != -2;
+    int buf = 0;
+    if (it >= 0) copy_b(m, 0);
+    while (ok && it >= 0) {
+      // every warp's share of this item's B scale rows is in buffer buf (and
+      // the item two back, the buffer's previous user, is long done)
       if (!(ok = group_sync())) break;
+      const uint8_t* sBb = sB + buf * kM8SBBytes;
       const uint8_t* sa0 = nullptr;
       const uint8_t* sa1 = nullptr;
       if (!m.fp8) {
@@ -395,7 +415,7 @@ __global__ void __launch_bounds__(kM8Threads, kM8CtasPerSm)
         int tk = 32 * c + lane;
         if (tk >= m.n16) tk -= m.n16;  // B rows n16 .. 2 n16 - 1 are the lo terms
         if (tk >= m.count) tk = 0;     // columns past the group: any valid row
-        sbw[c] = reinterpret_cast<const uint32_t*>(sB + tk * srow);
+        sbw[c] = reinterpret_cast<const uint32_t*>(sBb + tk * srow);
       }
       auto store = [&](uint32_t wa0, uint32_t wa1, int ks) -> bool {
         const int s = gs % kM8Stages;
@@ -435,6 +455,13 @@ __global__ void __launch_bounds__(kM8Threads, kM8CtasPerSm)
         }
       }
       if (!ok) break;
+      // the next item's B scale rows go to the other buffer while this item's
+      // last MMAs complete
+      M8Item mn;
+      const int nit = take_run(mn);
+      ok = nit != -2;
+      if (!ok) break;
+      if (nit >= 0) copy_b(mn, buf ^ 1);
 
       // epilogue
       if (!(ok = __all_sync(0xffffffffu, mbar_wait_fast(accf, i & 1, a.err)))) break;
@@ -515,6 +542,9 @@ __global__ void __launch_bounds__(kM8Threads, kM8CtasPerSm)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acce);
+      m = mn;
+      it = nit;
+      buf ^= 1;
     }
   }
   tc_fence_before();
