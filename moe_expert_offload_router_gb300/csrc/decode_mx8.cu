@@ -391,15 +391,23 @@ __global__ void __launch_bounds__(kM8Threads, kM8CtasPerSm)
       for (int c = tid; c < n; c += 128)
         *reinterpret_cast<uint4*>(dst + (c / cpr) * srow + 16 * (c % cpr)) = ldg_u128(gB + 16 * c);
     };
+    // Each copy is followed by a group sync, so every warp's share is in place
+    // before any warp reads the buffer; a buffer is copied into again only
+    // after every warp has passed the sync that followed the copy after its
+    // last reader (the item two back), so no copy overtakes a reader.  The
+    // sync sits before the epilogue: a warp goes from its own epilogue
+    // straight to the next item's scale factors.
     M8Item m;
     int it = take_run(m);
     ok = it != -2;
     int buf = 0;
-    if (it >= 0) copy_b(m, 0);
+    bool have_pre = false;  // pre0 / pre1 hold the item's first 16 scale bytes of each A row
+    uint4 pre0 = make_uint4(0, 0, 0, 0), pre1 = pre0;
+    if (it >= 0) {
+      copy_b(m, 0);
+      ok = group_sync();
+    }
     while (ok && it >= 0) {
-      // every warp's share of this item's B scale rows is in buffer buf (and
-      // the item two back, the buffer's previous user, is long done)
-      if (!(ok = group_sync())) break;
       const uint8_t* sBb = sB + buf * kM8SBBytes;
       const uint8_t* sa0 = nullptr;
       const uint8_t* sa1 = nullptr;
@@ -442,8 +450,9 @@ __global__ void __launch_bounds__(kM8Threads, kM8CtasPerSm)
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           const bool in = kc + 4 * g < nk;
-          ra0[g] = (m.fp8 || !in) ? unit : ldg_u128(sa0 + 4 * kc + 16 * g);
-          ra1[g] = (m.fp8 || !in) ? unit : ldg_u128(sa1 + 4 * kc + 16 * g);
+          const bool pre = have_pre && kc == 0 && g == 0;
+          ra0[g] = (m.fp8 || !in) ? unit : pre ? pre0 : ldg_u128(sa0 + 4 * kc + 16 * g);
+          ra1[g] = (m.fp8 || !in) ? unit : pre ? pre1 : ldg_u128(sa1 + 4 * kc + 16 * g);
         }
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
@@ -461,7 +470,19 @@ __global__ void __launch_bounds__(kM8Threads, kM8CtasPerSm)
       const int nit = take_run(mn);
       ok = nit != -2;
       if (!ok) break;
-      if (nit >= 0) copy_b(mn, buf ^ 1);
+      if (nit >= 0) {
+        copy_b(mn, buf ^ 1);
+        if (!(ok = group_sync())) break;
+      }
+      // and the first 16 bytes of this lane's two A scale rows (the first
+      // four stages' words), so the next item's first stores wait for no load
+      uint4 pre0n = make_uint4(0, 0, 0, 0), pre1n = pre0n;
+      if (nit >= 0 && !mn.fp8) {
+        const uint8_t* e = a.fp4 + (size_t)mn.slot * a.b4;
+        const int r0 = mn.f0 + 32 * q + lane, r1 = (a.mode == 0 ? mn.f0 : mn.f0 + 128) + 32 * q + lane;
+        pre0n = ldg_u128(e + a.sc0 + (size_t)r0 * sbytes);
+        pre1n = ldg_u128(e + a.sc1 + (size_t)r1 * sbytes);
+      }
 
       // epilogue
       if (!(ok = __all_sync(0xffffffffu, mbar_wait_fast(accf, i & 1, a.err)))) break;
@@ -545,6 +566,9 @@ __global__ void __launch_bounds__(kM8Threads, kM8CtasPerSm)
       m = mn;
       it = nit;
       buf ^= 1;
+      have_pre = nit >= 0 && !mn.fp8;
+      pre0 = pre0n;
+      pre1 = pre1n;
     }
   }
   tc_fence_before();
