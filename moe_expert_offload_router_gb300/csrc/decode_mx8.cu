@@ -349,11 +349,11 @@ __global__ void __launch_bounds__(kM8Threads, kM8CtasPerSm)
     // scale factors of every stage (A row 32 q + lane of each tile at column
     // +q of its 4-column group; B rows 32 c + lane at column +8 + c), then
     // the epilogue once the item's MMAs have completed.  The scale rows are
-    // read whole, once per item: each lane keeps its two A rows' words in
-    // registers (up to 32 stages at a time, one load per 16 bytes, the rest of
-    // each line from L1), and the group's B rows go to shared memory in one
-    // coalesced copy by the four warps; scattered 4-byte loads per stage cost
-    // about as many L2 requests as the TMA's own and slowed it down.  The B
+    // read whole, once per item: each lane reads its two A rows 16 bytes (four
+    // stages) at a time, one group of four ahead, and the group's B rows go to
+    // shared memory in one coalesced copy by the four warps; scattered 4-byte
+    // loads per stage cost about as many L2 requests as the TMA's own and
+    // slowed it down.  The B
     // rows have two buffers: the next item's are copied right after the
     // current item's last scale-factor store, while its last MMAs complete,
     // so the next item's first stage does not wait for the copy.
@@ -443,25 +443,21 @@ __global__ void __launch_bounds__(kM8Threads, kM8CtasPerSm)
         ++gs;
         return true;
       };
-      // nk is a multiple of 4 (K a multiple of 512)
-      for (int kc = 0; kc < nk && ok; kc += 32) {
-        uint4 ra0[8], ra1[8];
-        const uint4 unit = make_uint4(0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const bool in = kc + 4 * g < nk;
-          const bool pre = have_pre && kc == 0 && g == 0;
-          ra0[g] = (m.fp8 || !in) ? unit : pre ? pre0 : ldg_u128(sa0 + 4 * kc + 16 * g);
-          ra1[g] = (m.fp8 || !in) ? unit : pre ? pre1 : ldg_u128(sa1 + 4 * kc + 16 * g);
+      // nk is a multiple of 4 (K a multiple of 512): 16 bytes of an A row hold
+      // four stages' words; each group of four is loaded one group ahead
+      const uint4 unit = make_uint4(0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
+      uint4 n0 = m.fp8 ? unit : have_pre ? pre0 : ldg_u128(sa0);
+      uint4 n1 = m.fp8 ? unit : have_pre ? pre1 : ldg_u128(sa1);
+      for (int ks = 0; ks < nk && ok; ks += 4) {
+        const uint4 c0 = n0, c1 = n1;
+        if (!m.fp8 && ks + 4 < nk) {
+          n0 = ldg_u128(sa0 + 4 * (ks + 4));
+          n1 = ldg_u128(sa1 + 4 * (ks + 4));
         }
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          if (kc + 4 * g >= nk || !ok) break;
-          if (ok) ok = store(ra0[g].x, ra1[g].x, kc + 4 * g);
-          if (ok) ok = store(ra0[g].y, ra1[g].y, kc + 4 * g + 1);
-          if (ok) ok = store(ra0[g].z, ra1[g].z, kc + 4 * g + 2);
-          if (ok) ok = store(ra0[g].w, ra1[g].w, kc + 4 * g + 3);
-        }
+        if (ok) ok = store(c0.x, c1.x, ks);
+        if (ok) ok = store(c0.y, c1.y, ks + 1);
+        if (ok) ok = store(c0.z, c1.z, ks + 2);
+        if (ok) ok = store(c0.w, c1.w, ks + 3);
       }
       if (!ok) break;
       // the next item's B scale rows go to the other buffer while this item's
