@@ -91,7 +91,7 @@ def _peaks():
 # removed when its kernel changes.
 NCU_TRAFFIC = {
     ("mx8_gemm_kernel (gate/up)", "decode"): {
-        "dram_bytes": 503_352_064 + 4_839_936, "algorithmic_bytes": 505_278_464,
+        "dram_bytes": 503_437_056 + 5_178_112, "algorithmic_bytes": 505_278_464,
         "capture": "ncu dram__bytes_read/write.sum of mx8_gemm_kernel gate/up, bench.py --workload forward --T 64 "
                    "(trace step 3: 54 experts + shared), profiles/mx8_gemm_kernel_decode_forward_T64.md"},
     ("mxf4_gemm_kernel (gate/up)", "prefill"): {
@@ -99,7 +99,7 @@ NCU_TRAFFIC = {
         "capture": "ncu dram__bytes_read/write.sum of mxf4_gemm_kernel gate/up, bench.py --workload prefill "
                    "--prefill-experts 64 --prefill-tokens 2048, profiles/mxf4_gemm_kernel_prefill_E64_T2048.md"},
     ("prefill_gemm_kernel (gate/up)", "prefill"): {
-        "dram_bytes": 675_437_824 + 44_954_624, "algorithmic_bytes": 721_420_288,
+        "dram_bytes": 676_065_280 + 45_294_592, "algorithmic_bytes": 721_420_288,
         "capture": "ncu dram__bytes_read/write.sum of prefill_gemm_kernel gate/up, bench.py --workload prefill "
                    "--prefill-experts 64 --prefill-tokens 2048, profiles/prefill_gemm_kernel_prefill_E64_T2048.md"},
 }
