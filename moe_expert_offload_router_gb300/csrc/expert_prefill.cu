@@ -649,7 +649,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 // group holds, for A, row m's four block scales (bytes 0..3) in lane m, column
 // group + m / 32; for B, row n's in lane 32 q + n % 32, column group + n / 32 of
 // every quadrant q.
-constexpr int kMxThreads = 384;   // warp 0 TMA, warp 1 MMA, warps 4-7 scale factors, warps 4-11 the epilogue
+constexpr int kMxThreads = 512;   // warp 0 TMA, warp 1 MMA, warps 4-7 scale factors, warps 4-15 the epilogue
+constexpr int kMxEpiWarps = kMxThreads / 32 - 4;  // three per tensor-memory lane quadrant
+constexpr int kMxEpiParts = kMxEpiWarps / 4;
 constexpr int kMxQueue = 4;       // work indices published ahead to the consumer warps
 constexpr int kMxStages = 3;      // shared-memory stages of codes
 constexpr int kMxSfSlots = 2;     // tensor-memory slots of scale factors (stage ks in slot ks % 2)
@@ -755,13 +757,13 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(accf, 1);
-    mbar_init(acce, 8);
+    mbar_init(acce, kMxEpiWarps);
     mbar_init(drain, 1);
     for (int j = 0; j < kMxQueue; ++j) {
       mbar_init(&qfull[j], 1);
-      mbar_init(&qempty[j], 1 + 8);
+      mbar_init(&qempty[j], 1 + kMxEpiWarps);
     }
-    mbar_init(esync, 8);
+    mbar_init(esync, kMxEpiWarps);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -895,13 +897,14 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     mbar_wait(drain, 0, a.err);
   } else if (warp >= 4) {
     // warps 4-7: per item the scale factors of every stage into lane quadrant
-    // q (warp 4 + q may write only lanes 32 q .. 32 q + 31), then half 0 of the
-    // epilogue; warps 8-11: half 1 of the epilogue
-    const int q = warp & 3, half = (warp - 4) >> 2;
+    // q (warp 4 + q may write only lanes 32 q .. 32 q + 31), then part 0 of the
+    // epilogue; warps 8-11 and 12-15: parts 1 and 2 of the epilogue (a part
+    // takes every third chunk of columns)
+    const int q = warp & 3, part = (warp - 4) >> 2;
     bool ok = true;
     uint32_t gs = 0, i = 0, nsync = 0;
-    // the eight epilogue warps meet (bounded, so a warp that gave up cannot
-    // leave the others waiting)
+    // the epilogue warps meet (bounded, so a warp that gave up cannot leave
+    // the others waiting)
     auto epi_sync = [&]() -> bool {
       __syncwarp();
       if (lane == 0) mbar_arrive(esync);
@@ -914,7 +917,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       if (!m.run) continue;
       const PfItem it = m.it;
       const int f0 = m.f0, n_mma = m.n_mma;
-      if (half == 0) {
+      if (part == 0) {
         const uint8_t* base_a = a.sc0 + (size_t)it.slot * a.B;
         const uint8_t* sa0 = base_a + (size_t)(f0 + 32 * q + lane) * sbytes;
         const uint8_t* sa1 = a.mode == 0 ? a.sc1 + (size_t)it.slot * a.B + (size_t)(f0 + 32 * q + lane) * sbytes
@@ -979,14 +982,13 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         }
         if (!ok) break;
       }
-      // epilogue: warp w reads TMEM lane quadrant w % 4 and the columns
-      // [112 half, 112 half + 112) of each accumulator
+      // epilogue: warp w reads TMEM lane quadrant w % 4; part p takes chunks
+      // p, p + 3, ... of the columns (8 wide for gate/up, 16 for down)
       if (!(ok = __all_sync(0xffffffffu, mbar_wait_fast(accf, i & 1, a.err)))) break;
       ++i;
       tc_fence_after();
       const int row = q * 32 + lane;
       const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
-      const int cb = half * (kMxNMax / 2), ce = min(cb + kMxNMax / 2, n_mma);
       if (a.mode == 0) {
         // lane = feature f0 + row: gate (w1 row) in tile 0, up (w3 row) in tile 1.
         // The 16 columns of a chunk go through each step together (independent
@@ -996,34 +998,34 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         // one narrow store per column and warp cost half the epilogue.
         uint8_t* hs = sm + kMxOffH;
         if (!(ok = epi_sync())) break;  // the previous item's rows have left
-        for (int c0 = cb; c0 < ce; c0 += 16) {
-          uint32_t vg[16], vu[16];
-          tmem_ld16_nw(tq + (uint32_t)c0, vg);  // both loads in flight, one wait
-          tmem_ld16_nw(tq + (uint32_t)(kMxNMax + c0), vu);
-          tmem_ld_wait16(vg);
-          tmem_ld_fence16(vu);
-          float hv[16];
+        for (int c0 = 8 * part; c0 < n_mma; c0 += 8 * kMxEpiParts) {
+          uint32_t vg[8], vu[8];
+          tmem_ld8_nw(tq + (uint32_t)c0, vg);  // both loads in flight, one wait
+          tmem_ld8_nw(tq + (uint32_t)(kMxNMax + c0), vu);
+          tmem_ld_wait8(vg);
+          tmem_ld_fence8(vu);
+          float hv[8];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < 8; ++j) {
             const float hg = 0.5f * __uint_as_float(vg[j]), up = __uint_as_float(vu[j]);
             hv[j] = fmaf(hg, tanh_approx(hg), hg) * up;
           }
           // the warp's 32 lanes hold 32 consecutive features of a column: one MX block
-          uint32_t am[16];
+          uint32_t am[8];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) am[j] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv[j])));
-          uint32_t code[16], sbyte[16];
+          for (int j = 0; j < 8; ++j) am[j] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv[j])));
+          uint32_t code[8], sbyte[8];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < 8; ++j) {
             sbyte[j] = mx_scale_byte(__uint_as_float(am[j]));
             code[j] = mx_code(hv[j], mx_inv_scale(sbyte[j]));
           }
-          uint32_t hi[16];
+          uint32_t hi[8];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) hi[j] = __shfl_down_sync(0xffffffffu, code[j], 1);
+          for (int j = 0; j < 8; ++j) hi[j] = __shfl_down_sync(0xffffffffu, code[j], 1);
           // byte b of the block = codes of lanes 2b (low nibble) and 2b + 1
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < 8; ++j) {
             uint8_t* hr = hs + (c0 + j) * kMxHRow;
             if ((lane & 1) == 0) hr[16 * q + lane / 2] = (uint8_t)(code[j] | (hi[j] << 4));
             if (lane == 0) hr[64 + q] = (uint8_t)sbyte[j];
@@ -1034,20 +1036,20 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(acce);
         if (!(ok = epi_sync())) break;
-        const int et = threadIdx.x - 128;  // 0 .. 255 over the eight epilogue warps
-        for (int e = et; e < it.count * 4; e += 256) {
+        const int et = threadIdx.x - 128;  // over the epilogue warps
+        for (int e = et; e < it.count * 4; e += 32 * kMxEpiWarps) {
           const int r = e >> 2, part = e & 3;
           *reinterpret_cast<uint4*>(a.hq + (size_t)(it.row0 + r) * (a.I / 2) + f0 / 2 + 16 * part) =
               *reinterpret_cast<const uint4*>(hs + r * kMxHRow + 16 * part);
         }
-        for (int r = et; r < it.count; r += 256)
+        for (int r = et; r < it.count; r += 32 * kMxEpiWarps)
           *reinterpret_cast<uint32_t*>(a.hsc + (size_t)(it.row0 + r) * (a.I / 32) + f0 / 32) =
               *reinterpret_cast<const uint32_t*>(hs + r * kMxHRow + 64);
         continue;
       } else {
         for (int mt = 0; mt < 2; ++mt) {
           const int feat = f0 + 128 * mt + row;
-          for (int c0 = cb; c0 < ce; c0 += 16) {
+          for (int c0 = 16 * part; c0 < n_mma; c0 += 16 * kMxEpiParts) {
             uint32_t v[16];
             tmem_ld16(tq + (uint32_t)(mt * kMxNMax + c0), v);
             const int cl = c0 + (lane & 15);
