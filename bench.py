@@ -95,7 +95,7 @@ NCU_TRAFFIC = {
         "capture": "ncu dram__bytes_read/write.sum of mx8_gemm_kernel gate/up, bench.py --workload forward --T 64 "
                    "(trace step 3: 54 experts + shared), profiles/mx8_gemm_kernel_decode_forward_T64.md"},
     ("mxf4_gemm_kernel (gate/up)", "prefill"): {
-        "dram_bytes": 597_573_888 + 12_905_216, "algorithmic_bytes": 610_533_376,
+        "dram_bytes": 597_576_704 + 12_771_584, "algorithmic_bytes": 610_533_376,
         "capture": "ncu dram__bytes_read/write.sum of mxf4_gemm_kernel gate/up, bench.py --workload prefill "
                    "--prefill-experts 64 --prefill-tokens 2048, profiles/mxf4_gemm_kernel_prefill_E64_T2048.md"},
     ("prefill_gemm_kernel (gate/up)", "prefill"): {
