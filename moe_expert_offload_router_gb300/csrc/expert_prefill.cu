@@ -738,11 +738,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   uint64_t* full = (uint64_t*)(sm + kMxOffBar);  // [kMxStages]: TMA bytes + four scale-factor warps
   uint64_t* empty = full + kMxStages;             // [kMxStages]: the stage's MMAs completed
   uint64_t* accf = empty + kMxStages;             // the item's MMAs completed
-  uint64_t* acce = accf + 1;                      // the eight epilogue warps have read the accumulators
+  uint64_t* acce = accf + 1;                      // the epilogue warps have read the accumulators
   uint64_t* drain = acce + 1;
   uint64_t* qfull = drain + 1;                    // [kMxQueue]: an item index published
-  uint64_t* qempty = qfull + kMxQueue;            // [kMxQueue]: the nine consumer warps have read it
-  uint64_t* esync = qempty + kMxQueue;            // the eight epilogue warps meet (h staging)
+  uint64_t* qempty = qfull + kMxQueue;            // [kMxQueue]: the MMA warp and the epilogue warps have read it
+  uint64_t* esync = qempty + kMxQueue;            // the epilogue warps meet (h staging)
   uint32_t* tmem_slot = (uint32_t*)(esync + 1);
   volatile int* itq = (volatile int*)(tmem_slot + 1);  // [kMxQueue] work indices, -1 = no more
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
