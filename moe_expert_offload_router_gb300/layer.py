@@ -21,6 +21,12 @@ batch cannot need more distinct experts than there are slots
 does not wait at all: the status of each layer is checked on the next call
 (or by :meth:`check`).
 
+An expert forward reports a failure (a slot out of range, a pipeline wait that
+gave up) through an error word on the device.  The runner keeps that word in
+its status block, so the read-back that follows the next ensure brings it to
+the host with the ensure status: `run` raises a forward's failure one call
+later, and :meth:`synchronize` raises the last call's.
+
 With ``graph=True`` (device copy, no ladder) a layer step whose batch is one
 chunk by construction is captured once as a CUDA graph (router, ensure,
 status read-back, copies, forward) and replayed on static buffers, which
@@ -89,11 +95,14 @@ class DecodeLayerRunner:
         m4 = min(cache.S, P, E)
         m2 = min(int2_cache.S, P, E) if int2_cache is not None else 0
         self.m4, self.m2 = m4, m2
-        # [count4, done, count2, pad, keys4[m4], slots4[m4], keys2[m2], slots2[m2]]
+        # [count4, done, count2, err, keys4[m4], slots4[m4], keys2[m2], slots2[m2]]
         n = 4 + 2 * m4 + 2 * m2
         self.info = torch.zeros(n, dtype=torch.int32, device=dev)
         self.info_h = torch.zeros(n, dtype=torch.int32, pin_memory=True)
-        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        # the forward's error word sits in the status block: every status read-back
+        # (taken after ensure, before the next forward clears it) carries the
+        # previous forward's status to the host at no extra cost
+        self.err = self.info[3:4]
         self.ws = torch.empty(L.moe_expert_forward_workspace(views, T_max, k), dtype=torch.uint8,
                               device=dev)
         # high priority: a copy launched while the compute stream's GEMM still has
@@ -180,8 +189,15 @@ class DecodeLayerRunner:
         if self.pf_pending:
             stream.wait_event(self.pf_done)
 
+    @staticmethod
+    def _forward_status(e: int):
+        # the error word a read-back carries is that of the forward enqueued before it
+        if e != L.MOE_OK:
+            raise L.MoeError(e, "an earlier expert forward reported a failure on the device")
+
     def check(self):
-        """Reads the status of the last device-mode layer whose check was deferred."""
+        """Reads the status of the last device-mode layer whose check was deferred
+        (and with it the error word of the forward enqueued before that layer)."""
         if self.pending is None:
             return
         layer_id, T = self.pending
@@ -189,6 +205,7 @@ class DecodeLayerRunner:
         self.status_ev.synchronize()
         n4, done = int(self.status_h[0]), int(self.status_h[1])
         n2 = int(self.status_h[2]) if self.ladder is not None else 0
+        self._forward_status(int(self.status_h[3]))
         if n4 < 0 or n2 < 0:
             raise L.MoeError(-min(n4, n2), f"slot ensure failed on the device (layer {layer_id})")
         self.stats["misses"] += n4 + n2
@@ -259,6 +276,7 @@ class DecodeLayerRunner:
                 return y
             self.status_ev.synchronize()
             n4, done = int(self.status_h[0]), int(self.status_h[1])
+            self._forward_status(int(self.status_h[3]))
             if n4 < 0:
                 raise L.MoeError(-n4, f"slot ensure failed on the device (token_begin={tb})")
             self.stats["misses"] += n4
@@ -332,6 +350,17 @@ class DecodeLayerRunner:
             self.stats["calls"], self.stats["chunks"] = calls, chunks
         self.graphs[(layer_id, T)] = (g, lg, xb, yb)
 
+    def synchronize(self, stream=None):
+        """Waits for the work enqueued on `stream` and raises what the device
+        reported: a deferred ensure status or an expert forward's error word
+        (`run` reads each of those one call late, without waiting)."""
+        stream = stream or torch.cuda.current_stream(self.dev)
+        stream.synchronize()
+        self.check()
+        with torch.cuda.stream(stream):
+            e = int(self.err.item())
+        self._forward_status(e)
+
     def run(self, layer_id: int, logits, x, y, stream=None, prefetch=None):
         """y[T, H] (bf16 bits) = the MoE layer applied to x[T, H] with router logits [T, E].
 
@@ -385,11 +414,13 @@ class DecodeLayerRunner:
             if self.assume_resident and self.ladder is None:
                 done = T
             else:
-                self.info_h.copy_(self.info, non_blocking=True)
+                with torch.cuda.stream(stream):   # ordered after this call's ensure
+                    self.info_h.copy_(self.info, non_blocking=True)
                 stream.synchronize()
                 h = self.info_h
                 n4, done = int(h[0]), int(h[1])
                 n2 = int(h[2]) if self.ladder is not None else 0
+                self._forward_status(int(h[3]))
                 if n4 < 0 or n2 < 0:
                     code = -min(n4, n2)
                     raise L.MoeError(code, "slot ensure failed on the device "
