@@ -119,11 +119,15 @@ def _check(status: int):
 
 
 def _p(t):
-    """Raw data pointer of a tensor (or None)."""
+    """Raw data pointer of a tensor (or None).  The library reads every array
+    as dense row-major memory, so a strided view is refused here rather than
+    read as if it were dense."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_contiguous():
+        raise ValueError(f"tensor of shape {tuple(t.shape)} and strides {t.stride()} is not contiguous")
     return t.data_ptr()
 
 
@@ -283,7 +287,11 @@ def moe_copy_missing(cache: moe_cache, h_miss_key, h_miss_slot, n_miss: int, cop
     def hp(a):
         if a is None:
             return None
-        return a.data_ptr() if hasattr(a, "data_ptr") else a.ctypes.data
+        if hasattr(a, "data_ptr"):
+            return _p(a)
+        if not a.flags["C_CONTIGUOUS"]:
+            raise ValueError("host miss arrays must be contiguous")
+        return a.ctypes.data
     _check(_lib.moe_copy_missing(cache.handle, hp(h_miss_key), hp(h_miss_slot), n_miss,
                                  _s(copy_stream), _e(ready), _e(done)))
 

@@ -63,3 +63,21 @@ def test_profile_timeline_host_side(lib):
     assert lib.moe_profile_enable(0) == 0
     k, a, b = (C.c_int32 * 1)(), (C.c_double * 1)(), (C.c_double * 1)()
     assert lib.moe_profile_timeline(1, k, a, b, C.byref(n)) == 0 and n.value == 0
+
+
+def test_binding_refuses_strided_views():
+    # the binding hands raw pointers to a library that reads dense rows: a
+    # transposed or sliced-along-columns view is refused before any call
+    import numpy as np
+    import torch
+    from moe_expert_offload_router_gb300 import _lib as B
+    with pytest.raises(ValueError, match="not contiguous"):
+        B.moe_router_topk(torch.zeros((8, 4)).t(), 2)
+    with pytest.raises(ValueError, match="not contiguous"):
+        B.moe_rms_carry(torch.zeros((4, 64), dtype=torch.int16)[:, ::2], 1e-6,
+                        torch.zeros((4, 32), dtype=torch.int16))
+    keys = np.zeros((4, 2), dtype=np.int32)[:, 0]
+    no_cache = B.moe_cache.__new__(B.moe_cache)
+    no_cache.handle = None
+    with pytest.raises(ValueError, match="contiguous"):
+        B.moe_copy_missing(no_cache, keys, keys, 1)
