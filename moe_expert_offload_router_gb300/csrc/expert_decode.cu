@@ -8,8 +8,10 @@
 // experts, a 2.25-bit copy with fp8 group scales, one shared expert).
 //
 // Structure (all launches on the caller's stream):
-//   plan kernel   block 0 sorts the kept (pool, slot, pair) keys in shared
-//                 memory (bitonic) and cuts each slot's run into groups of up
+//   plan kernel   block 0 sorts the kept pairs by (pool, slot), stably, in
+//                 shared memory (a counting sort over the slots; a bitonic
+//                 sort of (pool, slot, pair) keys when the pools hold more
+//                 than 4096 slots) and cuts each slot's run into groups of up
 //                 to G tokens; blocks 1..T scale each token's activations by
 //                 a power of two so the largest is in [1, 2) and store fp16.
 //   gate/up       persistent; a work item is (group, 32-row tile).  The
