@@ -180,3 +180,26 @@ def test_binding_constants_match_header(lib):
         assert hasattr(L, name), name
         assert getattr(L, name) == v, (name, getattr(L, name), v)
     assert L.KERNEL_NAMES and len(L.KERNEL_NAMES) == vals["MOE_K_COUNT"]
+
+
+def test_plain_c_program_uses_the_header(tmp_path):
+    # the boundary is a C ABI: a C99 program compiled by gcc against the header
+    # links against the library and gets the declared results from the calls
+    # that need no GPU
+    import shutil
+    import subprocess
+    from moe_expert_offload_router_gb300 import build
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not installed")
+    so = build.build()
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    exe = str(tmp_path / "abi_consumer")
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                    "-I", os.path.join(ROOT, "include"), "-isystem", cuda_inc,
+                    os.path.join(ROOT, "tests", "c", "abi_consumer.c"), "-o", exe,
+                    "-L", os.path.dirname(so), "-l:" + os.path.basename(so),
+                    "-Wl,-rpath," + os.path.dirname(so)], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == "ok"
