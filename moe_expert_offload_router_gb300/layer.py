@@ -490,6 +490,16 @@ class PrefillStreamer:
         for layer in range(first_layer, min(first_layer + 2, self.L)):
             self._load(layer, stream)
 
+    def synchronize(self, stream=None):
+        """Waits for the work enqueued on `stream` and raises the error word of
+        the last layer's grouped GEMM (each call clears it first)."""
+        stream = stream or torch.cuda.current_stream(self.dev)
+        stream.synchronize()
+        with torch.cuda.stream(stream):
+            e = int(self.err.item())
+        if e != L.MOE_OK:
+            raise L.MoeError(e, "the streamed prefill's grouped GEMM reported a failure on the device")
+
     def run_layer(self, layer: int, logits, x, y, stream=None):
         """y[T, H] = the MoE layer `layer` on x[T, H] with router logits [T, E]."""
         stream = stream or torch.cuda.current_stream(self.dev)

@@ -29,7 +29,7 @@ def test_streamed_layers_match_resident_prefill_and_oracle():
         xd = torch.from_numpy(x.view(np.int16)).cuda()
         y = torch.empty((T, wl.H), dtype=torch.int16, device="cuda")
         st.run_layer(layer, torch.from_numpy(lg).cuda(), xd, y)
-        torch.cuda.synchronize()
+        st.synchronize()                       # raises if the grouped GEMM reported a failure
         assert int(st.err) == 0
         # the same layer resident in a pool of its own, through moe_expert_prefill
         pool = bank[layer * wl.E * B:(layer + 1) * wl.E * B].cuda()
