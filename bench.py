@@ -219,7 +219,11 @@ t0 = time.perf_counter()
 cache = SlotCacheLRU(wl.S, 1, wl.E)
 shw = F.decode_fp8_expert(shared_bytes, wl.H, wl.I)
 tokens = 0
-for step in range({steps}):
+step_seconds = []
+for step in range({warm} + {steps}):
+    if step == {warm}:
+        t0, tokens = time.perf_counter(), 0
+    ts = time.perf_counter()
     lg = gen.router_logits(wl, 0, step, wl.T)
     x = gen.activations(wl, 0, step, wl.T)
     ids, w = router_topk(lg, wl.k)
@@ -229,8 +233,9 @@ for step in range({steps}):
     y = moe_layer(x, ids, w, lambda e, tag: F.decode_fp4_expert(gen.fp4_expert(wl, 0, e), wl.H, wl.I),
                   shared=shw)
     tokens += wl.T
+    step_seconds.append(time.perf_counter() - ts)
 dt = time.perf_counter() - t0
-print(json.dumps({{"tokens": tokens, "seconds": dt}}))
+print(json.dumps({{"tokens": tokens, "seconds": dt, "step_seconds": step_seconds[{warm}:]}}))
 """
 
 
@@ -247,16 +252,24 @@ def aggregate(ms_local: float, tokens_local: int, world: int, device=None):
     return ms, world * tokens_local / (ms / 1e3)
 
 
-def cpu_baseline(T: int, steps: int = 1, threads: int = 1):
-    """The oracle timed on the host cores: `threads` BLAS/OpenMP threads."""
+def _run_oracle(T: int, steps: int, threads: int, warm: int = 0):
+    """The oracle over `warm` untimed and `steps` timed decode trace steps of
+    T tokens, in a child process with `threads` BLAS/OpenMP threads: its
+    record ({"tokens", "seconds", "step_seconds"}) or the error's last line."""
     n = str(threads)
     env = dict(os.environ, OMP_NUM_THREADS=n, OPENBLAS_NUM_THREADS=n, MKL_NUM_THREADS=n)
-    code = _CPU_SNIPPET.format(root=ROOT, T=T, steps=steps)
+    code = _CPU_SNIPPET.format(root=ROOT, T=T, steps=steps, warm=warm)
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
     if r.returncode != 0:
-        return {"value": None, "unit": UNIT, "cores": threads, "kind": "oracle",
-                "sample": "failed: " + r.stderr.strip().splitlines()[-1][:200] if r.stderr else "failed"}
-    d = json.loads(r.stdout.strip().splitlines()[-1])
+        return "failed: " + (r.stderr.strip().splitlines()[-1][:200] if r.stderr.strip() else "no output")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(T: int, steps: int = 1, threads: int = 1):
+    """The oracle timed on the host cores: `threads` BLAS/OpenMP threads."""
+    d = _run_oracle(T, steps, threads)
+    if isinstance(d, str):
+        return {"value": None, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": d}
     how = "single-threaded" if threads == 1 else f"{threads} threads"
     return {"value": d["tokens"] / d["seconds"], "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{steps} trace step(s) x {T} tokens of the decode workload (fp64 NumPy, "
@@ -1162,24 +1175,26 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    T = args.cpu_sample_tokens
-    per = []
-    for _ in range(max(1, min(args.steps, 3))):
-        d = cpu_baseline(T, 1)
-        if d["value"] is None:
-            print(json.dumps({"impl": "reference", "unavailable": d["sample"]}))
-            return
-        per.append(T / d["value"])
+    # every step is a bounded sample of the decode workload: T tokens of one
+    # trace step (one or two, so that the --warmup + --steps run stays within
+    # a few minutes of host time: ~0.5-1 s per token-step)
+    K, W = max(1, args.steps), max(0, args.warmup)
+    T = max(1, min(args.cpu_sample_tokens, 2 if K + W <= 60 else 1))
+    d = _run_oracle(T, K, 1, warm=W)
+    if isinstance(d, str):
+        print(json.dumps({"impl": "reference", "unavailable": d}))
+        return
+    per = d["step_seconds"]
     ms = 1e3 * sum(per) / len(per)
     value = T / (ms / 1e3)
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": len(per), "warmup": 0, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "steps": K, "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generator)",
         "config": {"workload": f"decode layer H=4096 I=2048 E=256 top_k=8 + FP8 shared, 64-slot cache, "
                                f"Zipf(1.1) routing trace, bounded sample of T={T} tokens per step"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{len(per)} step(s) x {T} tokens, single-threaded fp64 NumPy"},
+                         "sample": f"{W} untimed + {K} timed trace steps x {T} tokens, single-threaded fp64 NumPy"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
