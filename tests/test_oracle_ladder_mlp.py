@@ -167,6 +167,18 @@ def test_rms_carry_unit_rms():
     assert np.all(c[1] == 0.0)
 
 
+def test_rms_carry_eps_inside_the_root():
+    # a row whose mean square equals eps: the divisor is sqrt(2 eps), so every
+    # element becomes +-1/sqrt(2) (eps outside the root, or a sum in place of the
+    # mean, would give ~1 or 1/2); rows are independent and signs are kept
+    y = np.array([[1e-3, -1e-3], [30.0, -40.0]])
+    c = rms_carry(y, eps=1e-6)
+    assert np.allclose(c[0], [2 ** -0.5, -(2 ** -0.5)], rtol=1e-12)
+    assert np.allclose(c[1], np.array([30.0, -40.0]) / np.sqrt(1250.0 + 1e-6), rtol=1e-12)
+    # scale invariance far above eps
+    assert np.allclose(rms_carry(7.0 * y[1:], eps=1e-6), c[1:], rtol=1e-9)
+
+
 # ----------------------------------------------------------------- permute ----
 
 def test_group_pairs_matches_buckets():
